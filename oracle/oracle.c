@@ -1,0 +1,341 @@
+/*
+ * oracle.c -- plain CPU reference of the DCOCO draft-correction path.
+ *
+ * TEST INFRASTRUCTURE ONLY (see oracle.h).  Slow on purpose: every step is a
+ * plain loop written straight from its definition, in the order the pages
+ * give, with no blocking, fusion or algebraic rewriting.
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+double orc_bf16_to_double(uint16_t bits) {
+  uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* ---------------------------------------------------------------------------
+ * Step 1 -- candidate pool.  [DCOCO] Method step details (1) and Core method:
+ * each draft slot keeps the top-K candidates of its draft logits.  The order
+ * is value descending, then token id ascending (deterministic tie-break);
+ * -0 and +0 are the same value.  A full sort of the row, then the first K.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  double v;
+  int32_t id;
+} orc_entry;
+
+static int orc_entry_cmp(const void *pa, const void *pb) {
+  const orc_entry *a = (const orc_entry *)pa, *b = (const orc_entry *)pb;
+  if (a->v > b->v) return -1;
+  if (a->v < b->v) return 1;
+  return (a->id > b->id) - (a->id < b->id);
+}
+
+void orc_topk_row(const uint16_t *row, int V, int K, int32_t *ids, float *vals) {
+  orc_entry *e = (orc_entry *)malloc((size_t)V * sizeof *e);
+  if (!e) return;
+  for (int t = 0; t < V; ++t) {
+    double v = orc_bf16_to_double(row[t]);
+    if (v == 0.0) v = 0.0; /* -0 -> +0 */
+    e[t].v = v;
+    e[t].id = t;
+  }
+  qsort(e, (size_t)V, sizeof *e, orc_entry_cmp);
+  for (int k = 0; k < K; ++k) {
+    ids[k] = e[k].id;
+    vals[k] = (float)e[k].v;
+  }
+  free(e);
+}
+
+/* ---------------------------------------------------------------------------
+ * LayerNorm.  [DCOCO] Method step details (2): b and g use LayerNorm without
+ * affine parameters; z uses LayerNorm with gamma, beta.  Population variance
+ * over the r features, eps inside the square root.
+ * ------------------------------------------------------------------------- */
+void orc_ln0(const double *x, int n, double eps, double *y) {
+  double mean = 0.0;
+  for (int i = 0; i < n; ++i) mean += x[i];
+  mean /= n;
+  double var = 0.0;
+  for (int i = 0; i < n; ++i) var += (x[i] - mean) * (x[i] - mean);
+  var /= n;
+  double inv = 1.0 / sqrt(var + eps);
+  for (int i = 0; i < n; ++i) y[i] = (x[i] - mean) * inv;
+}
+
+void orc_matvec(const float *W, int out, int in, const double *x, double *y) {
+  for (int o = 0; o < out; ++o) {
+    double acc = 0.0;
+    const float *wr = W + (size_t)o * in;
+    for (int i = 0; i < in; ++i) acc += (double)wr[i] * x[i];
+    y[o] = acc;
+  }
+}
+
+double orc_gelu(double x) { return 0.5 * x * (1.0 + erf(x / sqrt(2.0))); }
+
+static void orc_widen(const uint16_t *src, int n, double *dst) {
+  for (int i = 0; i < n; ++i) dst[i] = orc_bf16_to_double(src[i]);
+}
+
+/* [DCOCO] Method step details (2): g_i = LN(W_ctx h_i), non-affine. */
+void orc_context(const orc_dims *dm, const orc_weights *w, const uint16_t *h, double *g) {
+  double *hd = (double *)malloc((size_t)dm->d * sizeof *hd);
+  double *t = (double *)malloc((size_t)dm->r * sizeof *t);
+  orc_widen(h, dm->d, hd);
+  orc_matvec(w->w_ctx, dm->r, dm->d, hd, t);
+  orc_ln0(t, dm->r, dm->ln_eps, g);
+  free(hd);
+  free(t);
+}
+
+/* [DCOCO] Method step details (2): b = LN(W_cand E[c]) non-affine,
+ * z = LN_{gamma,beta}(W_fuse [b; g]). */
+void orc_candidate(const orc_dims *dm, const orc_weights *w, const uint16_t *e,
+                   const double *g, double *b, double *z) {
+  const int r = dm->r;
+  double *ed = (double *)malloc((size_t)dm->d * sizeof *ed);
+  double *t = (double *)malloc((size_t)r * sizeof *t);
+  double *bg = (double *)malloc((size_t)2 * r * sizeof *bg);
+  double *u = (double *)malloc((size_t)r * sizeof *u);
+  orc_widen(e, dm->d, ed);
+  orc_matvec(w->w_cand, r, dm->d, ed, t);
+  orc_ln0(t, r, dm->ln_eps, b);
+  for (int i = 0; i < r; ++i) {
+    bg[i] = b[i];
+    bg[r + i] = g[i];
+  }
+  orc_matvec(w->w_fuse, r, 2 * r, bg, t);
+  orc_ln0(t, r, dm->ln_eps, u);
+  for (int i = 0; i < r; ++i) z[i] = (double)w->ln_gamma[i] * u[i] + (double)w->ln_beta[i];
+  free(ed);
+  free(t);
+  free(bg);
+  free(u);
+}
+
+/* [DCOCO] Method step details (3): s_p = W_pair [h_p; h_{p+1}], once per pair. */
+void orc_pair_state(const orc_dims *dm, const orc_weights *w, const uint16_t *h_p,
+                    const uint16_t *h_q, double *s) {
+  const int d = dm->d;
+  double *hh = (double *)malloc((size_t)2 * d * sizeof *hh);
+  orc_widen(h_p, d, hh);
+  orc_widen(h_q, d, hh + d);
+  orc_matvec(w->w_pair, dm->r, 2 * d, hh, s);
+  free(hh);
+}
+
+/* [DCOCO] Core method and Method step details (4):
+ * S_p(a,b) = l_{p+1}(b) + Delta([s_p; z_p^a; z_{p+1}^b; l_p(a); l_{p+1}(b)]),
+ * Delta a 386 -> 256 -> 1 MLP with GELU, evaluated directly on the
+ * concatenated 3r+2 input. */
+double orc_transition(const orc_dims *dm, const orc_weights *w, const double *s,
+                      const double *z_a, const double *z_b, double l_a, double l_b) {
+  const int r = dm->r, H = dm->H, in = 3 * r + 2;
+  double *x = (double *)malloc((size_t)in * sizeof *x);
+  for (int i = 0; i < r; ++i) {
+    x[i] = s[i];
+    x[r + i] = z_a[i];
+    x[2 * r + i] = z_b[i];
+  }
+  x[3 * r] = l_a;
+  x[3 * r + 1] = l_b;
+  double delta = (double)w->b2[0];
+  for (int j = 0; j < H; ++j) {
+    double a = (double)w->b1[j];
+    const float *row = w->w1 + (size_t)j * in;
+    for (int i = 0; i < in; ++i) a += (double)row[i] * x[i];
+    delta += (double)w->w2[j] * orc_gelu(a);
+  }
+  free(x);
+  return l_b + delta;
+}
+
+/* Cosine variant.  [LiLiCorr] Sec. 3.2 Eq. (1): adjacent candidates are
+ * coupled by sigma * cos(out_{s,k}, in_{s+1,k'}) of unit-norm out/in vectors.
+ * Here one bias-free projection of [E[c]; h_i] gives both vectors (first r
+ * rows: out, last r rows: in), and the successor's draft logit is added as
+ * the base score, as in the DCOCO transition. */
+void orc_cosine_vectors(const orc_dims *dm, const orc_weights *w, const uint16_t *e,
+                        const uint16_t *h, double *o, double *in) {
+  const int d = dm->d, r = dm->r;
+  double *x = (double *)malloc((size_t)2 * d * sizeof *x);
+  double *y = (double *)malloc((size_t)2 * r * sizeof *y);
+  orc_widen(e, d, x);
+  orc_widen(h, d, x + d);
+  orc_matvec(w->w_io, 2 * r, 2 * d, x, y);
+  double no = 0.0, ni = 0.0;
+  for (int i = 0; i < r; ++i) {
+    no += y[i] * y[i];
+    ni += y[r + i] * y[r + i];
+  }
+  no = sqrt(no);
+  ni = sqrt(ni);
+  if (no < 1e-12) no = 1e-12;
+  if (ni < 1e-12) ni = 1e-12;
+  for (int i = 0; i < r; ++i) {
+    o[i] = y[i] / no;
+    in[i] = y[r + i] / ni;
+  }
+  free(x);
+  free(y);
+}
+
+double orc_cosine_transition(int r, double sigma, const double *o_a, const double *in_b, double l_b) {
+  double dot = 0.0;
+  for (int i = 0; i < r; ++i) dot += o_a[i] * in_b[i];
+  return sigma * dot + l_b;
+}
+
+/* ---------------------------------------------------------------------------
+ * Step 5 -- prefix-first greedy walk.  [DCOCO] Core method and Method step
+ * details (5); same rule as [LiLiCorr] Sec. 3.5 Eq. (8): the first draft slot
+ * takes the draft argmax (candidate index 0 of its value-sorted pool), then
+ * k_{p+1} = argmax_b S_p(k_p, b), ties to the lowest b.  margin_p is the gap
+ * between the best and the second-best successor score.
+ * ------------------------------------------------------------------------- */
+void orc_walk(const double *scores, int B, int K, int32_t *choice, double *margin) {
+  choice[0] = 0;
+  for (int p = 0; p < B - 1; ++p) {
+    const double *row = scores + ((size_t)p * K + choice[p]) * K;
+    int best = 0;
+    for (int b = 1; b < K; ++b)
+      if (row[b] > row[best]) best = b;
+    double second = -INFINITY;
+    for (int b = 0; b < K; ++b)
+      if (b != best && row[b] > second) second = row[b];
+    choice[p + 1] = best;
+    if (margin) margin[p] = row[best] - second;
+  }
+}
+
+/* ---------------------------------------------------------------------------
+ * Greedy verification.  [FD] "Modified rejection sampling ..." section, the
+ * greedy-verification contract: accept the longest run that matches the
+ * target's greedy tokens.  The accepted length counts draft slots only.
+ * ------------------------------------------------------------------------- */
+int orc_verify(const int32_t *tokens, const int32_t *target, int B) {
+  int m = 0;
+  while (m < B && tokens[m] == target[m]) ++m;
+  return m;
+}
+
+/* [FD] "Verification can be parallel ..." section:
+ * s_k = P(A_1 and ... and A_k), E[Y] = 1 + sum_{k=1}^{gamma} s_k. */
+double orc_expected_yield(const double *cond, int n, double *survival) {
+  double alive = 1.0, ey = 1.0;
+  for (int k = 0; k < n; ++k) {
+    alive *= cond[k];
+    if (survival) survival[k] = alive;
+    ey += alive;
+  }
+  return ey;
+}
+
+/* Shapes read by orc_candidate / orc_context / orc_pair_state /
+ * orc_transition ([DCOCO] Method step details (2)-(4)). */
+long long orc_param_count(int d, int r, int H) {
+  long long n = 0;
+  n += (long long)r * d;            /* W_cand */
+  n += (long long)r * d;            /* W_ctx  */
+  n += (long long)r * 2 * r;        /* W_fuse */
+  n += 2LL * r;                     /* gamma, beta */
+  n += (long long)r * 2 * d;        /* W_pair */
+  n += (long long)H * (3 * r + 2);  /* W1 */
+  n += H;                           /* b1 */
+  n += H;                           /* w2 */
+  n += 1;                           /* b2 */
+  return n;
+}
+
+/* ---------------------------------------------------------------------------
+ * The whole path for one request, steps in the pages' order.
+ * ------------------------------------------------------------------------- */
+int orc_correct_request(const orc_dims *dm, const orc_weights *w, int variant, double sigma,
+                        const uint16_t *logits, int64_t stride, const uint16_t *hidden,
+                        const uint16_t *E, const int32_t *target,
+                        int32_t *topk_ids, float *topk_val, double *scores,
+                        int32_t *choice, int32_t *tokens, double *margin, int32_t *accept_len,
+                        orc_intermediates *inter) {
+  const int B = dm->slots - 1, K = dm->K, r = dm->r, d = dm->d;
+  if (B < 2 || K < 2 || K > dm->V || r < 1 || (variant != 0 && variant != 1)) return -1;
+
+  /* (1) top-K per draft slot; slot 0 (the anchor) is not read. */
+  for (int i = 0; i < B; ++i)
+    orc_topk_row(logits + (size_t)(i + 1) * stride, dm->V, K, topk_ids + (size_t)i * K,
+                 topk_val + (size_t)i * K);
+
+  double *zb = (double *)calloc((size_t)B * K * r, sizeof(double));   /* z, or o */
+  double *za = (double *)calloc((size_t)B * K * r, sizeof(double));   /* b, or in */
+  double *g = (double *)calloc((size_t)B * r, sizeof(double));
+  double *s = (double *)calloc((size_t)(B - 1) * r, sizeof(double));
+  if (!zb || !za || !g || !s) {
+    free(zb); free(za); free(g); free(s);
+    return -1;
+  }
+
+  if (variant == 0) {
+    /* (2) candidate representations */
+    for (int i = 0; i < B; ++i) {
+      const uint16_t *h = hidden + (size_t)(i + 1) * d;
+      orc_context(dm, w, h, g + (size_t)i * r);
+      for (int k = 0; k < K; ++k) {
+        const uint16_t *e = E + (size_t)topk_ids[(size_t)i * K + k] * d;
+        orc_candidate(dm, w, e, g + (size_t)i * r, za + ((size_t)i * K + k) * r,
+                      zb + ((size_t)i * K + k) * r);
+      }
+    }
+    /* (3) slot-pair states, pairs (1,2) .. (B-1,B) */
+    for (int p = 0; p < B - 1; ++p)
+      orc_pair_state(dm, w, hidden + (size_t)(p + 1) * d, hidden + (size_t)(p + 2) * d,
+                     s + (size_t)p * r);
+    /* (4) all (B-1) K^2 transitions */
+    for (int p = 0; p < B - 1; ++p)
+      for (int a = 0; a < K; ++a)
+        for (int b = 0; b < K; ++b)
+          scores[((size_t)p * K + a) * K + b] = orc_transition(
+              dm, w, s + (size_t)p * r, zb + ((size_t)p * K + a) * r,
+              zb + ((size_t)(p + 1) * K + b) * r, (double)topk_val[(size_t)p * K + a],
+              (double)topk_val[(size_t)(p + 1) * K + b]);
+  } else {
+    for (int i = 0; i < B; ++i)
+      for (int k = 0; k < K; ++k)
+        orc_cosine_vectors(dm, w, E + (size_t)topk_ids[(size_t)i * K + k] * d,
+                           hidden + (size_t)(i + 1) * d, zb + ((size_t)i * K + k) * r,
+                           za + ((size_t)i * K + k) * r);
+    for (int p = 0; p < B - 1; ++p)
+      for (int a = 0; a < K; ++a)
+        for (int b = 0; b < K; ++b)
+          scores[((size_t)p * K + a) * K + b] = orc_cosine_transition(
+              r, sigma, zb + ((size_t)p * K + a) * r, za + ((size_t)(p + 1) * K + b) * r,
+              (double)topk_val[(size_t)(p + 1) * K + b]);
+  }
+
+  /* (5) walk, then the chosen tokens */
+  orc_walk(scores, B, K, choice, margin);
+  for (int i = 0; i < B; ++i) tokens[i] = topk_ids[(size_t)i * K + choice[i]];
+  if (target && accept_len) accept_len[0] = orc_verify(tokens, target, B);
+
+  if (inter) {
+    if (variant == 0) {
+      if (inter->b) memcpy(inter->b, za, (size_t)B * K * r * sizeof(double));
+      if (inter->z) memcpy(inter->z, zb, (size_t)B * K * r * sizeof(double));
+      if (inter->g) memcpy(inter->g, g, (size_t)B * r * sizeof(double));
+      if (inter->s) memcpy(inter->s, s, (size_t)(B - 1) * r * sizeof(double));
+    } else {
+      if (inter->o) memcpy(inter->o, zb, (size_t)B * K * r * sizeof(double));
+      if (inter->in) memcpy(inter->in, za, (size_t)B * K * r * sizeof(double));
+    }
+  }
+  free(zb);
+  free(za);
+  free(g);
+  free(s);
+  return 0;
+}

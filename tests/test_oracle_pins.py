@@ -1,0 +1,377 @@
+"""Pins for the CPU oracle: each check ties it to something other than itself.
+
+Sources (pages, by title): the DCOCO page "Contextual Correction of Parallel
+Drafts for Speculative Decoding" (Core method; Method step details (1)-(5));
+"LiLiCorr" (Sec. 3.2 Eq. (1), Sec. 3.5 Eq. (8)); "Faster Decoding" (expected
+yield, greedy verification).
+"""
+import itertools
+import json
+import os
+
+import numpy as np
+import pytest
+from scipy.spatial.distance import cosine as scipy_cosine_distance
+from scipy.stats import norm
+
+import oracle
+import synth
+
+pytestmark = pytest.mark.filterwarnings("ignore::DeprecationWarning")
+
+
+# --------------------------------------------------------------- helpers
+def tiny_model(rng, V=257, d=64, K=4, r=16, H=24, slots=6, **kw):
+    w = synth.make_weights(rng, d, r=r, H=H, **kw)
+    w.update(synth.make_cosine_weights(rng, d, r=r))
+    return oracle.Model(w, V=V, d=d, slots=slots, K=K, r=r, H=H), w
+
+
+def perm_matrix(rng, out, in_, offset=0):
+    """[out, in_] 0/1 matrix selecting distinct input columns offset+pi(o)."""
+    W = np.zeros((out, in_), np.float32)
+    pi = rng.permutation(out)
+    W[np.arange(out), offset + pi] = 1.0
+    return W, pi
+
+
+# --------------------------------------------------------------- shapes
+def test_param_count_matches_page():
+    # DCOCO page: the corrector has 2,229,505 parameters at Qwen3-8B shapes.
+    assert oracle.param_count(4096, 128, 256) == 2_229_505
+    # The synthetic weight generator produces exactly those shapes.
+    w = synth.make_weights(np.random.default_rng(0), 4096)
+    assert sum(v.size for v in w.values()) == 2_229_505
+    # and the MLP input width is 386 = 3 r + 2
+    assert w["w1"].shape == (256, 386)
+
+
+def test_transition_count_matches_page():
+    # DCOCO page, Core method: (B-1) K^2 = 14 x 256 = 3584 transitions for B=15, K=16.
+    rng = np.random.default_rng(1)
+    m, _ = tiny_model(rng, slots=16, K=16, V=300)
+    logits = synth.make_logits(rng, 1, 16, 300, 8, (4, 12))
+    hidden = synth.make_hidden(rng, 1, 16, 64)
+    E = synth.make_embedding(rng, 300, 64)
+    out = oracle.correct_request(m, logits[0], hidden[0], E)
+    assert out["scores"].size == 3584
+
+
+# --------------------------------------------------------------- expected yield / verify
+def test_expected_yield_worked_example(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "expected_yield.json")))
+    ey, surv = oracle.expected_yield(g["conditional"])
+    np.testing.assert_allclose(surv, g["survival"], atol=1e-12)
+    assert abs(ey - g["expected_tokens_per_cycle"]) < 1e-12
+    # IID special case: closed form (1 - a^(g+1)) / (1 - a) from the same page.
+    a, n = g["alpha"], len(g["conditional"])
+    ey_iid, _ = oracle.expected_yield([a] * n)
+    assert abs(ey_iid - g["iid_estimate"]) < 1e-12
+    assert abs(ey_iid - (1 - a ** (n + 1)) / (1 - a)) < 1e-12
+    # alpha = 1 gives gamma + 1
+    assert oracle.expected_yield([1.0] * 7)[0] == 8.0
+
+
+def test_verify_enumeration_reproduces_expected_yield(golden_dir):
+    """E[accept_len] + 1 over all match patterns equals the page's E[Y] = 3.0230."""
+    g = json.load(open(os.path.join(golden_dir, "expected_yield.json")))
+    cond = g["conditional"]
+    n = len(cond)
+    target = np.arange(100, 100 + n, dtype=np.int32)
+    ey = 0.0
+    for pattern in itertools.product([0, 1], repeat=n):
+        prob = np.prod([c if m else 1 - c for c, m in zip(cond, pattern)])
+        tokens = np.where(np.array(pattern) == 1, target, target + 1000).astype(np.int32)
+        ey += prob * (oracle.verify(tokens, target) + 1)
+    assert abs(ey - g["expected_tokens_per_cycle"]) < 1e-12
+
+
+def test_verify_forced_cases():
+    # Faster Decoding checklist: force first rejection, later rejection, full acceptance.
+    t = np.arange(15, dtype=np.int32)
+    assert oracle.verify(t, t) == 15
+    bad = t.copy(); bad[0] = -1
+    assert oracle.verify(bad, t) == 0
+    bad = t.copy(); bad[7] = -1
+    assert oracle.verify(bad, t) == 7
+    bad = t.copy(); bad[14] = -1; bad[3] = -1
+    assert oracle.verify(bad, t) == 3
+
+
+# --------------------------------------------------------------- top-K
+def _lexsort_topk(vals, K):
+    ids = np.arange(vals.shape[0])
+    order = np.lexsort((ids, -vals.astype(np.float64)))
+    return order[:K].astype(np.int32), vals[order[:K]]
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_topk_vs_lexsort(seed):
+    rng = np.random.default_rng(seed)
+    V = int(rng.integers(40, 3000))
+    K = int(rng.choice([2, 8, 16, 32]))
+    K = min(K, V)
+    # coarse values -> many exact ties; plus -0/+0 and -inf entries
+    vals = np.round(rng.standard_normal(V) * 2, 1).astype(np.float32)
+    vals[rng.choice(V, size=V // 10, replace=False)] = -np.inf
+    z = rng.choice(V, size=min(V, 20), replace=False)
+    vals[z[:10]] = 0.0
+    vals[z[10:]] = -0.0
+    bits = synth.bf16_bits(vals)
+    f = synth.bf16_to_f32(bits)
+    ids, got = oracle.topk_row(bits, K)
+    ref_ids, ref_vals = _lexsort_topk(f, K)
+    np.testing.assert_array_equal(ids, ref_ids)
+    np.testing.assert_array_equal(got, ref_vals)
+    assert not np.any(np.signbit(got) & (got == 0)), "-0 must come out as +0"
+
+
+def test_topk_brute_force_all_equal():
+    # all-equal row: the K lowest ids, in order
+    bits = np.full(100, synth.bf16_bits(np.array([1.5], np.float32))[0], np.uint16)
+    ids, vals = oracle.topk_row(bits, 16)
+    np.testing.assert_array_equal(ids, np.arange(16))
+    assert np.all(vals == 1.5)
+
+
+def test_topk_brute_force_tiny():
+    rng = np.random.default_rng(7)
+    for _ in range(50):
+        V = int(rng.integers(3, 12))
+        K = int(rng.integers(1, V + 1))
+        vals = rng.integers(-3, 3, size=V).astype(np.float32)
+        bits = synth.bf16_bits(vals)
+        ids, _ = oracle.topk_row(bits, K)
+        # brute force: repeatedly take the best remaining (value desc, id asc)
+        left = list(range(V))
+        ref = []
+        for _k in range(K):
+            best = max(left, key=lambda i: (vals[i], -i))
+            ref.append(best)
+            left.remove(best)
+        assert list(ids) == ref
+
+
+# --------------------------------------------------------------- LayerNorm / GELU
+def test_ln0_closed_form():
+    rng = np.random.default_rng(3)
+    eps = 1e-5
+    for scale in (1e-3, 0.02, 1.0, 50.0):
+        x = rng.standard_normal(128) * scale + 3.0
+        y = oracle.ln0(x, eps)
+        var = x.var()
+        assert abs(y.mean()) < 1e-12 * max(1.0, scale)
+        assert abs(y.var() - var / (var + eps)) < 1e-12
+        # shift invariance
+        np.testing.assert_allclose(oracle.ln0(x + 7.0, eps), y, atol=1e-9)
+    # alternating +-c: population variance c^2, mean 0
+    c = 0.3
+    x = np.array([c, -c] * 64)
+    np.testing.assert_allclose(oracle.ln0(x, eps), x / np.sqrt(c * c + eps), atol=1e-15)
+
+
+def test_gelu_is_x_times_normal_cdf():
+    for x in (-6.0, -2.5, -1.0, -0.1, 0.0, 0.3, 1.0, 2.0, 7.0):
+        assert abs(oracle.gelu(x) - x * norm.cdf(x)) < 1e-15 + 1e-13 * abs(x)
+        # symmetry: GELU(-x) = GELU(x) - x
+        assert abs(oracle.gelu(-x) - (oracle.gelu(x) - x)) < 1e-13
+
+
+# --------------------------------------------------------------- representation structure
+def test_context_reads_rows_of_w_ctx():
+    rng = np.random.default_rng(4)
+    d, r = 64, 16
+    m, w = tiny_model(rng, d=d, r=r)
+    W, pi = perm_matrix(rng, r, d, offset=5)
+    w["w_ctx"] = W
+    m = oracle.Model(w, V=257, d=d, slots=6, K=4, r=r, H=24)
+    h = synth.make_hidden(rng, 1, 1, d)[0, 0]
+    hf = synth.bf16_to_f32(h).astype(np.float64)
+    picked = hf[5 + pi]
+    g = oracle.context(m, h)
+    # LN0 of the picked coordinates: an increasing affine map with mean 0
+    assert abs(g.mean()) < 1e-12
+    assert np.corrcoef(g, picked)[0, 1] > 1 - 1e-12
+    np.testing.assert_allclose(g, (picked - picked.mean()) / np.sqrt(picked.var() + 1e-5), atol=1e-12)
+
+
+def test_candidate_fuse_concatenation_order():
+    rng = np.random.default_rng(5)
+    d, r = 64, 16
+    m, w = tiny_model(rng, d=d, r=r, perturb=True)
+    e = synth.make_embedding(rng, 1, d)[0]
+    g = rng.standard_normal(r)
+    gam, bet = w["ln_gamma"].astype(np.float64), w["ln_beta"].astype(np.float64)
+    # W_fuse = [I | 0]: z depends on b only;  LN0 of an already-normalised b is b / sqrt(var(b)+eps)
+    w["w_fuse"] = np.hstack([np.eye(r), np.zeros((r, r))]).astype(np.float32)
+    m = oracle.Model(w, V=257, d=d, slots=6, K=4, r=r, H=24)
+    b, z = oracle.candidate(m, e, g)
+    np.testing.assert_allclose(z, gam * b / np.sqrt(b.var() + 1e-5) + bet, atol=1e-12)
+    # W_fuse = [0 | I]: z depends on g only
+    w["w_fuse"] = np.hstack([np.zeros((r, r)), np.eye(r)]).astype(np.float32)
+    m = oracle.Model(w, V=257, d=d, slots=6, K=4, r=r, H=24)
+    _, z2 = oracle.candidate(m, e, g)
+    e_other = synth.make_embedding(rng, 1, d)[0]
+    _, z3 = oracle.candidate(m, e_other, g)
+    np.testing.assert_allclose(z2, gam * (g - g.mean()) / np.sqrt(g.var() + 1e-5) + bet, atol=1e-12)
+    np.testing.assert_allclose(z2, z3, atol=1e-15)
+
+
+def test_candidate_reads_rows_of_w_cand():
+    rng = np.random.default_rng(6)
+    d, r = 64, 16
+    m, w = tiny_model(rng, d=d, r=r)
+    W, pi = perm_matrix(rng, r, d, offset=11)
+    w["w_cand"] = W
+    m = oracle.Model(w, V=257, d=d, slots=6, K=4, r=r, H=24)
+    e = synth.make_embedding(rng, 1, d, std=1.0)[0]
+    picked = synth.bf16_to_f32(e).astype(np.float64)[11 + pi]
+    b, _ = oracle.candidate(m, e, np.zeros(r))
+    np.testing.assert_allclose(b, (picked - picked.mean()) / np.sqrt(picked.var() + 1e-5), atol=1e-12)
+
+
+def test_pair_state_orientation():
+    rng = np.random.default_rng(8)
+    d, r = 64, 16
+    m, w = tiny_model(rng, d=d, r=r)
+    hp, hq = synth.make_hidden(rng, 1, 2, d)[0]
+    hpf, hqf = (synth.bf16_to_f32(x).astype(np.float64) for x in (hp, hq))
+    W, pi = perm_matrix(rng, r, 2 * d, offset=3)          # selects from h_p
+    w["w_pair"] = W
+    s = oracle.pair_state(oracle.Model(w, V=257, d=d, slots=6, K=4, r=r, H=24), hp, hq)
+    np.testing.assert_array_equal(s, hpf[3 + pi])
+    W, pi = perm_matrix(rng, r, 2 * d, offset=d + 9)      # selects from h_{p+1}
+    w["w_pair"] = W
+    s = oracle.pair_state(oracle.Model(w, V=257, d=d, slots=6, K=4, r=r, H=24), hp, hq)
+    np.testing.assert_array_equal(s, hqf[9 + pi])
+
+
+@pytest.mark.parametrize("block", ["s", "z_a", "z_b", "l_a", "l_b"])
+def test_transition_single_feature_probe(block):
+    """One nonzero W1 entry turns Delta into beta*GELU(alpha*x_c) + delta:
+    pins the MLP's input order [s; z_a; z_b; l_a; l_b] and the l_b base term."""
+    rng = np.random.default_rng(9)
+    r, H = 16, 24
+    m, w = tiny_model(rng, r=r, H=H)
+    s, za, zb = (rng.standard_normal(r) for _ in range(3))
+    la, lb = 3.25, -1.5
+    c = {"s": 5, "z_a": r + 7, "z_b": 2 * r + 2, "l_a": 3 * r, "l_b": 3 * r + 1}[block]
+    feat = {"s": s[5], "z_a": za[7], "z_b": zb[2], "l_a": la, "l_b": lb}[block]
+    alpha, beta, delta, j0 = 0.7, -1.3, 0.25, 11
+    w["w1"] = np.zeros((H, 3 * r + 2), np.float32); w["w1"][j0, c] = alpha
+    w["b1"] = np.zeros(H, np.float32); w["b1"][j0] = 0.125
+    w["w2"] = np.zeros(H, np.float32); w["w2"][j0] = beta
+    w["b2"] = np.array([delta], np.float32)
+    m = oracle.Model(w, V=257, d=64, slots=6, K=4, r=r, H=H)
+    got = oracle.transition(m, s, za, zb, la, lb)
+    x = np.float64(np.float32(alpha)) * feat + 0.125
+    want = lb + delta + np.float64(np.float32(beta)) * x * norm.cdf(x)
+    assert abs(got - want) < 1e-12
+
+
+def test_zero_output_layer_reproduces_draft_argmax():
+    """DCOCO page: with the MLP output layer zero-initialised, Delta = 0, every
+    transition equals the successor's draft logit and the walk returns the
+    per-slot draft argmax."""
+    rng = np.random.default_rng(10)
+    V, d, slots, K = 600, 64, 16, 8
+    m, _ = tiny_model(rng, V=V, d=d, K=K, slots=slots, zero_out=True)
+    logits = synth.make_logits(rng, 1, slots, V, 16, (4, 12))
+    hidden = synth.make_hidden(rng, 1, slots, d)
+    E = synth.make_embedding(rng, V, d)
+    out = oracle.correct_request(m, logits[0], hidden[0], E)
+    ids, vals = out["topk_ids"], out["topk_val"]
+    for p in range(slots - 2):
+        np.testing.assert_array_equal(out["scores"][p], np.broadcast_to(vals[p + 1], (K, K)))
+    np.testing.assert_array_equal(out["choice"], 0)
+    np.testing.assert_array_equal(out["tokens"], ids[:, 0])
+    # and the per-slot argmax is the plain argmax of each row (lowest id on ties)
+    for i in range(slots - 1):
+        f = synth.bf16_to_f32(logits[0, i + 1]).astype(np.float64)
+        assert ids[i, 0] == int(np.flatnonzero(f == f.max())[0])
+
+
+# --------------------------------------------------------------- walk
+def test_walk_golden(golden_dir):
+    g = json.load(open(os.path.join(golden_dir, "walk_example.json")))
+    choice, margin = oracle.walk(np.array(g["scores"]))
+    assert list(choice) == g["choice"]
+    np.testing.assert_allclose(margin, g["margin"], atol=0)
+    assert list(choice) != g["transposed_choice_would_be"]
+
+
+def test_walk_brute_force_random():
+    rng = np.random.default_rng(11)
+    for _ in range(30):
+        P, K = int(rng.integers(1, 15)), int(rng.integers(2, 33))
+        sc = np.round(rng.standard_normal((P, K, K)), 1)  # ties happen
+        choice, margin = oracle.walk(sc)
+        k = 0
+        assert choice[0] == 0
+        for p in range(P):
+            row = sc[p, k]
+            best = min(b for b in range(K) if row[b] == row.max())
+            second = max(row[b] for b in range(K) if b != best)
+            assert choice[p + 1] == best
+            assert margin[p] == row[best] - second
+            k = best
+
+
+# --------------------------------------------------------------- cosine variant
+def test_cosine_vectors_and_transition():
+    rng = np.random.default_rng(12)
+    d, r = 64, 16
+    m, w = tiny_model(rng, d=d, r=r)
+    e1, e2 = synth.make_embedding(rng, 2, d, std=1.0)
+    h1, h2 = synth.make_hidden(rng, 1, 2, d)[0]
+    o, _ = oracle.cosine_vectors(m, e1, h1)
+    _, i2 = oracle.cosine_vectors(m, e2, h2)
+    assert abs(np.linalg.norm(o) - 1) < 1e-12 and abs(np.linalg.norm(i2) - 1) < 1e-12
+    # the raw projection, its out/in halves, cosine against scipy's routine
+    x1 = np.concatenate([synth.bf16_to_f32(e1), synth.bf16_to_f32(h1)]).astype(np.float64)
+    x2 = np.concatenate([synth.bf16_to_f32(e2), synth.bf16_to_f32(h2)]).astype(np.float64)
+    Wio = w["w_io"].astype(np.float64)
+    cos = 1.0 - scipy_cosine_distance((Wio @ x1)[:r], (Wio @ x2)[r:])
+    sigma, lb = 2.5, 0.75
+    assert abs(oracle.cosine_transition(sigma, o, i2, lb) - (sigma * cos + lb)) < 1e-12
+    # out rows = in rows -> a candidate matched with itself scores sigma + l
+    w2 = dict(w); w2["w_io"] = np.vstack([w["w_io"][:r], w["w_io"][:r]])
+    m2 = oracle.Model(w2, V=257, d=d, slots=6, K=4, r=r, H=24)
+    oo, ii = oracle.cosine_vectors(m2, e1, h1)
+    assert abs(oracle.cosine_transition(sigma, oo, ii, lb) - (sigma + lb)) < 1e-12
+
+
+# --------------------------------------------------------------- the decomposition the GPU uses
+def test_layer1_decomposition_identity():
+    """W1 [s; z_a; z_b; l_a; l_b] = W1_s s + (W1_a z_a + w_la l_a) + (W1_b z_b + w_lb l_b):
+    the per-pair / per-candidate split used on the GPU reproduces the oracle's direct MLP."""
+    rng = np.random.default_rng(13)
+    r, H = 16, 24
+    m, w = tiny_model(rng, r=r, H=H, perturb=True)
+    W1 = w["w1"].astype(np.float64)
+    for _ in range(5):
+        s, za, zb = (rng.standard_normal(r) for _ in range(3))
+        la, lb = rng.standard_normal(2) * 5
+        P = W1[:, :r] @ s + w["b1"]
+        U = W1[:, r:2 * r] @ za + W1[:, 3 * r] * la
+        Vv = W1[:, 2 * r:3 * r] @ zb + W1[:, 3 * r + 1] * lb
+        x = P + U + Vv
+        dec = lb + w["b2"][0] + np.dot(w["w2"], x * norm.cdf(x))
+        assert abs(dec - oracle.transition(m, s, za, zb, la, lb)) < 1e-12
+
+
+def test_oracle_batch_matches_requests():
+    rng = np.random.default_rng(14)
+    V, d, slots, K = 400, 64, 6, 4
+    m, _ = tiny_model(rng, V=V, d=d, K=K, slots=slots)
+    logits = synth.make_logits(rng, 3, slots, V, 8, (4, 12), stride=408)
+    hidden = synth.make_hidden(rng, 3, slots, d)
+    E = synth.make_embedding(rng, V, d)
+    tg = synth.draw_targets(rng, np.stack([np.stack([oracle.topk_row(logits[n, i + 1, :V], 4)[0]
+                                                      for i in range(slots - 1)]) for n in range(3)]), V)
+    full = oracle.correct_batch(m, logits, hidden, E, tg, threads=3)
+    for n in range(3):
+        one = oracle.correct_request(m, logits[n], hidden[n], E, tg[n])
+        np.testing.assert_array_equal(one["tokens"], full["tokens"][n])
+        assert one["accept_len"] == full["accept_len"][n]
+        np.testing.assert_array_equal(one["scores"], full["scores"][n])
