@@ -1,0 +1,426 @@
+#!/usr/bin/env python
+"""Benchmark: corrected draft blocks/s at batch 32, Qwen3-8B shapes, and the
+fraction of the HBM roofline.
+
+A step is one call of the whole correction path (top-K, candidate
+representations, K x K transition scores, greedy walk, greedy verify) on one
+batch of 32 requests x 16 slots x V = 151,936 bf16 logits, d = 4096 hidden
+states, K = 16, r = 128, MLP 386 -> 256 -> 1.  Inputs are synthetic and
+seeded (recipe in synth/), generated on the GPU before timing; the step reads
+them from HBM.  Four input sets rotate so that every step's logits were last
+touched three steps earlier (4 x 160 MB > 129 MB L2), and the candidate rows
+are gathered from a 1.2 GB embedding table.
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle on
+the host cores instead (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "corrected draft blocks/s at batch 32, Qwen3-8B shapes; % of HBM roofline"
+WORKLOAD = dict(name="qwen3_8b_c32", N=32, slots=16, V=151936, d=4096, K=16, r=128, H=256,
+                planted=32, boost=(4.0, 12.0))
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--sets", type=int, default=4, help="rotating input sets")
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-requests", type=int, default=16,
+                    help="requests in the CPU-oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return dict(hbm_gbs=j["hbm_gbs"], bf16_tflops=j["bf16_tflops"],
+                    bf16_tflops_sustained=j.get("bf16_tflops_sustained"),
+                    sm_max_mhz=j.get("sm_max_mhz", 2070.0), source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, sm_max_mhz=2070.0,
+                source="fallback")
+
+
+# ------------------------------------------------------------------ per-stage algorithmic work
+def stage_model(w, pk):
+    """stage -> (bound, unit, algorithmic amount per launch, peak).  Bytes are
+    the bytes the step must move from HBM; flops are multiply-adds x 2."""
+    N, B, V, d, K, r, H = w["N"], w["slots"] - 1, w["V"], w["d"], w["K"], w["r"], w["H"]
+    alu_peak = 152 * 128 * 2 * pk["sm_max_mhz"] * 1e6 / 1e12  # fp32 FMA lanes, TFLOP/s
+    return {
+        "topk": ("hbm", "GB/s", N * B * V * 2, pk["hbm_gbs"]),
+        "slot_proj": ("hbm", "GB/s", N * B * d * 2, pk["hbm_gbs"]),
+        "slot_post": ("alu", "TFLOP/s", 2 * N * (B * r * r + (B - 1) * r * H), alu_peak),
+        "cand_proj": ("hbm", "GB/s", N * B * K * d * 2, pk["hbm_gbs"]),
+        "cand_post": ("alu", "TFLOP/s", 2 * N * B * K * (r * r + 2 * r * H), alu_peak),
+        "pair_score": ("alu", "TFLOP/s", 2 * N * (B - 1) * K * K * H, alu_peak),
+        "walk_verify": ("latency", "us", 0, None),
+    }
+
+
+def kernel_traffic(kernel: str):
+    """dram bytes per launch from a committed ncu summary, if its source hash is current."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    for fn in sorted(os.listdir(pdir)):
+        if not fn.endswith(".txt"):
+            continue
+        txt = open(os.path.join(pdir, fn)).read()
+        m = re.search(rf"^traffic_bytes_per_launch\[{kernel}\]:\s*([0-9.e+]+)\s+source_sha256:\s*(\w+)"
+                      rf"\s+source:\s*(\S+)", txt, re.M)
+        if not m:
+            continue
+        src = os.path.join(ROOT, m.group(3))
+        if os.path.exists(src) and hashlib.sha256(open(src, "rb").read()).hexdigest() == m.group(2):
+            return float(m.group(1))
+    return None
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(gpu_index), "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        win = [p for (t, p) in self.samples if t0 <= t <= t1]
+        note = "timed region"
+        if len(win) < 3:  # region shorter than a few sample periods: widen to the whole run
+            win = [p for (_, p) in self.samples]
+            note = "whole run (timed region shorter than the sampling period)"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in win if num(p[0]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in win for i in range(4) if p[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(win[0][1]), "power_w_max": max((num(p[2]) or 0) for p in win),
+                "reasons": reasons, "samples": len(win), "window": note}
+
+
+# ------------------------------------------------------------------ inputs (GPU, seeded)
+def gpu_inputs(torch, seed: int, w, device, with_targets=True):
+    """The synth recipe, drawn with torch's CUDA generator."""
+    N, S, V, d = w["N"], w["slots"], w["V"], w["d"]
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    x = torch.randn(N * S, V, generator=g, device=device) * 2.0
+    keys = torch.rand(N * S, V, generator=g, device=device)
+    ids = keys.argsort(dim=1)[:, :w["planted"]]
+    del keys
+    lo, hi = w["boost"]
+    boost = torch.rand(N * S, w["planted"], generator=g, device=device) * (hi - lo) + lo
+    x.scatter_add_(1, ids, boost)
+    logits = x.to(torch.bfloat16).view(N, S, V)
+    del x
+    hidden = torch.randn(N, S, d, generator=g, device=device).to(torch.bfloat16)
+    targets = None
+    if with_targets:
+        top16 = logits[:, 1:].float().topk(16, dim=-1).indices  # input recipe only
+        hit = torch.rand(N, S - 1, generator=g, device=device) < 0.6
+        pick = torch.randint(0, 16, (N, S - 1, 1), generator=g, device=device)
+        uni = torch.randint(0, V, (N, S - 1), generator=g, device=device)
+        targets = torch.where(hit, top16.gather(2, pick)[..., 0], uni).to(torch.int32)
+    return logits, hidden, targets
+
+
+def gpu_embedding(torch, seed, V, d, device):
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    E = torch.empty(V, d, dtype=torch.bfloat16, device=device)
+    step = 16384
+    for r0 in range(0, V, step):
+        r1 = min(V, r0 + step)
+        E[r0:r1] = (torch.randn(r1 - r0, d, generator=g, device=device) * 0.02).to(torch.bfloat16)
+    return E
+
+
+# ------------------------------------------------------------------ CPU oracle baseline
+def cpu_baseline(w, n_req: int, logits_np, hidden_np, E_np, targets_np, weights_np):
+    import oracle
+    m = oracle.Model(weights_np, V=w["V"], d=w["d"], slots=w["slots"], K=w["K"])
+    threads = os.cpu_count() or 1
+    req = list(range(min(n_req, w["N"])))
+    oracle.correct_batch(m, logits_np[:1], hidden_np[:1], E_np, targets_np[:1], requests=[0],
+                         threads=1)  # load + page-in
+    t0 = time.perf_counter()
+    oracle.correct_batch(m, logits_np, hidden_np, E_np, targets_np, requests=req, threads=threads)
+    dt = time.perf_counter() - t0
+    return {"value": len(req) / dt, "unit": "blocks/s", "cores": min(threads, len(req)),
+            "kind": "oracle",
+            "sample": f"{len(req)} of the 32 requests of one input set, one thread per request, "
+                      f"{dt:.2f} s wall on {threads} host cores"}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import draft_correction_slot_gb300 as dc
+    import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+    w = dict(WORKLOAD)
+    pk = peaks()
+    N, S, V, d, K = w["N"], w["slots"], w["V"], w["d"], w["K"]
+    B = S - 1
+
+    weights_np = synth.make_weights(np.random.default_rng(7 + rank), d)
+    E = gpu_embedding(torch, 11 + rank, V, d, device)
+    sets = [gpu_inputs(torch, 1000 + 97 * rank + s, w, device) for s in range(args.sets)]
+    corr = dc.Corrector({k: torch.from_numpy(v) for k, v in weights_np.items()}, V, d, S, K,
+                        max_batch=N, host_staging=True)
+    outs = [corr.alloc_outputs(N, device, full=False) for _ in range(args.sets)]
+    torch.cuda.synchronize()
+
+    def step(i):
+        lg, hd, tg = sets[i % args.sets]
+        corr.correct(lg, hd, E, tg, out=outs[i % args.sets], full=False)
+
+    sampler = ClockSampler(local)
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    launches0 = dc.dcoco_kernel_launches(corr.handle)
+    torch.cuda.synchronize()
+    t_host0 = time.time()
+    ev[0].record()
+    for i in range(args.steps):
+        step(args.warmup + i)
+        ev[i + 1].record()
+    torch.cuda.synchronize()
+    t_host1 = time.time()
+    if world > 1:
+        dist.barrier()
+    launches = dc.dcoco_kernel_launches(corr.handle) - launches0
+    total_ms = ev[0].elapsed_time(ev[-1])
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    if world > 1:
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    clocks = sampler.summary(t_host0, t_host1)
+
+    # per-kernel times, live, with stage events on the same stream
+    dc.dcoco_stage_timing(corr.handle, True)
+    n_stage_calls = min(args.steps, 200)
+    for i in range(n_stage_calls):
+        step(i)
+    stage_ms, calls = dc.dcoco_stage_read(corr.handle)
+    dc.dcoco_stage_timing(corr.handle, False)
+    sampler.stop()
+    model = stage_model(w, pk)
+    stages = {}
+    for name, ms in stage_ms.items():
+        avg_s = ms / max(calls, 1) / 1e3
+        bound, unit, amount, peak = model.get(name, ("latency", "us", 0, None))
+        ent = {"us": avg_s * 1e6, "share": ms / max(sum(stage_ms.values()), 1e-9), "bound": bound}
+        if bound == "hbm":
+            ent.update(achieved=amount / avg_s / 1e9, unit="GB/s", peak=peak, frac=amount / avg_s / 1e9 / peak,
+                       bytes=amount)
+        elif bound == "alu":
+            ent.update(achieved=amount / avg_s / 1e12, unit="TFLOP/s", peak=peak,
+                       frac=amount / avg_s / 1e12 / peak, flops=amount)
+        stages[name] = ent
+    dom = max(stages, key=lambda k: stages[k]["us"])
+    de = stages[dom]
+    roofline = {"kernel": dom, "bound": de["bound"], "achieved": de.get("achieved"),
+                "peak": de.get("peak"), "unit": de.get("unit"), "frac": de.get("frac"),
+                "traffic": kernel_traffic(dom),
+                "peak_source": f"{pk['source']} ({'hbm_gbs' if de['bound'] == 'hbm' else 'fp32 FMA lanes x sm_max_mhz'})"}
+
+    # whole step against the path's byte floor
+    path_bytes = N * B * V * 2 + N * B * K * d * 2
+    step_s = total_ms / args.steps / 1e3
+    value = world * N / step_s
+
+    # e2e: host buffers through the C ABI (copies inside the timed region)
+    e2e = None
+    if args.e2e_steps > 0:
+        lg, hd, tg = sets[0]
+        lg_h = lg.view(torch.int16).cpu().pin_memory()
+        hd_h = hd.view(torch.int16).cpu().pin_memory()
+        tg_h = tg.cpu().pin_memory()
+        tok_h = torch.empty(N, B, dtype=torch.int32).pin_memory()
+        acc_h = torch.empty(N, dtype=torch.int32).pin_memory()
+        for _ in range(3):
+            dc.dcoco_correct_host(corr.handle, corr.weights, N, lg_h, hd_h, E, tg_h, tokens=tok_h,
+                                  accept_len=acc_h)
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            dc.dcoco_correct_host(corr.handle, corr.weights, N, lg_h, hd_h, E, tg_h, tokens=tok_h,
+                                  accept_len=acc_h)
+        dt = (time.perf_counter() - t0) / args.e2e_steps
+        if world > 1:
+            t = torch.tensor([dt], device=device)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            dt = float(t.item())
+        e2e = {"value": world * N / dt, "unit": "blocks/s",
+               "h2d_bytes_per_step": lg_h.numel() * 2 + hd_h.numel() * 2 + tg_h.numel() * 4,
+               "d2h_bytes_per_step": tok_h.numel() * 4 + acc_h.numel() * 4,
+               "ms_per_step": dt * 1e3, "api": "dcoco_correct_host (pinned host buffers)"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        lg, hd, tg = sets[0]
+        cpu = cpu_baseline(w, args.cpu_requests, lg.view(torch.int16).cpu().numpy().view(np.uint16),
+                           hd.view(torch.int16).cpu().numpy().view(np.uint16),
+                           E.view(torch.int16).cpu().numpy().view(np.uint16), tg.cpu().numpy(), weights_np)
+    corr.close()
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "blocks/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded, synth/ recipe drawn on the GPU)",
+            "config": {"workload": "qwen3_8b_c32: 32 requests x 16 slots (1 anchor + 15 draft) x "
+                                   "V=151936 bf16 logits, d=4096 bf16 hidden, E[151936,4096] bf16, "
+                                   "K=16, r=128, MLP 386-256-1 fp32 weights",
+                       "global_batch": world * N, "per_gpu_batch": N, "parallelism": f"replicas x{world}",
+                       "inputs": "bf16; arithmetic fp32",
+                       "l2": f"{args.sets} rotating input sets of 160 MB (> 129 MB L2), no flush"},
+            "us_per_block": step_s * 1e6 / N,
+            "step_us": {"p10": 1e3 * sorted(per)[len(per) // 10], "p50": 1e3 * statistics.median(per),
+                        "p90": 1e3 * sorted(per)[(9 * len(per)) // 10]},
+            "path_hbm_roofline": {"bytes_per_step": path_bytes, "achieved_gbs": path_bytes / step_s / 1e9,
+                                  "peak_gbs": pk["hbm_gbs"],
+                                  "frac": path_bytes / step_s / 1e9 / pk["hbm_gbs"],
+                                  "note": f"logits + gathered embedding rows over {pk['source']} HBM peak"},
+            "roofline": roofline, "stages": stages, "cpu_baseline": cpu, "e2e": e2e,
+            "clocks": clocks, "gpu_launches": launches,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ reference arm (CPU oracle)
+def run_reference(args):
+    import numpy as np
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    import synth
+    oracle.build()
+    w = dict(WORKLOAD)
+    threads = os.cpu_count() or 1
+    per_step = max(1, min(threads, w["N"]))
+    rng = np.random.default_rng(1234)
+    log(f"[reference] generating inputs ({per_step} requests, embedding table {w['V']}x{w['d']})")
+    logits = synth.make_logits(rng, per_step, w["slots"], w["V"], w["planted"], w["boost"])
+    hidden = synth.make_hidden(rng, per_step, w["slots"], w["d"])
+    E = synth.make_embedding(rng, w["V"], w["d"])
+    weights = synth.make_weights(rng, w["d"])
+    m = oracle.Model(weights, V=w["V"], d=w["d"], slots=w["slots"], K=w["K"])
+    top16 = np.stack([np.stack([oracle.topk_row(logits[n, i + 1], 16)[0] for i in range(w["slots"] - 1)])
+                      for n in range(per_step)])
+    targets = synth.draw_targets(rng, top16, w["V"])
+
+    def step():
+        oracle.correct_batch(m, logits, hidden, E, targets, threads=threads)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = time.perf_counter() - t0
+    value = per_step * args.steps / dt
+    line = {
+        "metric": METRIC, "value": value, "unit": "blocks/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, synth/ recipe)",
+        "impl": "reference",
+        "config": {"workload": "qwen3_8b_c32 (per-step sample: see cpu_baseline)", "global_batch": w["N"],
+                   "per_gpu_batch": w["N"], "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "blocks/s", "cores": threads, "kind": "oracle",
+                         "sample": f"each step: {per_step} of the 32 requests, one host thread each"},
+        "e2e": {"value": value, "unit": "blocks/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

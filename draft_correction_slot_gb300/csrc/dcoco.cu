@@ -1,0 +1,589 @@
+// dcoco.cu -- C ABI: argument validation, workspace, weight packing and the
+// launch sequence of the correction path (declared in include/dcoco.h).
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/dcoco.h"
+#include "kernels.h"
+
+namespace {
+
+constexpr int kR = 128;
+constexpr int kH = 256;
+
+struct Workspace {
+  unsigned long long *part = nullptr;
+  unsigned *row_count = nullptr;
+  int32_t *ids = nullptr;
+  float *vals = nullptr;
+  float *slot_proj = nullptr;  // [N*B][3r]  (variant 1: [N*B][2r])
+  float *cand_proj = nullptr;  // [N*B*K][r] (variant 1: [N*B*K][2r])
+  float *Gf = nullptr;         // [N*B][r]
+  float *P = nullptr;          // [N*(B-1)][H]
+  float *U = nullptr;          // [N*B*K][H]  (variant 1: O [N*B*K][r])
+  float *V = nullptr;          // [N*B*K][H]  (variant 1: I [N*B*K][r])
+  float *scores = nullptr;     // [N*(B-1)][K][K]
+  int32_t *choice = nullptr;   // [N*B]
+  float *margin = nullptr;     // [N*(B-1)]
+  int *err = nullptr;          // device status word
+  // host staging (dcoco_correct_host)
+  uint16_t *st_logits = nullptr;  // [N][slots][st_stride]
+  int64_t st_stride = 0;
+  uint16_t *st_hidden = nullptr;  // [N][slots][d]
+  int32_t *st_target = nullptr;   // [N*B]
+  int32_t *st_tokens = nullptr;   // [N*B]
+  int32_t *st_accept = nullptr;   // [N]
+};
+
+}  // namespace
+
+namespace {
+constexpr int kMaxStages = 8;
+constexpr int kMaxTimedCalls = 1024;
+const char *const kStageNames[2][kMaxStages] = {
+    {"topk", "slot_proj", "slot_post", "cand_proj", "cand_post", "pair_score", "walk_verify", nullptr},
+    {"topk", "slot_proj", "cand_proj", "cos_post", "cos_score", "walk_verify", nullptr, nullptr}};
+int stage_count(int variant) {
+  int n = 0;
+  while (n < kMaxStages && kStageNames[variant][n]) ++n;
+  return n;
+}
+}  // namespace
+
+struct dcoco_handle {
+  dcoco_config cfg;
+  int device = 0;
+  int B = 0;
+  dc::TopkPlan plan{};
+  void *block = nullptr;  // one device allocation holding the workspace
+  Workspace ws;
+  cudaStream_t last_stream = nullptr;
+  long long launches = 0;            // kernels launched so far
+  bool timing = false;               // record per-stage events
+  int timed_calls = 0;               // calls recorded since the last read
+  std::vector<cudaEvent_t> events;   // kMaxTimedCalls x (stages + 1), created on demand
+};
+
+struct dcoco_weights {
+  const dcoco_handle *owner = nullptr;
+  int device = 0;
+  void *block = nullptr;
+  float *w_cand = nullptr;  // [r][d]
+  float *w_slot = nullptr;  // [3r][d] = W_ctx ; W_pair[:, :d] ; W_pair[:, d:]
+  float *w_io_e = nullptr;  // [2r][d]  W_io[:, :d]
+  float *w_io_h = nullptr;  // [2r][d]  W_io[:, d:]
+  dc::MlpWeightsDev mlp{};
+};
+
+namespace {
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Carver {  // sub-allocates a byte range, 256-byte aligned pieces
+  size_t off = 0;
+  char *base = nullptr;
+  template <class T>
+  T *take(size_t n) {
+    off = (off + 255) & ~size_t(255);
+    T *p = base ? reinterpret_cast<T *>(base + off) : nullptr;
+    off += n * sizeof(T);
+    return p;
+  }
+};
+
+void carve_workspace(Carver &c, const dcoco_config &cfg, int B, const dc::TopkPlan &plan,
+                     Workspace &ws) {
+  const size_t N = (size_t)cfg.max_batch, K = (size_t)cfg.topk, d = (size_t)cfg.hidden;
+  const size_t rows = N * B, cands = rows * K;
+  ws.part = c.take<unsigned long long>(rows * plan.nchunks * K);
+  ws.row_count = c.take<unsigned>(rows);
+  ws.ids = c.take<int32_t>(cands);
+  ws.vals = c.take<float>(cands);
+  ws.slot_proj = c.take<float>(rows * 3 * kR);
+  ws.cand_proj = c.take<float>(cands * 2 * kR);
+  ws.Gf = c.take<float>(rows * kR);
+  ws.P = c.take<float>(N * (B - 1) * kH);
+  ws.U = c.take<float>(cands * kH);
+  ws.V = c.take<float>(cands * kH);
+  ws.scores = c.take<float>(N * (B - 1) * K * K);
+  ws.choice = c.take<int32_t>(rows);
+  ws.margin = c.take<float>(N * (B - 1));
+  ws.err = c.take<int>(1);
+  if (cfg.host_staging) {
+    ws.st_stride = ((int64_t)cfg.vocab + 7) & ~int64_t(7);
+    ws.st_logits = c.take<uint16_t>(N * cfg.slots * (size_t)ws.st_stride);
+    ws.st_hidden = c.take<uint16_t>(N * cfg.slots * d);
+    ws.st_target = c.take<int32_t>(rows);
+    ws.st_tokens = c.take<int32_t>(rows);
+    ws.st_accept = c.take<int32_t>(N);
+  }
+}
+
+int validate_config(const dcoco_config *cfg) {
+  if (!cfg) return DCOCO_EINVAL;
+  if (cfg->rank != kR || cfg->mlp_hidden != kH) return DCOCO_EUNSUPPORTED;
+  if (cfg->topk != 8 && cfg->topk != 16 && cfg->topk != 32) return DCOCO_EUNSUPPORTED;
+  if (cfg->variant != 0 && cfg->variant != 1) return DCOCO_EUNSUPPORTED;
+  if (cfg->slots < 3 || cfg->slots > 32) return DCOCO_EUNSUPPORTED;
+  if (cfg->vocab < cfg->topk || cfg->vocab > (1 << 20)) return DCOCO_EINVAL;
+  if (cfg->hidden <= 0 || cfg->hidden % 64 != 0) return DCOCO_EINVAL;
+  if (cfg->max_batch < 1 || cfg->max_batch > (1 << 16)) return DCOCO_EINVAL;
+  if (!(cfg->ln_eps > 0.f)) return DCOCO_EINVAL;
+  if (dc::topk_plan(cfg->vocab).nchunks > dc::kTopkMaxChunks) return DCOCO_EUNSUPPORTED;
+  return DCOCO_OK;
+}
+
+int validate_call(const dcoco_handle *h, const dcoco_weights *w, int batch, const dcoco_inputs *in,
+                  const dcoco_outputs *out, bool device_ptrs) {
+  if (!h || !w || !in || !out) return DCOCO_EINVAL;
+  if (w->owner != h) return DCOCO_EINVAL;
+  if (batch < 0 || batch > h->cfg.max_batch) return DCOCO_EBATCH;
+  if (batch == 0) return DCOCO_OK;
+  if (!in->logits || !in->hidden || !in->cand_embed || !out->tokens) return DCOCO_EINVAL;
+  if (in->target_tokens && !out->accept_len) return DCOCO_EINVAL;
+  if (in->logits_slot_stride < h->cfg.vocab) return DCOCO_EINVAL;
+  if (device_ptrs) {
+    if (in->logits_slot_stride % 8 != 0) return DCOCO_EINVAL;
+    if (!aligned16(in->logits) || !aligned16(in->hidden) || !aligned16(in->cand_embed))
+      return DCOCO_EINVAL;
+  } else if (!aligned16(in->cand_embed)) {
+    return DCOCO_EINVAL;
+  }
+  return DCOCO_OK;
+}
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? DCOCO_OK : DCOCO_ECUDA; }
+
+#define DC_TRY(expr)                       \
+  do {                                     \
+    cudaError_t e_ = (expr);               \
+    if (e_ != cudaSuccess) return DCOCO_ECUDA; \
+  } while (0)
+
+// Records the stage boundaries of one call (when timing is on) and counts
+// the launches.
+struct StageClock {
+  dcoco_handle *h;
+  cudaStream_t st;
+  cudaEvent_t *ev = nullptr;  // stages + 1 events of this call, or null
+  int s = 0;
+  StageClock(dcoco_handle *h_, cudaStream_t st_) : h(h_), st(st_) {
+    if (h->timing && h->timed_calls < kMaxTimedCalls) {
+      const int ns = stage_count(h->cfg.variant) + 1;
+      ev = h->events.data() + (size_t)h->timed_calls * ns;
+      ++h->timed_calls;
+      cudaEventRecord(ev[0], st);
+    }
+  }
+  cudaError_t done(cudaError_t e) {
+    ++h->launches;
+    ++s;
+    if (e == cudaSuccess && ev) e = cudaEventRecord(ev[s], st);
+    return e;
+  }
+};
+
+// The launch sequence; all pointers are device pointers and validated.
+int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs *in,
+             const dcoco_outputs *out, cudaStream_t st) {
+  const dcoco_config &cfg = h->cfg;
+  const Workspace &ws = h->ws;
+  const int B = h->B, K = cfg.topk, d = cfg.hidden, V = cfg.vocab;
+  const uint16_t *logits = static_cast<const uint16_t *>(in->logits);
+  const uint16_t *hidden = static_cast<const uint16_t *>(in->hidden);
+  const uint16_t *E = static_cast<const uint16_t *>(in->cand_embed);
+  int32_t *ids = out->topk_ids ? out->topk_ids : ws.ids;
+  float *vals = out->topk_val ? out->topk_val : ws.vals;
+  float *scores = out->scores ? out->scores : ws.scores;
+  int32_t *choice = out->choice ? out->choice : ws.choice;
+  float *margin = out->margin ? out->margin : ws.margin;
+  h->last_stream = st;
+  StageClock clk(h, st);
+
+  // step 1: candidate pools
+  DC_TRY(clk.done(dc::launch_topk(K, logits, in->logits_slot_stride, cfg.slots, N, V, h->plan,
+                                  ws.part, ws.row_count, ids, vals, st)));
+  const int rows = N * B, cands = rows * K;
+  if (cfg.variant == 0) {
+    // steps 2-3: slot projections (W_ctx, W_pair halves) and per-slot / per-pair terms
+    DC_TRY(clk.done(dc::launch_rows_gemm(1, hidden, nullptr, cfg.slots, B, rows, d, V, w->w_slot,
+                                         3 * kR, ws.slot_proj, ws.err, st)));
+    DC_TRY(clk.done(dc::launch_slot_post(ws.slot_proj, N, B, cfg.ln_eps, w->mlp, ws.Gf, ws.P, st)));
+    // step 2: candidate projections, then z and the layer-1 partials U, V
+    DC_TRY(clk.done(dc::launch_rows_gemm(0, E, ids, cfg.slots, B, cands, d, V, w->w_cand, kR,
+                                         ws.cand_proj, ws.err, st)));
+    DC_TRY(clk.done(dc::launch_cand_post(K, ws.cand_proj, vals, ws.Gf, N, B, cfg.ln_eps, w->mlp,
+                                         ws.U, ws.V, st)));
+    // step 4: all (B-1) K^2 transition scores
+    DC_TRY(clk.done(dc::launch_pair_score(K, ws.U, ws.V, ws.P, vals, w->mlp.w2, w->mlp.b2, N, B,
+                                          scores, st)));
+  } else {
+    DC_TRY(clk.done(dc::launch_rows_gemm(1, hidden, nullptr, cfg.slots, B, rows, d, V, w->w_io_h,
+                                         2 * kR, ws.slot_proj, ws.err, st)));
+    DC_TRY(clk.done(dc::launch_rows_gemm(0, E, ids, cfg.slots, B, cands, d, V, w->w_io_e, 2 * kR,
+                                         ws.cand_proj, ws.err, st)));
+    DC_TRY(clk.done(dc::launch_cos_post(K, ws.cand_proj, ws.slot_proj, N, B, ws.U, ws.V, st)));
+    DC_TRY(clk.done(dc::launch_cos_score(K, ws.U, ws.V, vals, cfg.sigma, N, B, scores, st)));
+  }
+  // step 5: walk + verify
+  DC_TRY(clk.done(dc::launch_walk_verify(K, scores, ids, in->target_tokens, N, B, out->tokens,
+                                         choice, margin,
+                                         in->target_tokens ? out->accept_len : nullptr, st)));
+  return DCOCO_OK;
+}
+
+// Host-side packing of the fp32 weights into the device layout.
+void pack_mlp(const dcoco_weight_ptrs &w, int d, std::vector<float> &buf, size_t off[16]) {
+  (void)d;
+  const int r = kR, H = kH, in = 3 * kR + 2;
+  size_t o = 0;
+  auto take = [&](size_t n) { size_t at = (o + 63) & ~size_t(63); o = at + n; return at; };
+  off[0] = take(r * r);  // wfb_t
+  off[1] = take(r * r);  // wfg_t
+  off[2] = take(r);      // gamma
+  off[3] = take(r);      // beta
+  off[4] = take(r * H);  // w1s_t
+  off[5] = take(r * H);  // w1a_t
+  off[6] = take(r * H);  // w1b_t
+  off[7] = take(H);      // w_la
+  off[8] = take(H);      // w_lb
+  off[9] = take(H);      // b1
+  off[10] = take(H);     // w2
+  off[11] = take(1);     // b2
+  off[12] = o;
+  buf.assign(o, 0.f);
+  for (int oo = 0; oo < r; ++oo)
+    for (int k = 0; k < r; ++k) {
+      buf[off[0] + (size_t)k * r + oo] = w.w_fuse[(size_t)oo * 2 * r + k];
+      buf[off[1] + (size_t)k * r + oo] = w.w_fuse[(size_t)oo * 2 * r + r + k];
+    }
+  for (int k = 0; k < r; ++k) {
+    buf[off[2] + k] = w.ln_gamma[k];
+    buf[off[3] + k] = w.ln_beta[k];
+  }
+  for (int j = 0; j < H; ++j) {
+    for (int k = 0; k < r; ++k) {
+      buf[off[4] + (size_t)k * H + j] = w.w1[(size_t)j * in + k];
+      buf[off[5] + (size_t)k * H + j] = w.w1[(size_t)j * in + r + k];
+      buf[off[6] + (size_t)k * H + j] = w.w1[(size_t)j * in + 2 * r + k];
+    }
+    buf[off[7] + j] = w.w1[(size_t)j * in + 3 * r];
+    buf[off[8] + j] = w.w1[(size_t)j * in + 3 * r + 1];
+    buf[off[9] + j] = w.b1[j];
+    buf[off[10] + j] = w.w2[j];
+  }
+  buf[off[11]] = w.b2[0];
+}
+
+}  // namespace
+
+extern "C" {
+
+int dcoco_version(void) { return 100; }
+
+const char *dcoco_status_string(int s) {
+  switch (s) {
+    case DCOCO_OK: return "ok";
+    case DCOCO_EINVAL: return "invalid argument";
+    case DCOCO_EUNSUPPORTED: return "unsupported configuration";
+    case DCOCO_EBATCH: return "batch outside [0, max_batch]";
+    case DCOCO_ECUDA: return "CUDA runtime error";
+    case DCOCO_ENOMEM: return "out of memory";
+    case DCOCO_EDEVICE: return "a kernel flagged bad input data";
+    default: return "unknown status";
+  }
+}
+
+int dcoco_create(const dcoco_config *cfg, dcoco_handle **out) {
+  if (!out) return DCOCO_EINVAL;
+  int rc = validate_config(cfg);
+  if (rc != DCOCO_OK) return rc;
+  dcoco_handle *h = new (std::nothrow) dcoco_handle();
+  if (!h) return DCOCO_ENOMEM;
+  h->cfg = *cfg;
+  h->B = cfg->slots - 1;
+  h->plan = dc::topk_plan(cfg->vocab);
+  if (cudaGetDevice(&h->device) != cudaSuccess) {
+    delete h;
+    return DCOCO_ECUDA;
+  }
+  Carver sizer;
+  carve_workspace(sizer, h->cfg, h->B, h->plan, h->ws);
+  const size_t bytes = sizer.off + 256;
+  if (cudaMalloc(&h->block, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    delete h;
+    return DCOCO_ENOMEM;
+  }
+  Carver c;
+  c.base = static_cast<char *>(h->block);
+  carve_workspace(c, h->cfg, h->B, h->plan, h->ws);
+  if (cudaMemset(h->block, 0, bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+    cudaFree(h->block);
+    delete h;
+    return DCOCO_ECUDA;
+  }
+  *out = h;
+  return DCOCO_OK;
+}
+
+int dcoco_weights_create(dcoco_handle *h, const dcoco_weight_ptrs *wp, void *stream,
+                         dcoco_weights **out) {
+  if (!h || !wp || !out) return DCOCO_EINVAL;
+  const dcoco_config &cfg = h->cfg;
+  const int r = kR, d = cfg.hidden;
+  if (cfg.variant == 0) {
+    if (!wp->w_cand || !wp->w_ctx || !wp->w_fuse || !wp->ln_gamma || !wp->ln_beta || !wp->w_pair ||
+        !wp->w1 || !wp->b1 || !wp->w2 || !wp->b2)
+      return DCOCO_EINVAL;
+  } else if (!wp->w_io) {
+    return DCOCO_EINVAL;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+
+  // Bring the fp32 weights to the host (if needed).
+  auto fetch = [&](const float *p, size_t n, std::vector<float> &dst) -> int {
+    dst.resize(n);
+    if (wp->on_device) {
+      if (cudaMemcpy(dst.data(), p, n * sizeof(float), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return DCOCO_ECUDA;
+    } else {
+      std::memcpy(dst.data(), p, n * sizeof(float));
+    }
+    return DCOCO_OK;
+  };
+  std::vector<float> w_cand, w_ctx, w_fuse, gam, bet, w_pair, w1, b1, w2, b2, w_io;
+  int rc = DCOCO_OK;
+  if (cfg.variant == 0) {
+    if ((rc = fetch(wp->w_cand, (size_t)r * d, w_cand)) || (rc = fetch(wp->w_ctx, (size_t)r * d, w_ctx)) ||
+        (rc = fetch(wp->w_fuse, (size_t)r * 2 * r, w_fuse)) || (rc = fetch(wp->ln_gamma, r, gam)) ||
+        (rc = fetch(wp->ln_beta, r, bet)) || (rc = fetch(wp->w_pair, (size_t)r * 2 * d, w_pair)) ||
+        (rc = fetch(wp->w1, (size_t)kH * (3 * r + 2), w1)) || (rc = fetch(wp->b1, kH, b1)) ||
+        (rc = fetch(wp->w2, kH, w2)) || (rc = fetch(wp->b2, 1, b2)))
+      return rc;
+  } else if ((rc = fetch(wp->w_io, (size_t)2 * r * 2 * d, w_io))) {
+    return rc;
+  }
+
+  // Layout of the device block: [proj weights][mlp pack]
+  std::vector<float> proj;
+  size_t n_proj = 0;
+  if (cfg.variant == 0) {
+    n_proj = (size_t)r * d + (size_t)3 * r * d;
+    proj.resize(n_proj);
+    std::memcpy(proj.data(), w_cand.data(), (size_t)r * d * sizeof(float));
+    float *ws = proj.data() + (size_t)r * d;
+    for (int o = 0; o < r; ++o) {
+      std::memcpy(ws + (size_t)o * d, w_ctx.data() + (size_t)o * d, d * sizeof(float));
+      std::memcpy(ws + (size_t)(r + o) * d, w_pair.data() + (size_t)o * 2 * d, d * sizeof(float));
+      std::memcpy(ws + (size_t)(2 * r + o) * d, w_pair.data() + (size_t)o * 2 * d + d, d * sizeof(float));
+    }
+  } else {
+    n_proj = (size_t)4 * r * d;
+    proj.resize(n_proj);
+    for (int o = 0; o < 2 * r; ++o) {
+      std::memcpy(proj.data() + (size_t)o * d, w_io.data() + (size_t)o * 2 * d, d * sizeof(float));
+      std::memcpy(proj.data() + (size_t)(2 * r + o) * d, w_io.data() + (size_t)o * 2 * d + d,
+                  d * sizeof(float));
+    }
+  }
+  std::vector<float> mlp;
+  size_t off[16] = {};
+  if (cfg.variant == 0) {
+    dcoco_weight_ptrs hw = *wp;
+    hw.w_fuse = w_fuse.data(); hw.ln_gamma = gam.data(); hw.ln_beta = bet.data();
+    hw.w1 = w1.data(); hw.b1 = b1.data(); hw.w2 = w2.data(); hw.b2 = b2.data();
+    pack_mlp(hw, d, mlp, off);
+  }
+  const size_t proj_bytes = ((n_proj * sizeof(float)) + 255) & ~size_t(255);
+  const size_t total = proj_bytes + mlp.size() * sizeof(float) + 256;
+
+  dcoco_weights *w = new (std::nothrow) dcoco_weights();
+  if (!w) return DCOCO_ENOMEM;
+  w->owner = h;
+  w->device = h->device;
+  if (cudaMalloc(&w->block, total) != cudaSuccess) {
+    cudaGetLastError();
+    delete w;
+    return DCOCO_ENOMEM;
+  }
+  char *base = static_cast<char *>(w->block);
+  float *dproj = reinterpret_cast<float *>(base);
+  float *dmlp = reinterpret_cast<float *>(base + proj_bytes);
+  bool ok = cudaMemcpyAsync(dproj, proj.data(), n_proj * sizeof(float), cudaMemcpyHostToDevice, st) ==
+            cudaSuccess;
+  if (ok && !mlp.empty())
+    ok = cudaMemcpyAsync(dmlp, mlp.data(), mlp.size() * sizeof(float), cudaMemcpyHostToDevice, st) ==
+         cudaSuccess;
+  ok = ok && cudaStreamSynchronize(st) == cudaSuccess;
+  if (!ok) {
+    cudaFree(w->block);
+    delete w;
+    return DCOCO_ECUDA;
+  }
+  if (cfg.variant == 0) {
+    w->w_cand = dproj;
+    w->w_slot = dproj + (size_t)r * d;
+    dc::MlpWeightsDev &m = w->mlp;
+    m.wfb_t = dmlp + off[0]; m.wfg_t = dmlp + off[1]; m.gamma = dmlp + off[2]; m.beta = dmlp + off[3];
+    m.w1s_t = dmlp + off[4]; m.w1a_t = dmlp + off[5]; m.w1b_t = dmlp + off[6];
+    m.w_la = dmlp + off[7]; m.w_lb = dmlp + off[8]; m.b1 = dmlp + off[9]; m.w2 = dmlp + off[10];
+    m.b2 = dmlp + off[11];
+  } else {
+    w->w_io_e = dproj;
+    w->w_io_h = dproj + (size_t)2 * r * d;
+  }
+  *out = w;
+  return DCOCO_OK;
+}
+
+int dcoco_correct(dcoco_handle *h, const dcoco_weights *w, int batch, const dcoco_inputs *in,
+                  const dcoco_outputs *out, void *stream) {
+  int rc = validate_call(h, w, batch, in, out, true);
+  if (rc != DCOCO_OK || batch == 0) return rc;
+  return run_path(h, w, batch, in, out, static_cast<cudaStream_t>(stream));
+}
+
+int dcoco_correct_host(dcoco_handle *h, const dcoco_weights *w, int batch, const dcoco_inputs *in,
+                       const dcoco_outputs *out, void *stream) {
+  int rc = validate_call(h, w, batch, in, out, false);
+  if (rc != DCOCO_OK || batch == 0) return rc;
+  if (!h->cfg.host_staging) return DCOCO_EINVAL;
+  const dcoco_config &cfg = h->cfg;
+  const Workspace &ws = h->ws;
+  const int B = h->B, K = cfg.topk;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t rows = (size_t)batch * cfg.slots;
+  // inputs: logits rows (pitched copy to the dense staging stride), hidden, targets
+  DC_TRY(cudaMemcpy2DAsync(ws.st_logits, ws.st_stride * sizeof(uint16_t), in->logits,
+                           in->logits_slot_stride * sizeof(uint16_t), cfg.vocab * sizeof(uint16_t),
+                           rows, cudaMemcpyHostToDevice, st));
+  DC_TRY(cudaMemcpyAsync(ws.st_hidden, in->hidden, rows * cfg.hidden * sizeof(uint16_t),
+                         cudaMemcpyHostToDevice, st));
+  if (in->target_tokens)
+    DC_TRY(cudaMemcpyAsync(ws.st_target, in->target_tokens, (size_t)batch * B * sizeof(int32_t),
+                           cudaMemcpyHostToDevice, st));
+  dcoco_inputs din = *in;
+  din.logits = ws.st_logits;
+  din.logits_slot_stride = ws.st_stride;
+  din.hidden = ws.st_hidden;
+  din.target_tokens = in->target_tokens ? ws.st_target : nullptr;
+  dcoco_outputs dout = {};
+  dout.tokens = ws.st_tokens;
+  dout.accept_len = in->target_tokens ? ws.st_accept : nullptr;
+  rc = run_path(h, w, batch, &din, &dout, st);
+  if (rc != DCOCO_OK) return rc;
+  // outputs: tokens, accept_len (+ optional extras from the workspace)
+  DC_TRY(cudaMemcpyAsync(out->tokens, ws.st_tokens, (size_t)batch * B * sizeof(int32_t),
+                         cudaMemcpyDeviceToHost, st));
+  if (in->target_tokens)
+    DC_TRY(cudaMemcpyAsync(out->accept_len, ws.st_accept, (size_t)batch * sizeof(int32_t),
+                           cudaMemcpyDeviceToHost, st));
+  if (out->topk_ids)
+    DC_TRY(cudaMemcpyAsync(out->topk_ids, ws.ids, (size_t)batch * B * K * sizeof(int32_t),
+                           cudaMemcpyDeviceToHost, st));
+  if (out->topk_val)
+    DC_TRY(cudaMemcpyAsync(out->topk_val, ws.vals, (size_t)batch * B * K * sizeof(float),
+                           cudaMemcpyDeviceToHost, st));
+  if (out->scores)
+    DC_TRY(cudaMemcpyAsync(out->scores, ws.scores, (size_t)batch * (B - 1) * K * K * sizeof(float),
+                           cudaMemcpyDeviceToHost, st));
+  if (out->choice)
+    DC_TRY(cudaMemcpyAsync(out->choice, ws.choice, (size_t)batch * B * sizeof(int32_t),
+                           cudaMemcpyDeviceToHost, st));
+  if (out->margin)
+    DC_TRY(cudaMemcpyAsync(out->margin, ws.margin, (size_t)batch * (B - 1) * sizeof(float),
+                           cudaMemcpyDeviceToHost, st));
+  return cuda_status(cudaStreamSynchronize(st));
+}
+
+int dcoco_topk(dcoco_handle *h, int batch, const void *logits, int64_t stride, int32_t *topk_ids,
+               float *topk_val, void *stream) {
+  if (!h) return DCOCO_EINVAL;
+  if (batch < 0 || batch > h->cfg.max_batch) return DCOCO_EBATCH;
+  if (batch == 0) return DCOCO_OK;
+  if (!logits || !topk_ids || !topk_val) return DCOCO_EINVAL;
+  if (stride < h->cfg.vocab || stride % 8 != 0 || !aligned16(logits)) return DCOCO_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  h->last_stream = st;
+  ++h->launches;
+  return cuda_status(dc::launch_topk(h->cfg.topk, static_cast<const uint16_t *>(logits), stride,
+                                     h->cfg.slots, batch, h->cfg.vocab, h->plan, h->ws.part,
+                                     h->ws.row_count, topk_ids, topk_val, st));
+}
+
+int dcoco_get_device_status(dcoco_handle *h) {
+  if (!h) return DCOCO_EINVAL;
+  if (cudaStreamSynchronize(h->last_stream) != cudaSuccess) return DCOCO_ECUDA;
+  int flag = 0;
+  if (cudaMemcpy(&flag, h->ws.err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DCOCO_ECUDA;
+  if (flag != 0) {
+    if (cudaMemset(h->ws.err, 0, sizeof(int)) != cudaSuccess) return DCOCO_ECUDA;
+    return DCOCO_EDEVICE;
+  }
+  return DCOCO_OK;
+}
+
+void dcoco_weights_destroy(dcoco_weights *w) {
+  if (!w) return;
+  cudaDeviceSynchronize();
+  cudaFree(w->block);
+  delete w;
+}
+
+void dcoco_destroy(dcoco_handle *h) {
+  if (!h) return;
+  cudaDeviceSynchronize();
+  for (cudaEvent_t e : h->events) cudaEventDestroy(e);
+  cudaFree(h->block);
+  delete h;
+}
+
+long long dcoco_kernel_launches(const dcoco_handle *h) { return h ? h->launches : -1; }
+
+int dcoco_stage_timing(dcoco_handle *h, int enable) {
+  if (!h) return DCOCO_EINVAL;
+  if (enable && h->events.empty()) {
+    const size_t n = (size_t)kMaxTimedCalls * (stage_count(h->cfg.variant) + 1);
+    h->events.resize(n, nullptr);
+    for (size_t i = 0; i < n; ++i)
+      if (cudaEventCreate(&h->events[i]) != cudaSuccess) {
+        for (size_t j = 0; j < i; ++j) cudaEventDestroy(h->events[j]);
+        h->events.clear();
+        return DCOCO_ECUDA;
+      }
+  }
+  h->timing = enable != 0;
+  return DCOCO_OK;
+}
+
+int dcoco_stage_read(dcoco_handle *h, int max_stages, float *ms, int *calls, int *n_stages) {
+  if (!h || !ms || !calls || !n_stages || max_stages < 0) return DCOCO_EINVAL;
+  const int ns = stage_count(h->cfg.variant);
+  *n_stages = ns;
+  *calls = h->timed_calls;
+  for (int s = 0; s < max_stages && s < ns; ++s) ms[s] = 0.f;
+  for (int c = 0; c < h->timed_calls; ++c) {
+    cudaEvent_t *ev = h->events.data() + (size_t)c * (ns + 1);
+    if (cudaEventSynchronize(ev[ns]) != cudaSuccess) return DCOCO_ECUDA;
+    for (int s = 0; s < max_stages && s < ns; ++s) {
+      float t = 0.f;
+      if (cudaEventElapsedTime(&t, ev[s], ev[s + 1]) != cudaSuccess) return DCOCO_ECUDA;
+      ms[s] += t;
+    }
+  }
+  h->timed_calls = 0;
+  return DCOCO_OK;
+}
+
+const char *dcoco_stage_name(const dcoco_handle *h, int s) {
+  if (!h || s < 0 || s >= stage_count(h->cfg.variant)) return nullptr;
+  return kStageNames[h->cfg.variant][s];
+}
+
+}  // extern "C"

@@ -1,0 +1,332 @@
+// repr.cu -- steps 2-4 after the projections: LayerNorms, the fuse map, the
+// slot-pair states and the layer-1 partial products of the transition MLP,
+// then the K x K transition scores.
+//
+// DCOCO page ("Contextual Correction of Parallel Drafts for Speculative
+// Decoding"), Method step details:
+//   (2) b = LN(W_cand E[c]), g_i = LN(W_ctx h_i) (no affine);
+//       z = LN_{gamma,beta}(W_fuse [b; g_i]), width r = 128.
+//   (3) s_p = W_pair [h_p; h_{p+1}], once per adjacent slot pair.
+//   (4) S_p(a,b) = l_{p+1}(b) + Delta([s_p; z_p^a; z_{p+1}^b; l_p(a); l_{p+1}(b)]),
+//       Delta = 386 -> 256 -> 1 MLP with GELU, weights shared by all slots.
+//
+// Layer 1 of Delta is linear in its concatenated input, so it splits into a
+// per-pair part P_p = W1_s s_p + b1, a predecessor part U = W1_a z^a + w_la l(a)
+// and a successor part V = W1_b z^b + w_lb l(b).  Each of the (B-1) K^2 pairs
+// then costs one add, one GELU and one 256-long dot with w2.
+//
+// All arithmetic is fp32.  LN uses the population variance with eps inside
+// the square root.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dc {
+namespace {
+
+constexpr int R = 128;  // representation width
+constexpr int H = 256;  // MLP hidden width
+
+// LN0 of one 128-vector held as 4 values per lane of a warp (in place).
+__device__ __forceinline__ void warp_ln0_128(float (&x)[4], float eps) {
+  float s = warp_sum(x[0] + x[1] + x[2] + x[3]);
+  const float mean = s * (1.0f / R);
+  float q = 0.f;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    x[u] -= mean;
+    q += x[u] * x[u];
+  }
+  q = warp_sum(q);
+  const float inv = rsqrtf(q * (1.0f / R) + eps);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) x[u] *= inv;
+}
+
+// ---------------------------------------------------------------- per slot
+__global__ void __launch_bounds__(256)
+k_slot_post(const float *__restrict__ slot_proj, int B, float eps, MlpWeightsDev w,
+            float *__restrict__ Gf, float *__restrict__ Pout) {
+  __shared__ float g[32][R];
+  __shared__ float s[32][R];
+  const int n = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float *sp = slot_proj + (int64_t)n * B * 3 * R;
+
+  for (int i = warp; i < B; i += 8) {
+    float x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) x[u] = sp[(int64_t)i * 3 * R + lane + 32 * u];
+    warp_ln0_128(x, eps);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) g[i][lane + 32 * u] = x[u];
+  }
+  for (int e = tid; e < (B - 1) * R; e += 256) {
+    const int p = e / R, k = e - p * R;
+    s[p][k] = sp[(int64_t)p * 3 * R + R + k] + sp[(int64_t)(p + 1) * 3 * R + 2 * R + k];
+  }
+  __syncthreads();
+
+  // Gf_i = W_fuse[:, r:] g_i
+  {
+    const int o = tid & (R - 1), half = tid >> 7;
+    for (int i0 = half; i0 < B; i0 += 16) {
+      float acc[8] = {};
+      for (int k = 0; k < R; ++k) {
+        const float wv = w.wfg_t[k * R + o];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int i = i0 + 2 * u;
+          if (i < B) acc[u] = fmaf(wv, g[i][k], acc[u]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = i0 + 2 * u;
+        if (i < B) Gf[((int64_t)n * B + i) * R + o] = acc[u];
+      }
+    }
+  }
+  // P_p = W1_s s_p + b1
+  {
+    const int j = tid;
+    const float bj = w.b1[j];
+    for (int p0 = 0; p0 < B - 1; p0 += 8) {
+      float acc[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) acc[u] = bj;
+      for (int k = 0; k < R; ++k) {
+        const float wv = w.w1s_t[k * H + j];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (p0 + u < B - 1) acc[u] = fmaf(wv, s[p0 + u][k], acc[u]);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (p0 + u < B - 1) Pout[((int64_t)n * (B - 1) + p0 + u) * H + j] = acc[u];
+    }
+  }
+}
+
+// ---------------------------------------------------------------- per candidate
+template <int K>
+__global__ void __launch_bounds__(256)
+k_cand_post(const float *__restrict__ cand_proj, const float *__restrict__ topk_val,
+            const float *__restrict__ Gf, float eps, MlpWeightsDev w, float *__restrict__ U,
+            float *__restrict__ Vout) {
+  __shared__ float b[K][R];
+  __shared__ float z[K][R];
+  const int slot = blockIdx.x;  // n * B + i
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t c0 = (int64_t)slot * K;
+
+  for (int c = warp; c < K; c += 8) {
+    float x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) x[u] = cand_proj[(c0 + c) * R + lane + 32 * u];
+    warp_ln0_128(x, eps);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) b[c][lane + 32 * u] = x[u];
+  }
+  __syncthreads();
+
+  // y = W_fuse[:, :r] b + Gf  (thread: output o, candidates of one parity)
+  {
+    constexpr int KH = K / 2;
+    const int o = tid & (R - 1), half = tid >> 7;
+    float acc[KH] = {};
+    for (int k = 0; k < R; ++k) {
+      const float wv = w.wfb_t[k * R + o];
+#pragma unroll
+      for (int u = 0; u < KH; ++u) acc[u] = fmaf(wv, b[half + 2 * u][k], acc[u]);
+    }
+    const float gf = Gf[(int64_t)slot * R + o];
+#pragma unroll
+    for (int u = 0; u < KH; ++u) z[half + 2 * u][o] = acc[u] + gf;
+  }
+  __syncthreads();
+  for (int c = warp; c < K; c += 8) {
+    float x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) x[u] = z[c][lane + 32 * u];
+    warp_ln0_128(x, eps);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int k = lane + 32 * u;
+      z[c][k] = fmaf(w.gamma[k], x[u], w.beta[k]);
+    }
+  }
+  __syncthreads();
+
+  // U = W1_a z + w_la l ; V = W1_b z + w_lb l   (thread: hidden unit j)
+  const int j = tid;
+  for (int pass = 0; pass < 2; ++pass) {
+    const float *wt = pass == 0 ? w.w1a_t : w.w1b_t;
+    const float wl = pass == 0 ? w.w_la[j] : w.w_lb[j];
+    float *dst = pass == 0 ? U : Vout;
+    float acc[K] = {};
+    for (int k = 0; k < R; ++k) {
+      const float wv = wt[k * H + j];
+#pragma unroll
+      for (int c = 0; c < K; ++c) acc[c] = fmaf(wv, z[c][k], acc[c]);
+    }
+#pragma unroll
+    for (int c = 0; c < K; ++c) dst[(c0 + c) * H + j] = fmaf(wl, topk_val[c0 + c], acc[c]);
+  }
+}
+
+// ---------------------------------------------------------------- pair scores
+template <int K>
+__global__ void __launch_bounds__(256)
+k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
+             const float *__restrict__ P, const float *__restrict__ topk_val,
+             const float *__restrict__ w2, const float *__restrict__ b2, int B,
+             float *__restrict__ scores) {
+  extern __shared__ float sm[];
+  float *pu = sm;                   // [K][H+1]  P_p + U_{p,a}
+  float *vs = pu + K * (H + 1);     // [K][H+1]  V_{p+1,b}
+  float *w2s = vs + K * (H + 1);    // [H]
+  const int np = blockIdx.x;        // n * (B-1) + p
+  const int n = np / (B - 1), p = np - n * (B - 1);
+  const int tid = threadIdx.x;
+  const int64_t ca = ((int64_t)n * B + p) * K;      // first candidate of slot p
+  const int64_t cb = ca + K;                         // first candidate of slot p+1
+  const float *Pp = P + (int64_t)np * H;
+
+  for (int e = tid; e < K * H; e += 256) {
+    const int c = e / H, j = e - c * H;
+    pu[c * (H + 1) + j] = U[(ca + c) * H + j] + Pp[j];
+    vs[c * (H + 1) + j] = V[(cb + c) * H + j];
+  }
+  w2s[tid] = w2[tid];
+  __syncthreads();
+
+  const float bias = b2[0];
+  for (int e = tid; e < K * K; e += 256) {
+    const int a = e / K, bb = e - a * K;
+    const float *x = pu + a * (H + 1);
+    const float *y = vs + bb * (H + 1);
+    float acc = 0.f;
+#pragma unroll 4
+    for (int jj = 0; jj < H; ++jj) acc = fmaf(w2s[jj], gelu_erf(x[jj] + y[jj]), acc);
+    scores[(int64_t)np * K * K + e] = topk_val[cb + bb] + bias + acc;
+  }
+}
+
+// ---------------------------------------------------------------- cosine variant
+__global__ void __launch_bounds__(256)
+k_cos_post(const float *__restrict__ cand_io, const float *__restrict__ slot_io, int K, int M,
+           float *__restrict__ O, float *__restrict__ I) {
+  const int lane = threadIdx.x & 31;
+  const int m = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (m >= M) return;
+  const int slot = m / K;
+  float o[4], in[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int k = lane + 32 * u;
+    o[u] = cand_io[(int64_t)m * 2 * R + k] + slot_io[(int64_t)slot * 2 * R + k];
+    in[u] = cand_io[(int64_t)m * 2 * R + R + k] + slot_io[(int64_t)slot * 2 * R + R + k];
+  }
+  float no = warp_sum(o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3]);
+  float ni = warp_sum(in[0] * in[0] + in[1] * in[1] + in[2] * in[2] + in[3] * in[3]);
+  const float so = 1.0f / fmaxf(sqrtf(no), 1e-12f), si = 1.0f / fmaxf(sqrtf(ni), 1e-12f);
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int k = lane + 32 * u;
+    O[(int64_t)m * R + k] = o[u] * so;
+    I[(int64_t)m * R + k] = in[u] * si;
+  }
+}
+
+template <int K>
+__global__ void __launch_bounds__(256)
+k_cos_score(const float *__restrict__ O, const float *__restrict__ I,
+            const float *__restrict__ topk_val, float sigma, int B, float *__restrict__ scores) {
+  __shared__ float os[K][R + 1];
+  __shared__ float is[K][R + 1];
+  const int np = blockIdx.x;
+  const int n = np / (B - 1), p = np - n * (B - 1);
+  const int64_t ca = ((int64_t)n * B + p) * K, cb = ca + K;
+  for (int e = threadIdx.x; e < K * R; e += 256) {
+    const int c = e / R, k = e - c * R;
+    os[c][k] = O[(ca + c) * R + k];
+    is[c][k] = I[(cb + c) * R + k];
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < K * K; e += 256) {
+    const int a = e / K, bb = e - a * K;
+    float acc = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < R; ++k) acc = fmaf(os[a][k], is[bb][k], acc);
+    scores[(int64_t)np * K * K + e] = fmaf(sigma, acc, topk_val[cb + bb]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_slot_post(const float *slot_proj, int N, int B, float eps, const MlpWeightsDev &w,
+                             float *Gf, float *P, cudaStream_t st) {
+  if (N == 0) return cudaSuccess;
+  k_slot_post<<<N, 256, 0, st>>>(slot_proj, B, eps, w, Gf, P);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cand_post(int K, const float *cand_proj, const float *topk_val, const float *Gf,
+                             int N, int B, float eps, const MlpWeightsDev &w, float *U, float *V,
+                             cudaStream_t st) {
+  if (N == 0) return cudaSuccess;
+  const int grid = N * B;
+  switch (K) {
+    case 8: k_cand_post<8><<<grid, 256, 0, st>>>(cand_proj, topk_val, Gf, eps, w, U, V); break;
+    case 16: k_cand_post<16><<<grid, 256, 0, st>>>(cand_proj, topk_val, Gf, eps, w, U, V); break;
+    case 32: k_cand_post<32><<<grid, 256, 0, st>>>(cand_proj, topk_val, Gf, eps, w, U, V); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+template <int K>
+static cudaError_t pair_score_k(const float *U, const float *V, const float *P, const float *tv,
+                                const float *w2, const float *b2, int N, int B, float *scores,
+                                cudaStream_t st) {
+  const size_t smem = (size_t)(2 * K * (H + 1) + H) * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(k_pair_score<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  k_pair_score<K><<<N * (B - 1), 256, smem, st>>>(U, V, P, tv, w2, b2, B, scores);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pair_score(int K, const float *U, const float *V, const float *P,
+                              const float *topk_val, const float *w2, const float *b2, int N, int B,
+                              float *scores, cudaStream_t st) {
+  if (N == 0) return cudaSuccess;
+  switch (K) {
+    case 8: return pair_score_k<8>(U, V, P, topk_val, w2, b2, N, B, scores, st);
+    case 16: return pair_score_k<16>(U, V, P, topk_val, w2, b2, N, B, scores, st);
+    case 32: return pair_score_k<32>(U, V, P, topk_val, w2, b2, N, B, scores, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_cos_post(int K, const float *cand_io, const float *slot_io, int N, int B,
+                            float *O, float *I, cudaStream_t st) {
+  const int M = N * B * K;
+  if (M == 0) return cudaSuccess;
+  k_cos_post<<<(M + 7) / 8, 256, 0, st>>>(cand_io, slot_io, K, M, O, I);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cos_score(int K, const float *O, const float *I, const float *topk_val,
+                             float sigma, int N, int B, float *scores, cudaStream_t st) {
+  if (N == 0) return cudaSuccess;
+  const int grid = N * (B - 1);
+  switch (K) {
+    case 8: k_cos_score<8><<<grid, 256, 0, st>>>(O, I, topk_val, sigma, B, scores); break;
+    case 16: k_cos_score<16><<<grid, 256, 0, st>>>(O, I, topk_val, sigma, B, scores); break;
+    case 32: k_cos_score<32><<<grid, 256, 0, st>>>(O, I, topk_val, sigma, B, scores); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace dc

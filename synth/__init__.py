@@ -25,6 +25,8 @@ candidates, a frozen V x d embedding table, r = 128, a 386 -> 256 -> 1 MLP):
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 
 __all__ = [
@@ -82,11 +84,22 @@ def make_hidden(rng: np.random.Generator, N: int, slots: int, d: int) -> np.ndar
 
 
 def make_embedding(rng: np.random.Generator, V: int, d: int, std: float = 0.02,
-                   rows_per_draw: int = 8192) -> np.ndarray:
+                   rows_per_draw: int = 8192, threads: int | None = None) -> np.ndarray:
+    """bf16 N(0, std^2) table [V, d].  Row blocks are drawn from child generators
+    (seeded from `rng`) on a thread pool, so the result depends only on `rng`."""
+    from concurrent.futures import ThreadPoolExecutor
     out = np.empty((V, d), dtype=np.uint16)
-    for r0 in range(0, V, rows_per_draw):
+    starts = list(range(0, V, rows_per_draw))
+    children = np.random.SeedSequence(int(rng.integers(0, 2**63))).spawn(len(starts))
+
+    def fill(k):
+        r0 = starts[k]
         r1 = min(V, r0 + rows_per_draw)
-        out[r0:r1] = bf16_bits(rng.standard_normal((r1 - r0, d), dtype=np.float32) * np.float32(std))
+        g = np.random.Generator(np.random.PCG64(children[k]))
+        out[r0:r1] = bf16_bits(g.standard_normal((r1 - r0, d), dtype=np.float32) * np.float32(std))
+
+    with ThreadPoolExecutor(max_workers=threads or min(16, os.cpu_count() or 1)) as ex:
+        list(ex.map(fill, range(len(starts))))
     return out
 
 

@@ -1,0 +1,237 @@
+"""GPU parity: the CUDA library (through the C ABI) against the CPU oracle on
+the same seeded inputs.  Rules in tests/problem.py: ids, tokens and
+accept_len bit-exact; scores within 2e-3; walk divergences only at oracle
+near-ties (counted)."""
+import copy
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from problem import Problem, bf16_tensor, compare, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+V_QWEN, D_QWEN = 151936, 4096
+
+
+@pytest.fixture(scope="module")
+def torch_cuda():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    return torch
+
+
+def report(name, stats):
+    print(f"[parity] {name}: max|dS|={stats['max_score_err']:.2e} near-tie divergences={stats['diverged']}")
+
+
+# ------------------------------------------------------------------ top-K edge cases
+def _adversarial_rows(rng, V, stride):
+    rows = []
+    f = lambda a: synth.bf16_bits(np.asarray(a, np.float32))  # noqa: E731
+    rows.append(np.full(V, f([1.5])[0], np.uint16))                        # all equal
+    r = np.full(V, f([-np.inf])[0], np.uint16)                             # mostly -inf
+    r[rng.choice(V, 5, replace=False)] = f(rng.standard_normal(5))
+    rows.append(r)
+    rows.append(np.full(V, f([-np.inf])[0], np.uint16))                    # all -inf
+    r = f(np.round(rng.standard_normal(V)))                                # few levels, many ties
+    rows.append(r)
+    r = np.zeros(V, np.uint16); r[rng.choice(V, V // 2, replace=False)] = 0x8000  # -0 / +0 mix
+    rows.append(r)
+    r = f(rng.standard_normal(V) - 10); r[-(V % 8 or 8):] = f([50.0])[0]   # maxima in the tail
+    rows.append(r)
+    r = f(-np.abs(rng.standard_normal(V)) - 1)                             # all negative
+    rows.append(r)
+    r = f(rng.standard_normal(V)); r[::2048 * 8] = f([30.0])[0]            # chunk boundaries
+    r[2048 * 8 - 1::2048 * 8] = f([29.0])[0]
+    rows.append(r)
+    r = f(np.full(V, 2.0)); r[rng.choice(V, 3, replace=False)] = f([3.0])[0]  # K-th value tied
+    rows.append(r)
+    out = np.full((len(rows), stride), 0xFF80, np.uint16)
+    for i, r in enumerate(rows):
+        out[i, :V] = r
+    return out
+
+
+@pytest.mark.parametrize("V,K", [(151936, 16), (151933, 32), (4099, 8), (40, 16), (20000, 32)])
+def test_topk_adversarial(torch_cuda, V, K):
+    torch = torch_cuda
+    import draft_correction_slot_gb300 as dc
+    rng = np.random.default_rng(V + K)
+    stride = ((V + 7) // 8) * 8
+    rows = _adversarial_rows(rng, V, stride)
+    slots = rows.shape[0] + 1
+    logits = np.full((1, slots, stride), 0xFF80, np.uint16)
+    logits[0, 1:] = rows
+    h = dc.dcoco_create(V, 64, slots, K, max_batch=1)
+    try:
+        ids = torch.empty(1, slots - 1, K, dtype=torch.int32, device="cuda")
+        vals = torch.empty(1, slots - 1, K, dtype=torch.float32, device="cuda")
+        for _ in range(2):  # twice: the row counters must reset themselves
+            dc.dcoco_topk(h, 1, bf16_tensor(logits), ids, vals, logits_slot_stride=stride)
+            torch.cuda.synchronize()
+            gi, gv = ids.cpu().numpy()[0], vals.cpu().numpy()[0]
+            for i in range(slots - 1):
+                ri, rv = oracle.topk_row(logits[0, i + 1, :V], K)
+                np.testing.assert_array_equal(gi[i], ri, err_msg=f"row {i} ids")
+                np.testing.assert_array_equal(gv[i].view(np.uint32), rv.view(np.uint32),
+                                              err_msg=f"row {i} values (bitwise, +0 canonical)")
+    finally:
+        dc.dcoco_destroy(h)
+
+
+def test_topk_random_many_rows(torch_cuda):
+    prob = Problem(1, N=8, V=V_QWEN, d=64, targets=False)
+    import draft_correction_slot_gb300 as dc
+    torch = torch_cuda
+    h = dc.dcoco_create(V_QWEN, 64, 16, 16, max_batch=8)
+    ids = torch.empty(8, 15, 16, dtype=torch.int32, device="cuda")
+    vals = torch.empty(8, 15, 16, dtype=torch.float32, device="cuda")
+    dc.dcoco_topk(h, 8, bf16_tensor(prob.logits), ids, vals)
+    torch.cuda.synchronize()
+    dc.dcoco_destroy(h)
+    ref = prob.oracle_top16()
+    np.testing.assert_array_equal(ids.cpu().numpy(), ref)
+
+
+# ------------------------------------------------------------------ whole path
+def test_tiny_single_request(torch_cuda):
+    """One request, Qwen3-8B shapes: V=151,936, d=4096, K=16, 16 slots."""
+    prob = Problem(0, N=1, V=V_QWEN, d=D_QWEN)
+    report("tiny", compare(prob, run_gpu(prob), prob.oracle()))
+
+
+def test_tiny_zero_output_layer(torch_cuda):
+    """Output layer zeroed: scores equal l_{p+1}(b) exactly and the walk returns the draft argmax."""
+    prob = Problem(0, N=1, V=V_QWEN, d=D_QWEN, zero_out=True)
+    g = run_gpu(prob)
+    report("zero-output", compare(prob, g, prob.oracle()))
+    vals = g["topk_val"][0]
+    for p in range(prob.B - 1):
+        np.testing.assert_array_equal(g["scores"][0, p], np.broadcast_to(vals[p + 1], (16, 16)))
+    np.testing.assert_array_equal(g["choice"], 0)
+    np.testing.assert_array_equal(g["tokens"][0], g["topk_ids"][0, :, 0])
+
+
+def test_ragged_small_shapes(torch_cuda):
+    """Ragged vocabulary (V % 8 != 0, padded stride) and a small hidden width."""
+    prob = Problem(3, N=3, V=4099, d=256, stride=4112, perturb=True)
+    report("ragged", compare(prob, run_gpu(prob, max_batch=5), prob.oracle()))
+
+
+@pytest.mark.parametrize("K", [8, 32])
+def test_other_candidate_counts(torch_cuda, K):
+    prob = Problem(4 + K, N=2, V=20011, d=512, K=K, planted=8, boost=(8.0, 16.0))
+    report(f"K={K}", compare(prob, run_gpu(prob), prob.oracle()))
+
+
+def test_wide_k32_d5120(torch_cuda):
+    """K=32, d=5120, low-entropy logits (8 planted ids, U(8,16)): 14 x 32^2 transitions."""
+    prob = Problem(5, N=2, V=V_QWEN, d=5120, K=32, planted=8, boost=(8.0, 16.0))
+    report("wide", compare(prob, run_gpu(prob), prob.oracle()))
+
+
+def test_cosine_variant(torch_cuda):
+    prob = Problem(6, N=2, V=V_QWEN, d=D_QWEN, variant=1, sigma=1.0)
+    report("cosine", compare(prob, run_gpu(prob), prob.oracle()))
+
+
+def test_cosine_variant_sigma8(torch_cuda):
+    prob = Problem(7, N=2, V=5003, d=128, variant=1, sigma=8.0)
+    report("cosine-sigma8", compare(prob, run_gpu(prob), prob.oracle()))
+
+
+def test_short_block(torch_cuda):
+    """slots = 3 (B = 2 draft slots, one pair) and slots = 32 (B = 31)."""
+    for slots in (3, 32):
+        prob = Problem(8 + slots, N=2, V=3001, d=128, slots=slots)
+        report(f"slots={slots}", compare(prob, run_gpu(prob), prob.oracle()))
+
+
+def test_determinism_and_batch_invariance(torch_cuda):
+    prob = Problem(9, N=4, V=V_QWEN, d=D_QWEN, targets=True)
+    a = run_gpu(prob)
+    b = run_gpu(prob, max_batch=32)
+    for k in a:
+        np.testing.assert_array_equal(a[k], b[k], err_msg=f"{k} not deterministic")
+    one = copy.copy(prob)
+    one.N = 1
+    one.logits, one.hidden, one.targets = prob.logits[2:3], prob.hidden[2:3], prob.targets[2:3]
+    c = run_gpu(one)
+    for k in c:
+        np.testing.assert_array_equal(c[k][0], a[k][2], err_msg=f"{k} depends on the batch")
+
+
+@pytest.mark.parametrize("tier,boost", [("low", (2.0, 6.0)), ("mid", (4.0, 12.0)), ("high", (8.0, 16.0))])
+def test_entropy_tiers(torch_cuda, tier, boost):
+    """Serving-sweep tiers: 64 planted ids per slot; accept_len is oracle-checked."""
+    prob = Problem(20, N=4, V=V_QWEN, d=D_QWEN, planted=64, boost=boost)
+    ref = prob.oracle()
+    stats = compare(prob, run_gpu(prob), ref)
+    report(f"tier-{tier}", stats)
+    print(f"[tier] {tier}: mean accept_len = {ref['accept_len'].mean():.3f}")
+
+
+@pytest.mark.slow
+def test_full_size_batch32_sampled(torch_cuda):
+    """Batch 32 at Qwen3-8B shapes, the launch the benchmark times; the oracle
+    checks sampled requests."""
+    prob = Problem(1, N=32, V=V_QWEN, d=D_QWEN, targets=False)
+    sample = [0, 13, 31]
+    top16 = prob.oracle_top16()
+    prob.targets = synth.draw_targets(prob.rng, top16, prob.V)
+    g = run_gpu(prob)
+    report("batch32", compare(prob, g, prob.oracle(requests=sample)))
+    # top-K of every request is cheap to check in full
+    np.testing.assert_array_equal(g["topk_ids"], top16)
+
+
+def test_host_entry_matches_device_entry(torch_cuda):
+    torch = torch_cuda
+    import draft_correction_slot_gb300 as dc
+    prob = Problem(11, N=3, V=4099, d=256, stride=4104)
+    dev = run_gpu(prob)
+    corr = dc.Corrector({k: torch.from_numpy(v) for k, v in prob.w.items()}, prob.V, prob.d,
+                        max_batch=3, host_staging=True)
+    E = bf16_tensor(prob.E)
+    lg = torch.from_numpy(prob.logits.view(np.int16)).pin_memory()
+    hd = torch.from_numpy(prob.hidden.view(np.int16)).pin_memory()
+    tg = torch.from_numpy(prob.targets).pin_memory()
+    out = {k: torch.empty_like(torch.from_numpy(dev[k])).pin_memory()
+           for k in ("tokens", "accept_len", "scores", "topk_ids")}
+    dc.dcoco_correct_host(corr.handle, corr.weights, 3, lg, hd, E, tg, logits_slot_stride=prob.stride,
+                          **out)
+    for k, v in out.items():
+        np.testing.assert_array_equal(v.numpy(), dev[k], err_msg=k)
+    corr.close()
+
+
+def test_argument_errors(torch_cuda):
+    torch = torch_cuda
+    import draft_correction_slot_gb300 as dc
+    prob = Problem(12, N=2, V=4099, d=256, stride=4104)
+    corr = dc.Corrector({k: torch.from_numpy(v) for k, v in prob.w.items()}, prob.V, prob.d, max_batch=2)
+    lg, hd, E = bf16_tensor(prob.logits), bf16_tensor(prob.hidden), bf16_tensor(prob.E)
+    tok = torch.empty(3, 15, dtype=torch.int32, device="cuda")
+    with pytest.raises(dc.DcocoError) as e:       # batch above max_batch
+        dc.dcoco_correct(corr.handle, corr.weights, 3, lg, hd, E, tokens=tok, logits_slot_stride=4104)
+    assert e.value.status == dc.DCOCO_EBATCH
+    with pytest.raises(dc.DcocoError) as e:       # stride not a multiple of 8
+        dc.dcoco_correct(corr.handle, corr.weights, 1, lg, hd, E, tokens=tok, logits_slot_stride=4100)
+    assert e.value.status == dc.DCOCO_EINVAL
+    with pytest.raises(dc.DcocoError) as e:       # misaligned logits pointer
+        dc.dcoco_correct(corr.handle, corr.weights, 1, lg.view(-1)[1:], hd, E, tokens=tok,
+                         logits_slot_stride=4104)
+    assert e.value.status == dc.DCOCO_EINVAL
+    with pytest.raises(dc.DcocoError) as e:       # targets without accept_len
+        dc.dcoco_correct(corr.handle, corr.weights, 1, lg, hd, E, torch.zeros(2, 15, dtype=torch.int32,
+                         device="cuda"), tokens=tok, logits_slot_stride=4104)
+    assert e.value.status == dc.DCOCO_EINVAL
+    dc.dcoco_correct(corr.handle, corr.weights, 0, lg, hd, E, tokens=tok)  # batch 0: no-op
+    assert corr.status() == dc.DCOCO_OK
+    corr.close()
