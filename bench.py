@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--cpu-requests", type=int, default=16,
                     help="requests in the CPU-oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["topk"], default=None,
+                    help="time one kernel stage alone through its own entry point (for profiling)")
     return ap.parse_args()
 
 
@@ -365,6 +367,40 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------------ one stage alone
+def run_only(args):
+    """Step 1 alone (dcoco_topk) on the headline workload's logits; prints one JSON line."""
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import draft_correction_slot_gb300 as dc
+
+    w = dict(WORKLOAD)
+    pk = peaks()
+    N, S, V, K = w["N"], w["slots"], w["V"], w["K"]
+    device = torch.device("cuda", 0)
+    sets = [gpu_inputs(torch, 1000 + s, w, device, with_targets=False)[0] for s in range(args.sets)]
+    h = dc.dcoco_create(V, 64, S, K, max_batch=N)
+    ids = torch.empty(N, S - 1, K, dtype=torch.int32, device=device)
+    vals = torch.empty(N, S - 1, K, dtype=torch.float32, device=device)
+    for i in range(args.warmup):
+        dc.dcoco_topk(h, N, sets[i % args.sets], ids, vals)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        dc.dcoco_topk(h, N, sets[i % args.sets], ids, vals)
+    e1.record()
+    torch.cuda.synchronize()
+    dt = e0.elapsed_time(e1) / args.steps / 1e3
+    nbytes = N * (S - 1) * V * 2
+    dc.dcoco_destroy(h)
+    print(json.dumps({"stage": "topk", "us": dt * 1e6, "bytes": nbytes, "achieved_gbs": nbytes / dt / 1e9,
+                      "peak_gbs": pk["hbm_gbs"], "frac": nbytes / dt / 1e9 / pk["hbm_gbs"],
+                      "steps": args.steps, "workload": w["name"]}), flush=True)
+
+
 # ------------------------------------------------------------------ reference arm (CPU oracle)
 def run_reference(args):
     import numpy as np
@@ -418,6 +454,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.only:
+        run_only(args)
     else:
         run_ours(args)
 

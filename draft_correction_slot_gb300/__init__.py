@@ -5,7 +5,7 @@ the current CUDA stream) into the C ABI of libdcoco.so; every step of the
 correction path runs in the library's CUDA kernels.  There is no CPU path:
 importing the binding without the built library raises.
 
-Build the library first:  python -m draft_correction_slot_gb300.build
+Build the library first:  python draft_correction_slot_gb300/build.py
 """
 from __future__ import annotations
 
@@ -67,7 +67,7 @@ EXPORTED = ("dcoco_version", "dcoco_status_string", "dcoco_create", "dcoco_weigh
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"{LIB_PATH} is missing: build it with "
-                          "`python -m draft_correction_slot_gb300.build` (there is no CPU fallback)")
+                          "`python draft_correction_slot_gb300/build.py` (there is no CPU fallback)")
     L = C.CDLL(LIB_PATH)
     L.dcoco_version.restype = C.c_int
     L.dcoco_status_string.argtypes = [C.c_int]

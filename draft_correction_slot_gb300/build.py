@@ -3,7 +3,8 @@
 Each .cu file is compiled in parallel with
     nvcc -gencode arch=compute_103a,code=sm_103a -O3 -lineinfo -Xcompiler -fPIC
 and the objects are linked into one shared library exporting the C ABI of
-include/dcoco.h.  Run `python -m draft_correction_slot_gb300.build`.
+include/dcoco.h.  Run `python draft_correction_slot_gb300/build.py` (by path:
+importing the package loads the built library).
 """
 from __future__ import annotations
 

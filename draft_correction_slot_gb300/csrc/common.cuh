@@ -11,6 +11,7 @@ namespace dc {
 // Device error bits, OR-ed into the handle's device status word.
 enum : int {
   kErrBadCandidateId = 1,   // a gathered token id was outside [0, V)
+  kErrTimeout = 2,          // a bounded wait inside a kernel expired
 };
 
 // ---- bf16 bit helpers ------------------------------------------------------

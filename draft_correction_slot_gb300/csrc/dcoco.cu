@@ -18,10 +18,15 @@ constexpr int kH = 256;
 struct Workspace {
   unsigned long long *part = nullptr;
   unsigned *row_count = nullptr;
+  unsigned long long *row_bound = nullptr;
   int32_t *ids = nullptr;
   float *vals = nullptr;
   float *slot_proj = nullptr;  // [N*B][3r]  (variant 1: [N*B][2r])
   float *cand_proj = nullptr;  // [N*B*K][r] (variant 1: [N*B*K][2r])
+  float *slot_part = nullptr;  // split-K partials of the slot projection
+  float *cand_part = nullptr;  // split-K partials of the candidate projection
+  unsigned *slot_tiles = nullptr;
+  unsigned *cand_tiles = nullptr;
   float *Gf = nullptr;         // [N*B][r]
   float *P = nullptr;          // [N*(B-1)][H]
   float *U = nullptr;          // [N*B*K][H]  (variant 1: O [N*B*K][r])
@@ -58,7 +63,10 @@ struct dcoco_handle {
   dcoco_config cfg;
   int device = 0;
   int B = 0;
-  dc::TopkPlan plan{};
+  int topk_segments_max = 1;  // partial-list capacity per row
+  int topk_wave = 1;          // resident top-K CTAs on the device (SMs x occupancy)
+  int splits_slot = 1;        // fixed split-K of the projections (fixed per handle, so
+  int splits_cand = 1;        // results do not depend on the batch size)
   void *block = nullptr;  // one device allocation holding the workspace
   Workspace ws;
   cudaStream_t last_stream = nullptr;
@@ -72,16 +80,31 @@ struct dcoco_weights {
   const dcoco_handle *owner = nullptr;
   int device = 0;
   void *block = nullptr;
-  float *w_cand = nullptr;  // [r][d]
-  float *w_slot = nullptr;  // [3r][d] = W_ctx ; W_pair[:, :d] ; W_pair[:, d:]
-  float *w_io_e = nullptr;  // [2r][d]  W_io[:, :d]
-  float *w_io_h = nullptr;  // [2r][d]  W_io[:, d:]
+  // projection weights as bf16 hi / lo halves, [rows][d] each
+  uint16_t *cand_hi = nullptr, *cand_lo = nullptr;  // W_cand [r][d]  (variant 1: W_io[:, :d], [2r][d])
+  uint16_t *slot_hi = nullptr, *slot_lo = nullptr;  // [W_ctx ; W_pair[:, :d] ; W_pair[:, d:]] [3r][d]
+                                                    // (variant 1: W_io[:, d:], [2r][d])
   dc::MlpWeightsDev mlp{};
 };
 
 namespace {
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// fp32 -> bf16, round to nearest even (NaN -> quiet NaN)
+inline uint16_t f32_to_bf16(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, sizeof u);
+  if ((u & 0x7FFFFFFFu) > 0x7F800000u) return 0x7FC0u;
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+inline float bf16_to_f32(uint16_t b) {
+  const uint32_t u = (uint32_t)b << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return f;
+}
 
 struct Carver {  // sub-allocates a byte range, 256-byte aligned pieces
   size_t off = 0;
@@ -95,16 +118,22 @@ struct Carver {  // sub-allocates a byte range, 256-byte aligned pieces
   }
 };
 
-void carve_workspace(Carver &c, const dcoco_config &cfg, int B, const dc::TopkPlan &plan,
-                     Workspace &ws) {
+void carve_workspace(Carver &c, const dcoco_config &cfg, int B, int topk_segments_max,
+                     int splits_slot, int splits_cand, Workspace &ws) {
   const size_t N = (size_t)cfg.max_batch, K = (size_t)cfg.topk, d = (size_t)cfg.hidden;
   const size_t rows = N * B, cands = rows * K;
-  ws.part = c.take<unsigned long long>(rows * plan.nchunks * K);
+  ws.part = c.take<unsigned long long>(rows * (size_t)topk_segments_max * K);
   ws.row_count = c.take<unsigned>(rows);
+  ws.row_bound = c.take<unsigned long long>(rows);
   ws.ids = c.take<int32_t>(cands);
   ws.vals = c.take<float>(cands);
   ws.slot_proj = c.take<float>(rows * 3 * kR);
   ws.cand_proj = c.take<float>(cands * 2 * kR);
+  const size_t rows_pad = (rows + 127) / 128 * 128, cands_pad = (cands + 127) / 128 * 128;
+  ws.slot_part = c.take<float>((size_t)splits_slot * rows_pad * 3 * kR);
+  ws.cand_part = c.take<float>((size_t)splits_cand * cands_pad * 2 * kR);
+  ws.slot_tiles = c.take<unsigned>(rows_pad / 128 * 3);
+  ws.cand_tiles = c.take<unsigned>(cands_pad / 128 * 2);
   ws.Gf = c.take<float>(rows * kR);
   ws.P = c.take<float>(N * (B - 1) * kH);
   ws.U = c.take<float>(cands * kH);
@@ -133,7 +162,6 @@ int validate_config(const dcoco_config *cfg) {
   if (cfg->hidden <= 0 || cfg->hidden % 64 != 0) return DCOCO_EINVAL;
   if (cfg->max_batch < 1 || cfg->max_batch > (1 << 16)) return DCOCO_EINVAL;
   if (!(cfg->ln_eps > 0.f)) return DCOCO_EINVAL;
-  if (dc::topk_plan(cfg->vocab).nchunks > dc::kTopkMaxChunks) return DCOCO_EUNSUPPORTED;
   return DCOCO_OK;
 }
 
@@ -205,27 +233,32 @@ int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs 
   StageClock clk(h, st);
 
   // step 1: candidate pools
-  DC_TRY(clk.done(dc::launch_topk(K, logits, in->logits_slot_stride, cfg.slots, N, V, h->plan,
-                                  ws.part, ws.row_count, ids, vals, st)));
+  const dc::TopkPlan plan = dc::topk_plan(V, N * B, h->topk_wave);
+  DC_TRY(clk.done(dc::launch_topk(K, logits, in->logits_slot_stride, cfg.slots, N, V, plan,
+                                  ws.part, ws.row_count, ws.row_bound, ids, vals, st)));
   const int rows = N * B, cands = rows * K;
   if (cfg.variant == 0) {
     // steps 2-3: slot projections (W_ctx, W_pair halves) and per-slot / per-pair terms
-    DC_TRY(clk.done(dc::launch_rows_gemm(1, hidden, nullptr, cfg.slots, B, rows, d, V, w->w_slot,
-                                         3 * kR, ws.slot_proj, ws.err, st)));
+    DC_TRY(clk.done(dc::launch_proj_tc(1, hidden, nullptr, cfg.slots, B, rows, d, V, w->slot_hi,
+                                       w->slot_lo, 3 * kR, h->splits_slot, ws.slot_proj, ws.slot_part,
+                                       ws.slot_tiles, ws.err, st)));
     DC_TRY(clk.done(dc::launch_slot_post(ws.slot_proj, N, B, cfg.ln_eps, w->mlp, ws.Gf, ws.P, st)));
     // step 2: candidate projections, then z and the layer-1 partials U, V
-    DC_TRY(clk.done(dc::launch_rows_gemm(0, E, ids, cfg.slots, B, cands, d, V, w->w_cand, kR,
-                                         ws.cand_proj, ws.err, st)));
+    DC_TRY(clk.done(dc::launch_proj_tc(0, E, ids, cfg.slots, B, cands, d, V, w->cand_hi, w->cand_lo,
+                                       kR, h->splits_cand, ws.cand_proj, ws.cand_part, ws.cand_tiles,
+                                       ws.err, st)));
     DC_TRY(clk.done(dc::launch_cand_post(K, ws.cand_proj, vals, ws.Gf, N, B, cfg.ln_eps, w->mlp,
                                          ws.U, ws.V, st)));
     // step 4: all (B-1) K^2 transition scores
     DC_TRY(clk.done(dc::launch_pair_score(K, ws.U, ws.V, ws.P, vals, w->mlp.w2, w->mlp.b2, N, B,
                                           scores, st)));
   } else {
-    DC_TRY(clk.done(dc::launch_rows_gemm(1, hidden, nullptr, cfg.slots, B, rows, d, V, w->w_io_h,
-                                         2 * kR, ws.slot_proj, ws.err, st)));
-    DC_TRY(clk.done(dc::launch_rows_gemm(0, E, ids, cfg.slots, B, cands, d, V, w->w_io_e, 2 * kR,
-                                         ws.cand_proj, ws.err, st)));
+    DC_TRY(clk.done(dc::launch_proj_tc(1, hidden, nullptr, cfg.slots, B, rows, d, V, w->slot_hi,
+                                       w->slot_lo, 2 * kR, h->splits_slot, ws.slot_proj, ws.slot_part,
+                                       ws.slot_tiles, ws.err, st)));
+    DC_TRY(clk.done(dc::launch_proj_tc(0, E, ids, cfg.slots, B, cands, d, V, w->cand_hi, w->cand_lo,
+                                       2 * kR, h->splits_cand, ws.cand_proj, ws.cand_part,
+                                       ws.cand_tiles, ws.err, st)));
     DC_TRY(clk.done(dc::launch_cos_post(K, ws.cand_proj, ws.slot_proj, N, B, ws.U, ws.V, st)));
     DC_TRY(clk.done(dc::launch_cos_score(K, ws.U, ws.V, vals, cfg.sigma, N, B, scores, st)));
   }
@@ -306,13 +339,18 @@ int dcoco_create(const dcoco_config *cfg, dcoco_handle **out) {
   if (!h) return DCOCO_ENOMEM;
   h->cfg = *cfg;
   h->B = cfg->slots - 1;
-  h->plan = dc::topk_plan(cfg->vocab);
-  if (cudaGetDevice(&h->device) != cudaSuccess) {
+  h->topk_segments_max = dc::topk_max_segments(cfg->vocab);
+  int sms = 0;
+  if (cudaGetDevice(&h->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
     delete h;
     return DCOCO_ECUDA;
   }
+  h->topk_wave = sms * dc::topk_occupancy(cfg->topk);
+  h->splits_slot = dc::proj_tc_splits(cfg->hidden, 8);
+  h->splits_cand = dc::proj_tc_splits(cfg->hidden, 2);
   Carver sizer;
-  carve_workspace(sizer, h->cfg, h->B, h->plan, h->ws);
+  carve_workspace(sizer, h->cfg, h->B, h->topk_segments_max, h->splits_slot, h->splits_cand, h->ws);
   const size_t bytes = sizer.off + 256;
   if (cudaMalloc(&h->block, bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -321,7 +359,7 @@ int dcoco_create(const dcoco_config *cfg, dcoco_handle **out) {
   }
   Carver c;
   c.base = static_cast<char *>(h->block);
-  carve_workspace(c, h->cfg, h->B, h->plan, h->ws);
+  carve_workspace(c, h->cfg, h->B, h->topk_segments_max, h->splits_slot, h->splits_cand, h->ws);
   if (cudaMemset(h->block, 0, bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(h->block);
     delete h;
@@ -369,28 +407,34 @@ int dcoco_weights_create(dcoco_handle *h, const dcoco_weight_ptrs *wp, void *str
     return rc;
   }
 
-  // Layout of the device block: [proj weights][mlp pack]
-  std::vector<float> proj;
-  size_t n_proj = 0;
+  // Projection weights: rows of the stacked matrices, split into bf16 hi/lo.
+  const int cand_rows = cfg.variant == 0 ? r : 2 * r;
+  const int slot_rows = cfg.variant == 0 ? 3 * r : 2 * r;
+  std::vector<uint16_t> proj((size_t)2 * (cand_rows + slot_rows) * d);
+  uint16_t *c_hi = proj.data(), *c_lo = c_hi + (size_t)cand_rows * d;
+  uint16_t *s_hi = c_lo + (size_t)cand_rows * d, *s_lo = s_hi + (size_t)slot_rows * d;
+  auto split_row = [&](const float *src, uint16_t *hi, uint16_t *lo) {
+    for (int k = 0; k < d; ++k) {
+      const uint16_t hb = f32_to_bf16(src[k]);
+      hi[k] = hb;
+      lo[k] = f32_to_bf16(src[k] - bf16_to_f32(hb));
+    }
+  };
   if (cfg.variant == 0) {
-    n_proj = (size_t)r * d + (size_t)3 * r * d;
-    proj.resize(n_proj);
-    std::memcpy(proj.data(), w_cand.data(), (size_t)r * d * sizeof(float));
-    float *ws = proj.data() + (size_t)r * d;
     for (int o = 0; o < r; ++o) {
-      std::memcpy(ws + (size_t)o * d, w_ctx.data() + (size_t)o * d, d * sizeof(float));
-      std::memcpy(ws + (size_t)(r + o) * d, w_pair.data() + (size_t)o * 2 * d, d * sizeof(float));
-      std::memcpy(ws + (size_t)(2 * r + o) * d, w_pair.data() + (size_t)o * 2 * d + d, d * sizeof(float));
+      split_row(w_cand.data() + (size_t)o * d, c_hi + (size_t)o * d, c_lo + (size_t)o * d);
+      split_row(w_ctx.data() + (size_t)o * d, s_hi + (size_t)o * d, s_lo + (size_t)o * d);
+      split_row(w_pair.data() + (size_t)o * 2 * d, s_hi + (size_t)(r + o) * d, s_lo + (size_t)(r + o) * d);
+      split_row(w_pair.data() + (size_t)o * 2 * d + d, s_hi + (size_t)(2 * r + o) * d,
+                s_lo + (size_t)(2 * r + o) * d);
     }
   } else {
-    n_proj = (size_t)4 * r * d;
-    proj.resize(n_proj);
     for (int o = 0; o < 2 * r; ++o) {
-      std::memcpy(proj.data() + (size_t)o * d, w_io.data() + (size_t)o * 2 * d, d * sizeof(float));
-      std::memcpy(proj.data() + (size_t)(2 * r + o) * d, w_io.data() + (size_t)o * 2 * d + d,
-                  d * sizeof(float));
+      split_row(w_io.data() + (size_t)o * 2 * d, c_hi + (size_t)o * d, c_lo + (size_t)o * d);
+      split_row(w_io.data() + (size_t)o * 2 * d + d, s_hi + (size_t)o * d, s_lo + (size_t)o * d);
     }
   }
+  const size_t n_proj = proj.size();
   std::vector<float> mlp;
   size_t off[16] = {};
   if (cfg.variant == 0) {
@@ -399,7 +443,7 @@ int dcoco_weights_create(dcoco_handle *h, const dcoco_weight_ptrs *wp, void *str
     hw.w1 = w1.data(); hw.b1 = b1.data(); hw.w2 = w2.data(); hw.b2 = b2.data();
     pack_mlp(hw, d, mlp, off);
   }
-  const size_t proj_bytes = ((n_proj * sizeof(float)) + 255) & ~size_t(255);
+  const size_t proj_bytes = ((n_proj * sizeof(uint16_t)) + 255) & ~size_t(255);
   const size_t total = proj_bytes + mlp.size() * sizeof(float) + 256;
 
   dcoco_weights *w = new (std::nothrow) dcoco_weights();
@@ -412,10 +456,10 @@ int dcoco_weights_create(dcoco_handle *h, const dcoco_weight_ptrs *wp, void *str
     return DCOCO_ENOMEM;
   }
   char *base = static_cast<char *>(w->block);
-  float *dproj = reinterpret_cast<float *>(base);
+  uint16_t *dproj = reinterpret_cast<uint16_t *>(base);
   float *dmlp = reinterpret_cast<float *>(base + proj_bytes);
-  bool ok = cudaMemcpyAsync(dproj, proj.data(), n_proj * sizeof(float), cudaMemcpyHostToDevice, st) ==
-            cudaSuccess;
+  bool ok = cudaMemcpyAsync(dproj, proj.data(), n_proj * sizeof(uint16_t), cudaMemcpyHostToDevice,
+                            st) == cudaSuccess;
   if (ok && !mlp.empty())
     ok = cudaMemcpyAsync(dmlp, mlp.data(), mlp.size() * sizeof(float), cudaMemcpyHostToDevice, st) ==
          cudaSuccess;
@@ -425,17 +469,16 @@ int dcoco_weights_create(dcoco_handle *h, const dcoco_weight_ptrs *wp, void *str
     delete w;
     return DCOCO_ECUDA;
   }
+  w->cand_hi = dproj;
+  w->cand_lo = dproj + (size_t)cand_rows * d;
+  w->slot_hi = w->cand_lo + (size_t)cand_rows * d;
+  w->slot_lo = w->slot_hi + (size_t)slot_rows * d;
   if (cfg.variant == 0) {
-    w->w_cand = dproj;
-    w->w_slot = dproj + (size_t)r * d;
     dc::MlpWeightsDev &m = w->mlp;
     m.wfb_t = dmlp + off[0]; m.wfg_t = dmlp + off[1]; m.gamma = dmlp + off[2]; m.beta = dmlp + off[3];
     m.w1s_t = dmlp + off[4]; m.w1a_t = dmlp + off[5]; m.w1b_t = dmlp + off[6];
     m.w_la = dmlp + off[7]; m.w_lb = dmlp + off[8]; m.b1 = dmlp + off[9]; m.w2 = dmlp + off[10];
     m.b2 = dmlp + off[11];
-  } else {
-    w->w_io_e = dproj;
-    w->w_io_h = dproj + (size_t)2 * r * d;
   }
   *out = w;
   return DCOCO_OK;
@@ -511,9 +554,10 @@ int dcoco_topk(dcoco_handle *h, int batch, const void *logits, int64_t stride, i
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   h->last_stream = st;
   ++h->launches;
+  const dc::TopkPlan plan = dc::topk_plan(h->cfg.vocab, batch * h->B, h->topk_wave);
   return cuda_status(dc::launch_topk(h->cfg.topk, static_cast<const uint16_t *>(logits), stride,
-                                     h->cfg.slots, batch, h->cfg.vocab, h->plan, h->ws.part,
-                                     h->ws.row_count, topk_ids, topk_val, st));
+                                     h->cfg.slots, batch, h->cfg.vocab, plan, h->ws.part,
+                                     h->ws.row_count, h->ws.row_bound, topk_ids, topk_val, st));
 }
 
 int dcoco_get_device_status(dcoco_handle *h) {

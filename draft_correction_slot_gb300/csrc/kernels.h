@@ -9,31 +9,44 @@
 namespace dc {
 
 // ---------------------------------------------------------------- top-K
-// Split-vocabulary top-K: logits row size V is cut into `nchunks` chunks of
-// `chunk_vecs` 16-byte vectors; one CTA per (row, chunk) keeps its chunk's
-// best K in `part` (rows*nchunks*K packed keys), and the last CTA of each row
-// (counted in `row_count`, rows entries, zero between calls) merges them.
+// Segmented top-K: each logits row is cut into `nchunks` segments, one CTA
+// per (segment, row); each of the CTA's 8 warps streams `chunk_vecs` 16-byte
+// vectors.  With several segments, every CTA publishes its best K to `part`
+// (rows * nchunks * K packed keys) and the last CTA of the row, counted in
+// `row_count` (rows entries, zero between calls), merges them.  `row_bound`
+// (rows entries, zero between calls) carries the best published K-th key of
+// each row to the segments launched after it.
 struct TopkPlan {
-  int nchunks;
-  int chunk_vecs;
+  int nchunks;     // segments per row
+  int chunk_vecs;  // 16-byte vectors per warp
 };
 constexpr int kTopkThreads = 256;
-constexpr int kTopkVecPerThread = 8;
 constexpr int kTopkMaxChunks = 64;
-TopkPlan topk_plan(int V);
+// Segment count that best fills `slots_per_wave` resident CTAs for `rows` rows.
+TopkPlan topk_plan(int V, int rows, int slots_per_wave);
+int topk_max_segments(int V);
+int topk_occupancy(int K);  // resident top-K CTAs per SM
 cudaError_t launch_topk(int K, const uint16_t *logits, int64_t stride, int slots, int N, int V,
                         const TopkPlan &plan, unsigned long long *part, unsigned *row_count,
-                        int32_t *ids, float *vals, cudaStream_t st);
+                        unsigned long long *row_bound, int32_t *ids, float *vals, cudaStream_t st);
 
 // ---------------------------------------------------------------- projections
-// C[m][o] = sum_k A_m[k] * W[o][k] with A_m a bf16 row of length d and W fp32
-// [No][d].  Row addressing: mode 0 gathers A_m = base[ids[m]] (ids < V, else
-// the device error word gets kErrBadCandidateId and row 0 is used); mode 1
-// takes A_m = base[(m / B) * slots + (m % B) + 1] (the draft-slot rows of a
+// C[m][o] = sum_k A_m[k] * W[o][k] with A_m a bf16 row of length d.  Row
+// addressing: mode 0 gathers A_m = base[ids[m]] (ids < V, else the device
+// status word gets kErrBadCandidateId and row 0 is used); mode 1 takes
+// A_m = base[(m / B) * slots + (m % B) + 1] (the draft-slot rows of a
 // [N][slots][d] tensor).
-cudaError_t launch_rows_gemm(int mode, const uint16_t *base, const int32_t *ids, int slots, int B,
-                             int M, int d, int V, const float *W, int No, float *C, int *err,
-                             cudaStream_t st);
+// W is given as bf16 hi and lo
+// halves ([No][d] each, No % 128 == 0, d % 64 == 0).  `splits` >= 2 splits
+// the k range; then `part` holds splits * ceil(M/128)*128 * No floats and
+// `tile_count` (No/128 * ceil(M/128) entries, zero between calls) counts the
+// finished splits of each tile.
+size_t proj_tc_smem_bytes();
+int proj_tc_splits(int d, int requested);
+cudaError_t launch_proj_tc(int mode, const uint16_t *base, const int32_t *ids, int slots, int B, int M,
+                           int d, int V, const uint16_t *w_hi, const uint16_t *w_lo, int No,
+                           int splits, float *C, float *part, unsigned *tile_count, int *err,
+                           cudaStream_t st);
 
 // ---------------------------------------------------------------- representations
 struct MlpWeightsDev {

@@ -1,0 +1,366 @@
+// proj_tc.cu -- row-gathered projections C = A W^T on the 5th-generation
+// tensor cores (tcgen05.mma, accumulator in tensor memory).
+//
+// DCOCO page ("Contextual Correction of Parallel Drafts for Speculative
+// Decoding"), Method step details (2)-(3): the embedding rows E[c] of the
+// candidates (gathered by token id) and the draft-slot hidden states h_i are
+// projected by bias-free maps (W_cand; W_ctx and the two halves of W_pair).
+//
+// Precision: A (bf16) is exact; each fp32 weight is split into bf16 hi + lo
+// (w = hi + lo to ~2^-17 relative), and both products accumulate into the same
+// fp32 accumulator: C = A hi^T + A lo^T.
+//
+// Tile: 128 rows x 128 outputs, k-blocks of 64 (one 128-byte swizzle atom).
+// Warps 0-3 stage A, hi and lo into 128B-swizzled K-major shared memory with
+// cp.async (4-stage ring, mbarrier full/empty pairs) and afterwards drain the
+// accumulator with tcgen05.ld; warp 4 allocates tensor memory and one of its
+// lanes issues the MMAs.  Split-K over gridDim.z: every split writes an fp32
+// partial tile and the tile's last CTA (atomic counter) adds the partials in
+// split order, so the result does not depend on which CTA finished last.
+// Every wait is bounded in time; on expiry the kernel records kErrTimeout in
+// the device status word and leaves without touching the output.
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace dc {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kTileM = 128, kTileN = 128, kTileK = 64;
+constexpr int kTileBytes = kTileM * kTileK * 2;        // 16 KB (A, hi or lo)
+constexpr int kStageBytes = 3 * kTileBytes;             // A + hi + lo
+constexpr int kProducerThreads = 128;
+constexpr int kThreads = kProducerThreads + 32;         // + the MMA warp
+constexpr uint32_t kTmemCols = 128;
+constexpr unsigned long long kWaitNs = 1000000000ull;   // 1 s
+
+// instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M=128, N=128
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kTileN >> 3) << 17) |
+                            ((uint32_t)(kTileM >> 4) << 24);
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of `bar`; false on timeout or when another role
+// aborted (then `abort` is set and `err` records kErrTimeout).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          int *err) {
+  if (mbar_try(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try(bar, parity)) return true;
+    if ((it & 63u) == 0u) {
+      if (*abort) return false;
+      if (global_ns() - t0 > kWaitNs) {
+        *abort = 1;
+        atomicOr(err, kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (stride byte offset); the leading byte offset is unused
+// for swizzled K-major operands and set to 1.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "setp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+        "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+        "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+k_proj_tc(const uint16_t *__restrict__ base, const int32_t *__restrict__ ids, int slots, int B,
+          int M, int d, int V, const uint16_t *__restrict__ w_hi, const uint16_t *__restrict__ w_lo,
+          int No, int kb_per_split, float *__restrict__ C, float *__restrict__ part,
+          unsigned *__restrict__ tile_count, int *err) {
+  extern __shared__ uint8_t smem_raw[];
+  // the swizzle atoms need 1024-byte alignment in the shared window
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  __shared__ __align__(8) unsigned long long bar_full[kStages], bar_empty[kStages], bar_done;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  __shared__ int s_last;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int n0 = blockIdx.x * kTileN, m0 = blockIdx.y * kTileM, split = blockIdx.z;
+  const int nkb_total = d / kTileK;
+  const int kb0 = split * kb_per_split;
+  const int nkb = min(kb_per_split, nkb_total - kb0);
+  const uint32_t sbase = smem_u32(smem);
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(smem_u32(&bar_full[s]), kProducerThreads);
+      mbar_init(smem_u32(&bar_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&bar_done), 1);
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 4) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&s_tmem)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp < 4) {
+    // ------------------------------------------------------------ producers
+    const int t = tid;
+    const int c = t & 7;              // 16-byte chunk of the 128-byte k-row
+    const int rq = (t >> 3) & 7;      // row within an 8-row swizzle group
+    const uint32_t off0 = (uint32_t)((t >> 6) * 1024 + rq * 128 + ((c ^ rq) * 16));
+    const uint16_t *arow[8];
+    uint32_t abytes[8];
+    const uint16_t *hrow[8];
+    const uint16_t *lrow[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int r = (t >> 3) + 16 * j;
+      const int m = m0 + r;
+      abytes[j] = 16u;
+      if (m < M) {
+        if (MODE == 0) {
+          int id = ids[m];
+          if (id < 0 || id >= V) {
+            atomicOr(err, kErrBadCandidateId);
+            id = 0;
+          }
+          arow[j] = base + (int64_t)id * d;
+        } else {
+          const int n = m / B, i = m - n * B;
+          arow[j] = base + ((int64_t)n * slots + i + 1) * d;
+        }
+      } else {
+        arow[j] = base;
+        abytes[j] = 0u;  // rows past M are zero-filled
+      }
+      hrow[j] = w_hi + (int64_t)(n0 + r) * d;
+      lrow[j] = w_lo + (int64_t)(n0 + r) * d;
+    }
+    int it = 0;
+    for (; it < nkb; ++it) {
+      const int s = it % kStages;
+      if (it >= kStages &&
+          !mbar_wait(smem_u32(&bar_empty[s]), ((it / kStages) - 1) & 1, &s_abort, err))
+        break;
+      const int kel = (kb0 + it) * kTileK + c * 8;  // element offset of this chunk
+      const uint32_t sa = sbase + s * kStageBytes + off0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        cp_async16(sa + j * 2048, arow[j] + kel, abytes[j]);
+        cp_async16(sa + kTileBytes + j * 2048, hrow[j] + kel, 16u);
+        cp_async16(sa + 2 * kTileBytes + j * 2048, lrow[j] + kel, 16u);
+      }
+      cp_async_commit();
+      if (it >= kStages - 1) {
+        cp_async_wait<kStages - 1>();
+        fence_proxy_async();
+        mbar_arrive(smem_u32(&bar_full[(it - (kStages - 1)) % kStages]));
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async();
+    for (int r = max(0, it - (kStages - 1)); r < it; ++r) mbar_arrive(smem_u32(&bar_full[r % kStages]));
+  } else if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    for (int it = 0; it < nkb; ++it) {
+      const int s = it % kStages;
+      if (!mbar_wait(smem_u32(&bar_full[s]), (it / kStages) & 1, &s_abort, err)) break;
+      tc_fence_after();
+      const uint32_t sa = sbase + s * kStageBytes;
+#pragma unroll
+      for (int k = 0; k < kTileK / 16; ++k) {
+        const uint64_t ad = sw128_desc(sa + k * 32);
+        mma_bf16(tmem, ad, sw128_desc(sa + kTileBytes + k * 32), (it > 0 || k > 0) ? 1u : 0u);
+        mma_bf16(tmem, ad, sw128_desc(sa + 2 * kTileBytes + k * 32), 1u);
+      }
+      mma_commit(smem_u32(&bar_empty[s]));
+    }
+    mma_commit(smem_u32(&bar_done));
+  }
+  __syncwarp();
+
+  // ---------------------------------------------------------------- epilogue
+  const bool split_k = gridDim.z > 1;
+  if (warp < 4) {
+    bool ok = mbar_wait(smem_u32(&bar_done), 0, &s_abort, err) && !s_abort;
+    ok = __all_sync(DC_FULL_MASK, ok);  // tcgen05.ld below is warp-collective
+    tc_fence_after();
+    if (ok) {
+      const int row = m0 + warp * 32 + lane;
+      float *dst = split_k ? part + ((int64_t)split * gridDim.y * kTileM + row) * No + n0
+                           : C + (int64_t)row * No + n0;
+#pragma unroll 1
+      for (int cc = 0; cc < kTileN / 32; ++cc) {
+        float v[32];
+        tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(cc * 32), v);
+        if (row < M || split_k) {
+          float4 *d4 = reinterpret_cast<float4 *>(dst + cc * 32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                 : "memory");
+  }
+  if (!split_k || s_abort) return;
+
+  // ---------------------------------------------------------------- split-K reduction
+  __threadfence();
+  __syncthreads();
+  const int tile = blockIdx.y * gridDim.x + blockIdx.x;
+  if (tid == 0) s_last = (atomicAdd(&tile_count[tile], 1u) == gridDim.z - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const int rows = min(kTileM, M - m0);
+  const int64_t pstride = (int64_t)gridDim.y * kTileM * No;
+  for (int e = tid; e < rows * (kTileN / 4); e += kThreads) {
+    const int r = e / (kTileN / 4), q = e - r * (kTileN / 4);
+    const int64_t off = (int64_t)(m0 + r) * No + n0 + q * 4;
+    float4 acc = __ldcg(reinterpret_cast<const float4 *>(part + off));
+    for (int z = 1; z < (int)gridDim.z; ++z) {
+      const float4 p = __ldcg(reinterpret_cast<const float4 *>(part + z * pstride + off));
+      acc.x += p.x; acc.y += p.y; acc.z += p.z; acc.w += p.w;
+    }
+    *reinterpret_cast<float4 *>(C + off) = acc;
+  }
+  if (tid == 0) tile_count[tile] = 0u;
+}
+
+}  // namespace
+
+size_t proj_tc_smem_bytes() { return (size_t)kStages * kStageBytes + 1024; }
+
+int proj_tc_splits(int d, int requested) {
+  const int nkb = d / kTileK;
+  int s = std::max(1, std::min(requested, nkb));
+  const int per = (nkb + s - 1) / s;
+  return (nkb + per - 1) / per;  // no empty split
+}
+
+cudaError_t launch_proj_tc(int mode, const uint16_t *base, const int32_t *ids, int slots, int B, int M,
+                           int d, int V, const uint16_t *w_hi, const uint16_t *w_lo, int No,
+                           int splits, float *C, float *part, unsigned *tile_count, int *err,
+                           cudaStream_t st) {
+  if (M == 0) return cudaSuccess;
+  if (No % kTileN != 0 || d % kTileK != 0) return cudaErrorInvalidValue;
+  const int nkb = d / kTileK;
+  const int per = (nkb + splits - 1) / splits;
+  dim3 grid(No / kTileN, (M + kTileM - 1) / kTileM, splits);
+  const size_t smem = proj_tc_smem_bytes();
+  cudaError_t e;
+  if (mode == 0) {
+    e = cudaFuncSetAttribute(k_proj_tc<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k_proj_tc<0><<<grid, kThreads, smem, st>>>(base, ids, slots, B, M, d, V, w_hi, w_lo, No, per, C,
+                                              part, tile_count, err);
+  } else {
+    e = cudaFuncSetAttribute(k_proj_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k_proj_tc<1><<<grid, kThreads, smem, st>>>(base, ids, slots, B, M, d, V, w_hi, w_lo, No, per, C,
+                                              part, tile_count, err);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace dc

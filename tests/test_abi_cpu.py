@@ -12,8 +12,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def dc():
-    from draft_correction_slot_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import draft_correction_slot_gb300 as dc
     return dc
 
