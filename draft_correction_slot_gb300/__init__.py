@@ -61,7 +61,7 @@ class dcoco_outputs(C.Structure):
 EXPORTED = ("dcoco_version", "dcoco_status_string", "dcoco_create", "dcoco_weights_create",
             "dcoco_correct", "dcoco_correct_host", "dcoco_topk", "dcoco_get_device_status",
             "dcoco_weights_destroy", "dcoco_destroy", "dcoco_kernel_launches",
-            "dcoco_stage_timing", "dcoco_stage_read", "dcoco_stage_name")
+            "dcoco_stage_timing", "dcoco_stage_read", "dcoco_stage_name", "dcoco_topk_noalloc")
 
 
 def _load():
@@ -80,6 +80,8 @@ def _load():
                       C.POINTER(dcoco_outputs), C.c_void_p]
     L.dcoco_topk.argtypes = [C.c_void_p, C.c_int, C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p,
                              C.c_void_p]
+    L.dcoco_topk_noalloc.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_int64,
+                                     C.c_void_p, C.c_void_p, C.c_void_p]
     L.dcoco_get_device_status.argtypes = [C.c_void_p]
     L.dcoco_weights_destroy.argtypes = [C.c_void_p]
     L.dcoco_weights_destroy.restype = None
@@ -202,6 +204,15 @@ def dcoco_topk(handle, batch: int, logits, topk_ids, topk_val, logits_slot_strid
     stride = logits_slot_stride if logits_slot_stride is not None else logits.shape[-1]
     _check(_lib.dcoco_topk(handle, batch, _ptr(logits), int(stride), _ptr(topk_ids), _ptr(topk_val),
                            _stream(stream)), "dcoco_topk")
+
+
+def dcoco_topk_noalloc(batch: int, slots: int, vocab: int, topk: int, logits, topk_ids, topk_val,
+                       logits_slot_stride: int | None = None, stream=None) -> None:
+    """Step 1 without a handle and without any device allocation (for callers
+    that cannot allocate); same results as dcoco_topk."""
+    stride = logits_slot_stride if logits_slot_stride is not None else logits.shape[-1]
+    _check(_lib.dcoco_topk_noalloc(batch, slots, vocab, topk, _ptr(logits), int(stride), _ptr(topk_ids),
+                                   _ptr(topk_val), _stream(stream)), "dcoco_topk_noalloc")
 
 
 def dcoco_get_device_status(handle) -> int:

@@ -1,0 +1,103 @@
+// topk_noalloc.cu -- step 1 (per-slot top-K) for callers that cannot
+// allocate device memory.
+//
+// The handle-based entry points get their scratch from dcoco_create, which
+// calls cudaMalloc.  Some callers cannot do that: a plugin running inside a
+// serving engine that reserved all device memory for its own pool up front,
+// or code on a latency-critical path where a cudaMalloc (which can
+// synchronise the device) is not acceptable.  dcoco_topk_noalloc runs the
+// same top-K kernel with its scratch -- per-row segment lists, finished-segment
+// counters and published lower bounds -- in the fixed array below, which every
+// GPU that loads the library holds until the process exits.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/dcoco.h"
+#include "kernels.h"
+
+namespace {
+
+constexpr int kMaxRows = DCOCO_TOPK_NOALLOC_MAX_ROWS;          // batch * (slots - 1)
+constexpr size_t kScratchBytes = (size_t)4 << 20;              // 4 MiB
+constexpr size_t kCountOff = 0;                                // unsigned [kMaxRows]
+constexpr size_t kBoundOff = (size_t)kMaxRows * 4;             // u64 [kMaxRows]
+constexpr size_t kPartOff = kBoundOff + (size_t)kMaxRows * 8;  // u64 segment lists
+constexpr size_t kPartEntries = (kScratchBytes - kPartOff) / 8;
+static_assert(kPartOff % 256 == 0, "aligned sub-arrays");
+
+// The scratch.  In host code this name is only a stand-in for the device
+// symbol; its device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_topk_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_setup_mutex;
+unsigned char *g_scratch[kMaxDevices];  // device address of g_topk_scratch, per device
+int g_wave[kMaxDevices][3];             // resident top-K CTAs per device, K = 8, 16, 32
+
+int k_index(int K) { return K == 8 ? 0 : (K == 16 ? 1 : 2); }
+
+// Once per device, with that device current: look up the scratch address and
+// the top-K occupancy.  Returns DCOCO_OK or DCOCO_ECUDA.
+int setup_device(int dev) {
+  std::lock_guard<std::mutex> lock(g_setup_mutex);
+  if (g_scratch[dev]) return DCOCO_OK;
+  void *p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_topk_scratch) != cudaSuccess || p == nullptr) {
+    cudaGetLastError();
+    return DCOCO_ECUDA;
+  }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return DCOCO_ECUDA;
+  }
+  const int ks[3] = {8, 16, 32};
+  for (int j = 0; j < 3; ++j) g_wave[dev][j] = sms * dc::topk_occupancy(ks[j]);
+  g_scratch[dev] = static_cast<unsigned char *>(p);
+  return DCOCO_OK;
+}
+
+}  // namespace
+
+extern "C" int dcoco_topk_noalloc(int batch, int slots, int vocab, int topk, const void *logits,
+                                  int64_t logits_slot_stride, int32_t *topk_ids, float *topk_val,
+                                  void *stream) {
+  if (slots < 3 || slots > 32 || (topk != 8 && topk != 16 && topk != 32)) return DCOCO_EUNSUPPORTED;
+  if (vocab < topk || vocab > (1 << 20)) return DCOCO_EINVAL;
+  if (batch < 0 || (long long)batch * (slots - 1) > kMaxRows) return DCOCO_EBATCH;
+  if (batch == 0) return DCOCO_OK;
+  if (!logits || !topk_ids || !topk_val) return DCOCO_EINVAL;
+  if (logits_slot_stride < vocab || logits_slot_stride % 8 != 0 ||
+      (reinterpret_cast<uintptr_t>(logits) & 15u) != 0)
+    return DCOCO_EINVAL;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DCOCO_ECUDA;
+  if (!g_scratch[dev]) {
+    const int rc = setup_device(dev);
+    if (rc != DCOCO_OK) return rc;
+  }
+  unsigned char *base = g_scratch[dev];
+  const int rows = batch * (slots - 1);
+  // as many row segments as the plan wants and the fixed list area holds
+  dc::TopkPlan plan = dc::topk_plan(vocab, rows, g_wave[dev][k_index(topk)]);
+  const long long fit = (long long)kPartEntries / ((long long)rows * topk);
+  if (plan.nchunks > fit) {
+    plan.nchunks = (int)fit;  // >= 1: kMaxRows * 32 entries always fit
+    const int nvec = vocab >> 3;
+    plan.chunk_vecs = (nvec + plan.nchunks * 8 - 1) / (plan.nchunks * 8);
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned *row_count = reinterpret_cast<unsigned *>(base + kCountOff);
+  unsigned long long *row_bound = reinterpret_cast<unsigned long long *>(base + kBoundOff);
+  unsigned long long *part = reinterpret_cast<unsigned long long *>(base + kPartOff);
+  // The array keeps the previous call's contents: the counters and bounds
+  // must start at zero.
+  if (cudaMemsetAsync(row_count, 0, (size_t)rows * sizeof(unsigned), st) != cudaSuccess ||
+      cudaMemsetAsync(row_bound, 0, (size_t)rows * sizeof(unsigned long long), st) != cudaSuccess)
+    return DCOCO_ECUDA;
+  const cudaError_t e = dc::launch_topk(topk, static_cast<const uint16_t *>(logits), logits_slot_stride,
+                                        slots, batch, vocab, plan, part, row_count, row_bound, topk_ids,
+                                        topk_val, st);
+  return e == cudaSuccess ? DCOCO_OK : DCOCO_ECUDA;
+}

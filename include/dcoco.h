@@ -166,6 +166,31 @@ int dcoco_correct_host(dcoco_handle *h, const dcoco_weights *w, int batch,
 int dcoco_topk(dcoco_handle *h, int batch, const void *logits, int64_t logits_slot_stride,
                int32_t *topk_ids, float *topk_val, void *stream);
 
+/* Step 1 alone WITHOUT a handle and without allocating anything.  The page
+ * has no counterpart: this entry exists for callers that cannot allocate
+ * device memory (dcoco_create calls cudaMalloc) -- e.g. a plugin inside a
+ * serving engine that reserved all device memory for its own pool, or code on
+ * a latency-critical path where cudaMalloc, which can synchronise the device,
+ * is not acceptable.  Its scratch is a fixed 4 MiB array that every GPU
+ * loading the library holds until the process exits.
+ *   batch, slots, vocab, topk: as dcoco_config / dcoco_topk; the batch is
+ *     limited to batch * (slots - 1) <= DCOCO_TOPK_NOALLOC_MAX_ROWS (4096
+ *     draft-slot rows, i.e. 273 requests of 16 slots); larger requests are
+ *     rejected with DCOCO_EBATCH before any CUDA call.
+ *   logits, logits_slot_stride, topk_ids, topk_val, stream: as dcoco_topk
+ *     (device pointers, outputs [batch][slots-1][topk]).
+ * Results are identical to dcoco_topk's.  No cudaMalloc / cudaFree or other
+ * allocating routine is called.  The first call on a device (with that
+ * device current) looks up the scratch address and the device's SM count;
+ * make that first call before any stream capture.  Every call shares the one
+ * array per device, so calls whose work overlaps on the GPU (other streams,
+ * other host threads) race and corrupt each other: order them.  Errors:
+ * EUNSUPPORTED, EINVAL, EBATCH (sizes above), ECUDA. */
+#define DCOCO_TOPK_NOALLOC_MAX_ROWS 4096
+int dcoco_topk_noalloc(int batch, int slots, int vocab, int topk, const void *logits,
+                       int64_t logits_slot_stride, int32_t *topk_ids, float *topk_val,
+                       void *stream);
+
 /* Synchronise the handle's last stream and return DCOCO_OK, or DCOCO_EDEVICE
  * if a kernel recorded bad data (e.g. a candidate id outside [0,V)) since the
  * last call to this function (the flag is then cleared), or ECUDA. */
