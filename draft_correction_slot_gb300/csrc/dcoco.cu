@@ -18,7 +18,6 @@ constexpr int kH = 256;
 struct Workspace {
   unsigned long long *part = nullptr;
   unsigned *row_count = nullptr;
-  unsigned long long *row_bound = nullptr;
   int32_t *ids = nullptr;
   float *vals = nullptr;
   float *slot_proj = nullptr;  // [N*B][3r]  (variant 1: [N*B][2r])
@@ -84,6 +83,7 @@ struct dcoco_weights {
   uint16_t *cand_hi = nullptr, *cand_lo = nullptr;  // W_cand [r][d]  (variant 1: W_io[:, :d], [2r][d])
   uint16_t *slot_hi = nullptr, *slot_lo = nullptr;  // [W_ctx ; W_pair[:, :d] ; W_pair[:, d:]] [3r][d]
                                                     // (variant 1: W_io[:, d:], [2r][d])
+  CUtensorMap map_cand_hi, map_cand_lo, map_slot_hi, map_slot_lo;  // TMA maps of the halves
   dc::MlpWeightsDev mlp{};
 };
 
@@ -124,7 +124,6 @@ void carve_workspace(Carver &c, const dcoco_config &cfg, int B, int topk_segment
   const size_t rows = N * B, cands = rows * K;
   ws.part = c.take<unsigned long long>(rows * (size_t)topk_segments_max * K);
   ws.row_count = c.take<unsigned>(rows);
-  ws.row_bound = c.take<unsigned long long>(rows);
   ws.ids = c.take<int32_t>(cands);
   ws.vals = c.take<float>(cands);
   ws.slot_proj = c.take<float>(rows * 3 * kR);
@@ -235,29 +234,29 @@ int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs 
   // step 1: candidate pools
   const dc::TopkPlan plan = dc::topk_plan(V, N * B, h->topk_wave);
   DC_TRY(clk.done(dc::launch_topk(K, logits, in->logits_slot_stride, cfg.slots, N, V, plan,
-                                  ws.part, ws.row_count, ws.row_bound, ids, vals, st)));
+                                  ws.part, ws.row_count, ids, vals, st, E, d)));
   const int rows = N * B, cands = rows * K;
   if (cfg.variant == 0) {
     // steps 2-3: slot projections (W_ctx, W_pair halves) and per-slot / per-pair terms
-    DC_TRY(clk.done(dc::launch_proj_tc(1, hidden, nullptr, cfg.slots, B, rows, d, V, w->slot_hi,
-                                       w->slot_lo, 3 * kR, h->splits_slot, ws.slot_proj, ws.slot_part,
+    DC_TRY(clk.done(dc::launch_proj_tc(1, hidden, w->map_slot_hi, w->map_slot_lo, nullptr, cfg.slots, B,
+                                       rows, d, V, 3 * kR, h->splits_slot, ws.slot_proj, ws.slot_part,
                                        ws.slot_tiles, ws.err, st)));
     DC_TRY(clk.done(dc::launch_slot_post(ws.slot_proj, N, B, cfg.ln_eps, w->mlp, ws.Gf, ws.P, st)));
     // step 2: candidate projections, then z and the layer-1 partials U, V
-    DC_TRY(clk.done(dc::launch_proj_tc(0, E, ids, cfg.slots, B, cands, d, V, w->cand_hi, w->cand_lo,
-                                       kR, h->splits_cand, ws.cand_proj, ws.cand_part, ws.cand_tiles,
-                                       ws.err, st)));
+    DC_TRY(clk.done(dc::launch_proj_tc(0, E, w->map_cand_hi, w->map_cand_lo, ids, cfg.slots, B,
+                                       cands, d, V, kR, h->splits_cand, ws.cand_proj, ws.cand_part,
+                                       ws.cand_tiles, ws.err, st)));
     DC_TRY(clk.done(dc::launch_cand_post(K, ws.cand_proj, vals, ws.Gf, N, B, cfg.ln_eps, w->mlp,
                                          ws.U, ws.V, st)));
     // step 4: all (B-1) K^2 transition scores
     DC_TRY(clk.done(dc::launch_pair_score(K, ws.U, ws.V, ws.P, vals, w->mlp.w2, w->mlp.b2, N, B,
                                           scores, st)));
   } else {
-    DC_TRY(clk.done(dc::launch_proj_tc(1, hidden, nullptr, cfg.slots, B, rows, d, V, w->slot_hi,
-                                       w->slot_lo, 2 * kR, h->splits_slot, ws.slot_proj, ws.slot_part,
+    DC_TRY(clk.done(dc::launch_proj_tc(1, hidden, w->map_slot_hi, w->map_slot_lo, nullptr, cfg.slots, B,
+                                       rows, d, V, 2 * kR, h->splits_slot, ws.slot_proj, ws.slot_part,
                                        ws.slot_tiles, ws.err, st)));
-    DC_TRY(clk.done(dc::launch_proj_tc(0, E, ids, cfg.slots, B, cands, d, V, w->cand_hi, w->cand_lo,
-                                       2 * kR, h->splits_cand, ws.cand_proj, ws.cand_part,
+    DC_TRY(clk.done(dc::launch_proj_tc(0, E, w->map_cand_hi, w->map_cand_lo, ids, cfg.slots, B,
+                                       cands, d, V, 2 * kR, h->splits_cand, ws.cand_proj, ws.cand_part,
                                        ws.cand_tiles, ws.err, st)));
     DC_TRY(clk.done(dc::launch_cos_post(K, ws.cand_proj, ws.slot_proj, N, B, ws.U, ws.V, st)));
     DC_TRY(clk.done(dc::launch_cos_score(K, ws.U, ws.V, vals, cfg.sigma, N, B, scores, st)));
@@ -473,6 +472,14 @@ int dcoco_weights_create(dcoco_handle *h, const dcoco_weight_ptrs *wp, void *str
   w->cand_lo = dproj + (size_t)cand_rows * d;
   w->slot_hi = w->cand_lo + (size_t)cand_rows * d;
   w->slot_lo = w->slot_hi + (size_t)slot_rows * d;
+  if (!dc::encode_bf16_rows_map(&w->map_cand_hi, w->cand_hi, cand_rows, d, 128) ||
+      !dc::encode_bf16_rows_map(&w->map_cand_lo, w->cand_lo, cand_rows, d, 128) ||
+      !dc::encode_bf16_rows_map(&w->map_slot_hi, w->slot_hi, slot_rows, d, 128) ||
+      !dc::encode_bf16_rows_map(&w->map_slot_lo, w->slot_lo, slot_rows, d, 128)) {
+    cudaFree(w->block);
+    delete w;
+    return DCOCO_ECUDA;
+  }
   if (cfg.variant == 0) {
     dc::MlpWeightsDev &m = w->mlp;
     m.wfb_t = dmlp + off[0]; m.wfg_t = dmlp + off[1]; m.gamma = dmlp + off[2]; m.beta = dmlp + off[3];
@@ -557,7 +564,7 @@ int dcoco_topk(dcoco_handle *h, int batch, const void *logits, int64_t stride, i
   const dc::TopkPlan plan = dc::topk_plan(h->cfg.vocab, batch * h->B, h->topk_wave);
   return cuda_status(dc::launch_topk(h->cfg.topk, static_cast<const uint16_t *>(logits), stride,
                                      h->cfg.slots, batch, h->cfg.vocab, plan, h->ws.part,
-                                     h->ws.row_count, h->ws.row_bound, topk_ids, topk_val, st));
+                                     h->ws.row_count, topk_ids, topk_val, st));
 }
 
 int dcoco_get_device_status(dcoco_handle *h) {

@@ -3,50 +3,58 @@
 // launch; none allocates or synchronises.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace dc {
 
 // ---------------------------------------------------------------- top-K
-// Segmented top-K: each logits row is cut into `nchunks` segments, one CTA
-// per (segment, row); each of the CTA's 8 warps streams `chunk_vecs` 16-byte
-// vectors.  With several segments, every CTA publishes its best K to `part`
-// (rows * nchunks * K packed keys) and the last CTA of the row, counted in
-// `row_count` (rows entries, zero between calls), merges them.  `row_bound`
-// (rows entries, zero between calls) carries the best published K-th key of
-// each row to the segments launched after it.
+// Segmented top-K: each logits row is cut into `nchunks` segments of
+// `chunk_vecs` 16-byte vectors, one CTA per (row, segment).  With several
+// segments, every CTA publishes its best K to `part` (rows * nchunks * K
+// packed keys) and the last CTA of the row, counted in `row_count` (rows
+// entries, zero between calls), merges them.  When `emb` ([V][d] bf16) is
+// given, the final CTA of each row also prefetches the K chosen embedding
+// rows into L2 for the candidate projection that follows.
 struct TopkPlan {
   int nchunks;     // segments per row
-  int chunk_vecs;  // 16-byte vectors per warp
+  int chunk_vecs;  // 16-byte vectors per segment
 };
 constexpr int kTopkThreads = 256;
 constexpr int kTopkMaxChunks = 64;
-// Segment count that best fills `slots_per_wave` resident CTAs for `rows` rows.
+// Segment count that gives the shortest launch for `rows` rows on a device
+// holding `slots_per_wave` resident top-K CTAs.
 TopkPlan topk_plan(int V, int rows, int slots_per_wave);
+int topk_min_segments(int V);  // fewest segments whose per-vector maxima fit a CTA
 int topk_max_segments(int V);
 int topk_occupancy(int K);  // resident top-K CTAs per SM
 cudaError_t launch_topk(int K, const uint16_t *logits, int64_t stride, int slots, int N, int V,
                         const TopkPlan &plan, unsigned long long *part, unsigned *row_count,
-                        unsigned long long *row_bound, int32_t *ids, float *vals, cudaStream_t st);
+                        int32_t *ids, float *vals, cudaStream_t st, const uint16_t *emb = nullptr,
+                        int d = 0);
 
 // ---------------------------------------------------------------- projections
 // C[m][o] = sum_k A_m[k] * W[o][k] with A_m a bf16 row of length d.  Row
-// addressing: mode 0 gathers A_m = base[ids[m]] (ids < V, else the device
+// addressing: mode 0 gathers A_m = table[ids[m]] (ids < V, else the device
 // status word gets kErrBadCandidateId and row 0 is used); mode 1 takes
-// A_m = base[(m / B) * slots + (m % B) + 1] (the draft-slot rows of a
+// A_m = table[(m / B) * slots + (m % B) + 1] (the draft-slot rows of a
 // [N][slots][d] tensor).
-// W is given as bf16 hi and lo
-// halves ([No][d] each, No % 128 == 0, d % 64 == 0).  `splits` >= 2 splits
-// the k range; then `part` holds splits * ceil(M/128)*128 * No floats and
-// `tile_count` (No/128 * ceil(M/128) entries, zero between calls) counts the
-// finished splits of each tile.
+// Tensor-core projection.  A rows are gathered from `table` (bf16 [rows][d]:
+// E, or the hidden states viewed as [N*slots][d]); W comes as bf16 hi and lo
+// halves ([No][d] each, No % 128 == 0,
+// d % 64 == 0) through `map_hi` / `map_lo` (box 64 x 128).  `splits` >= 2
+// splits the k range; then `part` holds splits * ceil(M/128)*128 * No floats
+// and `tile_count` (No/128 * ceil(M/128) entries, zero between calls) counts
+// the finished splits of each tile.
 size_t proj_tc_smem_bytes();
 int proj_tc_splits(int d, int requested);
-cudaError_t launch_proj_tc(int mode, const uint16_t *base, const int32_t *ids, int slots, int B, int M,
-                           int d, int V, const uint16_t *w_hi, const uint16_t *w_lo, int No,
-                           int splits, float *C, float *part, unsigned *tile_count, int *err,
-                           cudaStream_t st);
+// 2D bf16 [rows][d] tensor map, 128B swizzle, box 64 x box_rows.
+bool encode_bf16_rows_map(CUtensorMap *map, const void *base, int rows, int d, int box_rows);
+cudaError_t launch_proj_tc(int mode, const uint16_t *table, const CUtensorMap &map_hi,
+                           const CUtensorMap &map_lo, const int32_t *ids, int slots, int B, int M, int d,
+                           int V, int No, int splits, float *C, float *part, unsigned *tile_count,
+                           int *err, cudaStream_t st);
 
 // ---------------------------------------------------------------- representations
 struct MlpWeightsDev {

@@ -10,15 +10,21 @@
 // (w = hi + lo to ~2^-17 relative), and both products accumulate into the same
 // fp32 accumulator: C = A hi^T + A lo^T.
 //
-// Tile: 128 rows x 128 outputs, k-blocks of 64 (one 128-byte swizzle atom).
-// Warps 0-3 stage A, hi and lo into 128B-swizzled K-major shared memory with
-// cp.async (4-stage ring, mbarrier full/empty pairs) and afterwards drain the
-// accumulator with tcgen05.ld; warp 4 allocates tensor memory and one of its
-// lanes issues the MMAs.  Split-K over gridDim.z: every split writes an fp32
+// Tile: 128 rows x 128 outputs, k-blocks of 64 (one 128-byte swizzle atom),
+// a 4-stage ring in 128B-swizzled K-major shared memory.  Each operand takes
+// the path that suits it: warps 0-3 gather the A rows with 16-byte cp.async
+// (many small independent rows), one thread of warp 4 brings the hi and lo
+// weight blocks as two 2D TMA tiles (large blocks, the same for every CTA);
+// a stage is full when the 128 gatherers have arrived and the TMA bytes have
+// landed.  One thread of warp 5 (which also owns the tensor-memory
+// allocation) issues the MMAs; warps 0-3 then drain the accumulator with
+// tcgen05.ld.  Split-K over gridDim.z: every split writes an fp32
 // partial tile and the tile's last CTA (atomic counter) adds the partials in
 // split order, so the result does not depend on which CTA finished last.
 // Every wait is bounded in time; on expiry the kernel records kErrTimeout in
 // the device status word and leaves without touching the output.
+#include <cuda.h>
+
 #include <algorithm>
 
 #include "common.cuh"
@@ -31,9 +37,11 @@ constexpr int kStages = 4;
 constexpr int kTileM = 128, kTileN = 128, kTileK = 64;
 constexpr int kTileBytes = kTileM * kTileK * 2;        // 16 KB (A, hi or lo)
 constexpr int kStageBytes = 3 * kTileBytes;             // A + hi + lo
-constexpr int kProducerThreads = 128;
-constexpr int kThreads = kProducerThreads + 32;         // + the MMA warp
+constexpr int kGatherThreads = 128;  // warps 0-3: A gather, then epilogue
+constexpr int kThreads = 192;        // + warp 4 (weight TMA) + warp 5 (MMA)
+constexpr uint32_t kStageTx = 2u * kTileBytes;  // weight bytes per stage
 constexpr uint32_t kTmemCols = 128;
+constexpr int kMaxSplits = 8;
 constexpr unsigned long long kWaitNs = 1000000000ull;   // 1 s
 
 // instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, M=128, N=128
@@ -52,10 +60,6 @@ __device__ __forceinline__ unsigned long long global_ns() {
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
@@ -89,9 +93,21 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+// Bounded wait used only on the abort path, ignoring the abort flag: lets
+// copies and MMAs already issued land before the CTA frees its resources.
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+  const unsigned long long t0 = global_ns();
+  while (!mbar_try(bar, parity))
+    if (global_ns() - t0 > kWaitNs) return;
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                : "memory");
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -100,6 +116,18 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// 2D tiled TMA load of one box at (x = column, y = row).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
 }
 
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
@@ -156,14 +184,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
-k_proj_tc(const uint16_t *__restrict__ base, const int32_t *__restrict__ ids, int slots, int B,
-          int M, int d, int V, const uint16_t *__restrict__ w_hi, const uint16_t *__restrict__ w_lo,
-          int No, int kb_per_split, float *__restrict__ C, float *__restrict__ part,
-          unsigned *__restrict__ tile_count, int *err) {
+k_proj_tc(const uint16_t *__restrict__ table, const __grid_constant__ CUtensorMap map_hi,
+          const __grid_constant__ CUtensorMap map_lo, const int32_t *__restrict__ ids, int slots,
+          int B, int M, int d, int V, int No, int kb_per_split, float *__restrict__ C,
+          float *__restrict__ part, unsigned *__restrict__ tile_count, int *err) {
   extern __shared__ uint8_t smem_raw[];
   // the swizzle atoms need 1024-byte alignment in the shared window
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ __align__(8) unsigned long long bar_full[kStages], bar_empty[kStages], bar_done;
+  __shared__ int s_rows[kTileM];  // table row of each tile row (A operand)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   __shared__ int s_last;
@@ -177,14 +206,31 @@ k_proj_tc(const uint16_t *__restrict__ base, const int32_t *__restrict__ ids, in
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&bar_full[s]), kProducerThreads);
+      mbar_init(smem_u32(&bar_full[s]), kGatherThreads + 1);
       mbar_init(smem_u32(&bar_empty[s]), 1);
     }
     mbar_init(smem_u32(&bar_done), 1);
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 4) {
+  if (tid < kTileM) {
+    const int m = m0 + tid;
+    int row = 0;  // rows past M load table row 0; their results are never stored
+    if (m < M) {
+      if (MODE == 0) {
+        row = ids[m];
+        if (row < 0 || row >= V) {
+          atomicOr(err, kErrBadCandidateId);
+          row = 0;
+        }
+      } else {
+        const int n = m / B, i = m - n * B;
+        row = n * slots + i + 1;
+      }
+    }
+    s_rows[tid] = row;
+  }
+  if (warp == 5) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_u32(&s_tmem)),
                  "r"(kTmemCols)
@@ -196,54 +242,26 @@ k_proj_tc(const uint16_t *__restrict__ base, const int32_t *__restrict__ ids, in
   tc_fence_after();
   const uint32_t tmem = s_tmem;
 
+  int issued = 0;  // stages whose weight TMA this thread issued
   if (warp < 4) {
-    // ------------------------------------------------------------ producers
+    // ------------------------------------------------------------ A gather (cp.async)
     const int t = tid;
     const int c = t & 7;              // 16-byte chunk of the 128-byte k-row
     const int rq = (t >> 3) & 7;      // row within an 8-row swizzle group
     const uint32_t off0 = (uint32_t)((t >> 6) * 1024 + rq * 128 + ((c ^ rq) * 16));
     const uint16_t *arow[8];
-    uint32_t abytes[8];
-    const uint16_t *hrow[8];
-    const uint16_t *lrow[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int r = (t >> 3) + 16 * j;
-      const int m = m0 + r;
-      abytes[j] = 16u;
-      if (m < M) {
-        if (MODE == 0) {
-          int id = ids[m];
-          if (id < 0 || id >= V) {
-            atomicOr(err, kErrBadCandidateId);
-            id = 0;
-          }
-          arow[j] = base + (int64_t)id * d;
-        } else {
-          const int n = m / B, i = m - n * B;
-          arow[j] = base + ((int64_t)n * slots + i + 1) * d;
-        }
-      } else {
-        arow[j] = base;
-        abytes[j] = 0u;  // rows past M are zero-filled
-      }
-      hrow[j] = w_hi + (int64_t)(n0 + r) * d;
-      lrow[j] = w_lo + (int64_t)(n0 + r) * d;
-    }
+    for (int j = 0; j < 8; ++j) arow[j] = table + (int64_t)s_rows[(t >> 3) + 16 * j] * d + c * 8;
     int it = 0;
     for (; it < nkb; ++it) {
       const int s = it % kStages;
       if (it >= kStages &&
           !mbar_wait(smem_u32(&bar_empty[s]), ((it / kStages) - 1) & 1, &s_abort, err))
         break;
-      const int kel = (kb0 + it) * kTileK + c * 8;  // element offset of this chunk
+      const int kel = (kb0 + it) * kTileK;
       const uint32_t sa = sbase + s * kStageBytes + off0;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        cp_async16(sa + j * 2048, arow[j] + kel, abytes[j]);
-        cp_async16(sa + kTileBytes + j * 2048, hrow[j] + kel, 16u);
-        cp_async16(sa + 2 * kTileBytes + j * 2048, lrow[j] + kel, 16u);
-      }
+      for (int j = 0; j < 8; ++j) cp_async16(sa + j * 2048, arow[j] + kel);
       cp_async_commit();
       if (it >= kStages - 1) {
         cp_async_wait<kStages - 1>();
@@ -254,7 +272,23 @@ k_proj_tc(const uint16_t *__restrict__ base, const int32_t *__restrict__ ids, in
     cp_async_wait<0>();
     fence_proxy_async();
     for (int r = max(0, it - (kStages - 1)); r < it; ++r) mbar_arrive(smem_u32(&bar_full[r % kStages]));
-  } else if (lane == 0) {
+  } else if (warp == 4) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ weight TMA
+      for (int it = 0; it < nkb; ++it, ++issued) {
+        const int s = it % kStages;
+        if (it >= kStages &&
+            !mbar_wait(smem_u32(&bar_empty[s]), ((it / kStages) - 1) & 1, &s_abort, err))
+          break;
+        const uint32_t full = smem_u32(&bar_full[s]);
+        const uint32_t sa = sbase + s * kStageBytes;
+        const int kx = (kb0 + it) * kTileK;
+        mbar_arrive_expect_tx(full, kStageTx);
+        tma_load_2d(sa + kTileBytes, &map_hi, kx, n0, full);
+        tma_load_2d(sa + 2 * kTileBytes, &map_lo, kx, n0, full);
+      }
+    }
+  } else if (warp == 5 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     for (int it = 0; it < nkb; ++it) {
       const int s = it % kStages;
@@ -297,7 +331,17 @@ k_proj_tc(const uint16_t *__restrict__ base, const int32_t *__restrict__ ids, in
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 4) {
+  if (s_abort) {
+    // a wait expired: let everything already issued land before leaving
+    if (warp == 4 && lane == 0)
+      for (int s = 0; s < kStages && s < issued; ++s) {
+        const int last = s + kStages * ((issued - 1 - s) / kStages);
+        mbar_drain(smem_u32(&bar_full[s]), (last / kStages) & 1);
+      }
+    if (warp == 5 && lane == 0) mbar_drain(smem_u32(&bar_done), 0);
+    __syncthreads();
+  }
+  if (warp == 5) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                  : "memory");
@@ -314,14 +358,20 @@ k_proj_tc(const uint16_t *__restrict__ base, const int32_t *__restrict__ ids, in
   __threadfence();
   const int rows = min(kTileM, M - m0);
   const int64_t pstride = (int64_t)gridDim.y * kTileM * No;
+  const int nz = (int)gridDim.z;  // <= kMaxSplits
   for (int e = tid; e < rows * (kTileN / 4); e += kThreads) {
     const int r = e / (kTileN / 4), q = e - r * (kTileN / 4);
     const int64_t off = (int64_t)(m0 + r) * No + n0 + q * 4;
-    float4 acc = __ldcg(reinterpret_cast<const float4 *>(part + off));
-    for (int z = 1; z < (int)gridDim.z; ++z) {
-      const float4 p = __ldcg(reinterpret_cast<const float4 *>(part + z * pstride + off));
-      acc.x += p.x; acc.y += p.y; acc.z += p.z; acc.w += p.w;
-    }
+    float4 p[kMaxSplits];
+#pragma unroll
+    for (int z = 0; z < kMaxSplits; ++z)  // every partial load in flight at once
+      if (z < nz) p[z] = __ldcg(reinterpret_cast<const float4 *>(part + z * pstride + off));
+    float4 acc = p[0];
+#pragma unroll
+    for (int z = 1; z < kMaxSplits; ++z)
+      if (z < nz) {
+        acc.x += p[z].x; acc.y += p[z].y; acc.z += p[z].z; acc.w += p[z].w;
+      }
     *reinterpret_cast<float4 *>(C + off) = acc;
   }
   if (tid == 0) tile_count[tile] = 0u;
@@ -333,17 +383,52 @@ size_t proj_tc_smem_bytes() { return (size_t)kStages * kStageBytes + 1024; }
 
 int proj_tc_splits(int d, int requested) {
   const int nkb = d / kTileK;
-  int s = std::max(1, std::min(requested, nkb));
+  int s = std::max(1, std::min(std::min(requested, kMaxSplits), nkb));
   const int per = (nkb + s - 1) / s;
   return (nkb + per - 1) / per;  // no empty split
 }
 
-cudaError_t launch_proj_tc(int mode, const uint16_t *base, const int32_t *ids, int slots, int B, int M,
-                           int d, int V, const uint16_t *w_hi, const uint16_t *w_lo, int No,
-                           int splits, float *C, float *part, unsigned *tile_count, int *err,
-                           cudaStream_t st) {
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+}  // namespace
+
+bool encode_bf16_rows_map(CUtensorMap *map, const void *base, int rows, int d, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows <= 0 || d % kTileK != 0 || (reinterpret_cast<uintptr_t>(base) & 15u)) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kTileK, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_proj_tc(int mode, const uint16_t *table, const CUtensorMap &map_hi,
+                           const CUtensorMap &map_lo, const int32_t *ids, int slots, int B, int M, int d,
+                           int V, int No, int splits, float *C, float *part, unsigned *tile_count,
+                           int *err, cudaStream_t st) {
   if (M == 0) return cudaSuccess;
-  if (No % kTileN != 0 || d % kTileK != 0) return cudaErrorInvalidValue;
+  if (No % kTileN != 0 || d % kTileK != 0 || splits < 1 || splits > kMaxSplits) return cudaErrorInvalidValue;
   const int nkb = d / kTileK;
   const int per = (nkb + splits - 1) / splits;
   dim3 grid(No / kTileN, (M + kTileM - 1) / kTileM, splits);
@@ -352,12 +437,12 @@ cudaError_t launch_proj_tc(int mode, const uint16_t *base, const int32_t *ids, i
   if (mode == 0) {
     e = cudaFuncSetAttribute(k_proj_tc<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k_proj_tc<0><<<grid, kThreads, smem, st>>>(base, ids, slots, B, M, d, V, w_hi, w_lo, No, per, C,
+    k_proj_tc<0><<<grid, kThreads, smem, st>>>(table, map_hi, map_lo, ids, slots, B, M, d, V, No, per, C,
                                               part, tile_count, err);
   } else {
     e = cudaFuncSetAttribute(k_proj_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k_proj_tc<1><<<grid, kThreads, smem, st>>>(base, ids, slots, B, M, d, V, w_hi, w_lo, No, per, C,
+    k_proj_tc<1><<<grid, kThreads, smem, st>>>(table, map_hi, map_lo, ids, slots, B, M, d, V, No, per, C,
                                               part, tile_count, err);
   }
   return cudaGetLastError();

@@ -43,65 +43,70 @@ __device__ __forceinline__ void warp_ln0_128(float (&x)[4], float eps) {
 }
 
 // ---------------------------------------------------------------- per slot
+// One CTA per 8 consecutive draft slots of the flattened [N*B] slot index
+// (warp w owns slot s0 + w for the LayerNorm); every thread then produces one
+// output feature for all 8 slots, so each weight is read once per CTA.
+constexpr int kSlotsPerCta = 8;
+
 __global__ void __launch_bounds__(256)
-k_slot_post(const float *__restrict__ slot_proj, int B, float eps, MlpWeightsDev w,
+k_slot_post(const float *__restrict__ slot_proj, int NB, int B, float eps, MlpWeightsDev w,
             float *__restrict__ Gf, float *__restrict__ Pout) {
-  __shared__ float g[32][R];
-  __shared__ float s[32][R];
-  const int n = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const float *sp = slot_proj + (int64_t)n * B * 3 * R;
-
-  for (int i = warp; i < B; i += 8) {
-    float x[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) x[u] = sp[(int64_t)i * 3 * R + lane + 32 * u];
-    warp_ln0_128(x, eps);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) g[i][lane + 32 * u] = x[u];
-  }
-  for (int e = tid; e < (B - 1) * R; e += 256) {
-    const int p = e / R, k = e - p * R;
-    s[p][k] = sp[(int64_t)p * 3 * R + R + k] + sp[(int64_t)(p + 1) * 3 * R + 2 * R + k];
-  }
-  __syncthreads();
-
-  // Gf_i = W_fuse[:, r:] g_i
+  __shared__ float g[kSlotsPerCta][R];
+  __shared__ float s[kSlotsPerCta][R];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int s0 = blockIdx.x * kSlotsPerCta;
   {
-    const int o = tid & (R - 1), half = tid >> 7;
-    for (int i0 = half; i0 < B; i0 += 16) {
-      float acc[8] = {};
-      for (int k = 0; k < R; ++k) {
-        const float wv = w.wfg_t[k * R + o];
+    const int gs = s0 + warp;  // this warp's slot
+    if (gs < NB) {
+      const float *sp = slot_proj + (int64_t)gs * 3 * R;
+      float x[4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int i = i0 + 2 * u;
-          if (i < B) acc[u] = fmaf(wv, g[i][k], acc[u]);
-        }
-      }
+      for (int u = 0; u < 4; ++u) x[u] = sp[lane + 32 * u];
+      warp_ln0_128(x, eps);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = i0 + 2 * u;
-        if (i < B) Gf[((int64_t)n * B + i) * R + o] = acc[u];
+      for (int u = 0; u < 4; ++u) g[warp][lane + 32 * u] = x[u];
+      // pair state s_p = W_pair[:, :d] h_p + W_pair[:, d:] h_{p+1} for p = this slot
+      const int i = gs % B;
+      if (i < B - 1) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          s[warp][lane + 32 * u] = sp[R + lane + 32 * u] + sp[3 * R + 2 * R + lane + 32 * u];
       }
     }
   }
-  // P_p = W1_s s_p + b1
+  __syncthreads();
+  // Gf = W_fuse[:, r:] g   (threads 0..127: one output feature, 8 slots)
+  if (tid < R) {
+    float acc[kSlotsPerCta] = {};
+#pragma unroll 16
+    for (int k = 0; k < R; ++k) {
+      const float wv = w.wfg_t[k * R + tid];
+#pragma unroll
+      for (int u = 0; u < kSlotsPerCta; ++u) acc[u] = fmaf(wv, g[u][k], acc[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < kSlotsPerCta; ++u)
+      if (s0 + u < NB) Gf[(int64_t)(s0 + u) * R + tid] = acc[u];
+  }
+  // P_p = W1_s s_p + b1   (all 256 threads: one hidden unit, 8 slots)
   {
     const int j = tid;
     const float bj = w.b1[j];
-    for (int p0 = 0; p0 < B - 1; p0 += 8) {
-      float acc[8];
+    float acc[kSlotsPerCta];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) acc[u] = bj;
-      for (int k = 0; k < R; ++k) {
-        const float wv = w.w1s_t[k * H + j];
+    for (int u = 0; u < kSlotsPerCta; ++u) acc[u] = bj;
+#pragma unroll 16
+    for (int k = 0; k < R; ++k) {
+      const float wv = w.w1s_t[k * H + j];
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (p0 + u < B - 1) acc[u] = fmaf(wv, s[p0 + u][k], acc[u]);
-      }
+      for (int u = 0; u < kSlotsPerCta; ++u) acc[u] = fmaf(wv, s[u][k], acc[u]);
+    }
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (p0 + u < B - 1) Pout[((int64_t)n * (B - 1) + p0 + u) * H + j] = acc[u];
+    for (int u = 0; u < kSlotsPerCta; ++u) {
+      const int gs = s0 + u;
+      if (gs >= NB) continue;
+      const int n = gs / B, i = gs - n * B;
+      if (i < B - 1) Pout[((int64_t)n * (B - 1) + i) * H + j] = acc[u];
     }
   }
 }
@@ -133,6 +138,7 @@ k_cand_post(const float *__restrict__ cand_proj, const float *__restrict__ topk_
     constexpr int KH = K / 2;
     const int o = tid & (R - 1), half = tid >> 7;
     float acc[KH] = {};
+#pragma unroll 16
     for (int k = 0; k < R; ++k) {
       const float wv = w.wfb_t[k * R + o];
 #pragma unroll
@@ -163,6 +169,7 @@ k_cand_post(const float *__restrict__ cand_proj, const float *__restrict__ topk_
     const float wl = pass == 0 ? w.w_la[j] : w.w_lb[j];
     float *dst = pass == 0 ? U : Vout;
     float acc[K] = {};
+#pragma unroll 8
     for (int k = 0; k < R; ++k) {
       const float wv = wt[k * H + j];
 #pragma unroll
@@ -191,6 +198,7 @@ k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
   const int64_t cb = ca + K;                         // first candidate of slot p+1
   const float *Pp = P + (int64_t)np * H;
 
+#pragma unroll 8
   for (int e = tid; e < K * H; e += 256) {
     const int c = e / H, j = e - c * H;
     pu[c * (H + 1) + j] = U[(ca + c) * H + j] + Pp[j];
@@ -266,7 +274,8 @@ k_cos_score(const float *__restrict__ O, const float *__restrict__ I,
 cudaError_t launch_slot_post(const float *slot_proj, int N, int B, float eps, const MlpWeightsDev &w,
                              float *Gf, float *P, cudaStream_t st) {
   if (N == 0) return cudaSuccess;
-  k_slot_post<<<N, 256, 0, st>>>(slot_proj, B, eps, w, Gf, P);
+  const int NB = N * B;
+  k_slot_post<<<(NB + kSlotsPerCta - 1) / kSlotsPerCta, 256, 0, st>>>(slot_proj, NB, B, eps, w, Gf, P);
   return cudaGetLastError();
 }
 

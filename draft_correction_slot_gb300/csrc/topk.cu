@@ -5,30 +5,28 @@
 // candidates of its draft logits.  Order: value descending, then token id
 // ascending; -0 == +0.
 //
-// Design (HBM-bound, one pass over the logits, no barrier while streaming):
-//   * A row (request n, draft slot i) is cut into `nseg` segments, one
-//     256-thread CTA each; the CTA's 8 warps each stream a contiguous slice of
-//     the segment, 4 coalesced 16-byte vectors per lane per iteration, with the
-//     next iteration's loads in flight while the current one is examined.
-//   * Each warp keeps its running top-K sorted in registers (lane k holds the
-//     k-th best as a 64-bit key  order16(value) << 32 | 0xFFFFFFFF - id, so one
-//     unsigned compare orders by value, then by lower id).
-//   * First iteration: the K-th largest of the 32 lane maxima (radix select
-//     with ballots) is a lower bound of the slice's K-th value -- K lanes each
-//     hold an element at least that large -- so only elements >= it are
-//     inserted.  Later iterations: a vector is examined only if its packed
-//     bf16x2 maximum beats the running K-th value strictly (an equal value
-//     cannot enter: its id is larger than every id already kept).
-//   * Each element must also reach a lower bound of the row's K-th value: the
-//     best K-th key published so far by any warp of the CTA (shared memory) or
-//     by an earlier segment of the row (global memory; segments are launched
-//     segment-major, so most CTAs start with a high bound).
-//   * Survivors are extracted divergently into a per-warp shared buffer, then
-//     inserted warp-cooperatively (shuffle-shift insert), so the cost follows
-//     the number of candidates.  The 8 warp lists are merged in shared memory by rank
-//     (own position + binary-search counts in the other lists); with several
-//     segments, each CTA publishes its list and the last CTA of the row
-//     (atomic counter, reset after use) merges them the same way.
+// Design (HBM-bound; every logit is read from HBM exactly once):
+//   * A row (request n, draft slot i) is cut into `nseg` segments of at most
+//     20480 16-byte vectors, one 256-thread CTA each (usually one per row).
+//   * Pass 1 -- stream: each warp reads a contiguous slice of the segment,
+//     4 coalesced 16-byte vectors per lane per iteration with the next ones in
+//     flight, and stores each vector's maximum (packed bf16x2 max) in shared
+//     memory.  Nothing else happens while streaming.
+//   * Pass 2 -- bound: T = the K-th largest maximum of the groups of 64
+//     vectors.  K groups each hold an element >= T, so the segment's K-th
+//     value is >= T: every element of the segment's top-K lies in a vector
+//     whose maximum reaches T.  Those vectors (typically about K of them) are
+//     listed in order.
+//   * Pass 3 -- select: the listed vectors are read again (L2) and their
+//     elements >= T ranked exactly, as 64-bit keys
+//     order16(value) << 32 | 0xFFFFFFFF - id (one unsigned compare orders by
+//     value, then by lower id), with bitonic warp merges.
+//   * Degenerate segments (many ties at the bound, -inf masks) list too many
+//     vectors; they are streamed again with per-warp running lists instead:
+//     each warp keeps its top-K in registers and only elements above the
+//     running bounds are inserted.
+//   * With several segments, each CTA publishes its list and the last CTA of
+//     the row (atomic counter, reset after use) merges them.
 #include <algorithm>
 
 #include "common.cuh"
@@ -42,6 +40,15 @@ constexpr int kThreads = kTopkThreads;
 constexpr int kWarps = kThreads / 32;
 constexpr int kU = 4;                 // vectors per lane per iteration
 constexpr int kStep = 32 * kU;        // vectors per warp iteration
+constexpr int kSerialMax = 8;         // up to this many candidates: serial inserts
+constexpr int kPrefetchAhead = 4;     // L2 prefetch distance, in iterations (fallback)
+constexpr int kGroup = 64;            // vectors per group in the bound of pass 2
+constexpr int kMaxSegVecs = 20480;    // vectors per segment (16-bit maxima in shared memory)
+constexpr int kRawWords = (kWarps * kStep * 8 > kMaxSegVecs / 2) ? kWarps * kStep * 8 : kMaxSegVecs / 2;
+constexpr int kMaxGroups = kMaxSegVecs / kGroup;
+constexpr int kCandGroups = 64;       // groups reaching the bound beyond this: degenerate path
+constexpr int kMaxHitsPerLane = 4;    // hit vectors a lane re-loads (more: degenerate path)
+constexpr int kCandElems = 8 * kWarps * 32 * kMaxHitsPerLane / 4;  // key buffer (fits s_raw)
 constexpr uint32_t kNegInf2 = 0xFF80FF80u;
 
 typedef unsigned long long u64;
@@ -112,155 +119,390 @@ __device__ __forceinline__ uint32_t bf16_from_key(uint32_t key) {
   return (key & 0x8000u) ? (key & 0x7FFFu) : (~key & 0xFFFFu);
 }
 
+// Logits are read exactly once: mark them evict-first in L2 so they do not
+// displace the candidate embedding rows prefetched for the next step.
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint4 ld_stream_ef(const void *ptr, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr), "l"(pol));
+  return v;
+}
+
 __device__ __forceinline__ void load_vecs(uint4 (&v)[kU], const uint16_t *rowp, int base, int end,
-                                          int lane) {
+                                          int lane, uint64_t pol) {
 #pragma unroll
   for (int u = 0; u < kU; ++u) {
     const int j = base + lane + 32 * u;
-    if (j < end) v[u] = ld_stream_v4(rowp + (int64_t)j * 8);
+    if (j < end) v[u] = ld_stream_ef(rowp + (int64_t)j * 8, pol);
     else v[u] = make_uint4(kNegInf2, kNegInf2, kNegInf2, kNegInf2);
   }
+}
+
+// Fallback for degenerate segments: each warp streams [w0, w1) again and
+// keeps its own top-K, inserting only elements whose key reaches the running
+// bound (the CTA-shared bound, never below `floor_key`, or its own K-th).
+template <int K>
+__device__ __forceinline__ u64 stream_fallback(const uint16_t *rowp, int w0, int w1, uint32_t floor_key,
+                                               u64 *s_cta_bound, uint32_t *s_bufw, int lane,
+                                               uint64_t pol) {
+  u64 list = 0ull, kth = 0ull;
+  uint4 cur[kU], nxt[kU];
+  if (w0 < w1) load_vecs(cur, rowp, w0, w1, lane, pol);
+  // one iteration: kU vectors per lane, starting at vector `base`
+  auto process = [&](const uint4 (&v)[kU], int base) {
+      uint32_t vm2[kU];
+  #pragma unroll
+      for (int u = 0; u < kU; ++u)
+        vm2[u] = bf16x2_max(bf16x2_max(v[u].x, v[u].y), bf16x2_max(v[u].z, v[u].w));
+      const uint32_t lm2 = bf16x2_max(bf16x2_max(vm2[0], vm2[1]), bf16x2_max(vm2[2], vm2[3]));
+      // An element can reach the row's top-K only if
+      //   key >= bound: bound = the K-th key of some slice of this row (another
+      //     warp's, an earlier segment's, or -- first iteration -- the K-th
+      //     largest lane maximum, since K lanes each hold an element that large);
+      //   and, once this warp holds K elements, value > its own K-th value (an
+      //     equal value arriving later has a larger id and cannot displace it).
+      // Both fold into one order-key threshold tkey: value key >= tkey.
+      const u64 sb = *(volatile u64 *)s_cta_bound;
+      uint32_t tkey = max(floor_key, sb ? (uint32_t)(sb >> 32) : 0u);
+      if (base == w0 && tkey == 0u) {
+        const float lm = fmaxf(bf16_bits_to_float(lm2 & 0xFFFFu), bf16_bits_to_float(lm2 >> 16));
+        const uint32_t key = bf16_order_key(__float_as_uint(lm) >> 16);
+        uint32_t pre = 0;
+  #pragma unroll
+        for (int bit = 15; bit >= 0; --bit) {
+          const uint32_t trial = pre | (1u << bit);
+          if (__popc(__ballot_sync(DC_FULL_MASK, key >= trial)) >= K) pre = trial;
+        }
+        tkey = max(tkey, pre);
+      }
+      if (base != w0 && kth != 0ull) tkey = max(tkey, min((uint32_t)(kth >> 32) + 1u, 0xFFFFu));
+      // packed skip test: every element of the lane is below tkey iff
+      // max(lane max, below) == below, with below = the value just under tkey
+      bool lane_hit = true;
+      uint32_t below2 = 0u;
+      if (tkey > 0x007Fu) {  // tkey above -inf: some elements can be skipped
+        // key 0x7FFF would decode to -0, and max(+0, -0) may return -0: step
+        // one further down there (skipping less is always safe)
+        const uint32_t b = bf16_from_key(tkey - 1u == 0x7FFFu ? 0x7FFEu : tkey - 1u);
+        below2 = b | (b << 16);
+        lane_hit = bf16x2_max(lm2, below2) != below2;
+      }
+      if (__any_sync(DC_FULL_MASK, lane_hit)) {
+        // this lane's candidate mask, bit 8u+q = element q of vector u: the
+        // packed test max(x, below) != below marks x above `below` (ties to
+        // +-0 may add false positives, which the exact key compare of the
+        // insert rejects or which cannot displace a real top-K member)
+        uint32_t emask = 0u;
+        if (lane_hit) {
+#pragma unroll
+          for (int u = 0; u < kU; ++u) {
+            const int j = base + lane + 32 * u;
+            if (j >= w1) continue;
+            if (below2 == 0u) {
+              emask |= 0xFFu << (8 * u);
+              continue;
+            }
+            const uint32_t wd[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const uint32_t dif = bf16x2_max(wd[h], below2) ^ below2;
+              emask |= (((dif & 0xFFFFu) != 0u ? 1u : 0u) | ((dif >> 16) != 0u ? 2u : 0u)) << (8 * u + 2 * h);
+            }
+          }
+        }
+        // warp-exclusive scan of the candidate counts gives each lane its slots
+        const int c = __popc(emask);
+        int incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(DC_FULL_MASK, incl, o);
+          if (lane >= o) incl += t;
+        }
+        const int cnt = __shfl_sync(DC_FULL_MASK, incl, 31);
+        int pos = incl - c;
+        while (emask) {
+          const int e = __ffs(emask) - 1;
+          emask &= emask - 1;
+          const int u = e >> 3, q = e & 7;
+          const uint4 vv = u == 0 ? v[0] : (u == 1 ? v[1] : (u == 2 ? v[2] : v[3]));
+          const uint32_t wd = (q >> 1) == 0 ? vv.x : ((q >> 1) == 1 ? vv.y : ((q >> 1) == 2 ? vv.z : vv.w));
+          const uint32_t bits = (q & 1) ? (wd >> 16) : (wd & 0xFFFFu);
+          const uint32_t off = (uint32_t)(lane + 32 * u) * 8u + (uint32_t)q;
+          s_bufw[pos++] = (bf16_order_key(bits) << 16) | (0xFFFFu - off);
+        }
+        __syncwarp();
+        const uint32_t id0 = (uint32_t)base * 8u;
+        if (cnt <= kSerialMax) {
+          for (int e = 0; e < cnt; ++e) {
+            const uint32_t k32 = s_bufw[e];
+            const u64 key = ((u64)(k32 >> 16) << 32) | (u64)(0xFFFFFFFFu - (id0 + 0xFFFFu - (k32 & 0xFFFFu)));
+            if (key > kth) warp_insert<K>(list, kth, key, lane);
+          }
+        } else {
+          for (int e0 = 0; e0 < cnt; e0 += 32) {
+            u64 key = 0ull;
+            if (e0 + lane < cnt) {
+              const uint32_t k32 = s_bufw[e0 + lane];
+              key = ((u64)(k32 >> 16) << 32) | (u64)(0xFFFFFFFFu - (id0 + 0xFFFFu - (k32 & 0xFFFFu)));
+            }
+            list = warp_merge_topk<K>(list, warp_sort32_desc(key, lane), lane);
+          }
+          kth = shfl_u64(list, K - 1);
+        }
+        if (lane == 0 && kth > sb) atomicMax(s_cta_bound, kth);
+        __syncwarp();  // s_buf is rewritten by the next iteration
+      }
+  };
+  // L2 prefetch kPrefetchAhead iterations ahead of the register loads, so
+  // DRAM keeps streaming while the warp examines its current vectors
+  auto prefetch = [&](int b) {
+    if (lane == 0 && b < w1)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(rowp + (int64_t)b * 8),
+                   "r"((uint32_t)min(kStep, w1 - b) * 16u)
+                   : "memory");
+  };
+#pragma unroll
+  for (int a = 1; a <= kPrefetchAhead; ++a) prefetch(w0 + a * kStep);
+  // ping-pong between two register buffers; the next loads are always in flight
+  for (int base = w0; base < w1; base += 2 * kStep) {
+    prefetch(base + (kPrefetchAhead + 1) * kStep);
+    if (base + kStep < w1) load_vecs(nxt, rowp, base + kStep, w1, lane, pol);
+    process(cur, base);
+    if (base + kStep >= w1) break;
+    prefetch(base + (kPrefetchAhead + 2) * kStep);
+    if (base + 2 * kStep < w1) load_vecs(cur, rowp, base + 2 * kStep, w1, lane, pol);
+    process(nxt, base + kStep);
+  }
+  return list;
 }
 
 template <int K>
 __global__ void __launch_bounds__(kThreads, 4)
 k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, int V, int nseg,
-       int vecs_per_warp, u64 *__restrict__ part, unsigned *__restrict__ row_count,
-       u64 *__restrict__ row_bound, int32_t *__restrict__ out_ids, float *__restrict__ out_val) {
-  // s_buf: one iteration's candidates per warp (streaming phase)
-  __shared__ __align__(16) uint32_t s_buf[kWarps][kStep * 8];
-  __shared__ int s_bcnt[kWarps];
+       int seg_vecs, u64 *__restrict__ part, unsigned *__restrict__ row_count,
+       int32_t *__restrict__ out_ids, float *__restrict__ out_val, const uint16_t *__restrict__ emb,
+       int emb_row_bytes) {
+  // s_vmax (pass 1-2: per-vector maxima, bf16 bits), s_keys (pass 3:
+  // candidate elements) and the fallback's per-warp candidate buffers share
+  // storage; each use ends at a barrier before the next begins
+  static_assert(kCandElems * 8 <= kRawWords * 4, "alias");
+  __shared__ __align__(16) uint32_t s_raw[kRawWords];
+  uint16_t *s_vmax = reinterpret_cast<uint16_t *>(s_raw);
+  u64 *s_keys = reinterpret_cast<u64 *>(s_raw);
+  __shared__ uint16_t s_gkey[kMaxGroups];   // order key of each group's maximum
+  __shared__ int s_cand[kCandGroups];       // candidate groups, in order
   __shared__ u64 s_lists[kWarps * K];
   __shared__ u64 s_top[K];
   __shared__ u64 s_cta_bound;
-  __shared__ int s_flag;
+  __shared__ int s_ncand, s_nkeys, s_flag;
+  __shared__ uint32_t s_tkey;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int row = blockIdx.x, seg = blockIdx.y;  // segment-major launch order
+  const int row = blockIdx.x, seg = blockIdx.y;
   const int n = row / B, i = row - n * B;
   const uint16_t *rowp = logits + ((int64_t)n * slots + i + 1) * stride;
   const int nvec = V >> 3, tail = V & 7;
-  const int gw = seg * kWarps + warp;
-  const int w0 = min(gw * vecs_per_warp, nvec);
-  const int w1 = min(w0 + vecs_per_warp, nvec);
-  if (lane == 0) s_bcnt[warp] = 0;
-  if (tid == 0) s_cta_bound = __ldcg(row_bound + row);  // K-th key of an earlier segment, or 0
+  const int v0 = min(seg * seg_vecs, nvec), v1 = min(v0 + seg_vecs, nvec);
+  const int nv = min(v1 - v0, kMaxSegVecs);           // vectors of this segment
+  const bool has_tail = tail && seg == nseg - 1;
+  const int per_warp = (nv + kWarps - 1) / kWarps;
+  const int w0 = v0 + min(warp * per_warp, nv), w1 = v0 + min((warp + 1) * per_warp, nv);
+  const uint64_t pol = evict_first_policy();
+  if (tid < K) s_top[tid] = 0ull;
+  if (tid == 0) {
+    s_ncand = 0;
+    s_nkeys = 0;
+    s_flag = 0;
+    s_cta_bound = 0ull;
+  }
+
+  // ---------------------------------------------------------------- pass 1: stream
+  {
+    uint4 a[kU], b[kU];
+    auto store = [&](const uint4 (&v)[kU], int base) {
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int j = base + lane + 32 * u;
+        if (j < w1 && j - v0 < kMaxSegVecs) {  // the plan keeps segments within the buffer
+          const uint32_t m2 = bf16x2_max(bf16x2_max(v[u].x, v[u].y), bf16x2_max(v[u].z, v[u].w));
+          s_vmax[j - v0] = (uint16_t)(bf16x2_max(m2, m2 >> 16) & 0xFFFFu);
+        }
+      }
+    };
+    if (w0 < w1) load_vecs(a, rowp, w0, w1, lane, pol);
+    for (int base = w0; base < w1; base += 2 * kStep) {
+      if (base + kStep < w1) load_vecs(b, rowp, base + kStep, w1, lane, pol);
+      store(a, base);
+      if (base + kStep >= w1) break;
+      if (base + 2 * kStep < w1) load_vecs(a, rowp, base + 2 * kStep, w1, lane, pol);
+      store(b, base + kStep);
+    }
+  }
   __syncthreads();
 
-  u64 list = 0ull, kth = 0ull;
-  uint4 cur[kU], nxt[kU];
-  if (w0 < w1) load_vecs(cur, rowp, w0, w1, lane);
-  for (int base = w0; base < w1; base += kStep) {
-    if (base + kStep < w1) load_vecs(nxt, rowp, base + kStep, w1, lane);
-    uint32_t vm2[kU];
-#pragma unroll
-    for (int u = 0; u < kU; ++u)
-      vm2[u] = bf16x2_max(bf16x2_max(cur[u].x, cur[u].y), bf16x2_max(cur[u].z, cur[u].w));
-    const uint32_t lm2 = bf16x2_max(bf16x2_max(vm2[0], vm2[1]), bf16x2_max(vm2[2], vm2[3]));
-    // An element can reach the row's top-K only if
-    //   key >= bound: bound = the K-th key of some slice of this row (another
-    //     warp's, an earlier segment's, or -- first iteration -- the K-th
-    //     largest lane maximum, since K lanes each hold an element that large);
-    //   and, once this warp holds K elements, value > its own K-th value (an
-    //     equal value arriving later has a larger id and cannot displace it).
-    // Both fold into one order-key threshold tkey: value key >= tkey.
-    const u64 sb = *(volatile u64 *)&s_cta_bound;
-    uint32_t tkey = sb ? (uint32_t)(sb >> 32) : 0u;
-    if (base == w0 && sb == 0ull) {
-      const float lm = fmaxf(bf16_bits_to_float(lm2 & 0xFFFFu), bf16_bits_to_float(lm2 >> 16));
-      const uint32_t key = bf16_order_key(__float_as_uint(lm) >> 16);
-      uint32_t pre = 0;
-#pragma unroll
-      for (int bit = 15; bit >= 0; --bit) {
-        const uint32_t trial = pre | (1u << bit);
-        if (__popc(__ballot_sync(DC_FULL_MASK, key >= trial)) >= K) pre = trial;
-      }
-      tkey = max(tkey, pre);
+  // ---------------------------------------------------------------- pass 2: bound
+  const int ng = (nv + kGroup - 1) / kGroup;
+  for (int g = tid; g < ng; g += kThreads) {
+    const int e1 = min((g + 1) * kGroup, nv);
+    uint32_t m2 = 0xFF80FF80u;
+    int e = g * kGroup;
+    for (; e + 8 <= e1; e += 8) {  // 8 maxima per 16-byte read
+      const uint4 q = *reinterpret_cast<const uint4 *>(s_vmax + e);
+      m2 = bf16x2_max(m2, bf16x2_max(bf16x2_max(q.x, q.y), bf16x2_max(q.z, q.w)));
     }
-    if (base != w0 && kth != 0ull) tkey = max(tkey, min((uint32_t)(kth >> 32) + 1u, 0xFFFFu));
-    // packed skip test: every element of the lane is below tkey iff
-    // max(lane max, below) == below, with below = the value just under tkey
-    bool lane_hit = true;
-    uint32_t below2 = 0u;
-    if (tkey > 0x007Fu) {  // tkey above -inf: some elements can be skipped
-      // key 0x7FFF would decode to -0, and max(+0, -0) may return -0: step
-      // one further down there (skipping less is always safe)
-      const uint32_t b = bf16_from_key(tkey - 1u == 0x7FFFu ? 0x7FFEu : tkey - 1u);
-      below2 = b | (b << 16);
-      lane_hit = bf16x2_max(lm2, below2) != below2;
-    }
-    if (__any_sync(DC_FULL_MASK, lane_hit)) {
-      if (lane_hit) {
-        const float thr = order_key_to_float(tkey);  // value >= thr <=> key >= tkey
-#pragma unroll
-        for (int u = 0; u < kU; ++u) {
-          const int j = base + lane + 32 * u;
-          if (j >= w1) continue;
-          if (below2 != 0u && bf16x2_max(vm2[u], below2) == below2) continue;
-          const uint32_t wd[4] = {cur[u].x, cur[u].y, cur[u].z, cur[u].w};
-          const uint32_t off = (uint32_t)(lane + 32 * u) * 8u;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const uint32_t bits = (q & 1) ? (wd[q >> 1] >> 16) : (wd[q >> 1] & 0xFFFFu);
-            if (bf16_bits_to_float(bits) >= thr || tkey <= 0x007Fu) {
-              const int pos = atomicAdd(&s_bcnt[warp], 1);
-              s_buf[warp][pos] = (bf16_order_key(bits) << 16) | (0xFFFFu - (off + (uint32_t)q));
-            }
-          }
-        }
-      }
-      __syncwarp();
-      const int cnt = s_bcnt[warp];
-      const uint32_t id0 = (uint32_t)base * 8u;
-      if (cnt <= 4) {
-        for (int e = 0; e < cnt; ++e) {
-          const uint32_t k32 = s_buf[warp][e];
-          const u64 key = ((u64)(k32 >> 16) << 32) | (u64)(0xFFFFFFFFu - (id0 + 0xFFFFu - (k32 & 0xFFFFu)));
-          if (key > kth) warp_insert<K>(list, kth, key, lane);
-        }
-      } else {
-        for (int e0 = 0; e0 < cnt; e0 += 32) {
-          u64 key = 0ull;
-          if (e0 + lane < cnt) {
-            const uint32_t k32 = s_buf[warp][e0 + lane];
-            key = ((u64)(k32 >> 16) << 32) | (u64)(0xFFFFFFFFu - (id0 + 0xFFFFu - (k32 & 0xFFFFu)));
-          }
-          list = warp_merge_topk<K>(list, warp_sort32_desc(key, lane), lane);
-        }
-        kth = shfl_u64(list, K - 1);
-      }
-      __syncwarp();
-      if (lane == 0) {
-        s_bcnt[warp] = 0;
-        if (kth) atomicMax(&s_cta_bound, kth);
-      }
-      __syncwarp();
-    }
-#pragma unroll
-    for (int u = 0; u < kU; ++u) cur[u] = nxt[u];
+    for (; e < e1; ++e) m2 = bf16x2_max(m2, 0xFF800000u | s_vmax[e]);
+    s_gkey[g] = (uint16_t)max(bf16_order_key(m2 & 0xFFFFu), bf16_order_key(m2 >> 16));
   }
-  // the scalar tail (V % 8 elements) belongs to the row's last warp
-  if (tail && seg == nseg - 1 && warp == kWarps - 1) {
-    uint32_t bits = 0u;
-    if (lane < tail) bits = rowp[(int64_t)nvec * 8 + lane];
-    unsigned m = __ballot_sync(DC_FULL_MASK, lane < tail);
-    const u64 mykey = make_key(bits, (uint32_t)(nvec * 8 + lane));
-    while (m) {
-      const int src = __ffs(m) - 1;
-      m &= m - 1;
-      const u64 key = shfl_u64(mykey, src);
-      if (key > kth) warp_insert<K>(list, kth, key, lane);
-    }
-  }
-  if (lane < K) s_lists[warp * K + lane] = list;
   __syncthreads();
-  if (warp == 0) {  // merge the 8 warp lists
+  // K-th largest group key: each warp sorts its share (bitonic, 32 at a time)
+  // and keeps its best K; warp 0 merges the 8 lists.  Fewer than K groups (a
+  // tiny segment) leave the bound at 0: every vector is listed.
+  {
+    u64 best = 0ull;  // group keys widened to u64 (unique: group index below)
+    for (int g0 = warp * 32; g0 < ng; g0 += kWarps * 32) {
+      const int g = g0 + lane;
+      const u64 k = g < ng ? (((u64)s_gkey[g] + 1ull) << 32) | (uint32_t)(0xFFFFFFFFu - g) : 0ull;
+      best = warp_merge_topk<K>(best, warp_sort32_desc(k, lane), lane);
+    }
+    if (lane < K) s_lists[warp * K + lane] = best;
+  }
+  __syncthreads();
+  if (warp == 0) {
     u64 acc = lane < K ? s_lists[lane] : 0ull;
-    for (int w = 1; w < kWarps; ++w)
-      acc = warp_merge_topk<K>(acc, lane < K ? s_lists[w * K + lane] : 0ull, lane);
-    if (lane < K) s_top[lane] = acc;
+    for (int w = 1; w < kWarps; ++w) acc = warp_merge_topk<K>(acc, lane < K ? s_lists[w * K + lane] : 0ull, lane);
+    const u64 kth = shfl_u64(acc, K - 1);
+    if (lane == 0) s_tkey = ng >= K && kth ? (uint32_t)(kth >> 32) - 1u : 0u;
   }
   __syncthreads();
+  const uint32_t tkey = s_tkey;
+  // candidate groups (maximum >= bound), in order
+  if (warp == 0) {
+    int base = 0;
+    for (int g0 = 0; g0 < ng; g0 += 32) {
+      const int g = g0 + lane;
+      const bool hit = g < ng && s_gkey[g] >= tkey;
+      const unsigned m = __ballot_sync(DC_FULL_MASK, hit);
+      const int pos = base + __popc(m & ((1u << lane) - 1u));
+      if (hit && pos < kCandGroups) s_cand[pos] = g;
+      base += __popc(m);
+    }
+    if (lane == 0) s_ncand = base;
+  }
+  __syncthreads();
+  const int ncg = s_ncand;
+  // each warp takes candidate groups; lane l checks maxima l and l+32 of each.
+  // A lane holding more hit vectors than its registers take sends the
+  // segment down the degenerate path.
+  int nhit = 0;
+  if (ncg <= kCandGroups) {
+    for (int c = warp; c < ncg; c += kWarps) {
+      const int g = s_cand[c];
+#pragma unroll
+      for (int h = 0; h < kGroup / 32; ++h) {
+        const int e = g * kGroup + h * 32 + lane;
+        nhit += (e < nv && bf16_order_key(s_vmax[e]) >= tkey);
+      }
+    }
+    if (nhit > kMaxHitsPerLane) atomicMax(&s_flag, 1);
+  }
+  __syncthreads();
+  bool fallback = ncg > kCandGroups || s_flag != 0;
+
+  if (!fallback) {
+    // ------------------------------------------------------------ pass 3: select
+    // re-load every hit vector of the warp's groups at once, then keep the
+    // elements >= bound as exact keys
+    nhit = 0;
+    int hj[kMaxHitsPerLane];
+    for (int c = warp; c < ncg; c += kWarps) {
+      const int g = s_cand[c];
+#pragma unroll
+      for (int h = 0; h < kGroup / 32; ++h) {
+        const int e = g * kGroup + h * 32 + lane;
+        if (e < nv && bf16_order_key(s_vmax[e]) >= tkey) {
+#pragma unroll
+          for (int t = 0; t < kMaxHitsPerLane; ++t)  // hj[nhit] with a constant index
+            if (t == nhit) hj[t] = v0 + e;
+          ++nhit;
+        }
+      }
+    }
+    uint4 q[kMaxHitsPerLane];
+#pragma unroll
+    for (int h = 0; h < kMaxHitsPerLane; ++h)
+      if (h < nhit) q[h] = ld_stream_ef(rowp + (int64_t)hj[h] * 8, pol);
+    __syncthreads();  // s_vmax is overwritten by the keys below
+#pragma unroll
+    for (int h = 0; h < kMaxHitsPerLane; ++h) {
+      if (h >= nhit) continue;
+      const uint32_t wd[4] = {q[h].x, q[h].y, q[h].z, q[h].w};
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t bits = (e & 1) ? (wd[e >> 1] >> 16) : (wd[e >> 1] & 0xFFFFu);
+        if (bf16_order_key(bits) >= tkey) {
+          const int pos = atomicAdd(&s_nkeys, 1);
+          if (pos < kCandElems) s_keys[pos] = make_key(bits, (uint32_t)hj[h] * 8u + (uint32_t)e);
+        }
+      }
+    }
+    if (has_tail && tid < tail) {
+      const uint32_t bits = rowp[(int64_t)nvec * 8 + tid];
+      if (bf16_order_key(bits) >= tkey) {
+        const int pos = atomicAdd(&s_nkeys, 1);
+        if (pos < kCandElems) s_keys[pos] = make_key(bits, (uint32_t)(nvec * 8 + tid));
+      }
+    }
+    __syncthreads();
+    const int nkeys = s_nkeys;
+    fallback = nkeys > kCandElems;  // too many elements at the bound: degenerate path
+    if (!fallback) {
+      // exact ranks (keys are unique)
+      for (int e = tid; e < nkeys; e += kThreads) {
+        const u64 x = s_keys[e];
+        int rank = 0;
+        for (int j = 0; j < nkeys; ++j) rank += s_keys[j] > x;
+        if (rank < K) s_top[rank] = x;
+      }
+    }
+    __syncthreads();
+  }
+  if (fallback) {
+    // ------------------------------------------------------------ degenerate segment
+    __syncthreads();  // s_vmax is reused as the candidate buffers below
+    const uint32_t floor_key = tkey;
+    u64 list = stream_fallback<K>(rowp, w0, w1, floor_key, &s_cta_bound,
+                                  s_raw + warp * (kStep * 8), lane, pol);
+    // the scalar tail (V % 8 elements) belongs to the last warp
+    if (has_tail && warp == kWarps - 1) {
+      u64 kth = shfl_u64(list, K - 1);
+      uint32_t bits = 0u;
+      if (lane < tail) bits = rowp[(int64_t)nvec * 8 + lane];
+      unsigned m = __ballot_sync(DC_FULL_MASK, lane < tail);
+      const u64 mykey = make_key(bits, (uint32_t)(nvec * 8 + lane));
+      while (m) {
+        const int src = __ffs(m) - 1;
+        m &= m - 1;
+        const u64 key = shfl_u64(mykey, src);
+        if (key > kth) warp_insert<K>(list, kth, key, lane);
+      }
+    }
+    if (lane < K) s_lists[warp * K + lane] = list;
+    __syncthreads();
+    if (warp == 0) {  // merge the 8 warp lists
+      u64 acc = lane < K ? s_lists[lane] : 0ull;
+      for (int w = 1; w < kWarps; ++w)
+        acc = warp_merge_topk<K>(acc, lane < K ? s_lists[w * K + lane] : 0ull, lane);
+      if (lane < K) s_top[lane] = acc;
+    }
+    __syncthreads();
+  }
 
   if (nseg > 1) {
     u64 *my = part + ((int64_t)row * nseg + seg) * K;
@@ -270,7 +512,6 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
     }
     __syncthreads();
     if (tid == 0) {
-      if (s_top[K - 1]) atomicMax(row_bound + row, s_top[K - 1]);  // for later segments
       const unsigned prev = atomicAdd(&row_count[row], 1u);
       s_flag = (prev == (unsigned)(nseg - 1));
     }
@@ -284,47 +525,57 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
       for (int sg = 1; sg < nseg; ++sg)
         acc = warp_merge_topk<K>(acc, lane < K ? __ldcg(rp + sg * K + lane) : 0ull, lane);
       if (lane < K) s_top[lane] = acc;
-      if (lane == 0) {  // ready for the next call
-        row_count[row] = 0u;
-        row_bound[row] = 0ull;
-      }
+      if (lane == 0) row_count[row] = 0u;  // ready for the next call
     }
     __syncthreads();
   }
   if (tid < K) {
     const u64 x = s_top[tid];
-    out_ids[(int64_t)row * K + tid] = (int32_t)(0xFFFFFFFFu - (uint32_t)(x & 0xFFFFFFFFull));
+    const uint32_t id = 0xFFFFFFFFu - (uint32_t)(x & 0xFFFFFFFFull);
+    out_ids[(int64_t)row * K + tid] = (int32_t)id;
     out_val[(int64_t)row * K + tid] = order_key_to_float((uint32_t)(x >> 32));
+    // start fetching this candidate's embedding row into L2 for the projection
+    if (emb && x != 0ull)
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                       reinterpret_cast<const char *>(emb) + (int64_t)id * emb_row_bytes),
+                   "r"((uint32_t)emb_row_bytes)
+                   : "memory");
   }
 }
 
 }  // namespace
 
 TopkPlan topk_plan(int V, int rows, int slots_per_wave) {
-  const int nvec = V >> 3;
+  const int nvec = std::max(1, V >> 3);
+  const int s_min = (nvec + kMaxSegVecs - 1) / kMaxSegVecs;
+  const int s_max = std::max(s_min, std::min(kTopkMaxChunks, nvec / 2048));
+  // cost of a launch: waves x (vectors per segment + a fixed per-CTA cost
+  // worth ~3000 vectors: the bound, the listing and the selection)
   TopkPlan p;
-  // every warp streams at least two iterations; at most kTopkMaxChunks segments
-  const int max_seg = std::max(1, std::min(kTopkMaxChunks, nvec / (kWarps * 2 * kStep)));
-  p.nchunks = 1;
-  if (rows > 0 && slots_per_wave > 0) {
-    double best = -1.0;
-    for (int s = 1; s <= max_seg; ++s) {
-      const long long total = (long long)rows * s;
-      const long long waves = (total + slots_per_wave - 1) / slots_per_wave;
-      const double eff = (double)total / (double)(waves * slots_per_wave);
-      if (eff > best + 1e-9) {
-        best = eff;
-        p.nchunks = s;
-      }
+  p.nchunks = s_min;
+  double best = -1.0;
+  for (int s = s_min; s <= s_max; ++s) {
+    const long long total = (long long)std::max(rows, 1) * s;
+    const long long waves = (total + std::max(slots_per_wave, 1) - 1) / std::max(slots_per_wave, 1);
+    const double cost = (double)waves * ((nvec + s - 1) / s + 3000);
+    if (best < 0 || cost < best - 1e-9) {
+      best = cost;
+      p.nchunks = s;
     }
   }
-  p.chunk_vecs = (nvec + p.nchunks * kWarps - 1) / (p.nchunks * kWarps);  // vectors per warp
+  p.chunk_vecs = (nvec + p.nchunks - 1) / p.nchunks;  // vectors per segment
   return p;
 }
 
+int topk_min_segments(int V) {
+  const int nvec = std::max(1, V >> 3);
+  return (nvec + kMaxSegVecs - 1) / kMaxSegVecs;
+}
+
 int topk_max_segments(int V) {
-  const int nvec = V >> 3;
-  return std::max(1, std::min(kTopkMaxChunks, nvec / (kWarps * 2 * kStep)));
+  const int nvec = std::max(1, V >> 3);
+  const int s_min = (nvec + kMaxSegVecs - 1) / kMaxSegVecs;
+  return std::max(s_min, std::min(kTopkMaxChunks, nvec / 2048));
 }
 
 template <int K>
@@ -348,22 +599,22 @@ int topk_occupancy(int K) {
 
 cudaError_t launch_topk(int K, const uint16_t *logits, int64_t stride, int slots, int N, int V,
                         const TopkPlan &plan, unsigned long long *part, unsigned *row_count,
-                        unsigned long long *row_bound, int32_t *ids, float *vals, cudaStream_t st) {
+                        int32_t *ids, float *vals, cudaStream_t st, const uint16_t *emb, int d) {
   const int B = slots - 1;
   if (N == 0) return cudaSuccess;
   dim3 grid(N * B, plan.nchunks);
   switch (K) {
     case 8:
       k_topk<8><<<grid, kThreads, 0, st>>>(logits, stride, slots, B, V, plan.nchunks, plan.chunk_vecs,
-                                           part, row_count, row_bound, ids, vals);
+                                           part, row_count, ids, vals, emb, d * 2);
       break;
     case 16:
       k_topk<16><<<grid, kThreads, 0, st>>>(logits, stride, slots, B, V, plan.nchunks, plan.chunk_vecs,
-                                            part, row_count, row_bound, ids, vals);
+                                            part, row_count, ids, vals, emb, d * 2);
       break;
     case 32:
       k_topk<32><<<grid, kThreads, 0, st>>>(logits, stride, slots, B, V, plan.nchunks, plan.chunk_vecs,
-                                            part, row_count, row_bound, ids, vals);
+                                            part, row_count, ids, vals, emb, d * 2);
       break;
     default:
       return cudaErrorInvalidValue;

@@ -7,7 +7,7 @@
 // or code on a latency-critical path where a cudaMalloc (which can
 // synchronise the device) is not acceptable.  dcoco_topk_noalloc runs the
 // same top-K kernel with its scratch -- per-row segment lists, finished-segment
-// counters and published lower bounds -- in the fixed array below, which every
+// counters -- in the fixed array below, which every
 // GPU that loads the library holds until the process exits.
 #include <cuda_runtime.h>
 
@@ -21,8 +21,7 @@ namespace {
 constexpr int kMaxRows = DCOCO_TOPK_NOALLOC_MAX_ROWS;          // batch * (slots - 1)
 constexpr size_t kScratchBytes = (size_t)4 << 20;              // 4 MiB
 constexpr size_t kCountOff = 0;                                // unsigned [kMaxRows]
-constexpr size_t kBoundOff = (size_t)kMaxRows * 4;             // u64 [kMaxRows]
-constexpr size_t kPartOff = kBoundOff + (size_t)kMaxRows * 8;  // u64 segment lists
+constexpr size_t kPartOff = (size_t)kMaxRows * 4;              // u64 segment lists
 constexpr size_t kPartEntries = (kScratchBytes - kPartOff) / 8;
 static_assert(kPartOff % 256 == 0, "aligned sub-arrays");
 
@@ -82,22 +81,20 @@ extern "C" int dcoco_topk_noalloc(int batch, int slots, int vocab, int topk, con
   // as many row segments as the plan wants and the fixed list area holds
   dc::TopkPlan plan = dc::topk_plan(vocab, rows, g_wave[dev][k_index(topk)]);
   const long long fit = (long long)kPartEntries / ((long long)rows * topk);
+  if (fit < dc::topk_min_segments(vocab)) return DCOCO_EBATCH;  // lists would not fit the scratch
   if (plan.nchunks > fit) {
-    plan.nchunks = (int)fit;  // >= 1: kMaxRows * 32 entries always fit
+    plan.nchunks = (int)fit;
     const int nvec = vocab >> 3;
-    plan.chunk_vecs = (nvec + plan.nchunks * 8 - 1) / (plan.nchunks * 8);
+    plan.chunk_vecs = (nvec + plan.nchunks - 1) / plan.nchunks;
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   unsigned *row_count = reinterpret_cast<unsigned *>(base + kCountOff);
-  unsigned long long *row_bound = reinterpret_cast<unsigned long long *>(base + kBoundOff);
   unsigned long long *part = reinterpret_cast<unsigned long long *>(base + kPartOff);
-  // The array keeps the previous call's contents: the counters and bounds
-  // must start at zero.
-  if (cudaMemsetAsync(row_count, 0, (size_t)rows * sizeof(unsigned), st) != cudaSuccess ||
-      cudaMemsetAsync(row_bound, 0, (size_t)rows * sizeof(unsigned long long), st) != cudaSuccess)
+  // The array keeps the previous call's contents: the counters must start
+  // at zero.
+  if (cudaMemsetAsync(row_count, 0, (size_t)rows * sizeof(unsigned), st) != cudaSuccess)
     return DCOCO_ECUDA;
   const cudaError_t e = dc::launch_topk(topk, static_cast<const uint16_t *>(logits), logits_slot_stride,
-                                        slots, batch, vocab, plan, part, row_count, row_bound, topk_ids,
-                                        topk_val, st);
+                                        slots, batch, vocab, plan, part, row_count, topk_ids, topk_val, st);
   return e == cudaSuccess ? DCOCO_OK : DCOCO_ECUDA;
 }
