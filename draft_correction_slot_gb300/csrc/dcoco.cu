@@ -84,6 +84,10 @@ struct dcoco_weights {
   uint16_t *slot_hi = nullptr, *slot_lo = nullptr;  // [W_ctx ; W_pair[:, :d] ; W_pair[:, d:]] [3r][d]
                                                     // (variant 1: W_io[:, d:], [2r][d])
   CUtensorMap map_cand_hi, map_cand_lo, map_slot_hi, map_slot_lo;  // TMA maps of the halves
+  // candidate-side maps of the MLP, bf16 hi / lo: W_fuse[:, :r] [r][r] and
+  // [W1[:, r:2r] ; W1[:, 2r:3r]] [2H][r]
+  uint16_t *fb_hi = nullptr, *fb_lo = nullptr, *w1ab_hi = nullptr, *w1ab_lo = nullptr;
+  dc::CandMlpMaps cand_maps;
   dc::MlpWeightsDev mlp{};
 };
 
@@ -246,8 +250,8 @@ int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs 
     DC_TRY(clk.done(dc::launch_proj_tc(0, E, w->map_cand_hi, w->map_cand_lo, ids, cfg.slots, B,
                                        cands, d, V, kR, h->splits_cand, ws.cand_proj, ws.cand_part,
                                        ws.cand_tiles, ws.err, st)));
-    DC_TRY(clk.done(dc::launch_cand_post(K, ws.cand_proj, vals, ws.Gf, N, B, cfg.ln_eps, w->mlp,
-                                         ws.U, ws.V, st)));
+    DC_TRY(clk.done(dc::launch_cand_mlp_tc(w->cand_maps, ws.cand_proj, ws.Gf, vals, w->mlp, K, cands,
+                                           cfg.ln_eps, ws.U, ws.V, ws.err, st)));
     // step 4: all (B-1) K^2 transition scores
     DC_TRY(clk.done(dc::launch_pair_score(K, ws.U, ws.V, ws.P, vals, w->mlp.w2, w->mlp.b2, N, B,
                                           scores, st)));
@@ -433,6 +437,28 @@ int dcoco_weights_create(dcoco_handle *h, const dcoco_weight_ptrs *wp, void *str
       split_row(w_io.data() + (size_t)o * 2 * d + d, s_hi + (size_t)o * d, s_lo + (size_t)o * d);
     }
   }
+  // Candidate-side MLP maps (variant 0), split the same way.
+  const size_t n_fb = (size_t)kR * kR, n_w1ab = (size_t)2 * kH * kR;
+  std::vector<uint16_t> cmlp;
+  if (cfg.variant == 0) {
+    cmlp.resize(2 * (n_fb + n_w1ab));
+    uint16_t *fbh = cmlp.data(), *fbl = fbh + n_fb, *w1h = fbl + n_fb, *w1l = w1h + n_w1ab;
+    auto split_vec = [&](const float *src, uint16_t *hi, uint16_t *lo) {
+      for (int k = 0; k < kR; ++k) {
+        const uint16_t hb = f32_to_bf16(src[k]);
+        hi[k] = hb;
+        lo[k] = f32_to_bf16(src[k] - bf16_to_f32(hb));
+      }
+    };
+    for (int o = 0; o < kR; ++o)
+      split_vec(w_fuse.data() + (size_t)o * 2 * kR, fbh + (size_t)o * kR, fbl + (size_t)o * kR);
+    const size_t in1 = 3 * kR + 2;
+    for (int j = 0; j < kH; ++j) {
+      split_vec(w1.data() + j * in1 + kR, w1h + (size_t)j * kR, w1l + (size_t)j * kR);
+      split_vec(w1.data() + j * in1 + 2 * kR, w1h + (size_t)(kH + j) * kR, w1l + (size_t)(kH + j) * kR);
+    }
+    proj.insert(proj.end(), cmlp.begin(), cmlp.end());
+  }
   const size_t n_proj = proj.size();
   std::vector<float> mlp;
   size_t off[16] = {};
@@ -472,10 +498,21 @@ int dcoco_weights_create(dcoco_handle *h, const dcoco_weight_ptrs *wp, void *str
   w->cand_lo = dproj + (size_t)cand_rows * d;
   w->slot_hi = w->cand_lo + (size_t)cand_rows * d;
   w->slot_lo = w->slot_hi + (size_t)slot_rows * d;
+  if (cfg.variant == 0) {
+    w->fb_hi = w->slot_lo + (size_t)slot_rows * d;
+    w->fb_lo = w->fb_hi + n_fb;
+    w->w1ab_hi = w->fb_lo + n_fb;
+    w->w1ab_lo = w->w1ab_hi + n_w1ab;
+  }
   if (!dc::encode_bf16_rows_map(&w->map_cand_hi, w->cand_hi, cand_rows, d, 128) ||
       !dc::encode_bf16_rows_map(&w->map_cand_lo, w->cand_lo, cand_rows, d, 128) ||
       !dc::encode_bf16_rows_map(&w->map_slot_hi, w->slot_hi, slot_rows, d, 128) ||
-      !dc::encode_bf16_rows_map(&w->map_slot_lo, w->slot_lo, slot_rows, d, 128)) {
+      !dc::encode_bf16_rows_map(&w->map_slot_lo, w->slot_lo, slot_rows, d, 128) ||
+      (cfg.variant == 0 &&
+       (!dc::encode_bf16_rows_map(&w->cand_maps.fb_hi, w->fb_hi, kR, kR, 128) ||
+        !dc::encode_bf16_rows_map(&w->cand_maps.fb_lo, w->fb_lo, kR, kR, 128) ||
+        !dc::encode_bf16_rows_map(&w->cand_maps.w1_hi, w->w1ab_hi, 2 * kH, kR, 128) ||
+        !dc::encode_bf16_rows_map(&w->cand_maps.w1_lo, w->w1ab_lo, 2 * kH, kR, 128)))) {
     cudaFree(w->block);
     delete w;
     return DCOCO_ECUDA;

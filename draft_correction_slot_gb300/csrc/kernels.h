@@ -84,6 +84,17 @@ cudaError_t launch_cand_post(int K, const float *cand_proj, const float *topk_va
                              int N, int B, float eps, const MlpWeightsDev &w, float *U, float *V,
                              cudaStream_t st);
 
+// Tensor-core form of the same per-candidate step.  The maps address bf16
+// hi / lo halves (box 64 x 128, 128B swizzle) of W_fuse[:, :r] ([r][r]) and of
+// [W1[:, r:2r] ; W1[:, 2r:3r]] ([2H][r]).  M = N * B * K candidates;
+// candidate m belongs to draft slot m / K.
+struct CandMlpMaps {
+  CUtensorMap fb_hi, fb_lo, w1_hi, w1_lo;
+};
+cudaError_t launch_cand_mlp_tc(const CandMlpMaps &maps, const float *cand_proj, const float *Gf,
+                               const float *topk_val, const MlpWeightsDev &w, int K, int M, float eps,
+                               float *U, float *V, int *err, cudaStream_t st);
+
 // S[n,p,a,b] = l_{p+1}(b) + b2 + sum_j w2_j GELU(P_pj + U_{p,a,j} + V_{p+1,b,j}).
 cudaError_t launch_pair_score(int K, const float *U, const float *V, const float *P,
                               const float *topk_val, const float *w2, const float *b2, int N, int B,
