@@ -68,6 +68,12 @@ struct dcoco_handle {
   int splits_cand = 1;        // results do not depend on the batch size)
   void *block = nullptr;  // one device allocation holding the workspace
   Workspace ws;
+  // The slot path (slot projections, per-slot maps) depends only on the hidden
+  // states: it runs on `side`, forked from and joined back into the caller's
+  // stream by the two events, while the top-K streams the logits.
+  cudaStream_t side = nullptr;
+  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+  dc::CandIoMaps cand_io;  // TMA maps of cand_proj, U, V (variant 0)
   cudaStream_t last_stream = nullptr;
   long long launches = 0;            // kernels launched so far
   bool timing = false;               // record per-stage events
@@ -84,10 +90,11 @@ struct dcoco_weights {
   uint16_t *slot_hi = nullptr, *slot_lo = nullptr;  // [W_ctx ; W_pair[:, :d] ; W_pair[:, d:]] [3r][d]
                                                     // (variant 1: W_io[:, d:], [2r][d])
   CUtensorMap map_cand_hi, map_cand_lo, map_slot_hi, map_slot_lo;  // TMA maps of the halves
-  // candidate-side maps of the MLP, bf16 hi / lo: W_fuse[:, :r] [r][r] and
-  // [W1[:, r:2r] ; W1[:, 2r:3r]] [2H][r]
-  uint16_t *fb_hi = nullptr, *fb_lo = nullptr, *w1ab_hi = nullptr, *w1ab_lo = nullptr;
-  dc::CandMlpMaps cand_maps;
+  // the 128-deep maps of the MLP as bf16 hi / lo (variant 0): W_fuse[:, :r],
+  // W_fuse[:, r:] ([r][r]), [W1[:, r:2r] ; W1[:, 2r:3r]] ([2H][r]), W1[:, :r] ([H][r])
+  uint16_t *fb_hi = nullptr, *fb_lo = nullptr, *fg_hi = nullptr, *fg_lo = nullptr;
+  uint16_t *w1ab_hi = nullptr, *w1ab_lo = nullptr, *w1s_hi = nullptr, *w1s_lo = nullptr;
+  dc::MlpMaps mlp_maps;
   dc::MlpWeightsDev mlp{};
 };
 
@@ -235,23 +242,36 @@ int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs 
   h->last_stream = st;
   StageClock clk(h, st);
 
-  // step 1: candidate pools
+  const int rows = N * B, cands = rows * K;
   const dc::TopkPlan plan = dc::topk_plan(V, N * B, h->topk_wave);
+  // Per-stage timing serialises the stages on `st`; otherwise the slot path
+  // runs on the side stream.  The top-K is launched first so that its CTAs
+  // are dispatched first and the slot kernels fill the SMs its last wave frees.
+  const bool overlap = clk.ev == nullptr && cfg.variant == 0;
+  if (overlap) DC_TRY(cudaEventRecord(h->ev_fork, st));
+  // step 1: candidate pools
   DC_TRY(clk.done(dc::launch_topk(K, logits, in->logits_slot_stride, cfg.slots, N, V, plan,
                                   ws.part, ws.row_count, ids, vals, st, E, d)));
-  const int rows = N * B, cands = rows * K;
   if (cfg.variant == 0) {
     // steps 2-3: slot projections (W_ctx, W_pair halves) and per-slot / per-pair terms
+    cudaStream_t ss = st;
+    if (overlap) {
+      DC_TRY(cudaStreamWaitEvent(h->side, h->ev_fork, 0));
+      ss = h->side;
+    }
     DC_TRY(clk.done(dc::launch_proj_tc(1, hidden, w->map_slot_hi, w->map_slot_lo, nullptr, cfg.slots, B,
                                        rows, d, V, 3 * kR, h->splits_slot, ws.slot_proj, ws.slot_part,
-                                       ws.slot_tiles, ws.err, st)));
-    DC_TRY(clk.done(dc::launch_slot_post(ws.slot_proj, N, B, cfg.ln_eps, w->mlp, ws.Gf, ws.P, st)));
+                                       ws.slot_tiles, ws.err, ss)));
+    DC_TRY(clk.done(dc::launch_slot_mlp_tc(w->mlp_maps, ws.slot_proj, w->mlp, N, B, cfg.ln_eps, ws.Gf, ws.P,
+                                           ws.err, ss)));
+    if (overlap) DC_TRY(cudaEventRecord(h->ev_join, h->side));
     // step 2: candidate projections, then z and the layer-1 partials U, V
     DC_TRY(clk.done(dc::launch_proj_tc(0, E, w->map_cand_hi, w->map_cand_lo, ids, cfg.slots, B,
                                        cands, d, V, kR, h->splits_cand, ws.cand_proj, ws.cand_part,
                                        ws.cand_tiles, ws.err, st)));
-    DC_TRY(clk.done(dc::launch_cand_mlp_tc(w->cand_maps, ws.cand_proj, ws.Gf, vals, w->mlp, K, cands,
-                                           cfg.ln_eps, ws.U, ws.V, ws.err, st)));
+    if (overlap) DC_TRY(cudaStreamWaitEvent(st, h->ev_join, 0));
+    DC_TRY(clk.done(dc::launch_cand_mlp_tc(w->mlp_maps, h->cand_io, ws.Gf, vals, w->mlp, K, cands,
+                                           cfg.ln_eps, ws.err, st)));
     // step 4: all (B-1) K^2 transition scores
     DC_TRY(clk.done(dc::launch_pair_score(K, ws.U, ws.V, ws.P, vals, w->mlp.w2, w->mlp.b2, N, B,
                                           scores, st)));
@@ -363,7 +383,19 @@ int dcoco_create(const dcoco_config *cfg, dcoco_handle **out) {
   Carver c;
   c.base = static_cast<char *>(h->block);
   carve_workspace(c, h->cfg, h->B, h->topk_segments_max, h->splits_slot, h->splits_cand, h->ws);
-  if (cudaMemset(h->block, 0, bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
+  const int cands_cap = cfg->max_batch * h->B * cfg->topk;
+  const bool maps_ok =
+      cfg->variant != 0 ||
+      (dc::encode_f32_rows_map(&h->cand_io.cp, h->ws.cand_proj, cands_cap, kR, 128) &&
+       dc::encode_f32_rows_map(&h->cand_io.u, h->ws.U, cands_cap, kH, 128) &&
+       dc::encode_f32_rows_map(&h->cand_io.v, h->ws.V, cands_cap, kH, 128));
+  if (!maps_ok || cudaMemset(h->block, 0, bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess ||
+      cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    if (h->ev_fork) cudaEventDestroy(h->ev_fork);
+    if (h->side) cudaStreamDestroy(h->side);
     cudaFree(h->block);
     delete h;
     return DCOCO_ECUDA;
@@ -437,12 +469,13 @@ int dcoco_weights_create(dcoco_handle *h, const dcoco_weight_ptrs *wp, void *str
       split_row(w_io.data() + (size_t)o * 2 * d + d, s_hi + (size_t)o * d, s_lo + (size_t)o * d);
     }
   }
-  // Candidate-side MLP maps (variant 0), split the same way.
-  const size_t n_fb = (size_t)kR * kR, n_w1ab = (size_t)2 * kH * kR;
-  std::vector<uint16_t> cmlp;
+  // The 128-deep MLP maps (variant 0), split the same way, in the order
+  // fb, fg, w1ab, w1s, each as hi then lo.
+  const size_t n_rr = (size_t)kR * kR, n_w1ab = (size_t)2 * kH * kR, n_w1s = (size_t)kH * kR;
   if (cfg.variant == 0) {
-    cmlp.resize(2 * (n_fb + n_w1ab));
-    uint16_t *fbh = cmlp.data(), *fbl = fbh + n_fb, *w1h = fbl + n_fb, *w1l = w1h + n_w1ab;
+    std::vector<uint16_t> cm(2 * (2 * n_rr + n_w1ab + n_w1s));
+    uint16_t *fbh = cm.data(), *fbl = fbh + n_rr, *fgh = fbl + n_rr, *fgl = fgh + n_rr;
+    uint16_t *w1h = fgl + n_rr, *w1l = w1h + n_w1ab, *wsh = w1l + n_w1ab, *wsl = wsh + n_w1s;
     auto split_vec = [&](const float *src, uint16_t *hi, uint16_t *lo) {
       for (int k = 0; k < kR; ++k) {
         const uint16_t hb = f32_to_bf16(src[k]);
@@ -450,14 +483,17 @@ int dcoco_weights_create(dcoco_handle *h, const dcoco_weight_ptrs *wp, void *str
         lo[k] = f32_to_bf16(src[k] - bf16_to_f32(hb));
       }
     };
-    for (int o = 0; o < kR; ++o)
+    for (int o = 0; o < kR; ++o) {
       split_vec(w_fuse.data() + (size_t)o * 2 * kR, fbh + (size_t)o * kR, fbl + (size_t)o * kR);
+      split_vec(w_fuse.data() + (size_t)o * 2 * kR + kR, fgh + (size_t)o * kR, fgl + (size_t)o * kR);
+    }
     const size_t in1 = 3 * kR + 2;
     for (int j = 0; j < kH; ++j) {
       split_vec(w1.data() + j * in1 + kR, w1h + (size_t)j * kR, w1l + (size_t)j * kR);
       split_vec(w1.data() + j * in1 + 2 * kR, w1h + (size_t)(kH + j) * kR, w1l + (size_t)(kH + j) * kR);
+      split_vec(w1.data() + j * in1, wsh + (size_t)j * kR, wsl + (size_t)j * kR);
     }
-    proj.insert(proj.end(), cmlp.begin(), cmlp.end());
+    proj.insert(proj.end(), cm.begin(), cm.end());
   }
   const size_t n_proj = proj.size();
   std::vector<float> mlp;
@@ -500,19 +536,27 @@ int dcoco_weights_create(dcoco_handle *h, const dcoco_weight_ptrs *wp, void *str
   w->slot_lo = w->slot_hi + (size_t)slot_rows * d;
   if (cfg.variant == 0) {
     w->fb_hi = w->slot_lo + (size_t)slot_rows * d;
-    w->fb_lo = w->fb_hi + n_fb;
-    w->w1ab_hi = w->fb_lo + n_fb;
+    w->fb_lo = w->fb_hi + n_rr;
+    w->fg_hi = w->fb_lo + n_rr;
+    w->fg_lo = w->fg_hi + n_rr;
+    w->w1ab_hi = w->fg_lo + n_rr;
     w->w1ab_lo = w->w1ab_hi + n_w1ab;
+    w->w1s_hi = w->w1ab_lo + n_w1ab;
+    w->w1s_lo = w->w1s_hi + n_w1s;
   }
   if (!dc::encode_bf16_rows_map(&w->map_cand_hi, w->cand_hi, cand_rows, d, 128) ||
       !dc::encode_bf16_rows_map(&w->map_cand_lo, w->cand_lo, cand_rows, d, 128) ||
       !dc::encode_bf16_rows_map(&w->map_slot_hi, w->slot_hi, slot_rows, d, 128) ||
       !dc::encode_bf16_rows_map(&w->map_slot_lo, w->slot_lo, slot_rows, d, 128) ||
       (cfg.variant == 0 &&
-       (!dc::encode_bf16_rows_map(&w->cand_maps.fb_hi, w->fb_hi, kR, kR, 128) ||
-        !dc::encode_bf16_rows_map(&w->cand_maps.fb_lo, w->fb_lo, kR, kR, 128) ||
-        !dc::encode_bf16_rows_map(&w->cand_maps.w1_hi, w->w1ab_hi, 2 * kH, kR, 128) ||
-        !dc::encode_bf16_rows_map(&w->cand_maps.w1_lo, w->w1ab_lo, 2 * kH, kR, 128)))) {
+       (!dc::encode_bf16_rows_map(&w->mlp_maps.fb_hi, w->fb_hi, kR, kR, 128) ||
+        !dc::encode_bf16_rows_map(&w->mlp_maps.fb_lo, w->fb_lo, kR, kR, 128) ||
+        !dc::encode_bf16_rows_map(&w->mlp_maps.fg_hi, w->fg_hi, kR, kR, 128) ||
+        !dc::encode_bf16_rows_map(&w->mlp_maps.fg_lo, w->fg_lo, kR, kR, 128) ||
+        !dc::encode_bf16_rows_map(&w->mlp_maps.w1_hi, w->w1ab_hi, 2 * kH, kR, 128) ||
+        !dc::encode_bf16_rows_map(&w->mlp_maps.w1_lo, w->w1ab_lo, 2 * kH, kR, 128) ||
+        !dc::encode_bf16_rows_map(&w->mlp_maps.w1s_hi, w->w1s_hi, kH, kR, 128) ||
+        !dc::encode_bf16_rows_map(&w->mlp_maps.w1s_lo, w->w1s_lo, kH, kR, 128)))) {
     cudaFree(w->block);
     delete w;
     return DCOCO_ECUDA;
@@ -628,6 +672,9 @@ void dcoco_destroy(dcoco_handle *h) {
   if (!h) return;
   cudaDeviceSynchronize();
   for (cudaEvent_t e : h->events) cudaEventDestroy(e);
+  cudaEventDestroy(h->ev_join);
+  cudaEventDestroy(h->ev_fork);
+  cudaStreamDestroy(h->side);
   cudaFree(h->block);
   delete h;
 }

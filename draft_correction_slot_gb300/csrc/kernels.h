@@ -51,6 +51,9 @@ size_t proj_tc_smem_bytes();
 int proj_tc_splits(int d, int requested);
 // 2D bf16 [rows][d] tensor map, 128B swizzle, box 64 x box_rows.
 bool encode_bf16_rows_map(CUtensorMap *map, const void *base, int rows, int d, int box_rows);
+// 2D fp32 [rows][cols] tensor map, 128B swizzle, box 32 x box_rows
+// (cols % 32 == 0).
+bool encode_f32_rows_map(CUtensorMap *map, const void *base, int rows, int cols, int box_rows);
 cudaError_t launch_proj_tc(int mode, const uint16_t *table, const CUtensorMap &map_hi,
                            const CUtensorMap &map_lo, const int32_t *ids, int slots, int B, int M, int d,
                            int V, int No, int splits, float *C, float *part, unsigned *tile_count,
@@ -84,16 +87,28 @@ cudaError_t launch_cand_post(int K, const float *cand_proj, const float *topk_va
                              int N, int B, float eps, const MlpWeightsDev &w, float *U, float *V,
                              cudaStream_t st);
 
-// Tensor-core form of the same per-candidate step.  The maps address bf16
-// hi / lo halves (box 64 x 128, 128B swizzle) of W_fuse[:, :r] ([r][r]) and of
-// [W1[:, r:2r] ; W1[:, 2r:3r]] ([2H][r]).  M = N * B * K candidates;
-// candidate m belongs to draft slot m / K.
-struct CandMlpMaps {
-  CUtensorMap fb_hi, fb_lo, w1_hi, w1_lo;
+// Tensor-core forms of the per-slot and per-candidate steps.  The maps
+// address bf16 hi / lo halves (box 64 x 128, 128B swizzle) of W_fuse[:, :r]
+// and W_fuse[:, r:] ([r][r] each), [W1[:, r:2r] ; W1[:, 2r:3r]] ([2H][r]) and
+// W1[:, :r] ([H][r]).
+struct MlpMaps {
+  CUtensorMap fb_hi, fb_lo, w1_hi, w1_lo, fg_hi, fg_lo, w1s_hi, w1s_lo;
 };
-cudaError_t launch_cand_mlp_tc(const CandMlpMaps &maps, const float *cand_proj, const float *Gf,
+// Same outputs as launch_slot_post.
+cudaError_t launch_slot_mlp_tc(const MlpMaps &maps, const float *slot_proj, const MlpWeightsDev &w, int N,
+                               int B, float eps, float *Gf, float *P, int *err, cudaStream_t st);
+// Same outputs as launch_cand_post; M = N * B * K candidates, candidate m
+// belongs to draft slot m / K.  The candidate tiles move by TMA: `io.cp`
+// reads cand_proj ([rows][r] fp32), `io.u` / `io.v` write U and V ([rows][H]
+// fp32); all three are fp32 maps with box 32 x 128 over the same row count
+// (>= M).  Rows of the last tile past M that lie inside the maps receive
+// the outputs of an all-zero input row.
+struct CandIoMaps {
+  CUtensorMap cp, u, v;
+};
+cudaError_t launch_cand_mlp_tc(const MlpMaps &maps, const CandIoMaps &io, const float *Gf,
                                const float *topk_val, const MlpWeightsDev &w, int K, int M, float eps,
-                               float *U, float *V, int *err, cudaStream_t st);
+                               int *err, cudaStream_t st);
 
 // S[n,p,a,b] = l_{p+1}(b) + b2 + sum_j w2_j GELU(P_pj + U_{p,a,j} + V_{p+1,b,j}).
 cudaError_t launch_pair_score(int K, const float *U, const float *V, const float *P,

@@ -1,0 +1,503 @@
+// mlp_tc.cu -- the 128-deep maps of the representation and transition steps
+// on the tensor cores: per draft slot, the context half of the fuse map and
+// the pair part of layer 1; per candidate, the LayerNorms, the fuse map and
+// the candidate parts of layer 1.
+//
+// DCOCO page ("Contextual Correction of Parallel Drafts for Speculative
+// Decoding"), Method step details (2)-(4):
+//   g_i = LN(W_ctx h_i),  b = LN(W_cand E[c])          (non-affine)
+//   z = gamma * LN(W_fuse[:, :r] b + W_fuse[:, r:] g_i) + beta
+//   s_p = W_pair [h_p; h_{p+1}]
+// and layer 1 of the transition MLP, which is linear in its concatenated
+// input [s_p; z^a; z^b; l(a); l(b)], split by input block:
+//   P_p = W1[:, :r] s_p + b1                        (per slot pair)
+//   U = W1[:, r:2r] z + W1[:, 3r] l(c),  V = W1[:, 2r:3r] z + W1[:, 3r+1] l(c)
+// (U feeds the candidate's transitions as predecessor, V as successor.)
+//
+// Every map here is a dense 128-deep contraction over 128-row tiles: A (the
+// LayerNormed or summed rows) is split in registers into bf16 hi + lo and
+// stored 128B-swizzled, the weights come pre-split through TMA, and three MMA
+// passes (hi.hi + hi.lo + lo.hi) accumulate in fp32 tensor memory, which
+// keeps fp32-level accuracy.  Sixteen row warps hold the tile: row r (a
+// tensor-memory lane) is shared by four threads, one per 32-column quarter,
+// which meet in shared memory for the LayerNorm sums; one thread of warp 16
+// issues the TMA copies and MMAs.  Every wait is bounded in time
+// (kErrTimeout in the status word).
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace dc {
+namespace {
+
+using namespace tc;
+
+constexpr int kR = 128, kH = 256;
+constexpr int kRows = 128;                 // tile rows (MMA M)
+constexpr int kKBlk = 128 * 64 * 2;        // 128 rows x 64 k of bf16: 16 KB
+constexpr int kMat = 2 * kKBlk;            // 128 rows x 128 k: 32 KB
+// shared memory: A (hi, lo) | W0 (hi, lo) | ...
+constexpr int kOffA = 0, kOffW0 = 2 * kMat;
+constexpr int kRowWarps = 16;
+constexpr int kRowThreads = kRowWarps * 32;  // 4 threads per tile row
+constexpr int kThreads = kRowThreads + 32;   // + the control warp
+constexpr int kQ = 32;                       // columns per row thread
+constexpr uint32_t kIdesc = idesc_bf16(128, 128);
+constexpr uint32_t kWTx = 2 * kMat;          // one matrix pair (hi + lo): 64 KB
+
+__device__ __forceinline__ uint32_t bf16_rn_bits(float f) {
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// Barrier over the row threads only (the control warp keeps issuing).
+__device__ __forceinline__ void rows_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kRowThreads) : "memory");
+}
+// The same barrier, returning whether `v` holds in every row thread.
+__device__ __forceinline__ bool rows_all(bool v) {
+  uint32_t out;
+  asm volatile(
+      "{\n.reg .pred p, q;\n"
+      "setp.ne.u32 q, %1, 0;\n"
+      "bar.red.and.pred p, 1, %2, q;\n"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(out)
+      : "r"((uint32_t)v), "n"(kRowThreads)
+      : "memory");
+  return out != 0;
+}
+
+// Row r's columns [32 q, 32 q + 32) as bf16 hi and lo into the 128B-swizzled
+// K-major A tiles (two 64-wide k-blocks each).
+__device__ __forceinline__ void store_split_part(uint8_t *a_hi, uint8_t *a_lo, int r, int q,
+                                                 const float (&x)[kQ]) {
+  const int kb = q >> 1;
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    const int c = (q & 1) * 4 + cc;  // 16-byte chunk within the 128-byte row
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      const float v0 = x[cc * 8 + 2 * p], v1 = x[cc * 8 + 2 * p + 1];
+      const uint32_t h0 = bf16_rn_bits(v0), h1 = bf16_rn_bits(v1);
+      const uint32_t l0 = bf16_rn_bits(v0 - __uint_as_float(h0 << 16));
+      const uint32_t l1 = bf16_rn_bits(v1 - __uint_as_float(h1 << 16));
+      hw[p] = h0 | (h1 << 16);
+      lw[p] = l0 | (l1 << 16);
+    }
+    const int off = kb * kKBlk + (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) * 16);
+    *reinterpret_cast<uint4 *>(a_hi + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4 *>(a_lo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  }
+}
+
+// Sum over a row's four quarter-threads, in quarter order (the same value in
+// all four).  `red` is [4][kRows] shared floats.
+__device__ __forceinline__ float row_sum(float v, float *red, int r, int q) {
+  red[q * kRows + r] = v;
+  rows_sync();
+  return (red[r] + red[kRows + r]) + (red[2 * kRows + r] + red[3 * kRows + r]);
+}
+
+__device__ __forceinline__ float sum32(const float (&x)[kQ]) {
+  float a0 = x[0], a1 = x[1], a2 = x[2], a3 = x[3];
+#pragma unroll
+  for (int k = 4; k < kQ; k += 4) {
+    a0 += x[k];
+    a1 += x[k + 1];
+    a2 += x[k + 2];
+    a3 += x[k + 3];
+  }
+  return (a0 + a1) + (a2 + a3);
+}
+
+// Non-affine LayerNorm of a 128-wide row held as four 32-column quarters:
+// population variance, eps inside the square root.  Every row thread calls
+// it (it holds two row barriers); red0 / red1 are two distinct [4][kRows]
+// buffers.
+__device__ __forceinline__ void ln0_part(float (&x)[kQ], float eps, float *red0, float *red1, int r, int q) {
+  const float mean = row_sum(sum32(x), red0, r, q) * (1.0f / kR);
+  float sq[kQ];
+#pragma unroll
+  for (int k = 0; k < kQ; ++k) {
+    x[k] -= mean;
+    sq[k] = x[k] * x[k];
+  }
+  const float var = row_sum(sum32(sq), red1, r, q) * (1.0f / kR);
+  const float inv = rsqrtf(var + eps);
+#pragma unroll
+  for (int k = 0; k < kQ; ++k) x[k] *= inv;
+}
+
+__device__ __forceinline__ void load32(float (&x)[kQ], const float *src) {
+  const float4 *s4 = reinterpret_cast<const float4 *>(src);
+#pragma unroll
+  for (int i = 0; i < kQ / 4; ++i) {
+    const float4 v = __ldg(s4 + i);
+    x[4 * i] = v.x; x[4 * i + 1] = v.y; x[4 * i + 2] = v.z; x[4 * i + 3] = v.w;
+  }
+}
+
+// 3-pass split product of one 128-deep contraction into tensor memory at `tmem`.
+__device__ __forceinline__ void mma_split(uint32_t tmem, uint32_t a_hi, uint32_t a_lo, uint32_t w_hi,
+                                          uint32_t w_lo) {
+#pragma unroll
+  for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t o = kb * kKBlk + k * 32;
+      const uint64_t ah = sw128_desc(a_hi + o), al = sw128_desc(a_lo + o);
+      mma_bf16(tmem, ah, sw128_desc(w_hi + o), kIdesc, (kb | k) ? 1u : 0u);
+      mma_bf16(tmem, ah, sw128_desc(w_lo + o), kIdesc, 1u);
+      mma_bf16(tmem, al, sw128_desc(w_hi + o), kIdesc, 1u);
+    }
+}
+
+__device__ __forceinline__ void load_pair(uint32_t w_hi, uint32_t w_lo, const CUtensorMap *mh,
+                                          const CUtensorMap *ml, int row, uint32_t bar) {
+  mbar_arrive_expect_tx(bar, kWTx);
+  for (int kb = 0; kb < 2; ++kb) {
+    tma_load_2d(w_hi + kb * kKBlk, mh, kb * 64, row, bar);
+    tma_load_2d(w_lo + kb * kKBlk, ml, kb * 64, row, bar);
+  }
+}
+
+// ---------------------------------------------------------------- per draft slot
+// One CTA per (128-slot tile, output chunk): chunk 0 writes Gf = W_fuse[:, r:] g
+// for every slot; chunks 1 and 2 write the two 128-wide halves of P_p for the
+// slots that start a pair (i < B-1).  slot_proj rows are
+// (W_ctx h | W_pair[:, :d] h | W_pair[:, d:] h).
+constexpr int kSlotSmemBytes = 4 * kMat + 1024;
+
+__global__ void __launch_bounds__(kThreads, 1)
+k_slot_mlp_tc(const __grid_constant__ CUtensorMap map_fg_hi, const __grid_constant__ CUtensorMap map_fg_lo,
+              const __grid_constant__ CUtensorMap map_w1s_hi, const __grid_constant__ CUtensorMap map_w1s_lo,
+              const float *__restrict__ slot_proj, const float *__restrict__ b1, int NB, int B, float eps,
+              float *__restrict__ Gf, float *__restrict__ P, int *err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  __shared__ __align__(8) unsigned long long bar_w, bar_a, bar_mma;
+  __shared__ float s_red[2][4 * kRows];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int chunk = blockIdx.x, m0 = blockIdx.y * kRows;
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t a_hi = sb + kOffA, a_lo = sb + kOffA + kMat;
+  const uint32_t w_hi = sb + kOffW0, w_lo = sb + kOffW0 + kMat;
+
+  if (tid == 0) {
+    mbar_init(smem_u32(&bar_w), 1);
+    mbar_init(smem_u32(&bar_a), kRowThreads);
+    mbar_init(smem_u32(&bar_mma), 1);
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kRowWarps) tmem_alloc(smem_u32(&s_tmem), 128);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  if (warp == kRowWarps) {
+    if (lane == 0) {
+      if (chunk == 0)
+        load_pair(w_hi, w_lo, &map_fg_hi, &map_fg_lo, 0, smem_u32(&bar_w));
+      else
+        load_pair(w_hi, w_lo, &map_w1s_hi, &map_w1s_lo, (chunk - 1) * 128, smem_u32(&bar_w));
+      if (mbar_wait(smem_u32(&bar_w), 0, &s_abort, err) && mbar_wait(smem_u32(&bar_a), 0, &s_abort, err)) {
+        tc_fence_after();
+        mma_split(tmem, a_hi, a_lo, w_hi, w_lo);
+      }
+      mma_commit(smem_u32(&bar_mma));
+    }
+    __syncwarp();
+  } else {
+    const int qd = warp & 3, q = warp >> 2;  // lane quadrant, column quarter
+    const int r = qd * 32 + lane;           // tile row = tensor-memory lane
+    const int gs = m0 + r;                  // flattened draft slot n * B + i
+    const int i = gs % B;
+    const bool live = gs < NB && (chunk == 0 || i < B - 1);
+    float x[kQ];
+#pragma unroll
+    for (int k = 0; k < kQ; ++k) x[k] = 0.f;
+    if (chunk == 0) {
+      if (live) load32(x, slot_proj + (int64_t)gs * 3 * kR + q * kQ);
+      ln0_part(x, eps, s_red[0], s_red[1], r, q);
+    } else if (live) {
+      // s_p = W_pair[:, :d] h_p + W_pair[:, d:] h_{p+1}
+      float y[kQ];
+      load32(x, slot_proj + (int64_t)gs * 3 * kR + kR + q * kQ);
+      load32(y, slot_proj + (int64_t)(gs + 1) * 3 * kR + 2 * kR + q * kQ);
+#pragma unroll
+      for (int k = 0; k < kQ; ++k) x[k] += y[k];
+    }
+    store_split_part(smem + kOffA, smem + kOffA + kMat, r, q, x);
+    fence_proxy_async();
+    mbar_arrive(smem_u32(&bar_a));
+
+    bool ok = mbar_wait(smem_u32(&bar_mma), 0, &s_abort, err) && !s_abort;
+    ok = __all_sync(DC_FULL_MASK, ok);
+    tc_fence_after();
+    if (ok) {
+      float v[kQ];
+      tmem_ld32(tmem + ((uint32_t)(qd * 32) << 16) + q * kQ, v);
+      if (live) {
+        float *dst;
+        if (chunk == 0) {
+          dst = Gf + (int64_t)gs * kR + q * kQ;
+        } else {
+          const int n = gs / B;
+          dst = P + ((int64_t)n * (B - 1) + i) * kH + (chunk - 1) * 128 + q * kQ;
+          float bb[kQ];
+          load32(bb, b1 + (chunk - 1) * 128 + q * kQ);
+#pragma unroll
+          for (int k = 0; k < kQ; ++k) v[k] += bb[k];
+        }
+        float4 *d4 = reinterpret_cast<float4 *>(dst);
+#pragma unroll
+        for (int k = 0; k < kQ / 4; ++k) d4[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (s_abort && warp == kRowWarps && lane == 0) {
+    mbar_drain(smem_u32(&bar_w), 0);
+    mbar_drain(smem_u32(&bar_mma), 0);
+  }
+  __syncthreads();
+  if (warp == kRowWarps) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
+  }
+}
+
+// ---------------------------------------------------------------- per candidate
+// One CTA per (128-candidate tile, half): half 0 writes U, half 1 writes V;
+// both recompute z (a 128x128 map, cheap).  Tensor memory: [0,128) the fuse
+// product, [128,384) the 256 layer-1 outputs of this half.  Shared memory
+// (three 64 KB regions), by phase:
+//   A:  b (hi, lo), then z (hi, lo);                  then outputs 128..255
+//   W0: W_fuse[:, :r] (hi, lo), then layer-1 rows 128..255 of this half
+//   S:  the cand_proj tile (fp32, 4 swizzled 32-column boxes),
+//       then layer-1 rows 0..127 of this half;       then outputs 0..127
+// All tiles move by TMA; the fp32 boxes use the same 128-byte swizzle as the
+// bf16 operands, so the row threads' 16-byte accesses are conflict-free.
+constexpr int kOffS = 4 * kMat;
+constexpr int kBox = 128 * 128;  // one fp32 box: 128 rows x 32 columns, 16 KB
+constexpr int kCandSmemBytes = 6 * kMat + 1024;
+constexpr uint32_t kCandTmemCols = 512;
+
+// 16-byte chunk c of row r in a swizzled 128-byte-row box at `box`.
+__device__ __forceinline__ uint8_t *box_chunk(uint8_t *box, int r, int c) {
+  return box + r * 128 + ((c ^ (r & 7)) * 16);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+k_cand_mlp_tc(const __grid_constant__ CUtensorMap map_fb_hi, const __grid_constant__ CUtensorMap map_fb_lo,
+              const __grid_constant__ CUtensorMap map_w1_hi, const __grid_constant__ CUtensorMap map_w1_lo,
+              const __grid_constant__ CUtensorMap map_cp, const __grid_constant__ CUtensorMap map_u,
+              const __grid_constant__ CUtensorMap map_v, const float *__restrict__ Gf,
+              const float *__restrict__ topk_val, const float *__restrict__ gamma,
+              const float *__restrict__ beta, const float *__restrict__ w_la,
+              const float *__restrict__ w_lb, int K, int M, float eps, int *err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  __shared__ __align__(8) unsigned long long bar_w0, bar_s, bar_w1, bar_w2, bar_a, bar_fuse, bar_a2,
+      bar_uv0, bar_uv1;
+  __shared__ float s_red[2][4 * kRows];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int half = blockIdx.x, m0 = blockIdx.y * kRows;
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t a_hi = sb + kOffA, a_lo = sb + kOffA + kMat;
+  const uint32_t w0_hi = sb + kOffW0, w0_lo = sb + kOffW0 + kMat;
+  const uint32_t s_hi = sb + kOffS, s_lo = sb + kOffS + kMat;
+
+  if (tid == 0) {
+    mbar_init(smem_u32(&bar_w0), 1);
+    mbar_init(smem_u32(&bar_s), 1);
+    mbar_init(smem_u32(&bar_w1), 1);
+    mbar_init(smem_u32(&bar_w2), 1);
+    mbar_init(smem_u32(&bar_a), kRowThreads);
+    mbar_init(smem_u32(&bar_fuse), 1);
+    mbar_init(smem_u32(&bar_a2), kRowThreads);
+    mbar_init(smem_u32(&bar_uv0), 1);
+    mbar_init(smem_u32(&bar_uv1), 1);
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kRowWarps) tmem_alloc(smem_u32(&s_tmem), kCandTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const int wrow0 = half * kH;  // first row of this half's block in [W1_a ; W1_b]
+  bool w1_issued = false, w2_issued = false;
+
+  if (warp == kRowWarps) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ control thread
+      load_pair(w0_hi, w0_lo, &map_fb_hi, &map_fb_lo, 0, smem_u32(&bar_w0));
+      mbar_arrive_expect_tx(smem_u32(&bar_s), 4 * kBox);
+      for (int bx = 0; bx < 4; ++bx) tma_load_2d(s_hi + bx * kBox, &map_cp, bx * 32, m0, smem_u32(&bar_s));
+      // y = W_fuse[:, :r] b
+      if (mbar_wait(smem_u32(&bar_w0), 0, &s_abort, err) && mbar_wait(smem_u32(&bar_a), 0, &s_abort, err)) {
+        tc_fence_after();
+        mma_split(tmem, a_hi, a_lo, w0_hi, w0_lo);
+        // the row threads are done with the cand_proj tile: S takes layer-1 rows 0..127
+        load_pair(s_hi, s_lo, &map_w1_hi, &map_w1_lo, wrow0, smem_u32(&bar_w1));
+        w1_issued = true;
+      }
+      mma_commit(smem_u32(&bar_fuse));
+      // once the fuse MMAs have read W0, it takes layer-1 rows 128..255
+      if (mbar_wait(smem_u32(&bar_fuse), 0, &s_abort, err)) {
+        load_pair(w0_hi, w0_lo, &map_w1_hi, &map_w1_lo, wrow0 + 128, smem_u32(&bar_w2));
+        w2_issued = true;
+      }
+      if (w1_issued && mbar_wait(smem_u32(&bar_a2), 0, &s_abort, err) &&
+          mbar_wait(smem_u32(&bar_w1), 0, &s_abort, err)) {
+        tc_fence_after();
+        mma_split(tmem + 128, a_hi, a_lo, s_hi, s_lo);
+      }
+      mma_commit(smem_u32(&bar_uv0));
+      if (w2_issued && mbar_wait(smem_u32(&bar_w2), 0, &s_abort, err)) {
+        tc_fence_after();
+        mma_split(tmem + 256, a_hi, a_lo, w0_hi, w0_lo);
+      }
+      mma_commit(smem_u32(&bar_uv1));
+    }
+    __syncwarp();
+  } else {
+    // -------------------------------------------------------------- row threads
+    const int qd = warp & 3, q = warp >> 2;  // lane quadrant, column quarter
+    const int r = qd * 32 + lane;           // tile row = tensor-memory lane
+    const int m = m0 + r;
+    const bool live = m < M;
+    const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16);
+    float x[kQ];
+    // b = LN0(cand_proj row): quarter q is box q of the staged tile
+    const bool ok0 = rows_all(mbar_wait(smem_u32(&bar_s), 0, &s_abort, err) && !s_abort);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ok0 && live) v = *reinterpret_cast<const float4 *>(box_chunk(smem + kOffS + q * kBox, r, c));
+      x[4 * c] = v.x; x[4 * c + 1] = v.y; x[4 * c + 2] = v.z; x[4 * c + 3] = v.w;
+    }
+    ln0_part(x, eps, s_red[0], s_red[1], r, q);
+    store_split_part(smem + kOffA, smem + kOffA + kMat, r, q, x);
+    fence_proxy_async();
+    mbar_arrive(smem_u32(&bar_a));
+
+    // z = gamma * LN0(y + Gf[slot]) + beta  (every row thread takes part: the
+    // LayerNorm holds row barriers)
+    const bool ok = rows_all(mbar_wait(smem_u32(&bar_fuse), 0, &s_abort, err) && !s_abort);
+    tc_fence_after();
+    if (ok) {
+      tmem_ld32(lane_base + q * kQ, x);
+      if (live) {
+        float g[kQ];
+        load32(g, Gf + (int64_t)(m / K) * kR + q * kQ);
+#pragma unroll
+        for (int k = 0; k < kQ; ++k) x[k] += g[k];
+      } else {
+#pragma unroll
+        for (int k = 0; k < kQ; ++k) x[k] = 0.f;
+      }
+      ln0_part(x, eps, s_red[0], s_red[1], r, q);
+      float ga[kQ], be[kQ];
+      load32(ga, gamma + q * kQ);
+      load32(be, beta + q * kQ);
+#pragma unroll
+      for (int k = 0; k < kQ; ++k) x[k] = fmaf(ga[k], x[k], be[k]);
+      store_split_part(smem + kOffA, smem + kOffA + kMat, r, q, x);
+    }
+    fence_proxy_async();
+    mbar_arrive(smem_u32(&bar_a2));
+
+    // U (or V) = W1 z + w_l l: quarter q takes outputs [64 q, 64 q + 64),
+    // staged as fp32 boxes 2q, 2q+1 (outputs 0..127 in S, 128..255 in A)
+    const float *wl = (half == 0 ? w_la : w_lb) + q * 64;
+    const float lv = live ? __ldg(topk_val + m) : 0.f;
+    bool ok2 = mbar_wait(smem_u32(q < 2 ? &bar_uv0 : &bar_uv1), 0, &s_abort, err) && !s_abort;
+    ok2 = __all_sync(DC_FULL_MASK, ok2);
+    tc_fence_after();
+    if (ok2) {
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
+        float v[kQ], wv[kQ];
+        tmem_ld32(lane_base + 128 + q * 64 + h * kQ, v);
+        load32(wv, wl + h * kQ);
+        const int bx = 2 * q + h;
+        uint8_t *box = smem + (bx < 4 ? kOffS + bx * kBox : kOffA + (bx - 4) * kBox);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          *reinterpret_cast<float4 *>(box_chunk(box, r, c)) =
+              make_float4(fmaf(wv[4 * c], lv, v[4 * c]), fmaf(wv[4 * c + 1], lv, v[4 * c + 1]),
+                          fmaf(wv[4 * c + 2], lv, v[4 * c + 2]), fmaf(wv[4 * c + 3], lv, v[4 * c + 3]));
+      }
+    }
+    fence_proxy_async();
+    if (rows_all(ok2) && tid == 0) {
+      const CUtensorMap *map = half == 0 ? &map_u : &map_v;
+      for (int bx = 0; bx < 8; ++bx)
+        tma_store_2d(map, sb + (bx < 4 ? kOffS + bx * kBox : kOffA + (bx - 4) * kBox), bx * 32, m0);
+      bulk_commit();
+      bulk_wait_all();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (s_abort && warp == kRowWarps && lane == 0) {
+    // a wait expired: let the copies and MMAs already issued land first
+    mbar_drain(smem_u32(&bar_w0), 0);
+    mbar_drain(smem_u32(&bar_s), 0);
+    if (w1_issued) mbar_drain(smem_u32(&bar_w1), 0);
+    if (w2_issued) mbar_drain(smem_u32(&bar_w2), 0);
+    mbar_drain(smem_u32(&bar_uv1), 0);
+  }
+  __syncthreads();
+  if (warp == kRowWarps) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kCandTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_slot_mlp_tc(const MlpMaps &maps, const float *slot_proj, const MlpWeightsDev &w, int N,
+                               int B, float eps, float *Gf, float *P, int *err, cudaStream_t st) {
+  const int NB = N * B;
+  if (NB == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(k_slot_mlp_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSlotSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(3, (NB + kRows - 1) / kRows);
+  k_slot_mlp_tc<<<grid, kThreads, kSlotSmemBytes, st>>>(maps.fg_hi, maps.fg_lo, maps.w1s_hi, maps.w1s_lo,
+                                                        slot_proj, w.b1, NB, B, eps, Gf, P, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_cand_mlp_tc(const MlpMaps &maps, const CandIoMaps &io, const float *Gf,
+                               const float *topk_val, const MlpWeightsDev &w, int K, int M, float eps,
+                               int *err, cudaStream_t st) {
+  if (M == 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(k_cand_mlp_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kCandSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(2, (M + kRows - 1) / kRows);
+  k_cand_mlp_tc<<<grid, kThreads, kCandSmemBytes, st>>>(maps.fb_hi, maps.fb_lo, maps.w1_hi, maps.w1_lo, io.cp,
+                                                        io.u, io.v, Gf, topk_val, w.gamma, w.beta, w.w_la,
+                                                        w.w_lb, K, M, eps, err);
+  return cudaGetLastError();
+}
+
+}  // namespace dc

@@ -299,6 +299,18 @@ bool encode_bf16_rows_map(CUtensorMap *map, const void *base, int rows, int d, i
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_f32_rows_map(CUtensorMap *map, const void *base, int rows, int cols, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rows <= 0 || cols % 32 != 0 || (reinterpret_cast<uintptr_t>(base) & 15u)) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+  const cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_proj_tc(int mode, const uint16_t *table, const CUtensorMap &map_hi,
                            const CUtensorMap &map_lo, const int32_t *ids, int slots, int B, int M, int d,
                            int V, int No, int splits, float *C, float *part, unsigned *tile_count,

@@ -181,41 +181,179 @@ k_cand_post(const float *__restrict__ cand_proj, const float *__restrict__ topk_
 }
 
 // ---------------------------------------------------------------- pair scores
+// With x = (P_p + U_{p,a} + V_{p+1,b}) / sqrt(2) and w' = w2 / sqrt(2),
+//   w2_j GELU(sqrt(2) x_j) = w'_j x_j (1 + erf(x_j)) = w'_j x_j + w'_j |x_j| erf(|x_j|).
+// The first term is separable, sum_j w'_j x_j = d_a + d_b with
+// d_a = sum_j w'_j (P_p + U_{p,a})_j / sqrt(2) and d_b = sum_j w'_j V_{p+1,b,j} / sqrt(2),
+// so the K^2 x H inner loop only evaluates w' |x| erf(|x|).
+//
+// erf on x >= 0 is Hastings' rational approximation as given in Abramowitz
+// & Stegun, Handbook of Mathematical Functions (1964), formula 7.1.28:
+//   erf(x) = 1 - (1 + a1 x + a2 x^2 + ... + a6 x^6)^-16,  |error| <= 3e-7,
+// evaluated in fp32 (measured: |x erf(x) error| < 1e-6 for x in [0, 10]):
+// one polynomial, four squarings and one hardware reciprocal.
+constexpr float kAs1 = 0.0705230784f, kAs2 = 0.0422820123f, kAs3 = 0.0092705272f;
+constexpr float kAs4 = 0.0001520143f, kAs5 = 0.0002765672f, kAs6 = 0.0000430638f;
+
+// Two fp32 lanes in one 64-bit register, for the packed f32x2 arithmetic.
+typedef unsigned long long f2_t;
+__device__ __forceinline__ f2_t f2_pack(float lo, float hi) {
+  f2_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+  return d;
+}
+__device__ __forceinline__ void f2_unpack(f2_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2_t f2_fma(f2_t a, f2_t b, f2_t c) {
+  f2_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
+  f2_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
+  f2_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f2_t f2_abs(f2_t a) { return a & 0x7FFFFFFF7FFFFFFFull; }
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// One CTA per slot pair (n, p).  Shared memory holds the K rows
+// (P_p + U_{p,a}) / sqrt(2) and the K rows V_{p+1,b} / sqrt(2); each thread
+// takes a 4 x 4 block of (a, b) over a strided slice of hidden-unit pairs
+// (j, j+1) = 2s, 2s + 2 NS, ... (NS slices), the pair in the two lanes of
+// the packed arithmetic, so every loaded value feeds four evaluations.  The
+// slices' partial sums meet in shared memory and are added in slice order,
+// so the result does not depend on scheduling.
+template <int K>
+struct PairGeom {
+  static constexpr int T = 4;                      // (a, b) block per thread
+  static constexpr int NT = (K / T) * (K / T);     // blocks
+  static constexpr int NS = 256 / NT;              // slices of hidden-unit pairs
+  static constexpr int JP = H / 2 / NS;            // pairs per slice
+  // row stride (floats, even): the 64-bit reads of a half-warp hit distinct banks
+  static constexpr int LD = K == 32 ? H + 2 : H + 4;
+  static constexpr int RED = K * K + 1;            // partial-sum row stride
+  static constexpr size_t smem_floats = 2 * (size_t)K * LD + H + 2 * K + (size_t)NS * RED;
+};
+
 template <int K>
 __global__ void __launch_bounds__(256)
 k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
              const float *__restrict__ P, const float *__restrict__ topk_val,
              const float *__restrict__ w2, const float *__restrict__ b2, int B,
              float *__restrict__ scores) {
+  using G = PairGeom<K>;
+  constexpr float kInvSqrt2 = 0.70710678118654752440f;
   extern __shared__ float sm[];
-  float *pu = sm;                   // [K][H+1]  P_p + U_{p,a}
-  float *vs = pu + K * (H + 1);     // [K][H+1]  V_{p+1,b}
-  float *w2s = vs + K * (H + 1);    // [H]
+  float *pu = sm;                   // [K][LD]  (P_p + U_{p,a}) / sqrt(2)
+  float *vs = pu + K * G::LD;       // [K][LD]  V_{p+1,b} / sqrt(2)
+  float *w2s = vs + K * G::LD;      // [H]      w2 / sqrt(2)
+  float *dab = w2s + H;             // [2K]     d_a, then d_b
+  float *red = dab + 2 * K;         // [NS][RED] partial sums
   const int np = blockIdx.x;        // n * (B-1) + p
   const int n = np / (B - 1), p = np - n * (B - 1);
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int64_t ca = ((int64_t)n * B + p) * K;      // first candidate of slot p
   const int64_t cb = ca + K;                         // first candidate of slot p+1
   const float *Pp = P + (int64_t)np * H;
 
-#pragma unroll 8
-  for (int e = tid; e < K * H; e += 256) {
-    const int c = e / H, j = e - c * H;
-    pu[c * (H + 1) + j] = U[(ca + c) * H + j] + Pp[j];
-    vs[c * (H + 1) + j] = V[(cb + c) * H + j];
+  for (int e4 = tid; e4 < K * H / 4; e4 += 256) {
+    const int c = e4 / (H / 4), j = (e4 - c * (H / 4)) * 4;
+    const float4 u = __ldg(reinterpret_cast<const float4 *>(U + (ca + c) * H + j));
+    const float4 pp = __ldg(reinterpret_cast<const float4 *>(Pp + j));
+    const float4 v = __ldg(reinterpret_cast<const float4 *>(V + (cb + c) * H + j));
+    float *x = pu + c * G::LD + j, *y = vs + c * G::LD + j;
+    x[0] = (u.x + pp.x) * kInvSqrt2; x[1] = (u.y + pp.y) * kInvSqrt2;
+    x[2] = (u.z + pp.z) * kInvSqrt2; x[3] = (u.w + pp.w) * kInvSqrt2;
+    y[0] = v.x * kInvSqrt2; y[1] = v.y * kInvSqrt2; y[2] = v.z * kInvSqrt2; y[3] = v.w * kInvSqrt2;
   }
-  w2s[tid] = w2[tid];
+  w2s[tid] = w2[tid] * kInvSqrt2;
+  __syncthreads();
+
+  // separable part: one warp per row, lane-strided, fixed order
+  for (int row = warp; row < 2 * K; row += 8) {
+    const float *xr = row < K ? pu + row * G::LD : vs + (row - K) * G::LD;
+    float d = 0.f;
+#pragma unroll
+    for (int j = lane; j < H; j += 32) d = fmaf(w2s[j], xr[j], d);
+    d = warp_sum(d);
+    if (lane == 0) dab[row] = d;
+  }
+
+  const int blk = tid / G::NS, sl = tid - blk * G::NS;
+  const int a0 = (blk / (K / G::T)) * G::T, b0 = (blk % (K / G::T)) * G::T;
+  const f2_t c1 = f2_pack(kAs1, kAs1), c2 = f2_pack(kAs2, kAs2), c3 = f2_pack(kAs3, kAs3);
+  const f2_t c4 = f2_pack(kAs4, kAs4), c5 = f2_pack(kAs5, kAs5), c6 = f2_pack(kAs6, kAs6);
+  const f2_t one = f2_pack(1.f, 1.f);
+  f2_t acc[G::T][G::T];
+#pragma unroll
+  for (int i = 0; i < G::T; ++i)
+#pragma unroll
+    for (int k = 0; k < G::T; ++k) acc[i][k] = 0ull;
+#pragma unroll 1
+  for (int jj = 0; jj < G::JP; ++jj) {
+    const int j = 2 * (sl + jj * G::NS);
+    const float2 wv = *reinterpret_cast<const float2 *>(w2s + j);
+    const f2_t w = f2_pack(wv.x, wv.y);
+    f2_t xa[G::T], yb[G::T];
+#pragma unroll
+    for (int i = 0; i < G::T; ++i) {
+      const float2 xv = *reinterpret_cast<const float2 *>(pu + (a0 + i) * G::LD + j);
+      const float2 yv = *reinterpret_cast<const float2 *>(vs + (b0 + i) * G::LD + j);
+      xa[i] = f2_pack(xv.x, xv.y);
+      yb[i] = f2_pack(yv.x, yv.y);
+    }
+#pragma unroll
+    for (int i = 0; i < G::T; ++i)
+#pragma unroll
+      for (int k = 0; k < G::T; ++k) {
+        const f2_t ax = f2_abs(f2_add(xa[i], yb[k]));
+        f2_t q = f2_fma(c6, ax, c5);
+        q = f2_fma(q, ax, c4);
+        q = f2_fma(q, ax, c3);
+        q = f2_fma(q, ax, c2);
+        q = f2_fma(q, ax, c1);
+        q = f2_fma(q, ax, one);
+        q = f2_mul(q, q);
+        q = f2_mul(q, q);
+        q = f2_mul(q, q);
+        q = f2_mul(q, q);
+        float q0, q1;
+        f2_unpack(q, q0, q1);
+        const f2_t nd = f2_pack(rcp_approx(-q0), rcp_approx(-q1));  // -(1 - erf(|x|))
+        const f2_t t = f2_mul(w, ax);
+        // acc += t erf(|x|) = t - t (1 - erf(|x|))
+        acc[i][k] = f2_fma(t, nd, f2_add(acc[i][k], t));
+      }
+  }
+  float *rs = red + sl * G::RED;
+#pragma unroll
+  for (int i = 0; i < G::T; ++i)
+#pragma unroll
+    for (int k = 0; k < G::T; ++k) {
+      float lo, hi;
+      f2_unpack(acc[i][k], lo, hi);
+      rs[(a0 + i) * K + b0 + k] = lo + hi;
+    }
   __syncthreads();
 
   const float bias = b2[0];
   for (int e = tid; e < K * K; e += 256) {
-    const int a = e / K, bb = e - a * K;
-    const float *x = pu + a * (H + 1);
-    const float *y = vs + bb * (H + 1);
-    float acc = 0.f;
-#pragma unroll 4
-    for (int jj = 0; jj < H; ++jj) acc = fmaf(w2s[jj], gelu_erf(x[jj] + y[jj]), acc);
-    scores[(int64_t)np * K * K + e] = topk_val[cb + bb] + bias + acc;
+    float sum = 0.f;
+#pragma unroll 8
+    for (int s2 = 0; s2 < G::NS; ++s2) sum += red[s2 * G::RED + e];
+    const int aa = e / K, bb = e - aa * K;
+    scores[(int64_t)np * K * K + e] = topk_val[cb + bb] + bias + (dab[aa] + dab[K + bb]) + sum;
   }
 }
 
@@ -297,7 +435,7 @@ template <int K>
 static cudaError_t pair_score_k(const float *U, const float *V, const float *P, const float *tv,
                                 const float *w2, const float *b2, int N, int B, float *scores,
                                 cudaStream_t st) {
-  const size_t smem = (size_t)(2 * K * (H + 1) + H) * sizeof(float);
+  const size_t smem = PairGeom<K>::smem_floats * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(k_pair_score<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
