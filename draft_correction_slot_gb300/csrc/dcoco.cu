@@ -22,10 +22,6 @@ struct Workspace {
   float *vals = nullptr;
   float *slot_proj = nullptr;  // [N*B][3r]  (variant 1: [N*B][2r])
   float *cand_proj = nullptr;  // [N*B*K][r] (variant 1: [N*B*K][2r])
-  float *slot_part = nullptr;  // split-K partials of the slot projection
-  float *cand_part = nullptr;  // split-K partials of the candidate projection
-  unsigned *slot_tiles = nullptr;
-  unsigned *cand_tiles = nullptr;
   float *Gf = nullptr;         // [N*B][r]
   float *P = nullptr;          // [N*(B-1)][H]
   float *U = nullptr;          // [N*B*K][H]  (variant 1: O [N*B*K][r])
@@ -129,8 +125,7 @@ struct Carver {  // sub-allocates a byte range, 256-byte aligned pieces
   }
 };
 
-void carve_workspace(Carver &c, const dcoco_config &cfg, int B, int topk_segments_max,
-                     int splits_slot, int splits_cand, Workspace &ws) {
+void carve_workspace(Carver &c, const dcoco_config &cfg, int B, int topk_segments_max, Workspace &ws) {
   const size_t N = (size_t)cfg.max_batch, K = (size_t)cfg.topk, d = (size_t)cfg.hidden;
   const size_t rows = N * B, cands = rows * K;
   ws.part = c.take<unsigned long long>(rows * (size_t)topk_segments_max * K);
@@ -139,11 +134,6 @@ void carve_workspace(Carver &c, const dcoco_config &cfg, int B, int topk_segment
   ws.vals = c.take<float>(cands);
   ws.slot_proj = c.take<float>(rows * 3 * kR);
   ws.cand_proj = c.take<float>(cands * 2 * kR);
-  const size_t rows_pad = (rows + 127) / 128 * 128, cands_pad = (cands + 127) / 128 * 128;
-  ws.slot_part = c.take<float>((size_t)splits_slot * rows_pad * 3 * kR);
-  ws.cand_part = c.take<float>((size_t)splits_cand * cands_pad * 2 * kR);
-  ws.slot_tiles = c.take<unsigned>(rows_pad / 128 * 3);
-  ws.cand_tiles = c.take<unsigned>(cands_pad / 128 * 2);
   ws.Gf = c.take<float>(rows * kR);
   ws.P = c.take<float>(N * (B - 1) * kH);
   ws.U = c.take<float>(cands * kH);
@@ -259,16 +249,16 @@ int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs 
       DC_TRY(cudaStreamWaitEvent(h->side, h->ev_fork, 0));
       ss = h->side;
     }
-    DC_TRY(clk.done(dc::launch_proj_tc(1, hidden, w->map_slot_hi, w->map_slot_lo, nullptr, cfg.slots, B,
-                                       rows, d, V, 3 * kR, h->splits_slot, ws.slot_proj, ws.slot_part,
-                                       ws.slot_tiles, ws.err, ss)));
+    DC_TRY(clk.done(dc::launch_proj_tc(1, 128, hidden, w->map_slot_hi, w->map_slot_lo, nullptr, cfg.slots, B,
+                                       rows, d, V, 3 * kR, h->splits_slot, ws.slot_proj,
+                                       ws.err, ss)));
     DC_TRY(clk.done(dc::launch_slot_mlp_tc(w->mlp_maps, ws.slot_proj, w->mlp, N, B, cfg.ln_eps, ws.Gf, ws.P,
                                            ws.err, ss)));
     if (overlap) DC_TRY(cudaEventRecord(h->ev_join, h->side));
     // step 2: candidate projections, then z and the layer-1 partials U, V
-    DC_TRY(clk.done(dc::launch_proj_tc(0, E, w->map_cand_hi, w->map_cand_lo, ids, cfg.slots, B,
-                                       cands, d, V, kR, h->splits_cand, ws.cand_proj, ws.cand_part,
-                                       ws.cand_tiles, ws.err, st)));
+    DC_TRY(clk.done(dc::launch_proj_tc(0, 256, E, w->map_cand_hi, w->map_cand_lo, ids, cfg.slots, B,
+                                       cands, d, V, kR, h->splits_cand, ws.cand_proj,
+                                       ws.err, st)));
     if (overlap) DC_TRY(cudaStreamWaitEvent(st, h->ev_join, 0));
     DC_TRY(clk.done(dc::launch_cand_mlp_tc(w->mlp_maps, h->cand_io, ws.Gf, vals, w->mlp, K, cands,
                                            cfg.ln_eps, ws.err, st)));
@@ -276,12 +266,12 @@ int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs 
     DC_TRY(clk.done(dc::launch_pair_score(K, ws.U, ws.V, ws.P, vals, w->mlp.w2, w->mlp.b2, N, B,
                                           scores, st)));
   } else {
-    DC_TRY(clk.done(dc::launch_proj_tc(1, hidden, w->map_slot_hi, w->map_slot_lo, nullptr, cfg.slots, B,
-                                       rows, d, V, 2 * kR, h->splits_slot, ws.slot_proj, ws.slot_part,
-                                       ws.slot_tiles, ws.err, st)));
-    DC_TRY(clk.done(dc::launch_proj_tc(0, E, w->map_cand_hi, w->map_cand_lo, ids, cfg.slots, B,
-                                       cands, d, V, 2 * kR, h->splits_cand, ws.cand_proj, ws.cand_part,
-                                       ws.cand_tiles, ws.err, st)));
+    DC_TRY(clk.done(dc::launch_proj_tc(1, 128, hidden, w->map_slot_hi, w->map_slot_lo, nullptr, cfg.slots, B,
+                                       rows, d, V, 2 * kR, h->splits_slot, ws.slot_proj,
+                                       ws.err, st)));
+    DC_TRY(clk.done(dc::launch_proj_tc(0, 256, E, w->map_cand_hi, w->map_cand_lo, ids, cfg.slots, B,
+                                       cands, d, V, 2 * kR, h->splits_cand, ws.cand_proj,
+                                       ws.err, st)));
     DC_TRY(clk.done(dc::launch_cos_post(K, ws.cand_proj, ws.slot_proj, N, B, ws.U, ws.V, st)));
     DC_TRY(clk.done(dc::launch_cos_score(K, ws.U, ws.V, vals, cfg.sigma, N, B, scores, st)));
   }
@@ -371,9 +361,9 @@ int dcoco_create(const dcoco_config *cfg, dcoco_handle **out) {
   }
   h->topk_wave = sms * dc::topk_occupancy(cfg->topk);
   h->splits_slot = dc::proj_tc_splits(cfg->hidden, 8);
-  h->splits_cand = dc::proj_tc_splits(cfg->hidden, 2);
+  h->splits_cand = dc::proj_tc_splits(cfg->hidden, 4);
   Carver sizer;
-  carve_workspace(sizer, h->cfg, h->B, h->topk_segments_max, h->splits_slot, h->splits_cand, h->ws);
+  carve_workspace(sizer, h->cfg, h->B, h->topk_segments_max, h->ws);
   const size_t bytes = sizer.off + 256;
   if (cudaMalloc(&h->block, bytes) != cudaSuccess) {
     cudaGetLastError();
@@ -382,7 +372,7 @@ int dcoco_create(const dcoco_config *cfg, dcoco_handle **out) {
   }
   Carver c;
   c.base = static_cast<char *>(h->block);
-  carve_workspace(c, h->cfg, h->B, h->topk_segments_max, h->splits_slot, h->splits_cand, h->ws);
+  carve_workspace(c, h->cfg, h->B, h->topk_segments_max, h->ws);
   const int cands_cap = cfg->max_batch * h->B * cfg->topk;
   const bool maps_ok =
       cfg->variant != 0 ||

@@ -42,22 +42,20 @@ cudaError_t launch_topk(int K, const uint16_t *logits, int64_t stride, int slots
 // [N][slots][d] tensor).
 // Tensor-core projection.  A rows are gathered from `table` (bf16 [rows][d]:
 // E, or the hidden states viewed as [N*slots][d]); W comes as bf16 hi and lo
-// halves ([No][d] each, No % 128 == 0,
-// d % 64 == 0) through `map_hi` / `map_lo` (box 64 x 128).  `splits` >= 2
-// splits the k range; then `part` holds splits * ceil(M/128)*128 * No floats
-// and `tile_count` (No/128 * ceil(M/128) entries, zero between calls) counts
-// the finished splits of each tile.
-size_t proj_tc_smem_bytes();
+// halves ([No][d] each, No % 128 == 0, d % 64 == 0) through `map_hi` /
+// `map_lo` (box 64 x 128).  `splits` (a power of two <= 8, from
+// proj_tc_splits) splits the k range over the CTAs of one cluster, which add
+// their partial tiles through distributed shared memory.  A CTA takes
+// `rows_per_cta` (128 or 256) rows: 256 halves the weight traffic per row.
 int proj_tc_splits(int d, int requested);
 // 2D bf16 [rows][d] tensor map, 128B swizzle, box 64 x box_rows.
 bool encode_bf16_rows_map(CUtensorMap *map, const void *base, int rows, int d, int box_rows);
 // 2D fp32 [rows][cols] tensor map, 128B swizzle, box 32 x box_rows
 // (cols % 32 == 0).
 bool encode_f32_rows_map(CUtensorMap *map, const void *base, int rows, int cols, int box_rows);
-cudaError_t launch_proj_tc(int mode, const uint16_t *table, const CUtensorMap &map_hi,
+cudaError_t launch_proj_tc(int mode, int rows_per_cta, const uint16_t *table, const CUtensorMap &map_hi,
                            const CUtensorMap &map_lo, const int32_t *ids, int slots, int B, int M, int d,
-                           int V, int No, int splits, float *C, float *part, unsigned *tile_count,
-                           int *err, cudaStream_t st);
+                           int V, int No, int splits, float *C, int *err, cudaStream_t st);
 
 // ---------------------------------------------------------------- representations
 struct MlpWeightsDev {

@@ -10,19 +10,20 @@
 // (w = hi + lo to ~2^-17 relative), and both products accumulate into the same
 // fp32 accumulator: C = A hi^T + A lo^T.
 //
-// Tile: 128 rows x 128 outputs, k-blocks of 64 (one 128-byte swizzle atom),
-// a 4-stage ring in 128B-swizzled K-major shared memory.  Each operand takes
-// the path that suits it: warps 0-3 gather the A rows with 16-byte cp.async
-// (many small independent rows), one thread of warp 4 brings the hi and lo
-// weight blocks as two 2D TMA tiles (large blocks, the same for every CTA);
-// a stage is full when the 128 gatherers have arrived and the TMA bytes have
-// landed.  One thread of warp 5 (which also owns the tensor-memory
-// allocation) issues the MMAs; warps 0-3 then drain the accumulator with
-// tcgen05.ld.  Split-K over gridDim.z: every split writes an fp32
-// partial tile and the tile's last CTA (atomic counter) adds the partials in
-// split order, so the result does not depend on which CTA finished last.
+// Tile: 128 rows x 128 outputs, k-blocks of 64 (one 128-byte swizzle atom)
+// in 128B-swizzled K-major shared memory.  Each operand takes the path that
+// suits it: warps 0-3 gather the A rows with 16-byte cp.async into an
+// 8-deep ring (many small independent rows from HBM: the depth keeps enough
+// bytes in flight), one thread of warp 4 brings the hi and lo weight blocks
+// as two 2D TMA tiles into a 3-deep ring (the same blocks for every CTA,
+// served from L2).  One thread of warp 5 (which also owns the tensor-memory
+// allocation) issues the MMAs once both rings hold the k-block; warps 0-3
+// then drain the accumulator with tcgen05.ld into shared memory.
+// Split-K over gridDim.z: the splits of a tile form one thread-block
+// cluster and add their partial tiles through distributed shared memory in
+// split order, so the result does not depend on timing.
 // Every wait is bounded in time; on expiry the kernel records kErrTimeout in
-// the device status word and leaves without touching the output.
+// the device status word and does not store its rows.
 #include <cuda.h>
 
 #include <algorithm>
@@ -34,17 +35,32 @@
 namespace dc {
 namespace {
 
-constexpr int kStages = 4;
-constexpr int kTileM = 128, kTileN = 128, kTileK = 64;
-constexpr int kTileBytes = kTileM * kTileK * 2;        // 16 KB (A, hi or lo)
-constexpr int kStageBytes = 3 * kTileBytes;             // A + hi + lo
-constexpr int kGatherThreads = 128;  // warps 0-3: A gather, then epilogue
-constexpr int kThreads = 192;        // + warp 4 (weight TMA) + warp 5 (MMA)
-constexpr uint32_t kStageTx = 2u * kTileBytes;  // weight bytes per stage
-constexpr uint32_t kTmemCols = 128;
-constexpr int kMaxSplits = 8;
+constexpr int kTileN = 128, kTileK = 64;
+constexpr int kSubM = 128;                             // rows per accumulator (MMA M)
+constexpr int kSubBytes = kSubM * kTileK * 2;          // 16 KB: 128 rows x 64 k of bf16
+constexpr uint32_t kStageTx = 2u * kSubBytes;          // weight bytes per k-block (hi + lo)
+constexpr int kMaxSplits = 8;       // a cluster of at most 8 CTAs (portable size)
+constexpr int kBoxBytes = kSubM * 128;  // one 32-column fp32 box of a 128-row output tile
+constexpr uint32_t kIdesc = tc::idesc_bf16(kSubM, kTileN);
 
-constexpr uint32_t kIdesc = tc::idesc_bf16(kTileM, kTileN);
+// A CTA owns MT x 128 rows (MT accumulators of 128 x 128 in tensor memory)
+// so that every weight k-block it brings in feeds MT MMAs.  Two rings: the
+// gathered A rows come from HBM (long latency: a deep ring keeps enough bytes
+// in flight), the weights from L2 (a shorter ring suffices).
+template <int MT>
+struct ProjGeom {
+  static constexpr int kTileM = MT * kSubM;
+  static constexpr int kGather = MT * 128;               // gather threads (warps 0 .. 4 MT - 1)
+  static constexpr int kThreads = kGather + 64;          // + weight-TMA warp + MMA warp
+  static constexpr int kWarpTma = 4 * MT, kWarpMma = 4 * MT + 1;
+  static constexpr int kStageA = MT * kSubBytes;
+  static constexpr int kStagesA = MT == 1 ? 8 : 4, kStagesW = 3;
+  static constexpr int kRingA = kStagesA * kStageA;      // A ring, then the W ring
+  static constexpr int kSmemUsed = kRingA + kStagesW * 2 * kSubBytes;
+  static constexpr uint32_t kTmemCols = MT * 128;
+  static_assert(kSmemUsed + 1024 <= 227 * 1024 - 1024, "shared memory");
+  static_assert(MT * 4 * kBoxBytes <= kRingA, "the output tile is staged in the A ring");
+};
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -58,20 +74,44 @@ __device__ __forceinline__ void cp_async_wait() {
 
 using namespace tc;
 
-template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory location in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, int rank) {
+  uint32_t d;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(saddr), "r"(rank));
+  return d;
+}
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+template <int MODE, int MT>
+__global__ void __launch_bounds__(ProjGeom<MT>::kThreads, 1)
 k_proj_tc(const uint16_t *__restrict__ table, const __grid_constant__ CUtensorMap map_hi,
           const __grid_constant__ CUtensorMap map_lo, const int32_t *__restrict__ ids, int slots,
-          int B, int M, int d, int V, int No, int kb_per_split, float *__restrict__ C,
-          float *__restrict__ part, unsigned *__restrict__ tile_count, int *err) {
+          int B, int M, int d, int V, int No, int kb_per_split, float *__restrict__ C, int *err) {
+  using G = ProjGeom<MT>;
+  constexpr int kTileM = G::kTileM, kStagesA = G::kStagesA, kStagesW = G::kStagesW;
   extern __shared__ uint8_t smem_raw[];
   // the swizzle atoms need 1024-byte alignment in the shared window
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  __shared__ __align__(8) unsigned long long bar_full[kStages], bar_empty[kStages], bar_done;
+  __shared__ __align__(8) unsigned long long full_a[kStagesA], empty_a[kStagesA], full_w[kStagesW],
+      empty_w[kStagesW], bar_done;
   __shared__ int s_rows[kTileM];  // table row of each tile row (A operand)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ int s_last;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n0 = blockIdx.x * kTileN, m0 = blockIdx.y * kTileM, split = blockIdx.z;
@@ -81,9 +121,13 @@ k_proj_tc(const uint16_t *__restrict__ table, const __grid_constant__ CUtensorMa
   const uint32_t sbase = smem_u32(smem);
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(smem_u32(&bar_full[s]), kGatherThreads + 1);
-      mbar_init(smem_u32(&bar_empty[s]), 1);
+    for (int s = 0; s < kStagesA; ++s) {
+      mbar_init(smem_u32(&full_a[s]), G::kGather);
+      mbar_init(smem_u32(&empty_a[s]), 1);
+    }
+    for (int s = 0; s < kStagesW; ++s) {
+      mbar_init(smem_u32(&full_w[s]), 1);
+      mbar_init(smem_u32(&empty_w[s]), 1);
     }
     mbar_init(smem_u32(&bar_done), 1);
     s_abort = 0;
@@ -106,102 +150,109 @@ k_proj_tc(const uint16_t *__restrict__ table, const __grid_constant__ CUtensorMa
     }
     s_rows[tid] = row;
   }
-  if (warp == 5) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_u32(&s_tmem)),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-  }
+  if (warp == G::kWarpMma) tmem_alloc(smem_u32(&s_tmem), G::kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
 
   int issued = 0;  // stages whose weight TMA this thread issued
-  if (warp < 4) {
+  if (warp < 4 * MT) {
     // ------------------------------------------------------------ A gather (cp.async)
-    const int t = tid;
+    // thread t: 16-byte chunk c of the 128-byte k-row, rows (t >> 3) + 16 j of
+    // its 128-row sub-tile t >> 7
+    const int t = tid & 127, sub = tid >> 7;
     const int c = t & 7;              // 16-byte chunk of the 128-byte k-row
     const int rq = (t >> 3) & 7;      // row within an 8-row swizzle group
-    const uint32_t off0 = (uint32_t)((t >> 6) * 1024 + rq * 128 + ((c ^ rq) * 16));
+    const uint32_t off0 = (uint32_t)(sub * kSubBytes + (t >> 6) * 1024 + rq * 128 + ((c ^ rq) * 16));
     const uint16_t *arow[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) arow[j] = table + (int64_t)s_rows[(t >> 3) + 16 * j] * d + c * 8;
+    for (int j = 0; j < 8; ++j) arow[j] = table + (int64_t)s_rows[sub * 128 + (t >> 3) + 16 * j] * d + c * 8;
     int it = 0;
     for (; it < nkb; ++it) {
-      const int s = it % kStages;
-      if (it >= kStages &&
-          !mbar_wait(smem_u32(&bar_empty[s]), ((it / kStages) - 1) & 1, &s_abort, err))
+      const int s = it % kStagesA;
+      if (it >= kStagesA &&
+          !mbar_wait(smem_u32(&empty_a[s]), ((it / kStagesA) - 1) & 1, &s_abort, err))
         break;
       const int kel = (kb0 + it) * kTileK;
-      const uint32_t sa = sbase + s * kStageBytes + off0;
+      const uint32_t sa = sbase + s * G::kStageA + off0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) cp_async16(sa + j * 2048, arow[j] + kel);
       cp_async_commit();
-      if (it >= kStages - 1) {
-        cp_async_wait<kStages - 1>();
+      if (it >= kStagesA - 1) {
+        cp_async_wait<kStagesA - 1>();
         fence_proxy_async();
-        mbar_arrive(smem_u32(&bar_full[(it - (kStages - 1)) % kStages]));
+        mbar_arrive(smem_u32(&full_a[(it - (kStagesA - 1)) % kStagesA]));
       }
     }
     cp_async_wait<0>();
     fence_proxy_async();
-    for (int r = max(0, it - (kStages - 1)); r < it; ++r) mbar_arrive(smem_u32(&bar_full[r % kStages]));
-  } else if (warp == 4) {
+    for (int r = max(0, it - (kStagesA - 1)); r < it; ++r) mbar_arrive(smem_u32(&full_a[r % kStagesA]));
+  } else if (warp == G::kWarpTma) {
     if (lane == 0) {
       // ------------------------------------------------------------ weight TMA
       for (int it = 0; it < nkb; ++it, ++issued) {
-        const int s = it % kStages;
-        if (it >= kStages &&
-            !mbar_wait(smem_u32(&bar_empty[s]), ((it / kStages) - 1) & 1, &s_abort, err))
+        const int s = it % kStagesW;
+        if (it >= kStagesW &&
+            !mbar_wait(smem_u32(&empty_w[s]), ((it / kStagesW) - 1) & 1, &s_abort, err))
           break;
-        const uint32_t full = smem_u32(&bar_full[s]);
-        const uint32_t sa = sbase + s * kStageBytes;
+        const uint32_t full = smem_u32(&full_w[s]);
+        const uint32_t sw = sbase + G::kRingA + s * 2 * kSubBytes;
         const int kx = (kb0 + it) * kTileK;
         mbar_arrive_expect_tx(full, kStageTx);
-        tma_load_2d(sa + kTileBytes, &map_hi, kx, n0, full);
-        tma_load_2d(sa + 2 * kTileBytes, &map_lo, kx, n0, full);
+        tma_load_2d(sw, &map_hi, kx, n0, full);
+        tma_load_2d(sw + kSubBytes, &map_lo, kx, n0, full);
       }
     }
-  } else if (warp == 5 && lane == 0) {
+  } else if (warp == G::kWarpMma && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
     for (int it = 0; it < nkb; ++it) {
-      const int s = it % kStages;
-      if (!mbar_wait(smem_u32(&bar_full[s]), (it / kStages) & 1, &s_abort, err)) break;
+      const int s = it % kStagesA, t = it % kStagesW;
+      if (!mbar_wait(smem_u32(&full_a[s]), (it / kStagesA) & 1, &s_abort, err) ||
+          !mbar_wait(smem_u32(&full_w[t]), (it / kStagesW) & 1, &s_abort, err))
+        break;
       tc_fence_after();
-      const uint32_t sa = sbase + s * kStageBytes;
+      const uint32_t sa = sbase + s * G::kStageA, sw = sbase + G::kRingA + t * 2 * kSubBytes;
 #pragma unroll
       for (int k = 0; k < kTileK / 16; ++k) {
-        const uint64_t ad = sw128_desc(sa + k * 32);
-        mma_bf16(tmem, ad, sw128_desc(sa + kTileBytes + k * 32), kIdesc, (it > 0 || k > 0) ? 1u : 0u);
-        mma_bf16(tmem, ad, sw128_desc(sa + 2 * kTileBytes + k * 32), kIdesc, 1u);
+        const uint64_t bh = sw128_desc(sw + k * 32), bl = sw128_desc(sw + kSubBytes + k * 32);
+#pragma unroll
+        for (int h = 0; h < MT; ++h) {
+          const uint64_t ad = sw128_desc(sa + h * kSubBytes + k * 32);
+          mma_bf16(tmem + h * 128, ad, bh, kIdesc, (it > 0 || k > 0) ? 1u : 0u);
+          mma_bf16(tmem + h * 128, ad, bl, kIdesc, 1u);
+        }
       }
-      mma_commit(smem_u32(&bar_empty[s]));
+      mma_commit(smem_u32(&empty_a[s]));
+      mma_commit(smem_u32(&empty_w[t]));
     }
     mma_commit(smem_u32(&bar_done));
   }
   __syncwarp();
 
   // ---------------------------------------------------------------- epilogue
-  const bool split_k = gridDim.z > 1;
-  if (warp < 4) {
+  // The accumulators go to shared memory (the A ring is idle once bar_done
+  // fired), each as four 32-column fp32 boxes, 128-byte swizzled so that the
+  // row threads' 16-byte stores and the reducers' reads are conflict-free.
+  if (warp < 4 * MT) {
     bool ok = mbar_wait(smem_u32(&bar_done), 0, &s_abort, err) && !s_abort;
     ok = __all_sync(DC_FULL_MASK, ok);  // tcgen05.ld below is warp-collective
     tc_fence_after();
     if (ok) {
-      const int row = m0 + warp * 32 + lane;
-      float *dst = split_k ? part + ((int64_t)split * gridDim.y * kTileM + row) * No + n0
-                           : C + (int64_t)row * No + n0;
+      const int sub = warp >> 2, q4 = warp & 3;  // accumulator, lane quadrant
+      const int r = q4 * 32 + lane;              // row within the accumulator
 #pragma unroll 1
       for (int cc = 0; cc < kTileN / 32; ++cc) {
         float v[32];
-        tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(cc * 32), v);
-        if (row < M || split_k) {
-          float4 *d4 = reinterpret_cast<float4 *>(dst + cc * 32);
+        tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(sub * 128 + cc * 32), v);
+        if (nkb <= 0)  // an empty split holds no products
 #pragma unroll
-          for (int q = 0; q < 8; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
-        }
+          for (int k = 0; k < 32; ++k) v[k] = 0.f;
+        uint8_t *box = smem + (sub * 4 + cc) * kBoxBytes + r * 128;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<float4 *>(box + ((q ^ (r & 7)) * 16)) =
+              make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
       }
     }
   }
@@ -209,59 +260,84 @@ k_proj_tc(const uint16_t *__restrict__ table, const __grid_constant__ CUtensorMa
   __syncthreads();
   if (s_abort) {
     // a wait expired: let everything already issued land before leaving
-    if (warp == 4 && lane == 0)
-      for (int s = 0; s < kStages && s < issued; ++s) {
-        const int last = s + kStages * ((issued - 1 - s) / kStages);
-        mbar_drain(smem_u32(&bar_full[s]), (last / kStages) & 1);
+    if (warp == G::kWarpTma && lane == 0)
+      for (int s = 0; s < kStagesW && s < issued; ++s) {
+        const int last = s + kStagesW * ((issued - 1 - s) / kStagesW);
+        mbar_drain(smem_u32(&full_w[s]), (last / kStagesW) & 1);
       }
-    if (warp == 5 && lane == 0) mbar_drain(smem_u32(&bar_done), 0);
+    if (warp == G::kWarpMma && lane == 0) mbar_drain(smem_u32(&bar_done), 0);
     __syncthreads();
   }
-  if (warp == 5) {
+  if (warp == G::kWarpMma) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
-                 : "memory");
+    tmem_dealloc(tmem, G::kTmemCols);
   }
-  if (!split_k || s_abort) return;
 
   // ---------------------------------------------------------------- split-K reduction
-  __threadfence();
-  __syncthreads();
-  const int tile = blockIdx.y * gridDim.x + blockIdx.x;
-  if (tid == 0) s_last = (atomicAdd(&tile_count[tile], 1u) == gridDim.z - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  const int rows = min(kTileM, M - m0);
-  const int64_t pstride = (int64_t)gridDim.y * kTileM * No;
-  const int nz = (int)gridDim.z;  // <= kMaxSplits
-  for (int e = tid; e < rows * (kTileN / 4); e += kThreads) {
-    const int r = e / (kTileN / 4), q = e - r * (kTileN / 4);
-    const int64_t off = (int64_t)(m0 + r) * No + n0 + q * 4;
-    float4 p[kMaxSplits];
+  // The splits of a tile form one cluster.  After the cluster barrier every
+  // partial tile is visible through distributed shared memory; CTA z adds
+  // rows [z R/S, (z+1) R/S) of all S partials in split order (so the result
+  // does not depend on timing) and stores them, 512 contiguous bytes per
+  // row.  Every CTA passes both cluster barriers on every path; the second
+  // keeps each partial alive until its readers are done.
+  cluster_sync();
+  const int S = (int)gridDim.z;
+  const int z = (int)cluster_ctarank();
+  const int rows_per = kTileM / S;  // S divides 128
+  const int r0 = z * rows_per;
+  const uint32_t own = smem_u32(smem);
+  uint32_t peer[kMaxSplits];
 #pragma unroll
-    for (int z = 0; z < kMaxSplits; ++z)  // every partial load in flight at once
-      if (z < nz) p[z] = __ldcg(reinterpret_cast<const float4 *>(part + z * pstride + off));
-    float4 acc = p[0];
+  for (int q = 0; q < kMaxSplits; ++q) peer[q] = q < S ? mapa_shared(own, q) : 0u;
+  const int nchunks = rows_per * (kTileN / 4);
+  for (int e0 = tid; e0 < nchunks; e0 += G::kThreads * 2) {
+    float4 acc[2];
 #pragma unroll
-    for (int z = 1; z < kMaxSplits; ++z)
-      if (z < nz) {
-        acc.x += p[z].x; acc.y += p[z].y; acc.z += p[z].z; acc.w += p[z].w;
+    for (int u = 0; u < 2; ++u) {
+      const int e = e0 + u * G::kThreads;
+      acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e < nchunks) {
+        const int r = r0 + e / (kTileN / 4), c = e % (kTileN / 4), rr = r & 127;
+        const uint32_t off =
+            (uint32_t)(((r >> 7) * 4 + (c >> 3)) * kBoxBytes + rr * 128 + (((c & 7) ^ (rr & 7)) * 16));
+        float4 p[kMaxSplits];
+#pragma unroll
+        for (int q = 0; q < kMaxSplits; ++q)  // every partial read in flight at once
+          if (q < S) p[q] = ld_dsmem_f4(peer[q] + off);
+        acc[u] = p[0];
+#pragma unroll
+        for (int q = 1; q < kMaxSplits; ++q)
+          if (q < S) {
+            acc[u].x += p[q].x; acc[u].y += p[q].y; acc[u].z += p[q].z; acc[u].w += p[q].w;
+          }
       }
-    *reinterpret_cast<float4 *>(C + off) = acc;
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int e = e0 + u * G::kThreads;
+      if (e < nchunks && !s_abort) {
+        const int r = r0 + e / (kTileN / 4), c = e % (kTileN / 4);
+        if (m0 + r < M) *reinterpret_cast<float4 *>(C + (int64_t)(m0 + r) * No + n0 + c * 4) = acc[u];
+      }
+    }
   }
-  if (tid == 0) tile_count[tile] = 0u;
+  cluster_sync();
 }
 
 }  // namespace
 
-size_t proj_tc_smem_bytes() { return (size_t)kStages * kStageBytes + 1024; }
 
 int proj_tc_splits(int d, int requested) {
+  // the largest power of two (it must divide the 128 tile rows that the
+  // cluster shares out) up to the request that leaves no split empty
   const int nkb = d / kTileK;
-  int s = std::max(1, std::min(std::min(requested, kMaxSplits), nkb));
-  const int per = (nkb + s - 1) / s;
-  return (nkb + per - 1) / per;  // no empty split
+  int s = 1;
+  while (s * 2 <= std::min(requested, kMaxSplits)) s *= 2;
+  for (; s > 1; s /= 2) {
+    const int per = (nkb + s - 1) / s;
+    if ((nkb + per - 1) / per == s) break;
+  }
+  return s;
 }
 
 namespace {
@@ -311,28 +387,48 @@ bool encode_f32_rows_map(CUtensorMap *map, const void *base, int rows, int cols,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t launch_proj_tc(int mode, const uint16_t *table, const CUtensorMap &map_hi,
-                           const CUtensorMap &map_lo, const int32_t *ids, int slots, int B, int M, int d,
-                           int V, int No, int splits, float *C, float *part, unsigned *tile_count,
-                           int *err, cudaStream_t st) {
-  if (M == 0) return cudaSuccess;
-  if (No % kTileN != 0 || d % kTileK != 0 || splits < 1 || splits > kMaxSplits) return cudaErrorInvalidValue;
+template <int MODE, int MT>
+static cudaError_t launch_mode(int M, int splits, int No, int d, cudaStream_t st, const uint16_t *table,
+                               const CUtensorMap &map_hi, const CUtensorMap &map_lo, const int32_t *ids,
+                               int slots, int B, int V, float *C, int *err) {
+  using G = ProjGeom<MT>;
   const int nkb = d / kTileK;
   const int per = (nkb + splits - 1) / splits;
-  dim3 grid(No / kTileN, (M + kTileM - 1) / kTileM, splits);
-  const size_t smem = proj_tc_smem_bytes();
+  const dim3 grid(No / kTileN, (M + G::kTileM - 1) / G::kTileM, splits);
+  const size_t smem = (size_t)G::kSmemUsed + 1024;
+  cudaError_t e = cudaFuncSetAttribute(k_proj_tc<MODE, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(G::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = grid.z;  // the splits of one tile
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k_proj_tc<MODE, MT>, table, map_hi, map_lo, ids, slots, B, M, d, V, No, per,
+                            C, err);
+}
+
+cudaError_t launch_proj_tc(int mode, int rows_per_cta, const uint16_t *table, const CUtensorMap &map_hi,
+                           const CUtensorMap &map_lo, const int32_t *ids, int slots, int B, int M, int d,
+                           int V, int No, int splits, float *C, int *err, cudaStream_t st) {
+  if (M == 0) return cudaSuccess;
+  if (No % kTileN != 0 || d % kTileK != 0 || splits < 1 || splits > kMaxSplits || (kSubM % splits) != 0 ||
+      (rows_per_cta != 128 && rows_per_cta != 256))
+    return cudaErrorInvalidValue;
   cudaError_t e;
-  if (mode == 0) {
-    e = cudaFuncSetAttribute(k_proj_tc<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    k_proj_tc<0><<<grid, kThreads, smem, st>>>(table, map_hi, map_lo, ids, slots, B, M, d, V, No, per, C,
-                                              part, tile_count, err);
-  } else {
-    e = cudaFuncSetAttribute(k_proj_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    k_proj_tc<1><<<grid, kThreads, smem, st>>>(table, map_hi, map_lo, ids, slots, B, M, d, V, No, per, C,
-                                              part, tile_count, err);
-  }
+  if (rows_per_cta == 128)
+    e = mode == 0 ? launch_mode<0, 1>(M, splits, No, d, st, table, map_hi, map_lo, ids, slots, B, V, C, err)
+                  : launch_mode<1, 1>(M, splits, No, d, st, table, map_hi, map_lo, ids, slots, B, V, C, err);
+  else
+    e = mode == 0 ? launch_mode<0, 2>(M, splits, No, d, st, table, map_hi, map_lo, ids, slots, B, V, C, err)
+                  : launch_mode<1, 2>(M, splits, No, d, st, table, map_hi, map_lo, ids, slots, B, V, C, err);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -78,19 +78,23 @@ __device__ __forceinline__ void warp_insert(u64 &list, u64 &kth, u64 key, int la
   kth = shfl_u64(list, K - 1);
 }
 
-__device__ __forceinline__ u64 shfl_xor_u64(u64 v, int m) {
+__device__ __forceinline__ u64 shfl_xor_key(u64 v, int m) {
   uint32_t lo = __shfl_xor_sync(DC_FULL_MASK, (uint32_t)v, m);
   uint32_t hi = __shfl_xor_sync(DC_FULL_MASK, (uint32_t)(v >> 32), m);
   return ((u64)hi << 32) | lo;
 }
+__device__ __forceinline__ uint32_t shfl_xor_key(uint32_t v, int m) { return __shfl_xor_sync(DC_FULL_MASK, v, m); }
+__device__ __forceinline__ uint32_t shfl_key(uint32_t v, int src) { return __shfl_sync(DC_FULL_MASK, v, src); }
+__device__ __forceinline__ u64 shfl_key(u64 v, int src) { return shfl_u64(v, src); }
 
 // Bitonic sort of one key per lane, descending over the 32 lanes.
-__device__ __forceinline__ u64 warp_sort32_desc(u64 x, int lane) {
+template <class T>
+__device__ __forceinline__ T warp_sort32_desc(T x, int lane) {
 #pragma unroll
   for (int k = 2; k <= 32; k <<= 1) {
 #pragma unroll
     for (int j = k >> 1; j > 0; j >>= 1) {
-      const u64 o = shfl_xor_u64(x, j);
+      const T o = shfl_xor_key(x, j);
       const bool keep_max = (((lane & j) == 0) == ((lane & k) == 0));
       x = keep_max ? (o > x ? o : x) : (o < x ? o : x);
     }
@@ -101,17 +105,17 @@ __device__ __forceinline__ u64 warp_sort32_desc(u64 x, int lane) {
 // Top K of two descending lists held in lanes (a: lanes < K, b: 32 lanes,
 // zero padded): max(a_i, b_{K-1-i}) is the top-K set as a bitonic sequence;
 // a half-cleaner network sorts it.
-template <int K>
-__device__ __forceinline__ u64 warp_merge_topk(u64 a, u64 b, int lane) {
-  const u64 br = shfl_u64(b, (K - 1 - lane) & 31);
-  u64 x = (lane < K) ? (a > br ? a : br) : 0ull;
+template <int K, class T>
+__device__ __forceinline__ T warp_merge_topk(T a, T b, int lane) {
+  const T br = shfl_key(b, (K - 1 - lane) & 31);
+  T x = (lane < K) ? (a > br ? a : br) : T(0);
 #pragma unroll
   for (int j = K >> 1; j > 0; j >>= 1) {
-    const u64 o = shfl_xor_u64(x, j);
+    const T o = shfl_xor_key(x, j);
     const bool lower = (lane & j) == 0;
     x = lower ? (o > x ? o : x) : (o < x ? o : x);
   }
-  return lane < K ? x : 0ull;
+  return lane < K ? x : T(0);
 }
 
 // bf16 bits with order key one below / above `key` (saturating).
@@ -299,6 +303,7 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
   __shared__ uint16_t s_gkey[kMaxGroups];   // order key of each group's maximum
   __shared__ int s_cand[kCandGroups];       // candidate groups, in order
   __shared__ u64 s_lists[kWarps * K];
+  __shared__ uint32_t s_glists[kWarps * K];  // per-warp best group keys
   __shared__ u64 s_top[K];
   __shared__ u64 s_cta_bound;
   __shared__ int s_ncand, s_nkeys, s_flag;
@@ -312,7 +317,10 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
   const int v0 = min(seg * seg_vecs, nvec), v1 = min(v0 + seg_vecs, nvec);
   const int nv = min(v1 - v0, kMaxSegVecs);           // vectors of this segment
   const bool has_tail = tail && seg == nseg - 1;
-  const int per_warp = (nv + kWarps - 1) / kWarps;
+  // warp ranges are whole 64-vector groups, so each 128-vector step of a warp
+  // covers exactly two groups and their maxima come from two warp reductions
+  const int per_warp = ((nv + kWarps - 1) / kWarps + kGroup - 1) / kGroup * kGroup;
+  const int ng = (nv + kGroup - 1) / kGroup;
   const int w0 = v0 + min(warp * per_warp, nv), w1 = v0 + min((warp + 1) * per_warp, nv);
   const uint64_t pol = evict_first_policy();
   if (tid < K) s_top[tid] = 0ull;
@@ -326,14 +334,25 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
   // ---------------------------------------------------------------- pass 1: stream
   {
     uint4 a[kU], b[kU];
+    static_assert(kStep == 2 * kGroup && kU == 4, "one step = two groups of 64 vectors");
     auto store = [&](const uint4 (&v)[kU], int base) {
+      uint32_t gk[2] = {0u, 0u};  // order keys of the two groups' maxima (0: empty)
 #pragma unroll
       for (int u = 0; u < kU; ++u) {
         const int j = base + lane + 32 * u;
         if (j < w1 && j - v0 < kMaxSegVecs) {  // the plan keeps segments within the buffer
           const uint32_t m2 = bf16x2_max(bf16x2_max(v[u].x, v[u].y), bf16x2_max(v[u].z, v[u].w));
-          s_vmax[j - v0] = (uint16_t)(bf16x2_max(m2, m2 >> 16) & 0xFFFFu);
+          const uint32_t m = bf16x2_max(m2, m2 >> 16) & 0xFFFFu;
+          s_vmax[j - v0] = (uint16_t)m;
+          gk[u >> 1] = max(gk[u >> 1], bf16_order_key(m));
         }
+      }
+      const int g = (base - v0) / kGroup;
+      const uint32_t k0 = __reduce_max_sync(DC_FULL_MASK, gk[0]);
+      const uint32_t k1 = __reduce_max_sync(DC_FULL_MASK, gk[1]);
+      if (lane == 0) {  // the second group may start the next warp's range
+        if (g < ng) s_gkey[g] = (uint16_t)k0;
+        if (g + 1 < ng && base + kGroup < w1) s_gkey[g + 1] = (uint16_t)k1;
       }
     };
     if (w0 < w1) load_vecs(a, rowp, w0, w1, lane, pol);
@@ -348,37 +367,33 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
   __syncthreads();
 
   // ---------------------------------------------------------------- pass 2: bound
-  const int ng = (nv + kGroup - 1) / kGroup;
-  for (int g = tid; g < ng; g += kThreads) {
-    const int e1 = min((g + 1) * kGroup, nv);
-    uint32_t m2 = 0xFF80FF80u;
-    int e = g * kGroup;
-    for (; e + 8 <= e1; e += 8) {  // 8 maxima per 16-byte read
-      const uint4 q = *reinterpret_cast<const uint4 *>(s_vmax + e);
-      m2 = bf16x2_max(m2, bf16x2_max(bf16x2_max(q.x, q.y), bf16x2_max(q.z, q.w)));
-    }
-    for (; e < e1; ++e) m2 = bf16x2_max(m2, 0xFF800000u | s_vmax[e]);
-    s_gkey[g] = (uint16_t)max(bf16_order_key(m2 & 0xFFFFu), bf16_order_key(m2 >> 16));
-  }
-  __syncthreads();
-  // K-th largest group key: each warp sorts its share (bitonic, 32 at a time)
-  // and keeps its best K; warp 0 merges the 8 lists.  Fewer than K groups (a
-  // tiny segment) leave the bound at 0: every vector is listed.
+  // K-th largest group key: each warp sorts its share of the group keys
+  // (bitonic, 32 at a time; key | inverted group index, unique) and keeps its
+  // best K; three rounds of pairwise merges give the CTA's best K.  Fewer than
+  // K groups (a tiny segment) leave the bound at 0: every vector is listed.
   {
-    u64 best = 0ull;  // group keys widened to u64 (unique: group index below)
+    uint32_t best = 0u;
     for (int g0 = warp * 32; g0 < ng; g0 += kWarps * 32) {
       const int g = g0 + lane;
-      const u64 k = g < ng ? (((u64)s_gkey[g] + 1ull) << 32) | (uint32_t)(0xFFFFFFFFu - g) : 0ull;
+      const uint32_t k = g < ng ? ((uint32_t)s_gkey[g] << 16) | (0xFFFFu - (uint32_t)g) : 0u;
       best = warp_merge_topk<K>(best, warp_sort32_desc(k, lane), lane);
     }
-    if (lane < K) s_lists[warp * K + lane] = best;
+    if (lane < K) s_glists[warp * K + lane] = best;
   }
   __syncthreads();
-  if (warp == 0) {
-    u64 acc = lane < K ? s_lists[lane] : 0ull;
-    for (int w = 1; w < kWarps; ++w) acc = warp_merge_topk<K>(acc, lane < K ? s_lists[w * K + lane] : 0ull, lane);
-    const u64 kth = shfl_u64(acc, K - 1);
-    if (lane == 0) s_tkey = ng >= K && kth ? (uint32_t)(kth >> 32) - 1u : 0u;
+#pragma unroll
+  for (int span = 1; span < kWarps; span <<= 1) {
+    if ((warp & (2 * span - 1)) == 0) {
+      const uint32_t a = lane < K ? s_glists[warp * K + lane] : 0u;
+      const uint32_t b = lane < K ? s_glists[(warp + span) * K + lane] : 0u;
+      const uint32_t m = warp_merge_topk<K>(a, b, lane);
+      if (lane < K) s_glists[warp * K + lane] = m;
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    const uint32_t kth = s_glists[K - 1];
+    s_tkey = ng >= K && kth ? (kth >> 16) : 0u;
   }
   __syncthreads();
   const uint32_t tkey = s_tkey;
