@@ -241,7 +241,7 @@ int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs 
   if (overlap) DC_TRY(cudaEventRecord(h->ev_fork, st));
   // step 1: candidate pools
   DC_TRY(clk.done(dc::launch_topk(K, logits, in->logits_slot_stride, cfg.slots, N, V, plan,
-                                  ws.part, ws.row_count, ids, vals, st, E, d)));
+                                  ws.part, ws.row_count, ids, vals, st)));
   if (cfg.variant == 0) {
     // steps 2-3: slot projections (W_ctx, W_pair halves) and per-slot / per-pair terms
     cudaStream_t ss = st;

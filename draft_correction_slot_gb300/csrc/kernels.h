@@ -14,9 +14,7 @@ namespace dc {
 // `chunk_vecs` 16-byte vectors, one CTA per (row, segment).  With several
 // segments, every CTA publishes its best K to `part` (rows * nchunks * K
 // packed keys) and the last CTA of the row, counted in `row_count` (rows
-// entries, zero between calls), merges them.  When `emb` ([V][d] bf16) is
-// given, the final CTA of each row also prefetches the K chosen embedding
-// rows into L2 for the candidate projection that follows.
+// entries, zero between calls), merges them.
 struct TopkPlan {
   int nchunks;     // segments per row
   int chunk_vecs;  // 16-byte vectors per segment
@@ -31,8 +29,7 @@ int topk_max_segments(int V);
 int topk_occupancy(int K);  // resident top-K CTAs per SM
 cudaError_t launch_topk(int K, const uint16_t *logits, int64_t stride, int slots, int N, int V,
                         const TopkPlan &plan, unsigned long long *part, unsigned *row_count,
-                        int32_t *ids, float *vals, cudaStream_t st, const uint16_t *emb = nullptr,
-                        int d = 0);
+                        int32_t *ids, float *vals, cudaStream_t st);
 
 // ---------------------------------------------------------------- projections
 // C[m][o] = sum_k A_m[k] * W[o][k] with A_m a bf16 row of length d.  Row

@@ -83,8 +83,6 @@ __device__ __forceinline__ u64 shfl_xor_key(u64 v, int m) {
   uint32_t hi = __shfl_xor_sync(DC_FULL_MASK, (uint32_t)(v >> 32), m);
   return ((u64)hi << 32) | lo;
 }
-__device__ __forceinline__ uint32_t shfl_xor_key(uint32_t v, int m) { return __shfl_xor_sync(DC_FULL_MASK, v, m); }
-__device__ __forceinline__ uint32_t shfl_key(uint32_t v, int src) { return __shfl_sync(DC_FULL_MASK, v, src); }
 __device__ __forceinline__ u64 shfl_key(u64 v, int src) { return shfl_u64(v, src); }
 
 // Bitonic sort of one key per lane, descending over the 32 lanes.
@@ -123,28 +121,23 @@ __device__ __forceinline__ uint32_t bf16_from_key(uint32_t key) {
   return (key & 0x8000u) ? (key & 0x7FFFu) : (~key & 0xFFFFu);
 }
 
-// Logits are read exactly once: mark them evict-first in L2 so they do not
-// displace the candidate embedding rows prefetched for the next step.
-__device__ __forceinline__ uint64_t evict_first_policy() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-
-__device__ __forceinline__ uint4 ld_stream_ef(const void *ptr, uint64_t pol) {
+// Logits are read once by the stream and again, for the few vectors that
+// reach the bound, right after it: normal L2 priority keeps those re-reads
+// in L2; L1 is bypassed.
+__device__ __forceinline__ uint4 ld_stream(const void *ptr) {
   uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(ptr), "l"(pol));
+               : "l"(ptr));
   return v;
 }
 
 __device__ __forceinline__ void load_vecs(uint4 (&v)[kU], const uint16_t *rowp, int base, int end,
-                                          int lane, uint64_t pol) {
+                                          int lane) {
 #pragma unroll
   for (int u = 0; u < kU; ++u) {
     const int j = base + lane + 32 * u;
-    if (j < end) v[u] = ld_stream_ef(rowp + (int64_t)j * 8, pol);
+    if (j < end) v[u] = ld_stream(rowp + (int64_t)j * 8);
     else v[u] = make_uint4(kNegInf2, kNegInf2, kNegInf2, kNegInf2);
   }
 }
@@ -154,11 +147,10 @@ __device__ __forceinline__ void load_vecs(uint4 (&v)[kU], const uint16_t *rowp, 
 // bound (the CTA-shared bound, never below `floor_key`, or its own K-th).
 template <int K>
 __device__ __forceinline__ u64 stream_fallback(const uint16_t *rowp, int w0, int w1, uint32_t floor_key,
-                                               u64 *s_cta_bound, uint32_t *s_bufw, int lane,
-                                               uint64_t pol) {
+                                               u64 *s_cta_bound, uint32_t *s_bufw, int lane) {
   u64 list = 0ull, kth = 0ull;
   uint4 cur[kU], nxt[kU];
-  if (w0 < w1) load_vecs(cur, rowp, w0, w1, lane, pol);
+  if (w0 < w1) load_vecs(cur, rowp, w0, w1, lane);
   // one iteration: kU vectors per lane, starting at vector `base`
   auto process = [&](const uint4 (&v)[kU], int base) {
       uint32_t vm2[kU];
@@ -277,22 +269,63 @@ __device__ __forceinline__ u64 stream_fallback(const uint16_t *rowp, int w0, int
   // ping-pong between two register buffers; the next loads are always in flight
   for (int base = w0; base < w1; base += 2 * kStep) {
     prefetch(base + (kPrefetchAhead + 1) * kStep);
-    if (base + kStep < w1) load_vecs(nxt, rowp, base + kStep, w1, lane, pol);
+    if (base + kStep < w1) load_vecs(nxt, rowp, base + kStep, w1, lane);
     process(cur, base);
     if (base + kStep >= w1) break;
     prefetch(base + (kPrefetchAhead + 2) * kStep);
-    if (base + 2 * kStep < w1) load_vecs(cur, rowp, base + 2 * kStep, w1, lane, pol);
+    if (base + 2 * kStep < w1) load_vecs(cur, rowp, base + 2 * kStep, w1, lane);
     process(nxt, base + kStep);
   }
   return list;
+}
+
+// One warp: the digit d of a 256-bin histogram (bins scanned from 255 down)
+// whose bin holds the rank-th largest key (rank >= 1), and the count of keys
+// in the bins above it.  *digit = -1 when the histogram holds fewer than rank
+// keys.  Lane l owns bins 255 - 8l ... 248 - 8l.
+__device__ __forceinline__ void radix_digit(const int *hist, int rank, int lane, int *digit, int *above) {
+  int c[8], sum = 0;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    c[q] = hist[255 - 8 * lane - q];
+    sum += c[q];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(DC_FULL_MASK, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const int excl = incl - sum;  // keys in the bins above this lane's
+  int d = -1, ab = 0;
+  if (excl < rank && rank <= incl) {
+    int acc = excl;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (d < 0 && acc + c[q] >= rank) {
+        d = 255 - 8 * lane - q;
+        ab = acc;
+      }
+      acc += c[q];
+    }
+  }
+  const unsigned m = __ballot_sync(DC_FULL_MASK, d >= 0);
+  if (m) {
+    const int src = __ffs(m) - 1;
+    d = __shfl_sync(DC_FULL_MASK, d, src);
+    ab = __shfl_sync(DC_FULL_MASK, ab, src);
+  }
+  if (lane == 0) {
+    *digit = m ? d : -1;
+    *above = ab;
+  }
 }
 
 template <int K>
 __global__ void __launch_bounds__(kThreads, 4)
 k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, int V, int nseg,
        int seg_vecs, u64 *__restrict__ part, unsigned *__restrict__ row_count,
-       int32_t *__restrict__ out_ids, float *__restrict__ out_val, const uint16_t *__restrict__ emb,
-       int emb_row_bytes) {
+       int32_t *__restrict__ out_ids, float *__restrict__ out_val) {
   // s_vmax (pass 1-2: per-vector maxima, bf16 bits), s_keys (pass 3:
   // candidate elements) and the fallback's per-warp candidate buffers share
   // storage; each use ends at a barrier before the next begins
@@ -301,9 +334,10 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
   uint16_t *s_vmax = reinterpret_cast<uint16_t *>(s_raw);
   u64 *s_keys = reinterpret_cast<u64 *>(s_raw);
   __shared__ uint16_t s_gkey[kMaxGroups];   // order key of each group's maximum
-  __shared__ int s_cand[kCandGroups];       // candidate groups, in order
+  __shared__ int s_cand[kCandGroups];       // candidate groups
   __shared__ u64 s_lists[kWarps * K];
-  __shared__ uint32_t s_glists[kWarps * K];  // per-warp best group keys
+  __shared__ int s_hist[2][256];  // radix-select histograms of the group keys
+  __shared__ int s_digit, s_above;
   __shared__ u64 s_top[K];
   __shared__ u64 s_cta_bound;
   __shared__ int s_ncand, s_nkeys, s_flag;
@@ -322,8 +356,8 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
   const int per_warp = ((nv + kWarps - 1) / kWarps + kGroup - 1) / kGroup * kGroup;
   const int ng = (nv + kGroup - 1) / kGroup;
   const int w0 = v0 + min(warp * per_warp, nv), w1 = v0 + min((warp + 1) * per_warp, nv);
-  const uint64_t pol = evict_first_policy();
   if (tid < K) s_top[tid] = 0ull;
+  for (int e = tid; e < 2 * 256; e += kThreads) (&s_hist[0][0])[e] = 0;
   if (tid == 0) {
     s_ncand = 0;
     s_nkeys = 0;
@@ -355,61 +389,45 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
         if (g + 1 < ng && base + kGroup < w1) s_gkey[g + 1] = (uint16_t)k1;
       }
     };
-    if (w0 < w1) load_vecs(a, rowp, w0, w1, lane, pol);
+    if (w0 < w1) load_vecs(a, rowp, w0, w1, lane);
     for (int base = w0; base < w1; base += 2 * kStep) {
-      if (base + kStep < w1) load_vecs(b, rowp, base + kStep, w1, lane, pol);
+      if (base + kStep < w1) load_vecs(b, rowp, base + kStep, w1, lane);
       store(a, base);
       if (base + kStep >= w1) break;
-      if (base + 2 * kStep < w1) load_vecs(a, rowp, base + 2 * kStep, w1, lane, pol);
+      if (base + 2 * kStep < w1) load_vecs(a, rowp, base + 2 * kStep, w1, lane);
       store(b, base + kStep);
     }
   }
   __syncthreads();
 
   // ---------------------------------------------------------------- pass 2: bound
-  // K-th largest group key: each warp sorts its share of the group keys
-  // (bitonic, 32 at a time; key | inverted group index, unique) and keeps its
-  // best K; three rounds of pairwise merges give the CTA's best K.  Fewer than
-  // K groups (a tiny segment) leave the bound at 0: every vector is listed.
-  {
-    uint32_t best = 0u;
-    for (int g0 = warp * 32; g0 < ng; g0 += kWarps * 32) {
-      const int g = g0 + lane;
-      const uint32_t k = g < ng ? ((uint32_t)s_gkey[g] << 16) | (0xFFFFu - (uint32_t)g) : 0u;
-      best = warp_merge_topk<K>(best, warp_sort32_desc(k, lane), lane);
-    }
-    if (lane < K) s_glists[warp * K + lane] = best;
-  }
+  // The bound is the K-th largest group key, found by a two-digit radix
+  // select over the (16-bit) group keys: a histogram of the high bytes, the
+  // bin holding the K-th largest, then a histogram of the low bytes within
+  // it.  Fewer than K groups (a tiny segment) leave the bound at 0: every
+  // vector is listed.
+  for (int g = tid; g < ng; g += kThreads) atomicAdd(&s_hist[0][s_gkey[g] >> 8], 1);
   __syncthreads();
-#pragma unroll
-  for (int span = 1; span < kWarps; span <<= 1) {
-    if ((warp & (2 * span - 1)) == 0) {
-      const uint32_t a = lane < K ? s_glists[warp * K + lane] : 0u;
-      const uint32_t b = lane < K ? s_glists[(warp + span) * K + lane] : 0u;
-      const uint32_t m = warp_merge_topk<K>(a, b, lane);
-      if (lane < K) s_glists[warp * K + lane] = m;
-    }
-    __syncthreads();
-  }
-  if (tid == 0) {
-    const uint32_t kth = s_glists[K - 1];
-    s_tkey = ng >= K && kth ? (kth >> 16) : 0u;
+  if (warp == 0) radix_digit(s_hist[0], K, lane, &s_digit, &s_above);
+  __syncthreads();
+  const int hb = s_digit;
+  if (hb >= 0)
+    for (int g = tid; g < ng; g += kThreads)
+      if ((s_gkey[g] >> 8) == hb) atomicAdd(&s_hist[1][s_gkey[g] & 0xFF], 1);
+  __syncthreads();
+  if (warp == 0) {
+    int lb = -1, dummy = 0;
+    if (hb >= 0) radix_digit(s_hist[1], K - s_above, lane, &lb, &dummy);
+    if (lane == 0) s_tkey = (hb >= 0 && lb >= 0) ? ((uint32_t)hb << 8) | (uint32_t)lb : 0u;
   }
   __syncthreads();
   const uint32_t tkey = s_tkey;
-  // candidate groups (maximum >= bound), in order
-  if (warp == 0) {
-    int base = 0;
-    for (int g0 = 0; g0 < ng; g0 += 32) {
-      const int g = g0 + lane;
-      const bool hit = g < ng && s_gkey[g] >= tkey;
-      const unsigned m = __ballot_sync(DC_FULL_MASK, hit);
-      const int pos = base + __popc(m & ((1u << lane) - 1u));
-      if (hit && pos < kCandGroups) s_cand[pos] = g;
-      base += __popc(m);
+  // candidate groups (maximum >= bound), in any order
+  for (int g = tid; g < ng; g += kThreads)
+    if (s_gkey[g] >= tkey) {
+      const int pos = atomicAdd(&s_ncand, 1);
+      if (pos < kCandGroups) s_cand[pos] = g;
     }
-    if (lane == 0) s_ncand = base;
-  }
   __syncthreads();
   const int ncg = s_ncand;
   // each warp takes candidate groups; lane l checks maxima l and l+32 of each.
@@ -452,7 +470,7 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
     uint4 q[kMaxHitsPerLane];
 #pragma unroll
     for (int h = 0; h < kMaxHitsPerLane; ++h)
-      if (h < nhit) q[h] = ld_stream_ef(rowp + (int64_t)hj[h] * 8, pol);
+      if (h < nhit) q[h] = ld_stream(rowp + (int64_t)hj[h] * 8);
     __syncthreads();  // s_vmax is overwritten by the keys below
 #pragma unroll
     for (int h = 0; h < kMaxHitsPerLane; ++h) {
@@ -493,7 +511,7 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
     __syncthreads();  // s_vmax is reused as the candidate buffers below
     const uint32_t floor_key = tkey;
     u64 list = stream_fallback<K>(rowp, w0, w1, floor_key, &s_cta_bound,
-                                  s_raw + warp * (kStep * 8), lane, pol);
+                                  s_raw + warp * (kStep * 8), lane);
     // the scalar tail (V % 8 elements) belongs to the last warp
     if (has_tail && warp == kWarps - 1) {
       u64 kth = shfl_u64(list, K - 1);
@@ -549,12 +567,6 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
     const uint32_t id = 0xFFFFFFFFu - (uint32_t)(x & 0xFFFFFFFFull);
     out_ids[(int64_t)row * K + tid] = (int32_t)id;
     out_val[(int64_t)row * K + tid] = order_key_to_float((uint32_t)(x >> 32));
-    // start fetching this candidate's embedding row into L2 for the projection
-    if (emb && x != 0ull)
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
-                       reinterpret_cast<const char *>(emb) + (int64_t)id * emb_row_bytes),
-                   "r"((uint32_t)emb_row_bytes)
-                   : "memory");
   }
 }
 
@@ -614,22 +626,22 @@ int topk_occupancy(int K) {
 
 cudaError_t launch_topk(int K, const uint16_t *logits, int64_t stride, int slots, int N, int V,
                         const TopkPlan &plan, unsigned long long *part, unsigned *row_count,
-                        int32_t *ids, float *vals, cudaStream_t st, const uint16_t *emb, int d) {
+                        int32_t *ids, float *vals, cudaStream_t st) {
   const int B = slots - 1;
   if (N == 0) return cudaSuccess;
   dim3 grid(N * B, plan.nchunks);
   switch (K) {
     case 8:
       k_topk<8><<<grid, kThreads, 0, st>>>(logits, stride, slots, B, V, plan.nchunks, plan.chunk_vecs,
-                                           part, row_count, ids, vals, emb, d * 2);
+                                           part, row_count, ids, vals);
       break;
     case 16:
       k_topk<16><<<grid, kThreads, 0, st>>>(logits, stride, slots, B, V, plan.nchunks, plan.chunk_vecs,
-                                            part, row_count, ids, vals, emb, d * 2);
+                                            part, row_count, ids, vals);
       break;
     case 32:
       k_topk<32><<<grid, kThreads, 0, st>>>(logits, stride, slots, B, V, plan.nchunks, plan.chunk_vecs,
-                                            part, row_count, ids, vals, emb, d * 2);
+                                            part, row_count, ids, vals);
       break;
     default:
       return cudaErrorInvalidValue;
