@@ -78,8 +78,7 @@ def stage_model(w, pk):
         "slot_post": ("alu", "TFLOP/s", 2 * N * (B * r * r + (B - 1) * r * H), alu_peak),
         "cand_proj": ("hbm", "GB/s", N * B * K * d * 2, pk["hbm_gbs"]),
         "cand_post": ("alu", "TFLOP/s", 2 * N * B * K * (r * r + 2 * r * H), alu_peak),
-        "pair_score": ("alu", "TFLOP/s", 2 * N * (B - 1) * K * K * H, alu_peak),
-        "walk_verify": ("latency", "us", 0, None),
+        "pair_walk": ("alu", "TFLOP/s", 2 * N * (B - 1) * K * K * H, alu_peak),
     }
 
 

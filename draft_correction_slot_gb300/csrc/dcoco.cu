@@ -30,6 +30,7 @@ struct Workspace {
   int32_t *choice = nullptr;   // [N*B]
   float *margin = nullptr;     // [N*(B-1)]
   int *err = nullptr;          // device status word
+  unsigned *req_count = nullptr;  // finished pairs per request (zero between calls)
   // host staging (dcoco_correct_host)
   uint16_t *st_logits = nullptr;  // [N][slots][st_stride]
   int64_t st_stride = 0;
@@ -45,7 +46,7 @@ namespace {
 constexpr int kMaxStages = 8;
 constexpr int kMaxTimedCalls = 1024;
 const char *const kStageNames[2][kMaxStages] = {
-    {"topk", "slot_proj", "slot_post", "cand_proj", "cand_post", "pair_score", "walk_verify", nullptr},
+    {"topk", "slot_proj", "slot_post", "cand_proj", "cand_post", "pair_walk", nullptr, nullptr},
     {"topk", "slot_proj", "cand_proj", "cos_post", "cos_score", "walk_verify", nullptr, nullptr}};
 int stage_count(int variant) {
   int n = 0;
@@ -142,6 +143,7 @@ void carve_workspace(Carver &c, const dcoco_config &cfg, int B, int topk_segment
   ws.choice = c.take<int32_t>(rows);
   ws.margin = c.take<float>(N * (B - 1));
   ws.err = c.take<int>(1);
+  ws.req_count = c.take<unsigned>(N);
   if (cfg.host_staging) {
     ws.st_stride = ((int64_t)cfg.vocab + 7) & ~int64_t(7);
     ws.st_logits = c.take<uint16_t>(N * cfg.slots * (size_t)ws.st_stride);
@@ -262,9 +264,13 @@ int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs 
     if (overlap) DC_TRY(cudaStreamWaitEvent(st, h->ev_join, 0));
     DC_TRY(clk.done(dc::launch_cand_mlp_tc(w->mlp_maps, h->cand_io, ws.Gf, vals, w->mlp, K, cands,
                                            cfg.ln_eps, ws.err, st)));
-    // step 4: all (B-1) K^2 transition scores
-    DC_TRY(clk.done(dc::launch_pair_score(K, ws.U, ws.V, ws.P, vals, w->mlp.w2, w->mlp.b2, N, B,
-                                          scores, st)));
+    // steps 4-5: all (B-1) K^2 transition scores, then each request's walk
+    // and verify in its last block
+    const dc::WalkArgs wk{ids, in->target_tokens, out->tokens, choice,
+                          in->target_tokens ? out->accept_len : nullptr, margin, ws.req_count};
+    DC_TRY(clk.done(dc::launch_pair_score_walk(K, ws.U, ws.V, ws.P, vals, w->mlp.w2, w->mlp.b2, N, B,
+                                               scores, wk, st)));
+    return DCOCO_OK;
   } else {
     DC_TRY(clk.done(dc::launch_proj_tc(1, 128, hidden, w->map_slot_hi, w->map_slot_lo, nullptr, cfg.slots, B,
                                        rows, d, V, 2 * kR, h->splits_slot, ws.slot_proj,

@@ -105,10 +105,23 @@ cudaError_t launch_cand_mlp_tc(const MlpMaps &maps, const CandIoMaps &io, const 
                                const float *topk_val, const MlpWeightsDev &w, int K, int M, float eps,
                                int *err, cudaStream_t st);
 
-// S[n,p,a,b] = l_{p+1}(b) + b2 + sum_j w2_j GELU(P_pj + U_{p,a,j} + V_{p+1,b,j}).
-cudaError_t launch_pair_score(int K, const float *U, const float *V, const float *P,
-                              const float *topk_val, const float *w2, const float *b2, int N, int B,
-                              float *scores, cudaStream_t st);
+// Step 5 outputs and state for a launch that ends with the walk: per-request
+// arrays as in launch_walk_verify, and req_count (N entries, zero between
+// calls) counting each request's finished pairs.
+struct WalkArgs {
+  const int32_t *topk_ids;
+  const int32_t *target;  // or null
+  int32_t *tokens, *choice, *accept_len;
+  float *margin;
+  unsigned *req_count;
+};
+
+// S[n,p,a,b] = l_{p+1}(b) + b2 + sum_j w2_j GELU(P_pj + U_{p,a,j} + V_{p+1,b,j}),
+// then, in the last block of each request, the walk and verify of
+// launch_walk_verify.
+cudaError_t launch_pair_score_walk(int K, const float *U, const float *V, const float *P,
+                                   const float *topk_val, const float *w2, const float *b2, int N, int B,
+                                   float *scores, const WalkArgs &wk, cudaStream_t st);
 
 // ---------------------------------------------------------------- cosine variant
 // y = cand_io[m] + slot_io[slot(m)]; out/in halves L2-normalised -> O, I [M][r].

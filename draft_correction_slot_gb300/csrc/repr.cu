@@ -19,6 +19,7 @@
 // the square root.
 #include "common.cuh"
 #include "kernels.h"
+#include "walk.cuh"
 
 namespace dc {
 namespace {
@@ -243,7 +244,9 @@ struct PairGeom {
   // row stride (floats, even): the 64-bit reads of a half-warp hit distinct banks
   static constexpr int LD = K == 32 ? H + 2 : H + 4;
   static constexpr int RED = K * K + 1;            // partial-sum row stride
-  static constexpr size_t smem_floats = 2 * (size_t)K * LD + H + 2 * K + (size_t)NS * RED;
+  static constexpr size_t pair_floats = 2 * (size_t)K * LD + H + 2 * K + (size_t)NS * RED;
+  // the walk reuses the first 2 kWalkMaxRows words
+  static constexpr size_t smem_floats = pair_floats > 2 * (size_t)kWalkMaxRows ? pair_floats : 2 * (size_t)kWalkMaxRows;
 };
 
 template <int K>
@@ -251,7 +254,7 @@ __global__ void __launch_bounds__(256)
 k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
              const float *__restrict__ P, const float *__restrict__ topk_val,
              const float *__restrict__ w2, const float *__restrict__ b2, int B,
-             float *__restrict__ scores) {
+             float *__restrict__ scores, WalkArgs wk) {
   using G = PairGeom<K>;
   constexpr float kInvSqrt2 = 0.70710678118654752440f;
   extern __shared__ float sm[];
@@ -355,6 +358,27 @@ k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
     const int aa = e / K, bb = e - aa * K;
     scores[(int64_t)np * K * K + e] = topk_val[cb + bb] + bias + (dab[aa] + dab[K + bb]) + sum;
   }
+
+  // ---------------------------------------------------------------- step 5
+  // The last block of request n to finish its pair (counted in req_count,
+  // zero between calls) walks the request's scores.
+  __shared__ int s_last;
+  __shared__ int s_choice[32];
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(&wk.req_count[n], 1u) == (unsigned)(B - 2);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  int *s_best = reinterpret_cast<int *>(sm);
+  float *s_gap = sm + kWalkMaxRows;
+  const int64_t slot0 = (int64_t)n * B;
+  walk_verify_request<K>(scores + (int64_t)n * (B - 1) * K * K, wk.topk_ids + slot0 * K,
+                         wk.target ? wk.target + slot0 : nullptr, B, wk.tokens + slot0,
+                         wk.choice ? wk.choice + slot0 : nullptr,
+                         wk.margin ? wk.margin + (int64_t)n * (B - 1) : nullptr,
+                         wk.accept_len ? wk.accept_len + n : nullptr, s_best, s_gap, s_choice);
+  if (tid == 0) wk.req_count[n] = 0u;  // ready for the next call
 }
 
 // ---------------------------------------------------------------- cosine variant
@@ -434,23 +458,23 @@ cudaError_t launch_cand_post(int K, const float *cand_proj, const float *topk_va
 template <int K>
 static cudaError_t pair_score_k(const float *U, const float *V, const float *P, const float *tv,
                                 const float *w2, const float *b2, int N, int B, float *scores,
-                                cudaStream_t st) {
+                                const WalkArgs &wk, cudaStream_t st) {
   const size_t smem = PairGeom<K>::smem_floats * sizeof(float);
   cudaError_t e = cudaFuncSetAttribute(k_pair_score<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  k_pair_score<K><<<N * (B - 1), 256, smem, st>>>(U, V, P, tv, w2, b2, B, scores);
+  k_pair_score<K><<<N * (B - 1), 256, smem, st>>>(U, V, P, tv, w2, b2, B, scores, wk);
   return cudaGetLastError();
 }
 
-cudaError_t launch_pair_score(int K, const float *U, const float *V, const float *P,
-                              const float *topk_val, const float *w2, const float *b2, int N, int B,
-                              float *scores, cudaStream_t st) {
+cudaError_t launch_pair_score_walk(int K, const float *U, const float *V, const float *P,
+                                   const float *topk_val, const float *w2, const float *b2, int N, int B,
+                                   float *scores, const WalkArgs &wk, cudaStream_t st) {
   if (N == 0) return cudaSuccess;
   switch (K) {
-    case 8: return pair_score_k<8>(U, V, P, topk_val, w2, b2, N, B, scores, st);
-    case 16: return pair_score_k<16>(U, V, P, topk_val, w2, b2, N, B, scores, st);
-    case 32: return pair_score_k<32>(U, V, P, topk_val, w2, b2, N, B, scores, st);
+    case 8: return pair_score_k<8>(U, V, P, topk_val, w2, b2, N, B, scores, wk, st);
+    case 16: return pair_score_k<16>(U, V, P, topk_val, w2, b2, N, B, scores, wk, st);
+    case 32: return pair_score_k<32>(U, V, P, topk_val, w2, b2, N, B, scores, wk, st);
     default: return cudaErrorInvalidValue;
   }
 }
