@@ -61,9 +61,11 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// GELU, erf form: x * Phi(x) = x/2 (1 + erf(x / sqrt 2)).
-__device__ __forceinline__ float gelu_erf(float x) {
-  return 0.5f * x * (1.0f + erff(x * 0.70710678118654752440f));
-}
+// Programmatic dependent launch.  pdl_trigger lets the next kernel in the
+// stream be scheduled; pdl_wait blocks until the previous kernel has finished
+// and its memory operations are visible (a no-op without a programmatic
+// dependency).
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 }  // namespace dc

@@ -243,7 +243,7 @@ int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs 
   if (overlap) DC_TRY(cudaEventRecord(h->ev_fork, st));
   // step 1: candidate pools
   DC_TRY(clk.done(dc::launch_topk(K, logits, in->logits_slot_stride, cfg.slots, N, V, plan,
-                                  ws.part, ws.row_count, ids, vals, st)));
+                                  ws.part, ws.row_count, ids, vals, st, false)));
   if (cfg.variant == 0) {
     // steps 2-3: slot projections (W_ctx, W_pair halves) and per-slot / per-pair terms
     cudaStream_t ss = st;
@@ -288,47 +288,31 @@ int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs 
   return DCOCO_OK;
 }
 
-// Host-side packing of the fp32 weights into the device layout.
-void pack_mlp(const dcoco_weight_ptrs &w, int d, std::vector<float> &buf, size_t off[16]) {
-  (void)d;
+// Host-side packing of the fp32 vectors of the MLP (the 128-deep maps go to
+// the device as bf16 hi / lo halves, see dcoco_weights_create).
+void pack_mlp(const dcoco_weight_ptrs &w, std::vector<float> &buf, size_t off[8]) {
   const int r = kR, H = kH, in = 3 * kR + 2;
   size_t o = 0;
   auto take = [&](size_t n) { size_t at = (o + 63) & ~size_t(63); o = at + n; return at; };
-  off[0] = take(r * r);  // wfb_t
-  off[1] = take(r * r);  // wfg_t
-  off[2] = take(r);      // gamma
-  off[3] = take(r);      // beta
-  off[4] = take(r * H);  // w1s_t
-  off[5] = take(r * H);  // w1a_t
-  off[6] = take(r * H);  // w1b_t
-  off[7] = take(H);      // w_la
-  off[8] = take(H);      // w_lb
-  off[9] = take(H);      // b1
-  off[10] = take(H);     // w2
-  off[11] = take(1);     // b2
-  off[12] = o;
+  off[0] = take(r);      // gamma
+  off[1] = take(r);      // beta
+  off[2] = take(H);      // w_la = W1[:, 3r]
+  off[3] = take(H);      // w_lb = W1[:, 3r+1]
+  off[4] = take(H);      // b1
+  off[5] = take(H);      // w2
+  off[6] = take(1);      // b2
   buf.assign(o, 0.f);
-  for (int oo = 0; oo < r; ++oo)
-    for (int k = 0; k < r; ++k) {
-      buf[off[0] + (size_t)k * r + oo] = w.w_fuse[(size_t)oo * 2 * r + k];
-      buf[off[1] + (size_t)k * r + oo] = w.w_fuse[(size_t)oo * 2 * r + r + k];
-    }
   for (int k = 0; k < r; ++k) {
-    buf[off[2] + k] = w.ln_gamma[k];
-    buf[off[3] + k] = w.ln_beta[k];
+    buf[off[0] + k] = w.ln_gamma[k];
+    buf[off[1] + k] = w.ln_beta[k];
   }
   for (int j = 0; j < H; ++j) {
-    for (int k = 0; k < r; ++k) {
-      buf[off[4] + (size_t)k * H + j] = w.w1[(size_t)j * in + k];
-      buf[off[5] + (size_t)k * H + j] = w.w1[(size_t)j * in + r + k];
-      buf[off[6] + (size_t)k * H + j] = w.w1[(size_t)j * in + 2 * r + k];
-    }
-    buf[off[7] + j] = w.w1[(size_t)j * in + 3 * r];
-    buf[off[8] + j] = w.w1[(size_t)j * in + 3 * r + 1];
-    buf[off[9] + j] = w.b1[j];
-    buf[off[10] + j] = w.w2[j];
+    buf[off[2] + j] = w.w1[(size_t)j * in + 3 * r];
+    buf[off[3] + j] = w.w1[(size_t)j * in + 3 * r + 1];
+    buf[off[4] + j] = w.b1[j];
+    buf[off[5] + j] = w.w2[j];
   }
-  buf[off[11]] = w.b2[0];
+  buf[off[6]] = w.b2[0];
 }
 
 }  // namespace
@@ -493,12 +477,12 @@ int dcoco_weights_create(dcoco_handle *h, const dcoco_weight_ptrs *wp, void *str
   }
   const size_t n_proj = proj.size();
   std::vector<float> mlp;
-  size_t off[16] = {};
+  size_t off[8] = {};
   if (cfg.variant == 0) {
     dcoco_weight_ptrs hw = *wp;
     hw.w_fuse = w_fuse.data(); hw.ln_gamma = gam.data(); hw.ln_beta = bet.data();
     hw.w1 = w1.data(); hw.b1 = b1.data(); hw.w2 = w2.data(); hw.b2 = b2.data();
-    pack_mlp(hw, d, mlp, off);
+    pack_mlp(hw, mlp, off);
   }
   const size_t proj_bytes = ((n_proj * sizeof(uint16_t)) + 255) & ~size_t(255);
   const size_t total = proj_bytes + mlp.size() * sizeof(float) + 256;
@@ -559,10 +543,8 @@ int dcoco_weights_create(dcoco_handle *h, const dcoco_weight_ptrs *wp, void *str
   }
   if (cfg.variant == 0) {
     dc::MlpWeightsDev &m = w->mlp;
-    m.wfb_t = dmlp + off[0]; m.wfg_t = dmlp + off[1]; m.gamma = dmlp + off[2]; m.beta = dmlp + off[3];
-    m.w1s_t = dmlp + off[4]; m.w1a_t = dmlp + off[5]; m.w1b_t = dmlp + off[6];
-    m.w_la = dmlp + off[7]; m.w_lb = dmlp + off[8]; m.b1 = dmlp + off[9]; m.w2 = dmlp + off[10];
-    m.b2 = dmlp + off[11];
+    m.gamma = dmlp + off[0]; m.beta = dmlp + off[1]; m.w_la = dmlp + off[2]; m.w_lb = dmlp + off[3];
+    m.b1 = dmlp + off[4]; m.w2 = dmlp + off[5]; m.b2 = dmlp + off[6];
   }
   *out = w;
   return DCOCO_OK;
@@ -641,7 +623,7 @@ int dcoco_topk(dcoco_handle *h, int batch, const void *logits, int64_t stride, i
   const dc::TopkPlan plan = dc::topk_plan(h->cfg.vocab, batch * h->B, h->topk_wave);
   return cuda_status(dc::launch_topk(h->cfg.topk, static_cast<const uint16_t *>(logits), stride,
                                      h->cfg.slots, batch, h->cfg.vocab, plan, h->ws.part,
-                                     h->ws.row_count, topk_ids, topk_val, st));
+                                     h->ws.row_count, topk_ids, topk_val, st, true));
 }
 
 int dcoco_get_device_status(dcoco_handle *h) {

@@ -14,7 +14,9 @@ namespace dc {
 // `chunk_vecs` 16-byte vectors, one CTA per (row, segment).  With several
 // segments, every CTA publishes its best K to `part` (rows * nchunks * K
 // packed keys) and the last CTA of the row, counted in `row_count` (rows
-// entries, zero between calls), merges them.
+// entries, zero between calls), merges them.  With `pdl` the launch may
+// overlap the end of the previous kernel in the stream (the kernel waits for
+// it before its first global write).
 struct TopkPlan {
   int nchunks;     // segments per row
   int chunk_vecs;  // 16-byte vectors per segment
@@ -29,7 +31,7 @@ int topk_max_segments(int V);
 int topk_occupancy(int K);  // resident top-K CTAs per SM
 cudaError_t launch_topk(int K, const uint16_t *logits, int64_t stride, int slots, int N, int V,
                         const TopkPlan &plan, unsigned long long *part, unsigned *row_count,
-                        int32_t *ids, float *vals, cudaStream_t st);
+                        int32_t *ids, float *vals, cudaStream_t st, bool pdl);
 
 // ---------------------------------------------------------------- projections
 // C[m][o] = sum_k A_m[k] * W[o][k] with A_m a bf16 row of length d.  Row
@@ -44,6 +46,8 @@ cudaError_t launch_topk(int K, const uint16_t *logits, int64_t stride, int slots
 // proj_tc_splits) splits the k range over the CTAs of one cluster, which add
 // their partial tiles through distributed shared memory.  A CTA takes
 // `rows_per_cta` (128 or 256) rows: 256 halves the weight traffic per row.
+// With `pdl` the launch may overlap the end of the previous kernel in the
+// stream (the kernel waits for it before it reads the row ids).
 int proj_tc_splits(int d, int requested);
 // 2D bf16 [rows][d] tensor map, 128B swizzle, box 64 x box_rows.
 bool encode_bf16_rows_map(CUtensorMap *map, const void *base, int rows, int d, int box_rows);
@@ -52,35 +56,18 @@ bool encode_bf16_rows_map(CUtensorMap *map, const void *base, int rows, int d, i
 bool encode_f32_rows_map(CUtensorMap *map, const void *base, int rows, int cols, int box_rows);
 cudaError_t launch_proj_tc(int mode, int rows_per_cta, const uint16_t *table, const CUtensorMap &map_hi,
                            const CUtensorMap &map_lo, const int32_t *ids, int slots, int B, int M, int d,
-                           int V, int No, int splits, float *C, int *err, cudaStream_t st);
+                           int V, int No, int splits, float *C, int *err, cudaStream_t st, bool pdl = false);
 
 // ---------------------------------------------------------------- representations
 struct MlpWeightsDev {
-  const float *wfb_t;   // [r][r]  W_fuse[:, :r] transposed ([in][out])
-  const float *wfg_t;   // [r][r]  W_fuse[:, r:] transposed
   const float *gamma;   // [r]
   const float *beta;    // [r]
-  const float *w1s_t;   // [r][H]  W1[:, 0:r] transposed
-  const float *w1a_t;   // [r][H]  W1[:, r:2r] transposed
-  const float *w1b_t;   // [r][H]  W1[:, 2r:3r] transposed
   const float *w_la;    // [H]     W1[:, 3r]
   const float *w_lb;    // [H]     W1[:, 3r+1]
   const float *b1;      // [H]
   const float *w2;      // [H]
   const float *b2;      // [1]
 };
-
-// Per draft slot: g = LN0(ctx), Gf = W_fuse[:, r:] g; per pair:
-// s_p = Hp_p + Hq_{p+1}, P_p = W1_s s_p + b1.  slot_proj is [N*B][3r] =
-// (W_ctx h | W_pair[:, :d] h | W_pair[:, d:] h).
-cudaError_t launch_slot_post(const float *slot_proj, int N, int B, float eps, const MlpWeightsDev &w,
-                             float *Gf, float *P, cudaStream_t st);
-
-// Per candidate: b = LN0(cand_proj), z = gamma*LN0(W_fuse[:, :r] b + Gf) + beta,
-// U = W1_a z + w_la l, V = W1_b z + w_lb l.
-cudaError_t launch_cand_post(int K, const float *cand_proj, const float *topk_val, const float *Gf,
-                             int N, int B, float eps, const MlpWeightsDev &w, float *U, float *V,
-                             cudaStream_t st);
 
 // Tensor-core forms of the per-slot and per-candidate steps.  The maps
 // address bf16 hi / lo halves (box 64 x 128, 128B swizzle) of W_fuse[:, :r]
@@ -89,11 +76,14 @@ cudaError_t launch_cand_post(int K, const float *cand_proj, const float *topk_va
 struct MlpMaps {
   CUtensorMap fb_hi, fb_lo, w1_hi, w1_lo, fg_hi, fg_lo, w1s_hi, w1s_lo;
 };
-// Same outputs as launch_slot_post.
+// Per draft slot: Gf = W_fuse[:, r:] LN0(W_ctx h) ([N*B][r]); per pair p < B-1:
+// P_p = W1[:, :r] (W_pair[:, :d] h_p + W_pair[:, d:] h_{p+1}) + b1 ([N*(B-1)][H]).
+// slot_proj is [N*B][3r] = (W_ctx h | W_pair[:, :d] h | W_pair[:, d:] h).
 cudaError_t launch_slot_mlp_tc(const MlpMaps &maps, const float *slot_proj, const MlpWeightsDev &w, int N,
                                int B, float eps, float *Gf, float *P, int *err, cudaStream_t st);
-// Same outputs as launch_cand_post; M = N * B * K candidates, candidate m
-// belongs to draft slot m / K.  The candidate tiles move by TMA: `io.cp`
+// Per candidate: b = LN0(cand_proj), z = gamma*LN0(W_fuse[:, :r] b + Gf) + beta,
+// U = W1_a z + w_la l, V = W1_b z + w_lb l.  M = N * B * K candidates,
+// candidate m belongs to draft slot m / K.  The candidate tiles move by TMA: `io.cp`
 // reads cand_proj ([rows][r] fp32), `io.u` / `io.v` write U and V ([rows][H]
 // fp32); all three are fp32 maps with box 32 x 128 over the same row count
 // (>= M).  Rows of the last tile past M that lie inside the maps receive

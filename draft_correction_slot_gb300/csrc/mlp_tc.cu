@@ -28,6 +28,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
+#include "launch.h"
 
 namespace dc {
 namespace {
@@ -316,6 +317,7 @@ k_cand_mlp_tc(const __grid_constant__ CUtensorMap map_fb_hi, const __grid_consta
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int half = blockIdx.x, m0 = blockIdx.y * kRows;
+  pdl_trigger();
   const uint32_t sb = smem_u32(smem);
   const uint32_t a_hi = sb + kOffA, a_lo = sb + kOffA + kMat;
   const uint32_t w0_hi = sb + kOffW0, w0_lo = sb + kOffW0 + kMat;
@@ -346,6 +348,7 @@ k_cand_mlp_tc(const __grid_constant__ CUtensorMap map_fb_hi, const __grid_consta
     if (lane == 0) {
       // ------------------------------------------------------------ control thread
       load_pair(w0_hi, w0_lo, &map_fb_hi, &map_fb_lo, 0, smem_u32(&bar_w0));
+      pdl_wait();  // cand_proj comes from the previous kernel
       mbar_arrive_expect_tx(smem_u32(&bar_s), 4 * kBox);
       for (int bx = 0; bx < 4; ++bx) tma_load_2d(s_hi + bx * kBox, &map_cp, bx * 32, m0, smem_u32(&bar_s));
       // y = W_fuse[:, :r] b
@@ -377,6 +380,7 @@ k_cand_mlp_tc(const __grid_constant__ CUtensorMap map_fb_hi, const __grid_consta
     __syncwarp();
   } else {
     // -------------------------------------------------------------- row threads
+    pdl_wait();
     const int qd = warp & 3, q = warp >> 2;  // lane quadrant, column quarter
     const int r = qd * 32 + lane;           // tile row = tensor-memory lane
     const int m = m0 + r;
@@ -494,9 +498,10 @@ cudaError_t launch_cand_mlp_tc(const MlpMaps &maps, const CandIoMaps &io, const 
                                        kCandSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(2, (M + kRows - 1) / kRows);
-  k_cand_mlp_tc<<<grid, kThreads, kCandSmemBytes, st>>>(maps.fb_hi, maps.fb_lo, maps.w1_hi, maps.w1_lo, io.cp,
-                                                        io.u, io.v, Gf, topk_val, w.gamma, w.beta, w.w_la,
-                                                        w.w_lb, K, M, eps, err);
+  e = launch_ex(k_cand_mlp_tc, grid, dim3(kThreads), kCandSmemBytes, st, true, 0, maps.fb_hi, maps.fb_lo,
+                maps.w1_hi, maps.w1_lo, io.cp, io.u, io.v, Gf, topk_val, w.gamma, w.beta, w.w_la, w.w_lb, K, M,
+                eps, err);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -31,6 +31,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
+#include "launch.h"
 
 namespace dc {
 namespace {
@@ -119,6 +120,7 @@ k_proj_tc(const uint16_t *__restrict__ table, const __grid_constant__ CUtensorMa
   const int kb0 = split * kb_per_split;
   const int nkb = min(kb_per_split, nkb_total - kb0);
   const uint32_t sbase = smem_u32(smem);
+  pdl_trigger();
 
   if (tid == 0) {
     for (int s = 0; s < kStagesA; ++s) {
@@ -133,6 +135,7 @@ k_proj_tc(const uint16_t *__restrict__ table, const __grid_constant__ CUtensorMa
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  pdl_wait();  // the row ids (and this call's outputs) belong to the previous kernel until here
   if (tid < kTileM) {
     const int m = m0 + tid;
     int row = 0;  // rows past M load table row 0; their results are never stored
@@ -388,7 +391,7 @@ bool encode_f32_rows_map(CUtensorMap *map, const void *base, int rows, int cols,
 }
 
 template <int MODE, int MT>
-static cudaError_t launch_mode(int M, int splits, int No, int d, cudaStream_t st, const uint16_t *table,
+static cudaError_t launch_mode(int M, int splits, int No, int d, cudaStream_t st, bool pdl, const uint16_t *table,
                                const CUtensorMap &map_hi, const CUtensorMap &map_lo, const int32_t *ids,
                                int slots, int B, int V, float *C, int *err) {
   using G = ProjGeom<MT>;
@@ -398,36 +401,25 @@ static cudaError_t launch_mode(int M, int splits, int No, int d, cudaStream_t st
   const size_t smem = (size_t)G::kSmemUsed + 1024;
   cudaError_t e = cudaFuncSetAttribute(k_proj_tc<MODE, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(G::kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = grid.z;  // the splits of one tile
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_proj_tc<MODE, MT>, table, map_hi, map_lo, ids, slots, B, M, d, V, No, per,
-                            C, err);
+  // the splits of one tile form a cluster
+  return launch_ex(k_proj_tc<MODE, MT>, grid, dim3(G::kThreads), smem, st, pdl, grid.z, table, map_hi, map_lo, ids,
+                   slots, B, M, d, V, No, per, C, err);
 }
 
 cudaError_t launch_proj_tc(int mode, int rows_per_cta, const uint16_t *table, const CUtensorMap &map_hi,
                            const CUtensorMap &map_lo, const int32_t *ids, int slots, int B, int M, int d,
-                           int V, int No, int splits, float *C, int *err, cudaStream_t st) {
+                           int V, int No, int splits, float *C, int *err, cudaStream_t st, bool pdl) {
   if (M == 0) return cudaSuccess;
   if (No % kTileN != 0 || d % kTileK != 0 || splits < 1 || splits > kMaxSplits || (kSubM % splits) != 0 ||
       (rows_per_cta != 128 && rows_per_cta != 256))
     return cudaErrorInvalidValue;
   cudaError_t e;
   if (rows_per_cta == 128)
-    e = mode == 0 ? launch_mode<0, 1>(M, splits, No, d, st, table, map_hi, map_lo, ids, slots, B, V, C, err)
-                  : launch_mode<1, 1>(M, splits, No, d, st, table, map_hi, map_lo, ids, slots, B, V, C, err);
+    e = mode == 0 ? launch_mode<0, 1>(M, splits, No, d, st, pdl, table, map_hi, map_lo, ids, slots, B, V, C, err)
+                  : launch_mode<1, 1>(M, splits, No, d, st, pdl, table, map_hi, map_lo, ids, slots, B, V, C, err);
   else
-    e = mode == 0 ? launch_mode<0, 2>(M, splits, No, d, st, table, map_hi, map_lo, ids, slots, B, V, C, err)
-                  : launch_mode<1, 2>(M, splits, No, d, st, table, map_hi, map_lo, ids, slots, B, V, C, err);
+    e = mode == 0 ? launch_mode<0, 2>(M, splits, No, d, st, pdl, table, map_hi, map_lo, ids, slots, B, V, C, err)
+                  : launch_mode<1, 2>(M, splits, No, d, st, pdl, table, map_hi, map_lo, ids, slots, B, V, C, err);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

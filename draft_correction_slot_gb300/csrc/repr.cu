@@ -1,25 +1,22 @@
-// repr.cu -- steps 2-4 after the projections: LayerNorms, the fuse map, the
-// slot-pair states and the layer-1 partial products of the transition MLP,
-// then the K x K transition scores.
+// repr.cu -- step 4, the K x K transition scores of every slot pair (with
+// step 5 in the last block of each request), and the cosine variant's
+// per-candidate vectors and scores.
 //
 // DCOCO page ("Contextual Correction of Parallel Drafts for Speculative
-// Decoding"), Method step details:
-//   (2) b = LN(W_cand E[c]), g_i = LN(W_ctx h_i) (no affine);
-//       z = LN_{gamma,beta}(W_fuse [b; g_i]), width r = 128.
-//   (3) s_p = W_pair [h_p; h_{p+1}], once per adjacent slot pair.
-//   (4) S_p(a,b) = l_{p+1}(b) + Delta([s_p; z_p^a; z_{p+1}^b; l_p(a); l_{p+1}(b)]),
-//       Delta = 386 -> 256 -> 1 MLP with GELU, weights shared by all slots.
-//
+// Decoding"), Method step details (4):
+//   S_p(a,b) = l_{p+1}(b) + Delta([s_p; z_p^a; z_{p+1}^b; l_p(a); l_{p+1}(b)]),
+//   Delta = 386 -> 256 -> 1 MLP with GELU, weights shared by all slots.
 // Layer 1 of Delta is linear in its concatenated input, so it splits into a
 // per-pair part P_p = W1_s s_p + b1, a predecessor part U = W1_a z^a + w_la l(a)
-// and a successor part V = W1_b z^b + w_lb l(b).  Each of the (B-1) K^2 pairs
-// then costs one add, one GELU and one 256-long dot with w2.
-//
-// All arithmetic is fp32.  LN uses the population variance with eps inside
-// the square root.
+// and a successor part V = W1_b z^b + w_lb l(b) (computed in mlp_tc.cu).  Each
+// of the (B-1) K^2 pairs then costs one add, one GELU and one 256-long dot
+// with w2.  All arithmetic is fp32.
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "walk.cuh"
+#include "launch.h"
 
 namespace dc {
 namespace {
@@ -27,159 +24,6 @@ namespace {
 constexpr int R = 128;  // representation width
 constexpr int H = 256;  // MLP hidden width
 
-// LN0 of one 128-vector held as 4 values per lane of a warp (in place).
-__device__ __forceinline__ void warp_ln0_128(float (&x)[4], float eps) {
-  float s = warp_sum(x[0] + x[1] + x[2] + x[3]);
-  const float mean = s * (1.0f / R);
-  float q = 0.f;
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    x[u] -= mean;
-    q += x[u] * x[u];
-  }
-  q = warp_sum(q);
-  const float inv = rsqrtf(q * (1.0f / R) + eps);
-#pragma unroll
-  for (int u = 0; u < 4; ++u) x[u] *= inv;
-}
-
-// ---------------------------------------------------------------- per slot
-// One CTA per 8 consecutive draft slots of the flattened [N*B] slot index
-// (warp w owns slot s0 + w for the LayerNorm); every thread then produces one
-// output feature for all 8 slots, so each weight is read once per CTA.
-constexpr int kSlotsPerCta = 8;
-
-__global__ void __launch_bounds__(256)
-k_slot_post(const float *__restrict__ slot_proj, int NB, int B, float eps, MlpWeightsDev w,
-            float *__restrict__ Gf, float *__restrict__ Pout) {
-  __shared__ float g[kSlotsPerCta][R];
-  __shared__ float s[kSlotsPerCta][R];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int s0 = blockIdx.x * kSlotsPerCta;
-  {
-    const int gs = s0 + warp;  // this warp's slot
-    if (gs < NB) {
-      const float *sp = slot_proj + (int64_t)gs * 3 * R;
-      float x[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) x[u] = sp[lane + 32 * u];
-      warp_ln0_128(x, eps);
-#pragma unroll
-      for (int u = 0; u < 4; ++u) g[warp][lane + 32 * u] = x[u];
-      // pair state s_p = W_pair[:, :d] h_p + W_pair[:, d:] h_{p+1} for p = this slot
-      const int i = gs % B;
-      if (i < B - 1) {
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          s[warp][lane + 32 * u] = sp[R + lane + 32 * u] + sp[3 * R + 2 * R + lane + 32 * u];
-      }
-    }
-  }
-  __syncthreads();
-  // Gf = W_fuse[:, r:] g   (threads 0..127: one output feature, 8 slots)
-  if (tid < R) {
-    float acc[kSlotsPerCta] = {};
-#pragma unroll 16
-    for (int k = 0; k < R; ++k) {
-      const float wv = w.wfg_t[k * R + tid];
-#pragma unroll
-      for (int u = 0; u < kSlotsPerCta; ++u) acc[u] = fmaf(wv, g[u][k], acc[u]);
-    }
-#pragma unroll
-    for (int u = 0; u < kSlotsPerCta; ++u)
-      if (s0 + u < NB) Gf[(int64_t)(s0 + u) * R + tid] = acc[u];
-  }
-  // P_p = W1_s s_p + b1   (all 256 threads: one hidden unit, 8 slots)
-  {
-    const int j = tid;
-    const float bj = w.b1[j];
-    float acc[kSlotsPerCta];
-#pragma unroll
-    for (int u = 0; u < kSlotsPerCta; ++u) acc[u] = bj;
-#pragma unroll 16
-    for (int k = 0; k < R; ++k) {
-      const float wv = w.w1s_t[k * H + j];
-#pragma unroll
-      for (int u = 0; u < kSlotsPerCta; ++u) acc[u] = fmaf(wv, s[u][k], acc[u]);
-    }
-#pragma unroll
-    for (int u = 0; u < kSlotsPerCta; ++u) {
-      const int gs = s0 + u;
-      if (gs >= NB) continue;
-      const int n = gs / B, i = gs - n * B;
-      if (i < B - 1) Pout[((int64_t)n * (B - 1) + i) * H + j] = acc[u];
-    }
-  }
-}
-
-// ---------------------------------------------------------------- per candidate
-template <int K>
-__global__ void __launch_bounds__(256)
-k_cand_post(const float *__restrict__ cand_proj, const float *__restrict__ topk_val,
-            const float *__restrict__ Gf, float eps, MlpWeightsDev w, float *__restrict__ U,
-            float *__restrict__ Vout) {
-  __shared__ float b[K][R];
-  __shared__ float z[K][R];
-  const int slot = blockIdx.x;  // n * B + i
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t c0 = (int64_t)slot * K;
-
-  for (int c = warp; c < K; c += 8) {
-    float x[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) x[u] = cand_proj[(c0 + c) * R + lane + 32 * u];
-    warp_ln0_128(x, eps);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) b[c][lane + 32 * u] = x[u];
-  }
-  __syncthreads();
-
-  // y = W_fuse[:, :r] b + Gf  (thread: output o, candidates of one parity)
-  {
-    constexpr int KH = K / 2;
-    const int o = tid & (R - 1), half = tid >> 7;
-    float acc[KH] = {};
-#pragma unroll 16
-    for (int k = 0; k < R; ++k) {
-      const float wv = w.wfb_t[k * R + o];
-#pragma unroll
-      for (int u = 0; u < KH; ++u) acc[u] = fmaf(wv, b[half + 2 * u][k], acc[u]);
-    }
-    const float gf = Gf[(int64_t)slot * R + o];
-#pragma unroll
-    for (int u = 0; u < KH; ++u) z[half + 2 * u][o] = acc[u] + gf;
-  }
-  __syncthreads();
-  for (int c = warp; c < K; c += 8) {
-    float x[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) x[u] = z[c][lane + 32 * u];
-    warp_ln0_128(x, eps);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int k = lane + 32 * u;
-      z[c][k] = fmaf(w.gamma[k], x[u], w.beta[k]);
-    }
-  }
-  __syncthreads();
-
-  // U = W1_a z + w_la l ; V = W1_b z + w_lb l   (thread: hidden unit j)
-  const int j = tid;
-  for (int pass = 0; pass < 2; ++pass) {
-    const float *wt = pass == 0 ? w.w1a_t : w.w1b_t;
-    const float wl = pass == 0 ? w.w_la[j] : w.w_lb[j];
-    float *dst = pass == 0 ? U : Vout;
-    float acc[K] = {};
-#pragma unroll 8
-    for (int k = 0; k < R; ++k) {
-      const float wv = wt[k * H + j];
-#pragma unroll
-      for (int c = 0; c < K; ++c) acc[c] = fmaf(wv, z[c][k], acc[c]);
-    }
-#pragma unroll
-    for (int c = 0; c < K; ++c) dst[(c0 + c) * H + j] = fmaf(wl, topk_val[c0 + c], acc[c]);
-  }
-}
 
 // ---------------------------------------------------------------- pair scores
 // With x = (P_p + U_{p,a} + V_{p+1,b}) / sqrt(2) and w' = w2 / sqrt(2),
@@ -266,6 +110,8 @@ k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
   const int np = blockIdx.x;        // n * (B-1) + p
   const int n = np / (B - 1), p = np - n * (B - 1);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_trigger();
+  pdl_wait();  // U, V (and this call's outputs) belong to the previous kernel until here
   const int64_t ca = ((int64_t)n * B + p) * K;      // first candidate of slot p
   const int64_t cb = ca + K;                         // first candidate of slot p+1
   const float *Pp = P + (int64_t)np * H;
@@ -433,28 +279,6 @@ k_cos_score(const float *__restrict__ O, const float *__restrict__ I,
 
 }  // namespace
 
-cudaError_t launch_slot_post(const float *slot_proj, int N, int B, float eps, const MlpWeightsDev &w,
-                             float *Gf, float *P, cudaStream_t st) {
-  if (N == 0) return cudaSuccess;
-  const int NB = N * B;
-  k_slot_post<<<(NB + kSlotsPerCta - 1) / kSlotsPerCta, 256, 0, st>>>(slot_proj, NB, B, eps, w, Gf, P);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_cand_post(int K, const float *cand_proj, const float *topk_val, const float *Gf,
-                             int N, int B, float eps, const MlpWeightsDev &w, float *U, float *V,
-                             cudaStream_t st) {
-  if (N == 0) return cudaSuccess;
-  const int grid = N * B;
-  switch (K) {
-    case 8: k_cand_post<8><<<grid, 256, 0, st>>>(cand_proj, topk_val, Gf, eps, w, U, V); break;
-    case 16: k_cand_post<16><<<grid, 256, 0, st>>>(cand_proj, topk_val, Gf, eps, w, U, V); break;
-    case 32: k_cand_post<32><<<grid, 256, 0, st>>>(cand_proj, topk_val, Gf, eps, w, U, V); break;
-    default: return cudaErrorInvalidValue;
-  }
-  return cudaGetLastError();
-}
-
 template <int K>
 static cudaError_t pair_score_k(const float *U, const float *V, const float *P, const float *tv,
                                 const float *w2, const float *b2, int N, int B, float *scores,
@@ -463,7 +287,9 @@ static cudaError_t pair_score_k(const float *U, const float *V, const float *P, 
   cudaError_t e = cudaFuncSetAttribute(k_pair_score<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  k_pair_score<K><<<N * (B - 1), 256, smem, st>>>(U, V, P, tv, w2, b2, B, scores, wk);
+  e = launch_ex(k_pair_score<K>, dim3(N * (B - 1)), dim3(256), smem, st, true, 0, U, V, P, tv, w2, b2, B, scores,
+                wk);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

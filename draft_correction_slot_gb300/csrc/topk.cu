@@ -31,6 +31,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "launch.h"
 
 namespace dc {
 
@@ -356,6 +357,7 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
   const int per_warp = ((nv + kWarps - 1) / kWarps + kGroup - 1) / kGroup * kGroup;
   const int ng = (nv + kGroup - 1) / kGroup;
   const int w0 = v0 + min(warp * per_warp, nv), w1 = v0 + min((warp + 1) * per_warp, nv);
+  pdl_trigger();
   if (tid < K) s_top[tid] = 0ull;
   for (int e = tid; e < 2 * 256; e += kThreads) (&s_hist[0][0])[e] = 0;
   if (tid == 0) {
@@ -537,6 +539,9 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
     __syncthreads();
   }
 
+  // everything above only reads the logits; the previous kernel in the stream
+  // may still read the buffers written below
+  pdl_wait();
   if (nseg > 1) {
     u64 *my = part + ((int64_t)row * nseg + seg) * K;
     if (tid < K) {
@@ -626,26 +631,28 @@ int topk_occupancy(int K) {
 
 cudaError_t launch_topk(int K, const uint16_t *logits, int64_t stride, int slots, int N, int V,
                         const TopkPlan &plan, unsigned long long *part, unsigned *row_count,
-                        int32_t *ids, float *vals, cudaStream_t st) {
+                        int32_t *ids, float *vals, cudaStream_t st, bool pdl) {
   const int B = slots - 1;
   if (N == 0) return cudaSuccess;
-  dim3 grid(N * B, plan.nchunks);
+  const dim3 grid(N * B, plan.nchunks), block(kThreads);
+  cudaError_t e;
   switch (K) {
     case 8:
-      k_topk<8><<<grid, kThreads, 0, st>>>(logits, stride, slots, B, V, plan.nchunks, plan.chunk_vecs,
-                                           part, row_count, ids, vals);
+      e = launch_ex(k_topk<8>, grid, block, 0, st, pdl, 0, logits, stride, slots, B, V, plan.nchunks,
+                    plan.chunk_vecs, part, row_count, ids, vals);
       break;
     case 16:
-      k_topk<16><<<grid, kThreads, 0, st>>>(logits, stride, slots, B, V, plan.nchunks, plan.chunk_vecs,
-                                            part, row_count, ids, vals);
+      e = launch_ex(k_topk<16>, grid, block, 0, st, pdl, 0, logits, stride, slots, B, V, plan.nchunks,
+                    plan.chunk_vecs, part, row_count, ids, vals);
       break;
     case 32:
-      k_topk<32><<<grid, kThreads, 0, st>>>(logits, stride, slots, B, V, plan.nchunks, plan.chunk_vecs,
-                                            part, row_count, ids, vals);
+      e = launch_ex(k_topk<32>, grid, block, 0, st, pdl, 0, logits, stride, slots, B, V, plan.nchunks,
+                    plan.chunk_vecs, part, row_count, ids, vals);
       break;
     default:
       return cudaErrorInvalidValue;
   }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -95,6 +95,6 @@ extern "C" int dcoco_topk_noalloc(int batch, int slots, int vocab, int topk, con
   if (cudaMemsetAsync(row_count, 0, (size_t)rows * sizeof(unsigned), st) != cudaSuccess)
     return DCOCO_ECUDA;
   const cudaError_t e = dc::launch_topk(topk, static_cast<const uint16_t *>(logits), logits_slot_stride,
-                                        slots, batch, vocab, plan, part, row_count, topk_ids, topk_val, st);
+                                        slots, batch, vocab, plan, part, row_count, topk_ids, topk_val, st, true);
   return e == cudaSuccess ? DCOCO_OK : DCOCO_ECUDA;
 }
