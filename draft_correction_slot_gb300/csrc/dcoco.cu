@@ -23,7 +23,7 @@ struct Workspace {
   float *slot_proj = nullptr;  // [N*B][3r]  (variant 1: [N*B][2r])
   float *cand_proj = nullptr;  // [N*B*K][r] (variant 1: [N*B*K][2r])
   float *Gf = nullptr;         // [N*B][r]
-  float *P = nullptr;          // [N*(B-1)][H]
+  float *P = nullptr;          // [N*B][H] (rows of the last slot unused)
   float *U = nullptr;          // [N*B*K][H]  (variant 1: O [N*B*K][r])
   float *V = nullptr;          // [N*B*K][H]  (variant 1: I [N*B*K][r])
   float *scores = nullptr;     // [N*(B-1)][K][K]
@@ -46,8 +46,8 @@ namespace {
 constexpr int kMaxStages = 8;
 constexpr int kMaxTimedCalls = 1024;
 const char *const kStageNames[2][kMaxStages] = {
-    {"topk", "slot_proj", "slot_post", "cand_proj", "cand_post", "pair_walk", nullptr, nullptr},
-    {"topk", "slot_proj", "cand_proj", "cos_post", "cos_score", "walk_verify", nullptr, nullptr}};
+    {"topk", "proj", "slot_post", "cand_post", "pair_walk", nullptr, nullptr, nullptr},
+    {"topk", "proj", "cos_post", "cos_score", "walk_verify", nullptr, nullptr, nullptr}};
 int stage_count(int variant) {
   int n = 0;
   while (n < kMaxStages && kStageNames[variant][n]) ++n;
@@ -61,16 +61,12 @@ struct dcoco_handle {
   int B = 0;
   int topk_segments_max = 1;  // partial-list capacity per row
   int topk_wave = 1;          // resident top-K CTAs on the device (SMs x occupancy)
-  int splits_slot = 1;        // fixed split-K of the projections (fixed per handle, so
-  int splits_cand = 1;        // results do not depend on the batch size)
+  int splits = 1;             // split-K of the projections (fixed per handle, so
+                              // results do not depend on the batch size)
   void *block = nullptr;  // one device allocation holding the workspace
   Workspace ws;
-  // The slot path (slot projections, per-slot maps) depends only on the hidden
-  // states: it runs on `side`, forked from and joined back into the caller's
-  // stream by the two events, while the top-K streams the logits.
-  cudaStream_t side = nullptr;
-  cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
   dc::CandIoMaps cand_io;  // TMA maps of cand_proj, U, V (variant 0)
+  dc::SlotIoMaps slot_io;  // TMA maps of slot_proj, Gf, P (variant 0)
   cudaStream_t last_stream = nullptr;
   long long launches = 0;            // kernels launched so far
   bool timing = false;               // record per-stage events
@@ -136,7 +132,7 @@ void carve_workspace(Carver &c, const dcoco_config &cfg, int B, int topk_segment
   ws.slot_proj = c.take<float>(rows * 3 * kR);
   ws.cand_proj = c.take<float>(cands * 2 * kR);
   ws.Gf = c.take<float>(rows * kR);
-  ws.P = c.take<float>(N * (B - 1) * kH);
+  ws.P = c.take<float>(N * B * kH);
   ws.U = c.take<float>(cands * kH);
   ws.V = c.take<float>(cands * kH);
   ws.scores = c.take<float>(N * (B - 1) * K * K);
@@ -236,32 +232,23 @@ int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs 
 
   const int rows = N * B, cands = rows * K;
   const dc::TopkPlan plan = dc::topk_plan(V, N * B, h->topk_wave);
-  // Per-stage timing serialises the stages on `st`; otherwise the slot path
-  // runs on the side stream.  The top-K is launched first so that its CTAs
-  // are dispatched first and the slot kernels fill the SMs its last wave frees.
-  const bool overlap = clk.ev == nullptr && cfg.variant == 0;
-  if (overlap) DC_TRY(cudaEventRecord(h->ev_fork, st));
   // step 1: candidate pools
   DC_TRY(clk.done(dc::launch_topk(K, logits, in->logits_slot_stride, cfg.slots, N, V, plan,
                                   ws.part, ws.row_count, ids, vals, st, false)));
+  // step 2 (and the slot-pair state): the candidate rows and the draft-slot
+  // rows go through one projection launch, which fills the device in one wave.
+  // It overlaps the top-K's tail: its blocks take SMs as the top-K's leave,
+  // the draft-slot tiles start at once and the candidate tiles wait for the ids.
+  const int r_out = cfg.variant == 0 ? kR : 2 * kR;          // candidate outputs
+  const int s_out = cfg.variant == 0 ? 3 * kR : 2 * kR;      // draft-slot outputs
+  const dc::ProjJob cj{E, ids, ws.cand_proj, cands, r_out, dc::proj_tc_tiles(cands, r_out)};
+  const dc::ProjJob sj{hidden, nullptr, ws.slot_proj, rows, s_out, dc::proj_tc_tiles(rows, s_out)};
+  DC_TRY(clk.done(dc::launch_proj_tc(cj, w->map_cand_hi, w->map_cand_lo, &sj, &w->map_slot_hi,
+                                     &w->map_slot_lo, cfg.slots, B, d, V, h->splits, ws.err, st, true)));
   if (cfg.variant == 0) {
-    // steps 2-3: slot projections (W_ctx, W_pair halves) and per-slot / per-pair terms
-    cudaStream_t ss = st;
-    if (overlap) {
-      DC_TRY(cudaStreamWaitEvent(h->side, h->ev_fork, 0));
-      ss = h->side;
-    }
-    DC_TRY(clk.done(dc::launch_proj_tc(1, 128, hidden, w->map_slot_hi, w->map_slot_lo, nullptr, cfg.slots, B,
-                                       rows, d, V, 3 * kR, h->splits_slot, ws.slot_proj,
-                                       ws.err, ss)));
-    DC_TRY(clk.done(dc::launch_slot_mlp_tc(w->mlp_maps, ws.slot_proj, w->mlp, N, B, cfg.ln_eps, ws.Gf, ws.P,
-                                           ws.err, ss)));
-    if (overlap) DC_TRY(cudaEventRecord(h->ev_join, h->side));
-    // step 2: candidate projections, then z and the layer-1 partials U, V
-    DC_TRY(clk.done(dc::launch_proj_tc(0, 256, E, w->map_cand_hi, w->map_cand_lo, ids, cfg.slots, B,
-                                       cands, d, V, kR, h->splits_cand, ws.cand_proj,
-                                       ws.err, st)));
-    if (overlap) DC_TRY(cudaStreamWaitEvent(st, h->ev_join, 0));
+    // steps 2-3: per-slot / per-pair terms, then z and the layer-1 partials U, V
+    DC_TRY(clk.done(dc::launch_slot_mlp_tc(w->mlp_maps, h->slot_io, w->mlp, N, B, cfg.ln_eps, ws.err, st,
+                                           true)));
     DC_TRY(clk.done(dc::launch_cand_mlp_tc(w->mlp_maps, h->cand_io, ws.Gf, vals, w->mlp, K, cands,
                                            cfg.ln_eps, ws.err, st)));
     // steps 4-5: all (B-1) K^2 transition scores, then each request's walk
@@ -271,16 +258,9 @@ int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs 
     DC_TRY(clk.done(dc::launch_pair_score_walk(K, ws.U, ws.V, ws.P, vals, w->mlp.w2, w->mlp.b2, N, B,
                                                scores, wk, st)));
     return DCOCO_OK;
-  } else {
-    DC_TRY(clk.done(dc::launch_proj_tc(1, 128, hidden, w->map_slot_hi, w->map_slot_lo, nullptr, cfg.slots, B,
-                                       rows, d, V, 2 * kR, h->splits_slot, ws.slot_proj,
-                                       ws.err, st)));
-    DC_TRY(clk.done(dc::launch_proj_tc(0, 256, E, w->map_cand_hi, w->map_cand_lo, ids, cfg.slots, B,
-                                       cands, d, V, 2 * kR, h->splits_cand, ws.cand_proj,
-                                       ws.err, st)));
-    DC_TRY(clk.done(dc::launch_cos_post(K, ws.cand_proj, ws.slot_proj, N, B, ws.U, ws.V, st)));
-    DC_TRY(clk.done(dc::launch_cos_score(K, ws.U, ws.V, vals, cfg.sigma, N, B, scores, st)));
   }
+  DC_TRY(clk.done(dc::launch_cos_post(K, ws.cand_proj, ws.slot_proj, N, B, ws.U, ws.V, st)));
+  DC_TRY(clk.done(dc::launch_cos_score(K, ws.U, ws.V, vals, cfg.sigma, N, B, scores, st)));
   // step 5: walk + verify
   DC_TRY(clk.done(dc::launch_walk_verify(K, scores, ids, in->target_tokens, N, B, out->tokens,
                                          choice, margin,
@@ -350,8 +330,7 @@ int dcoco_create(const dcoco_config *cfg, dcoco_handle **out) {
     return DCOCO_ECUDA;
   }
   h->topk_wave = sms * dc::topk_occupancy(cfg->topk);
-  h->splits_slot = dc::proj_tc_splits(cfg->hidden, 8);
-  h->splits_cand = dc::proj_tc_splits(cfg->hidden, 4);
+  h->splits = dc::proj_tc_splits(cfg->hidden, 4);
   Carver sizer;
   carve_workspace(sizer, h->cfg, h->B, h->topk_segments_max, h->ws);
   const size_t bytes = sizer.off + 256;
@@ -363,19 +342,17 @@ int dcoco_create(const dcoco_config *cfg, dcoco_handle **out) {
   Carver c;
   c.base = static_cast<char *>(h->block);
   carve_workspace(c, h->cfg, h->B, h->topk_segments_max, h->ws);
-  const int cands_cap = cfg->max_batch * h->B * cfg->topk;
+  const int rows_cap = cfg->max_batch * h->B, cands_cap = rows_cap * cfg->topk;
   const bool maps_ok =
       cfg->variant != 0 ||
       (dc::encode_f32_rows_map(&h->cand_io.cp, h->ws.cand_proj, cands_cap, kR, 128) &&
        dc::encode_f32_rows_map(&h->cand_io.u, h->ws.U, cands_cap, kH, 128) &&
-       dc::encode_f32_rows_map(&h->cand_io.v, h->ws.V, cands_cap, kH, 128));
-  if (!maps_ok || cudaMemset(h->block, 0, bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess ||
-      cudaStreamCreateWithFlags(&h->side, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaEventCreateWithFlags(&h->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
-      cudaEventCreateWithFlags(&h->ev_join, cudaEventDisableTiming) != cudaSuccess) {
+       dc::encode_f32_rows_map(&h->cand_io.v, h->ws.V, cands_cap, kH, 128) &&
+       dc::encode_f32_rows_map(&h->slot_io.sp, h->ws.slot_proj, rows_cap, 3 * kR, 128) &&
+       dc::encode_f32_rows_map(&h->slot_io.gf, h->ws.Gf, rows_cap, kR, 128) &&
+       dc::encode_f32_rows_map(&h->slot_io.p, h->ws.P, rows_cap, kH, 128));
+  if (!maps_ok || cudaMemset(h->block, 0, bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     cudaGetLastError();
-    if (h->ev_fork) cudaEventDestroy(h->ev_fork);
-    if (h->side) cudaStreamDestroy(h->side);
     cudaFree(h->block);
     delete h;
     return DCOCO_ECUDA;
@@ -650,9 +627,6 @@ void dcoco_destroy(dcoco_handle *h) {
   if (!h) return;
   cudaDeviceSynchronize();
   for (cudaEvent_t e : h->events) cudaEventDestroy(e);
-  cudaEventDestroy(h->ev_join);
-  cudaEventDestroy(h->ev_fork);
-  cudaStreamDestroy(h->side);
   cudaFree(h->block);
   delete h;
 }

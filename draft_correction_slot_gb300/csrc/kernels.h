@@ -34,29 +34,36 @@ cudaError_t launch_topk(int K, const uint16_t *logits, int64_t stride, int slots
                         int32_t *ids, float *vals, cudaStream_t st, bool pdl);
 
 // ---------------------------------------------------------------- projections
-// C[m][o] = sum_k A_m[k] * W[o][k] with A_m a bf16 row of length d.  Row
-// addressing: mode 0 gathers A_m = table[ids[m]] (ids < V, else the device
-// status word gets kErrBadCandidateId and row 0 is used); mode 1 takes
-// A_m = table[(m / B) * slots + (m % B) + 1] (the draft-slot rows of a
-// [N][slots][d] tensor).
-// Tensor-core projection.  A rows are gathered from `table` (bf16 [rows][d]:
-// E, or the hidden states viewed as [N*slots][d]); W comes as bf16 hi and lo
-// halves ([No][d] each, No % 128 == 0, d % 64 == 0) through `map_hi` /
-// `map_lo` (box 64 x 128).  `splits` (a power of two <= 8, from
-// proj_tc_splits) splits the k range over the CTAs of one cluster, which add
-// their partial tiles through distributed shared memory.  A CTA takes
-// `rows_per_cta` (128 or 256) rows: 256 halves the weight traffic per row.
+// C[m][o] = sum_k A_m[k] * W[o][k] with A_m a bf16 row of length d, on the
+// tensor cores.  A job with `ids` gathers A_m = table[ids[m]] (ids < V, else
+// the device status word gets kErrBadCandidateId and row 0 is used); a job
+// without takes A_m = table[(m / B) * slots + (m % B) + 1] (the draft-slot
+// rows of a [N][slots][d] tensor).  W comes as bf16 hi and lo halves ([No][d]
+// each, No % 128 == 0, d % 64 == 0) through two TMA maps (box 64 x 128).
+// A CTA owns 256 rows x 128 outputs of one job; `splits` (a power of two
+// <= 8, from proj_tc_splits) splits the k range over the CTAs of one
+// cluster, which add their partial tiles through distributed shared memory.
+// One launch runs one or two jobs, the second one's tiles after the first's.
 // With `pdl` the launch may overlap the end of the previous kernel in the
-// stream (the kernel waits for it before it reads the row ids).
+// stream (a gathering job waits for it before it reads the row ids; a
+// draft-slot job does not wait).
+struct ProjJob {
+  const uint16_t *table;  // bf16 [rows][d]
+  const int32_t *ids;     // [M] table rows, or null for draft-slot rows
+  float *C;               // fp32 [M][No]
+  int M, No;
+  int tiles;              // proj_tc_tiles(M, No)
+};
 int proj_tc_splits(int d, int requested);
+int proj_tc_tiles(int M, int No);
 // 2D bf16 [rows][d] tensor map, 128B swizzle, box 64 x box_rows.
 bool encode_bf16_rows_map(CUtensorMap *map, const void *base, int rows, int d, int box_rows);
 // 2D fp32 [rows][cols] tensor map, 128B swizzle, box 32 x box_rows
 // (cols % 32 == 0).
 bool encode_f32_rows_map(CUtensorMap *map, const void *base, int rows, int cols, int box_rows);
-cudaError_t launch_proj_tc(int mode, int rows_per_cta, const uint16_t *table, const CUtensorMap &map_hi,
-                           const CUtensorMap &map_lo, const int32_t *ids, int slots, int B, int M, int d,
-                           int V, int No, int splits, float *C, int *err, cudaStream_t st, bool pdl = false);
+cudaError_t launch_proj_tc(const ProjJob &a, const CUtensorMap &a_hi, const CUtensorMap &a_lo,
+                           const ProjJob *b, const CUtensorMap *b_hi, const CUtensorMap *b_lo, int slots,
+                           int B, int d, int V, int splits, int *err, cudaStream_t st, bool pdl);
 
 // ---------------------------------------------------------------- representations
 struct MlpWeightsDev {
@@ -76,11 +83,18 @@ struct MlpWeightsDev {
 struct MlpMaps {
   CUtensorMap fb_hi, fb_lo, w1_hi, w1_lo, fg_hi, fg_lo, w1s_hi, w1s_lo;
 };
-// Per draft slot: Gf = W_fuse[:, r:] LN0(W_ctx h) ([N*B][r]); per pair p < B-1:
-// P_p = W1[:, :r] (W_pair[:, :d] h_p + W_pair[:, d:] h_{p+1}) + b1 ([N*(B-1)][H]).
-// slot_proj is [N*B][3r] = (W_ctx h | W_pair[:, :d] h | W_pair[:, d:] h).
-cudaError_t launch_slot_mlp_tc(const MlpMaps &maps, const float *slot_proj, const MlpWeightsDev &w, int N,
-                               int B, float eps, float *Gf, float *P, int *err, cudaStream_t st);
+// Per draft slot: Gf = W_fuse[:, r:] LN0(W_ctx h) ([N*B][r]); per draft slot
+// i (used for i < B-1): P_i = W1[:, :r] (W_pair[:, :d] h_i + W_pair[:, d:] h_{i+1})
+// + b1 ([N*B][H]).  slot_proj is [N*B][3r] = (W_ctx h | W_pair[:, :d] h | W_pair[:, d:] h).
+// The tiles move by TMA: `sp` reads slot_proj, `gf` and `p` write Gf and P;
+// all three are fp32 maps with box 32 x 128 over the same row count (>= N*B).
+// With `pdl` the launch may overlap the end of the previous kernel in the
+// stream (the kernel waits for it before it reads slot_proj).
+struct SlotIoMaps {
+  CUtensorMap sp, gf, p;
+};
+cudaError_t launch_slot_mlp_tc(const MlpMaps &maps, const SlotIoMaps &io, const MlpWeightsDev &w, int N, int B,
+                               float eps, int *err, cudaStream_t st, bool pdl);
 // Per candidate: b = LN0(cand_proj), z = gamma*LN0(W_fuse[:, :r] b + Gf) + beta,
 // U = W1_a z + w_la l, V = W1_b z + w_lb l.  M = N * B * K candidates,
 // candidate m belongs to draft slot m / K.  The candidate tiles move by TMA: `io.cp`
@@ -107,6 +121,7 @@ struct WalkArgs {
 };
 
 // S[n,p,a,b] = l_{p+1}(b) + b2 + sum_j w2_j GELU(P_pj + U_{p,a,j} + V_{p+1,b,j}),
+// with P indexed by draft slot ([N*B][H]),
 // then, in the last block of each request, the walk and verify of
 // launch_walk_verify.
 cudaError_t launch_pair_score_walk(int K, const float *U, const float *V, const float *P,

@@ -141,6 +141,13 @@ __device__ __forceinline__ void load32(float (&x)[kQ], const float *src) {
   }
 }
 
+constexpr int kBox = 128 * 128;  // one fp32 box: 128 rows x 32 columns, 16 KB
+
+// 16-byte chunk c of row r in a swizzled 128-byte-row box at `box`.
+__device__ __forceinline__ uint8_t *box_chunk(uint8_t *box, int r, int c) {
+  return box + r * 128 + ((c ^ (r & 7)) * 16);
+}
+
 // 3-pass split product of one 128-deep contraction into tensor memory at `tmem`.
 __device__ __forceinline__ void mma_split(uint32_t tmem, uint32_t a_hi, uint32_t a_lo, uint32_t w_hi,
                                           uint32_t w_lo) {
@@ -167,31 +174,41 @@ __device__ __forceinline__ void load_pair(uint32_t w_hi, uint32_t w_lo, const CU
 
 // ---------------------------------------------------------------- per draft slot
 // One CTA per (128-slot tile, output chunk): chunk 0 writes Gf = W_fuse[:, r:] g
-// for every slot; chunks 1 and 2 write the two 128-wide halves of P_p for the
-// slots that start a pair (i < B-1).  slot_proj rows are
-// (W_ctx h | W_pair[:, :d] h | W_pair[:, d:] h).
-constexpr int kSlotSmemBytes = 4 * kMat + 1024;
+// for every slot; chunks 1 and 2 write the two 128-wide halves of
+// P_i = W1[:, :r] s_i + b1, s_i = W_pair[:, :d] h_i + W_pair[:, d:] h_{i+1},
+// indexed by draft slot (rows of the last slot of a request are not used).
+// slot_proj rows are (W_ctx h | W_pair[:, :d] h | W_pair[:, d:] h).
+// The input tiles arrive and the output tile leaves by TMA (fp32 boxes of 128
+// rows x 32 columns, 128-byte swizzled), so every row thread's 16-byte
+// shared-memory access is conflict-free and the global traffic is whole lines.
+// Shared memory: X (64 KB): the first input tile, then the A operand (hi, lo);
+// Y (64 KB): the second input tile (chunks 1, 2), then the output tile;
+// W (64 KB): the weight pair.
+constexpr int kSlotOffX = 0, kSlotOffY = 2 * kMat, kSlotOffW = 4 * kMat;
+constexpr int kSlotSmemBytes = 6 * kMat + 1024;
 
 __global__ void __launch_bounds__(kThreads, 1)
 k_slot_mlp_tc(const __grid_constant__ CUtensorMap map_fg_hi, const __grid_constant__ CUtensorMap map_fg_lo,
               const __grid_constant__ CUtensorMap map_w1s_hi, const __grid_constant__ CUtensorMap map_w1s_lo,
-              const float *__restrict__ slot_proj, const float *__restrict__ b1, int NB, int B, float eps,
-              float *__restrict__ Gf, float *__restrict__ P, int *err) {
+              const __grid_constant__ CUtensorMap map_sp, const __grid_constant__ CUtensorMap map_gf,
+              const __grid_constant__ CUtensorMap map_p, const float *__restrict__ b1, float eps, int *err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  __shared__ __align__(8) unsigned long long bar_w, bar_a, bar_mma;
+  __shared__ __align__(8) unsigned long long bar_w, bar_in, bar_a, bar_mma;
   __shared__ float s_red[2][4 * kRows];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int chunk = blockIdx.x, m0 = blockIdx.y * kRows;
+  pdl_trigger();
   const uint32_t sb = smem_u32(smem);
-  const uint32_t a_hi = sb + kOffA, a_lo = sb + kOffA + kMat;
-  const uint32_t w_hi = sb + kOffW0, w_lo = sb + kOffW0 + kMat;
+  const uint32_t a_hi = sb + kSlotOffX, a_lo = sb + kSlotOffX + kMat;
+  const uint32_t w_hi = sb + kSlotOffW, w_lo = sb + kSlotOffW + kMat;
 
   if (tid == 0) {
     mbar_init(smem_u32(&bar_w), 1);
+    mbar_init(smem_u32(&bar_in), 1);
     mbar_init(smem_u32(&bar_a), kRowThreads);
     mbar_init(smem_u32(&bar_mma), 1);
     s_abort = 0;
@@ -205,10 +222,24 @@ k_slot_mlp_tc(const __grid_constant__ CUtensorMap map_fg_hi, const __grid_consta
 
   if (warp == kRowWarps) {
     if (lane == 0) {
+      // ------------------------------------------------------------ control thread
       if (chunk == 0)
         load_pair(w_hi, w_lo, &map_fg_hi, &map_fg_lo, 0, smem_u32(&bar_w));
       else
         load_pair(w_hi, w_lo, &map_w1s_hi, &map_w1s_lo, (chunk - 1) * 128, smem_u32(&bar_w));
+      pdl_wait();  // slot_proj comes from the previous kernel
+      // chunk 0: W_ctx h of the tile's slots; chunks 1, 2: W_pair[:, :d] h of
+      // the tile's slots and W_pair[:, d:] h of the slots one row further on
+      const uint32_t in = smem_u32(&bar_in);
+      mbar_arrive_expect_tx(in, (chunk == 0 ? 4 : 8) * kBox);
+      if (chunk == 0) {
+        for (int bx = 0; bx < 4; ++bx) tma_load_2d(sb + kSlotOffX + bx * kBox, &map_sp, bx * 32, m0, in);
+      } else {
+        for (int bx = 0; bx < 4; ++bx) {
+          tma_load_2d(sb + kSlotOffX + bx * kBox, &map_sp, kR + bx * 32, m0, in);
+          tma_load_2d(sb + kSlotOffY + bx * kBox, &map_sp, 2 * kR + bx * 32, m0 + 1, in);
+        }
+      }
       if (mbar_wait(smem_u32(&bar_w), 0, &s_abort, err) && mbar_wait(smem_u32(&bar_a), 0, &s_abort, err)) {
         tc_fence_after();
         mma_split(tmem, a_hi, a_lo, w_hi, w_lo);
@@ -217,26 +248,28 @@ k_slot_mlp_tc(const __grid_constant__ CUtensorMap map_fg_hi, const __grid_consta
     }
     __syncwarp();
   } else {
+    // -------------------------------------------------------------- row threads
     const int qd = warp & 3, q = warp >> 2;  // lane quadrant, column quarter
     const int r = qd * 32 + lane;           // tile row = tensor-memory lane
-    const int gs = m0 + r;                  // flattened draft slot n * B + i
-    const int i = gs % B;
-    const bool live = gs < NB && (chunk == 0 || i < B - 1);
     float x[kQ];
+    const bool ok0 = rows_all(mbar_wait(smem_u32(&bar_in), 0, &s_abort, err) && !s_abort);
 #pragma unroll
-    for (int k = 0; k < kQ; ++k) x[k] = 0.f;
-    if (chunk == 0) {
-      if (live) load32(x, slot_proj + (int64_t)gs * 3 * kR + q * kQ);
-      ln0_part(x, eps, s_red[0], s_red[1], r, q);
-    } else if (live) {
-      // s_p = W_pair[:, :d] h_p + W_pair[:, d:] h_{p+1}
-      float y[kQ];
-      load32(x, slot_proj + (int64_t)gs * 3 * kR + kR + q * kQ);
-      load32(y, slot_proj + (int64_t)(gs + 1) * 3 * kR + 2 * kR + q * kQ);
-#pragma unroll
-      for (int k = 0; k < kQ; ++k) x[k] += y[k];
+    for (int c = 0; c < 8; ++c) {
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (ok0) {
+        v = *reinterpret_cast<const float4 *>(box_chunk(smem + kSlotOffX + q * kBox, r, c));
+        if (chunk != 0) {
+          const float4 y = *reinterpret_cast<const float4 *>(box_chunk(smem + kSlotOffY + q * kBox, r, c));
+          v.x += y.x; v.y += y.y; v.z += y.z; v.w += y.w;
+        }
+      }
+      x[4 * c] = v.x; x[4 * c + 1] = v.y; x[4 * c + 2] = v.z; x[4 * c + 3] = v.w;
     }
-    store_split_part(smem + kOffA, smem + kOffA + kMat, r, q, x);
+    if (chunk == 0)
+      ln0_part(x, eps, s_red[0], s_red[1], r, q);  // holds row barriers
+    else
+      rows_sync();  // every row thread has read X before it becomes the A operand
+    store_split_part(smem + kSlotOffX, smem + kSlotOffX + kMat, r, q, x);
     fence_proxy_async();
     mbar_arrive(smem_u32(&bar_a));
 
@@ -246,22 +279,25 @@ k_slot_mlp_tc(const __grid_constant__ CUtensorMap map_fg_hi, const __grid_consta
     if (ok) {
       float v[kQ];
       tmem_ld32(tmem + ((uint32_t)(qd * 32) << 16) + q * kQ, v);
-      if (live) {
-        float *dst;
-        if (chunk == 0) {
-          dst = Gf + (int64_t)gs * kR + q * kQ;
-        } else {
-          const int n = gs / B;
-          dst = P + ((int64_t)n * (B - 1) + i) * kH + (chunk - 1) * 128 + q * kQ;
-          float bb[kQ];
-          load32(bb, b1 + (chunk - 1) * 128 + q * kQ);
+      if (chunk != 0) {
+        float bb[kQ];
+        load32(bb, b1 + (chunk - 1) * 128 + q * kQ);
 #pragma unroll
-          for (int k = 0; k < kQ; ++k) v[k] += bb[k];
-        }
-        float4 *d4 = reinterpret_cast<float4 *>(dst);
-#pragma unroll
-        for (int k = 0; k < kQ / 4; ++k) d4[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+        for (int k = 0; k < kQ; ++k) v[k] += bb[k];
       }
+      // the output tile: quarter q is box q of Y (free since the row barrier above)
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<float4 *>(box_chunk(smem + kSlotOffY + q * kBox, r, c)) =
+            make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+    }
+    fence_proxy_async();
+    if (rows_all(ok) && tid == 0) {
+      const CUtensorMap *map = chunk == 0 ? &map_gf : &map_p;
+      const int x0 = chunk == 0 ? 0 : (chunk - 1) * 128;
+      for (int bx = 0; bx < 4; ++bx) tma_store_2d(map, sb + kSlotOffY + bx * kBox, x0 + bx * 32, m0);
+      bulk_commit();
+      bulk_wait_all();
     }
   }
 
@@ -269,6 +305,7 @@ k_slot_mlp_tc(const __grid_constant__ CUtensorMap map_fg_hi, const __grid_consta
   __syncthreads();
   if (s_abort && warp == kRowWarps && lane == 0) {
     mbar_drain(smem_u32(&bar_w), 0);
+    mbar_drain(smem_u32(&bar_in), 0);
     mbar_drain(smem_u32(&bar_mma), 0);
   }
   __syncthreads();
@@ -290,14 +327,8 @@ k_slot_mlp_tc(const __grid_constant__ CUtensorMap map_fg_hi, const __grid_consta
 // All tiles move by TMA; the fp32 boxes use the same 128-byte swizzle as the
 // bf16 operands, so the row threads' 16-byte accesses are conflict-free.
 constexpr int kOffS = 4 * kMat;
-constexpr int kBox = 128 * 128;  // one fp32 box: 128 rows x 32 columns, 16 KB
 constexpr int kCandSmemBytes = 6 * kMat + 1024;
 constexpr uint32_t kCandTmemCols = 512;
-
-// 16-byte chunk c of row r in a swizzled 128-byte-row box at `box`.
-__device__ __forceinline__ uint8_t *box_chunk(uint8_t *box, int r, int c) {
-  return box + r * 128 + ((c ^ (r & 7)) * 16);
-}
 
 __global__ void __launch_bounds__(kThreads, 1)
 k_cand_mlp_tc(const __grid_constant__ CUtensorMap map_fb_hi, const __grid_constant__ CUtensorMap map_fb_lo,
@@ -348,7 +379,7 @@ k_cand_mlp_tc(const __grid_constant__ CUtensorMap map_fb_hi, const __grid_consta
     if (lane == 0) {
       // ------------------------------------------------------------ control thread
       load_pair(w0_hi, w0_lo, &map_fb_hi, &map_fb_lo, 0, smem_u32(&bar_w0));
-      pdl_wait();  // cand_proj comes from the previous kernel
+      pdl_wait();  // cand_proj and Gf come from the previous kernels
       mbar_arrive_expect_tx(smem_u32(&bar_s), 4 * kBox);
       for (int bx = 0; bx < 4; ++bx) tma_load_2d(s_hi + bx * kBox, &map_cp, bx * 32, m0, smem_u32(&bar_s));
       // y = W_fuse[:, :r] b
@@ -477,16 +508,17 @@ k_cand_mlp_tc(const __grid_constant__ CUtensorMap map_fb_hi, const __grid_consta
 
 }  // namespace
 
-cudaError_t launch_slot_mlp_tc(const MlpMaps &maps, const float *slot_proj, const MlpWeightsDev &w, int N,
-                               int B, float eps, float *Gf, float *P, int *err, cudaStream_t st) {
+cudaError_t launch_slot_mlp_tc(const MlpMaps &maps, const SlotIoMaps &io, const MlpWeightsDev &w, int N, int B,
+                               float eps, int *err, cudaStream_t st, bool pdl) {
   const int NB = N * B;
   if (NB == 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(k_slot_mlp_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSlotSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid(3, (NB + kRows - 1) / kRows);
-  k_slot_mlp_tc<<<grid, kThreads, kSlotSmemBytes, st>>>(maps.fg_hi, maps.fg_lo, maps.w1s_hi, maps.w1s_lo,
-                                                        slot_proj, w.b1, NB, B, eps, Gf, P, err);
+  e = launch_ex(k_slot_mlp_tc, grid, dim3(kThreads), kSlotSmemBytes, st, pdl, 0, maps.fg_hi, maps.fg_lo,
+                maps.w1s_hi, maps.w1s_lo, io.sp, io.gf, io.p, w.b1, eps, err);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

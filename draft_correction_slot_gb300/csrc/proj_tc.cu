@@ -22,6 +22,10 @@
 // Split-K over gridDim.z: the splits of a tile form one thread-block
 // cluster and add their partial tiles through distributed shared memory in
 // split order, so the result does not depend on timing.
+// One launch serves up to two products ("jobs": the candidate rows and the
+// draft-slot rows), their tiles listed one after the other along gridDim.y,
+// so that both fill the device in a single wave.  Draft-slot tiles depend on
+// nothing the previous kernel writes and start without waiting for it.
 // Every wait is bounded in time; on expiry the kernel records kErrTimeout in
 // the device status word and does not store its rows.
 #include <cuda.h>
@@ -98,11 +102,12 @@ __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
   return v;
 }
 
-template <int MODE, int MT>
+template <int MT>
 __global__ void __launch_bounds__(ProjGeom<MT>::kThreads, 1)
-k_proj_tc(const uint16_t *__restrict__ table, const __grid_constant__ CUtensorMap map_hi,
-          const __grid_constant__ CUtensorMap map_lo, const int32_t *__restrict__ ids, int slots,
-          int B, int M, int d, int V, int No, int kb_per_split, float *__restrict__ C, int *err) {
+k_proj_tc(ProjJob job0, ProjJob job1, const __grid_constant__ CUtensorMap map0_hi,
+          const __grid_constant__ CUtensorMap map0_lo, const __grid_constant__ CUtensorMap map1_hi,
+          const __grid_constant__ CUtensorMap map1_lo, int slots, int B, int d, int V, int kb_per_split,
+          int *err) {
   using G = ProjGeom<MT>;
   constexpr int kTileM = G::kTileM, kStagesA = G::kStagesA, kStagesW = G::kStagesW;
   extern __shared__ uint8_t smem_raw[];
@@ -115,7 +120,18 @@ k_proj_tc(const uint16_t *__restrict__ table, const __grid_constant__ CUtensorMa
   __shared__ int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n0 = blockIdx.x * kTileN, m0 = blockIdx.y * kTileM, split = blockIdx.z;
+  // this CTA's job and tile: job 0's tiles come first along y
+  const bool second = (int)blockIdx.y >= job0.tiles;
+  const ProjJob &job = second ? job1 : job0;
+  const CUtensorMap *map_hi = second ? &map1_hi : &map0_hi;
+  const CUtensorMap *map_lo = second ? &map1_lo : &map0_lo;
+  const int tile = (int)blockIdx.y - (second ? job0.tiles : 0);
+  const int ntn = job.No / kTileN;
+  const int n0 = (tile % ntn) * kTileN, m0 = (tile / ntn) * kTileM, split = blockIdx.z;
+  const int M = job.M, No = job.No;
+  const uint16_t *__restrict__ table = job.table;
+  const int32_t *__restrict__ ids = job.ids;
+  float *__restrict__ C = job.C;
   const int nkb_total = d / kTileK;
   const int kb0 = split * kb_per_split;
   const int nkb = min(kb_per_split, nkb_total - kb0);
@@ -135,12 +151,15 @@ k_proj_tc(const uint16_t *__restrict__ table, const __grid_constant__ CUtensorMa
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  pdl_wait();  // the row ids (and this call's outputs) belong to the previous kernel until here
+  // A gathered job's row ids come from the previous kernel; a draft-slot job
+  // reads only the call's inputs and writes a buffer no earlier kernel of the
+  // call touches, so it need not wait.
+  if (ids) pdl_wait();
   if (tid < kTileM) {
     const int m = m0 + tid;
     int row = 0;  // rows past M load table row 0; their results are never stored
     if (m < M) {
-      if (MODE == 0) {
+      if (ids) {
         row = ids[m];
         if (row < 0 || row >= V) {
           atomicOr(err, kErrBadCandidateId);
@@ -203,8 +222,8 @@ k_proj_tc(const uint16_t *__restrict__ table, const __grid_constant__ CUtensorMa
         const uint32_t sw = sbase + G::kRingA + s * 2 * kSubBytes;
         const int kx = (kb0 + it) * kTileK;
         mbar_arrive_expect_tx(full, kStageTx);
-        tma_load_2d(sw, &map_hi, kx, n0, full);
-        tma_load_2d(sw + kSubBytes, &map_lo, kx, n0, full);
+        tma_load_2d(sw, map_hi, kx, n0, full);
+        tma_load_2d(sw + kSubBytes, map_lo, kx, n0, full);
       }
     }
   } else if (warp == G::kWarpMma && lane == 0) {
@@ -390,38 +409,35 @@ bool encode_f32_rows_map(CUtensorMap *map, const void *base, int rows, int cols,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE, int MT>
-static cudaError_t launch_mode(int M, int splits, int No, int d, cudaStream_t st, bool pdl, const uint16_t *table,
-                               const CUtensorMap &map_hi, const CUtensorMap &map_lo, const int32_t *ids,
-                               int slots, int B, int V, float *C, int *err) {
+cudaError_t launch_proj_tc(const ProjJob &a, const CUtensorMap &a_hi, const CUtensorMap &a_lo,
+                           const ProjJob *b, const CUtensorMap *b_hi, const CUtensorMap *b_lo, int slots,
+                           int B, int d, int V, int splits, int *err, cudaStream_t st, bool pdl) {
+  constexpr int MT = 2;
   using G = ProjGeom<MT>;
+  auto bad = [&](const ProjJob &j) {
+    return j.No % kTileN != 0 || j.M < 0 || !j.table || !j.C ||
+           j.tiles != ((j.M + G::kTileM - 1) / G::kTileM) * (j.No / kTileN);
+  };
+  if (d % kTileK != 0 || splits < 1 || splits > kMaxSplits || (kSubM % splits) != 0 || bad(a) ||
+      (b && (bad(*b) || !b_hi || !b_lo)))
+    return cudaErrorInvalidValue;
+  const ProjJob none{};
+  const ProjJob &j1 = b ? *b : none;
+  const int tiles = a.tiles + j1.tiles;
+  if (tiles == 0) return cudaSuccess;
   const int nkb = d / kTileK;
   const int per = (nkb + splits - 1) / splits;
-  const dim3 grid(No / kTileN, (M + G::kTileM - 1) / G::kTileM, splits);
+  const dim3 grid(1, tiles, splits);
   const size_t smem = (size_t)G::kSmemUsed + 1024;
-  cudaError_t e = cudaFuncSetAttribute(k_proj_tc<MODE, MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = cudaFuncSetAttribute(k_proj_tc<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   // the splits of one tile form a cluster
-  return launch_ex(k_proj_tc<MODE, MT>, grid, dim3(G::kThreads), smem, st, pdl, grid.z, table, map_hi, map_lo, ids,
-                   slots, B, M, d, V, No, per, C, err);
-}
-
-cudaError_t launch_proj_tc(int mode, int rows_per_cta, const uint16_t *table, const CUtensorMap &map_hi,
-                           const CUtensorMap &map_lo, const int32_t *ids, int slots, int B, int M, int d,
-                           int V, int No, int splits, float *C, int *err, cudaStream_t st, bool pdl) {
-  if (M == 0) return cudaSuccess;
-  if (No % kTileN != 0 || d % kTileK != 0 || splits < 1 || splits > kMaxSplits || (kSubM % splits) != 0 ||
-      (rows_per_cta != 128 && rows_per_cta != 256))
-    return cudaErrorInvalidValue;
-  cudaError_t e;
-  if (rows_per_cta == 128)
-    e = mode == 0 ? launch_mode<0, 1>(M, splits, No, d, st, pdl, table, map_hi, map_lo, ids, slots, B, V, C, err)
-                  : launch_mode<1, 1>(M, splits, No, d, st, pdl, table, map_hi, map_lo, ids, slots, B, V, C, err);
-  else
-    e = mode == 0 ? launch_mode<0, 2>(M, splits, No, d, st, pdl, table, map_hi, map_lo, ids, slots, B, V, C, err)
-                  : launch_mode<1, 2>(M, splits, No, d, st, pdl, table, map_hi, map_lo, ids, slots, B, V, C, err);
+  e = launch_ex(k_proj_tc<MT>, grid, dim3(G::kThreads), smem, st, pdl, grid.z, a, j1, a_hi, a_lo,
+                b ? *b_hi : a_hi, b ? *b_lo : a_lo, slots, B, d, V, per, err);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
+
+int proj_tc_tiles(int M, int No) { return ((M + 2 * kSubM - 1) / (2 * kSubM)) * (No / kTileN); }
 
 }  // namespace dc

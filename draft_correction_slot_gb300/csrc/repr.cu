@@ -114,7 +114,7 @@ k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
   pdl_wait();  // U, V (and this call's outputs) belong to the previous kernel until here
   const int64_t ca = ((int64_t)n * B + p) * K;      // first candidate of slot p
   const int64_t cb = ca + K;                         // first candidate of slot p+1
-  const float *Pp = P + (int64_t)np * H;
+  const float *Pp = P + ((int64_t)n * B + p) * H;  // P is indexed by draft slot
 
   for (int e4 = tid; e4 < K * H / 4; e4 += 256) {
     const int c = e4 / (H / 4), j = (e4 - c * (H / 4)) * 4;
