@@ -283,11 +283,27 @@ template <int K>
 static cudaError_t pair_score_k(const float *U, const float *V, const float *P, const float *tv,
                                 const float *w2, const float *b2, int N, int B, float *scores,
                                 const WalkArgs &wk, cudaStream_t st) {
-  const size_t smem = PairGeom<K>::smem_floats * sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(k_pair_score<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  // The blocks are launched early (programmatic overlap) onto whatever SMs
+  // the previous kernel frees first; more than the even share per SM would
+  // leave those SMs finishing last.  The shared-memory request caps the
+  // resident blocks per SM at ceil(blocks / SMs).
+  const int blocks = N * (B - 1);
+  int dev = 0, sms = 1, sm_smem = 0, reserved = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
   if (e != cudaSuccess) return e;
-  e = launch_ex(k_pair_score<K>, dim3(N * (B - 1)), dim3(256), smem, st, true, 0, U, V, P, tv, w2, b2, B, scores,
+  size_t smem = PairGeom<K>::smem_floats * sizeof(float);
+  const int per_sm = (blocks + sms - 1) / sms;
+  if (per_sm < 8) {
+    // one block more than per_sm must not fit: (per_sm + 1) (smem + reserved) > sm_smem
+    const size_t cap = (size_t)(sm_smem / (per_sm + 1) - reserved + 16) & ~size_t(15);
+    if (cap > smem && (size_t)per_sm * (cap + reserved) <= (size_t)sm_smem) smem = cap;
+  }
+  e = cudaFuncSetAttribute(k_pair_score<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  e = launch_ex(k_pair_score<K>, dim3(blocks), dim3(256), smem, st, true, 0, U, V, P, tv, w2, b2, B, scores,
                 wk);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
