@@ -7,18 +7,22 @@
 // projected by bias-free maps (W_cand; W_ctx and the two halves of W_pair).
 //
 // Precision: A (bf16) is exact; each fp32 weight is split into bf16 hi + lo
-// (w = hi + lo to ~2^-17 relative), and both products accumulate into the same
-// fp32 accumulator: C = A hi^T + A lo^T.
+// (w = hi + lo to ~2^-17 relative).  The hi and lo blocks of a k-block sit
+// one after the other in shared memory, so one N = 256 MMA takes both: its
+// accumulator holds A hi^T in columns [0, 128) and A lo^T in [128, 256), and
+// the epilogue adds the two (fp32).  One N = 256 instruction reads the A
+// block once for both halves.
 //
-// Tile: 128 rows x 128 outputs, k-blocks of 64 (one 128-byte swizzle atom)
-// in 128B-swizzled K-major shared memory.  Each operand takes the path that
-// suits it: warps 0-3 gather the A rows with 16-byte cp.async into an
-// 8-deep ring (many small independent rows from HBM: the depth keeps enough
-// bytes in flight), one thread of warp 4 brings the hi and lo weight blocks
-// as two 2D TMA tiles into a 3-deep ring (the same blocks for every CTA,
-// served from L2).  One thread of warp 5 (which also owns the tensor-memory
-// allocation) issues the MMAs once both rings hold the k-block; warps 0-3
-// then drain the accumulator with tcgen05.ld into shared memory.
+// Tile: 256 rows (two 128-row accumulators) x 128 outputs, k-blocks of 64
+// (one 128-byte swizzle atom) in 128B-swizzled K-major shared memory.  Each
+// operand takes the path that suits it: warps 0-7 gather the A rows with
+// 16-byte cp.async into a 4-deep ring (many small independent rows from HBM:
+// the depth keeps enough bytes in flight), one thread of warp 8 brings the hi
+// and lo weight blocks as two 2D TMA tiles into a 3-deep ring (the same
+// blocks for every CTA, served from L2).  One thread of warp 9 (which also
+// owns the tensor-memory allocation) issues the MMAs once both rings hold the
+// k-block; warps 0-7 then drain the accumulators with tcgen05.ld into shared
+// memory.
 // Split-K over gridDim.z: the splits of a tile form one thread-block
 // cluster and add their partial tiles through distributed shared memory in
 // split order, so the result does not depend on timing.
@@ -46,7 +50,7 @@ constexpr int kSubBytes = kSubM * kTileK * 2;          // 16 KB: 128 rows x 64 k
 constexpr uint32_t kStageTx = 2u * kSubBytes;          // weight bytes per k-block (hi + lo)
 constexpr int kMaxSplits = 8;       // a cluster of at most 8 CTAs (portable size)
 constexpr int kBoxBytes = kSubM * 128;  // one 32-column fp32 box of a 128-row output tile
-constexpr uint32_t kIdesc = tc::idesc_bf16(kSubM, kTileN);
+constexpr uint32_t kIdesc = tc::idesc_bf16(kSubM, 2 * kTileN);  // hi and lo blocks stacked
 
 // A CTA owns MT x 128 rows (MT accumulators of 128 x 128 in tensor memory)
 // so that every weight k-block it brings in feeds MT MMAs.  Two rings: the
@@ -62,7 +66,7 @@ struct ProjGeom {
   static constexpr int kStagesA = MT == 1 ? 8 : 4, kStagesW = 3;
   static constexpr int kRingA = kStagesA * kStageA;      // A ring, then the W ring
   static constexpr int kSmemUsed = kRingA + kStagesW * 2 * kSubBytes;
-  static constexpr uint32_t kTmemCols = MT * 128;
+  static constexpr uint32_t kTmemCols = MT * 256;  // per accumulator: hi products, then lo
   static_assert(kSmemUsed + 1024 <= 227 * 1024 - 1024, "shared memory");
   static_assert(MT * 4 * kBoxBytes <= kRingA, "the output tile is staged in the A ring");
 };
@@ -237,12 +241,13 @@ k_proj_tc(ProjJob job0, ProjJob job1, const __grid_constant__ CUtensorMap map0_h
       const uint32_t sa = sbase + s * G::kStageA, sw = sbase + G::kRingA + t * 2 * kSubBytes;
 #pragma unroll
       for (int k = 0; k < kTileK / 16; ++k) {
-        const uint64_t bh = sw128_desc(sw + k * 32), bl = sw128_desc(sw + kSubBytes + k * 32);
+        // B = 256 rows: the hi block's 128, then the lo block's (16 KB further,
+        // the next 8-row groups at the descriptor's 1024-byte stride)
+        const uint64_t bd = sw128_desc(sw + k * 32);
 #pragma unroll
         for (int h = 0; h < MT; ++h) {
           const uint64_t ad = sw128_desc(sa + h * kSubBytes + k * 32);
-          mma_bf16(tmem + h * 128, ad, bh, kIdesc, (it > 0 || k > 0) ? 1u : 0u);
-          mma_bf16(tmem + h * 128, ad, bl, kIdesc, 1u);
+          mma_bf16(tmem + h * 256, ad, bd, kIdesc, (it > 0 || k > 0) ? 1u : 0u);
         }
       }
       mma_commit(smem_u32(&empty_a[s]));
@@ -265,8 +270,12 @@ k_proj_tc(ProjJob job0, ProjJob job1, const __grid_constant__ CUtensorMap map0_h
       const int r = q4 * 32 + lane;              // row within the accumulator
 #pragma unroll 1
       for (int cc = 0; cc < kTileN / 32; ++cc) {
-        float v[32];
-        tmem_ld32(tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(sub * 128 + cc * 32), v);
+        float v[32], vl[32];
+        const uint32_t t0 = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(sub * 256 + cc * 32);
+        tmem_ld32(t0, v);
+        tmem_ld32(t0 + 128, vl);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] += vl[k];
         if (nkb <= 0)  // an empty split holds no products
 #pragma unroll
           for (int k = 0; k < 32; ++k) v[k] = 0.f;
