@@ -76,8 +76,8 @@ def stage_model(w, pk):
     return {
         "topk": ("hbm", "GB/s", N * B * V * 2, pk["hbm_gbs"]),
         "proj": ("hbm", "GB/s", N * B * K * d * 2 + N * B * d * 2, pk["hbm_gbs"]),
-        "slot_post": ("alu", "TFLOP/s", 2 * N * (B * r * r + (B - 1) * r * H), alu_peak),
-        "cand_post": ("alu", "TFLOP/s", 2 * N * B * K * (r * r + 2 * r * H), alu_peak),
+        "maps": ("alu", "TFLOP/s", 2 * N * (B * r * r + (B - 1) * r * H) + 2 * N * B * K * (r * r + 2 * r * H),
+                 alu_peak),
         "pair_walk": ("alu", "TFLOP/s", 2 * N * (B - 1) * K * K * H, alu_peak),
     }
 

@@ -31,6 +31,7 @@ struct Workspace {
   float *margin = nullptr;     // [N*(B-1)]
   int *err = nullptr;          // device status word
   unsigned *req_count = nullptr;  // finished pairs per request (zero between calls)
+  unsigned *gf_ready = nullptr;   // per 128-slot tile: its Gf rows are written (zero between calls)
   // host staging (dcoco_correct_host)
   uint16_t *st_logits = nullptr;  // [N][slots][st_stride]
   int64_t st_stride = 0;
@@ -46,7 +47,7 @@ namespace {
 constexpr int kMaxStages = 8;
 constexpr int kMaxTimedCalls = 1024;
 const char *const kStageNames[2][kMaxStages] = {
-    {"topk", "proj", "slot_post", "cand_post", "pair_walk", nullptr, nullptr, nullptr},
+    {"topk", "proj", "maps", "pair_walk", nullptr, nullptr, nullptr, nullptr},
     {"topk", "proj", "cos_post", "cos_score", "walk_verify", nullptr, nullptr, nullptr}};
 int stage_count(int variant) {
   int n = 0;
@@ -66,7 +67,7 @@ struct dcoco_handle {
   void *block = nullptr;  // one device allocation holding the workspace
   Workspace ws;
   dc::CandIoMaps cand_io;  // TMA maps of cand_proj, U, V (variant 0)
-  dc::SlotIoMaps slot_io;  // TMA maps of slot_proj, Gf, P (variant 0)
+  dc::SlotIoMaps slot_io;  // TMA maps of slot_proj, P (variant 0)
   cudaStream_t last_stream = nullptr;
   long long launches = 0;            // kernels launched so far
   bool timing = false;               // record per-stage events
@@ -140,6 +141,7 @@ void carve_workspace(Carver &c, const dcoco_config &cfg, int B, int topk_segment
   ws.margin = c.take<float>(N * (B - 1));
   ws.err = c.take<int>(1);
   ws.req_count = c.take<unsigned>(N);
+  ws.gf_ready = c.take<unsigned>((rows + 127) / 128);
   if (cfg.host_staging) {
     ws.st_stride = ((int64_t)cfg.vocab + 7) & ~int64_t(7);
     ws.st_logits = c.take<uint16_t>(N * cfg.slots * (size_t)ws.st_stride);
@@ -246,15 +248,14 @@ int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs 
   DC_TRY(clk.done(dc::launch_proj_tc(cj, w->map_cand_hi, w->map_cand_lo, &sj, &w->map_slot_hi,
                                      &w->map_slot_lo, cfg.slots, B, d, V, h->splits, ws.err, st, true)));
   if (cfg.variant == 0) {
-    // steps 2-3: per-slot / per-pair terms, then z and the layer-1 partials U, V
-    DC_TRY(clk.done(dc::launch_slot_mlp_tc(w->mlp_maps, h->slot_io, w->mlp, N, B, cfg.ln_eps, ws.err, st,
-                                           true)));
-    DC_TRY(clk.done(dc::launch_cand_mlp_tc(w->mlp_maps, h->cand_io, ws.Gf, vals, w->mlp, K, cands,
-                                           cfg.ln_eps, ws.err, st)));
+    // steps 2-3: per-slot / per-pair terms, z and the layer-1 partials U, V
+    DC_TRY(clk.done(dc::launch_maps_tc(w->mlp_maps, h->slot_io, h->cand_io, ws.Gf, ws.gf_ready,
+                                       cfg.max_batch * B, vals, w->mlp, N, B, K, cfg.ln_eps, ws.err, st)));
     // steps 4-5: all (B-1) K^2 transition scores, then each request's walk
     // and verify in its last block
     const dc::WalkArgs wk{ids, in->target_tokens, out->tokens, choice,
-                          in->target_tokens ? out->accept_len : nullptr, margin, ws.req_count};
+                          in->target_tokens ? out->accept_len : nullptr, margin, ws.req_count,
+                          ws.gf_ready, (rows + 127) / 128};
     DC_TRY(clk.done(dc::launch_pair_score_walk(K, ws.U, ws.V, ws.P, vals, w->mlp.w2, w->mlp.b2, N, B,
                                                scores, wk, st)));
     return DCOCO_OK;
@@ -349,7 +350,6 @@ int dcoco_create(const dcoco_config *cfg, dcoco_handle **out) {
        dc::encode_f32_rows_map(&h->cand_io.u, h->ws.U, cands_cap, kH, 128) &&
        dc::encode_f32_rows_map(&h->cand_io.v, h->ws.V, cands_cap, kH, 128) &&
        dc::encode_f32_rows_map(&h->slot_io.sp, h->ws.slot_proj, rows_cap, 3 * kR, 128) &&
-       dc::encode_f32_rows_map(&h->slot_io.gf, h->ws.Gf, rows_cap, kR, 128) &&
        dc::encode_f32_rows_map(&h->slot_io.p, h->ws.P, rows_cap, kH, 128));
   if (!maps_ok || cudaMemset(h->block, 0, bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) {
     cudaGetLastError();

@@ -83,31 +83,32 @@ struct MlpWeightsDev {
 struct MlpMaps {
   CUtensorMap fb_hi, fb_lo, w1_hi, w1_lo, fg_hi, fg_lo, w1s_hi, w1s_lo;
 };
-// Per draft slot: Gf = W_fuse[:, r:] LN0(W_ctx h) ([N*B][r]); per draft slot
+// The per-slot and per-candidate maps, in one launch.
+// Per draft slot: Gf = W_fuse[:, r:] LN0(W_ctx h) ([rows][r]); per draft slot
 // i (used for i < B-1): P_i = W1[:, :r] (W_pair[:, :d] h_i + W_pair[:, d:] h_{i+1})
-// + b1 ([N*B][H]).  slot_proj is [N*B][3r] = (W_ctx h | W_pair[:, :d] h | W_pair[:, d:] h).
-// The tiles move by TMA: `sp` reads slot_proj, `gf` and `p` write Gf and P;
-// all three are fp32 maps with box 32 x 128 over the same row count (>= N*B).
-// With `pdl` the launch may overlap the end of the previous kernel in the
-// stream (the kernel waits for it before it reads slot_proj).
-struct SlotIoMaps {
-  CUtensorMap sp, gf, p;
-};
-cudaError_t launch_slot_mlp_tc(const MlpMaps &maps, const SlotIoMaps &io, const MlpWeightsDev &w, int N, int B,
-                               float eps, int *err, cudaStream_t st, bool pdl);
+// + b1 ([rows][H]).  slot_proj is [N*B][3r] = (W_ctx h | W_pair[:, :d] h | W_pair[:, d:] h).
 // Per candidate: b = LN0(cand_proj), z = gamma*LN0(W_fuse[:, :r] b + Gf) + beta,
 // U = W1_a z + w_la l, V = W1_b z + w_lb l.  M = N * B * K candidates,
-// candidate m belongs to draft slot m / K.  The candidate tiles move by TMA: `io.cp`
-// reads cand_proj ([rows][r] fp32), `io.u` / `io.v` write U and V ([rows][H]
-// fp32); all three are fp32 maps with box 32 x 128 over the same row count
-// (>= M).  Rows of the last tile past M that lie inside the maps receive
-// the outputs of an all-zero input row.
+// candidate m belongs to draft slot m / K.
+// Tiles move by TMA: `slot.sp` reads slot_proj, `slot.p` writes P, `cand.cp`
+// reads cand_proj ([rows][r]), `cand.u` / `cand.v` write U and V ([rows][H]);
+// all are fp32 maps with box 32 x 128 over at least the call's rows (rows of
+// the last tile past the call's count receive the outputs of stale or
+// all-zero input rows).  Gf ([rows_cap][r]) is written and read inside the
+// launch: its slot blocks set gf_ready[tile] (ceil(N*B / 128) entries, zero
+// before the launch) and the candidate blocks wait for it, so the grid
+// (3 blocks per 128 slots + 2 per 128 candidates) must fit on the device at
+// once; the next kernel in the stream zeroes the flags again.  The launch
+// may overlap the end of the previous kernel (programmatic serialization).
+struct SlotIoMaps {
+  CUtensorMap sp, p;
+};
 struct CandIoMaps {
   CUtensorMap cp, u, v;
 };
-cudaError_t launch_cand_mlp_tc(const MlpMaps &maps, const CandIoMaps &io, const float *Gf,
-                               const float *topk_val, const MlpWeightsDev &w, int K, int M, float eps,
-                               int *err, cudaStream_t st);
+cudaError_t launch_maps_tc(const MlpMaps &maps, const SlotIoMaps &slot, const CandIoMaps &cand, const float *Gf,
+                           unsigned *gf_ready, int rows_cap, const float *topk_val, const MlpWeightsDev &w,
+                           int N, int B, int K, float eps, int *err, cudaStream_t st);
 
 // Step 5 outputs and state for a launch that ends with the walk: per-request
 // arrays as in launch_walk_verify, and req_count (N entries, zero between
@@ -118,6 +119,8 @@ struct WalkArgs {
   int32_t *tokens, *choice, *accept_len;
   float *margin;
   unsigned *req_count;
+  unsigned *flags;  // zeroed once the launch may start (the previous kernel is done), or null
+  int nflags;
 };
 
 // S[n,p,a,b] = l_{p+1}(b) + b2 + sum_j w2_j GELU(P_pj + U_{p,a,j} + V_{p+1,b,j}),

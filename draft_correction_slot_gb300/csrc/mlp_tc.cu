@@ -48,6 +48,22 @@ constexpr int kQ = 32;                       // columns per row thread
 constexpr uint32_t kIdesc = idesc_bf16(128, 128);
 constexpr uint32_t kWTx = 2 * kMat;          // one matrix pair (hi + lo): 64 KB
 
+// Everything one launch of k_maps_tc needs (a __grid_constant__ parameter, so
+// the tensor maps stay in parameter space for the TMA instructions).
+struct MapsParams {
+  MlpMaps maps;
+  SlotIoMaps slot;
+  CandIoMaps cand;
+  float *Gf;             // [rows_cap][r]
+  unsigned *gf_ready;    // per slot tile: 1 once its Gf rows are written (zeroed by the next kernel)
+  const float *topk_val, *gamma, *beta, *w_la, *w_lb, *b1;
+  int rows_cap;          // rows of Gf
+  int slot_ctas;         // 3 per 128-slot tile
+  int K, M;              // candidates per slot, candidates in the call
+  float eps;
+  int *err;
+};
+
 __device__ __forceinline__ uint32_t bf16_rn_bits(float f) {
   return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
@@ -172,26 +188,57 @@ __device__ __forceinline__ void load_pair(uint32_t w_hi, uint32_t w_lo, const CU
   }
 }
 
+// Bounded spin on a ready flag written by another block of the same launch
+// (acquire at gpu scope).  false on timeout (kErrTimeout) or abort.
+__device__ __forceinline__ bool flag_wait(const unsigned *flag, volatile int *abort, int *err) {
+  const unsigned long long t0 = global_ns();
+  for (uint32_t it = 0;; ++it) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v != 0u) return true;
+    if ((it & 15u) == 15u) {
+      if (*abort) return false;
+      if (global_ns() - t0 > kWaitNs) {
+        *abort = 1;
+        atomicOr(err, ::dc::kErrTimeout);
+        return false;
+      }
+      __nanosleep(64);
+    }
+  }
+}
+__device__ __forceinline__ void st_release_gpu(unsigned *flag, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(v) : "memory");
+}
+// load32 through L2 only: data written earlier in the same launch.
+__device__ __forceinline__ void load32_cg(float (&x)[kQ], const float *src) {
+  const float4 *s4 = reinterpret_cast<const float4 *>(src);
+#pragma unroll
+  for (int i = 0; i < kQ / 4; ++i) {
+    const float4 v = __ldcg(s4 + i);
+    x[4 * i] = v.x; x[4 * i + 1] = v.y; x[4 * i + 2] = v.z; x[4 * i + 3] = v.w;
+  }
+}
+
 // ---------------------------------------------------------------- per draft slot
 // One CTA per (128-slot tile, output chunk): chunk 0 writes Gf = W_fuse[:, r:] g
 // for every slot; chunks 1 and 2 write the two 128-wide halves of
 // P_i = W1[:, :r] s_i + b1, s_i = W_pair[:, :d] h_i + W_pair[:, d:] h_{i+1},
 // indexed by draft slot (rows of the last slot of a request are not used).
 // slot_proj rows are (W_ctx h | W_pair[:, :d] h | W_pair[:, d:] h).
-// The input tiles arrive and the output tile leaves by TMA (fp32 boxes of 128
-// rows x 32 columns, 128-byte swizzled), so every row thread's 16-byte
-// shared-memory access is conflict-free and the global traffic is whole lines.
+// The input tiles arrive by TMA (fp32 boxes of 128 rows x 32 columns,
+// 128-byte swizzled), so every row thread's 16-byte shared-memory access is
+// conflict-free and the global traffic is whole lines.  P leaves by TMA; Gf is
+// read by candidate blocks of the same launch, so it is written with ordinary
+// coalesced stores and published by a per-tile ready flag (release), which
+// the candidate blocks wait for (acquire).
 // Shared memory: X (64 KB): the first input tile, then the A operand (hi, lo);
 // Y (64 KB): the second input tile (chunks 1, 2), then the output tile;
 // W (64 KB): the weight pair.
 constexpr int kSlotOffX = 0, kSlotOffY = 2 * kMat, kSlotOffW = 4 * kMat;
 constexpr int kSlotSmemBytes = 6 * kMat + 1024;
 
-__global__ void __launch_bounds__(kThreads, 1)
-k_slot_mlp_tc(const __grid_constant__ CUtensorMap map_fg_hi, const __grid_constant__ CUtensorMap map_fg_lo,
-              const __grid_constant__ CUtensorMap map_w1s_hi, const __grid_constant__ CUtensorMap map_w1s_lo,
-              const __grid_constant__ CUtensorMap map_sp, const __grid_constant__ CUtensorMap map_gf,
-              const __grid_constant__ CUtensorMap map_p, const float *__restrict__ b1, float eps, int *err) {
+__device__ __forceinline__ void slot_role(const MapsParams &mp, int chunk, int tile, float eps, int *err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ __align__(8) unsigned long long bar_w, bar_in, bar_a, bar_mma;
@@ -200,8 +247,7 @@ k_slot_mlp_tc(const __grid_constant__ CUtensorMap map_fg_hi, const __grid_consta
   __shared__ int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int chunk = blockIdx.x, m0 = blockIdx.y * kRows;
-  pdl_trigger();
+  const int m0 = tile * kRows;
   const uint32_t sb = smem_u32(smem);
   const uint32_t a_hi = sb + kSlotOffX, a_lo = sb + kSlotOffX + kMat;
   const uint32_t w_hi = sb + kSlotOffW, w_lo = sb + kSlotOffW + kMat;
@@ -224,20 +270,20 @@ k_slot_mlp_tc(const __grid_constant__ CUtensorMap map_fg_hi, const __grid_consta
     if (lane == 0) {
       // ------------------------------------------------------------ control thread
       if (chunk == 0)
-        load_pair(w_hi, w_lo, &map_fg_hi, &map_fg_lo, 0, smem_u32(&bar_w));
+        load_pair(w_hi, w_lo, &mp.maps.fg_hi, &mp.maps.fg_lo, 0, smem_u32(&bar_w));
       else
-        load_pair(w_hi, w_lo, &map_w1s_hi, &map_w1s_lo, (chunk - 1) * 128, smem_u32(&bar_w));
-      pdl_wait();  // slot_proj comes from the previous kernel
+        load_pair(w_hi, w_lo, &mp.maps.w1s_hi, &mp.maps.w1s_lo, (chunk - 1) * 128, smem_u32(&bar_w));
+      pdl_wait();  // slot_proj comes from the previous kernels
       // chunk 0: W_ctx h of the tile's slots; chunks 1, 2: W_pair[:, :d] h of
       // the tile's slots and W_pair[:, d:] h of the slots one row further on
       const uint32_t in = smem_u32(&bar_in);
       mbar_arrive_expect_tx(in, (chunk == 0 ? 4 : 8) * kBox);
       if (chunk == 0) {
-        for (int bx = 0; bx < 4; ++bx) tma_load_2d(sb + kSlotOffX + bx * kBox, &map_sp, bx * 32, m0, in);
+        for (int bx = 0; bx < 4; ++bx) tma_load_2d(sb + kSlotOffX + bx * kBox, &mp.slot.sp, bx * 32, m0, in);
       } else {
         for (int bx = 0; bx < 4; ++bx) {
-          tma_load_2d(sb + kSlotOffX + bx * kBox, &map_sp, kR + bx * 32, m0, in);
-          tma_load_2d(sb + kSlotOffY + bx * kBox, &map_sp, 2 * kR + bx * 32, m0 + 1, in);
+          tma_load_2d(sb + kSlotOffX + bx * kBox, &mp.slot.sp, kR + bx * 32, m0, in);
+          tma_load_2d(sb + kSlotOffY + bx * kBox, &mp.slot.sp, 2 * kR + bx * 32, m0 + 1, in);
         }
       }
       if (mbar_wait(smem_u32(&bar_w), 0, &s_abort, err) && mbar_wait(smem_u32(&bar_a), 0, &s_abort, err)) {
@@ -281,7 +327,7 @@ k_slot_mlp_tc(const __grid_constant__ CUtensorMap map_fg_hi, const __grid_consta
       tmem_ld32(tmem + ((uint32_t)(qd * 32) << 16) + q * kQ, v);
       if (chunk != 0) {
         float bb[kQ];
-        load32(bb, b1 + (chunk - 1) * 128 + q * kQ);
+        load32(bb, mp.b1 + (chunk - 1) * 128 + q * kQ);
 #pragma unroll
         for (int k = 0; k < kQ; ++k) v[k] += bb[k];
       }
@@ -291,13 +337,32 @@ k_slot_mlp_tc(const __grid_constant__ CUtensorMap map_fg_hi, const __grid_consta
         *reinterpret_cast<float4 *>(box_chunk(smem + kSlotOffY + q * kBox, r, c)) =
             make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
     }
-    fence_proxy_async();
-    if (rows_all(ok) && tid == 0) {
-      const CUtensorMap *map = chunk == 0 ? &map_gf : &map_p;
-      const int x0 = chunk == 0 ? 0 : (chunk - 1) * 128;
-      for (int bx = 0; bx < 4; ++bx) tma_store_2d(map, sb + kSlotOffY + bx * kBox, x0 + bx * 32, m0);
-      bulk_commit();
-      bulk_wait_all();
+    if (chunk == 0) {
+      // Gf: whole 512-byte rows, 16 bytes per thread per step, then the flag
+      const bool all_ok = rows_all(ok);
+      if (all_ok) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int e = tid + kRowThreads * j;  // 16-byte chunk of the 64 KB tile
+          const int row = e >> 5, c16 = e & 31;
+          if (m0 + row < mp.rows_cap) {
+            const float4 v4 = *reinterpret_cast<const float4 *>(
+                box_chunk(smem + kSlotOffY + (c16 >> 3) * kBox, row, c16 & 7));
+            __stcg(reinterpret_cast<float4 *>(mp.Gf + (int64_t)(m0 + row) * kR + c16 * 4), v4);
+          }
+        }
+      }
+      __threadfence();
+      rows_sync();
+      if (all_ok && tid == 0) st_release_gpu(mp.gf_ready + tile, 1u);
+    } else {
+      fence_proxy_async();
+      if (rows_all(ok) && tid == 0) {
+        for (int bx = 0; bx < 4; ++bx)
+          tma_store_2d(&mp.slot.p, sb + kSlotOffY + bx * kBox, (chunk - 1) * 128 + bx * 32, m0);
+        bulk_commit();
+        bulk_wait_all();
+      }
     }
   }
 
@@ -328,16 +393,11 @@ k_slot_mlp_tc(const __grid_constant__ CUtensorMap map_fg_hi, const __grid_consta
 // bf16 operands, so the row threads' 16-byte accesses are conflict-free.
 constexpr int kOffS = 4 * kMat;
 constexpr int kCandSmemBytes = 6 * kMat + 1024;
+constexpr int kMapsSmemBytes = kCandSmemBytes > kSlotSmemBytes ? kCandSmemBytes : kSlotSmemBytes;
 constexpr uint32_t kCandTmemCols = 512;
 
-__global__ void __launch_bounds__(kThreads, 1)
-k_cand_mlp_tc(const __grid_constant__ CUtensorMap map_fb_hi, const __grid_constant__ CUtensorMap map_fb_lo,
-              const __grid_constant__ CUtensorMap map_w1_hi, const __grid_constant__ CUtensorMap map_w1_lo,
-              const __grid_constant__ CUtensorMap map_cp, const __grid_constant__ CUtensorMap map_u,
-              const __grid_constant__ CUtensorMap map_v, const float *__restrict__ Gf,
-              const float *__restrict__ topk_val, const float *__restrict__ gamma,
-              const float *__restrict__ beta, const float *__restrict__ w_la,
-              const float *__restrict__ w_lb, int K, int M, float eps, int *err) {
+__device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int tile, int K, int M, float eps,
+                                          int *err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   __shared__ __align__(8) unsigned long long bar_w0, bar_s, bar_w1, bar_w2, bar_a, bar_fuse, bar_a2,
@@ -347,8 +407,8 @@ k_cand_mlp_tc(const __grid_constant__ CUtensorMap map_fb_hi, const __grid_consta
   __shared__ int s_abort;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int half = blockIdx.x, m0 = blockIdx.y * kRows;
-  pdl_trigger();
+  const int m0 = tile * kRows;
+  const int gf_tile = (m0 / K) / kRows;  // the slot tile holding this tile's draft slots
   const uint32_t sb = smem_u32(smem);
   const uint32_t a_hi = sb + kOffA, a_lo = sb + kOffA + kMat;
   const uint32_t w0_hi = sb + kOffW0, w0_lo = sb + kOffW0 + kMat;
@@ -378,22 +438,22 @@ k_cand_mlp_tc(const __grid_constant__ CUtensorMap map_fb_hi, const __grid_consta
   if (warp == kRowWarps) {
     if (lane == 0) {
       // ------------------------------------------------------------ control thread
-      load_pair(w0_hi, w0_lo, &map_fb_hi, &map_fb_lo, 0, smem_u32(&bar_w0));
-      pdl_wait();  // cand_proj and Gf come from the previous kernels
+      load_pair(w0_hi, w0_lo, &mp.maps.fb_hi, &mp.maps.fb_lo, 0, smem_u32(&bar_w0));
+      pdl_wait();  // cand_proj comes from the previous kernel
       mbar_arrive_expect_tx(smem_u32(&bar_s), 4 * kBox);
-      for (int bx = 0; bx < 4; ++bx) tma_load_2d(s_hi + bx * kBox, &map_cp, bx * 32, m0, smem_u32(&bar_s));
+      for (int bx = 0; bx < 4; ++bx) tma_load_2d(s_hi + bx * kBox, &mp.cand.cp, bx * 32, m0, smem_u32(&bar_s));
       // y = W_fuse[:, :r] b
       if (mbar_wait(smem_u32(&bar_w0), 0, &s_abort, err) && mbar_wait(smem_u32(&bar_a), 0, &s_abort, err)) {
         tc_fence_after();
         mma_split(tmem, a_hi, a_lo, w0_hi, w0_lo);
         // the row threads are done with the cand_proj tile: S takes layer-1 rows 0..127
-        load_pair(s_hi, s_lo, &map_w1_hi, &map_w1_lo, wrow0, smem_u32(&bar_w1));
+        load_pair(s_hi, s_lo, &mp.maps.w1_hi, &mp.maps.w1_lo, wrow0, smem_u32(&bar_w1));
         w1_issued = true;
       }
       mma_commit(smem_u32(&bar_fuse));
       // once the fuse MMAs have read W0, it takes layer-1 rows 128..255
       if (mbar_wait(smem_u32(&bar_fuse), 0, &s_abort, err)) {
-        load_pair(w0_hi, w0_lo, &map_w1_hi, &map_w1_lo, wrow0 + 128, smem_u32(&bar_w2));
+        load_pair(w0_hi, w0_lo, &mp.maps.w1_hi, &mp.maps.w1_lo, wrow0 + 128, smem_u32(&bar_w2));
         w2_issued = true;
       }
       if (w1_issued && mbar_wait(smem_u32(&bar_a2), 0, &s_abort, err) &&
@@ -411,7 +471,6 @@ k_cand_mlp_tc(const __grid_constant__ CUtensorMap map_fb_hi, const __grid_consta
     __syncwarp();
   } else {
     // -------------------------------------------------------------- row threads
-    pdl_wait();
     const int qd = warp & 3, q = warp >> 2;  // lane quadrant, column quarter
     const int r = qd * 32 + lane;           // tile row = tensor-memory lane
     const int m = m0 + r;
@@ -433,13 +492,17 @@ k_cand_mlp_tc(const __grid_constant__ CUtensorMap map_fb_hi, const __grid_consta
 
     // z = gamma * LN0(y + Gf[slot]) + beta  (every row thread takes part: the
     // LayerNorm holds row barriers)
-    const bool ok = rows_all(mbar_wait(smem_u32(&bar_fuse), 0, &s_abort, err) && !s_abort);
+    // Gf of this tile's slots comes from a slot block of the same launch:
+    // one thread waits for its tile's flag (acquire), the row barrier passes
+    // the ordering on to the others
+    const bool ok = rows_all(mbar_wait(smem_u32(&bar_fuse), 0, &s_abort, err) && !s_abort &&
+                             (tid != 0 || flag_wait(mp.gf_ready + gf_tile, &s_abort, err)));
     tc_fence_after();
     if (ok) {
       tmem_ld32(lane_base + q * kQ, x);
       if (live) {
         float g[kQ];
-        load32(g, Gf + (int64_t)(m / K) * kR + q * kQ);
+        load32_cg(g, mp.Gf + (int64_t)(m / K) * kR + q * kQ);
 #pragma unroll
         for (int k = 0; k < kQ; ++k) x[k] += g[k];
       } else {
@@ -448,8 +511,8 @@ k_cand_mlp_tc(const __grid_constant__ CUtensorMap map_fb_hi, const __grid_consta
       }
       ln0_part(x, eps, s_red[0], s_red[1], r, q);
       float ga[kQ], be[kQ];
-      load32(ga, gamma + q * kQ);
-      load32(be, beta + q * kQ);
+      load32(ga, mp.gamma + q * kQ);
+      load32(be, mp.beta + q * kQ);
 #pragma unroll
       for (int k = 0; k < kQ; ++k) x[k] = fmaf(ga[k], x[k], be[k]);
       store_split_part(smem + kOffA, smem + kOffA + kMat, r, q, x);
@@ -459,8 +522,8 @@ k_cand_mlp_tc(const __grid_constant__ CUtensorMap map_fb_hi, const __grid_consta
 
     // U (or V) = W1 z + w_l l: quarter q takes outputs [64 q, 64 q + 64),
     // staged as fp32 boxes 2q, 2q+1 (outputs 0..127 in S, 128..255 in A)
-    const float *wl = (half == 0 ? w_la : w_lb) + q * 64;
-    const float lv = live ? __ldg(topk_val + m) : 0.f;
+    const float *wl = (half == 0 ? mp.w_la : mp.w_lb) + q * 64;
+    const float lv = live ? __ldg(mp.topk_val + m) : 0.f;
     bool ok2 = mbar_wait(smem_u32(q < 2 ? &bar_uv0 : &bar_uv1), 0, &s_abort, err) && !s_abort;
     ok2 = __all_sync(DC_FULL_MASK, ok2);
     tc_fence_after();
@@ -481,7 +544,7 @@ k_cand_mlp_tc(const __grid_constant__ CUtensorMap map_fb_hi, const __grid_consta
     }
     fence_proxy_async();
     if (rows_all(ok2) && tid == 0) {
-      const CUtensorMap *map = half == 0 ? &map_u : &map_v;
+      const CUtensorMap *map = half == 0 ? &mp.cand.u : &mp.cand.v;
       for (int bx = 0; bx < 8; ++bx)
         tma_store_2d(map, sb + (bx < 4 ? kOffS + bx * kBox : kOffA + (bx - 4) * kBox), bx * 32, m0);
       bulk_commit();
@@ -506,33 +569,67 @@ k_cand_mlp_tc(const __grid_constant__ CUtensorMap map_fb_hi, const __grid_consta
   }
 }
 
-}  // namespace
-
-cudaError_t launch_slot_mlp_tc(const MlpMaps &maps, const SlotIoMaps &io, const MlpWeightsDev &w, int N, int B,
-                               float eps, int *err, cudaStream_t st, bool pdl) {
-  const int NB = N * B;
-  if (NB == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(k_slot_mlp_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kSlotSmemBytes);
-  if (e != cudaSuccess) return e;
-  dim3 grid(3, (NB + kRows - 1) / kRows);
-  e = launch_ex(k_slot_mlp_tc, grid, dim3(kThreads), kSlotSmemBytes, st, pdl, 0, maps.fg_hi, maps.fg_lo,
-                maps.w1s_hi, maps.w1s_lo, io.sp, io.gf, io.p, w.b1, eps, err);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+// ---------------------------------------------------------------- the launch
+// One launch runs both: blocks [0, slot_ctas) are the per-slot blocks
+// (chunk, slot tile), the rest the per-candidate blocks (half, candidate
+// tile).  The slot blocks come first so that they are dispatched first; the
+// grid must fit on the device at once (the candidate blocks wait for Gf).
+__global__ void __launch_bounds__(kThreads, 1)
+k_maps_tc(const __grid_constant__ MapsParams mp) {
+  pdl_trigger();
+  const int b = (int)blockIdx.x;
+  if (b < mp.slot_ctas)
+    slot_role(mp, b % 3, b / 3, mp.eps, mp.err);
+  else
+    cand_role(mp, (b - mp.slot_ctas) & 1, (b - mp.slot_ctas) >> 1, mp.K, mp.M, mp.eps, mp.err);
 }
 
-cudaError_t launch_cand_mlp_tc(const MlpMaps &maps, const CandIoMaps &io, const float *Gf,
-                               const float *topk_val, const MlpWeightsDev &w, int K, int M, float eps,
-                               int *err, cudaStream_t st) {
-  if (M == 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(k_cand_mlp_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kCandSmemBytes);
+}  // namespace
+
+cudaError_t launch_maps_tc(const MlpMaps &maps, const SlotIoMaps &slot, const CandIoMaps &cand, const float *Gf,
+                           unsigned *gf_ready, int rows_cap, const float *topk_val, const MlpWeightsDev &w,
+                           int N, int B, int K, float eps, int *err, cudaStream_t st) {
+  const int NB = N * B, M = NB * K;
+  if (NB == 0) return cudaSuccess;
+  MapsParams mp;
+  mp.maps = maps;
+  mp.slot = slot;
+  mp.cand = cand;
+  mp.Gf = const_cast<float *>(Gf);
+  mp.gf_ready = gf_ready;
+  mp.topk_val = topk_val;
+  mp.gamma = w.gamma;
+  mp.beta = w.beta;
+  mp.w_la = w.w_la;
+  mp.w_lb = w.w_lb;
+  mp.b1 = w.b1;
+  mp.rows_cap = rows_cap;
+  mp.slot_ctas = 3 * ((NB + kRows - 1) / kRows);
+  mp.K = K;
+  mp.M = M;
+  mp.eps = eps;
+  mp.err = err;
+  const int slot_ctas = mp.slot_ctas, cand_ctas = 2 * ((M + kRows - 1) / kRows);
+  cudaError_t e = cudaFuncSetAttribute(k_maps_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kMapsSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(2, (M + kRows - 1) / kRows);
-  e = launch_ex(k_cand_mlp_tc, grid, dim3(kThreads), kCandSmemBytes, st, true, 0, maps.fb_hi, maps.fb_lo,
-                maps.w1_hi, maps.w1_lo, io.cp, io.u, io.v, Gf, topk_val, w.gamma, w.beta, w.w_la, w.w_lb, K, M,
-                eps, err);
+  // The candidate blocks wait for the slot blocks, so one launch needs room
+  // for all of them at once; otherwise the slot blocks go first on their own
+  // and the candidate blocks find their flags already set.
+  int dev = 0, sms = 0, per_sm = 0;
+  e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_maps_tc, kThreads, kMapsSmemBytes);
+  if (e != cudaSuccess) return e;
+  if (slot_ctas + cand_ctas <= sms * per_sm) {
+    e = launch_ex(k_maps_tc, dim3(slot_ctas + cand_ctas), dim3(kThreads), kMapsSmemBytes, st, true, 0, mp);
+  } else {
+    e = launch_ex(k_maps_tc, dim3(slot_ctas), dim3(kThreads), kMapsSmemBytes, st, true, 0, mp);
+    if (e == cudaSuccess) {
+      mp.slot_ctas = 0;
+      e = launch_ex(k_maps_tc, dim3(cand_ctas), dim3(kThreads), kMapsSmemBytes, st, true, 0, mp);
+    }
+  }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

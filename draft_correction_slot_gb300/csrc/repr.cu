@@ -112,6 +112,8 @@ k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_trigger();
   pdl_wait();  // U, V (and this call's outputs) belong to the previous kernel until here
+  if (np == 0)  // the previous kernel's ready flags, for the next call
+    for (int i = tid; i < wk.nflags; i += 256) wk.flags[i] = 0u;
   const int64_t ca = ((int64_t)n * B + p) * K;      // first candidate of slot p
   const int64_t cb = ca + K;                         // first candidate of slot p+1
   const float *Pp = P + ((int64_t)n * B + p) * H;  // P is indexed by draft slot
