@@ -22,7 +22,6 @@ struct Workspace {
   float *vals = nullptr;
   float *slot_proj = nullptr;  // [N*B][3r]  (variant 1: [N*B][2r])
   float *cand_proj = nullptr;  // [N*B*K][r] (variant 1: [N*B*K][2r])
-  float *Gf = nullptr;         // [N*B][r]
   float *P = nullptr;          // [N*B][H] (rows of the last slot unused)
   float *U = nullptr;          // [N*B*K][H]  (variant 1: O [N*B*K][r])
   float *V = nullptr;          // [N*B*K][H]  (variant 1: I [N*B*K][r])
@@ -31,7 +30,6 @@ struct Workspace {
   float *margin = nullptr;     // [N*(B-1)]
   int *err = nullptr;          // device status word
   unsigned *req_count = nullptr;  // finished pairs per request (zero between calls)
-  unsigned *gf_ready = nullptr;   // per 128-slot tile: its Gf rows are written (zero between calls)
   // host staging (dcoco_correct_host)
   uint16_t *st_logits = nullptr;  // [N][slots][st_stride]
   int64_t st_stride = 0;
@@ -132,7 +130,6 @@ void carve_workspace(Carver &c, const dcoco_config &cfg, int B, int topk_segment
   ws.vals = c.take<float>(cands);
   ws.slot_proj = c.take<float>(rows * 3 * kR);
   ws.cand_proj = c.take<float>(cands * 2 * kR);
-  ws.Gf = c.take<float>(rows * kR);
   ws.P = c.take<float>(N * B * kH);
   ws.U = c.take<float>(cands * kH);
   ws.V = c.take<float>(cands * kH);
@@ -141,7 +138,6 @@ void carve_workspace(Carver &c, const dcoco_config &cfg, int B, int topk_segment
   ws.margin = c.take<float>(N * (B - 1));
   ws.err = c.take<int>(1);
   ws.req_count = c.take<unsigned>(N);
-  ws.gf_ready = c.take<unsigned>((rows + 127) / 128);
   if (cfg.host_staging) {
     ws.st_stride = ((int64_t)cfg.vocab + 7) & ~int64_t(7);
     ws.st_logits = c.take<uint16_t>(N * cfg.slots * (size_t)ws.st_stride);
@@ -249,13 +245,12 @@ int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs 
                                      &w->map_slot_lo, cfg.slots, B, d, V, h->splits, ws.err, st, true)));
   if (cfg.variant == 0) {
     // steps 2-3: per-slot / per-pair terms, z and the layer-1 partials U, V
-    DC_TRY(clk.done(dc::launch_maps_tc(w->mlp_maps, h->slot_io, h->cand_io, ws.Gf, ws.gf_ready,
-                                       cfg.max_batch * B, vals, w->mlp, N, B, K, cfg.ln_eps, ws.err, st)));
+    DC_TRY(clk.done(dc::launch_maps_tc(w->mlp_maps, h->slot_io, h->cand_io, ws.slot_proj, vals, w->mlp, N, B,
+                                       K, cfg.ln_eps, ws.err, st)));
     // steps 4-5: all (B-1) K^2 transition scores, then each request's walk
     // and verify in its last block
     const dc::WalkArgs wk{ids, in->target_tokens, out->tokens, choice,
-                          in->target_tokens ? out->accept_len : nullptr, margin, ws.req_count,
-                          ws.gf_ready, (rows + 127) / 128};
+                          in->target_tokens ? out->accept_len : nullptr, margin, ws.req_count, nullptr, 0};
     DC_TRY(clk.done(dc::launch_pair_score_walk(K, ws.U, ws.V, ws.P, vals, w->mlp.w2, w->mlp.b2, N, B,
                                                scores, wk, st)));
     return DCOCO_OK;
@@ -282,6 +277,7 @@ void pack_mlp(const dcoco_weight_ptrs &w, std::vector<float> &buf, size_t off[8]
   off[4] = take(H);      // b1
   off[5] = take(H);      // w2
   off[6] = take(1);      // b2
+  off[7] = take((size_t)r * r);  // W_fuse[:, r:], in the candidate maps' register order
   buf.assign(o, 0.f);
   for (int k = 0; k < r; ++k) {
     buf[off[0] + k] = w.ln_gamma[k];
@@ -294,6 +290,17 @@ void pack_mlp(const dcoco_weight_ptrs &w, std::vector<float> &buf, size_t off[8]
     buf[off[5] + j] = w.w2[j];
   }
   buf[off[6]] = w.b2[0];
+  // Thread `lane` of warp `wp` holds W_fuse[o][r + 32 g + e], o = 8 wp + lane / 4,
+  // g = lane % 4, e < 32, and loads it as 8 float4 steps; step i of the warp
+  // reads 512 contiguous bytes: element ((wp * 8 + i) * 32 + lane) * 4 + j
+  // is e = 4 i + j.
+  for (int wp = 0; wp < r / 8; ++wp)
+    for (int i = 0; i < 8; ++i)
+      for (int lane = 0; lane < 32; ++lane)
+        for (int j = 0; j < 4; ++j) {
+          const int o2 = 8 * wp + lane / 4, k = 32 * (lane % 4) + 4 * i + j;
+          buf[off[7] + ((size_t)(wp * 8 + i) * 32 + lane) * 4 + j] = w.w_fuse[(size_t)o2 * 2 * r + r + k];
+        }
 }
 
 }  // namespace
@@ -521,7 +528,7 @@ int dcoco_weights_create(dcoco_handle *h, const dcoco_weight_ptrs *wp, void *str
   if (cfg.variant == 0) {
     dc::MlpWeightsDev &m = w->mlp;
     m.gamma = dmlp + off[0]; m.beta = dmlp + off[1]; m.w_la = dmlp + off[2]; m.w_lb = dmlp + off[3];
-    m.b1 = dmlp + off[4]; m.w2 = dmlp + off[5]; m.b2 = dmlp + off[6];
+    m.b1 = dmlp + off[4]; m.w2 = dmlp + off[5]; m.b2 = dmlp + off[6]; m.w_fg = dmlp + off[7];
   }
   *out = w;
   return DCOCO_OK;

@@ -74,6 +74,7 @@ struct MlpWeightsDev {
   const float *b1;      // [H]
   const float *w2;      // [H]
   const float *b2;      // [1]
+  const float *w_fg;    // [r][r]  W_fuse[:, r:], in the candidate maps' register order
 };
 
 // Tensor-core forms of the per-slot and per-candidate steps.  The maps
@@ -83,32 +84,29 @@ struct MlpWeightsDev {
 struct MlpMaps {
   CUtensorMap fb_hi, fb_lo, w1_hi, w1_lo, fg_hi, fg_lo, w1s_hi, w1s_lo;
 };
-// The per-slot and per-candidate maps, in one launch.
-// Per draft slot: Gf = W_fuse[:, r:] LN0(W_ctx h) ([rows][r]); per draft slot
-// i (used for i < B-1): P_i = W1[:, :r] (W_pair[:, :d] h_i + W_pair[:, d:] h_{i+1})
-// + b1 ([rows][H]).  slot_proj is [N*B][3r] = (W_ctx h | W_pair[:, :d] h | W_pair[:, d:] h).
-// Per candidate: b = LN0(cand_proj), z = gamma*LN0(W_fuse[:, :r] b + Gf) + beta,
-// U = W1_a z + w_la l, V = W1_b z + w_lb l.  M = N * B * K candidates,
-// candidate m belongs to draft slot m / K.
+// The per-slot and per-candidate maps, in one launch (no block waits for
+// another).  Per draft slot i (used for i < B-1):
+// P_i = W1[:, :r] (W_pair[:, :d] h_i + W_pair[:, d:] h_{i+1}) + b1 ([rows][H]).
+// slot_proj is [N*B][3r] = (W_ctx h | W_pair[:, :d] h | W_pair[:, d:] h).
+// Per candidate: b = LN0(cand_proj), g = LN0(W_ctx h) of its slot,
+// z = gamma*LN0(W_fuse[:, :r] b + W_fuse[:, r:] g) + beta,
+// U = W1_a z + w_la l, V = W1_b z + w_lb l.  M = N * B * K candidates
+// (8 <= K, K divides 128), candidate m belongs to draft slot m / K.
 // Tiles move by TMA: `slot.sp` reads slot_proj, `slot.p` writes P, `cand.cp`
 // reads cand_proj ([rows][r]), `cand.u` / `cand.v` write U and V ([rows][H]);
 // all are fp32 maps with box 32 x 128 over at least the call's rows (rows of
 // the last tile past the call's count receive the outputs of stale or
-// all-zero input rows).  Gf ([rows_cap][r]) is written and read inside the
-// launch: its slot blocks set gf_ready[tile] (ceil(N*B / 128) entries, zero
-// before the launch) and the candidate blocks wait for it, so the grid
-// (3 blocks per 128 slots + 2 per 128 candidates) must fit on the device at
-// once; the next kernel in the stream zeroes the flags again.  The launch
-// may overlap the end of the previous kernel (programmatic serialization).
+// all-zero input rows).  The launch may overlap the end of the previous
+// kernel (programmatic serialization).
 struct SlotIoMaps {
   CUtensorMap sp, p;
 };
 struct CandIoMaps {
   CUtensorMap cp, u, v;
 };
-cudaError_t launch_maps_tc(const MlpMaps &maps, const SlotIoMaps &slot, const CandIoMaps &cand, const float *Gf,
-                           unsigned *gf_ready, int rows_cap, const float *topk_val, const MlpWeightsDev &w,
-                           int N, int B, int K, float eps, int *err, cudaStream_t st);
+cudaError_t launch_maps_tc(const MlpMaps &maps, const SlotIoMaps &slot, const CandIoMaps &cand,
+                           const float *slot_proj, const float *topk_val, const MlpWeightsDev &w, int N, int B,
+                           int K, float eps, int *err, cudaStream_t st);
 
 // Step 5 outputs and state for a launch that ends with the walk: per-request
 // arrays as in launch_walk_verify, and req_count (N entries, zero between

@@ -54,12 +54,12 @@ struct MapsParams {
   MlpMaps maps;
   SlotIoMaps slot;
   CandIoMaps cand;
-  float *Gf;             // [rows_cap][r]
-  unsigned *gf_ready;    // per slot tile: 1 once its Gf rows are written (zeroed by the next kernel)
+  const float *slot_proj;  // [N*B][3r]
+  const float *w_fg;       // W_fuse[:, r:], fp32 [r][r]
   const float *topk_val, *gamma, *beta, *w_la, *w_lb, *b1;
-  int rows_cap;          // rows of Gf
-  int slot_ctas;         // 3 per 128-slot tile
-  int K, M;              // candidates per slot, candidates in the call
+  int NB;                  // draft slots in the call
+  int slot_ctas;           // 2 per 128-slot tile (the two halves of P)
+  int K, M;                // candidates per slot, candidates in the call
   float eps;
   int *err;
 };
@@ -130,6 +130,21 @@ __device__ __forceinline__ float sum32(const float (&x)[kQ]) {
   return (a0 + a1) + (a2 + a3);
 }
 
+// Barrier over half of the row threads (group 0: warps 0-7, group 1: warps
+// 8-15), returning whether `v` holds in all of them.
+__device__ __forceinline__ bool half_rows_all(int grp, bool v) {
+  uint32_t out;
+  asm volatile(
+      "{\n.reg .pred p, q;\n"
+      "setp.ne.u32 q, %1, 0;\n"
+      "bar.red.and.pred p, %2, %3, q;\n"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(out)
+      : "r"((uint32_t)v), "r"(2 + grp), "n"(kRowThreads / 2)
+      : "memory");
+  return out != 0;
+}
+
 // Non-affine LayerNorm of a 128-wide row held as four 32-column quarters:
 // population variance, eps inside the square root.  Every row thread calls
 // it (it holds two row barriers); red0 / red1 are two distinct [4][kRows]
@@ -188,50 +203,16 @@ __device__ __forceinline__ void load_pair(uint32_t w_hi, uint32_t w_lo, const CU
   }
 }
 
-// Bounded spin on a ready flag written by another block of the same launch
-// (acquire at gpu scope).  false on timeout (kErrTimeout) or abort.
-__device__ __forceinline__ bool flag_wait(const unsigned *flag, volatile int *abort, int *err) {
-  const unsigned long long t0 = global_ns();
-  for (uint32_t it = 0;; ++it) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-    if (v != 0u) return true;
-    if ((it & 15u) == 15u) {
-      if (*abort) return false;
-      if (global_ns() - t0 > kWaitNs) {
-        *abort = 1;
-        atomicOr(err, ::dc::kErrTimeout);
-        return false;
-      }
-      __nanosleep(64);
-    }
-  }
-}
-__device__ __forceinline__ void st_release_gpu(unsigned *flag, unsigned v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(v) : "memory");
-}
-// load32 through L2 only: data written earlier in the same launch.
-__device__ __forceinline__ void load32_cg(float (&x)[kQ], const float *src) {
-  const float4 *s4 = reinterpret_cast<const float4 *>(src);
-#pragma unroll
-  for (int i = 0; i < kQ / 4; ++i) {
-    const float4 v = __ldcg(s4 + i);
-    x[4 * i] = v.x; x[4 * i + 1] = v.y; x[4 * i + 2] = v.z; x[4 * i + 3] = v.w;
-  }
-}
-
 // ---------------------------------------------------------------- per draft slot
-// One CTA per (128-slot tile, output chunk): chunk 0 writes Gf = W_fuse[:, r:] g
-// for every slot; chunks 1 and 2 write the two 128-wide halves of
-// P_i = W1[:, :r] s_i + b1, s_i = W_pair[:, :d] h_i + W_pair[:, d:] h_{i+1},
-// indexed by draft slot (rows of the last slot of a request are not used).
+// One CTA per (128-slot tile, output chunk): chunks 1 and 2 write the two
+// 128-wide halves of P_i = W1[:, :r] s_i + b1,
+// s_i = W_pair[:, :d] h_i + W_pair[:, d:] h_{i+1}, indexed by draft slot (rows
+// of the last slot of a request are not used).  (Chunk 0, Gf = W_fuse[:, r:] g,
+// is computed by the candidate blocks themselves.)
 // slot_proj rows are (W_ctx h | W_pair[:, :d] h | W_pair[:, d:] h).
 // The input tiles arrive by TMA (fp32 boxes of 128 rows x 32 columns,
 // 128-byte swizzled), so every row thread's 16-byte shared-memory access is
-// conflict-free and the global traffic is whole lines.  P leaves by TMA; Gf is
-// read by candidate blocks of the same launch, so it is written with ordinary
-// coalesced stores and published by a per-tile ready flag (release), which
-// the candidate blocks wait for (acquire).
+// conflict-free and the global traffic is whole lines; P leaves by TMA.
 // Shared memory: X (64 KB): the first input tile, then the A operand (hi, lo);
 // Y (64 KB): the second input tile (chunks 1, 2), then the output tile;
 // W (64 KB): the weight pair.
@@ -337,32 +318,12 @@ __device__ __forceinline__ void slot_role(const MapsParams &mp, int chunk, int t
         *reinterpret_cast<float4 *>(box_chunk(smem + kSlotOffY + q * kBox, r, c)) =
             make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
     }
-    if (chunk == 0) {
-      // Gf: whole 512-byte rows, 16 bytes per thread per step, then the flag
-      const bool all_ok = rows_all(ok);
-      if (all_ok) {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int e = tid + kRowThreads * j;  // 16-byte chunk of the 64 KB tile
-          const int row = e >> 5, c16 = e & 31;
-          if (m0 + row < mp.rows_cap) {
-            const float4 v4 = *reinterpret_cast<const float4 *>(
-                box_chunk(smem + kSlotOffY + (c16 >> 3) * kBox, row, c16 & 7));
-            __stcg(reinterpret_cast<float4 *>(mp.Gf + (int64_t)(m0 + row) * kR + c16 * 4), v4);
-          }
-        }
-      }
-      __threadfence();
-      rows_sync();
-      if (all_ok && tid == 0) st_release_gpu(mp.gf_ready + tile, 1u);
-    } else {
-      fence_proxy_async();
-      if (rows_all(ok) && tid == 0) {
-        for (int bx = 0; bx < 4; ++bx)
-          tma_store_2d(&mp.slot.p, sb + kSlotOffY + bx * kBox, (chunk - 1) * 128 + bx * 32, m0);
-        bulk_commit();
-        bulk_wait_all();
-      }
+    fence_proxy_async();
+    if (rows_all(ok) && tid == 0) {
+      for (int bx = 0; bx < 4; ++bx)
+        tma_store_2d(&mp.slot.p, sb + kSlotOffY + bx * kBox, (chunk - 1) * 128 + bx * 32, m0);
+      bulk_commit();
+      bulk_wait_all();
     }
   }
 
@@ -382,7 +343,11 @@ __device__ __forceinline__ void slot_role(const MapsParams &mp, int chunk, int t
 
 // ---------------------------------------------------------------- per candidate
 // One CTA per (128-candidate tile, half): half 0 writes U, half 1 writes V;
-// both recompute z (a 128x128 map, cheap).  Tensor memory: [0,128) the fuse
+// both recompute z (a 128x128 map, cheap) and the context term
+// Gf = W_fuse[:, r:] LN0(W_ctx h) of the tile's draft slots (128 / K of them):
+// fp32 dot products, each thread holding a 32-long slice of one W_fuse row
+// (loaded while the block waits for the previous kernel), partial sums met
+// by warp shuffles.  Tensor memory: [0,128) the fuse
 // product, [128,384) the 256 layer-1 outputs of this half.  Shared memory
 // (three 64 KB regions), by phase:
 //   A:  b (hi, lo), then z (hi, lo);                  then outputs 128..255
@@ -395,6 +360,9 @@ constexpr int kOffS = 4 * kMat;
 constexpr int kCandSmemBytes = 6 * kMat + 1024;
 constexpr int kMapsSmemBytes = kCandSmemBytes > kSlotSmemBytes ? kCandSmemBytes : kSlotSmemBytes;
 constexpr uint32_t kCandTmemCols = 512;
+constexpr int kMaxSlots = kRows / 8;  // draft slots in a candidate tile, K >= 8
+constexpr int kGSeg = 36;             // s_g row: four 32-float segments padded to 36 (bank spread)
+constexpr int kGLd = 4 * kGSeg;
 
 __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int tile, int K, int M, float eps,
                                           int *err) {
@@ -405,10 +373,13 @@ __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int ti
   __shared__ float s_red[2][4 * kRows];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
+  __shared__ float s_gam[kR], s_bet[kR], s_wl[kH];         // gamma, beta, this half's w_l
+  __shared__ __align__(16) float s_g[kMaxSlots][kGLd];     // LN0(W_ctx h) of the tile's slots
+  __shared__ __align__(16) float s_gf[kMaxSlots][kR];      // Gf of the tile's slots
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int m0 = tile * kRows;
-  const int gf_tile = (m0 / K) / kRows;  // the slot tile holding this tile's draft slots
+  const int slot0 = m0 / K, nslots = kRows / K;  // the tile's draft slots (K divides 128)
   const uint32_t sb = smem_u32(smem);
   const uint32_t a_hi = sb + kOffA, a_lo = sb + kOffA + kMat;
   const uint32_t w0_hi = sb + kOffW0, w0_lo = sb + kOffW0 + kMat;
@@ -476,9 +447,35 @@ __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int ti
     const int m = m0 + r;
     const bool live = m < M;
     const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16);
+    // Weights first (they do not depend on the previous kernel): gamma, beta
+    // and w_l to shared memory; this thread's slice of W_fuse[:, r:] (output
+    // go, inputs [32 gk, 32 gk + 32)) to registers.
+    if (tid < kR) {
+      s_gam[tid] = __ldg(mp.gamma + tid);
+      s_bet[tid] = __ldg(mp.beta + tid);
+    }
+    if (tid < kH) s_wl[tid] = __ldg((half == 0 ? mp.w_la : mp.w_lb) + tid);
+    const int gk = lane & 3, go = warp * 8 + (lane >> 2);
+    float wfg[32];
+    {
+      // packed so that each step of the warp reads 512 contiguous bytes
+      const float4 *src = reinterpret_cast<const float4 *>(mp.w_fg) + warp * 8 * 32 + lane;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 v = __ldg(src + i * 32);
+        wfg[4 * i] = v.x; wfg[4 * i + 1] = v.y; wfg[4 * i + 2] = v.z; wfg[4 * i + 3] = v.w;
+      }
+    }
     float x[kQ];
     // b = LN0(cand_proj row): quarter q is box q of the staged tile
     const bool ok0 = rows_all(mbar_wait(smem_u32(&bar_s), 0, &s_abort, err) && !s_abort);
+    // W_ctx h of the tile's slots (slot_proj, from the previous kernel: the
+    // tile's arrival orders it after the wait for that kernel); one warp per
+    // slot, four columns per lane, in flight during the LayerNorm of b
+    const int gs = slot0 + warp;
+    float4 gx = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (ok0 && warp < nslots && gs < mp.NB)
+      gx = __ldcg(reinterpret_cast<const float4 *>(mp.slot_proj + (int64_t)gs * 3 * kR) + lane);
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -490,31 +487,58 @@ __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int ti
     fence_proxy_async();
     mbar_arrive(smem_u32(&bar_a));
 
+    // g = LN0(W_ctx h) of each slot (warp-wide sums), then
+    // Gf[s][o] = sum_k W_fuse[o][r + k] g[s][k]: thread (go, gk) adds its
+    // 32-long slice for every slot, the four slices meet by shuffles.  This
+    // runs while the tensor cores compute the fuse product.
+    if (warp < nslots) {
+      const float mean = warp_sum((gx.x + gx.y) + (gx.z + gx.w)) * (1.0f / kR);
+      const float4 dv = make_float4(gx.x - mean, gx.y - mean, gx.z - mean, gx.w - mean);
+      const float var = warp_sum((dv.x * dv.x + dv.y * dv.y) + (dv.z * dv.z + dv.w * dv.w)) * (1.0f / kR);
+      const float inv = rsqrtf(var + eps);
+      const int k0 = lane * 4;
+      *reinterpret_cast<float4 *>(&s_g[warp][(k0 >> 5) * kGSeg + (k0 & 31)]) =
+          make_float4(dv.x * inv, dv.y * inv, dv.z * inv, dv.w * inv);
+    }
+    rows_sync();
+    for (int sl = 0; sl < nslots; ++sl) {
+      const float4 *gv = reinterpret_cast<const float4 *>(&s_g[sl][gk * kGSeg]);
+      float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 g4 = gv[i];
+        a0 = fmaf(wfg[4 * i], g4.x, a0);
+        a1 = fmaf(wfg[4 * i + 1], g4.y, a1);
+        a0 = fmaf(wfg[4 * i + 2], g4.z, a0);
+        a1 = fmaf(wfg[4 * i + 3], g4.w, a1);
+      }
+      float acc = a0 + a1;
+      acc += __shfl_xor_sync(DC_FULL_MASK, acc, 1);
+      acc += __shfl_xor_sync(DC_FULL_MASK, acc, 2);
+      if (gk == 0) s_gf[sl][go] = acc;
+    }
+
     // z = gamma * LN0(y + Gf[slot]) + beta  (every row thread takes part: the
     // LayerNorm holds row barriers)
-    // Gf of this tile's slots comes from a slot block of the same launch:
-    // one thread waits for its tile's flag (acquire), the row barrier passes
-    // the ordering on to the others
-    const bool ok = rows_all(mbar_wait(smem_u32(&bar_fuse), 0, &s_abort, err) && !s_abort &&
-                             (tid != 0 || flag_wait(mp.gf_ready + gf_tile, &s_abort, err)));
+    // (the row barrier also publishes s_gf)
+    const bool ok = rows_all(mbar_wait(smem_u32(&bar_fuse), 0, &s_abort, err) && !s_abort);
     tc_fence_after();
     if (ok) {
       tmem_ld32(lane_base + q * kQ, x);
       if (live) {
-        float g[kQ];
-        load32_cg(g, mp.Gf + (int64_t)(m / K) * kR + q * kQ);
+        const float4 *g4 = reinterpret_cast<const float4 *>(&s_gf[r / K][q * kQ]);
 #pragma unroll
-        for (int k = 0; k < kQ; ++k) x[k] += g[k];
+        for (int i = 0; i < kQ / 4; ++i) {
+          const float4 v = g4[i];
+          x[4 * i] += v.x; x[4 * i + 1] += v.y; x[4 * i + 2] += v.z; x[4 * i + 3] += v.w;
+        }
       } else {
 #pragma unroll
         for (int k = 0; k < kQ; ++k) x[k] = 0.f;
       }
       ln0_part(x, eps, s_red[0], s_red[1], r, q);
-      float ga[kQ], be[kQ];
-      load32(ga, mp.gamma + q * kQ);
-      load32(be, mp.beta + q * kQ);
 #pragma unroll
-      for (int k = 0; k < kQ; ++k) x[k] = fmaf(ga[k], x[k], be[k]);
+      for (int k = 0; k < kQ; ++k) x[k] = fmaf(s_gam[q * kQ + k], x[k], s_bet[q * kQ + k]);
       store_split_part(smem + kOffA, smem + kOffA + kMat, r, q, x);
     }
     fence_proxy_async();
@@ -522,7 +546,7 @@ __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int ti
 
     // U (or V) = W1 z + w_l l: quarter q takes outputs [64 q, 64 q + 64),
     // staged as fp32 boxes 2q, 2q+1 (outputs 0..127 in S, 128..255 in A)
-    const float *wl = (half == 0 ? mp.w_la : mp.w_lb) + q * 64;
+    const float *wl = s_wl + q * 64;
     const float lv = live ? __ldg(mp.topk_val + m) : 0.f;
     bool ok2 = mbar_wait(smem_u32(q < 2 ? &bar_uv0 : &bar_uv1), 0, &s_abort, err) && !s_abort;
     ok2 = __all_sync(DC_FULL_MASK, ok2);
@@ -530,9 +554,9 @@ __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int ti
     if (ok2) {
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
-        float v[kQ], wv[kQ];
+        float v[kQ];
         tmem_ld32(lane_base + 128 + q * 64 + h * kQ, v);
-        load32(wv, wl + h * kQ);
+        const float *wv = wl + h * kQ;
         const int bx = 2 * q + h;
         uint8_t *box = smem + (bx < 4 ? kOffS + bx * kBox : kOffA + (bx - 4) * kBox);
 #pragma unroll
@@ -542,13 +566,18 @@ __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int ti
                           fmaf(wv[4 * c + 2], lv, v[4 * c + 2]), fmaf(wv[4 * c + 3], lv, v[4 * c + 3]));
       }
     }
+    // Each output half leaves as soon as its quarters are staged: warps of
+    // quarters 0-1 (outputs 0..127, boxes 0-3) and of quarters 2-3 (outputs
+    // 128..255, boxes 4-7) meet at their own barrier and their first thread
+    // issues the group's four stores.
     fence_proxy_async();
-    if (rows_all(ok2) && tid == 0) {
+    const int grp = q >> 1;
+    if (half_rows_all(grp, ok2) && (tid & 255) == 0) {
       const CUtensorMap *map = half == 0 ? &mp.cand.u : &mp.cand.v;
-      for (int bx = 0; bx < 8; ++bx)
+      for (int bx = 4 * grp; bx < 4 * grp + 4; ++bx)
         tma_store_2d(map, sb + (bx < 4 ? kOffS + bx * kBox : kOffA + (bx - 4) * kBox), bx * 32, m0);
       bulk_commit();
-      bulk_wait_all();
+      bulk_wait_read();  // the block may leave once the tile is read; the writes land before the grid ends
     }
   }
 
@@ -571,65 +600,48 @@ __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int ti
 
 // ---------------------------------------------------------------- the launch
 // One launch runs both: blocks [0, slot_ctas) are the per-slot blocks
-// (chunk, slot tile), the rest the per-candidate blocks (half, candidate
-// tile).  The slot blocks come first so that they are dispatched first; the
-// grid must fit on the device at once (the candidate blocks wait for Gf).
+// (P half, slot tile), the rest the per-candidate blocks (half, candidate
+// tile).  No block waits for another.
 __global__ void __launch_bounds__(kThreads, 1)
 k_maps_tc(const __grid_constant__ MapsParams mp) {
   pdl_trigger();
   const int b = (int)blockIdx.x;
   if (b < mp.slot_ctas)
-    slot_role(mp, b % 3, b / 3, mp.eps, mp.err);
+    slot_role(mp, 1 + (b & 1), b >> 1, mp.eps, mp.err);
   else
     cand_role(mp, (b - mp.slot_ctas) & 1, (b - mp.slot_ctas) >> 1, mp.K, mp.M, mp.eps, mp.err);
 }
 
 }  // namespace
 
-cudaError_t launch_maps_tc(const MlpMaps &maps, const SlotIoMaps &slot, const CandIoMaps &cand, const float *Gf,
-                           unsigned *gf_ready, int rows_cap, const float *topk_val, const MlpWeightsDev &w,
-                           int N, int B, int K, float eps, int *err, cudaStream_t st) {
+cudaError_t launch_maps_tc(const MlpMaps &maps, const SlotIoMaps &slot, const CandIoMaps &cand,
+                           const float *slot_proj, const float *topk_val, const MlpWeightsDev &w, int N, int B,
+                           int K, float eps, int *err, cudaStream_t st) {
   const int NB = N * B, M = NB * K;
   if (NB == 0) return cudaSuccess;
+  if (K < 8 || kRows % K != 0) return cudaErrorInvalidValue;
   MapsParams mp;
   mp.maps = maps;
   mp.slot = slot;
   mp.cand = cand;
-  mp.Gf = const_cast<float *>(Gf);
-  mp.gf_ready = gf_ready;
+  mp.slot_proj = slot_proj;
+  mp.w_fg = w.w_fg;
   mp.topk_val = topk_val;
   mp.gamma = w.gamma;
   mp.beta = w.beta;
   mp.w_la = w.w_la;
   mp.w_lb = w.w_lb;
   mp.b1 = w.b1;
-  mp.rows_cap = rows_cap;
-  mp.slot_ctas = 3 * ((NB + kRows - 1) / kRows);
+  mp.NB = NB;
+  mp.slot_ctas = 2 * ((NB + kRows - 1) / kRows);
   mp.K = K;
   mp.M = M;
   mp.eps = eps;
   mp.err = err;
-  const int slot_ctas = mp.slot_ctas, cand_ctas = 2 * ((M + kRows - 1) / kRows);
+  const int blocks = mp.slot_ctas + 2 * ((M + kRows - 1) / kRows);
   cudaError_t e = cudaFuncSetAttribute(k_maps_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, kMapsSmemBytes);
   if (e != cudaSuccess) return e;
-  // The candidate blocks wait for the slot blocks, so one launch needs room
-  // for all of them at once; otherwise the slot blocks go first on their own
-  // and the candidate blocks find their flags already set.
-  int dev = 0, sms = 0, per_sm = 0;
-  e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess)
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_maps_tc, kThreads, kMapsSmemBytes);
-  if (e != cudaSuccess) return e;
-  if (slot_ctas + cand_ctas <= sms * per_sm) {
-    e = launch_ex(k_maps_tc, dim3(slot_ctas + cand_ctas), dim3(kThreads), kMapsSmemBytes, st, true, 0, mp);
-  } else {
-    e = launch_ex(k_maps_tc, dim3(slot_ctas), dim3(kThreads), kMapsSmemBytes, st, true, 0, mp);
-    if (e == cudaSuccess) {
-      mp.slot_ctas = 0;
-      e = launch_ex(k_maps_tc, dim3(cand_ctas), dim3(kThreads), kMapsSmemBytes, st, true, 0, mp);
-    }
-  }
+  e = launch_ex(k_maps_tc, dim3(blocks), dim3(kThreads), kMapsSmemBytes, st, true, 0, mp);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
