@@ -155,27 +155,6 @@ k_proj_tc(ProjJob job0, ProjJob job1, const __grid_constant__ CUtensorMap map0_h
     s_abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  // A gathered job's row ids come from the previous kernel; a draft-slot job
-  // reads only the call's inputs and writes a buffer no earlier kernel of the
-  // call touches, so it need not wait.
-  if (ids) pdl_wait();
-  if (tid < kTileM) {
-    const int m = m0 + tid;
-    int row = 0;  // rows past M load table row 0; their results are never stored
-    if (m < M) {
-      if (ids) {
-        row = ids[m];
-        if (row < 0 || row >= V) {
-          atomicOr(err, kErrBadCandidateId);
-          row = 0;
-        }
-      } else {
-        const int n = m / B, i = m - n * B;
-        row = n * slots + i + 1;
-      }
-    }
-    s_rows[tid] = row;
-  }
   if (warp == G::kWarpMma) tmem_alloc(smem_u32(&s_tmem), G::kTmemCols);
   tc_fence_before();
   __syncthreads();
@@ -185,6 +164,30 @@ k_proj_tc(ProjJob job0, ProjJob job1, const __grid_constant__ CUtensorMap map0_h
   int issued = 0;  // stages whose weight TMA this thread issued
   if (warp < 4 * MT) {
     // ------------------------------------------------------------ A gather (cp.async)
+    // The row table first.  A gathered job's row ids come from the previous
+    // kernel; a draft-slot job reads only the call's inputs and writes a
+    // buffer no earlier kernel of the call touches, so it need not wait.  (The
+    // weight stream below starts at once either way.)
+    static_assert(G::kGather == kTileM, "one gather thread per tile row");
+    if (ids) pdl_wait();
+    {
+      const int m = m0 + tid;
+      int row = 0;  // rows past M load table row 0; their results are never stored
+      if (m < M) {
+        if (ids) {
+          row = ids[m];
+          if (row < 0 || row >= V) {
+            atomicOr(err, kErrBadCandidateId);
+            row = 0;
+          }
+        } else {
+          const int n = m / B, i = m - n * B;
+          row = n * slots + i + 1;
+        }
+      }
+      s_rows[tid] = row;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(G::kGather) : "memory");  // the gather threads only
     // thread t: 16-byte chunk c of the 128-byte k-row, rows (t >> 3) + 16 j of
     // its 128-row sub-tile t >> 7
     const int t = tid & 127, sub = tid >> 7;
