@@ -75,6 +75,7 @@ def lib():
             L.orc_cosine_transition.argtypes = [C.c_int, C.c_double, _PD, _PD, C.c_double]
             L.orc_cosine_transition.restype = C.c_double
             L.orc_walk.argtypes = [_PD, C.c_int, C.c_int, _PI, _PD]
+            L.orc_viterbi.argtypes = [_PD, C.c_int, C.c_int, _PI, _PD]
             L.orc_verify.argtypes = [_PI, _PI, C.c_int]
             L.orc_verify.restype = C.c_int
             L.orc_expected_yield.argtypes = [_PD, C.c_int, _PD]
@@ -82,7 +83,7 @@ def lib():
             L.orc_param_count.argtypes = [C.c_int, C.c_int, C.c_int]
             L.orc_param_count.restype = C.c_longlong
             L.orc_correct_request.argtypes = [
-                C.POINTER(Dims), C.POINTER(Weights), C.c_int, C.c_double,
+                C.POINTER(Dims), C.POINTER(Weights), C.c_int, C.c_double, C.c_int,
                 _PU, C.c_int64, _PU, _PU, _PI,
                 _PI, _PF, _PD, _PI, _PI, _PD, _PI, C.POINTER(Inter)]
             L.orc_correct_request.restype = C.c_int
@@ -191,6 +192,21 @@ def walk(scores: np.ndarray):
     return choice, margin
 
 
+def viterbi(scores: np.ndarray):
+    """scores [B-1, K, K] -> (choice [B], margin [B-1]) of the highest-scoring path."""
+    s = np.ascontiguousarray(scores, dtype=np.float64)
+    P, K, _ = s.shape
+    choice = np.empty(P + 1, np.int32)
+    margin = np.empty(P, np.float64)
+    lib().orc_viterbi(_p(s, C.c_double), P + 1, K, _p(choice, C.c_int32), _p(margin, C.c_double))
+    return choice, margin
+
+
+def select_path(scores: np.ndarray, path_rule: int = 0):
+    """path_rule 0: greedy walk, 1: highest-scoring path."""
+    return viterbi(scores) if path_rule == 1 else walk(scores)
+
+
 def verify(tokens, target) -> int:
     t = np.ascontiguousarray(tokens, dtype=np.int32)
     g = np.ascontiguousarray(target, dtype=np.int32)
@@ -210,7 +226,7 @@ def param_count(d: int, r: int = 128, H: int = 256) -> int:
 
 # ------------------------------------------------------------------ whole path
 def correct_request(m: Model, logits_req, hidden_req, E, target=None, variant: int = 0,
-                    sigma: float = 1.0, intermediates: bool = False):
+                    sigma: float = 1.0, intermediates: bool = False, path_rule: int = 0):
     """One request.  logits_req [slots, stride] u16, hidden_req [slots, d] u16, E [V, d] u16."""
     dm = m.dims
     B, K, r = dm.slots - 1, dm.K, dm.r
@@ -238,7 +254,7 @@ def correct_request(m: Model, logits_req, hidden_req, E, target=None, variant: i
             out["o"] = np.empty((B, K, r)); out["in"] = np.empty((B, K, r))
             inter = Inter(None, None, None, None, _p(out["o"], C.c_double), _p(out["in"], C.c_double))
     rc = lib().orc_correct_request(
-        C.byref(dm), C.byref(m.cw), variant, sigma, _p(lg, C.c_uint16), lg.shape[-1],
+        C.byref(dm), C.byref(m.cw), variant, sigma, path_rule, _p(lg, C.c_uint16), lg.shape[-1],
         _p(hd, C.c_uint16), _p(E, C.c_uint16), _p(tg, C.c_int32),
         _p(out["topk_ids"], C.c_int32), _p(out["topk_val"], C.c_float), _p(out["scores"], C.c_double),
         _p(out["choice"], C.c_int32), _p(out["tokens"], C.c_int32), _p(out["margin"], C.c_double),
@@ -251,7 +267,7 @@ def correct_request(m: Model, logits_req, hidden_req, E, target=None, variant: i
 
 
 def correct_batch(m: Model, logits, hidden, E, targets=None, variant: int = 0, sigma: float = 1.0,
-                  requests=None, threads: int | None = None):
+                  requests=None, threads: int | None = None, path_rule: int = 0):
     """Run `correct_request` over requests (all, or the listed indices) on a thread pool."""
     N = logits.shape[0]
     req = list(range(N)) if requests is None else list(requests)
@@ -260,7 +276,7 @@ def correct_batch(m: Model, logits, hidden, E, targets=None, variant: int = 0, s
 
     def one(n):
         return correct_request(m, logits[n], hidden[n], E, None if targets is None else targets[n],
-                               variant, sigma)
+                               variant, sigma, path_rule=path_rule)
 
     if threads <= 1:
         res = [one(n) for n in req]

@@ -216,6 +216,66 @@ void orc_walk(const double *scores, int B, int K, int32_t *choice, double *margi
 }
 
 /* ---------------------------------------------------------------------------
+ * Highest-scoring path (the Viterbi rule).  [LiLiCorr] App. E, "Path
+ * selection", Eq. (12): a path scores as the sum of its adjacent-pair terms,
+ * g(c) = sum_p S_p(c_p, c_{p+1}), and its maximizer comes from a left-to-right
+ * dynamic program that keeps, for every candidate, the best score of a path
+ * ending there and that path's predecessor, then traces the predecessors back
+ * from the best final candidate.  Here the first draft slot keeps the draft
+ * argmax (candidate 0), as in the greedy walk, and ties go to the lowest
+ * candidate index (predecessor and final candidate alike).
+ * margin[p] = best minus second best, over predecessors a, of
+ * best_p(a) + S_p(a, c_{p+1}) for the chosen c_{p+1} (+inf when K == 1).
+ * ------------------------------------------------------------------------- */
+void orc_viterbi(const double *scores, int B, int K, int32_t *choice, double *margin) {
+  double *best = (double *)malloc((size_t)B * K * sizeof(double));
+  int32_t *pred = (int32_t *)malloc((size_t)B * K * sizeof(int32_t));
+  if (!best || !pred) {
+    free(best);
+    free(pred);
+    orc_walk(scores, B, K, choice, margin); /* unreachable in practice */
+    return;
+  }
+  for (int a = 0; a < K; ++a) best[a] = a == 0 ? 0.0 : -INFINITY;
+  for (int p = 0; p < B - 1; ++p) {
+    const double *S = scores + (size_t)p * K * K;
+    for (int b = 0; b < K; ++b) {
+      int arg = 0;
+      double v = best[(size_t)p * K] + S[b];
+      for (int a = 1; a < K; ++a) {
+        const double t = best[(size_t)p * K + a] + S[(size_t)a * K + b];
+        if (t > v) {
+          v = t;
+          arg = a;
+        }
+      }
+      best[(size_t)(p + 1) * K + b] = v;
+      pred[(size_t)(p + 1) * K + b] = arg;
+    }
+  }
+  int last = 0;
+  for (int b = 1; b < K; ++b)
+    if (best[(size_t)(B - 1) * K + b] > best[(size_t)(B - 1) * K + last]) last = b;
+  choice[B - 1] = last;
+  for (int p = B - 1; p > 0; --p) choice[p - 1] = pred[(size_t)p * K + choice[p]];
+  if (margin)
+    for (int p = 0; p < B - 1; ++p) {
+      const double *S = scores + (size_t)p * K * K;
+      const int b = choice[p + 1], a0 = choice[p];
+      const double top = best[(size_t)p * K + a0] + S[(size_t)a0 * K + b];
+      double second = -INFINITY;
+      for (int a = 0; a < K; ++a)
+        if (a != a0) {
+          const double t = best[(size_t)p * K + a] + S[(size_t)a * K + b];
+          if (t > second) second = t;
+        }
+      margin[p] = top - second;
+    }
+  free(best);
+  free(pred);
+}
+
+/* ---------------------------------------------------------------------------
  * Greedy verification.  [FD] "Modified rejection sampling ..." section, the
  * greedy-verification contract: accept the longest run that matches the
  * target's greedy tokens.  The accepted length counts draft slots only.
@@ -257,14 +317,16 @@ long long orc_param_count(int d, int r, int H) {
 /* ---------------------------------------------------------------------------
  * The whole path for one request, steps in the pages' order.
  * ------------------------------------------------------------------------- */
-int orc_correct_request(const orc_dims *dm, const orc_weights *w, int variant, double sigma,
+int orc_correct_request(const orc_dims *dm, const orc_weights *w, int variant, double sigma, int path_rule,
                         const uint16_t *logits, int64_t stride, const uint16_t *hidden,
                         const uint16_t *E, const int32_t *target,
                         int32_t *topk_ids, float *topk_val, double *scores,
                         int32_t *choice, int32_t *tokens, double *margin, int32_t *accept_len,
                         orc_intermediates *inter) {
   const int B = dm->slots - 1, K = dm->K, r = dm->r, d = dm->d;
-  if (B < 2 || K < 2 || K > dm->V || r < 1 || (variant != 0 && variant != 1)) return -1;
+  if (B < 2 || K < 2 || K > dm->V || r < 1 || (variant != 0 && variant != 1) ||
+      (path_rule != 0 && path_rule != 1))
+    return -1;
 
   /* (1) top-K per draft slot; slot 0 (the anchor) is not read. */
   for (int i = 0; i < B; ++i)
@@ -318,7 +380,10 @@ int orc_correct_request(const orc_dims *dm, const orc_weights *w, int variant, d
   }
 
   /* (5) walk, then the chosen tokens */
-  orc_walk(scores, B, K, choice, margin);
+  if (path_rule == 1)
+    orc_viterbi(scores, B, K, choice, margin);
+  else
+    orc_walk(scores, B, K, choice, margin);
   for (int i = 0; i < B; ++i) tokens[i] = topk_ids[(size_t)i * K + choice[i]];
   if (target && accept_len) accept_len[0] = orc_verify(tokens, target, B);
 

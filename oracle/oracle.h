@@ -11,7 +11,8 @@
  *              "Method step details" items (1)-(5).
  *   [LiLiCorr] "LiLiCorr: Lightweight Likelihood Correlation of Parallel
  *              Drafts for Speculative Decoding": Sec. 3.2 Eq. (1) (cosine
- *              matching), Sec. 3.5 Eq. (8) (greedy walk).
+ *              matching), Sec. 3.5 Eq. (8) (greedy walk), App. E Eq. (12)
+ *              (highest-scoring path, Viterbi).
  *   [FD]       "Faster Decoding" (textbook chapter): the expected-yield
  *              identity E[Y] = 1 + sum_k s_k and the greedy-verification
  *              contract.
@@ -105,6 +106,11 @@ double orc_cosine_transition(int r, double sigma, const double *o_a, const doubl
 /* Step 5: prefix-first greedy walk over scores [B-1][K][K]. choice[0] = 0. */
 void orc_walk(const double *scores, int B, int K, int32_t *choice, double *margin);
 
+/* Highest-scoring path over scores [B-1][K][K] by dynamic programming
+ * (Viterbi), choice[0] = 0, ties to the lowest index; margin[p] = gap between
+ * the best and second-best predecessor of the chosen candidate at p+1. */
+void orc_viterbi(const double *scores, int B, int K, int32_t *choice, double *margin);
+
 /* Greedy verify: number of leading slots whose token equals the target. */
 int orc_verify(const int32_t *tokens, const int32_t *target, int B);
 
@@ -115,12 +121,13 @@ double orc_expected_yield(const double *cond, int n, double *survival);
 long long orc_param_count(int d, int r, int H);
 
 /* Whole path for one request.
- * variant 0 = MLP transition (DCOCO), 1 = cosine matching (LiLiCorr-style).
+ * variant 0 = MLP transition (DCOCO), 1 = cosine matching (LiLiCorr-style);
+ * path_rule 0 = prefix-first greedy walk, 1 = highest-scoring path (Viterbi).
  * logits [slots][stride] bf16, hidden [slots][d] bf16, E [V][d] bf16,
  * target [B] or NULL.  Outputs: topk_ids/topk_val [B][K], scores [B-1][K][K],
  * choice/tokens [B], margin [B-1], accept_len [1] (when target != NULL).
  * Returns 0, or -1 on bad arguments / allocation failure. */
-int orc_correct_request(const orc_dims *dm, const orc_weights *w, int variant, double sigma,
+int orc_correct_request(const orc_dims *dm, const orc_weights *w, int variant, double sigma, int path_rule,
                         const uint16_t *logits, int64_t stride, const uint16_t *hidden,
                         const uint16_t *E, const int32_t *target,
                         int32_t *topk_ids, float *topk_val, double *scores,

@@ -2,8 +2,8 @@
 
 Sources (pages, by title): the DCOCO page "Contextual Correction of Parallel
 Drafts for Speculative Decoding" (Core method; Method step details (1)-(5));
-"LiLiCorr" (Sec. 3.2 Eq. (1), Sec. 3.5 Eq. (8)); "Faster Decoding" (expected
-yield, greedy verification).
+"LiLiCorr" (Sec. 3.2 Eq. (1), Sec. 3.5 Eq. (8), App. E Eq. (12)); "Faster
+Decoding" (expected yield, greedy verification).
 """
 import itertools
 import json
@@ -315,6 +315,86 @@ def test_walk_brute_force_random():
             assert choice[p + 1] == best
             assert margin[p] == row[best] - second
             k = best
+
+
+# --------------------------------------------------------------- highest-scoring path
+def path_total(sc, path):
+    return sum(sc[p, path[p], path[p + 1]] for p in range(sc.shape[0]))
+
+
+@pytest.mark.parametrize("P,K", [(1, 5), (3, 4), (5, 3), (6, 4), (4, 6)])
+def test_viterbi_brute_force(P, K):
+    """LiLiCorr App. E Eq. (12): the exact maximizer of the summed pair terms,
+    found here by enumerating all K^P paths (first slot fixed to the draft
+    argmax); continuous random scores, so the maximizer is unique."""
+    rng = np.random.default_rng(100 + 7 * P + K)
+    for _ in range(5):
+        sc = rng.standard_normal((P, K, K))
+        choice, margin = oracle.viterbi(sc)
+        best_path, best_val = None, -np.inf
+        for tail in itertools.product(range(K), repeat=P):
+            path = (0,) + tail
+            v = path_total(sc, path)
+            if v > best_val:
+                best_path, best_val = path, v
+        assert tuple(choice) == best_path
+        assert abs(path_total(sc, choice) - best_val) < 1e-12
+        # margin: best minus second best predecessor of each chosen candidate,
+        # each predecessor carrying its best prefix (again by enumeration)
+        for p in range(P):
+            b = choice[p + 1]
+            ends = []
+            for a in range(K):
+                if p == 0:
+                    pref = 0.0 if a == 0 else -np.inf
+                else:
+                    pref = max(path_total(sc[:p], (0,) + head + (a,))
+                               for head in itertools.product(range(K), repeat=p - 1))
+                ends.append(pref + sc[p, a, b])
+            top = ends[choice[p]]
+            second = max(e for a, e in enumerate(ends) if a != choice[p])
+            assert top == max(ends)
+            np.testing.assert_allclose(margin[p], top - second, rtol=0, atol=1e-12)
+
+
+def test_viterbi_ties_go_to_lowest_index():
+    sc = np.zeros((4, 5, 5))
+    choice, margin = oracle.viterbi(sc)
+    assert list(choice) == [0] * 5
+    # only one finite predecessor at p = 0 (the first slot is fixed)
+    assert margin[0] == np.inf and np.all(margin[1:] == 0.0)
+
+
+def test_viterbi_never_below_greedy_and_can_differ():
+    """The exact optimizer scores at least the greedy walk's path; a lattice
+    whose best first step leads nowhere separates them."""
+    rng = np.random.default_rng(12)
+    for _ in range(50):
+        P, K = int(rng.integers(1, 8)), int(rng.integers(2, 9))
+        sc = rng.standard_normal((P, K, K))
+        cv, _ = oracle.viterbi(sc)
+        cg, _ = oracle.walk(sc)
+        assert path_total(sc, cv) >= path_total(sc, cg) - 1e-12
+    sc = np.zeros((2, 2, 2))
+    sc[0, 0] = [1.0, 0.0]          # greedy takes candidate 0 at slot 2 ...
+    sc[1, 0] = [-5.0, -5.0]        # ... which has no good successor
+    sc[1, 1] = [3.0, 0.0]
+    assert list(oracle.walk(sc)[0]) == [0, 0, 0]
+    assert list(oracle.viterbi(sc)[0]) == [0, 1, 0]
+
+
+def test_zero_output_layer_viterbi_reproduces_draft_argmax():
+    """With Delta = 0 every pair term is the successor's draft logit, so the
+    highest-scoring path is the per-slot draft argmax as well."""
+    rng = np.random.default_rng(13)
+    V, d, slots, K = 600, 64, 12, 8
+    m, _ = tiny_model(rng, V=V, d=d, K=K, slots=slots, zero_out=True)
+    logits = synth.make_logits(rng, 1, slots, V, 16, (4, 12))
+    hidden = synth.make_hidden(rng, 1, slots, d)
+    E = synth.make_embedding(rng, V, d)
+    out = oracle.correct_request(m, logits[0], hidden[0], E, path_rule=1)
+    np.testing.assert_array_equal(out["choice"], 0)
+    np.testing.assert_array_equal(out["tokens"], out["topk_ids"][:, 0])
 
 
 # --------------------------------------------------------------- cosine variant
