@@ -153,6 +153,7 @@ int validate_config(const dcoco_config *cfg) {
   if (cfg->rank != kR || cfg->mlp_hidden != kH) return DCOCO_EUNSUPPORTED;
   if (cfg->topk != 8 && cfg->topk != 16 && cfg->topk != 32) return DCOCO_EUNSUPPORTED;
   if (cfg->variant != 0 && cfg->variant != 1) return DCOCO_EUNSUPPORTED;
+  if (cfg->path_rule != 0 && cfg->path_rule != 1) return DCOCO_EUNSUPPORTED;
   if (cfg->slots < 3 || cfg->slots > 32) return DCOCO_EUNSUPPORTED;
   if (cfg->vocab < cfg->topk || cfg->vocab > (1 << 20)) return DCOCO_EINVAL;
   if (cfg->hidden <= 0 || cfg->hidden % 64 != 0) return DCOCO_EINVAL;
@@ -250,7 +251,8 @@ int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs 
     // steps 4-5: all (B-1) K^2 transition scores, then each request's walk
     // and verify in its last block
     const dc::WalkArgs wk{ids, in->target_tokens, out->tokens, choice,
-                          in->target_tokens ? out->accept_len : nullptr, margin, ws.req_count, nullptr, 0};
+                          in->target_tokens ? out->accept_len : nullptr, margin, ws.req_count,
+                          cfg.path_rule};
     DC_TRY(clk.done(dc::launch_pair_score_walk(K, ws.U, ws.V, ws.P, vals, w->mlp.w2, w->mlp.b2, N, B,
                                                scores, wk, st)));
     return DCOCO_OK;
@@ -260,7 +262,7 @@ int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs 
   // step 5: walk + verify
   DC_TRY(clk.done(dc::launch_walk_verify(K, scores, ids, in->target_tokens, N, B, out->tokens,
                                          choice, margin,
-                                         in->target_tokens ? out->accept_len : nullptr, st)));
+                                         in->target_tokens ? out->accept_len : nullptr, cfg.path_rule, st)));
   return DCOCO_OK;
 }
 

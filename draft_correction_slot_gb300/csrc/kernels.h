@@ -117,8 +117,7 @@ struct WalkArgs {
   int32_t *tokens, *choice, *accept_len;
   float *margin;
   unsigned *req_count;
-  unsigned *flags;  // zeroed once the launch may start (the previous kernel is done), or null
-  int nflags;
+  int path_rule;    // 0: prefix-first greedy walk, 1: highest-scoring path
 };
 
 // S[n,p,a,b] = l_{p+1}(b) + b2 + sum_j w2_j GELU(P_pj + U_{p,a,j} + V_{p+1,b,j}),
@@ -137,9 +136,10 @@ cudaError_t launch_cos_score(int K, const float *O, const float *I, const float 
                              float sigma, int N, int B, float *scores, cudaStream_t st);
 
 // ---------------------------------------------------------------- walk + verify
+// path_rule 0: prefix-first greedy walk; 1: highest-scoring path (Viterbi).
 cudaError_t launch_walk_verify(int K, const float *scores, const int32_t *topk_ids,
                                const int32_t *target, int N, int B, int32_t *tokens,
                                int32_t *choice, float *margin, int32_t *accept_len,
-                               cudaStream_t st);
+                               int path_rule, cudaStream_t st);
 
 }  // namespace dc

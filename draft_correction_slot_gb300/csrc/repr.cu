@@ -112,8 +112,6 @@ k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_trigger();
   pdl_wait();  // U, V (and this call's outputs) belong to the previous kernel until here
-  if (np == 0)  // the previous kernel's ready flags, for the next call
-    for (int i = tid; i < wk.nflags; i += 256) wk.flags[i] = 0u;
   const int64_t ca = ((int64_t)n * B + p) * K;      // first candidate of slot p
   const int64_t cb = ca + K;                         // first candidate of slot p+1
   const float *Pp = P + ((int64_t)n * B + p) * H;  // P is indexed by draft slot
@@ -209,7 +207,8 @@ k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
 
   // ---------------------------------------------------------------- step 5
   // The last block of request n to finish its pair (counted in req_count,
-  // zero between calls) walks the request's scores.
+  // zero between calls) selects the request's path (greedy walk or highest-
+  // scoring path) and verifies it.
   __shared__ int s_last;
   __shared__ int s_choice[32];
   __threadfence();
@@ -221,11 +220,16 @@ k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
   int *s_best = reinterpret_cast<int *>(sm);
   float *s_gap = sm + kWalkMaxRows;
   const int64_t slot0 = (int64_t)n * B;
-  walk_verify_request<K>(scores + (int64_t)n * (B - 1) * K * K, wk.topk_ids + slot0 * K,
-                         wk.target ? wk.target + slot0 : nullptr, B, wk.tokens + slot0,
-                         wk.choice ? wk.choice + slot0 : nullptr,
-                         wk.margin ? wk.margin + (int64_t)n * (B - 1) : nullptr,
-                         wk.accept_len ? wk.accept_len + n : nullptr, s_best, s_gap, s_choice);
+  const float *sc = scores + (int64_t)n * (B - 1) * K * K;
+  const int32_t *tg = wk.target ? wk.target + slot0 : nullptr;
+  int32_t *ch = wk.choice ? wk.choice + slot0 : nullptr, *al = wk.accept_len ? wk.accept_len + n : nullptr;
+  float *mg = wk.margin ? wk.margin + (int64_t)n * (B - 1) : nullptr;
+  if (wk.path_rule == 1)
+    viterbi_verify_request<K>(sc, wk.topk_ids + slot0 * K, tg, B, wk.tokens + slot0, ch, mg, al, s_best, s_gap,
+                              s_choice);
+  else
+    walk_verify_request<K>(sc, wk.topk_ids + slot0 * K, tg, B, wk.tokens + slot0, ch, mg, al, s_best, s_gap,
+                           s_choice);
   if (tid == 0) wk.req_count[n] = 0u;  // ready for the next call
 }
 

@@ -1,6 +1,6 @@
 // walk.cu -- step 5 as its own launch (the cosine variant; the MLP variant
 // runs it in the last block of each request's pair scores): one block per
-// request, see walk.cuh.
+// request, see walk.cuh.  path_rule 0: greedy walk, 1: highest-scoring path.
 #include <algorithm>
 
 #include "common.cuh"
@@ -15,16 +15,20 @@ __global__ void __launch_bounds__(256)
 k_walk_verify(const float *__restrict__ scores, const int32_t *__restrict__ topk_ids,
               const int32_t *__restrict__ target, int N, int B, int32_t *__restrict__ tokens,
               int32_t *__restrict__ choice, float *__restrict__ margin,
-              int32_t *__restrict__ accept_len) {
+              int32_t *__restrict__ accept_len, int path_rule) {
   __shared__ int s_best[kWalkMaxRows];
   __shared__ float s_gap[kWalkMaxRows];
   __shared__ int s_choice[32];
   const int n = blockIdx.x, P = B - 1;
   const int64_t slot0 = (int64_t)n * B;
-  walk_verify_request<K>(scores + (int64_t)n * P * K * K, topk_ids + slot0 * K, target ? target + slot0 : nullptr,
-                         B, tokens + slot0, choice ? choice + slot0 : nullptr,
-                         margin ? margin + (int64_t)n * P : nullptr, accept_len ? accept_len + n : nullptr,
-                         s_best, s_gap, s_choice);
+  const float *sc = scores + (int64_t)n * P * K * K;
+  const int32_t *tg = target ? target + slot0 : nullptr;
+  int32_t *ch = choice ? choice + slot0 : nullptr, *al = accept_len ? accept_len + n : nullptr;
+  float *mg = margin ? margin + (int64_t)n * P : nullptr;
+  if (path_rule == 1)
+    viterbi_verify_request<K>(sc, topk_ids + slot0 * K, tg, B, tokens + slot0, ch, mg, al, s_best, s_gap, s_choice);
+  else
+    walk_verify_request<K>(sc, topk_ids + slot0 * K, tg, B, tokens + slot0, ch, mg, al, s_best, s_gap, s_choice);
 }
 
 }  // namespace
@@ -32,21 +36,21 @@ k_walk_verify(const float *__restrict__ scores, const int32_t *__restrict__ topk
 template <int K>
 static cudaError_t walk_k(const float *scores, const int32_t *topk_ids, const int32_t *target, int N,
                           int B, int32_t *tokens, int32_t *choice, float *margin, int32_t *accept_len,
-                          cudaStream_t st) {
+                          int path_rule, cudaStream_t st) {
   k_walk_verify<K><<<N, 256, 0, st>>>(scores, topk_ids, target, N, B, tokens, choice, margin,
-                                         accept_len);
+                                         accept_len, path_rule);
   return cudaGetLastError();
 }
 
 cudaError_t launch_walk_verify(int K, const float *scores, const int32_t *topk_ids,
                                const int32_t *target, int N, int B, int32_t *tokens,
                                int32_t *choice, float *margin, int32_t *accept_len,
-                               cudaStream_t st) {
+                               int path_rule, cudaStream_t st) {
   if (N == 0) return cudaSuccess;
   switch (K) {
-    case 8: return walk_k<8>(scores, topk_ids, target, N, B, tokens, choice, margin, accept_len, st);
-    case 16: return walk_k<16>(scores, topk_ids, target, N, B, tokens, choice, margin, accept_len, st);
-    case 32: return walk_k<32>(scores, topk_ids, target, N, B, tokens, choice, margin, accept_len, st);
+    case 8: return walk_k<8>(scores, topk_ids, target, N, B, tokens, choice, margin, accept_len, path_rule, st);
+    case 16: return walk_k<16>(scores, topk_ids, target, N, B, tokens, choice, margin, accept_len, path_rule, st);
+    case 32: return walk_k<32>(scores, topk_ids, target, N, B, tokens, choice, margin, accept_len, path_rule, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -1,5 +1,6 @@
-// walk.cuh -- step 5 for one request: prefix-first greedy walk and greedy
-// verify, as a block-wide device function (256 threads).
+// walk.cuh -- step 5 for one request: path selection (the prefix-first
+// greedy walk, or the highest-scoring path) and greedy verify, as block-wide
+// device functions (256 threads).
 //
 // DCOCO page, Method step details (5) and Core method; LiLiCorr Sec. 3.5
 // Eq. (8): the first draft slot takes the draft argmax (candidate 0 of its
@@ -80,6 +81,95 @@ __device__ __forceinline__ void walk_verify_request(const float *scores, const i
       if (tid == 0) *accept_len = mm ? (__ffs(mm) - 1) : B;
     }
   }
+}
+
+// Chosen tokens, choices, margins (the path's margin at pair p is s_gap[p K +
+// choice[p+1]]) and the verify of one request, from s_choice.
+template <int K>
+__device__ __forceinline__ void emit_request(const int32_t *ids, const int32_t *target, int B, int32_t *tokens,
+                                             int32_t *choice, float *margin, int32_t *accept_len,
+                                             const float *s_gap, const int *s_choice) {
+  const int tid = threadIdx.x, P = B - 1;
+  if (tid < 32) {
+    int tok = 0;
+    if (tid < B) {
+      const int k = s_choice[tid];
+      tok = ids[tid * K + k];
+      tokens[tid] = tok;
+      if (choice) choice[tid] = k;
+      if (margin && tid < P) margin[tid] = s_gap[tid * K + s_choice[tid + 1]];
+    }
+    if (target) {
+      const bool mismatch = tid < B && tok != target[tid];
+      const unsigned mm = __ballot_sync(DC_FULL_MASK, mismatch);
+      if (tid == 0) *accept_len = mm ? (__ffs(mm) - 1) : B;
+    }
+  }
+}
+
+// Highest-scoring path for one request.  LiLiCorr page, App. E "Path
+// selection", Eq. (12): the path total is the sum of its adjacent-pair
+// terms, g(c) = sum_p S_p(c_p, c_{p+1}); a left-to-right dynamic program keeps,
+// for every candidate, the best total of a path ending there and that path's
+// predecessor, and the path is traced back from the best final candidate.
+// The first draft slot keeps candidate 0 (the draft argmax, as in the greedy
+// walk); ties go to the lowest index.  Totals are fp64 sums of the fp32
+// scores, left to right.  One warp runs the program, lane b holding candidate
+// b; s_pred / s_gap (kWalkMaxRows entries) keep each step's predecessor and
+// its margin over the second-best predecessor.  Called by every thread of the
+// block, which must have 256 threads.
+template <int K>
+__device__ __forceinline__ void viterbi_verify_request(const float *scores, const int32_t *ids,
+                                                       const int32_t *target, int B, int32_t *tokens,
+                                                       int32_t *choice, float *margin, int32_t *accept_len,
+                                                       int *s_pred, float *s_gap, int *s_choice) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int P = B - 1;
+  if (tid < 32) {
+    double cur = lane == 0 ? 0.0 : -INFINITY;  // best total of a path ending at candidate `lane`
+#pragma unroll 1
+    for (int p = 0; p < P; ++p) {
+      const float *Sp = scores + (int64_t)p * K * K;
+      double best = -INFINITY, second = -INFINITY;
+      int arg = 0;
+#pragma unroll
+      for (int a = 0; a < K; ++a) {
+        const double va = __shfl_sync(DC_FULL_MASK, cur, a);
+        const double t = va + (double)(lane < K ? __ldcg(Sp + a * K + lane) : 0.f);
+        if (t > best) {
+          second = best;
+          best = t;
+          arg = a;
+        } else if (t > second) {
+          second = t;
+        }
+      }
+      if (lane < K) {
+        s_pred[p * K + lane] = arg;
+        s_gap[p * K + lane] = (float)(best - second);
+      }
+      cur = best;
+    }
+    // best final candidate, lowest index on ties
+    double v = lane < K ? cur : -INFINITY;
+    int idx = lane;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const double ov = __shfl_down_sync(DC_FULL_MASK, v, off);
+      const int oi = __shfl_down_sync(DC_FULL_MASK, idx, off);
+      if (ov > v || (ov == v && oi < idx)) {
+        v = ov;
+        idx = oi;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      s_choice[P] = idx;
+      for (int p = P - 1; p >= 0; --p) s_choice[p] = s_pred[p * K + s_choice[p + 1]];
+    }
+  }
+  __syncthreads();
+  emit_request<K>(ids, target, B, tokens, choice, margin, accept_len, s_gap, s_choice);
 }
 
 }  // namespace dc

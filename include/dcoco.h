@@ -6,7 +6,8 @@
  *              Decoding": Core method; Method step details (1)-(5).
  *   [LiLiCorr] "LiLiCorr: Lightweight Likelihood Correlation of Parallel
  *              Drafts for Speculative Decoding": Sec. 3.2 Eq. (1) (cosine
- *              in/out matching), Sec. 3.5 Eq. (8) (greedy walk).
+ *              in/out matching), Sec. 3.5 Eq. (8) (greedy walk), App. E
+ *              Eq. (12) (highest-scoring path).
  *   [FD]       "Faster Decoding": greedy-verification contract.
  *
  * One DFlash-style drafter forward pass gives, per request, a block of
@@ -25,9 +26,12 @@
  *      Delta = 386 -> 256 -> 1 MLP with (erf) GELU          [DCOCO] step (4)
  *      (variant 1: S_p(a,b) = sigma cos(o_p^a, in_{p+1}^b) + l_{p+1}(b),
  *       [o; in] = W_io [E[c]; h_i]                          [LiLiCorr] Eq. (1))
- *   4. prefix-first greedy walk: k_1 = 0 (draft argmax), then
- *      k_{p+1} = argmax_b S_p(k_p, b), ties to the lowest b
+ *   4. path selection, k_1 = 0 (draft argmax) in both rules:
+ *      path_rule 0, prefix-first greedy walk:
+ *        k_{p+1} = argmax_b S_p(k_p, b), ties to the lowest b
  *                                                [DCOCO] step (5); [LiLiCorr] Eq. (8)
+ *      path_rule 1, highest-scoring path: the k maximizing sum_p S_p(k_p, k_{p+1})
+ *        (dynamic program in fp64, ties to the lowest index) [LiLiCorr] App. E Eq. (12)
  *   5. greedy verify: accept_len = length of the longest prefix of the chosen
  *      tokens equal to the target tokens                    [FD]
  *
@@ -83,6 +87,7 @@ typedef struct {
   float ln_eps;     /* LayerNorm epsilon (1e-5)                                */
   int host_staging; /* nonzero: also allocate device staging buffers so that
                        dcoco_correct_host can be used                        */
+  int path_rule;    /* 0 = prefix-first greedy walk, 1 = highest-scoring path */
 } dcoco_config;
 
 /* Corrector weights, fp32, PyTorch Linear layout [out][in], row-major.
@@ -120,7 +125,11 @@ typedef struct {
                           target_tokens != NULL                             */
   int32_t *topk_ids;   /* [N][B][K] candidate token ids, best first         */
   float *topk_val;     /* [N][B][K] candidate logits (exact bf16 values)    */
-  float *margin;       /* [N][B-1] best minus second-best successor score   */
+  float *margin;       /* [N][B-1] path_rule 0: best minus second-best
+                          successor score; path_rule 1: best minus
+                          second-best predecessor total of the chosen
+                          candidate at slot p+1 (+inf when only one
+                          predecessor is possible)                         */
 } dcoco_outputs;
 
 /* Library version, major*10000 + minor*100 + patch. */

@@ -1,7 +1,8 @@
 """Seeded problems shared by the GPU parity tests: synthetic inputs (synth),
 the CPU oracle's answer, the CUDA library's answer, and the comparison rules.
 
-Comparison rules (fixed before any kernel ran):
+Comparison rules (fixed before any kernel ran; `compare_path` holds the
+rules of the highest-scoring-path selection):
   * top-K ids and values, chosen tokens and accept_len: bit-exact;
   * scores: max |GPU - oracle| <= SCORE_TOL = 2e-3 (fp32 vs fp64);
   * the walk: a choice may differ from the oracle only where the oracle's
@@ -37,10 +38,10 @@ class Problem:
     def __init__(self, seed: int, N: int, V: int, d: int, K: int = 16, slots: int = 16,
                  planted: int = 32, boost=(4.0, 12.0), stride: int | None = None, variant: int = 0,
                  sigma: float = 1.0, zero_out: bool = False, perturb: bool = False,
-                 targets: bool = True):
+                 targets: bool = True, path_rule: int = 0):
         rng = np.random.default_rng(seed)
         self.N, self.V, self.d, self.K, self.slots, self.B = N, V, d, K, slots, slots - 1
-        self.variant, self.sigma = variant, sigma
+        self.variant, self.sigma, self.path_rule = variant, sigma, path_rule
         self.stride = stride if stride is not None else ((V + 7) // 8) * 8
         self.logits = synth.make_logits(rng, N, slots, V, planted, boost, stride=self.stride)
         self.hidden = synth.make_hidden(rng, N, slots, d)
@@ -64,7 +65,8 @@ class Problem:
 
     def oracle(self, requests=None):
         return oracle.correct_batch(self.model, self.logits, self.hidden, self.E, self.targets,
-                                    variant=self.variant, sigma=self.sigma, requests=requests)
+                                    variant=self.variant, sigma=self.sigma, requests=requests,
+                                    path_rule=self.path_rule)
 
 
 def bf16_tensor(a: np.ndarray, device="cuda"):
@@ -79,7 +81,7 @@ def run_gpu(prob: Problem, max_batch: int | None = None, corr=None, E_dev=None):
     if own:
         corr = dc.Corrector({k: torch.from_numpy(v) for k, v in prob.w.items()}, prob.V, prob.d,
                             prob.slots, prob.K, max_batch=max_batch or prob.N, variant=prob.variant,
-                            sigma=prob.sigma)
+                            sigma=prob.sigma, path_rule=prob.path_rule)
     E_dev = E_dev if E_dev is not None else bf16_tensor(prob.E)
     tg = None if prob.targets is None else torch.from_numpy(prob.targets).cuda()
     out = corr.correct(bf16_tensor(prob.logits), bf16_tensor(prob.hidden), E_dev, tg,
@@ -125,4 +127,49 @@ def compare(prob: Problem, gpu: dict, ref: dict, tol: float = SCORE_TOL) -> dict
                 assert g["accept_len"][j] == ref["accept_len"][j]
     if diverged == 0:
         np.testing.assert_array_equal(g["tokens"], ref["tokens"])
+    return {"max_score_err": err, "diverged": diverged}
+
+
+def path_total(sc: np.ndarray, path) -> float:
+    return float(sum(sc[p, path[p], path[p + 1]] for p in range(sc.shape[0])))
+
+
+def compare_path(prob: Problem, gpu: dict, ref: dict, tol: float = SCORE_TOL) -> dict:
+    """Rules for the highest-scoring path (path_rule 1):
+      * top-K ids and values bit-exact, scores within tol (as `compare`);
+      * on the GPU's own scores the oracle's dynamic program (fp64, the same
+        order of additions and the same tie rule) must give the GPU's path
+        exactly, and the same margins up to the fp32 rounding of the stored gap;
+      * on the oracle's scores the GPU's path must score within 2 (B-1) tol of
+        the oracle's optimum (each of the B-1 terms moves by at most tol);
+        paths that differ are counted as divergences;
+      * tokens are the chosen candidates' ids and accept_len the verify of
+        those tokens (and the oracle's own when no request diverged)."""
+    req = ref["requests"]
+    g = {k: v[req] for k, v in gpu.items()}
+    np.testing.assert_array_equal(g["topk_ids"], ref["topk_ids"], err_msg="top-K ids")
+    np.testing.assert_array_equal(g["topk_val"], ref["topk_val"], err_msg="top-K values")
+    err = float(np.abs(g["scores"].astype(np.float64) - ref["scores"]).max()) if ref["scores"].size else 0.0
+    assert err <= tol, f"max |score error| {err:.3e} > {tol}"
+    diverged = 0
+    for j, n in enumerate(req):
+        gc = g["choice"][j]
+        own_choice, own_margin = oracle.viterbi(g["scores"][j].astype(np.float64))
+        np.testing.assert_array_equal(gc, own_choice, err_msg=f"request {n}: path on the GPU's scores")
+        np.testing.assert_allclose(g["margin"][j], own_margin.astype(np.float32), rtol=1e-6, atol=1e-6)
+        sc = ref["scores"][j]
+        best = path_total(sc, ref["choice"][j])
+        mine = path_total(sc, gc)
+        assert mine >= best - 2 * (prob.B - 1) * tol, (
+            f"request {n}: GPU path total {mine:.6f} vs optimum {best:.6f}")
+        if not np.array_equal(gc, ref["choice"][j]):
+            diverged += 1
+        toks = ref["topk_ids"][j][np.arange(prob.B), gc]
+        np.testing.assert_array_equal(g["tokens"][j], toks, err_msg=f"tokens of request {n}")
+        if prob.targets is not None:
+            assert g["accept_len"][j] == oracle.verify(toks, prob.targets[n])
+    if diverged == 0:
+        np.testing.assert_array_equal(g["tokens"], ref["tokens"])
+        if prob.targets is not None:
+            np.testing.assert_array_equal(g["accept_len"][:len(req)], ref["accept_len"])
     return {"max_score_err": err, "diverged": diverged}

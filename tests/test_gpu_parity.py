@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 import synth
-from problem import Problem, bf16_tensor, compare, run_gpu
+from problem import compare_path, Problem, bf16_tensor, compare, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -235,3 +235,40 @@ def test_argument_errors(torch_cuda):
     dc.dcoco_correct(corr.handle, corr.weights, 0, lg, hd, E, tokens=tok)  # batch 0: no-op
     assert corr.status() == dc.DCOCO_OK
     corr.close()
+
+
+# ------------------------------------------------------------------ highest-scoring path
+def test_viterbi_tiny_single_request(torch_cuda):
+    """Path rule 1 (LiLiCorr App. E Eq. (12)) at Qwen3-8B shapes, one request."""
+    prob = Problem(20, N=1, V=V_QWEN, d=D_QWEN, path_rule=1)
+    report("viterbi tiny", compare_path(prob, run_gpu(prob), prob.oracle()))
+
+
+def test_viterbi_zero_output_layer(torch_cuda):
+    """Delta = 0: the highest-scoring path is the per-slot draft argmax."""
+    prob = Problem(21, N=2, V=20011, d=512, zero_out=True, path_rule=1)
+    g = run_gpu(prob)
+    report("viterbi zero-output", compare_path(prob, g, prob.oracle()))
+    np.testing.assert_array_equal(g["choice"], 0)
+
+
+@pytest.mark.parametrize("K", [8, 16, 32])
+def test_viterbi_batch(torch_cuda, K):
+    prob = Problem(22 + K, N=4, V=20011, d=512, K=K, perturb=True, path_rule=1)
+    report(f"viterbi K={K}", compare_path(prob, run_gpu(prob), prob.oracle()))
+
+
+def test_viterbi_cosine_variant(torch_cuda):
+    """The cosine variant selects its path in the stand-alone step-5 launch."""
+    prob = Problem(23, N=3, V=20011, d=512, variant=1, path_rule=1)
+    report("viterbi cosine", compare_path(prob, run_gpu(prob), prob.oracle()))
+
+
+def test_viterbi_and_greedy_agree_on_top_k_and_scores(torch_cuda):
+    """Only step 5 depends on the path rule: the top-K and the scores of the
+    two rules are bit-identical on the same inputs."""
+    a = Problem(24, N=2, V=20011, d=512, perturb=True, path_rule=0)
+    b = Problem(24, N=2, V=20011, d=512, perturb=True, path_rule=1)
+    ga, gb = run_gpu(a), run_gpu(b)
+    for k in ("topk_ids", "topk_val", "scores"):
+        np.testing.assert_array_equal(ga[k], gb[k])
