@@ -25,8 +25,11 @@ k_walk_verify(const float *__restrict__ scores, const int32_t *__restrict__ topk
   const int32_t *tg = target ? target + slot0 : nullptr;
   int32_t *ch = choice ? choice + slot0 : nullptr, *al = accept_len ? accept_len + n : nullptr;
   float *mg = margin ? margin + (int64_t)n * P : nullptr;
+  extern __shared__ float4 s_dyn[];  // the request's scores, when the launch gave room for them
+  const bool fits = (size_t)P * K * K * sizeof(float) <= dynamic_smem_bytes();
   if (path_rule == 1)
-    viterbi_verify_request<K>(sc, topk_ids + slot0 * K, tg, B, tokens + slot0, ch, mg, al, s_best, s_gap, s_choice);
+    viterbi_verify_request<K>(sc, topk_ids + slot0 * K, tg, B, tokens + slot0, ch, mg, al, s_best, s_gap, s_choice,
+                              fits ? reinterpret_cast<float *>(s_dyn) : nullptr);
   else
     walk_verify_request<K>(sc, topk_ids + slot0 * K, tg, B, tokens + slot0, ch, mg, al, s_best, s_gap, s_choice);
 }
@@ -37,8 +40,12 @@ template <int K>
 static cudaError_t walk_k(const float *scores, const int32_t *topk_ids, const int32_t *target, int N,
                           int B, int32_t *tokens, int32_t *choice, float *margin, int32_t *accept_len,
                           int path_rule, cudaStream_t st) {
-  k_walk_verify<K><<<N, 256, 0, st>>>(scores, topk_ids, target, N, B, tokens, choice, margin,
-                                         accept_len, path_rule);
+  // the highest-scoring path reads the request's scores from shared memory
+  // when they fit the default 48 KB window
+  const size_t sc_bytes = (size_t)(B - 1) * K * K * sizeof(float);
+  const size_t dyn = path_rule == 1 && sc_bytes <= 48 * 1024 ? sc_bytes : 0;
+  k_walk_verify<K><<<N, 256, dyn, st>>>(scores, topk_ids, target, N, B, tokens, choice, margin,
+                                           accept_len, path_rule);
   return cudaGetLastError();
 }
 

@@ -23,6 +23,13 @@ namespace dc {
 
 constexpr int kWalkMaxRows = 31 * 32;  // (B-1) * K, B <= 31, K <= 32
 
+// Bytes of dynamic shared memory this block was launched with.
+__device__ __forceinline__ uint32_t dynamic_smem_bytes() {
+  uint32_t n;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(n));
+  return n;
+}
+
 // scores: [(B-1)][K][K] of this request; ids: [B][K]; target: [B] or null.
 // s_best / s_gap: kWalkMaxRows entries; s_choice: 32.  Called by every thread
 // of the block, which must have 256 threads.
@@ -107,55 +114,100 @@ __device__ __forceinline__ void emit_request(const int32_t *ids, const int32_t *
   }
 }
 
+// One step of the highest-scoring-path program for the warp: lane b (< K)
+// returns max_a cur_a + S(a, b) (lowest a on ties) in *best, that a in *arg and
+// the best total over the other predecessors in *second.  Every lane loads
+// (lanes past K read a copy of another column): no divergent branch sits
+// between the shuffles.
+template <int K, bool kSmem>
+__device__ __forceinline__ void path_step(const float *Sp, float cur, int lane, float *best_out, int *arg_out,
+                                          float *second_out) {
+  const int col = lane & (K - 1);
+  float t[K];
+#pragma unroll
+  for (int a = 0; a < K; ++a) {
+    const float s = kSmem ? Sp[a * K + col] : __ldcg(Sp + a * K + col);
+    t[a] = __shfl_sync(DC_FULL_MASK, cur, a) + s;
+  }
+  // two max trees: the best (the lower index keeps ties), then the best of the others
+  float bv[K];
+  int bi[K];
+#pragma unroll
+  for (int a = 0; a < K; ++a) {
+    bv[a] = t[a];
+    bi[a] = a;
+  }
+#pragma unroll
+  for (int w = 1; w < K; w *= 2)
+#pragma unroll
+    for (int a = 0; a + w < K; a += 2 * w) {
+      const bool right = bv[a + w] > bv[a];
+      bv[a] = right ? bv[a + w] : bv[a];
+      bi[a] = right ? bi[a + w] : bi[a];
+    }
+  const int arg = bi[0];
+  const float best = bv[0];
+#pragma unroll
+  for (int a = 0; a < K; ++a) bv[a] = a == arg ? -INFINITY : t[a];
+#pragma unroll
+  for (int w = 1; w < K; w *= 2)
+#pragma unroll
+    for (int a = 0; a + w < K; a += 2 * w) bv[a] = fmaxf(bv[a], bv[a + w]);
+  *best_out = best;
+  *arg_out = arg;
+  *second_out = bv[0];
+}
+
 // Highest-scoring path for one request.  LiLiCorr page, App. E "Path
 // selection", Eq. (12): the path total is the sum of its adjacent-pair
 // terms, g(c) = sum_p S_p(c_p, c_{p+1}); a left-to-right dynamic program keeps,
 // for every candidate, the best total of a path ending there and that path's
 // predecessor, and the path is traced back from the best final candidate.
 // The first draft slot keeps candidate 0 (the draft argmax, as in the greedy
-// walk); ties go to the lowest index.  Totals are fp64 sums of the fp32
-// scores, left to right.  One warp runs the program, lane b holding candidate
-// b; s_pred / s_gap (kWalkMaxRows entries) keep each step's predecessor and
-// its margin over the second-best predecessor.  Called by every thread of the
-// block, which must have 256 threads.
+// walk); ties go to the lowest index.  Totals are fp32 sums of the scores,
+// left to right.  All threads first copy the request's scores to `s_sc`
+// (when it is not null: (B-1) K^2 floats, 16-byte aligned); one warp then
+// runs the program, lane b holding candidate b; s_pred / s_gap (kWalkMaxRows
+// entries) keep each step's predecessor and its margin over the second-best
+// predecessor.  Called by every thread of the block, which must have 256
+// threads.
 template <int K>
 __device__ __forceinline__ void viterbi_verify_request(const float *scores, const int32_t *ids,
                                                        const int32_t *target, int B, int32_t *tokens,
                                                        int32_t *choice, float *margin, int32_t *accept_len,
-                                                       int *s_pred, float *s_gap, int *s_choice) {
+                                                       int *s_pred, float *s_gap, int *s_choice, float *s_sc) {
   const int tid = threadIdx.x, lane = tid & 31;
   const int P = B - 1;
+  if (s_sc) {
+    // one pass through L2 for the whole request (written by other blocks of
+    // the launch: read past L1)
+    const int n4 = P * K * K / 4;
+    for (int i = tid; i < n4; i += 256)
+      reinterpret_cast<float4 *>(s_sc)[i] = __ldcg(reinterpret_cast<const float4 *>(scores) + i);
+    __syncthreads();
+  }
   if (tid < 32) {
-    double cur = lane == 0 ? 0.0 : -INFINITY;  // best total of a path ending at candidate `lane`
+    float cur = lane == 0 ? 0.f : -INFINITY;  // best total of a path ending at candidate `lane`
 #pragma unroll 1
     for (int p = 0; p < P; ++p) {
-      const float *Sp = scores + (int64_t)p * K * K;
-      double best = -INFINITY, second = -INFINITY;
-      int arg = 0;
-#pragma unroll
-      for (int a = 0; a < K; ++a) {
-        const double va = __shfl_sync(DC_FULL_MASK, cur, a);
-        const double t = va + (double)(lane < K ? __ldcg(Sp + a * K + lane) : 0.f);
-        if (t > best) {
-          second = best;
-          best = t;
-          arg = a;
-        } else if (t > second) {
-          second = t;
-        }
-      }
+      float best, second;
+      int arg;
+      if (s_sc)
+        path_step<K, true>(s_sc + p * K * K, cur, lane, &best, &arg, &second);
+      else
+        path_step<K, false>(scores + p * K * K, cur, lane, &best, &arg, &second);
       if (lane < K) {
         s_pred[p * K + lane] = arg;
-        s_gap[p * K + lane] = (float)(best - second);
+        s_gap[p * K + lane] = best - second;
       }
       cur = best;
     }
     // best final candidate, lowest index on ties
-    double v = lane < K ? cur : -INFINITY;
+    float v = lane < K ? cur : -INFINITY;
     int idx = lane;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-      const double ov = __shfl_down_sync(DC_FULL_MASK, v, off);
+      const float ov = __shfl_down_sync(DC_FULL_MASK, v, off);
       const int oi = __shfl_down_sync(DC_FULL_MASK, idx, off);
       if (ov > v || (ov == v && oi < idx)) {
         v = ov;

@@ -76,6 +76,7 @@ def lib():
             L.orc_cosine_transition.restype = C.c_double
             L.orc_walk.argtypes = [_PD, C.c_int, C.c_int, _PI, _PD]
             L.orc_viterbi.argtypes = [_PD, C.c_int, C.c_int, _PI, _PD]
+            L.orc_viterbi_f32.argtypes = [_PF, C.c_int, C.c_int, _PI, _PF]
             L.orc_verify.argtypes = [_PI, _PI, C.c_int]
             L.orc_verify.restype = C.c_int
             L.orc_expected_yield.argtypes = [_PD, C.c_int, _PD]
@@ -199,6 +200,16 @@ def viterbi(scores: np.ndarray):
     choice = np.empty(P + 1, np.int32)
     margin = np.empty(P, np.float64)
     lib().orc_viterbi(_p(s, C.c_double), P + 1, K, _p(choice, C.c_int32), _p(margin, C.c_double))
+    return choice, margin
+
+
+def viterbi_f32(scores: np.ndarray):
+    """The highest-scoring path with single-precision totals (scores given as float32)."""
+    s = np.ascontiguousarray(scores, dtype=np.float32)
+    P, K, _ = s.shape
+    choice = np.empty(P + 1, np.int32)
+    margin = np.empty(P, np.float32)
+    lib().orc_viterbi_f32(_p(s, C.c_float), P + 1, K, _p(choice, C.c_int32), _p(margin, C.c_float))
     return choice, margin
 
 

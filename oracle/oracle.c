@@ -227,6 +227,56 @@ void orc_walk(const double *scores, int B, int K, int32_t *choice, double *margi
  * margin[p] = best minus second best, over predecessors a, of
  * best_p(a) + S_p(a, c_{p+1}) for the chosen c_{p+1} (+inf when K == 1).
  * ------------------------------------------------------------------------- */
+void orc_viterbi_f32(const float *scores, int B, int K, int32_t *choice, float *margin) {
+  /* The same program with every total kept in single precision, for
+   * comparing decisions with a single-precision kernel on identical scores. */
+  float *best = (float *)malloc((size_t)B * K * sizeof(float));
+  int32_t *pred = (int32_t *)malloc((size_t)B * K * sizeof(int32_t));
+  if (!best || !pred) {
+    free(best);
+    free(pred);
+    for (int i = 0; i < B; ++i) choice[i] = -1;
+    return;
+  }
+  for (int a = 0; a < K; ++a) best[a] = a == 0 ? 0.0f : -INFINITY;
+  for (int p = 0; p < B - 1; ++p) {
+    const float *S = scores + (size_t)p * K * K;
+    for (int b = 0; b < K; ++b) {
+      int arg = 0;
+      float v = best[(size_t)p * K] + S[b];
+      for (int a = 1; a < K; ++a) {
+        const float t = best[(size_t)p * K + a] + S[(size_t)a * K + b];
+        if (t > v) {
+          v = t;
+          arg = a;
+        }
+      }
+      best[(size_t)(p + 1) * K + b] = v;
+      pred[(size_t)(p + 1) * K + b] = arg;
+    }
+  }
+  int last = 0;
+  for (int b = 1; b < K; ++b)
+    if (best[(size_t)(B - 1) * K + b] > best[(size_t)(B - 1) * K + last]) last = b;
+  choice[B - 1] = last;
+  for (int p = B - 1; p > 0; --p) choice[p - 1] = pred[(size_t)p * K + choice[p]];
+  if (margin)
+    for (int p = 0; p < B - 1; ++p) {
+      const float *S = scores + (size_t)p * K * K;
+      const int b = choice[p + 1], a0 = choice[p];
+      const float top = best[(size_t)p * K + a0] + S[(size_t)a0 * K + b];
+      float second = -INFINITY;
+      for (int a = 0; a < K; ++a)
+        if (a != a0) {
+          const float t = best[(size_t)p * K + a] + S[(size_t)a * K + b];
+          if (t > second) second = t;
+        }
+      margin[p] = top - second;
+    }
+  free(best);
+  free(pred);
+}
+
 void orc_viterbi(const double *scores, int B, int K, int32_t *choice, double *margin) {
   double *best = (double *)malloc((size_t)B * K * sizeof(double));
   int32_t *pred = (int32_t *)malloc((size_t)B * K * sizeof(int32_t));

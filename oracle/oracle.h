@@ -110,6 +110,9 @@ void orc_walk(const double *scores, int B, int K, int32_t *choice, double *margi
  * (Viterbi), choice[0] = 0, ties to the lowest index; margin[p] = gap between
  * the best and second-best predecessor of the chosen candidate at p+1. */
 void orc_viterbi(const double *scores, int B, int K, int32_t *choice, double *margin);
+/* The same program with single-precision totals (t = total + score rounded to
+ * float at every step), to compare decisions with a single-precision kernel. */
+void orc_viterbi_f32(const float *scores, int B, int K, int32_t *choice, float *margin);
 
 /* Greedy verify: number of leading slots whose token equals the target. */
 int orc_verify(const int32_t *tokens, const int32_t *target, int B);

@@ -357,6 +357,26 @@ def test_viterbi_brute_force(P, K):
             np.testing.assert_allclose(margin[p], top - second, rtol=0, atol=1e-12)
 
 
+def test_viterbi_f32_brute_force():
+    """The single-precision program against enumeration with float32 totals
+    summed left to right (the program's own order along any path)."""
+    rng = np.random.default_rng(31)
+    for P, K in [(3, 4), (5, 3), (4, 5)]:
+        for _ in range(5):
+            sc = rng.standard_normal((P, K, K)).astype(np.float32)
+            choice, margin = oracle.viterbi_f32(sc)
+            best_path, best_val = None, np.float32(-np.inf)
+            for tail in itertools.product(range(K), repeat=P):
+                path = (0,) + tail
+                v = np.float32(0.0)
+                for p in range(P):
+                    v = np.float32(v + sc[p, path[p], path[p + 1]])
+                if v > best_val:
+                    best_path, best_val = path, v
+            assert tuple(choice) == best_path
+            assert tuple(oracle.viterbi(sc.astype(np.float64))[0]) == best_path
+
+
 def test_viterbi_ties_go_to_lowest_index():
     sc = np.zeros((4, 5, 5))
     choice, margin = oracle.viterbi(sc)
