@@ -38,7 +38,8 @@ def build(force: bool = False) -> str:
 
 class Dims(C.Structure):
     _fields_ = [("V", C.c_int), ("d", C.c_int), ("slots", C.c_int), ("K", C.c_int),
-                ("r", C.c_int), ("H", C.c_int), ("ln_eps", C.c_double)]
+                ("r", C.c_int), ("H", C.c_int), ("ln_eps", C.c_double),
+                ("beam_width", C.c_int), ("beam_topm", C.c_int)]
 
 
 class Weights(C.Structure):
@@ -77,6 +78,8 @@ def lib():
             L.orc_walk.argtypes = [_PD, C.c_int, C.c_int, _PI, _PD]
             L.orc_viterbi.argtypes = [_PD, C.c_int, C.c_int, _PI, _PD]
             L.orc_viterbi_f32.argtypes = [_PF, C.c_int, C.c_int, _PI, _PF]
+            L.orc_beam.argtypes = [_PD, C.c_int, C.c_int, C.c_int, C.c_int, _PI, _PD]
+            L.orc_beam_f32.argtypes = [_PF, C.c_int, C.c_int, C.c_int, C.c_int, _PI, _PF]
             L.orc_verify.argtypes = [_PI, _PI, C.c_int]
             L.orc_verify.restype = C.c_int
             L.orc_expected_yield.argtypes = [_PD, C.c_int, _PD]
@@ -107,9 +110,10 @@ class Model:
     """Holds fp32 weights (kept alive) and the dims struct for the C calls."""
 
     def __init__(self, weights: dict[str, np.ndarray], V: int, d: int, slots: int = 16,
-                 K: int = 16, r: int = 128, H: int = 256, ln_eps: float = 1e-5):
+                 K: int = 16, r: int = 128, H: int = 256, ln_eps: float = 1e-5, beam_width: int = 2,
+                 beam_topm: int = 0):
         self.w = {k: np.ascontiguousarray(v, dtype=np.float32) for k, v in weights.items()}
-        self.dims = Dims(V, d, slots, K, r, H, ln_eps)
+        self.dims = Dims(V, d, slots, K, r, H, ln_eps, beam_width, beam_topm)
         self.cw = Weights(*[_p(self.w.get(f[0]), C.c_float) for f in Weights._fields_])
 
     @property
@@ -213,9 +217,33 @@ def viterbi_f32(scores: np.ndarray):
     return choice, margin
 
 
-def select_path(scores: np.ndarray, path_rule: int = 0):
-    """path_rule 0: greedy walk, 1: highest-scoring path."""
-    return viterbi(scores) if path_rule == 1 else walk(scores)
+def beam(scores: np.ndarray, width: int, topm: int = 0):
+    """scores [B-1, K, K] -> (choice [B], margin [B-1]) of the beam walk."""
+    s = np.ascontiguousarray(scores, dtype=np.float64)
+    P, K, _ = s.shape
+    choice = np.empty(P + 1, np.int32)
+    margin = np.empty(P, np.float64)
+    lib().orc_beam(_p(s, C.c_double), P + 1, K, width, topm, _p(choice, C.c_int32), _p(margin, C.c_double))
+    return choice, margin
+
+
+def beam_f32(scores: np.ndarray, width: int, topm: int = 0):
+    """The beam walk with float totals (scores given as float32)."""
+    s = np.ascontiguousarray(scores, dtype=np.float32)
+    P, K, _ = s.shape
+    choice = np.empty(P + 1, np.int32)
+    margin = np.empty(P, np.float32)
+    lib().orc_beam_f32(_p(s, C.c_float), P + 1, K, width, topm, _p(choice, C.c_int32), _p(margin, C.c_float))
+    return choice, margin
+
+
+def select_path(scores: np.ndarray, path_rule: int = 0, width: int = 2, topm: int = 0):
+    """path_rule 0: greedy walk, 1: highest-scoring path, 2: beam walk."""
+    if path_rule == 1:
+        return viterbi(scores)
+    if path_rule == 2:
+        return beam(scores, width, topm)
+    return walk(scores)
 
 
 def verify(tokens, target) -> int:

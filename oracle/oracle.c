@@ -326,6 +326,125 @@ void orc_viterbi(const double *scores, int B, int K, int32_t *choice, double *ma
 }
 
 /* ---------------------------------------------------------------------------
+ * Beam walk.  [DCOCO] page, reproduction assessment, weaknesses (2) and (3):
+ * the greedy walk can be widened at almost no cost into a narrow beam search
+ * (beam = 2-4, O(B K beam)), and the K^2 transitions sparsified by keeping only
+ * the top-m successors of each predecessor (O(B K m)).  Reading: the beam
+ * holds the W partial paths of highest cumulative score
+ * sum_p S_p(k_p, k_{p+1}), starting from the draft argmax of the first slot;
+ * each is extended to its m best successors (by S_p(k_p, .), ties to the lower
+ * index; m = K: all); the W best extensions are kept, ordered by score
+ * descending, then parent rank, then successor index; the answer is the best
+ * complete path.  margin[p] = S_p(k_p, k_{p+1}) - max over b != k_{p+1} of
+ * S_p(k_p, b) along the answer (+inf when K == 1).  One body, instantiated
+ * for double totals (the plain definition) and for float totals (the
+ * precision of a single-precision kernel, for comparing decisions).
+ * ------------------------------------------------------------------------- */
+#define ORC_BEAM_BODY(REAL)                                                                   \
+  typedef struct {                                                                            \
+    REAL total;                                                                               \
+    int parent, b;                                                                            \
+  } ext_t;                                                                                    \
+  const int P = B - 1;                                                                        \
+  if (W < 1) W = 1;                                                                           \
+  if (m < 1 || m > K) m = K;                                                                  \
+  REAL *total = (REAL *)malloc((size_t)W * sizeof(REAL));                                     \
+  REAL *ntotal = (REAL *)malloc((size_t)W * sizeof(REAL));                                    \
+  int32_t *last = (int32_t *)malloc((size_t)W * sizeof(int32_t));                            \
+  int32_t *nlast = (int32_t *)malloc((size_t)W * sizeof(int32_t));                           \
+  int32_t *par = (int32_t *)malloc((size_t)(P > 0 ? P : 1) * W * sizeof(int32_t));           \
+  int32_t *cand = (int32_t *)malloc((size_t)(P > 0 ? P : 1) * W * sizeof(int32_t));          \
+  ext_t *ext = (ext_t *)malloc((size_t)W * K * sizeof(ext_t));                                \
+  int32_t *order = (int32_t *)malloc((size_t)K * sizeof(int32_t));                           \
+  if (!total || !ntotal || !last || !nlast || !par || !cand || !ext || !order) {              \
+    for (int i = 0; i < B; ++i) choice[i] = -1;                                               \
+    goto done;                                                                                \
+  }                                                                                           \
+  {                                                                                           \
+    int nb = 1;                                                                               \
+    total[0] = 0;                                                                             \
+    last[0] = 0;                                                                              \
+    for (int p = 0; p < P; ++p) {                                                             \
+      const REAL *S = scores + (size_t)p * K * K;                                             \
+      int ne = 0;                                                                             \
+      for (int i = 0; i < nb; ++i) {                                                          \
+        const REAL *row = S + (size_t)last[i] * K;                                            \
+        /* successors by score descending, ties to the lower index (insertion sort) */        \
+        for (int b = 0; b < K; ++b) {                                                         \
+          int j = b;                                                                          \
+          while (j > 0 && row[order[j - 1]] < row[b]) {                                       \
+            order[j] = order[j - 1];                                                          \
+            --j;                                                                              \
+          }                                                                                   \
+          order[j] = b;                                                                       \
+        }                                                                                     \
+        for (int t = 0; t < m; ++t) {                                                         \
+          const int b = order[t];                                                             \
+          ext[ne].total = total[i] + row[b];                                                  \
+          ext[ne].parent = i;                                                                 \
+          ext[ne].b = b;                                                                      \
+          ++ne;                                                                               \
+        }                                                                                     \
+      }                                                                                       \
+      /* the W best extensions: score desc, then parent rank, then successor */               \
+      const int keep = ne < W ? ne : W;                                                       \
+      for (int r = 0; r < keep; ++r) {                                                        \
+        int best = -1;                                                                        \
+        for (int e = 0; e < ne; ++e) {                                                        \
+          if (ext[e].parent < 0) continue;                                                    \
+          if (best < 0 || ext[e].total > ext[best].total ||                                   \
+              (ext[e].total == ext[best].total &&                                             \
+               (ext[e].parent < ext[best].parent ||                                           \
+                (ext[e].parent == ext[best].parent && ext[e].b < ext[best].b))))              \
+            best = e;                                                                         \
+        }                                                                                     \
+        ntotal[r] = ext[best].total;                                                          \
+        nlast[r] = ext[best].b;                                                               \
+        par[(size_t)p * W + r] = ext[best].parent;                                            \
+        cand[(size_t)p * W + r] = ext[best].b;                                                \
+        ext[best].parent = -1; /* taken */                                                    \
+      }                                                                                       \
+      nb = keep;                                                                              \
+      for (int r = 0; r < nb; ++r) {                                                          \
+        total[r] = ntotal[r];                                                                 \
+        last[r] = nlast[r];                                                                   \
+      }                                                                                       \
+    }                                                                                         \
+    /* trace the best beam (rank 0) back */                                                   \
+    int r = 0;                                                                                \
+    for (int p = P - 1; p >= 0; --p) {                                                        \
+      choice[p + 1] = cand[(size_t)p * W + r];                                                \
+      r = par[(size_t)p * W + r];                                                             \
+    }                                                                                         \
+    choice[0] = 0;                                                                            \
+    if (margin)                                                                               \
+      for (int p = 0; p < P; ++p) {                                                           \
+        const REAL *row = scores + ((size_t)p * K + choice[p]) * K;                           \
+        REAL second = -INFINITY;                                                              \
+        for (int b = 0; b < K; ++b)                                                           \
+          if (b != choice[p + 1] && row[b] > second) second = row[b];                         \
+        margin[p] = row[choice[p + 1]] - second;                                              \
+      }                                                                                       \
+  }                                                                                           \
+  done:                                                                                       \
+  free(total);                                                                                \
+  free(ntotal);                                                                               \
+  free(last);                                                                                 \
+  free(nlast);                                                                                \
+  free(par);                                                                                  \
+  free(cand);                                                                                 \
+  free(ext);                                                                                  \
+  free(order);
+
+void orc_beam(const double *scores, int B, int K, int W, int m, int32_t *choice, double *margin) {
+  ORC_BEAM_BODY(double)
+}
+
+void orc_beam_f32(const float *scores, int B, int K, int W, int m, int32_t *choice, float *margin) {
+  ORC_BEAM_BODY(float)
+}
+
+/* ---------------------------------------------------------------------------
  * Greedy verification.  [FD] "Modified rejection sampling ..." section, the
  * greedy-verification contract: accept the longest run that matches the
  * target's greedy tokens.  The accepted length counts draft slots only.
@@ -375,7 +494,7 @@ int orc_correct_request(const orc_dims *dm, const orc_weights *w, int variant, d
                         orc_intermediates *inter) {
   const int B = dm->slots - 1, K = dm->K, r = dm->r, d = dm->d;
   if (B < 2 || K < 2 || K > dm->V || r < 1 || (variant != 0 && variant != 1) ||
-      (path_rule != 0 && path_rule != 1))
+      path_rule < 0 || path_rule > 2)
     return -1;
 
   /* (1) top-K per draft slot; slot 0 (the anchor) is not read. */
@@ -432,6 +551,8 @@ int orc_correct_request(const orc_dims *dm, const orc_weights *w, int variant, d
   /* (5) walk, then the chosen tokens */
   if (path_rule == 1)
     orc_viterbi(scores, B, K, choice, margin);
+  else if (path_rule == 2)
+    orc_beam(scores, B, K, dm->beam_width, dm->beam_topm, choice, margin);
   else
     orc_walk(scores, B, K, choice, margin);
   for (int i = 0; i < B; ++i) tokens[i] = topk_ids[(size_t)i * K + choice[i]];

@@ -417,6 +417,73 @@ def test_zero_output_layer_viterbi_reproduces_draft_argmax():
     np.testing.assert_array_equal(out["tokens"], out["topk_ids"][:, 0])
 
 
+# --------------------------------------------------------------- beam walk
+BEAM_EXAMPLE = np.array([
+    # pair 1 (slot 1 -> 2); only row 0 is reachable (slot 1 keeps candidate 0)
+    [[1.0, 0.9, 0.0], [0.0, 0.0, 0.0], [0.0, 0.0, 0.0]],
+    # pair 2 (slot 2 -> 3)
+    [[0.0, 0.1, 0.0], [0.5, 0.0, 0.0], [5.0, 0.0, 0.0]],
+])
+
+
+def test_beam_hand_example():
+    """Worked by hand from the definition (DCOCO page, reproduction
+    assessment, weaknesses (2)-(3)): greedy takes 0 then 1 (total 1.1); a
+    beam of 2 keeps {0: 1.0, 1: 0.9} after pair 1 and then extends 1 -> 0 for
+    1.4; a beam of 3 keeps candidate 2 as well and reaches 2 -> 0 for 5.0 (the
+    highest-scoring path); top-2 successors give the beam-2 path again,
+    top-1 the greedy one."""
+    sc = BEAM_EXAMPLE
+    assert list(oracle.walk(sc)[0]) == [0, 0, 1]
+    choice, margin = oracle.beam(sc, 2)
+    assert list(choice) == [0, 1, 0]
+    np.testing.assert_allclose(margin, [0.9 - 1.0, 0.5 - 0.0], atol=1e-15)
+    assert list(oracle.beam(sc, 3)[0]) == [0, 2, 0]
+    assert list(oracle.viterbi(sc)[0]) == [0, 2, 0]
+    assert list(oracle.beam(sc, 2, topm=2)[0]) == [0, 1, 0]
+    assert list(oracle.beam(sc, 2, topm=1)[0]) == [0, 0, 1]
+    assert list(oracle.beam_f32(sc.astype(np.float32), 2)[0]) == [0, 1, 0]
+
+
+def test_beam_width_one_and_top_one_are_the_greedy_walk():
+    rng = np.random.default_rng(41)
+    for _ in range(40):
+        P, K = int(rng.integers(1, 15)), int(rng.integers(2, 33))
+        sc = np.round(rng.standard_normal((P, K, K)), 1)  # ties happen
+        cg, mg = oracle.walk(sc)
+        for width, topm in ((1, 0), (1, K), (3, 1)):
+            cb, mb = oracle.beam(sc, width, topm)
+            np.testing.assert_array_equal(cb, cg)
+            np.testing.assert_array_equal(mb, mg)
+
+
+@pytest.mark.parametrize("P,K", [(3, 3), (4, 3), (3, 4)])
+def test_beam_wide_enough_is_exhaustive(P, K):
+    """A beam at least as wide as the number of paths keeps every path: its
+    answer is the maximizer found by enumeration."""
+    rng = np.random.default_rng(42 + P * K)
+    for _ in range(5):
+        sc = rng.standard_normal((P, K, K))
+        best_path, best_val = None, -np.inf
+        for tail in itertools.product(range(K), repeat=P):
+            v = path_total(sc, (0,) + tail)
+            if v > best_val:
+                best_path, best_val = (0,) + tail, v
+        assert tuple(oracle.beam(sc, K ** P)[0]) == best_path
+
+
+def test_zero_output_layer_beam_reproduces_draft_argmax():
+    rng = np.random.default_rng(43)
+    V, d, slots, K = 600, 64, 12, 8
+    m, _ = tiny_model(rng, V=V, d=d, K=K, slots=slots, zero_out=True)
+    m.dims.beam_width = 4
+    logits = synth.make_logits(rng, 1, slots, V, 16, (4, 12))
+    hidden = synth.make_hidden(rng, 1, slots, d)
+    E = synth.make_embedding(rng, V, d)
+    out = oracle.correct_request(m, logits[0], hidden[0], E, path_rule=2)
+    np.testing.assert_array_equal(out["choice"], 0)
+
+
 # --------------------------------------------------------------- cosine variant
 def test_cosine_vectors_and_transition():
     rng = np.random.default_rng(12)
