@@ -51,8 +51,10 @@ def parse():
                     help="requests in the CPU-oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true", help="time eager calls only")
-    ap.add_argument("--path-rule", choices=["greedy", "viterbi"], default="greedy",
-                    help="step 5: prefix-first greedy walk (default) or the highest-scoring path")
+    ap.add_argument("--path-rule", choices=["greedy", "viterbi", "beam"], default="greedy",
+                    help="step 5: prefix-first greedy walk (default), highest-scoring path or beam walk")
+    ap.add_argument("--beam-width", type=int, default=4, help="beam walk: partial paths kept (1..4)")
+    ap.add_argument("--beam-topm", type=int, default=0, help="beam walk: successors per predecessor (0 = K)")
     ap.add_argument("--only", choices=["topk"], default=None,
                     help="time one kernel stage alone through its own entry point (for profiling)")
     return ap.parse_args()
@@ -196,9 +198,11 @@ def gpu_embedding(torch, seed, V, d, device):
 
 
 # ------------------------------------------------------------------ CPU oracle baseline
-def cpu_baseline(w, n_req: int, logits_np, hidden_np, E_np, targets_np, weights_np, path_rule: int = 0):
+def cpu_baseline(w, n_req: int, logits_np, hidden_np, E_np, targets_np, weights_np, path_rule: int = 0,
+                 beam_width: int = 4, beam_topm: int = 0):
     import oracle
-    m = oracle.Model(weights_np, V=w["V"], d=w["d"], slots=w["slots"], K=w["K"])
+    m = oracle.Model(weights_np, V=w["V"], d=w["d"], slots=w["slots"], K=w["K"], beam_width=beam_width,
+                     beam_topm=beam_topm)
     threads = os.cpu_count() or 1
     req = list(range(min(n_req, w["N"])))
     oracle.correct_batch(m, logits_np[:1], hidden_np[:1], E_np, targets_np[:1], requests=[0], path_rule=path_rule,
@@ -239,9 +243,10 @@ def run_ours(args):
     weights_np = synth.make_weights(np.random.default_rng(7 + rank), d)
     E = gpu_embedding(torch, 11 + rank, V, d, device)
     sets = [gpu_inputs(torch, 1000 + 97 * rank + s, w, device) for s in range(args.sets)]
-    path_rule = 1 if args.path_rule == "viterbi" else 0
+    path_rule = {"greedy": 0, "viterbi": 1, "beam": 2}[args.path_rule]
     corr = dc.Corrector({k: torch.from_numpy(v) for k, v in weights_np.items()}, V, d, S, K,
-                        max_batch=N, host_staging=True, path_rule=path_rule)
+                        max_batch=N, host_staging=True, path_rule=path_rule, beam_width=args.beam_width,
+                        beam_topm=args.beam_topm)
     outs = [corr.alloc_outputs(N, device, full=False) for _ in range(args.sets)]
     torch.cuda.synchronize()
 
@@ -375,7 +380,7 @@ def run_ours(args):
         cpu = cpu_baseline(w, args.cpu_requests, lg.view(torch.int16).cpu().numpy().view(np.uint16),
                            hd.view(torch.int16).cpu().numpy().view(np.uint16),
                            E.view(torch.int16).cpu().numpy().view(np.uint16), tg.cpu().numpy(), weights_np,
-                           path_rule)
+                           path_rule, args.beam_width, args.beam_topm)
     corr.close()
 
     if rank == 0:
@@ -389,7 +394,8 @@ def run_ours(args):
                                    "K=16, r=128, MLP 386-256-1 fp32 weights",
                        "global_batch": world * N, "per_gpu_batch": N, "parallelism": f"replicas x{world}",
                        "inputs": "bf16; arithmetic fp32",
-                       "path_rule": args.path_rule,
+                       "path_rule": args.path_rule if args.path_rule != "beam" else
+                       f"beam (width {args.beam_width}, top-m {args.beam_topm or K})",
                        "l2": f"{args.sets} rotating input sets of 160 MB (> 129 MB L2), no flush"},
             "us_per_block": step_s * 1e6 / N,
             "step_us": {"p10": 1e3 * sorted(per)[len(per) // 10], "p50": 1e3 * statistics.median(per),
@@ -469,7 +475,8 @@ def run_reference(args):
                       for n in range(per_step)])
     targets = synth.draw_targets(rng, top16, w["V"])
 
-    path_rule = 1 if args.path_rule == "viterbi" else 0
+    path_rule = {"greedy": 0, "viterbi": 1, "beam": 2}[args.path_rule]
+    m.dims.beam_width, m.dims.beam_topm = args.beam_width, args.beam_topm
 
     def step():
         oracle.correct_batch(m, logits, hidden, E, targets, threads=threads, path_rule=path_rule)

@@ -36,7 +36,8 @@ class dcoco_config(C.Structure):
     _fields_ = [("vocab", C.c_int), ("hidden", C.c_int), ("slots", C.c_int), ("topk", C.c_int),
                 ("rank", C.c_int), ("mlp_hidden", C.c_int), ("max_batch", C.c_int),
                 ("variant", C.c_int), ("sigma", C.c_float), ("ln_eps", C.c_float),
-                ("host_staging", C.c_int), ("path_rule", C.c_int)]
+                ("host_staging", C.c_int), ("path_rule", C.c_int), ("beam_width", C.c_int),
+                ("beam_topm", C.c_int)]
 
 
 WEIGHT_NAMES = ("w_cand", "w_ctx", "w_fuse", "ln_gamma", "ln_beta", "w_pair", "w1", "b1", "w2",
@@ -136,10 +137,12 @@ def dcoco_status_string(status: int) -> str:
 
 def dcoco_create(vocab: int, hidden: int, slots: int = 16, topk: int = 16, max_batch: int = 32,
                  variant: int = 0, sigma: float = 1.0, ln_eps: float = 1e-5, rank: int = 128,
-                 mlp_hidden: int = 256, host_staging: bool = False, path_rule: int = 0) -> C.c_void_p:
-    """path_rule 0: prefix-first greedy walk; 1: highest-scoring path."""
+                 mlp_hidden: int = 256, host_staging: bool = False, path_rule: int = 0,
+                 beam_width: int = 2, beam_topm: int = 0) -> C.c_void_p:
+    """path_rule 0: prefix-first greedy walk; 1: highest-scoring path; 2: beam walk
+    (beam_width partial paths, beam_topm successors each, 0 = all)."""
     cfg = dcoco_config(vocab, hidden, slots, topk, rank, mlp_hidden, max_batch, variant, sigma, ln_eps,
-                       int(host_staging), int(path_rule))
+                       int(host_staging), int(path_rule), int(beam_width), int(beam_topm))
     h = C.c_void_p()
     _check(_lib.dcoco_create(C.byref(cfg), C.byref(h)), "dcoco_create")
     return h
@@ -255,13 +258,14 @@ class Corrector:
 
     def __init__(self, weights: dict, vocab: int, hidden: int, slots: int = 16, topk: int = 16,
                  max_batch: int = 32, variant: int = 0, sigma: float = 1.0, ln_eps: float = 1e-5,
-                 host_staging: bool = False, path_rule: int = 0):
+                 host_staging: bool = False, path_rule: int = 0, beam_width: int = 2, beam_topm: int = 0):
         self.vocab, self.hidden, self.slots, self.topk = vocab, hidden, slots, topk
         self.B = slots - 1
         self.max_batch = max_batch
         self.path_rule = path_rule
         self.handle = dcoco_create(vocab, hidden, slots, topk, max_batch, variant, sigma, ln_eps,
-                                   host_staging=host_staging, path_rule=path_rule)
+                                   host_staging=host_staging, path_rule=path_rule, beam_width=beam_width,
+                                   beam_topm=beam_topm)
         try:
             self.weights = dcoco_weights_create(self.handle, weights)
         except Exception:

@@ -153,7 +153,10 @@ int validate_config(const dcoco_config *cfg) {
   if (cfg->rank != kR || cfg->mlp_hidden != kH) return DCOCO_EUNSUPPORTED;
   if (cfg->topk != 8 && cfg->topk != 16 && cfg->topk != 32) return DCOCO_EUNSUPPORTED;
   if (cfg->variant != 0 && cfg->variant != 1) return DCOCO_EUNSUPPORTED;
-  if (cfg->path_rule != 0 && cfg->path_rule != 1) return DCOCO_EUNSUPPORTED;
+  if (cfg->path_rule < 0 || cfg->path_rule > 2) return DCOCO_EUNSUPPORTED;
+  if (cfg->path_rule == 2 && (cfg->beam_width < 1 || cfg->beam_width > 4 || cfg->beam_topm < 0 ||
+                              cfg->beam_topm > cfg->topk))
+    return DCOCO_EUNSUPPORTED;
   if (cfg->slots < 3 || cfg->slots > 32) return DCOCO_EUNSUPPORTED;
   if (cfg->vocab < cfg->topk || cfg->vocab > (1 << 20)) return DCOCO_EINVAL;
   if (cfg->hidden <= 0 || cfg->hidden % 64 != 0) return DCOCO_EINVAL;
@@ -182,6 +185,9 @@ int validate_call(const dcoco_handle *h, const dcoco_weights *w, int batch, cons
 }
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? DCOCO_OK : DCOCO_ECUDA; }
+
+// Successors each beam keeps (0 in the config means all K).
+inline int beam_topm(const dcoco_config &cfg) { return cfg.beam_topm > 0 ? cfg.beam_topm : cfg.topk; }
 
 #define DC_TRY(expr)                       \
   do {                                     \
@@ -252,7 +258,7 @@ int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs 
     // and verify in its last block
     const dc::WalkArgs wk{ids, in->target_tokens, out->tokens, choice,
                           in->target_tokens ? out->accept_len : nullptr, margin, ws.req_count,
-                          cfg.path_rule};
+                          cfg.path_rule, cfg.beam_width, beam_topm(cfg)};
     DC_TRY(clk.done(dc::launch_pair_score_walk(K, ws.U, ws.V, ws.P, vals, w->mlp.w2, w->mlp.b2, N, B,
                                                scores, wk, st)));
     return DCOCO_OK;
@@ -262,7 +268,8 @@ int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs 
   // step 5: walk + verify
   DC_TRY(clk.done(dc::launch_walk_verify(K, scores, ids, in->target_tokens, N, B, out->tokens,
                                          choice, margin,
-                                         in->target_tokens ? out->accept_len : nullptr, cfg.path_rule, st)));
+                                         in->target_tokens ? out->accept_len : nullptr, cfg.path_rule,
+                                         cfg.beam_width, beam_topm(cfg), st)));
   return DCOCO_OK;
 }
 

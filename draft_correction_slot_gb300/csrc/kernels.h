@@ -117,7 +117,9 @@ struct WalkArgs {
   int32_t *tokens, *choice, *accept_len;
   float *margin;
   unsigned *req_count;
-  int path_rule;    // 0: prefix-first greedy walk, 1: highest-scoring path
+  int path_rule;    // 0: prefix-first greedy walk, 1: highest-scoring path, 2: beam walk
+  int beam_width;   // path rule 2: partial paths kept, 1..4
+  int beam_topm;    // path rule 2: successors per predecessor, 1..K
 };
 
 // S[n,p,a,b] = l_{p+1}(b) + b2 + sum_j w2_j GELU(P_pj + U_{p,a,j} + V_{p+1,b,j}),
@@ -136,10 +138,11 @@ cudaError_t launch_cos_score(int K, const float *O, const float *I, const float 
                              float sigma, int N, int B, float *scores, cudaStream_t st);
 
 // ---------------------------------------------------------------- walk + verify
-// path_rule 0: prefix-first greedy walk; 1: highest-scoring path (Viterbi).
+// path_rule 0: prefix-first greedy walk; 1: highest-scoring path (Viterbi);
+// 2: beam walk (beam_width 1..4, beam_topm 1..K).
 cudaError_t launch_walk_verify(int K, const float *scores, const int32_t *topk_ids,
                                const int32_t *target, int N, int B, int32_t *tokens,
                                int32_t *choice, float *margin, int32_t *accept_len,
-                               int path_rule, cudaStream_t st);
+                               int path_rule, int beam_width, int beam_topm, cudaStream_t st);
 
 }  // namespace dc

@@ -207,8 +207,8 @@ k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
 
   // ---------------------------------------------------------------- step 5
   // The last block of request n to finish its pair (counted in req_count,
-  // zero between calls) selects the request's path (greedy walk or highest-
-  // scoring path) and verifies it.
+  // zero between calls) selects the request's path (greedy walk, highest-
+  // scoring path or beam walk) and verifies it.
   __shared__ int s_last;
   __shared__ int s_choice[32];
   __threadfence();
@@ -224,12 +224,16 @@ k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
   const int32_t *tg = wk.target ? wk.target + slot0 : nullptr;
   int32_t *ch = wk.choice ? wk.choice + slot0 : nullptr, *al = wk.accept_len ? wk.accept_len + n : nullptr;
   float *mg = wk.margin ? wk.margin + (int64_t)n * (B - 1) : nullptr;
-  if (wk.path_rule == 1) {
+  if (wk.path_rule != 0) {
     // the request's scores go to shared memory past the walk's tables when they fit
     float *s_sc = sm + 2 * kWalkMaxRows;
     const bool fits = (2 * kWalkMaxRows + (size_t)(B - 1) * K * K) * sizeof(float) <= dynamic_smem_bytes();
-    viterbi_verify_request<K>(sc, wk.topk_ids + slot0 * K, tg, B, wk.tokens + slot0, ch, mg, al, s_best, s_gap,
-                              s_choice, fits ? s_sc : nullptr);
+    if (wk.path_rule == 1)
+      viterbi_verify_request<K>(sc, wk.topk_ids + slot0 * K, tg, B, wk.tokens + slot0, ch, mg, al, s_best, s_gap,
+                                s_choice, fits ? s_sc : nullptr);
+    else
+      beam_verify_request<K>(sc, wk.topk_ids + slot0 * K, tg, B, wk.tokens + slot0, ch, mg, al, wk.beam_width,
+                             wk.beam_topm, s_best, s_gap, s_choice, fits ? s_sc : nullptr);
   } else {
     walk_verify_request<K>(sc, wk.topk_ids + slot0 * K, tg, B, wk.tokens + slot0, ch, mg, al, s_best, s_gap,
                            s_choice);

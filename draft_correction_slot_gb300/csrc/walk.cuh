@@ -209,15 +209,146 @@ __device__ __forceinline__ void viterbi_verify_request(const float *scores, cons
     for (int off = 16; off > 0; off >>= 1) {
       const float ov = __shfl_down_sync(DC_FULL_MASK, v, off);
       const int oi = __shfl_down_sync(DC_FULL_MASK, idx, off);
-      if (ov > v || (ov == v && oi < idx)) {
-        v = ov;
-        idx = oi;
-      }
+      const bool take = (ov > v) | ((ov == v) & (oi < idx));
+      v = take ? ov : v;
+      idx = take ? oi : idx;
     }
     __syncwarp();
     if (lane == 0) {
       s_choice[P] = idx;
       for (int p = P - 1; p >= 0; --p) s_choice[p] = s_pred[p * K + s_choice[p + 1]];
+    }
+  }
+  __syncthreads();
+  emit_request<K>(ids, target, B, tokens, choice, margin, accept_len, s_gap, s_choice);
+}
+
+constexpr int kBeamMax = 4;  // widest beam the warp program keeps
+
+// Beam walk for one request.  The DCOCO page's reproduction assessment,
+// weaknesses (2)-(3): the greedy walk widened into a narrow beam (2-4) over the
+// same scores, each predecessor extended only to its top-m successors.  The
+// beam holds the W partial paths of highest cumulative score
+// sum_p S_p(k_p, k_{p+1}) (fp32, left to right), starting from candidate 0 of
+// the first slot; extensions are ordered by score, then parent rank, then
+// successor index; the answer is the best complete path, and margin[p] is the
+// chosen successor's score minus the best other successor score along it.
+// One warp runs it, lane b holding successor b of every beam; the scores are
+// staged in `s_sc` first when it is not null.  s_tab needs 2 * 30 * kBeamMax
+// ints (parents and successors per step), s_gap kWalkMaxRows floats.
+// W in [1, kBeamMax]; m in [1, K] (K: every successor).  Called by every
+// thread of the block, which must have 256 threads.
+// Beam walk for one request.  The DCOCO page's reproduction assessment,
+// weaknesses (2)-(3): the greedy walk widened into a narrow beam (2-4) over the
+// same scores, each predecessor extended only to its top-m successors.  The
+// beam holds the W partial paths of highest cumulative score
+// sum_p S_p(k_p, k_{p+1}) (fp32, left to right), starting from candidate 0 of
+// the first slot; extensions are ordered by score, then parent rank, then
+// successor index; the answer is the best complete path, and margin[p] is the
+// chosen successor's score minus the best other successor score along it.
+// Per step every thread e < W K takes one extension (beam e / K, successor
+// e % K) and counts the open extensions that precede it in that order: the
+// extension with count r < W becomes beam r.  The scores are staged in
+// `s_sc` first when it is not null.  s_tab needs 30 kBeamMax * 2 + 4 kBeamMax
+// + 2 W K ints (at most 560), s_gap kWalkMaxRows floats.  W in [1, kBeamMax];
+// m in [1, K] (K: every successor).  Called by every thread of the block,
+// which must have 256 threads.
+template <int K>
+__device__ __forceinline__ void beam_verify_request(const float *scores, const int32_t *ids, const int32_t *target,
+                                                    int B, int32_t *tokens, int32_t *choice, float *margin,
+                                                    int32_t *accept_len, int W, int m, int *s_tab, float *s_gap,
+                                                    int *s_choice, float *s_sc) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int P = B - 1, E = W * K;
+  int *s_par = s_tab, *s_cand = s_tab + 30 * kBeamMax;          // per step and rank
+  float *s_tot = reinterpret_cast<float *>(s_tab + 60 * kBeamMax);  // the beams: totals,
+  int *s_last = s_tab + 61 * kBeamMax;                             // last candidates,
+  float *s_ntot = reinterpret_cast<float *>(s_tab + 62 * kBeamMax);  // and the next ones
+  int *s_nlast = s_tab + 63 * kBeamMax;
+  float *s_ev = reinterpret_cast<float *>(s_tab + 64 * kBeamMax);  // [W K] extension totals
+  int *s_ok = s_tab + 64 * kBeamMax + kBeamMax * 32;               // [W K] open extensions
+  if (s_sc) {
+    const int n4 = P * K * K / 4;
+    for (int i = tid; i < n4; i += 256)
+      reinterpret_cast<float4 *>(s_sc)[i] = __ldcg(reinterpret_cast<const float4 *>(scores) + i);
+  }
+  if (tid == 0) {
+    s_tot[0] = 0.f;
+    s_last[0] = 0;
+  }
+  __syncthreads();
+  const float *sc = s_sc ? s_sc : scores;
+  const int w = tid / K, b = tid - w * K;
+  int nb = 1;
+#pragma unroll 1
+  for (int p = 0; p < P; ++p) {
+    bool ok = false;
+    float ev = 0.f;
+    if (tid < E && w < nb) {
+      const float *row = sc + (p * K + s_last[w]) * K;
+      const float sv = s_sc ? row[b] : __ldcg(row + b);
+      ev = s_tot[w] + sv;
+      ok = true;
+      if (m < K) {  // rank of b in its row: higher scores, then equal scores at lower indices
+        int rank = 0;
+#pragma unroll
+        for (int o = 0; o < K; ++o) {
+          const float ov = s_sc ? row[o] : __ldcg(row + o);
+          rank += (int)((ov > sv) | ((ov == sv) & (o < b)));
+        }
+        ok = rank < m;
+      }
+    }
+    if (tid < E) {
+      s_ev[tid] = ev;
+      s_ok[tid] = ok ? 1 : 0;
+    }
+    __syncthreads();
+    if (ok) {
+      int before = 0;  // open extensions ahead of this one (E is a multiple of 8)
+#pragma unroll 8
+      for (int e = 0; e < E; ++e)
+      {  // bitwise, not short-circuit: no per-lane branch
+        const float o = s_ev[e];
+        before += (int)((s_ok[e] != 0) & ((o > ev) | ((o == ev) & (e < tid))));
+      }
+      if (before < W) {
+        s_par[p * kBeamMax + before] = w;
+        s_cand[p * kBeamMax + before] = b;
+        s_ntot[before] = ev;
+        s_nlast[before] = b;
+      }
+    }
+    const int open = __syncthreads_count(ok);
+    nb = open < W ? open : W;
+    if (tid < nb) {
+      s_tot[tid] = s_ntot[tid];
+      s_last[tid] = s_nlast[tid];
+    }
+    __syncthreads();
+  }
+  if (tid == 0) {
+    int r = 0;
+    for (int q = P - 1; q >= 0; --q) {
+      s_choice[q + 1] = s_cand[q * kBeamMax + r];
+      r = s_par[q * kBeamMax + r];
+    }
+    s_choice[0] = 0;
+  }
+  __syncthreads();
+  if (tid < 32) {
+    // margins along the answer: the chosen successor against the best other
+    const int col = lane & (K - 1);
+#pragma unroll 1
+    for (int q = 0; q < P; ++q) {
+      const int a = s_choice[q], c = s_choice[q + 1];
+      const float *row = sc + (q * K + a) * K;
+      const float sv = s_sc ? row[col] : __ldcg(row + col);
+      float o = (lane < K && lane != c) ? sv : -INFINITY;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) o = fmaxf(o, __shfl_xor_sync(DC_FULL_MASK, o, off));
+      const float cv = __shfl_sync(DC_FULL_MASK, sv, c);
+      if (lane == 0) s_gap[q * K + c] = cv - o;
     }
   }
   __syncthreads();

@@ -31,7 +31,10 @@
  *        k_{p+1} = argmax_b S_p(k_p, b), ties to the lowest b
  *                                                [DCOCO] step (5); [LiLiCorr] Eq. (8)
  *      path_rule 1, highest-scoring path: the k maximizing sum_p S_p(k_p, k_{p+1})
- *        (dynamic program in fp64, ties to the lowest index) [LiLiCorr] App. E Eq. (12)
+ *        (dynamic program, fp32 totals, ties to the lowest index) [LiLiCorr] App. E Eq. (12)
+ *      path_rule 2, beam walk: the beam_width partial paths of highest
+ *        cumulative score, each extended to its beam_topm best successors;
+ *        the best complete path       [DCOCO] reproduction assessment (2)-(3)
  *   5. greedy verify: accept_len = length of the longest prefix of the chosen
  *      tokens equal to the target tokens                    [FD]
  *
@@ -87,7 +90,10 @@ typedef struct {
   float ln_eps;     /* LayerNorm epsilon (1e-5)                                */
   int host_staging; /* nonzero: also allocate device staging buffers so that
                        dcoco_correct_host can be used                        */
-  int path_rule;    /* 0 = prefix-first greedy walk, 1 = highest-scoring path */
+  int path_rule;    /* 0 = prefix-first greedy walk, 1 = highest-scoring path,
+                       2 = beam walk                                          */
+  int beam_width;   /* path_rule 2: partial paths kept, 1..4                  */
+  int beam_topm;    /* path_rule 2: successors per predecessor, 1..K (0 = K)  */
 } dcoco_config;
 
 /* Corrector weights, fp32, PyTorch Linear layout [out][in], row-major.
@@ -125,8 +131,10 @@ typedef struct {
                           target_tokens != NULL                             */
   int32_t *topk_ids;   /* [N][B][K] candidate token ids, best first         */
   float *topk_val;     /* [N][B][K] candidate logits (exact bf16 values)    */
-  float *margin;       /* [N][B-1] path_rule 0: best minus second-best
-                          successor score; path_rule 1: best minus
+  float *margin;       /* [N][B-1] path_rule 0 and 2: the chosen successor's
+                          score minus the best other successor score
+                          (for rule 0, best minus second best); path_rule 1:
+                          best minus
                           second-best predecessor total of the chosen
                           candidate at slot p+1 (+inf when only one
                           predecessor is possible)                         */

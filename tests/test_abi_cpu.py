@@ -48,7 +48,8 @@ def test_version_and_status_strings(dc):
 
 @pytest.mark.parametrize("kw,status", [
     (dict(topk=12), -2), (dict(topk=64), -2), (dict(rank=64), -2), (dict(mlp_hidden=512), -2),
-    (dict(variant=2), -2), (dict(slots=2), -2), (dict(slots=40), -2), (dict(path_rule=2), -2),
+    (dict(variant=2), -2), (dict(slots=2), -2), (dict(slots=40), -2), (dict(path_rule=3), -2), (dict(path_rule=2, beam_width=0), -2),
+    (dict(path_rule=2, beam_width=5), -2), (dict(path_rule=2, beam_topm=17), -2),
     (dict(hidden=4000), -1), (dict(hidden=0), -1), (dict(vocab=8), -1),
     (dict(max_batch=0), -1), (dict(ln_eps=0.0), -1), (dict(vocab=1 << 21), -1),
 ])

@@ -272,3 +272,32 @@ def test_viterbi_and_greedy_agree_on_top_k_and_scores(torch_cuda):
     ga, gb = run_gpu(a), run_gpu(b)
     for k in ("topk_ids", "topk_val", "scores"):
         np.testing.assert_array_equal(ga[k], gb[k])
+
+
+# ------------------------------------------------------------------ beam walk
+@pytest.mark.parametrize("width,topm", [(1, 0), (2, 0), (4, 0), (3, 4)])
+def test_beam_batch(torch_cuda, width, topm):
+    """Path rule 2 (the DCOCO page's reproduction assessment (2)-(3)):
+    decisions equal the oracle's in the kernel's precision on the GPU's scores."""
+    prob = Problem(30 + width, N=4, V=20011, d=512, perturb=True, path_rule=2, beam_width=width, beam_topm=topm)
+    report(f"beam W={width} m={topm}", compare_path(prob, run_gpu(prob), prob.oracle()))
+
+
+def test_beam_width_one_equals_greedy(torch_cuda):
+    a = Problem(35, N=3, V=20011, d=512, perturb=True, path_rule=0)
+    b = Problem(35, N=3, V=20011, d=512, perturb=True, path_rule=2, beam_width=1)
+    ga, gb = run_gpu(a), run_gpu(b)
+    for k in ("choice", "tokens", "accept_len", "margin"):
+        np.testing.assert_array_equal(ga[k], gb[k])
+
+
+@pytest.mark.parametrize("K", [8, 32])
+def test_beam_other_candidate_counts(torch_cuda, K):
+    prob = Problem(36 + K, N=2, V=20011, d=512, K=K, planted=8, boost=(8.0, 16.0), path_rule=2, beam_width=4,
+                   beam_topm=K // 2)
+    report(f"beam K={K}", compare_path(prob, run_gpu(prob), prob.oracle()))
+
+
+def test_beam_cosine_variant(torch_cuda):
+    prob = Problem(37, N=3, V=20011, d=512, variant=1, path_rule=2, beam_width=3)
+    report("beam cosine", compare_path(prob, run_gpu(prob), prob.oracle()))
