@@ -79,6 +79,8 @@ def lib():
             L.orc_viterbi.argtypes = [_PD, C.c_int, C.c_int, _PI, _PD]
             L.orc_viterbi_f32.argtypes = [_PF, C.c_int, C.c_int, _PI, _PF]
             L.orc_beam.argtypes = [_PD, C.c_int, C.c_int, C.c_int, C.c_int, _PI, _PD]
+            L.orc_verify_stochastic.argtypes = [_PU, C.c_int64, C.c_int, C.c_int, _PI, _PF, C.c_float, _PI, _PI,
+                                                _PD]
             L.orc_beam_f32.argtypes = [_PF, C.c_int, C.c_int, C.c_int, C.c_int, _PI, _PF]
             L.orc_verify.argtypes = [_PI, _PI, C.c_int]
             L.orc_verify.restype = C.c_int
@@ -244,6 +246,22 @@ def select_path(scores: np.ndarray, path_rule: int = 0, width: int = 2, topm: in
     if path_rule == 2:
         return beam(scores, width, topm)
     return walk(scores)
+
+
+def verify_stochastic(target_logits, tokens, u_acc, u_draw: float, V: int | None = None):
+    """target_logits [B+1, stride] u16 (bf16 bits; the first V columns are the
+    vocabulary), tokens [B], u_acc [B] -> (accept_len, next_token, q_acc [B])."""
+    tl = _u16(target_logits)
+    tk = np.ascontiguousarray(tokens, dtype=np.int32)
+    ua = np.ascontiguousarray(u_acc, dtype=np.float32)
+    B = tk.shape[0]
+    al = np.zeros(1, np.int32)
+    nt = np.zeros(1, np.int32)
+    q = np.empty(B, np.float64)
+    lib().orc_verify_stochastic(_p(tl, C.c_uint16), tl.shape[-1], V or tl.shape[-1], B, _p(tk, C.c_int32),
+                                _p(ua, C.c_float), float(u_draw), _p(al, C.c_int32), _p(nt, C.c_int32),
+                                _p(q, C.c_double))
+    return int(al[0]), int(nt[0]), q
 
 
 def verify(tokens, target) -> int:

@@ -455,6 +455,80 @@ int orc_verify(const int32_t *tokens, const int32_t *target, int B) {
   return m;
 }
 
+/* ---------------------------------------------------------------------------
+ * Stochastic verification of a point-mass proposal (temperature 1).
+ * [DCOCO] page, "Core method": a drafter that emits one token deterministically
+ * proposes the point mass p_j(v) = 1[v = y_j]; standard speculative sampling
+ * then accepts y_j with probability min(1, q_j(y_j) / p_j(y_j)) = q_j(y_j) and,
+ * on rejection, resamples from r_j(v) = q_j(v) 1[v != y_j] / (1 - q_j(y_j)).
+ * [FD] "Modified rejection sampling preserves the target distribution": the
+ * rule runs left to right, stops at the first rejection with the corrected
+ * token, and after B acceptances draws one bonus token from the target at the
+ * next position.
+ *
+ * target: [B+1][stride] bf16 target logits (rows 0..B-1 at the draft slots,
+ * row B at the bonus position); q_j = softmax of row j.  tokens [B] are the
+ * proposal y.  u_acc [B] and u_draw are uniforms in [0, 1) supplied by the
+ * caller: slot j is accepted iff u_acc[j] < q_j(y_j).  A draw from weights w
+ * over the vocabulary is the smallest v with w(0) + ... + w(v) > u_draw W,
+ * W = sum of w (inverse transform in vocabulary order).  Outputs: accept_len
+ * (accepted draft tokens, 0..B), next_token (the corrected or bonus token),
+ * q_acc [B] (q_j(y_j); may be NULL).  Sums in double.
+ * ------------------------------------------------------------------------- */
+static double orc_row_lse(const uint16_t *row, int V) {
+  double m = -INFINITY, s = 0.0;
+  for (int v = 0; v < V; ++v) {
+    const double x = orc_bf16_to_double(row[v]);
+    if (x > m) m = x;
+  }
+  if (m == -INFINITY) return -INFINITY;
+  for (int v = 0; v < V; ++v) s += exp(orc_bf16_to_double(row[v]) - m);
+  return m + log(s);
+}
+
+static int orc_draw(const uint16_t *row, int V, double lse, int exclude, double u) {
+  double total = 0.0;
+  for (int v = 0; v < V; ++v)
+    if (v != exclude) total += exp(orc_bf16_to_double(row[v]) - lse);
+  const double t = u * total;
+  double c = 0.0;
+  int last = -1;
+  for (int v = 0; v < V; ++v) {
+    if (v == exclude) continue;
+    const double w = exp(orc_bf16_to_double(row[v]) - lse);
+    if (w > 0.0) last = v;
+    c += w;
+    if (c > t && w > 0.0) return v;
+  }
+  return last; /* rounding at the very end of the cumulative sum */
+}
+
+void orc_verify_stochastic(const uint16_t *target, int64_t stride, int V, int B, const int32_t *tokens,
+                           const float *u_acc, float u_draw, int32_t *accept_len, int32_t *next_token,
+                           double *q_acc) {
+  int j = 0;
+  double lse_j = 0.0;
+  for (; j < B; ++j) {
+    const uint16_t *row = target + (size_t)j * stride;
+    lse_j = orc_row_lse(row, V);
+    const double q = exp(orc_bf16_to_double(row[tokens[j]]) - lse_j);
+    if (q_acc) q_acc[j] = q;
+    if (!((double)u_acc[j] < q)) break;
+  }
+  if (q_acc)
+    for (int i = j + 1; i < B; ++i) {
+      const uint16_t *row = target + (size_t)i * stride;
+      q_acc[i] = exp(orc_bf16_to_double(row[tokens[i]]) - orc_row_lse(row, V));
+    }
+  *accept_len = j;
+  if (j < B)
+    *next_token = orc_draw(target + (size_t)j * stride, V, lse_j, tokens[j], (double)u_draw);
+  else {
+    const uint16_t *row = target + (size_t)B * stride;
+    *next_token = orc_draw(row, V, orc_row_lse(row, V), -1, (double)u_draw);
+  }
+}
+
 /* [FD] "Verification can be parallel ..." section:
  * s_k = P(A_1 and ... and A_k), E[Y] = 1 + sum_{k=1}^{gamma} s_k. */
 double orc_expected_yield(const double *cond, int n, double *survival) {

@@ -14,7 +14,8 @@
  *              matching), Sec. 3.5 Eq. (8) (greedy walk), App. E Eq. (12)
  *              (highest-scoring path, Viterbi).
  *   The [DCOCO] page's reproduction assessment, weaknesses (2)-(3): the beam
- *              walk with top-m successors.
+ *              walk with top-m successors; its "Core method": stochastic
+ *              verification of a point-mass proposal.
  *   [FD]       "Faster Decoding" (textbook chapter): the expected-yield
  *              identity E[Y] = 1 + sum_k s_k and the greedy-verification
  *              contract.
@@ -127,6 +128,16 @@ void orc_beam_f32(const float *scores, int B, int K, int W, int m, int32_t *choi
 
 /* Greedy verify: number of leading slots whose token equals the target. */
 int orc_verify(const int32_t *tokens, const int32_t *target, int B);
+
+/* Stochastic verification of the point-mass proposal `tokens` [B] against
+ * target logits [B+1][stride] (temperature 1): slot j accepted iff
+ * u_acc[j] < q_j(tokens[j]); at the first rejection j, next_token is drawn
+ * from q_j without tokens[j]; after B acceptances from q_B (the bonus
+ * position).  A draw takes the smallest v whose cumulative weight (vocabulary
+ * order) exceeds u_draw times the total.  q_acc [B] may be NULL. */
+void orc_verify_stochastic(const uint16_t *target, int64_t stride, int V, int B, const int32_t *tokens,
+                           const float *u_acc, float u_draw, int32_t *accept_len, int32_t *next_token,
+                           double *q_acc);
 
 /* E[Y] = 1 + sum_k prod_{j<=k} cond[j]; survival[k] receives the products. */
 double orc_expected_yield(const double *cond, int n, double *survival);

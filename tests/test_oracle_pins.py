@@ -484,6 +484,80 @@ def test_zero_output_layer_beam_reproduces_draft_argmax():
     np.testing.assert_array_equal(out["choice"], 0)
 
 
+# --------------------------------------------------------------- stochastic verification
+def _bf16_rows(x):
+    """fp32 array -> bf16 bit patterns (round to nearest even) as uint16."""
+    return synth.bf16_bits(np.asarray(x, np.float32))
+
+
+def test_stochastic_accept_probability_is_the_target_softmax():
+    """q_j(y_j) is the softmax of the target row (scipy) at the proposed token."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(50)
+    V, B = 300, 4
+    tl = _bf16_rows(rng.standard_normal((B + 1, V)) * 2)
+    toks = rng.integers(0, V, B).astype(np.int32)
+    _, _, q = oracle.verify_stochastic(tl, toks, np.full(B, 0.999999, np.float32), 0.5)
+    rows = synth.bf16_to_f32(tl).astype(np.float64)
+    for j in range(B):
+        np.testing.assert_allclose(q[j], softmax(rows[j])[toks[j]], rtol=1e-12)
+
+
+def test_stochastic_forced_cases():
+    V = 8
+    rows = np.zeros((3, V), np.float32)
+    rows[0, 3] = 80.0          # q_1(3) = 1 (to fp64 precision of exp(-80))
+    rows[1, 5] = -np.inf       # q_2(5) = 0: always rejected, never redrawn
+    rows[2, :] = -np.inf
+    rows[2, 6] = 0.0           # the bonus row is a point mass at 6
+    tl = _bf16_rows(rows)
+    toks = np.array([3, 5], np.int32)
+    for u in (0.0, 0.5, 0.9999):
+        al, nt, q = oracle.verify_stochastic(tl, toks, np.array([u, u], np.float32), u)
+        assert al == 1 and nt != 5 and q[1] == 0.0
+    # u_draw = 0 takes the first positive-weight token, u_draw -> 1 the last
+    assert oracle.verify_stochastic(tl, toks, np.array([0.1, 0.1], np.float32), 0.0)[1] == 0
+    assert oracle.verify_stochastic(tl, toks, np.array([0.1, 0.1], np.float32), 0.999999)[1] == 7
+    toks2 = np.array([3, 2], np.int32)
+    rows2 = rows.copy()
+    rows2[1, :] = -np.inf
+    rows2[1, 2] = 0.0          # q_2(2) = 1
+    al, nt, _ = oracle.verify_stochastic(_bf16_rows(rows2), toks2, np.array([0.3, 0.7], np.float32), 0.4)
+    assert (al, nt) == (2, 6)  # full acceptance: the bonus point mass
+
+
+@pytest.mark.parametrize("case", ["concentrated", "partial", "excluded"])
+def test_stochastic_output_frequencies_equal_the_target(case):
+    """Faster Decoding, "Correctness and failure tests": on a tiny vocabulary
+    the emitted token of the first position (the accepted draft token, or the
+    correction drawn at a rejection) has the target distribution q_1, and
+    P(accept_len = 2) = q_1(y_1) q_2(y_2).  Monte Carlo over supplied
+    uniforms, tolerance 5 standard errors."""
+    rng = np.random.default_rng({"concentrated": 60, "partial": 61, "excluded": 62}[case])
+    V, B, n = 6, 2, 60000
+    rows = rng.standard_normal((B + 1, V)).astype(np.float32)
+    if case == "concentrated":
+        rows[0, 2] += 3.0
+    elif case == "excluded":
+        rows[0, 2] = -np.inf   # the draft token has no target mass at all
+    tl = _bf16_rows(rows)
+    toks = np.array([2, 4], np.int32)
+    w = np.exp(synth.bf16_to_f32(tl).astype(np.float64))
+    q = w / w.sum(axis=1, keepdims=True)
+    u = rng.random((n, B + 1)).astype(np.float32)
+    first = np.empty(n, np.int64)
+    full = 0
+    for i in range(n):
+        al, nt, _ = oracle.verify_stochastic(tl, toks, u[i, :B], u[i, B])
+        first[i] = toks[0] if al >= 1 else nt
+        full += al == 2
+    freq = np.bincount(first, minlength=V) / n
+    se = np.sqrt(q[0] * (1 - q[0]) / n)
+    assert np.all(np.abs(freq - q[0]) <= 5 * se + 1e-12), (freq, q[0])
+    pf = q[0, 2] * q[1, 4]
+    assert abs(full / n - pf) <= 5 * np.sqrt(pf * (1 - pf) / n) + 1e-12
+
+
 # --------------------------------------------------------------- cosine variant
 def test_cosine_vectors_and_transition():
     rng = np.random.default_rng(12)
