@@ -55,6 +55,8 @@ def parse():
                     help="step 5: prefix-first greedy walk (default), highest-scoring path or beam walk")
     ap.add_argument("--beam-width", type=int, default=4, help="beam walk: partial paths kept (1..4)")
     ap.add_argument("--beam-topm", type=int, default=0, help="beam walk: successors per predecessor (0 = K)")
+    ap.add_argument("--stochastic-verify", action="store_true",
+                    help="also time dcoco_verify_stochastic on [N, B+1, V] target logits (reported apart)")
     ap.add_argument("--only", choices=["topk"], default=None,
                     help="time one kernel stage alone through its own entry point (for profiling)")
     return ap.parse_args()
@@ -348,6 +350,41 @@ def run_ours(args):
     step_s = total_ms / args.steps / 1e3
     value = world * N / step_s
 
+    # stochastic verification (an entry of its own, reported apart from the headline)
+    stoch = None
+    if args.stochastic_verify:
+        tgen = torch.Generator(device=device)
+        tgen.manual_seed(4242 + rank)
+        tset = []
+        for s_ in range(args.sets):
+            x = torch.randn(N * (B + 1), V, generator=tgen, device=device) * 2.0
+            hot = torch.randint(0, V, (N * (B + 1), 2), generator=tgen, device=device)
+            x.scatter_add_(1, hot, torch.rand(N * (B + 1), 2, generator=tgen, device=device) * 4.0 + 14.0)
+            tl = x.to(torch.bfloat16).view(N, B + 1, V)
+            del x
+            toks = tl[:, :B].float().argmax(-1).to(torch.int32)  # input recipe only: a plausible proposal
+            tset.append((tl, toks, torch.rand(N, B, generator=tgen, device=device),
+                         torch.rand(N, generator=tgen, device=device)))
+        vouts = [corr.verify_stochastic(*tset[i]) for i in range(args.sets)]  # warm-up and outputs
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = max(10, args.steps)
+        e0.record()
+        for i in range(reps):
+            tl, toks, ua, ud = tset[i % args.sets]
+            dc.dcoco_verify_stochastic(corr.handle, N, tl, toks, ua, ud, vouts[i % args.sets]["accept_len"],
+                                       vouts[i % args.sets]["next_token"], vouts[i % args.sets]["q_accept"])
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) / reps * 1e3
+        vb = N * (B + 1) * V * 2
+        stoch = {"us_per_call": us, "blocks_per_s": N / (us * 1e-6), "target_logits_bytes": vb,
+                 "achieved_gbs": vb / (us * 1e-6) / 1e9, "frac_of_hbm_peak": vb / (us * 1e-6) / 1e9 / pk["hbm_gbs"],
+                 "mean_accept_len": float(torch.cat([o["accept_len"] for o in vouts]).float().mean()),
+                 "inputs": f"{args.sets} sets of [N, B+1, V] bf16 target logits, 2 boosted tokens per row "
+                           "(U(14,18) over 2 N(0,1)), proposal = per-slot target argmax, uniforms from torch"}
+        del tset, vouts
+
     # e2e: host buffers through the C ABI (copies inside the timed region)
     e2e = None
     if args.e2e_steps > 0:
@@ -406,6 +443,7 @@ def run_ours(args):
                                   "note": f"logits + gathered embedding rows over {pk['source']} HBM peak"},
             "roofline": roofline, "stages": stages, "cpu_baseline": cpu, "e2e": e2e,
             "clocks": clocks, "gpu_launches": launches,
+            **({"stochastic_verify": stoch} if stoch is not None else {}),
             "execution": ("CUDA graph replay of dcoco_correct, one graph per input set" if graphs is not None
                           else "one dcoco_correct call per step"),
             "eager": {"ms_per_step": eager_ms / args.steps, "value": world * N / (eager_ms / args.steps / 1e3),

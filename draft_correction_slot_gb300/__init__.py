@@ -62,7 +62,8 @@ class dcoco_outputs(C.Structure):
 EXPORTED = ("dcoco_version", "dcoco_status_string", "dcoco_create", "dcoco_weights_create",
             "dcoco_correct", "dcoco_correct_host", "dcoco_topk", "dcoco_get_device_status",
             "dcoco_weights_destroy", "dcoco_destroy", "dcoco_kernel_launches",
-            "dcoco_stage_timing", "dcoco_stage_read", "dcoco_stage_name", "dcoco_topk_noalloc")
+            "dcoco_stage_timing", "dcoco_stage_read", "dcoco_stage_name", "dcoco_topk_noalloc",
+            "dcoco_verify_stochastic")
 
 
 def _load():
@@ -79,6 +80,8 @@ def _load():
     for f in (L.dcoco_correct, L.dcoco_correct_host):
         f.argtypes = [C.c_void_p, C.c_void_p, C.c_int, C.POINTER(dcoco_inputs),
                       C.POINTER(dcoco_outputs), C.c_void_p]
+    L.dcoco_verify_stochastic.argtypes = [C.c_void_p, C.c_int, C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p,
+                                          C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p]
     L.dcoco_topk.argtypes = [C.c_void_p, C.c_int, C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p,
                              C.c_void_p]
     L.dcoco_topk_noalloc.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_int64,
@@ -210,6 +213,17 @@ def dcoco_topk(handle, batch: int, logits, topk_ids, topk_val, logits_slot_strid
                            _stream(stream)), "dcoco_topk")
 
 
+def dcoco_verify_stochastic(handle, batch: int, target_logits, tokens, u_accept, u_draw, accept_len,
+                            next_token, q_accept=None, target_stride: int | None = None, stream=None) -> None:
+    """Stochastic verification (temperature 1) of the proposal `tokens` against
+    target_logits [batch, B+1, stride] (bf16), with caller-drawn uniforms."""
+    stride = target_stride if target_stride is not None else target_logits.shape[-1]
+    _check(_lib.dcoco_verify_stochastic(handle, batch, _ptr(target_logits), int(stride), _ptr(tokens),
+                                        _ptr(u_accept), _ptr(u_draw), _ptr(accept_len), _ptr(next_token),
+                                        _ptr(q_accept) if q_accept is not None else None, _stream(stream)),
+           "dcoco_verify_stochastic")
+
+
 def dcoco_topk_noalloc(batch: int, slots: int, vocab: int, topk: int, logits, topk_ids, topk_val,
                        logits_slot_stride: int | None = None, stream=None) -> None:
     """Step 1 without a handle and without any device allocation (for callers
@@ -305,6 +319,17 @@ class Corrector:
         dcoco_correct(self.handle, self.weights, N, logits, hidden, cand_embed, target_tokens,
                       accept_len=out.get("accept_len") if target_tokens is not None else None,
                       logits_slot_stride=logits_slot_stride, stream=stream, **kw)
+        return out
+
+    def verify_stochastic(self, target_logits, tokens, u_accept, u_draw, target_stride=None, stream=None):
+        """-> dict(accept_len [N], next_token [N], q_accept [N, B]) on the tokens' device."""
+        N = tokens.shape[0]
+        dev = tokens.device
+        out = {"accept_len": torch.empty(N, dtype=torch.int32, device=dev),
+               "next_token": torch.empty(N, dtype=torch.int32, device=dev),
+               "q_accept": torch.empty(N, self.B, dtype=torch.float32, device=dev)}
+        dcoco_verify_stochastic(self.handle, N, target_logits, tokens, u_accept, u_draw, out["accept_len"],
+                                out["next_token"], out["q_accept"], target_stride, stream)
         return out
 
     def status(self) -> int:

@@ -30,6 +30,9 @@ struct Workspace {
   float *margin = nullptr;     // [N*(B-1)]
   int *err = nullptr;          // device status word
   unsigned *req_count = nullptr;  // finished pairs per request (zero between calls)
+  // stochastic verify: per target row chunk statistics, log-sum-exp, q_j(y_j), counters
+  float *v_chunk_m = nullptr, *v_chunk_s = nullptr, *v_lse = nullptr, *v_q = nullptr;
+  unsigned *v_count = nullptr;
   // host staging (dcoco_correct_host)
   uint16_t *st_logits = nullptr;  // [N][slots][st_stride]
   int64_t st_stride = 0;
@@ -138,6 +141,12 @@ void carve_workspace(Carver &c, const dcoco_config &cfg, int B, int topk_segment
   ws.margin = c.take<float>(N * (B - 1));
   ws.err = c.take<int>(1);
   ws.req_count = c.take<unsigned>(N);
+  const size_t vrows = N * (size_t)cfg.slots, vch = (size_t)dc::verify_chunks(cfg.vocab);
+  ws.v_chunk_m = c.take<float>(vrows * vch);
+  ws.v_chunk_s = c.take<float>(vrows * vch);
+  ws.v_lse = c.take<float>(vrows);
+  ws.v_q = c.take<float>(rows);
+  ws.v_count = c.take<unsigned>(N);
   if (cfg.host_staging) {
     ws.st_stride = ((int64_t)cfg.vocab + 7) & ~int64_t(7);
     ws.st_logits = c.take<uint16_t>(N * cfg.slots * (size_t)ws.st_stride);
@@ -617,6 +626,24 @@ int dcoco_topk(dcoco_handle *h, int batch, const void *logits, int64_t stride, i
   return cuda_status(dc::launch_topk(h->cfg.topk, static_cast<const uint16_t *>(logits), stride,
                                      h->cfg.slots, batch, h->cfg.vocab, plan, h->ws.part,
                                      h->ws.row_count, topk_ids, topk_val, st, true));
+}
+
+int dcoco_verify_stochastic(dcoco_handle *h, int batch, const void *target_logits, int64_t target_stride,
+                            const int32_t *tokens, const float *u_accept, const float *u_draw, int32_t *accept_len,
+                            int32_t *next_token, float *q_accept, void *stream) {
+  if (!h) return DCOCO_EINVAL;
+  if (batch < 0 || batch > h->cfg.max_batch) return DCOCO_EBATCH;
+  if (batch == 0) return DCOCO_OK;
+  if (!target_logits || !tokens || !u_accept || !u_draw || !accept_len || !next_token) return DCOCO_EINVAL;
+  if (target_stride < h->cfg.vocab || target_stride % 8 != 0 || !aligned16(target_logits)) return DCOCO_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  h->last_stream = st;
+  ++h->launches;
+  const Workspace &ws = h->ws;
+  return cuda_status(dc::launch_verify_stochastic(
+      static_cast<const uint16_t *>(target_logits), target_stride, h->cfg.vocab, batch, h->B, tokens, u_accept,
+      u_draw, ws.v_chunk_m, ws.v_chunk_s, ws.v_lse, q_accept ? q_accept : ws.v_q, ws.v_count, accept_len,
+      next_token, st));
 }
 
 int dcoco_get_device_status(dcoco_handle *h) {

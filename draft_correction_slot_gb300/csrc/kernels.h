@@ -137,6 +137,22 @@ cudaError_t launch_cos_post(int K, const float *cand_io, const float *slot_io, i
 cudaError_t launch_cos_score(int K, const float *O, const float *I, const float *topk_val,
                              float sigma, int N, int B, float *scores, cudaStream_t st);
 
+// ---------------------------------------------------------------- stochastic verify
+// Point-mass proposal `tokens` [N][B] against target logits [N][B+1][stride]
+// (bf16; row B of a request is the bonus position), temperature 1: slot j is
+// accepted iff u_acc[n][j] < q_j(y_j); at the first rejection the corrected
+// token is drawn from q_j without y_j, after B acceptances from row B; a draw
+// takes the smallest token whose cumulative weight (vocabulary order)
+// exceeds u_draw[n] times the total.  Scratch: chunk_m / chunk_s
+// [N*(B+1)][verify_chunks(V)], row_lse [N*(B+1)], req_count [N] (zero
+// between calls).  q_acc [N][B] receives q_j(y_j).
+int verify_chunks(int V);
+cudaError_t launch_verify_stochastic(const uint16_t *target, int64_t stride, int V, int N, int B,
+                                     const int32_t *tokens, const float *u_acc, const float *u_draw,
+                                     float *chunk_m, float *chunk_s, float *row_lse, float *q_acc,
+                                     unsigned *req_count, int32_t *accept_len, int32_t *next_token,
+                                     cudaStream_t st);
+
 // ---------------------------------------------------------------- walk + verify
 // path_rule 0: prefix-first greedy walk; 1: highest-scoring path (Viterbi);
 // 2: beam walk (beam_width 1..4, beam_topm 1..K).

@@ -177,6 +177,33 @@ int dcoco_correct(dcoco_handle *h, const dcoco_weights *w, int batch,
 int dcoco_correct_host(dcoco_handle *h, const dcoco_weights *w, int batch,
                        const dcoco_inputs *in, const dcoco_outputs *out, void *stream);
 
+/* Stochastic verification (temperature 1) of a point-mass proposal, the
+ * alternative to the greedy verify of step 5 for sampling targets.
+ *   [DCOCO] Core method: the proposal y_j is accepted with probability
+ *   q_j(y_j); on rejection the corrected token is resampled from
+ *   q_j(v) 1[v != y_j] / (1 - q_j(y_j)).  [FD] Modified rejection sampling:
+ *   left to right, stop at the first rejection; after all B acceptances one
+ *   bonus token from the target at the next position.
+ * target_logits: bf16 [batch][B+1][target_stride] (B = slots - 1), the
+ *   target's logits at draft slots 1..B (rows 0..B-1) and at the bonus
+ *   position (row B); q_j is the softmax of row j.  target_stride >= vocab,
+ *   multiple of 8; 16-byte aligned base.
+ * tokens: int32 [batch][B], the proposal (e.g. dcoco_correct's tokens).
+ * u_accept: fp32 [batch][B], u_draw: fp32 [batch]: uniforms in [0, 1) that
+ *   the caller draws; slot j is accepted iff u_accept[n][j] < q_j(y_j), and a
+ *   draw takes the smallest token whose cumulative weight in vocabulary order
+ *   exceeds u_draw[n] times the total weight.
+ * Outputs (device): accept_len int32 [batch] (accepted draft tokens, 0..B),
+ *   next_token int32 [batch] (the corrected token, or the bonus token),
+ *   q_accept fp32 [batch][B] (q_j(y_j); NULL = not wanted).
+ * fp32 arithmetic: decisions within ~1e-6 of a threshold may differ from an
+ * exact computation.  One launch; uses the handle's workspace, never
+ * allocates.  Errors: EINVAL (null pointer, bad stride or alignment), EBATCH,
+ * ECUDA. */
+int dcoco_verify_stochastic(dcoco_handle *h, int batch, const void *target_logits, int64_t target_stride,
+                            const int32_t *tokens, const float *u_accept, const float *u_draw, int32_t *accept_len,
+                            int32_t *next_token, float *q_accept, void *stream);
+
 /* Step 1 alone: top-K ids and values of every draft slot, written to
  * topk_ids / topk_val ([N][B][K], device).  Uses the handle's workspace,
  * never allocates.  Errors as dcoco_correct. */

@@ -301,3 +301,98 @@ def test_beam_other_candidate_counts(torch_cuda, K):
 def test_beam_cosine_variant(torch_cuda):
     prob = Problem(37, N=3, V=20011, d=512, variant=1, path_rule=2, beam_width=3)
     report("beam cosine", compare_path(prob, run_gpu(prob), prob.oracle()))
+
+
+# ------------------------------------------------------------------ stochastic verification
+def _stochastic_problem(seed, N, V, B=15, stride=None, u_scale=1.0):
+    """Target logits [N, B+1, stride] bf16 with a peaked target; the proposal
+    takes each slot's target argmax with probability 0.7, else a random token."""
+    rng = np.random.default_rng(seed)
+    stride = stride or ((V + 7) // 8) * 8
+    tl = synth.make_logits(rng, N, B + 1, V, 2, (14.0, 18.0), stride=stride)  # q(top) ~ 0.3-0.9
+    f = synth.bf16_to_f32(tl[:, :, :V])
+    top = f.argmax(axis=2)[:, :B]
+    toks = np.where(rng.random((N, B)) < 0.7, top, rng.integers(0, V, (N, B))).astype(np.int32)
+    u_acc = (rng.random((N, B)) * u_scale).astype(np.float32)
+    u_draw = rng.random(N).astype(np.float32)
+    return tl, toks, u_acc, u_draw, V
+
+
+def _check_stochastic(tl, toks, u_acc, u_draw, V, g, tol=1e-5):
+    N, B = toks.shape
+    near = 0
+    for n in range(N):
+        al, nt, q = oracle.verify_stochastic(tl[n], toks[n], u_acc[n], float(u_draw[n]), V=V)
+        np.testing.assert_allclose(g["q_accept"][n], q, rtol=2e-5, atol=1e-7, err_msg=f"request {n} q")
+        ga, gt = int(g["accept_len"][n]), int(g["next_token"][n])
+        if ga != al:
+            j = min(ga, al)  # the slot where the decisions split must be a near tie
+            assert abs(float(u_acc[n, j]) - q[j]) < tol, f"request {n}: accept_len {ga} vs {al}"
+            near += 1
+            continue
+        if gt != nt:
+            # the draw split at a near tie: the two tokens are neighbours in the
+            # cumulative weight and the threshold sits within tol of their boundary
+            row = synth.bf16_to_f32(tl[n, ga if ga < B else B, :V]).astype(np.float64)
+            w = np.exp(row - row.max())
+            if ga < B:
+                w[toks[n, ga]] = 0.0
+            c = np.cumsum(w) / w.sum()
+            lo, hi = min(gt, nt), max(gt, nt)
+            assert np.all(w[lo + 1:hi] == 0.0), f"request {n}: draws {gt} vs {nt} not adjacent"
+            assert abs(c[lo] - float(u_draw[n])) < tol, f"request {n}: draw {gt} vs {nt}"
+            near += 1
+    return near
+
+
+def _gpu_stochastic(tl, toks, u_acc, u_draw, V, B=15):
+    import torch
+    import draft_correction_slot_gb300 as dc
+    w = synth.make_weights(np.random.default_rng(1), 64)
+    corr = dc.Corrector({k: torch.from_numpy(v) for k, v in w.items()}, V, 64, B + 1, 16, max_batch=tl.shape[0])
+    try:
+        g = corr.verify_stochastic(bf16_tensor(tl), torch.from_numpy(toks).cuda(), torch.from_numpy(u_acc).cuda(),
+                                   torch.from_numpy(u_draw).cuda(), target_stride=tl.shape[-1])
+        torch.cuda.synchronize()
+        assert corr.status() == dc.DCOCO_OK
+        return {k: v.cpu().numpy() for k, v in g.items()}
+    finally:
+        corr.close()
+
+
+def test_stochastic_verify_qwen_shapes(torch_cuda):
+    """DCOCO Core method / Faster Decoding: point-mass proposal, temperature 1."""
+    tl, toks, ua, ud, V = _stochastic_problem(70, N=8, V=V_QWEN)
+    g = _gpu_stochastic(tl, toks, ua, ud, V)
+    print(f"[parity] stochastic verify: accept_len {g['accept_len'].tolist()} near ties "
+          f"{_check_stochastic(tl, toks, ua, ud, V, g)}")
+
+
+def test_stochastic_verify_ragged_and_forced(torch_cuda):
+    # ragged vocabulary with a padded stride
+    tl, toks, ua, ud, V = _stochastic_problem(71, N=6, V=4099, stride=4112)
+    _check_stochastic(tl, toks, ua, ud, V, _gpu_stochastic(tl, toks, ua, ud, V))
+    # u_accept = 0: every proposal with target mass is accepted -> bonus draws
+    tl, toks, ua, ud, V = _stochastic_problem(72, N=3, V=4099, u_scale=0.0)
+    f = synth.bf16_to_f32(tl[:, :, :V])
+    toks = f.argmax(axis=2)[:, :15].astype(np.int32)
+    g = _gpu_stochastic(tl, toks, ua, ud, V)
+    np.testing.assert_array_equal(g["accept_len"], 15)
+    _check_stochastic(tl, toks, ua, ud, V, g)
+    # u_accept -> 1 with proposals of tiny mass: rejected at slot 1 and redrawn
+    tl, toks, ua, ud, V = _stochastic_problem(73, N=3, V=4099)
+    f = synth.bf16_to_f32(tl[:, :, :V])
+    toks = f.argmin(axis=2)[:, :15].astype(np.int32)
+    ua = np.full_like(ua, 0.999999)
+    g = _gpu_stochastic(tl, toks, ua, ud, V)
+    np.testing.assert_array_equal(g["accept_len"], 0)
+    assert np.all(g["next_token"] != toks[:, 0])
+    _check_stochastic(tl, toks, ua, ud, V, g)
+
+
+def test_stochastic_verify_deterministic(torch_cuda):
+    tl, toks, ua, ud, V = _stochastic_problem(74, N=5, V=20011)
+    a = _gpu_stochastic(tl, toks, ua, ud, V)
+    b = _gpu_stochastic(tl, toks, ua, ud, V)
+    for k in a:
+        np.testing.assert_array_equal(a[k], b[k])
