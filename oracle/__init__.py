@@ -79,6 +79,7 @@ def lib():
             L.orc_viterbi.argtypes = [_PD, C.c_int, C.c_int, _PI, _PD]
             L.orc_viterbi_f32.argtypes = [_PF, C.c_int, C.c_int, _PI, _PF]
             L.orc_beam.argtypes = [_PD, C.c_int, C.c_int, C.c_int, C.c_int, _PI, _PD]
+            L.orc_topk_features.argtypes = [_PU, C.c_int, C.c_int, _PD]
             L.orc_verify_stochastic.argtypes = [_PU, C.c_int64, C.c_int, C.c_int, _PI, _PF, C.c_float, _PI, _PI,
                                                 _PD]
             L.orc_beam_f32.argtypes = [_PF, C.c_int, C.c_int, C.c_int, C.c_int, _PI, _PF]
@@ -246,6 +247,15 @@ def select_path(scores: np.ndarray, path_rule: int = 0, width: int = 2, topm: in
     if path_rule == 2:
         return beam(scores, width, topm)
     return walk(scores)
+
+
+def topk_features(row_bits, K: int, V: int | None = None):
+    """row [stride] u16 (bf16 bits; the first V columns are the vocabulary) ->
+    features [K, 5] = (log p, p, l_0 - l_k, k / K, k == 0)."""
+    r = _u16(row_bits)
+    feat = np.empty((K, 5), np.float64)
+    lib().orc_topk_features(_p(r, C.c_uint16), V or r.shape[-1], K, _p(feat, C.c_double))
+    return feat
 
 
 def verify_stochastic(target_logits, tokens, u_acc, u_draw: float, V: int | None = None):

@@ -456,6 +456,43 @@ int orc_verify(const int32_t *tokens, const int32_t *target, int B) {
 }
 
 /* ---------------------------------------------------------------------------
+ * Vocabulary-normalised candidate features.  [LiLiCorr] page, Sec. 3 and
+ * App. A: the candidate features are normalised over the whole vocabulary
+ * (log-softmax, computed with the top-K in one pass over the logits).  For
+ * the K best tokens of a row (orc_topk_row order), feat[k] =
+ * [log p_k, p_k, l_0 - l_k, k / K, k == 0], p = softmax of the row.
+ * ------------------------------------------------------------------------- */
+void orc_topk_features(const uint16_t *row, int V, int K, double *feat) {
+  int32_t *ids = (int32_t *)malloc((size_t)K * sizeof(int32_t));
+  float *vals = (float *)malloc((size_t)K * sizeof(float));
+  if (!ids || !vals) {
+    free(ids);
+    free(vals);
+    return;
+  }
+  orc_topk_row(row, V, K, ids, vals);
+  double m = -INFINITY, s = 0.0;
+  for (int v = 0; v < V; ++v) {
+    const double x = orc_bf16_to_double(row[v]);
+    if (x > m) m = x;
+  }
+  if (m > -INFINITY)
+    for (int v = 0; v < V; ++v) s += exp(orc_bf16_to_double(row[v]) - m);
+  const double lse = m > -INFINITY ? m + log(s) : -INFINITY;
+  for (int k = 0; k < K; ++k) {
+    const double l = (double)vals[k];
+    double *f = feat + (size_t)k * 5;
+    f[0] = l == -INFINITY ? -INFINITY : l - lse;
+    f[1] = l == -INFINITY ? 0.0 : exp(l - lse);
+    f[2] = (double)vals[0] - l;
+    f[3] = (double)k / (double)K;
+    f[4] = k == 0 ? 1.0 : 0.0;
+  }
+  free(ids);
+  free(vals);
+}
+
+/* ---------------------------------------------------------------------------
  * Stochastic verification of a point-mass proposal (temperature 1).
  * [DCOCO] page, "Core method": a drafter that emits one token deterministically
  * proposes the point mass p_j(v) = 1[v = y_j]; standard speculative sampling

@@ -12,7 +12,8 @@
  *   [LiLiCorr] "LiLiCorr: Lightweight Likelihood Correlation of Parallel
  *              Drafts for Speculative Decoding": Sec. 3.2 Eq. (1) (cosine
  *              matching), Sec. 3.5 Eq. (8) (greedy walk), App. E Eq. (12)
- *              (highest-scoring path, Viterbi).
+ *              (highest-scoring path, Viterbi), App. A (top-K fused with
+ *              the vocabulary normalisation of the candidate features).
  *   The [DCOCO] page's reproduction assessment, weaknesses (2)-(3): the beam
  *              walk with top-m successors; its "Core method": stochastic
  *              verification of a point-mass proposal.
@@ -128,6 +129,10 @@ void orc_beam_f32(const float *scores, int B, int K, int W, int m, int32_t *choi
 
 /* Greedy verify: number of leading slots whose token equals the target. */
 int orc_verify(const int32_t *tokens, const int32_t *target, int B);
+
+/* Candidate features of one row: for its K best tokens (orc_topk_row order),
+ * feat [K][5] = [log p, p, l_0 - l_k, k/K, k == 0], p = softmax over V. */
+void orc_topk_features(const uint16_t *row, int V, int K, double *feat);
 
 /* Stochastic verification of the point-mass proposal `tokens` [B] against
  * target logits [B+1][stride] (temperature 1): slot j accepted iff

@@ -484,6 +484,36 @@ def test_zero_output_layer_beam_reproduces_draft_argmax():
     np.testing.assert_array_equal(out["choice"], 0)
 
 
+# --------------------------------------------------------------- candidate features
+def test_topk_features_against_scipy_logsumexp():
+    """LiLiCorr App. A features: log p is the row's log-softmax (scipy's
+    logsumexp on the widened bf16 row), p its exponential, the gap to the top
+    candidate, the normalised rank and the is-top flag."""
+    from scipy.special import logsumexp
+    rng = np.random.default_rng(80)
+    for V, K in [(1000, 8), (5000, 16), (301, 32)]:
+        row = synth.make_logits(rng, 1, 1, V, 4, (4.0, 8.0))[0, 0]
+        f = oracle.topk_features(row, K)
+        ids, vals = oracle.topk_row(row, K)
+        x = synth.bf16_to_f32(row).astype(np.float64)
+        lse = logsumexp(x)
+        np.testing.assert_allclose(f[:, 0], vals.astype(np.float64) - lse, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(f[:, 1], np.exp(x[ids] - lse), rtol=1e-12)
+        np.testing.assert_array_equal(f[:, 2], vals[0] - vals.astype(np.float64))
+        np.testing.assert_array_equal(f[:, 3], np.arange(K) / K)
+        np.testing.assert_array_equal(f[:, 4], (np.arange(K) == 0).astype(float))
+        assert f[:, 1].sum() <= 1.0 + 1e-12
+
+
+def test_topk_features_mass_on_candidates_sums_to_one():
+    row = np.full(64, np.float32(-np.inf))
+    row[[3, 7, 9, 40]] = [1.0, 2.0, 0.5, -1.0]
+    f = oracle.topk_features(synth.bf16_bits(row), 8)
+    np.testing.assert_allclose(f[:4, 1].sum(), 1.0, rtol=1e-12)
+    np.testing.assert_array_equal(f[4:, 1], 0.0)
+    assert np.all(np.isneginf(f[4:, 0]))
+
+
 # --------------------------------------------------------------- stochastic verification
 def _bf16_rows(x):
     """fp32 array -> bf16 bit patterns (round to nearest even) as uint16."""
