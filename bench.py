@@ -55,6 +55,8 @@ def parse():
                     help="step 5: prefix-first greedy walk (default), highest-scoring path or beam walk")
     ap.add_argument("--beam-width", type=int, default=4, help="beam walk: partial paths kept (1..4)")
     ap.add_argument("--beam-topm", type=int, default=0, help="beam walk: successors per predecessor (0 = K)")
+    ap.add_argument("--features", action="store_true",
+                    help="also request the vocabulary-normalised candidate features (top-K with log-sum-exp)")
     ap.add_argument("--stochastic-verify", action="store_true",
                     help="also time dcoco_verify_stochastic on [N, B+1, V] target logits (reported apart)")
     ap.add_argument("--only", choices=["topk"], default=None,
@@ -249,7 +251,7 @@ def run_ours(args):
     corr = dc.Corrector({k: torch.from_numpy(v) for k, v in weights_np.items()}, V, d, S, K,
                         max_batch=N, host_staging=True, path_rule=path_rule, beam_width=args.beam_width,
                         beam_topm=args.beam_topm)
-    outs = [corr.alloc_outputs(N, device, full=False) for _ in range(args.sets)]
+    outs = [corr.alloc_outputs(N, device, full=False, features=args.features) for _ in range(args.sets)]
     torch.cuda.synchronize()
 
     def step(i):
@@ -431,6 +433,7 @@ def run_ours(args):
                                    "K=16, r=128, MLP 386-256-1 fp32 weights",
                        "global_batch": world * N, "per_gpu_batch": N, "parallelism": f"replicas x{world}",
                        "inputs": "bf16; arithmetic fp32",
+                       "candidate_features": bool(args.features),
                        "path_rule": args.path_rule if args.path_rule != "beam" else
                        f"beam (width {args.beam_width}, top-m {args.beam_topm or K})",
                        "l2": f"{args.sets} rotating input sets of 160 MB (> 129 MB L2), no flush"},

@@ -56,7 +56,7 @@ class dcoco_inputs(C.Structure):
 class dcoco_outputs(C.Structure):
     _fields_ = [("tokens", C.c_void_p), ("choice", C.c_void_p), ("scores", C.c_void_p),
                 ("accept_len", C.c_void_p), ("topk_ids", C.c_void_p), ("topk_val", C.c_void_p),
-                ("margin", C.c_void_p)]
+                ("margin", C.c_void_p), ("cand_feat", C.c_void_p)]
 
 
 EXPORTED = ("dcoco_version", "dcoco_status_string", "dcoco_create", "dcoco_weights_create",
@@ -179,17 +179,17 @@ def _io(logits, hidden, cand_embed, target_tokens, logits_slot_stride, outs):
     stride = logits_slot_stride if logits_slot_stride is not None else logits.shape[-1]
     ins = dcoco_inputs(_ptr(logits), int(stride), _ptr(hidden), _ptr(cand_embed), _ptr(target_tokens))
     o = dcoco_outputs(*[_ptr(outs.get(k)) for k in ("tokens", "choice", "scores", "accept_len",
-                                                    "topk_ids", "topk_val", "margin")])
+                                                    "topk_ids", "topk_val", "margin", "cand_feat")])
     return ins, o
 
 
 def dcoco_correct(handle, weights, batch: int, logits, hidden, cand_embed, target_tokens=None, *,
                   tokens, choice=None, scores=None, accept_len=None, topk_ids=None, topk_val=None,
-                  margin=None, logits_slot_stride: int | None = None, stream=None) -> None:
+                  margin=None, cand_feat=None, logits_slot_stride: int | None = None, stream=None) -> None:
     """Device buffers in, device buffers out (see include/dcoco.h for layouts)."""
     ins, o = _io(logits, hidden, cand_embed, target_tokens, logits_slot_stride,
                  dict(tokens=tokens, choice=choice, scores=scores, accept_len=accept_len,
-                      topk_ids=topk_ids, topk_val=topk_val, margin=margin))
+                      topk_ids=topk_ids, topk_val=topk_val, margin=margin, cand_feat=cand_feat))
     _check(_lib.dcoco_correct(handle, weights, batch, C.byref(ins), C.byref(o), _stream(stream)),
            "dcoco_correct")
 
@@ -300,7 +300,7 @@ class Corrector:
         except Exception:
             pass
 
-    def alloc_outputs(self, N: int, device="cuda", full: bool = True):
+    def alloc_outputs(self, N: int, device="cuda", full: bool = True, features: bool = False):
         B, K = self.B, self.topk
         i32 = dict(dtype=torch.int32, device=device)
         f32 = dict(dtype=torch.float32, device=device)
@@ -309,6 +309,8 @@ class Corrector:
             out.update(choice=torch.empty(N, B, **i32), scores=torch.empty(N, B - 1, K, K, **f32),
                        topk_ids=torch.empty(N, B, K, **i32), topk_val=torch.empty(N, B, K, **f32),
                        margin=torch.empty(N, B - 1, **f32))
+        if features:
+            out["cand_feat"] = torch.empty(N, B, K, 5, **f32)
         return out
 
     def correct(self, logits, hidden, cand_embed, target_tokens=None, out=None, full=True,

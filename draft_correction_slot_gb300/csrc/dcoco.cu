@@ -17,6 +17,7 @@ constexpr int kH = 256;
 
 struct Workspace {
   unsigned long long *part = nullptr;
+  float2 *part_lse = nullptr;  // per (row, segment) (maximum, sum of exp) for the candidate features
   unsigned *row_count = nullptr;
   int32_t *ids = nullptr;
   float *vals = nullptr;
@@ -128,6 +129,7 @@ void carve_workspace(Carver &c, const dcoco_config &cfg, int B, int topk_segment
   const size_t N = (size_t)cfg.max_batch, K = (size_t)cfg.topk, d = (size_t)cfg.hidden;
   const size_t rows = N * B, cands = rows * K;
   ws.part = c.take<unsigned long long>(rows * (size_t)topk_segments_max * K);
+  ws.part_lse = c.take<float2>(rows * (size_t)topk_segments_max);
   ws.row_count = c.take<unsigned>(rows);
   ws.ids = c.take<int32_t>(cands);
   ws.vals = c.take<float>(cands);
@@ -187,7 +189,7 @@ int validate_call(const dcoco_handle *h, const dcoco_weights *w, int batch, cons
     if (in->logits_slot_stride % 8 != 0) return DCOCO_EINVAL;
     if (!aligned16(in->logits) || !aligned16(in->hidden) || !aligned16(in->cand_embed))
       return DCOCO_EINVAL;
-  } else if (!aligned16(in->cand_embed)) {
+  } else if (!aligned16(in->cand_embed) || out->cand_feat) {  // features: device entry only
     return DCOCO_EINVAL;
   }
   return DCOCO_OK;
@@ -248,7 +250,7 @@ int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs 
   const dc::TopkPlan plan = dc::topk_plan(V, N * B, h->topk_wave);
   // step 1: candidate pools
   DC_TRY(clk.done(dc::launch_topk(K, logits, in->logits_slot_stride, cfg.slots, N, V, plan,
-                                  ws.part, ws.row_count, ids, vals, st, false)));
+                                  ws.part, ws.row_count, ids, vals, st, false, ws.part_lse, out->cand_feat)));
   // step 2 (and the slot-pair state): the candidate rows and the draft-slot
   // rows go through one projection launch, which fills the device in one wave.
   // It overlaps the top-K's tail: its blocks take SMs as the top-K's leave,

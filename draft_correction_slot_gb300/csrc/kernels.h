@@ -29,9 +29,14 @@ TopkPlan topk_plan(int V, int rows, int slots_per_wave);
 int topk_min_segments(int V);  // fewest segments whose per-vector maxima fit a CTA
 int topk_max_segments(int V);
 int topk_occupancy(int K);  // resident top-K CTAs per SM
+// With `feat` (fp32 [rows][K][5]) the same pass also accumulates each row's
+// log-sum-exp and writes the candidates' vocabulary-normalised features
+// [log p, p, l_0 - l_k, k / K, k == 0]; part_lse (float2 [rows][nchunks]) is
+// then needed when nchunks > 1.
 cudaError_t launch_topk(int K, const uint16_t *logits, int64_t stride, int slots, int N, int V,
                         const TopkPlan &plan, unsigned long long *part, unsigned *row_count,
-                        int32_t *ids, float *vals, cudaStream_t st, bool pdl);
+                        int32_t *ids, float *vals, cudaStream_t st, bool pdl, float2 *part_lse = nullptr,
+                        float *feat = nullptr);
 
 // ---------------------------------------------------------------- projections
 // C[m][o] = sum_k A_m[k] * W[o][k] with A_m a bf16 row of length d, on the

@@ -322,11 +322,27 @@ __device__ __forceinline__ void radix_digit(const int *hist, int rank, int lane,
   }
 }
 
-template <int K>
+// Merge (m, s) pairs, s a sum of exp(x - m) (m = -inf: empty).
+__device__ __forceinline__ void lse_merge(float &m, float &s, float m2, float s2) {
+  const float mm = fmaxf(m, m2);
+  if (mm == -INFINITY) return;
+  s = (m == -INFINITY ? 0.f : s * __expf(m - mm)) + (m2 == -INFINITY ? 0.f : s2 * __expf(m2 - mm));
+  m = mm;
+}
+
+// kLse: the stream also accumulates the row's log-sum-exp (each lane a running
+// maximum and sum of exp(x - maximum) over the vectors it reads), and the
+// publishing block writes the candidates' vocabulary-normalised features
+// (LiLiCorr page, App. A: top-K fused with the normalisation, in one pass
+// over the logits): per candidate k, [log p, p, l_0 - l_k, k / K, k == 0],
+// p the softmax over the whole vocabulary.  With several segments each block
+// leaves its (maximum, sum) in part_lse and the merging block combines them.
+template <int K, bool kLse>
 __global__ void __launch_bounds__(kThreads, 4)
 k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, int V, int nseg,
        int seg_vecs, u64 *__restrict__ part, unsigned *__restrict__ row_count,
-       int32_t *__restrict__ out_ids, float *__restrict__ out_val) {
+       int32_t *__restrict__ out_ids, float *__restrict__ out_val, float2 *__restrict__ part_lse,
+       float *__restrict__ out_feat) {
   // s_vmax (pass 1-2: per-vector maxima, bf16 bits), s_keys (pass 3:
   // candidate elements) and the fallback's per-warp candidate buffers share
   // storage; each use ends at a barrier before the next begins
@@ -343,6 +359,7 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
   __shared__ u64 s_cta_bound;
   __shared__ int s_ncand, s_nkeys, s_flag;
   __shared__ uint32_t s_tkey;
+  __shared__ float s_lm[kWarps], s_ls[kWarps];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int row = blockIdx.x, seg = blockIdx.y;
@@ -368,6 +385,7 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
   }
 
   // ---------------------------------------------------------------- pass 1: stream
+  float lm = -INFINITY, ls = 0.f;  // kLse: this lane's running (maximum, sum of exp)
   {
     uint4 a[kU], b[kU];
     static_assert(kStep == 2 * kGroup && kU == 4, "one step = two groups of 64 vectors");
@@ -381,6 +399,19 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
           const uint32_t m = bf16x2_max(m2, m2 >> 16) & 0xFFFFu;
           s_vmax[j - v0] = (uint16_t)m;
           gk[u >> 1] = max(gk[u >> 1], bf16_order_key(m));
+          if (kLse) {
+            const float vm = bf16_bits_to_float(m);
+            if (vm > lm) {
+              ls = lm == -INFINITY ? 0.f : ls * __expf(lm - vm);
+              lm = vm;
+            }
+            if (lm != -INFINITY) {
+              const uint32_t wd[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+              for (int h = 0; h < 4; ++h)
+                ls += __expf(bf16_bits_to_float(wd[h] & 0xFFFFu) - lm) + __expf(bf16_bits_to_float(wd[h] >> 16) - lm);
+            }
+          }
         }
       }
       const int g = (base - v0) / kGroup;
@@ -400,7 +431,26 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
       store(b, base + kStep);
     }
   }
+  if (kLse) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float om = __shfl_xor_sync(DC_FULL_MASK, lm, off), os = __shfl_xor_sync(DC_FULL_MASK, ls, off);
+      lse_merge(lm, ls, om, os);
+    }
+    if (lane == 0) {
+      s_lm[warp] = lm;
+      s_ls[warp] = ls;
+    }
+  }
   __syncthreads();
+  if (kLse && tid == 0) {
+    float m = s_lm[0], sum = s_ls[0];
+    for (int w = 1; w < kWarps; ++w) lse_merge(m, sum, s_lm[w], s_ls[w]);
+    if (has_tail)  // the last V % 8 tokens, outside the vector stream
+      for (int t = nvec * 8; t < V; ++t) lse_merge(m, sum, bf16_bits_to_float(rowp[t]), 1.f);
+    s_lm[0] = m;
+    s_ls[0] = sum;
+  }
 
   // ---------------------------------------------------------------- pass 2: bound
   // The bound is the K-th largest group key, found by a two-digit radix
@@ -548,6 +598,10 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
       my[tid] = s_top[tid];
       __threadfence();
     }
+    if (kLse && tid == 0) {
+      part_lse[(int64_t)row * nseg + seg] = make_float2(s_lm[0], s_ls[0]);
+      __threadfence();
+    }
     __syncthreads();
     if (tid == 0) {
       const unsigned prev = atomicAdd(&row_count[row], 1u);
@@ -564,14 +618,36 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
         acc = warp_merge_topk<K>(acc, lane < K ? __ldcg(rp + sg * K + lane) : 0ull, lane);
       if (lane < K) s_top[lane] = acc;
       if (lane == 0) row_count[row] = 0u;  // ready for the next call
+      if (kLse && lane == 0) {
+        float m = -INFINITY, sum = 0.f;
+        for (int sg = 0; sg < nseg; ++sg) {
+          const float2 ms = __ldcg(part_lse + (int64_t)row * nseg + sg);
+          lse_merge(m, sum, ms.x, ms.y);
+        }
+        s_lm[0] = m;
+        s_ls[0] = sum;
+      }
     }
     __syncthreads();
   }
   if (tid < K) {
     const u64 x = s_top[tid];
     const uint32_t id = 0xFFFFFFFFu - (uint32_t)(x & 0xFFFFFFFFull);
+    const float val = order_key_to_float((uint32_t)(x >> 32));
     out_ids[(int64_t)row * K + tid] = (int32_t)id;
-    out_val[(int64_t)row * K + tid] = order_key_to_float((uint32_t)(x >> 32));
+    out_val[(int64_t)row * K + tid] = val;
+    if (kLse) {
+      const float m = s_lm[0];
+      const float lse = m == -INFINITY ? -INFINITY : m + __logf(s_ls[0]);
+      const float top = order_key_to_float((uint32_t)(s_top[0] >> 32));
+      const float logp = val == -INFINITY ? -INFINITY : val - lse;
+      float *f = out_feat + ((int64_t)row * K + tid) * 5;
+      f[0] = logp;
+      f[1] = val == -INFINITY ? 0.f : __expf(logp);
+      f[2] = top - val;
+      f[3] = (float)tid / (float)K;
+      f[4] = tid == 0 ? 1.f : 0.f;
+    }
   }
 }
 
@@ -613,7 +689,7 @@ int topk_max_segments(int V) {
 template <int K>
 static int topk_occupancy_k() {
   int occ = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_topk<K>, kThreads, 0) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k_topk<K, false>, kThreads, 0) != cudaSuccess) {
     cudaGetLastError();
     return 1;
   }
@@ -629,25 +705,38 @@ int topk_occupancy(int K) {
   }
 }
 
+template <int K>
+static cudaError_t launch_topk_k(const dim3 &grid, const dim3 &block, cudaStream_t st, bool pdl,
+                                 const uint16_t *logits, int64_t stride, int slots, int B, int V, const TopkPlan &plan,
+                                 unsigned long long *part, unsigned *row_count, int32_t *ids, float *vals,
+                                 float2 *part_lse, float *feat) {
+  if (feat)
+    return launch_ex(k_topk<K, true>, grid, block, 0, st, pdl, 0, logits, stride, slots, B, V, plan.nchunks,
+                     plan.chunk_vecs, part, row_count, ids, vals, part_lse, feat);
+  return launch_ex(k_topk<K, false>, grid, block, 0, st, pdl, 0, logits, stride, slots, B, V, plan.nchunks,
+                   plan.chunk_vecs, part, row_count, ids, vals, part_lse, feat);
+}
+
 cudaError_t launch_topk(int K, const uint16_t *logits, int64_t stride, int slots, int N, int V,
                         const TopkPlan &plan, unsigned long long *part, unsigned *row_count,
-                        int32_t *ids, float *vals, cudaStream_t st, bool pdl) {
+                        int32_t *ids, float *vals, cudaStream_t st, bool pdl, float2 *part_lse, float *feat) {
   const int B = slots - 1;
   if (N == 0) return cudaSuccess;
+  if (feat && plan.nchunks > 1 && !part_lse) return cudaErrorInvalidValue;
   const dim3 grid(N * B, plan.nchunks), block(kThreads);
   cudaError_t e;
   switch (K) {
     case 8:
-      e = launch_ex(k_topk<8>, grid, block, 0, st, pdl, 0, logits, stride, slots, B, V, plan.nchunks,
-                    plan.chunk_vecs, part, row_count, ids, vals);
+      e = launch_topk_k<8>(grid, block, st, pdl, logits, stride, slots, B, V, plan, part, row_count, ids, vals,
+                           part_lse, feat);
       break;
     case 16:
-      e = launch_ex(k_topk<16>, grid, block, 0, st, pdl, 0, logits, stride, slots, B, V, plan.nchunks,
-                    plan.chunk_vecs, part, row_count, ids, vals);
+      e = launch_topk_k<16>(grid, block, st, pdl, logits, stride, slots, B, V, plan, part, row_count, ids, vals,
+                            part_lse, feat);
       break;
     case 32:
-      e = launch_ex(k_topk<32>, grid, block, 0, st, pdl, 0, logits, stride, slots, B, V, plan.nchunks,
-                    plan.chunk_vecs, part, row_count, ids, vals);
+      e = launch_topk_k<32>(grid, block, st, pdl, logits, stride, slots, B, V, plan, part, row_count, ids, vals,
+                            part_lse, feat);
       break;
     default:
       return cudaErrorInvalidValue;

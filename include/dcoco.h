@@ -138,6 +138,15 @@ typedef struct {
                           second-best predecessor total of the chosen
                           candidate at slot p+1 (+inf when only one
                           predecessor is possible)                         */
+  float *cand_feat;    /* [N][B][K][5] vocabulary-normalised candidate
+                          features, or NULL (then not computed): per
+                          candidate k of a slot, [log p, p, l_0 - l_k, k/K,
+                          1 if k == 0], p = softmax of the slot's logits over
+                          the whole vocabulary.  The top-K pass then also
+                          accumulates each row's log-sum-exp ([LiLiCorr]
+                          App. A: top-K fused with the normalisation); the
+                          path itself still uses the raw logits.  Device
+                          entry only (dcoco_correct_host: EINVAL).         */
 } dcoco_outputs;
 
 /* Library version, major*10000 + minor*100 + patch. */

@@ -396,3 +396,49 @@ def test_stochastic_verify_deterministic(torch_cuda):
     b = _gpu_stochastic(tl, toks, ua, ud, V)
     for k in a:
         np.testing.assert_array_equal(a[k], b[k])
+
+
+# ------------------------------------------------------------------ candidate features
+def _run_features(prob: Problem):
+    import torch
+    import draft_correction_slot_gb300 as dc
+    corr = dc.Corrector({k: torch.from_numpy(v) for k, v in prob.w.items()}, prob.V, prob.d, prob.slots, prob.K,
+                        max_batch=prob.N)
+    try:
+        E = bf16_tensor(prob.E)
+        lg, hd = bf16_tensor(prob.logits), bf16_tensor(prob.hidden)
+        tg = torch.from_numpy(prob.targets).cuda()
+        with_f = corr.correct(lg, hd, E, tg, out=corr.alloc_outputs(prob.N, lg.device, True, features=True),
+                              logits_slot_stride=prob.stride)
+        without = corr.correct(lg, hd, E, tg, logits_slot_stride=prob.stride)
+        torch.cuda.synchronize()
+        assert corr.status() == dc.DCOCO_OK
+        return ({k: v.cpu().numpy() for k, v in with_f.items()}, {k: v.cpu().numpy() for k, v in without.items()})
+    finally:
+        corr.close()
+
+
+@pytest.mark.parametrize("N,K,V", [(2, 16, V_QWEN), (1, 16, V_QWEN), (3, 8, 4099), (2, 32, 20011)])
+def test_candidate_features(torch_cuda, N, K, V):
+    """LiLiCorr App. A: the top-K pass also yields the candidates' log-softmax
+    features (one pass; at N = 1 the rows are split into segments whose
+    partial sums the last block combines).  Features match the oracle's fp64
+    log-sum-exp within fp32 accuracy; the rest of the path is bit-identical
+    with and without them."""
+    prob = Problem(90 + N + K, N=N, V=V, d=512, K=K, planted=8, boost=(4.0, 12.0),
+                   stride=((V + 7) // 8) * 8 + (8 if V % 8 else 0))
+    g, plain = _run_features(prob)
+    for k in plain:
+        np.testing.assert_array_equal(g[k], plain[k], err_msg=k)
+    worst = 0.0
+    for n in range(N):
+        for i in range(prob.B):
+            ref = oracle.topk_features(prob.logits[n, i + 1], K, V=V)
+            f = g["cand_feat"][n, i]
+            worst = max(worst, float(np.abs(f[:, 0] - ref[:, 0]).max()))
+            np.testing.assert_allclose(f[:, 0], ref[:, 0], rtol=0, atol=2e-5)
+            np.testing.assert_allclose(f[:, 1], ref[:, 1], rtol=5e-5, atol=1e-12)
+            np.testing.assert_array_equal(f[:, 2], ref[:, 2].astype(np.float32))
+            np.testing.assert_array_equal(f[:, 3], ref[:, 3].astype(np.float32))
+            np.testing.assert_array_equal(f[:, 4], ref[:, 4].astype(np.float32))
+    print(f"[parity] candidate features N={N} K={K} V={V}: max |log p error| {worst:.2e}")
