@@ -571,18 +571,31 @@ int dcoco_correct_host(dcoco_handle *h, const dcoco_weights *w, int batch, const
   const int B = h->B, K = cfg.topk;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const size_t rows = (size_t)batch * cfg.slots;
-  // inputs: logits rows (pitched copy to the dense staging stride), hidden, targets
-  DC_TRY(cudaMemcpy2DAsync(ws.st_logits, ws.st_stride * sizeof(uint16_t), in->logits,
-                           in->logits_slot_stride * sizeof(uint16_t), cfg.vocab * sizeof(uint16_t),
-                           rows, cudaMemcpyHostToDevice, st));
+  // inputs.  Logits in page-locked host memory that the device can address
+  // are read in place by the top-K (over the host link, at the rate a copy
+  // would get, without the copy's serial step before the kernel); otherwise
+  // their rows are copied to the dense staging buffer first.  Hidden states
+  // and targets (small) are copied.
+  const void *logits_dev = nullptr;
+  {
+    cudaPointerAttributes pa;
+    if (cudaPointerGetAttributes(&pa, in->logits) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
+        pa.devicePointer && aligned16(pa.devicePointer) && in->logits_slot_stride % 8 == 0)
+      logits_dev = pa.devicePointer;
+    cudaGetLastError();  // an unregistered pointer is not an error here
+  }
+  if (!logits_dev)
+    DC_TRY(cudaMemcpy2DAsync(ws.st_logits, ws.st_stride * sizeof(uint16_t), in->logits,
+                             in->logits_slot_stride * sizeof(uint16_t), cfg.vocab * sizeof(uint16_t),
+                             rows, cudaMemcpyHostToDevice, st));
   DC_TRY(cudaMemcpyAsync(ws.st_hidden, in->hidden, rows * cfg.hidden * sizeof(uint16_t),
                          cudaMemcpyHostToDevice, st));
   if (in->target_tokens)
     DC_TRY(cudaMemcpyAsync(ws.st_target, in->target_tokens, (size_t)batch * B * sizeof(int32_t),
                            cudaMemcpyHostToDevice, st));
   dcoco_inputs din = *in;
-  din.logits = ws.st_logits;
-  din.logits_slot_stride = ws.st_stride;
+  din.logits = logits_dev ? logits_dev : ws.st_logits;
+  din.logits_slot_stride = logits_dev ? in->logits_slot_stride : ws.st_stride;
   din.hidden = ws.st_hidden;
   din.target_tokens = in->target_tokens ? ws.st_target : nullptr;
   dcoco_outputs dout = {};

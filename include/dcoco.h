@@ -177,11 +177,14 @@ int dcoco_weights_create(dcoco_handle *h, const dcoco_weight_ptrs *w, void *stre
 int dcoco_correct(dcoco_handle *h, const dcoco_weights *w, int batch,
                   const dcoco_inputs *in, const dcoco_outputs *out, void *stream);
 
-/* Same path with HOST buffers: copies logits and hidden (and target tokens)
- * from host memory (pinned for full speed) into the handle's staging buffers,
- * runs dcoco_correct, copies the requested outputs back to the host pointers
- * in `out`, and synchronises `stream`.  `in->cand_embed` stays a DEVICE
- * pointer (the frozen table is resident).  Requires host_staging at create.
+/* Same path with HOST buffers: copies hidden (and target tokens) from host
+ * memory into the handle's staging buffers; logits in page-locked host memory
+ * the device can address (e.g. cudaHostAlloc) are read in place by the top-K
+ * over the host link, other logits are copied to staging first.  Runs
+ * dcoco_correct, copies the requested outputs back to the host pointers in
+ * `out`, and synchronises `stream`.  The host buffers must stay unchanged
+ * until the call returns.  `in->cand_embed` stays a DEVICE pointer (the
+ * frozen table is resident).  Requires host_staging at create.
  * Errors: as dcoco_correct, plus EINVAL if the handle has no staging. */
 int dcoco_correct_host(dcoco_handle *h, const dcoco_weights *w, int batch,
                        const dcoco_inputs *in, const dcoco_outputs *out, void *stream);

@@ -199,15 +199,18 @@ def test_host_entry_matches_device_entry(torch_cuda):
     corr = dc.Corrector({k: torch.from_numpy(v) for k, v in prob.w.items()}, prob.V, prob.d,
                         max_batch=3, host_staging=True)
     E = bf16_tensor(prob.E)
-    lg = torch.from_numpy(prob.logits.view(np.int16)).pin_memory()
-    hd = torch.from_numpy(prob.hidden.view(np.int16)).pin_memory()
-    tg = torch.from_numpy(prob.targets).pin_memory()
-    out = {k: torch.empty_like(torch.from_numpy(dev[k])).pin_memory()
-           for k in ("tokens", "accept_len", "scores", "topk_ids")}
-    dc.dcoco_correct_host(corr.handle, corr.weights, 3, lg, hd, E, tg, logits_slot_stride=prob.stride,
-                          **out)
-    for k, v in out.items():
-        np.testing.assert_array_equal(v.numpy(), dev[k], err_msg=k)
+    # pinned logits are read in place; pageable ones go through the staging copy
+    for pinned in (True, False):
+        lg = torch.from_numpy(prob.logits.view(np.int16).copy())
+        lg = lg.pin_memory() if pinned else lg
+        hd = torch.from_numpy(prob.hidden.view(np.int16)).pin_memory()
+        tg = torch.from_numpy(prob.targets).pin_memory()
+        out = {k: torch.empty_like(torch.from_numpy(dev[k])).pin_memory()
+               for k in ("tokens", "accept_len", "scores", "topk_ids")}
+        dc.dcoco_correct_host(corr.handle, corr.weights, 3, lg, hd, E, tg, logits_slot_stride=prob.stride,
+                              **out)
+        for k, v in out.items():
+            np.testing.assert_array_equal(v.numpy(), dev[k], err_msg=f"{k} (pinned={pinned})")
     corr.close()
 
 
