@@ -421,7 +421,7 @@ def _run_features(prob: Problem):
         corr.close()
 
 
-@pytest.mark.parametrize("N,K,V", [(2, 16, V_QWEN), (1, 16, V_QWEN), (3, 8, 4099), (2, 32, 20011)])
+@pytest.mark.parametrize("N,K,V", [(2, 16, V_QWEN), (1, 16, V_QWEN), (3, 8, 4099), (2, 32, 20011), (11, 16, V_QWEN)])
 def test_candidate_features(torch_cuda, N, K, V):
     """LiLiCorr App. A: the top-K pass also yields the candidates' log-softmax
     features (one pass; at N = 1 the rows are split into segments whose
