@@ -1,6 +1,7 @@
 // common.cuh -- device helpers shared by the library's kernels (sm_103a).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -17,6 +18,10 @@ enum : int {
 // ---- bf16 bit helpers ------------------------------------------------------
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t bits16) {
   return __uint_as_float(bits16 << 16);
+}
+// fp32 -> bf16 bits, round to nearest even.
+__device__ __forceinline__ uint32_t bf16_rn_bits(float f) {
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
 // Order-preserving 16-bit key of a bf16 value: larger key <=> larger value.

@@ -22,7 +22,8 @@ struct Workspace {
   int32_t *ids = nullptr;
   float *vals = nullptr;
   float *slot_proj = nullptr;  // [N*B][3r]  (variant 1: [N*B][2r])
-  float *cand_proj = nullptr;  // [N*B*K][r] (variant 1: [N*B*K][2r])
+  float *cand_proj = nullptr;  // variant 1: [N*B*K][2r]
+  uint16_t *b_hi = nullptr, *b_lo = nullptr;  // variant 0: LN0(W_cand E[c]) as bf16 hi, lo [N*B*K][r]
   float *P = nullptr;          // [N*B][H] (rows of the last slot unused)
   float *U = nullptr;          // [N*B*K][H]  (variant 1: O [N*B*K][r])
   float *V = nullptr;          // [N*B*K][H]  (variant 1: I [N*B*K][r])
@@ -68,7 +69,7 @@ struct dcoco_handle {
                               // results do not depend on the batch size)
   void *block = nullptr;  // one device allocation holding the workspace
   Workspace ws;
-  dc::CandIoMaps cand_io;  // TMA maps of cand_proj, U, V (variant 0)
+  dc::CandIoMaps cand_io;  // TMA maps of b (hi, lo), U, V (variant 0)
   dc::SlotIoMaps slot_io;  // TMA maps of slot_proj, P (variant 0)
   cudaStream_t last_stream = nullptr;
   long long launches = 0;            // kernels launched so far
@@ -135,6 +136,8 @@ void carve_workspace(Carver &c, const dcoco_config &cfg, int B, int topk_segment
   ws.vals = c.take<float>(cands);
   ws.slot_proj = c.take<float>(rows * 3 * kR);
   ws.cand_proj = c.take<float>(cands * 2 * kR);
+  ws.b_hi = c.take<uint16_t>(cands * kR);
+  ws.b_lo = c.take<uint16_t>(cands * kR);
   ws.P = c.take<float>(N * B * kH);
   ws.U = c.take<float>(cands * kH);
   ws.V = c.take<float>(cands * kH);
@@ -257,7 +260,14 @@ int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs 
   // the draft-slot tiles start at once and the candidate tiles wait for the ids.
   const int r_out = cfg.variant == 0 ? kR : 2 * kR;          // candidate outputs
   const int s_out = cfg.variant == 0 ? 3 * kR : 2 * kR;      // draft-slot outputs
-  const dc::ProjJob cj{E, ids, ws.cand_proj, cands, r_out, dc::proj_tc_tiles(cands, r_out)};
+  dc::ProjJob cj{E, ids, ws.cand_proj, cands, r_out, dc::proj_tc_tiles(cands, r_out)};
+  if (cfg.variant == 0) {
+    // the reduction leaves b = LN0(W_cand E[c]) ready for the fuse product
+    cj.C = nullptr;
+    cj.ln_hi = ws.b_hi;
+    cj.ln_lo = ws.b_lo;
+    cj.ln_eps = cfg.ln_eps;
+  }
   const dc::ProjJob sj{hidden, nullptr, ws.slot_proj, rows, s_out, dc::proj_tc_tiles(rows, s_out)};
   DC_TRY(clk.done(dc::launch_proj_tc(cj, w->map_cand_hi, w->map_cand_lo, &sj, &w->map_slot_hi,
                                      &w->map_slot_lo, cfg.slots, B, d, V, h->splits, ws.err, st, true)));
@@ -373,7 +383,8 @@ int dcoco_create(const dcoco_config *cfg, dcoco_handle **out) {
   const int rows_cap = cfg->max_batch * h->B, cands_cap = rows_cap * cfg->topk;
   const bool maps_ok =
       cfg->variant != 0 ||
-      (dc::encode_f32_rows_map(&h->cand_io.cp, h->ws.cand_proj, cands_cap, kR, 128) &&
+      (dc::encode_bf16_rows_map(&h->cand_io.bh, h->ws.b_hi, cands_cap, kR, 128) &&
+       dc::encode_bf16_rows_map(&h->cand_io.bl, h->ws.b_lo, cands_cap, kR, 128) &&
        dc::encode_f32_rows_map(&h->cand_io.u, h->ws.U, cands_cap, kH, 128) &&
        dc::encode_f32_rows_map(&h->cand_io.v, h->ws.V, cands_cap, kH, 128) &&
        dc::encode_f32_rows_map(&h->slot_io.sp, h->ws.slot_proj, rows_cap, 3 * kR, 128) &&

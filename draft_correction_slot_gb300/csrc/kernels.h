@@ -58,6 +58,11 @@ struct ProjJob {
   float *C;               // fp32 [M][No]
   int M, No;
   int tiles;              // proj_tc_tiles(M, No)
+  // With ln_hi set (No == 128), each output row leaves as LN0(row) (non-
+  // affine, eps ln_eps) split into bf16 hi ([M][128], ln_hi) and lo (the
+  // rounding remainder, ln_lo) instead of fp32 in C.
+  uint16_t *ln_hi = nullptr, *ln_lo = nullptr;
+  float ln_eps = 0.f;
 };
 int proj_tc_splits(int d, int requested);
 int proj_tc_tiles(int M, int No);
@@ -93,21 +98,23 @@ struct MlpMaps {
 // another).  Per draft slot i (used for i < B-1):
 // P_i = W1[:, :r] (W_pair[:, :d] h_i + W_pair[:, d:] h_{i+1}) + b1 ([rows][H]).
 // slot_proj is [N*B][3r] = (W_ctx h | W_pair[:, :d] h | W_pair[:, d:] h).
-// Per candidate: b = LN0(cand_proj), g = LN0(W_ctx h) of its slot,
+// Per candidate: b = LN0(W_cand E[c]) (from the projection, as bf16 hi and
+// lo), g = LN0(W_ctx h) of its slot,
 // z = gamma*LN0(W_fuse[:, :r] b + W_fuse[:, r:] g) + beta,
 // U = W1_a z + w_la l, V = W1_b z + w_lb l.  M = N * B * K candidates
 // (8 <= K, K divides 128), candidate m belongs to draft slot m / K.
-// Tiles move by TMA: `slot.sp` reads slot_proj, `slot.p` writes P, `cand.cp`
-// reads cand_proj ([rows][r]), `cand.u` / `cand.v` write U and V ([rows][H]);
-// all are fp32 maps with box 32 x 128 over at least the call's rows (rows of
-// the last tile past the call's count receive the outputs of stale or
-// all-zero input rows).  The launch may overlap the end of the previous
-// kernel (programmatic serialization).
+// Tiles move by TMA: `slot.sp` reads slot_proj, `slot.p` writes P,
+// `cand.u` / `cand.v` write U and V ([rows][H]) -- fp32 maps with box
+// 32 x 128 -- and `cand.bh` / `cand.bl` read b's hi and lo halves (bf16
+// [rows][r], box 64 x 128), all over at least the call's rows (rows of the
+// last tile past the call's count receive the outputs of stale or all-zero
+// input rows).  The launch may overlap the end of the previous kernel
+// (programmatic serialization).
 struct SlotIoMaps {
   CUtensorMap sp, p;
 };
 struct CandIoMaps {
-  CUtensorMap cp, u, v;
+  CUtensorMap bh, bl, u, v;
 };
 cudaError_t launch_maps_tc(const MlpMaps &maps, const SlotIoMaps &slot, const CandIoMaps &cand,
                            const float *slot_proj, const float *topk_val, const MlpWeightsDev &w, int N, int B,

@@ -64,10 +64,6 @@ struct MapsParams {
   int *err;
 };
 
-__device__ __forceinline__ uint32_t bf16_rn_bits(float f) {
-  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
-}
-
 // Barrier over the row threads only (the control warp keeps issuing).
 __device__ __forceinline__ void rows_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kRowThreads) : "memory");
@@ -347,15 +343,17 @@ __device__ __forceinline__ void slot_role(const MapsParams &mp, int chunk, int t
 // Gf = W_fuse[:, r:] LN0(W_ctx h) of the tile's draft slots (128 / K of them):
 // fp32 dot products, each thread holding a 32-long slice of one W_fuse row
 // (loaded while the block waits for the previous kernel), partial sums met
-// by warp shuffles.  Tensor memory: [0,128) the fuse
+// by warp shuffles.  b = LN0(W_cand E[c]) arrives ready as bf16 hi and lo
+// (the projection's reduction normalises and splits each row), straight
+// into the fuse product's A operand.  Tensor memory: [0,128) the fuse
 // product, [128,384) the 256 layer-1 outputs of this half.  Shared memory
 // (three 64 KB regions), by phase:
 //   A:  b (hi, lo), then z (hi, lo);                  then outputs 128..255
 //   W0: W_fuse[:, :r] (hi, lo), then layer-1 rows 128..255 of this half
-//   S:  the cand_proj tile (fp32, 4 swizzled 32-column boxes),
-//       then layer-1 rows 0..127 of this half;       then outputs 0..127
-// All tiles move by TMA; the fp32 boxes use the same 128-byte swizzle as the
-// bf16 operands, so the row threads' 16-byte accesses are conflict-free.
+//   S:  layer-1 rows 0..127 of this half;             then outputs 0..127
+// All tiles move by TMA; the fp32 output boxes use the same 128-byte swizzle
+// as the bf16 operands, so the row threads' 16-byte accesses are
+// conflict-free.
 constexpr int kOffS = 4 * kMat;
 constexpr int kCandSmemBytes = 6 * kMat + 1024;
 constexpr int kMapsSmemBytes = kCandSmemBytes > kSlotSmemBytes ? kCandSmemBytes : kSlotSmemBytes;
@@ -368,8 +366,7 @@ __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int ti
                                           int *err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  __shared__ __align__(8) unsigned long long bar_w0, bar_s, bar_w1, bar_w2, bar_a, bar_fuse, bar_a2,
-      bar_uv0, bar_uv1;
+  __shared__ __align__(8) unsigned long long bar_w0, bar_b, bar_w1, bar_w2, bar_fuse, bar_a2, bar_uv0, bar_uv1;
   __shared__ float s_red[2][4 * kRows];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -387,10 +384,9 @@ __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int ti
 
   if (tid == 0) {
     mbar_init(smem_u32(&bar_w0), 1);
-    mbar_init(smem_u32(&bar_s), 1);
+    mbar_init(smem_u32(&bar_b), 1);
     mbar_init(smem_u32(&bar_w1), 1);
     mbar_init(smem_u32(&bar_w2), 1);
-    mbar_init(smem_u32(&bar_a), kRowThreads);
     mbar_init(smem_u32(&bar_fuse), 1);
     mbar_init(smem_u32(&bar_a2), kRowThreads);
     mbar_init(smem_u32(&bar_uv0), 1);
@@ -404,22 +400,20 @@ __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int ti
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   const int wrow0 = half * kH;  // first row of this half's block in [W1_a ; W1_b]
-  bool w1_issued = false, w2_issued = false;
+  bool w2_issued = false;
 
   if (warp == kRowWarps) {
     if (lane == 0) {
       // ------------------------------------------------------------ control thread
+      // the weights first: W_fuse[:, :r] to W0, layer-1 rows 0..127 to S
       load_pair(w0_hi, w0_lo, &mp.maps.fb_hi, &mp.maps.fb_lo, 0, smem_u32(&bar_w0));
-      pdl_wait();  // cand_proj comes from the previous kernel
-      mbar_arrive_expect_tx(smem_u32(&bar_s), 4 * kBox);
-      for (int bx = 0; bx < 4; ++bx) tma_load_2d(s_hi + bx * kBox, &mp.cand.cp, bx * 32, m0, smem_u32(&bar_s));
+      load_pair(s_hi, s_lo, &mp.maps.w1_hi, &mp.maps.w1_lo, wrow0, smem_u32(&bar_w1));
+      pdl_wait();  // b comes from the previous kernel
+      load_pair(a_hi, a_lo, &mp.cand.bh, &mp.cand.bl, m0, smem_u32(&bar_b));
       // y = W_fuse[:, :r] b
-      if (mbar_wait(smem_u32(&bar_w0), 0, &s_abort, err) && mbar_wait(smem_u32(&bar_a), 0, &s_abort, err)) {
+      if (mbar_wait(smem_u32(&bar_w0), 0, &s_abort, err) && mbar_wait(smem_u32(&bar_b), 0, &s_abort, err)) {
         tc_fence_after();
         mma_split(tmem, a_hi, a_lo, w0_hi, w0_lo);
-        // the row threads are done with the cand_proj tile: S takes layer-1 rows 0..127
-        load_pair(s_hi, s_lo, &mp.maps.w1_hi, &mp.maps.w1_lo, wrow0, smem_u32(&bar_w1));
-        w1_issued = true;
       }
       mma_commit(smem_u32(&bar_fuse));
       // once the fuse MMAs have read W0, it takes layer-1 rows 128..255
@@ -427,8 +421,7 @@ __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int ti
         load_pair(w0_hi, w0_lo, &mp.maps.w1_hi, &mp.maps.w1_lo, wrow0 + 128, smem_u32(&bar_w2));
         w2_issued = true;
       }
-      if (w1_issued && mbar_wait(smem_u32(&bar_a2), 0, &s_abort, err) &&
-          mbar_wait(smem_u32(&bar_w1), 0, &s_abort, err)) {
+      if (mbar_wait(smem_u32(&bar_a2), 0, &s_abort, err) && mbar_wait(smem_u32(&bar_w1), 0, &s_abort, err)) {
         tc_fence_after();
         mma_split(tmem + 128, a_hi, a_lo, s_hi, s_lo);
       }
@@ -467,25 +460,13 @@ __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int ti
       }
     }
     float x[kQ];
-    // b = LN0(cand_proj row): quarter q is box q of the staged tile
-    const bool ok0 = rows_all(mbar_wait(smem_u32(&bar_s), 0, &s_abort, err) && !s_abort);
-    // W_ctx h of the tile's slots (slot_proj, from the previous kernel: the
-    // tile's arrival orders it after the wait for that kernel); one warp per
-    // slot, four columns per lane, in flight during the LayerNorm of b
+    // W_ctx h of the tile's slots (slot_proj, from the previous kernel); one
+    // warp per slot, four columns per lane
+    pdl_wait();
     const int gs = slot0 + warp;
     float4 gx = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (ok0 && warp < nslots && gs < mp.NB)
+    if (warp < nslots && gs < mp.NB)
       gx = __ldcg(reinterpret_cast<const float4 *>(mp.slot_proj + (int64_t)gs * 3 * kR) + lane);
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (ok0 && live) v = *reinterpret_cast<const float4 *>(box_chunk(smem + kOffS + q * kBox, r, c));
-      x[4 * c] = v.x; x[4 * c + 1] = v.y; x[4 * c + 2] = v.z; x[4 * c + 3] = v.w;
-    }
-    ln0_part(x, eps, s_red[0], s_red[1], r, q);
-    store_split_part(smem + kOffA, smem + kOffA + kMat, r, q, x);
-    fence_proxy_async();
-    mbar_arrive(smem_u32(&bar_a));
 
     // g = LN0(W_ctx h) of each slot (warp-wide sums), then
     // Gf[s][o] = sum_k W_fuse[o][r + k] g[s][k]: thread (go, gk) adds its
@@ -586,8 +567,8 @@ __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int ti
   if (s_abort && warp == kRowWarps && lane == 0) {
     // a wait expired: let the copies and MMAs already issued land first
     mbar_drain(smem_u32(&bar_w0), 0);
-    mbar_drain(smem_u32(&bar_s), 0);
-    if (w1_issued) mbar_drain(smem_u32(&bar_w1), 0);
+    mbar_drain(smem_u32(&bar_b), 0);
+    mbar_drain(smem_u32(&bar_w1), 0);
     if (w2_issued) mbar_drain(smem_u32(&bar_w2), 0);
     mbar_drain(smem_u32(&bar_uv1), 0);
   }

@@ -30,6 +30,10 @@
 // draft-slot rows), their tiles listed one after the other along gridDim.y,
 // so that both fill the device in a single wave.  Draft-slot tiles depend on
 // nothing the previous kernel writes and start without waiting for it.
+// A job may ask for its rows LayerNormed instead (non-affine, the step (2)
+// normalisation of the candidate representation): the reduction holds each
+// finished 128-wide row in one warp, normalises it there and stores it as
+// bf16 hi + lo, the operand format of the next map's tensor-core product.
 // Every wait is bounded in time; on expiry the kernel records kErrTimeout in
 // the device status word and does not store its rows.
 #include <cuda.h>
@@ -136,6 +140,9 @@ k_proj_tc(ProjJob job0, ProjJob job1, const __grid_constant__ CUtensorMap map0_h
   const uint16_t *__restrict__ table = job.table;
   const int32_t *__restrict__ ids = job.ids;
   float *__restrict__ C = job.C;
+  uint16_t *__restrict__ ln_hi = job.ln_hi;
+  uint16_t *__restrict__ ln_lo = job.ln_lo;
+  const float ln_eps = job.ln_eps;
   const int nkb_total = d / kTileK;
   const int kb0 = split * kb_per_split;
   const int nkb = min(kb_per_split, nkb_total - kb0);
@@ -346,12 +353,59 @@ k_proj_tc(ProjJob job0, ProjJob job1, const __grid_constant__ CUtensorMap map0_h
           }
       }
     }
+    // e < nchunks and s_abort are warp-uniform: a warp's 32 chunks are one
+    // whole row (nchunks and the thread count are multiples of 32)
+    if (s_abort) continue;
+    const int c = tid & 31;  // = e % (kTileN / 4) for both rows
+    if (ln_hi) {
+      // LN0 of the two finished rows (lane c holds columns 4c .. 4c + 3 of
+      // each): the mean, then the population variance of the deviations; the
+      // two rows' warp sums interleave
+      float4 v[2];
+      float sm[2], sq[2];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int e = e0 + u * G::kThreads;
-      if (e < nchunks && !s_abort) {
-        const int r = r0 + e / (kTileN / 4), c = e % (kTileN / 4);
-        if (m0 + r < M) *reinterpret_cast<float4 *>(C + (int64_t)(m0 + r) * No + n0 + c * 4) = acc[u];
+      for (int u = 0; u < 2; ++u) {
+        v[u] = acc[u];
+        sm[u] = (v[u].x + v[u].y) + (v[u].z + v[u].w);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) sm[u] += __shfl_xor_sync(DC_FULL_MASK, sm[u], o);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const float mean = sm[u] * (1.0f / kTileN);
+        v[u].x -= mean; v[u].y -= mean; v[u].z -= mean; v[u].w -= mean;
+        sq[u] = (v[u].x * v[u].x + v[u].y * v[u].y) + (v[u].z * v[u].z + v[u].w * v[u].w);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int u = 0; u < 2; ++u) sq[u] += __shfl_xor_sync(DC_FULL_MASK, sq[u], o);
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int e = e0 + u * G::kThreads;
+        const int r = r0 + e / (kTileN / 4);
+        if (e >= nchunks || m0 + r >= M) continue;
+        const float inv = rsqrtf(sq[u] * (1.0f / kTileN) + ln_eps);
+        const float x[4] = {v[u].x * inv, v[u].y * inv, v[u].z * inv, v[u].w * inv};
+        uint32_t h[4], l[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          h[k] = bf16_rn_bits(x[k]);
+          l[k] = bf16_rn_bits(x[k] - bf16_bits_to_float(h[k]));
+        }
+        const int64_t o = (int64_t)(m0 + r) * kTileN + c * 4;
+        *reinterpret_cast<uint2 *>(ln_hi + o) = make_uint2(h[0] | (h[1] << 16), h[2] | (h[3] << 16));
+        *reinterpret_cast<uint2 *>(ln_lo + o) = make_uint2(l[0] | (l[1] << 16), l[2] | (l[3] << 16));
+      }
+    } else {
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int e = e0 + u * G::kThreads;
+        const int r = r0 + e / (kTileN / 4);
+        if (e < nchunks && m0 + r < M)
+          *reinterpret_cast<float4 *>(C + (int64_t)(m0 + r) * No + n0 + c * 4) = acc[u];
       }
     }
   }
@@ -427,7 +481,8 @@ cudaError_t launch_proj_tc(const ProjJob &a, const CUtensorMap &a_hi, const CUte
   constexpr int MT = 2;
   using G = ProjGeom<MT>;
   auto bad = [&](const ProjJob &j) {
-    return j.No % kTileN != 0 || j.M < 0 || !j.table || !j.C ||
+    return j.No % kTileN != 0 || j.M < 0 || !j.table || (!j.C && !j.ln_hi) ||
+           (j.ln_hi && (j.No != kTileN || !j.ln_lo)) ||
            j.tiles != ((j.M + G::kTileM - 1) / G::kTileM) * (j.No / kTileN);
   };
   if (d % kTileK != 0 || splits < 1 || splits > kMaxSplits || (kSubM % splits) != 0 || bad(a) ||
