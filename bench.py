@@ -76,17 +76,25 @@ def peaks():
 
 
 # ------------------------------------------------------------------ per-stage algorithmic work
+PEAK_SOURCE = {"hbm": "hbm_gbs", "tensor": "bf16_tflops",
+               "alu": "152 SMs x 128 fp32 lanes x sm_max_mhz / 14 lane-ops per element"}
+
+
 def stage_model(w, pk):
     """stage -> (bound, unit, algorithmic amount per launch, peak).  Bytes are
     the bytes the step must move from HBM; flops are multiply-adds x 2."""
     N, B, V, d, K, r, H = w["N"], w["slots"] - 1, w["V"], w["d"], w["K"], w["r"], w["H"]
-    alu_peak = 152 * 128 * 2 * pk["sm_max_mhz"] * 1e6 / 1e12  # fp32 FMA lanes, TFLOP/s
+    # the pair scores evaluate w2 * GELU on the fp32 FMA pipe: 14 lane-operations
+    # per element (add, the degree-6 polynomial, four squarings, the products
+    # around the reciprocal), so its peak is the pipe's element rate
+    gelu_peak = 152 * 128 * pk["sm_max_mhz"] * 1e6 / 14 / 1e9  # Gelem/s
+    # the maps run their 128-deep products as three bf16 tensor-core passes
+    maps_flops = 3 * (2 * N * (B * r * r + (B - 1) * r * H) + 2 * N * B * K * (r * r + 2 * r * H))
     return {
         "topk": ("hbm", "GB/s", N * B * V * 2, pk["hbm_gbs"]),
         "proj": ("hbm", "GB/s", N * B * K * d * 2 + N * B * d * 2, pk["hbm_gbs"]),
-        "maps": ("alu", "TFLOP/s", 2 * N * (B * r * r + (B - 1) * r * H) + 2 * N * B * K * (r * r + 2 * r * H),
-                 alu_peak),
-        "pair_walk": ("alu", "TFLOP/s", 2 * N * (B - 1) * K * K * H, alu_peak),
+        "maps": ("tensor", "TFLOP/s", maps_flops, pk["bf16_tflops"]),
+        "pair_walk": ("alu", "Gelem/s", N * (B - 1) * K * K * H, gelu_peak),
     }
 
 
@@ -336,16 +344,21 @@ def run_ours(args):
         if bound == "hbm":
             ent.update(achieved=amount / avg_s / 1e9, unit="GB/s", peak=peak, frac=amount / avg_s / 1e9 / peak,
                        bytes=amount)
-        elif bound == "alu":
+        elif bound == "tensor":
             ent.update(achieved=amount / avg_s / 1e12, unit="TFLOP/s", peak=peak,
-                       frac=amount / avg_s / 1e12 / peak, flops=amount)
+                       frac=amount / avg_s / 1e12 / peak, flops=amount,
+                       note="latency-bound chain of short phases; tensor flops over the bf16 peak")
+        elif bound == "alu":
+            ent.update(achieved=amount / avg_s / 1e9, unit="Gelem/s", peak=peak,
+                       frac=amount / avg_s / 1e9 / peak, elements=amount,
+                       note="GELU elements over the fp32 FMA pipe's element rate (14 lane-ops each)")
         stages[name] = ent
     dom = max(stages, key=lambda k: stages[k]["us"])
     de = stages[dom]
     roofline = {"kernel": dom, "bound": de["bound"], "achieved": de.get("achieved"),
                 "peak": de.get("peak"), "unit": de.get("unit"), "frac": de.get("frac"),
                 "traffic": kernel_traffic(dom),
-                "peak_source": f"{pk['source']} ({'hbm_gbs' if de['bound'] == 'hbm' else 'fp32 FMA lanes x sm_max_mhz'})"}
+                "peak_source": f"{pk['source']} ({PEAK_SOURCE.get(de['bound'], 'none')})"}
 
     # whole step against the path's byte floor
     path_bytes = N * B * V * 2 + N * B * K * d * 2

@@ -528,7 +528,7 @@ __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int ti
     // U (or V) = W1 z + w_l l: quarter q takes outputs [64 q, 64 q + 64),
     // staged as fp32 boxes 2q, 2q+1 (outputs 0..127 in S, 128..255 in A)
     const float *wl = s_wl + q * 64;
-    const float lv = live ? __ldg(mp.topk_val + m) : 0.f;
+    const float lv = live ? __ldcg(mp.topk_val + m) : 0.f;  // the top-K's output: via L2
     bool ok2 = mbar_wait(smem_u32(q < 2 ? &bar_uv0 : &bar_uv1), 0, &s_abort, err) && !s_abort;
     ok2 = __all_sync(DC_FULL_MASK, ok2);
     tc_fence_after();

@@ -182,7 +182,7 @@ k_proj_tc(ProjJob job0, ProjJob job1, const __grid_constant__ CUtensorMap map0_h
       int row = 0;  // rows past M load table row 0; their results are never stored
       if (m < M) {
         if (ids) {
-          row = ids[m];
+          row = __ldcg(ids + m);  // the previous kernel's output: via L2
           if (row < 0 || row >= V) {
             atomicOr(err, kErrBadCandidateId);
             row = 0;

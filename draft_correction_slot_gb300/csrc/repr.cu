@@ -35,8 +35,10 @@ constexpr int H = 256;  // MLP hidden width
 // erf on x >= 0 is Hastings' rational approximation as given in Abramowitz
 // & Stegun, Handbook of Mathematical Functions (1964), formula 7.1.28:
 //   erf(x) = 1 - (1 + a1 x + a2 x^2 + ... + a6 x^6)^-16,  |error| <= 3e-7,
-// evaluated in fp32 (measured: |x erf(x) error| < 1e-6 for x in [0, 10]):
-// one polynomial, four squarings and one hardware reciprocal.
+// evaluated in fp32 (|x erf(x) error| < 1.1e-6 for x in [0, 10]): one
+// polynomial q, then q^-16 = 2^(-16 log2 q) by the hardware base-2 logarithm
+// and exponential (two special-function operations per element instead of
+// four squarings and a reciprocal on the FMA pipe, which bounds this loop).
 constexpr float kAs1 = 0.0705230784f, kAs2 = 0.0422820123f, kAs3 = 0.0092705272f;
 constexpr float kAs4 = 0.0001520143f, kAs5 = 0.0002765672f, kAs6 = 0.0000430638f;
 
@@ -66,9 +68,14 @@ __device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
   return d;
 }
 __device__ __forceinline__ f2_t f2_abs(f2_t a) { return a & 0x7FFFFFFF7FFFFFFFull; }
-__device__ __forceinline__ float rcp_approx(float x) {
+__device__ __forceinline__ float lg2_approx(float x) {
   float y;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
@@ -89,8 +96,8 @@ struct PairGeom {
   static constexpr int LD = K == 32 ? H + 2 : H + 4;
   static constexpr int RED = K * K + 1;            // partial-sum row stride
   static constexpr size_t pair_floats = 2 * (size_t)K * LD + H + 2 * K + (size_t)NS * RED;
-  // the walk reuses the first 2 kWalkMaxRows words
-  static constexpr size_t smem_floats = pair_floats > 2 * (size_t)kWalkMaxRows ? pair_floats : 2 * (size_t)kWalkMaxRows;
+  // the walk reuses the first 3 kWalkMaxRows words (best, gap, the request's ids)
+  static constexpr size_t smem_floats = pair_floats > 3 * (size_t)kWalkMaxRows ? pair_floats : 3 * (size_t)kWalkMaxRows;
 };
 
 template <int K>
@@ -109,18 +116,27 @@ k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
   float *red = dab + 2 * K;         // [NS][RED] partial sums
   const int np = blockIdx.x;        // n * (B-1) + p
   const int n = np / (B - 1), p = np - n * (B - 1);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   pdl_trigger();
   pdl_wait();  // U, V (and this call's outputs) belong to the previous kernel until here
   const int64_t ca = ((int64_t)n * B + p) * K;      // first candidate of slot p
   const int64_t cb = ca + K;                         // first candidate of slot p+1
   const float *Pp = P + ((int64_t)n * B + p) * H;  // P is indexed by draft slot
+  // Everything this call's earlier kernels wrote is read through L2 (ld.cg),
+  // never the non-coherent path: with the programmatic launch this kernel is
+  // already alive while they write it.
+  __shared__ float s_tv[32];  // l_{p+1}(b), read at the end; loaded now
+  const float bias = __ldg(b2);
+  if (tid < K) s_tv[tid] = __ldcg(topk_val + cb + tid);
 
+  // K * H / 4 is a multiple of 256: every thread has K / 4 chunks, all loads in flight together
+  static_assert((K * H / 4) % 256 == 0, "whole staging rounds");
+#pragma unroll
   for (int e4 = tid; e4 < K * H / 4; e4 += 256) {
     const int c = e4 / (H / 4), j = (e4 - c * (H / 4)) * 4;
-    const float4 u = __ldg(reinterpret_cast<const float4 *>(U + (ca + c) * H + j));
-    const float4 pp = __ldg(reinterpret_cast<const float4 *>(Pp + j));
-    const float4 v = __ldg(reinterpret_cast<const float4 *>(V + (cb + c) * H + j));
+    const float4 u = __ldcg(reinterpret_cast<const float4 *>(U + (ca + c) * H + j));
+    const float4 pp = __ldcg(reinterpret_cast<const float4 *>(Pp + j));
+    const float4 v = __ldcg(reinterpret_cast<const float4 *>(V + (cb + c) * H + j));
     float *x = pu + c * G::LD + j, *y = vs + c * G::LD + j;
     x[0] = (u.x + pp.x) * kInvSqrt2; x[1] = (u.y + pp.y) * kInvSqrt2;
     x[2] = (u.z + pp.z) * kInvSqrt2; x[3] = (u.w + pp.w) * kInvSqrt2;
@@ -129,21 +145,34 @@ k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
   w2s[tid] = w2[tid] * kInvSqrt2;
   __syncthreads();
 
-  // separable part: one warp per row, lane-strided, fixed order
-  for (int row = warp; row < 2 * K; row += 8) {
+  // separable part: 256 / 2K threads per row, each the hidden-unit pairs
+  // part, part + TPR, ... (neighbouring lanes read neighbouring pairs), the
+  // partial sums met by shuffles in a fixed order
+  {
+    constexpr int TPR = 256 / (2 * K);
+    static_assert(TPR * 2 * K == 256 && TPR <= 32, "whole rows per warp");
+    const int row = tid / TPR, part = tid - row * TPR;
     const float *xr = row < K ? pu + row * G::LD : vs + (row - K) * G::LD;
-    float d = 0.f;
+    float d0 = 0.f, d1 = 0.f;
 #pragma unroll
-    for (int j = lane; j < H; j += 32) d = fmaf(w2s[j], xr[j], d);
-    d = warp_sum(d);
-    if (lane == 0) dab[row] = d;
+    for (int i = 0; i < H / (2 * TPR); ++i) {
+      const int j = 2 * (part + TPR * i);
+      const float2 x = *reinterpret_cast<const float2 *>(xr + j);
+      const float2 wv = *reinterpret_cast<const float2 *>(w2s + j);
+      d0 = fmaf(wv.x, x.x, d0);
+      d1 = fmaf(wv.y, x.y, d1);
+    }
+    float d = d0 + d1;
+#pragma unroll
+    for (int o = TPR / 2; o > 0; o >>= 1) d += __shfl_xor_sync(DC_FULL_MASK, d, o);
+    if (part == 0) dab[row] = d;
   }
 
   const int blk = tid / G::NS, sl = tid - blk * G::NS;
   const int a0 = (blk / (K / G::T)) * G::T, b0 = (blk % (K / G::T)) * G::T;
   const f2_t c1 = f2_pack(kAs1, kAs1), c2 = f2_pack(kAs2, kAs2), c3 = f2_pack(kAs3, kAs3);
   const f2_t c4 = f2_pack(kAs4, kAs4), c5 = f2_pack(kAs5, kAs5), c6 = f2_pack(kAs6, kAs6);
-  const f2_t one = f2_pack(1.f, 1.f);
+  const f2_t one = f2_pack(1.f, 1.f), mone = f2_pack(-1.f, -1.f), m16 = f2_pack(-16.f, -16.f);
   f2_t acc[G::T][G::T];
 #pragma unroll
   for (int i = 0; i < G::T; ++i)
@@ -173,16 +202,14 @@ k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
         q = f2_fma(q, ax, c2);
         q = f2_fma(q, ax, c1);
         q = f2_fma(q, ax, one);
-        q = f2_mul(q, q);
-        q = f2_mul(q, q);
-        q = f2_mul(q, q);
-        q = f2_mul(q, q);
         float q0, q1;
         f2_unpack(q, q0, q1);
-        const f2_t nd = f2_pack(rcp_approx(-q0), rcp_approx(-q1));  // -(1 - erf(|x|))
+        f2_t lq = f2_mul(f2_pack(lg2_approx(q0), lg2_approx(q1)), m16);
+        float l0, l1;
+        f2_unpack(lq, l0, l1);
+        const f2_t rr = f2_pack(ex2_approx(l0), ex2_approx(l1));  // 1 - erf(|x|) = q^-16
         const f2_t t = f2_mul(w, ax);
-        // acc += t erf(|x|) = t - t (1 - erf(|x|))
-        acc[i][k] = f2_fma(t, nd, f2_add(acc[i][k], t));
+        acc[i][k] = f2_fma(t, f2_fma(rr, mone, one), acc[i][k]);
       }
   }
   float *rs = red + sl * G::RED;
@@ -196,13 +223,12 @@ k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
     }
   __syncthreads();
 
-  const float bias = b2[0];
   for (int e = tid; e < K * K; e += 256) {
     float sum = 0.f;
 #pragma unroll 8
     for (int s2 = 0; s2 < G::NS; ++s2) sum += red[s2 * G::RED + e];
     const int aa = e / K, bb = e - aa * K;
-    scores[(int64_t)np * K * K + e] = topk_val[cb + bb] + bias + (dab[aa] + dab[K + bb]) + sum;
+    scores[(int64_t)np * K * K + e] = s_tv[bb] + bias + (dab[aa] + dab[K + bb]) + sum;
   }
 
   // ---------------------------------------------------------------- step 5
@@ -236,7 +262,7 @@ k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
                              wk.beam_topm, s_best, s_gap, s_choice, fits ? s_sc : nullptr);
   } else {
     walk_verify_request<K>(sc, wk.topk_ids + slot0 * K, tg, B, wk.tokens + slot0, ch, mg, al, s_best, s_gap,
-                           s_choice);
+                           s_choice, reinterpret_cast<int *>(sm + 2 * kWalkMaxRows));
   }
   if (tid == 0) wk.req_count[n] = 0u;  // ready for the next call
 }

@@ -31,15 +31,21 @@ __device__ __forceinline__ uint32_t dynamic_smem_bytes() {
 }
 
 // scores: [(B-1)][K][K] of this request; ids: [B][K]; target: [B] or null.
-// s_best / s_gap: kWalkMaxRows entries; s_choice: 32.  Called by every thread
-// of the block, which must have 256 threads.
+// s_best / s_gap: kWalkMaxRows entries; s_choice: 32; s_ids: B K entries, or
+// null to read the chosen ids from global memory.  Called by every thread of
+// the block, which must have 256 threads.
 template <int K>
 __device__ __forceinline__ void walk_verify_request(const float *scores, const int32_t *ids,
                                                     const int32_t *target, int B, int32_t *tokens,
                                                     int32_t *choice, float *margin, int32_t *accept_len,
-                                                    int *s_best, float *s_gap, int *s_choice) {
+                                                    int *s_best, float *s_gap, int *s_choice,
+                                                    int *s_ids = nullptr) {
   const int tid = threadIdx.x;
   const int P = B - 1, rows = P * K;
+  // the request's candidate ids and target tokens load while the scores do
+  if (s_ids)
+    for (int e = tid; e < B * K; e += 256) s_ids[e] = __ldcg(ids + e);
+  const int tgt = (target && tid < B) ? target[tid] : 0;
   for (int r = tid; r < rows; r += 256) {
     float row[K];
     const float4 *src = reinterpret_cast<const float4 *>(scores + (int64_t)r * K);
@@ -77,13 +83,13 @@ __device__ __forceinline__ void walk_verify_request(const float *scores, const i
     int tok = 0;
     if (tid < B) {
       const int k = s_choice[tid];
-      tok = ids[tid * K + k];
+      tok = s_ids ? s_ids[tid * K + k] : __ldcg(ids + tid * K + k);
       tokens[tid] = tok;
       if (choice) choice[tid] = k;
       if (margin && tid < P) margin[tid] = s_gap[tid * K + k];
     }
     if (target) {
-      const bool mismatch = tid < B && tok != target[tid];
+      const bool mismatch = tid < B && tok != tgt;
       const unsigned mm = __ballot_sync(DC_FULL_MASK, mismatch);
       if (tid == 0) *accept_len = mm ? (__ffs(mm) - 1) : B;
     }
@@ -101,7 +107,7 @@ __device__ __forceinline__ void emit_request(const int32_t *ids, const int32_t *
     int tok = 0;
     if (tid < B) {
       const int k = s_choice[tid];
-      tok = ids[tid * K + k];
+      tok = __ldcg(ids + tid * K + k);
       tokens[tid] = tok;
       if (choice) choice[tid] = k;
       if (margin && tid < P) margin[tid] = s_gap[tid * K + s_choice[tid + 1]];
