@@ -440,14 +440,11 @@ __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int ti
     const int m = m0 + r;
     const bool live = m < M;
     const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16);
-    // Weights first (they do not depend on the previous kernel): gamma, beta
-    // and w_l to shared memory; this thread's slice of W_fuse[:, r:] (output
-    // go, inputs [32 gk, 32 gk + 32)) to registers.
-    if (tid < kR) {
-      s_gam[tid] = __ldg(mp.gamma + tid);
-      s_bet[tid] = __ldg(mp.beta + tid);
-    }
-    if (tid < kH) s_wl[tid] = __ldg((half == 0 ? mp.w_la : mp.w_lb) + tid);
+    // Weights first (they do not depend on the previous kernel), all loads in
+    // flight before any use: this thread's slice of W_fuse[:, r:] (output go,
+    // inputs [32 gk, 32 gk + 32)) to registers; gamma, beta and w_l reach
+    // shared memory after the dependency wait (the z phase reads them, behind
+    // several row barriers).
     const int gk = lane & 3, go = warp * 8 + (lane >> 2);
     float wfg[32];
     {
@@ -459,10 +456,17 @@ __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int ti
         wfg[4 * i] = v.x; wfg[4 * i + 1] = v.y; wfg[4 * i + 2] = v.z; wfg[4 * i + 3] = v.w;
       }
     }
+    const float gam = tid < kR ? __ldg(mp.gamma + tid) : 0.f, bet = tid < kR ? __ldg(mp.beta + tid) : 0.f;
+    const float wlv = tid < kH ? __ldg((half == 0 ? mp.w_la : mp.w_lb) + tid) : 0.f;
     float x[kQ];
     // W_ctx h of the tile's slots (slot_proj, from the previous kernel); one
     // warp per slot, four columns per lane
     pdl_wait();
+    if (tid < kR) {
+      s_gam[tid] = gam;
+      s_bet[tid] = bet;
+    }
+    if (tid < kH) s_wl[tid] = wlv;
     const int gs = slot0 + warp;
     float4 gx = make_float4(0.f, 0.f, 0.f, 0.f);
     if (warp < nslots && gs < mp.NB)

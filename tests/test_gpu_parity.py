@@ -136,6 +136,17 @@ def test_wide_k32_d5120(torch_cuda):
     report("wide", compare(prob, run_gpu(prob), prob.oracle()))
 
 
+def test_back_to_back_handles(torch_cuda):
+    """Two handles in turn, the second after the first is closed: its buffers
+    may take the first one's addresses, and every kernel must read this
+    call's results, not lines cached from the earlier handle's calls (the
+    kernels launched early read the previous kernel's outputs through L2)."""
+    first = Problem(36, N=2, V=20011, d=512, K=32, planted=8, boost=(8.0, 16.0))
+    report("handle-1", compare(first, run_gpu(first), first.oracle()))
+    second = Problem(5, N=2, V=V_QWEN, d=5120, K=32, planted=8, boost=(8.0, 16.0))
+    report("handle-2", compare(second, run_gpu(second), second.oracle()))
+
+
 def test_cosine_variant(torch_cuda):
     prob = Problem(6, N=2, V=V_QWEN, d=D_QWEN, variant=1, sigma=1.0)
     report("cosine", compare(prob, run_gpu(prob), prob.oracle()))
