@@ -104,7 +104,7 @@ def kernel_traffic(kernel: str):
     if not os.path.isdir(pdir):
         return None
     for fn in sorted(os.listdir(pdir)):
-        if not fn.endswith(".txt"):
+        if not fn.endswith((".txt", ".md")):
             continue
         txt = open(os.path.join(pdir, fn)).read()
         m = re.search(rf"^traffic_bytes_per_launch\[{kernel}\]:\s*([0-9.e+]+)\s+source_sha256:\s*(\w+)"
