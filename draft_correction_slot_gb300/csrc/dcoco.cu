@@ -320,15 +320,15 @@ void pack_mlp(const dcoco_weight_ptrs &w, std::vector<float> &buf, size_t off[8]
     buf[off[5] + j] = w.w2[j];
   }
   buf[off[6]] = w.b2[0];
-  // Thread `lane` of warp `wp` holds W_fuse[o][r + 32 g + e], o = 8 wp + lane / 4,
-  // g = lane % 4, e < 32, and loads it as 8 float4 steps; step i of the warp
-  // reads 512 contiguous bytes: element ((wp * 8 + i) * 32 + lane) * 4 + j
+  // Thread `lane` of warp `wp` holds W_fuse[o][r + 32 g + e], o = 32 (wp / 4)
+  // + lane, g = wp % 4, e < 32, and loads it as 8 float4 steps; step i of the
+  // warp reads 512 contiguous bytes: element ((wp * 8 + i) * 32 + lane) * 4 + j
   // is e = 4 i + j.
   for (int wp = 0; wp < r / 8; ++wp)
     for (int i = 0; i < 8; ++i)
       for (int lane = 0; lane < 32; ++lane)
         for (int j = 0; j < 4; ++j) {
-          const int o2 = 8 * wp + lane / 4, k = 32 * (lane % 4) + 4 * i + j;
+          const int o2 = 32 * (wp / 4) + lane, k = 32 * (wp % 4) + 4 * i + j;
           buf[off[7] + ((size_t)(wp * 8 + i) * 32 + lane) * 4 + j] = w.w_fuse[(size_t)o2 * 2 * r + r + k];
         }
 }

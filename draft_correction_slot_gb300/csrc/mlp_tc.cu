@@ -373,6 +373,7 @@ __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int ti
   __shared__ float s_gam[kR], s_bet[kR], s_wl[kH];         // gamma, beta, this half's w_l
   __shared__ __align__(16) float s_g[kMaxSlots][kGLd];     // LN0(W_ctx h) of the tile's slots
   __shared__ __align__(16) float s_gf[kMaxSlots][kR];      // Gf of the tile's slots
+  __shared__ float s_gq[2][4][kR];                         // Gf quarter partials, two slots in flight
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int m0 = tile * kRows;
@@ -444,8 +445,9 @@ __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int ti
     // flight before any use: this thread's slice of W_fuse[:, r:] (output go,
     // inputs [32 gk, 32 gk + 32)) to registers; gamma, beta and w_l reach
     // shared memory after the dependency wait (the z phase reads them, behind
-    // several row barriers).
-    const int gk = lane & 3, go = warp * 8 + (lane >> 2);
+    // several row barriers).  The input quarter gk is the same for the whole
+    // warp, so every read of g below is a broadcast.
+    const int gk = warp & 3, go = (warp >> 2) * 32 + lane;
     float wfg[32];
     {
       // packed so that each step of the warp reads 512 contiguous bytes
@@ -474,8 +476,10 @@ __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int ti
 
     // g = LN0(W_ctx h) of each slot (warp-wide sums), then
     // Gf[s][o] = sum_k W_fuse[o][r + k] g[s][k]: thread (go, gk) adds its
-    // 32-long slice for every slot, the four slices meet by shuffles.  This
-    // runs while the tensor cores compute the fuse product.
+    // 32-long slice for every slot; the four quarter sums meet in shared
+    // memory (two slots' buffers alternate, one row barrier per slot) and
+    // are added as (q0 + q1) + (q2 + q3).  This runs while the tensor cores
+    // compute the fuse product.
     if (warp < nslots) {
       const float mean = warp_sum((gx.x + gx.y) + (gx.z + gx.w)) * (1.0f / kR);
       const float4 dv = make_float4(gx.x - mean, gx.y - mean, gx.z - mean, gx.w - mean);
@@ -497,10 +501,10 @@ __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int ti
         a0 = fmaf(wfg[4 * i + 2], g4.z, a0);
         a1 = fmaf(wfg[4 * i + 3], g4.w, a1);
       }
-      float acc = a0 + a1;
-      acc += __shfl_xor_sync(DC_FULL_MASK, acc, 1);
-      acc += __shfl_xor_sync(DC_FULL_MASK, acc, 2);
-      if (gk == 0) s_gf[sl][go] = acc;
+      float(&gq)[4][kR] = s_gq[sl & 1];
+      gq[gk][go] = a0 + a1;
+      rows_sync();  // also orders the previous use of this buffer before the next write to it
+      if (gk == 0) s_gf[sl][go] = (gq[0][go] + gq[1][go]) + (gq[2][go] + gq[3][go]);
     }
 
     // z = gamma * LN0(y + Gf[slot]) + beta  (every row thread takes part: the
