@@ -100,8 +100,11 @@ struct PairGeom {
   static constexpr size_t smem_floats = pair_floats > 3 * (size_t)kWalkMaxRows ? pair_floats : 3 * (size_t)kWalkMaxRows;
 };
 
+// Three blocks per SM (the launch's residency cap): up to 85 registers a
+// thread, enough for the compiler to interleave several of a thread's 16
+// independent evaluations (64 serialised them and left the FMA pipe idle).
 template <int K>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 3)
 k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
              const float *__restrict__ P, const float *__restrict__ topk_val,
              const float *__restrict__ w2, const float *__restrict__ b2, int B,
@@ -178,7 +181,7 @@ k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
   for (int i = 0; i < G::T; ++i)
 #pragma unroll
     for (int k = 0; k < G::T; ++k) acc[i][k] = 0ull;
-#pragma unroll 1
+#pragma unroll 2
   for (int jj = 0; jj < G::JP; ++jj) {
     const int j = 2 * (sl + jj * G::NS);
     const float2 wv = *reinterpret_cast<const float2 *>(w2s + j);
