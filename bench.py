@@ -77,17 +77,17 @@ def peaks():
 
 # ------------------------------------------------------------------ per-stage algorithmic work
 PEAK_SOURCE = {"hbm": "hbm_gbs", "tensor": "bf16_tflops",
-               "alu": "152 SMs x 128 fp32 lanes x sm_max_mhz / 14 lane-ops per element"}
+               "alu": "152 SMs x 128 fp32 lanes x sm_max_mhz / 11 lane-ops per element"}
 
 
 def stage_model(w, pk):
     """stage -> (bound, unit, algorithmic amount per launch, peak).  Bytes are
     the bytes the step must move from HBM; flops are multiply-adds x 2."""
     N, B, V, d, K, r, H = w["N"], w["slots"] - 1, w["V"], w["d"], w["K"], w["r"], w["H"]
-    # the pair scores evaluate w2 * GELU on the fp32 FMA pipe: 14 lane-operations
-    # per element (add, the degree-6 polynomial, four squarings, the products
-    # around the reciprocal), so its peak is the pipe's element rate
-    gelu_peak = 152 * 128 * pk["sm_max_mhz"] * 1e6 / 14 / 1e9  # Gelem/s
+    # the pair scores evaluate w2 * GELU on the fp32 FMA pipe: 11 lane-operations
+    # per element (the add, the degree-6 polynomial, the scaling of log2 q, the
+    # products around 1 - erf), so its peak is the pipe's element rate
+    gelu_peak = 152 * 128 * pk["sm_max_mhz"] * 1e6 / 11 / 1e9  # Gelem/s
     # the maps run their 128-deep products as three bf16 tensor-core passes
     maps_flops = 3 * (2 * N * (B * r * r + (B - 1) * r * H) + 2 * N * B * K * (r * r + 2 * r * H))
     return {
@@ -351,7 +351,7 @@ def run_ours(args):
         elif bound == "alu":
             ent.update(achieved=amount / avg_s / 1e9, unit="Gelem/s", peak=peak,
                        frac=amount / avg_s / 1e9 / peak, elements=amount,
-                       note="GELU elements over the fp32 FMA pipe's element rate (14 lane-ops each)")
+                       note="GELU elements over the fp32 FMA pipe's element rate (11 lane-ops each)")
         stages[name] = ent
     dom = max(stages, key=lambda k: stages[k]["us"])
     de = stages[dom]
