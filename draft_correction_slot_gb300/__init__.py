@@ -61,6 +61,7 @@ class dcoco_outputs(C.Structure):
 
 EXPORTED = ("dcoco_version", "dcoco_status_string", "dcoco_create", "dcoco_weights_create",
             "dcoco_correct", "dcoco_correct_host", "dcoco_topk", "dcoco_get_device_status",
+            "dcoco_selftest_wait_timeout",
             "dcoco_weights_destroy", "dcoco_destroy", "dcoco_kernel_launches",
             "dcoco_stage_timing", "dcoco_stage_read", "dcoco_stage_name", "dcoco_topk_noalloc",
             "dcoco_verify_stochastic")
@@ -87,6 +88,7 @@ def _load():
     L.dcoco_topk_noalloc.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_int64,
                                      C.c_void_p, C.c_void_p, C.c_void_p]
     L.dcoco_get_device_status.argtypes = [C.c_void_p]
+    L.dcoco_selftest_wait_timeout.argtypes = [C.c_void_p, C.c_longlong, C.c_void_p]
     L.dcoco_weights_destroy.argtypes = [C.c_void_p]
     L.dcoco_weights_destroy.restype = None
     L.dcoco_destroy.argtypes = [C.c_void_p]
@@ -235,6 +237,13 @@ def dcoco_topk_noalloc(batch: int, slots: int, vocab: int, topk: int, logits, to
 
 def dcoco_get_device_status(handle) -> int:
     return _lib.dcoco_get_device_status(handle)
+
+
+def dcoco_selftest_wait_timeout(handle, limit_ns: int, stream: int = 0) -> None:
+    """One block waits on an mbarrier nothing completes, with the kernels' own
+    bounded wait (limit_ns); the handle's device status then reads DCOCO_EDEVICE."""
+    _check(_lib.dcoco_selftest_wait_timeout(handle, int(limit_ns), C.c_void_p(stream)),
+           "dcoco_selftest_wait_timeout")
 
 
 def dcoco_weights_destroy(weights) -> None:

@@ -672,6 +672,14 @@ int dcoco_verify_stochastic(dcoco_handle *h, int batch, const void *target_logit
       next_token, st));
 }
 
+int dcoco_selftest_wait_timeout(dcoco_handle *h, long long limit_ns, void *stream) {
+  if (!h || limit_ns < 1000 || limit_ns > 1000000000LL) return DCOCO_EINVAL;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  h->last_stream = st;
+  ++h->launches;
+  return cuda_status(dc::launch_wait_timeout((unsigned long long)limit_ns, h->ws.err, st));
+}
+
 int dcoco_get_device_status(dcoco_handle *h) {
   if (!h) return DCOCO_EINVAL;
   if (cudaStreamSynchronize(h->last_stream) != cudaSuccess) return DCOCO_ECUDA;

@@ -173,4 +173,8 @@ cudaError_t launch_walk_verify(int K, const float *scores, const int32_t *topk_i
                                int32_t *choice, float *margin, int32_t *accept_len,
                                int path_rule, int beam_width, int beam_topm, cudaStream_t st);
 
+// One CTA waits (tc::mbar_wait, limit_ns) on an mbarrier nothing completes:
+// the wait expires and ORs kErrTimeout into *err.
+cudaError_t launch_wait_timeout(unsigned long long limit_ns, int *err, cudaStream_t st);
+
 }  // namespace dc

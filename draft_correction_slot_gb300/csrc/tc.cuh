@@ -44,17 +44,18 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for phase `parity` of `bar`; false on timeout or when another role
-// aborted (then `abort` is set and `err` records kErrTimeout).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort,
-                                          int *err) {
+// Wait for phase `parity` of `bar`; false on timeout (after limit_ns) or
+// when another role aborted (then `abort` is set and `err` records
+// kErrTimeout).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort, int *err,
+                                          unsigned long long limit_ns = kWaitNs) {
   if (mbar_try(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try(bar, parity)) return true;
     if ((it & 63u) == 0u) {
       if (*abort) return false;
-      if (global_ns() - t0 > kWaitNs) {
+      if (global_ns() - t0 > limit_ns) {
         *abort = 1;
         atomicOr(err, ::dc::kErrTimeout);
         return false;

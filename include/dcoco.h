@@ -248,9 +248,19 @@ int dcoco_topk_noalloc(int batch, int slots, int vocab, int topk, const void *lo
                        void *stream);
 
 /* Synchronise the handle's last stream and return DCOCO_OK, or DCOCO_EDEVICE
- * if a kernel recorded bad data (e.g. a candidate id outside [0,V)) since the
- * last call to this function (the flag is then cleared), or ECUDA. */
+ * if a kernel recorded bad data (e.g. a candidate id outside [0,V)) or a
+ * bounded wait that expired (the kernel then skips its stores and returns)
+ * since the last call to this function (the flag is then cleared), or ECUDA. */
 int dcoco_get_device_status(dcoco_handle *h);
+
+/* Self-test of the failure path shared by every bounded wait in the kernels:
+ * launches, on `stream`, one block that waits (with the kernels' own wait
+ * routine) on an mbarrier that nothing completes, giving up after limit_ns
+ * nanoseconds (1e3 .. 1e9).  The handle's device status word then records
+ * the timeout: dcoco_get_device_status returns DCOCO_EDEVICE once, and the
+ * context stays usable.  No fault, no trap, no hang.  Errors: EINVAL (NULL
+ * handle, limit out of range), ECUDA (launch). */
+int dcoco_selftest_wait_timeout(dcoco_handle *h, long long limit_ns, void *stream);
 
 /* Tracing: number of kernels this handle has launched since it was created
  * (every launch of dcoco_correct / dcoco_correct_host / dcoco_topk counts).

@@ -71,6 +71,8 @@ def test_null_arguments_rejected(dc):
     lib.dcoco_topk.argtypes = [C.c_void_p, C.c_int, C.c_void_p, C.c_int64, C.c_void_p, C.c_void_p,
                                C.c_void_p]
     assert lib.dcoco_topk(None, 1, None, 0, None, None, None) == -1
+    lib.dcoco_selftest_wait_timeout.argtypes = [C.c_void_p, C.c_longlong, C.c_void_p]
+    assert lib.dcoco_selftest_wait_timeout(None, 1_000_000, None) == -1
     lib.dcoco_destroy.argtypes = [C.c_void_p]
     lib.dcoco_destroy(None)  # NULL is allowed
     lib.dcoco_weights_destroy.argtypes = [C.c_void_p]

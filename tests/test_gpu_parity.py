@@ -147,6 +147,27 @@ def test_back_to_back_handles(torch_cuda):
     report("handle-2", compare(second, run_gpu(second), second.oracle()))
 
 
+def test_bounded_wait_expires_into_device_status(torch_cuda):
+    """The kernels' bounded wait, on an mbarrier nothing completes, gives up
+    after its limit: the status word reads DCOCO_EDEVICE once, is cleared by
+    the read, and the context keeps working (a parity run on the same handle)."""
+    import torch
+    import draft_correction_slot_gb300 as dc
+    prob = Problem(21, N=1, V=4099, d=128)
+    corr = dc.Corrector({k: torch.from_numpy(v) for k, v in prob.w.items()}, prob.V, prob.d, prob.slots,
+                        prob.K, max_batch=1)
+    try:
+        assert corr.status() == dc.DCOCO_OK
+        dc.dcoco_selftest_wait_timeout(corr.handle, 2_000_000, torch.cuda.current_stream().cuda_stream)
+        assert corr.status() == dc.DCOCO_EDEVICE
+        assert corr.status() == dc.DCOCO_OK
+        report("after-timeout", compare(prob, run_gpu(prob, corr=corr), prob.oracle()))
+        with pytest.raises(dc.DcocoError):
+            dc.dcoco_selftest_wait_timeout(corr.handle, 10, 0)  # below the 1 us floor
+    finally:
+        corr.close()
+
+
 def test_cosine_variant(torch_cuda):
     prob = Problem(6, N=2, V=V_QWEN, d=D_QWEN, variant=1, sigma=1.0)
     report("cosine", compare(prob, run_gpu(prob), prob.oracle()))
