@@ -17,7 +17,9 @@
 // then finds the first rejection (u_j >= q_j(y_j)), and draws the corrected or
 // bonus token by inverse transform in vocabulary order: a scan over the row's
 // chunk weights picks the chunk, a scan inside the chunk picks the token.
-// fp32 throughout (CUDA's __expf / __logf).
+// fp32 throughout: the row pass takes exp(x - m) as 2^(x log2 e - m log2 e)
+// (one fma and the hardware ex2 per token, four partial sums, the next
+// chunk's loads in flight); the rest uses CUDA's __expf / __logf.
 #include <cstdint>
 
 #include "common.cuh"
@@ -29,6 +31,12 @@ namespace {
 constexpr int kThreads = 256, kWarps = kThreads / 32;
 constexpr int kChunk = 1024;  // tokens per chunk statistic (128 vectors of 8)
 
+constexpr float kLog2e = 1.44269504088896340736f;
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
@@ -64,8 +72,8 @@ __device__ __forceinline__ float block_scan(float v, float *s_warp, float *total
   return before + x;
 }
 
-// One exp per token (the special-function unit) and a few ALU operations per
-// token bound the row pass, not the loads.
+// The row pass: one fma, one ex2 and a few ALU operations per token; the
+// next chunk's loads are issued before the current chunk's arithmetic.
 __global__ void __launch_bounds__(kThreads)
 k_verify_stochastic(const uint16_t *__restrict__ target, int64_t stride, int V, int B,
                     const int32_t *__restrict__ tokens, const float *__restrict__ u_acc,
@@ -83,9 +91,8 @@ k_verify_stochastic(const uint16_t *__restrict__ target, int64_t stride, int V, 
 
   // ---------------------------------------------------------------- row statistics
   float wm = -INFINITY, ws = 0.f;  // this warp's running (max, sum)
-  for (int c = warp; c < nchunks; c += kWarps) {
+  auto load_chunk = [&](int c, uint32_t (&wr)[16]) {
     const int v0 = c * kChunk;
-    float xv[32];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int t0 = v0 + (q * 32 + lane) * 8;  // first token of this lane's vector
@@ -99,21 +106,34 @@ k_verify_stochastic(const uint16_t *__restrict__ target, int64_t stride, int V, 
         w4 = make_uint4(e[0] | (uint32_t)e[1] << 16, e[2] | (uint32_t)e[3] << 16, e[4] | (uint32_t)e[5] << 16,
                         e[6] | (uint32_t)e[7] << 16);
       }
-      const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        xv[q * 8 + 2 * k] = bf16_lo(wv[k]);
-        xv[q * 8 + 2 * k + 1] = bf16_hi(wv[k]);
-      }
+      wr[4 * q] = w4.x; wr[4 * q + 1] = w4.y; wr[4 * q + 2] = w4.z; wr[4 * q + 3] = w4.w;
     }
-    float m = xv[0];
+  };
+  uint32_t wnext[16];
+  if (warp < nchunks) load_chunk(warp, wnext);
+  for (int c = warp; c < nchunks; c += kWarps) {
+    uint32_t wr[16];  // this lane's 32 tokens as packed bf16 pairs, in token order
 #pragma unroll
-    for (int k = 1; k < 32; ++k) m = fmaxf(m, xv[k]);
-    m = warp_max(m);
+    for (int k = 0; k < 16; ++k) wr[k] = wnext[k];
+    if (c + kWarps < nchunks) load_chunk(c + kWarps, wnext);  // in flight during this chunk's arithmetic
+    // the chunk maximum on the packed pairs (exact), then over the warp
+    uint32_t mx = bf16x2_max(wr[0], wr[1]);
+#pragma unroll
+    for (int k = 2; k < 16; ++k) mx = bf16x2_max(mx, wr[k]);
+    float m = warp_max(fmaxf(bf16_lo(mx), bf16_hi(mx)));
     float s = 0.f;
-    if (m != -INFINITY)
+    if (m != -INFINITY) {
+      // exp(x - m) = 2^(x log2 e - m log2 e): one fma and one ex2 per token,
+      // four partial sums
+      const float mb = -m * kLog2e;
+      float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int k = 0; k < 32; ++k) s += __expf(xv[k] - m);
+      for (int k = 0; k < 16; ++k) {
+        s4[(2 * k) & 3] += ex2_approx(fmaf(bf16_lo(wr[k]), kLog2e, mb));
+        s4[(2 * k + 1) & 3] += ex2_approx(fmaf(bf16_hi(wr[k]), kLog2e, mb));
+      }
+      s = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+    }
     s = warp_sum(s);
     if (lane == 0) {
       chunk_m[(int64_t)row * nchunks + c] = m;
