@@ -323,6 +323,13 @@ __device__ __forceinline__ void radix_digit(const int *hist, int rank, int lane,
 }
 
 // Merge (m, s) pairs, s a sum of exp(x - m) (m = -inf: empty).
+constexpr float kLog2e = 1.44269504088896340736f;
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void lse_merge(float &m, float &s, float m2, float s2) {
   const float mm = fmaxf(m, m2);
   if (mm == -INFINITY) return;
@@ -385,7 +392,9 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
   }
 
   // ---------------------------------------------------------------- pass 1: stream
-  float lm = -INFINITY, ls = 0.f;  // kLse: this lane's running (maximum, sum of exp)
+  // kLse: this lane's running maximum and its sum of exp(x - lm), kept as two
+  // partial sums; nb = -lm log2 e, so exp(x - lm) = 2^(fma(x, log2 e, nb))
+  float lm = -INFINITY, ls = 0.f, ls2 = 0.f, nb = 0.f;
   {
     uint4 a[kU], b[kU];
     static_assert(kStep == 2 * kGroup && kU == 4, "one step = two groups of 64 vectors");
@@ -402,14 +411,19 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
           if (kLse) {
             const float vm = bf16_bits_to_float(m);
             if (vm > lm) {
-              ls = lm == -INFINITY ? 0.f : ls * __expf(lm - vm);
+              const float f = lm == -INFINITY ? 0.f : __expf(lm - vm);
+              ls *= f;
+              ls2 *= f;
               lm = vm;
+              nb = -vm * kLog2e;
             }
             if (lm != -INFINITY) {
               const uint32_t wd[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
-              for (int h = 0; h < 4; ++h)
-                ls += __expf(bf16_bits_to_float(wd[h] & 0xFFFFu) - lm) + __expf(bf16_bits_to_float(wd[h] >> 16) - lm);
+              for (int h = 0; h < 4; ++h) {
+                ls += ex2_approx(fmaf(bf16_bits_to_float(wd[h] & 0xFFFFu), kLog2e, nb));
+                ls2 += ex2_approx(fmaf(bf16_bits_to_float(wd[h] >> 16), kLog2e, nb));
+              }
             }
           }
         }
@@ -432,6 +446,7 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
     }
   }
   if (kLse) {
+    ls += ls2;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       const float om = __shfl_xor_sync(DC_FULL_MASK, lm, off), os = __shfl_xor_sync(DC_FULL_MASK, ls, off);
