@@ -181,7 +181,7 @@ k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
   for (int i = 0; i < G::T; ++i)
 #pragma unroll
     for (int k = 0; k < G::T; ++k) acc[i][k] = 0ull;
-#pragma unroll 2
+#pragma unroll 4
   for (int jj = 0; jj < G::JP; ++jj) {
     const int j = 2 * (sl + jj * G::NS);
     const float2 wv = *reinterpret_cast<const float2 *>(w2s + j);
