@@ -135,9 +135,10 @@ void carve_workspace(Carver &c, const dcoco_config &cfg, int B, int topk_segment
   ws.ids = c.take<int32_t>(cands);
   ws.vals = c.take<float>(cands);
   ws.slot_proj = c.take<float>(rows * 3 * kR);
-  ws.cand_proj = c.take<float>(cands * 2 * kR);
-  ws.b_hi = c.take<uint16_t>(cands * kR);
-  ws.b_lo = c.take<uint16_t>(cands * kR);
+  // the candidate rows: LN0'd bf16 hi/lo (MLP variant) or fp32 [2r] (cosine)
+  ws.cand_proj = c.take<float>(cfg.variant == 0 ? 0 : cands * 2 * kR);
+  ws.b_hi = c.take<uint16_t>(cfg.variant == 0 ? cands * kR : 0);
+  ws.b_lo = c.take<uint16_t>(cfg.variant == 0 ? cands * kR : 0);
   ws.P = c.take<float>(N * B * kH);
   ws.U = c.take<float>(cands * kH);
   ws.V = c.take<float>(cands * kH);
