@@ -11,7 +11,9 @@
 //   * Pass 1 -- stream: each warp reads a contiguous slice of the segment,
 //     4 coalesced 16-byte vectors per lane per iteration with the next ones in
 //     flight, and stores each vector's maximum (packed bf16x2 max) in shared
-//     memory.  Nothing else happens while streaming.
+//     memory.  Nothing else happens while streaming, except that with the
+//     candidate features each lane also keeps a running log-sum-exp
+//     (exp(x - m) as 2^(fma(x, log2 e, -m log2 e)), two partial sums).
 //   * Pass 2 -- bound: T = the K-th largest maximum of the groups of 64
 //     vectors.  K groups each hold an element >= T, so the segment's K-th
 //     value is >= T: every element of the segment's top-K lies in a vector
