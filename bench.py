@@ -78,6 +78,14 @@ def peaks():
 # ------------------------------------------------------------------ per-stage algorithmic work
 NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal
 
+def algorithmic_bytes(w) -> int:
+    """Bytes one call must move from HBM: the draft slots' logits (15 V bf16 per
+    request) and the gathered candidate embedding rows (15 K d bf16 per
+    request); hidden states and weights are not counted."""
+    B = w["slots"] - 1
+    return w["N"] * B * w["V"] * 2 + w["N"] * B * w["K"] * w["d"] * 2
+
+
 PEAK_SOURCE = {"hbm": "hbm_gbs", "tensor": "bf16_tflops",
                "alu": "152 SMs x 128 fp32 lanes x sm_max_mhz / 11 lane-ops per element"}
 
@@ -363,7 +371,7 @@ def run_ours(args):
                 "peak_source": f"{pk['source']} ({PEAK_SOURCE.get(de['bound'], 'none')})"}
 
     # whole step against the path's byte floor
-    path_bytes = N * B * V * 2 + N * B * K * d * 2
+    path_bytes = algorithmic_bytes(w)
     step_s = total_ms / args.steps / 1e3
     value = world * N / step_s
 
