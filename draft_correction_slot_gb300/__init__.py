@@ -64,7 +64,7 @@ EXPORTED = ("dcoco_version", "dcoco_status_string", "dcoco_create", "dcoco_weigh
             "dcoco_selftest_wait_timeout",
             "dcoco_weights_destroy", "dcoco_destroy", "dcoco_kernel_launches",
             "dcoco_stage_timing", "dcoco_stage_read", "dcoco_stage_name", "dcoco_topk_noalloc",
-            "dcoco_verify_stochastic")
+            "dcoco_topk_noalloc_plan", "dcoco_verify_stochastic", "dcoco_host_range_covers")
 
 
 def _load():
@@ -87,6 +87,9 @@ def _load():
                              C.c_void_p]
     L.dcoco_topk_noalloc.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_void_p, C.c_int64,
                                      C.c_void_p, C.c_void_p, C.c_void_p]
+    L.dcoco_topk_noalloc_plan.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.POINTER(C.c_int),
+                                          C.POINTER(C.c_int)]
+    L.dcoco_host_range_covers.argtypes = [C.c_uint64, C.c_uint64, C.c_uint64, C.c_uint64]
     L.dcoco_get_device_status.argtypes = [C.c_void_p]
     L.dcoco_selftest_wait_timeout.argtypes = [C.c_void_p, C.c_longlong, C.c_void_p]
     L.dcoco_weights_destroy.argtypes = [C.c_void_p]
@@ -233,6 +236,19 @@ def dcoco_topk_noalloc(batch: int, slots: int, vocab: int, topk: int, logits, to
     stride = logits_slot_stride if logits_slot_stride is not None else logits.shape[-1]
     _check(_lib.dcoco_topk_noalloc(batch, slots, vocab, topk, _ptr(logits), int(stride), _ptr(topk_ids),
                                    _ptr(topk_val), _stream(stream)), "dcoco_topk_noalloc")
+
+
+def dcoco_topk_noalloc_plan(batch: int, slots: int, vocab: int, topk: int) -> tuple[int, int]:
+    """-> (segments per row dcoco_topk_noalloc would use, segments dcoco_topk would use)."""
+    seg, planned = C.c_int(), C.c_int()
+    _check(_lib.dcoco_topk_noalloc_plan(batch, slots, vocab, topk, C.byref(seg), C.byref(planned)),
+           "dcoco_topk_noalloc_plan")
+    return seg.value, planned.value
+
+
+def dcoco_host_range_covers(range_start: int, range_size: int, ptr: int, nbytes: int) -> bool:
+    """Whether [ptr, ptr + nbytes) lies inside the range (the host entry's in-place test)."""
+    return bool(_lib.dcoco_host_range_covers(range_start, range_size, ptr, nbytes))
 
 
 def dcoco_get_device_status(handle) -> int:

@@ -1,5 +1,6 @@
 // dcoco.cu -- C ABI: argument validation, workspace, weight packing and the
 // launch sequence of the correction path (declared in include/dcoco.h).
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdlib>
@@ -201,6 +202,36 @@ int validate_call(const dcoco_handle *h, const dcoco_weights *w, int batch, cons
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? DCOCO_OK : DCOCO_ECUDA; }
 
+// The base address and size of the allocation (or registered range) that
+// holds `p`, from the driver's pointer attributes.  False when the driver
+// does not know the pointer.
+bool host_range_of(const void *p, uint64_t *start, uint64_t *size) {
+  typedef CUresult (*PtrAttrFn)(void *, CUpointer_attribute, CUdeviceptr);
+  static PtrAttrFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void *f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuPointerGetAttribute", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PtrAttrFn>(f);
+    else
+      cudaGetLastError();
+  }
+  if (!fn) return false;
+  CUdeviceptr base = 0;
+  size_t n = 0;
+  const CUdeviceptr dp = (CUdeviceptr) reinterpret_cast<uintptr_t>(p);
+  if (fn(&base, CU_POINTER_ATTRIBUTE_RANGE_START_ADDR, dp) != CUDA_SUCCESS ||
+      fn(&n, CU_POINTER_ATTRIBUTE_RANGE_SIZE, dp) != CUDA_SUCCESS)
+    return false;
+  *start = (uint64_t)base;
+  *size = (uint64_t)n;
+  return true;
+}
+
 // Successors each beam keeps (0 in the config means all K).
 inline int beam_topm(const dcoco_config &cfg) { return cfg.beam_topm > 0 ? cfg.beam_topm : cfg.topk; }
 
@@ -339,6 +370,12 @@ void pack_mlp(const dcoco_weight_ptrs &w, std::vector<float> &buf, size_t off[8]
 extern "C" {
 
 int dcoco_version(void) { return 100; }
+
+int dcoco_host_range_covers(uint64_t range_start, uint64_t range_size, uint64_t ptr, uint64_t bytes) {
+  if (range_size == 0 || ptr < range_start) return 0;
+  const uint64_t off = ptr - range_start;
+  return off <= range_size && bytes <= range_size - off ? 1 : 0;
+}
 
 const char *dcoco_status_string(int s) {
   switch (s) {
@@ -590,9 +627,15 @@ int dcoco_correct_host(dcoco_handle *h, const dcoco_weights *w, int batch, const
   // and targets (small) are copied.
   const void *logits_dev = nullptr;
   {
+    // In place only if the whole extent the top-K reads lies inside one
+    // page-locked range (a caller may have registered part of a buffer).
+    const uint64_t extent = (uint64_t)((rows - 1) * in->logits_slot_stride + cfg.vocab) * sizeof(uint16_t);
     cudaPointerAttributes pa;
+    uint64_t r0 = 0, rsize = 0;
     if (cudaPointerGetAttributes(&pa, in->logits) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
-        pa.devicePointer && aligned16(pa.devicePointer) && in->logits_slot_stride % 8 == 0)
+        pa.devicePointer && aligned16(pa.devicePointer) && in->logits_slot_stride % 8 == 0 &&
+        host_range_of(in->logits, &r0, &rsize) &&
+        dcoco_host_range_covers(r0, rsize, reinterpret_cast<uintptr_t>(in->logits), extent))
       logits_dev = pa.devicePointer;
     cudaGetLastError();  // an unregistered pointer is not an error here
   }
@@ -650,9 +693,12 @@ int dcoco_topk(dcoco_handle *h, int batch, const void *logits, int64_t stride, i
   h->last_stream = st;
   ++h->launches;
   const dc::TopkPlan plan = dc::topk_plan(h->cfg.vocab, batch * h->B, h->topk_wave);
+  // Launched without programmatic overlap: the kernel streams the logits
+  // before its dependency wait, so it must not start while the caller's
+  // previous kernel on the stream may still be writing them.
   return cuda_status(dc::launch_topk(h->cfg.topk, static_cast<const uint16_t *>(logits), stride,
                                      h->cfg.slots, batch, h->cfg.vocab, plan, h->ws.part,
-                                     h->ws.row_count, topk_ids, topk_val, st, true));
+                                     h->ws.row_count, topk_ids, topk_val, st, false));
 }
 
 int dcoco_verify_stochastic(dcoco_handle *h, int batch, const void *target_logits, int64_t target_stride,

@@ -11,6 +11,7 @@
 // GPU that loads the library holds until the process exits.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/dcoco.h"
@@ -31,8 +32,13 @@ static __device__ __align__(256) unsigned char g_topk_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
-unsigned char *g_scratch[kMaxDevices];  // device address of g_topk_scratch, per device
-int g_wave[kMaxDevices][3];             // resident top-K CTAs per device, K = 8, 16, 32
+// Per device: the top-K occupancy (resident CTAs on the device for K = 8,
+// 16, 32), then the device address of g_topk_scratch.  The address is
+// published with release order after the occupancy is written, and read
+// with acquire order, so a thread that sees the address also sees the
+// occupancy.
+int g_wave[kMaxDevices][3];
+std::atomic<unsigned char *> g_scratch[kMaxDevices];
 
 int k_index(int K) { return K == 8 ? 0 : (K == 16 ? 1 : 2); }
 
@@ -40,7 +46,7 @@ int k_index(int K) { return K == 8 ? 0 : (K == 16 ? 1 : 2); }
 // the top-K occupancy.  Returns DCOCO_OK or DCOCO_ECUDA.
 int setup_device(int dev) {
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (g_scratch[dev]) return DCOCO_OK;
+  if (g_scratch[dev].load(std::memory_order_acquire)) return DCOCO_OK;
   void *p = nullptr;
   if (cudaGetSymbolAddress(&p, g_topk_scratch) != cudaSuccess || p == nullptr) {
     cudaGetLastError();
@@ -53,40 +59,79 @@ int setup_device(int dev) {
   }
   const int ks[3] = {8, 16, 32};
   for (int j = 0; j < 3; ++j) g_wave[dev][j] = sms * dc::topk_occupancy(ks[j]);
-  g_scratch[dev] = static_cast<unsigned char *>(p);
+  g_scratch[dev].store(static_cast<unsigned char *>(p), std::memory_order_release);
+  return DCOCO_OK;
+}
+
+// Argument checks that need no CUDA call.  The segment lists of a call take
+// rows * topk * segments entries of the fixed list area; a call whose rows
+// do not fit even at the fewest segments the vocabulary allows is rejected.
+int check_args(int batch, int slots, int vocab, int topk) {
+  if (slots < 3 || slots > 32 || (topk != 8 && topk != 16 && topk != 32)) return DCOCO_EUNSUPPORTED;
+  if (vocab < topk || vocab > (1 << 20)) return DCOCO_EINVAL;
+  if (batch < 0 || (long long)batch * (slots - 1) > kMaxRows) return DCOCO_EBATCH;
+  if (batch == 0) return DCOCO_OK;
+  const long long fit = (long long)kPartEntries / ((long long)batch * (slots - 1) * topk);
+  if (fit < dc::topk_min_segments(vocab)) return DCOCO_EBATCH;
+  return DCOCO_OK;
+}
+
+// The segment plan of a call on the current device: the plan the handle-based
+// entry would take, limited to what the fixed list area holds.
+int noalloc_plan(int batch, int slots, int vocab, int topk, dc::TopkPlan *plan, int *planned) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DCOCO_ECUDA;
+  if (!g_scratch[dev].load(std::memory_order_acquire)) {
+    const int rc = setup_device(dev);
+    if (rc != DCOCO_OK) return rc;
+  }
+  const int rows = batch * (slots - 1);
+  *plan = dc::topk_plan(vocab, rows, g_wave[dev][k_index(topk)]);
+  *planned = plan->nchunks;
+  const long long fit = (long long)kPartEntries / ((long long)rows * topk);
+  if (plan->nchunks > fit) {
+    plan->nchunks = (int)fit;
+    const int nvec = vocab >> 3;
+    plan->chunk_vecs = (nvec + plan->nchunks - 1) / plan->nchunks;
+  }
   return DCOCO_OK;
 }
 
 }  // namespace
 
+extern "C" int dcoco_topk_noalloc_plan(int batch, int slots, int vocab, int topk, int *segments,
+                                       int *planned_segments) {
+  if (!segments || !planned_segments) return DCOCO_EINVAL;
+  int rc = check_args(batch, slots, vocab, topk);
+  if (rc != DCOCO_OK) return rc;
+  if (batch == 0) {
+    *segments = *planned_segments = 0;
+    return DCOCO_OK;
+  }
+  dc::TopkPlan plan;
+  rc = noalloc_plan(batch, slots, vocab, topk, &plan, planned_segments);
+  if (rc != DCOCO_OK) return rc;
+  *segments = plan.nchunks;
+  return DCOCO_OK;
+}
+
 extern "C" int dcoco_topk_noalloc(int batch, int slots, int vocab, int topk, const void *logits,
                                   int64_t logits_slot_stride, int32_t *topk_ids, float *topk_val,
                                   void *stream) {
-  if (slots < 3 || slots > 32 || (topk != 8 && topk != 16 && topk != 32)) return DCOCO_EUNSUPPORTED;
-  if (vocab < topk || vocab > (1 << 20)) return DCOCO_EINVAL;
-  if (batch < 0 || (long long)batch * (slots - 1) > kMaxRows) return DCOCO_EBATCH;
-  if (batch == 0) return DCOCO_OK;
+  int rc = check_args(batch, slots, vocab, topk);
+  if (rc != DCOCO_OK || batch == 0) return rc;
   if (!logits || !topk_ids || !topk_val) return DCOCO_EINVAL;
   if (logits_slot_stride < vocab || logits_slot_stride % 8 != 0 ||
       (reinterpret_cast<uintptr_t>(logits) & 15u) != 0)
     return DCOCO_EINVAL;
+  dc::TopkPlan plan;
+  int planned = 0;
+  rc = noalloc_plan(batch, slots, vocab, topk, &plan, &planned);
+  if (rc != DCOCO_OK) return rc;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DCOCO_ECUDA;
-  if (!g_scratch[dev]) {
-    const int rc = setup_device(dev);
-    if (rc != DCOCO_OK) return rc;
-  }
-  unsigned char *base = g_scratch[dev];
+  if (cudaGetDevice(&dev) != cudaSuccess) return DCOCO_ECUDA;
+  unsigned char *base = g_scratch[dev].load(std::memory_order_acquire);
   const int rows = batch * (slots - 1);
-  // as many row segments as the plan wants and the fixed list area holds
-  dc::TopkPlan plan = dc::topk_plan(vocab, rows, g_wave[dev][k_index(topk)]);
-  const long long fit = (long long)kPartEntries / ((long long)rows * topk);
-  if (fit < dc::topk_min_segments(vocab)) return DCOCO_EBATCH;  // lists would not fit the scratch
-  if (plan.nchunks > fit) {
-    plan.nchunks = (int)fit;
-    const int nvec = vocab >> 3;
-    plan.chunk_vecs = (nvec + plan.nchunks - 1) / plan.nchunks;
-  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   unsigned *row_count = reinterpret_cast<unsigned *>(base + kCountOff);
   unsigned long long *part = reinterpret_cast<unsigned long long *>(base + kPartOff);
@@ -94,7 +139,9 @@ extern "C" int dcoco_topk_noalloc(int batch, int slots, int vocab, int topk, con
   // at zero.
   if (cudaMemsetAsync(row_count, 0, (size_t)rows * sizeof(unsigned), st) != cudaSuccess)
     return DCOCO_ECUDA;
+  // No programmatic overlap with the caller's previous kernel, which may
+  // still be writing the logits.
   const cudaError_t e = dc::launch_topk(topk, static_cast<const uint16_t *>(logits), logits_slot_stride,
-                                        slots, batch, vocab, plan, part, row_count, topk_ids, topk_val, st, true);
+                                        slots, batch, vocab, plan, part, row_count, topk_ids, topk_val, st, false);
   return e == cudaSuccess ? DCOCO_OK : DCOCO_ECUDA;
 }

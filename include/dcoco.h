@@ -180,7 +180,9 @@ int dcoco_correct(dcoco_handle *h, const dcoco_weights *w, int batch,
 /* Same path with HOST buffers: copies hidden (and target tokens) from host
  * memory into the handle's staging buffers; logits in page-locked host memory
  * the device can address (e.g. cudaHostAlloc) are read in place by the top-K
- * over the host link, other logits are copied to staging first.  Runs
+ * over the host link, provided the driver reports one page-locked range
+ * that holds every byte the call reads ((batch * slots - 1) * stride + vocab
+ * elements from `logits`); other logits are copied to staging first.  Runs
  * dcoco_correct, copies the requested outputs back to the host pointers in
  * `out`, and synchronises `stream`.  The host buffers must stay unchanged
  * until the call returns.  `in->cand_embed` stays a DEVICE pointer (the
@@ -188,6 +190,12 @@ int dcoco_correct(dcoco_handle *h, const dcoco_weights *w, int batch,
  * Errors: as dcoco_correct, plus EINVAL if the handle has no staging. */
 int dcoco_correct_host(dcoco_handle *h, const dcoco_weights *w, int batch,
                        const dcoco_inputs *in, const dcoco_outputs *out, void *stream);
+
+/* The test dcoco_correct_host applies before it reads host logits in
+ * place: 1 if [ptr, ptr + bytes) lies inside [range_start, range_start +
+ * range_size) (the page-locked range the driver reports for ptr), else 0.
+ * Pure arithmetic: no CUDA call. */
+int dcoco_host_range_covers(uint64_t range_start, uint64_t range_size, uint64_t ptr, uint64_t bytes);
 
 /* Stochastic verification (temperature 1) of a point-mass proposal, the
  * alternative to the greedy verify of step 5 for sampling targets.
@@ -229,10 +237,17 @@ int dcoco_topk(dcoco_handle *h, int batch, const void *logits, int64_t logits_sl
  * a latency-critical path where cudaMalloc, which can synchronise the device,
  * is not acceptable.  Its scratch is a fixed 4 MiB array that every GPU
  * loading the library holds until the process exits.
- *   batch, slots, vocab, topk: as dcoco_config / dcoco_topk; the batch is
- *     limited to batch * (slots - 1) <= DCOCO_TOPK_NOALLOC_MAX_ROWS (4096
- *     draft-slot rows, i.e. 273 requests of 16 slots); larger requests are
- *     rejected with DCOCO_EBATCH before any CUDA call.
+ *   batch, slots, vocab, topk: as dcoco_config / dcoco_topk.  Two limits,
+ *     both checked before any CUDA call, reject a call with DCOCO_EBATCH:
+ *     (1) batch * (slots - 1) <= DCOCO_TOPK_NOALLOC_MAX_ROWS (4096 draft-slot
+ *     rows, i.e. 273 requests of 16 slots);
+ *     (2) the per-segment candidate lists must fit the array's list area of
+ *     (4 MiB - 16 KiB) / 8 = 522,240 entries at the fewest segments the
+ *     vocabulary allows: rows * topk * ceil((vocab / 8) / 20480) <= 522,240
+ *     (rows = batch * (slots - 1)).  At vocab 151,936 that is always met; at
+ *     vocab 2^20 and topk 32 it allows at most 2331 rows.
+ *     Within limit (2), a call whose plan wants more segments than the area
+ *     holds runs with fewer, longer segments (same results, slower).
  *   logits, logits_slot_stride, topk_ids, topk_val, stream: as dcoco_topk
  *     (device pointers, outputs [batch][slots-1][topk]).
  * Results are identical to dcoco_topk's.  No cudaMalloc / cudaFree or other
@@ -246,6 +261,16 @@ int dcoco_topk(dcoco_handle *h, int batch, const void *logits, int64_t logits_sl
 int dcoco_topk_noalloc(int batch, int slots, int vocab, int topk, const void *logits,
                        int64_t logits_slot_stride, int32_t *topk_ids, float *topk_val,
                        void *stream);
+
+/* Planning query for dcoco_topk_noalloc on the current device (no kernel
+ * launch, no allocation): *segments receives the number of segments per row
+ * the call would use and *planned_segments the number the handle-based
+ * dcoco_topk would use for the same rows; they differ when the fixed list
+ * area holds fewer.  The first query on a device performs the same one-time
+ * set-up as the first dcoco_topk_noalloc call.  Errors: EINVAL (NULL
+ * outputs), EUNSUPPORTED / EINVAL / EBATCH as dcoco_topk_noalloc, ECUDA. */
+int dcoco_topk_noalloc_plan(int batch, int slots, int vocab, int topk, int *segments,
+                            int *planned_segments);
 
 /* Synchronise the handle's last stream and return DCOCO_OK, or DCOCO_EDEVICE
  * if a kernel recorded bad data (e.g. a candidate id outside [0,V)) or a

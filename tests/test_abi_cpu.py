@@ -87,3 +87,18 @@ def test_library_never_loads_the_oracle(dc):
             if fn.endswith((".py", ".cu", ".cuh", ".h")):
                 src = open(os.path.join(dirpath, fn)).read()
                 assert "oracle" not in re.sub(r"#.*|//.*", "", src).replace("oracle's", ""), fn
+
+
+def test_host_range_predicate(dc):
+    """dcoco_correct_host reads host logits in place only when the page-locked
+    range the driver reports holds the whole extent the top-K reads."""
+    f = dc.dcoco_host_range_covers
+    base, size = 0x10000, 0x8000
+    assert f(base, size, base, size)                 # the whole range
+    assert f(base, size, base + 0x100, size - 0x100)  # ends exactly at the range end
+    assert not f(base, size, base + 0x100, size - 0xFF)  # one byte past the end
+    assert not f(base, size, base - 16, 32)          # starts before the range
+    assert not f(base, size, base + size, 16)        # starts at the end
+    assert f(base, size, base + size, 0)             # empty extent at the end
+    assert not f(base, 0, base, 0)                   # no range
+    assert not f(0, 2**64 - 1, 2**63, 2**63 + 1)     # no wrap-around
