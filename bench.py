@@ -4,12 +4,21 @@ fraction of the HBM roofline.
 
 A step is one call of the whole correction path (top-K, candidate
 representations, K x K transition scores, greedy walk, greedy verify) on one
-batch of 32 requests x 16 slots x V = 151,936 bf16 logits, d = 4096 hidden
-states, K = 16, r = 128, MLP 386 -> 256 -> 1.  Inputs are synthetic and
-seeded (recipe in synth/), generated on the GPU before timing; the step reads
-them from HBM.  Four input sets rotate so that every step's logits were last
-touched three steps earlier (4 x 160 MB > 129 MB L2), and the candidate rows
-are gathered from a 1.2 GB embedding table.
+batch of synthetic inputs.  Workloads (`--workload`, default c32):
+
+  c32       32 requests x 16 slots x V = 151,936 bf16 logits, d = 4096 hidden
+            states, K = 16, r = 128, MLP 386 -> 256 -> 1 (the headline);
+  tiny      the same shapes for one request (latency);
+  cosine16  the in/out cosine-similarity variant at 16 requests;
+  wide32    d = 5120, K = 32, low-entropy logits, 32 requests;
+  sweep     requests in {1, 2, 4, 8, 16, 32} x three entropy tiers (64 planted
+            tokens per slot with boosts U(2,6), U(4,12), U(8,16)).
+
+Inputs are seeded and generated on the GPU before timing (the recipe of
+synth/), rotating input sets so that the logits of every step exceed the
+129 MB L2; the candidate rows are gathered from a >= 1.2 GB embedding table.
+Timed iterations on one input set are checked against the CPU oracle on
+sampled requests, with the oracle runs that also give the CPU baseline.
 
 Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle on
 the host cores instead (the reference arm).
@@ -31,8 +40,25 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "corrected draft blocks/s at batch 32, Qwen3-8B shapes; % of HBM roofline"
-WORKLOAD = dict(name="qwen3_8b_c32", N=32, slots=16, V=151936, d=4096, K=16, r=128, H=256,
-                planted=32, boost=(4.0, 12.0))
+SCORE_TOL = 2e-3  # max |score error| allowed against the oracle (fp32 vs fp64)
+
+_QWEN = dict(slots=16, V=151936, d=4096, K=16, r=128, H=256, planted=32, boost=(4.0, 12.0), variant=0, sigma=1.0)
+WORKLOADS = {
+    "c32": dict(_QWEN, name="qwen3_8b_c32", N=32, sets=4,
+                desc="32 requests x 16 slots (1 anchor + 15 draft) x V=151936 bf16 logits, d=4096 bf16 hidden, "
+                     "E[151936,4096] bf16, K=16, r=128, MLP 386-256-1 fp32 weights"),
+    "tiny": dict(_QWEN, name="qwen3_8b_n1", N=1, sets=32,
+                 desc="1 request x 16 slots x V=151936 bf16 logits, d=4096, K=16, r=128, MLP 386-256-1"),
+    "cosine16": dict(_QWEN, name="cosine_n16", N=16, sets=4, variant=1,
+                     desc="cosine variant: 16 requests x 16 slots x V=151936, d=4096, K=16, in/out width 128 "
+                          "from W_io[256, 8192], sigma 1"),
+    "wide32": dict(_QWEN, name="wide_k32_d5120_c32", N=32, d=5120, K=32, planted=8, boost=(8.0, 16.0), sets=4,
+                   desc="32 requests x 16 slots x V=151936, d=5120, K=32 (14,336 transitions per request), "
+                        "8 planted tokens per slot with boost U(8,16)"),
+}
+SWEEP_NS = (1, 2, 4, 8, 16, 32)
+SWEEP_TIERS = (("U(2,6)", (2.0, 6.0)), ("U(4,12)", (4.0, 12.0)), ("U(8,16)", (8.0, 16.0)))
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal
 
 
 def log(*a):
@@ -45,11 +71,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--sets", type=int, default=4, help="rotating input sets")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS) + ["sweep"], default="c32")
+    ap.add_argument("--sets", type=int, default=0, help="rotating input sets (0: the workload's default)")
     ap.add_argument("--e2e-steps", type=int, default=30)
-    ap.add_argument("--cpu-requests", type=int, default=16,
-                    help="requests in the CPU-oracle baseline sample")
-    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle leg (baseline and parity)")
     ap.add_argument("--no-graph", action="store_true", help="time eager calls only")
     ap.add_argument("--path-rule", choices=["greedy", "viterbi", "beam"], default="greedy",
                     help="step 5: prefix-first greedy walk (default), highest-scoring path or beam walk")
@@ -75,9 +100,21 @@ def peaks():
                 source="fallback")
 
 
-# ------------------------------------------------------------------ per-stage algorithmic work
-NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal
+def host_cpu():
+    """(model name, logical cores) of the host, from lscpu when it is there."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            key = line.split(":")[0].strip()
+            if key in ("Model name", "Model") and model is None or key == "Model name":
+                model = line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return model, os.cpu_count() or 1
 
+
+# ------------------------------------------------------------------ per-stage algorithmic work
 def algorithmic_bytes(w) -> int:
     """Bytes one call must move from HBM: the draft slots' logits (15 V bf16 per
     request) and the gathered candidate embedding rows (15 K d bf16 per
@@ -86,25 +123,34 @@ def algorithmic_bytes(w) -> int:
     return w["N"] * B * w["V"] * 2 + w["N"] * B * w["K"] * w["d"] * 2
 
 
-PEAK_SOURCE = {"hbm": "hbm_gbs", "tensor": "bf16_tflops",
-               "alu": "152 SMs x 128 fp32 lanes x sm_max_mhz / 11 lane-ops per element"}
+def maps_method_flops(w) -> int:
+    """The maps kernel's work as the method defines it (multiply-adds x 2):
+    per slot W_fuse[:, r:] g and W1_s s, per candidate W_fuse[:, :r] b, W1_a z and
+    W1_b z.  The kernel issues each as three bf16 tensor-core passes (hi/lo
+    operand splits), i.e. 3x these flops on the tensor pipe."""
+    N, B, K, r, H = w["N"], w["slots"] - 1, w["K"], w["r"], w["H"]
+    return 2 * N * (B * r * r + (B - 1) * r * H) + 2 * N * B * K * (r * r + 2 * r * H)
+
+
+FMA_LANE_OPS_PER_GELU = 11  # the pair loop's FMA-pipe lane operations per w2*GELU element
+
+
+def fma_lane_rate(pk) -> float:
+    """fp32 FMA-pipe lane operations per second: 152 SMs x 128 lanes x the maximum SM clock."""
+    return 152 * 128 * pk["sm_max_mhz"] * 1e6
 
 
 def stage_model(w, pk):
-    """stage -> (bound, unit, algorithmic amount per launch, peak).  Bytes are
-    the bytes the step must move from HBM; flops are multiply-adds x 2."""
-    N, B, V, d, K, r, H = w["N"], w["slots"] - 1, w["V"], w["d"], w["K"], w["r"], w["H"]
-    # the pair scores evaluate w2 * GELU on the fp32 FMA pipe: 11 lane-operations
-    # per element (the add, the degree-6 polynomial, the scaling of log2 q, the
-    # products around 1 - erf), so its peak is the pipe's element rate
-    gelu_peak = 152 * 128 * pk["sm_max_mhz"] * 1e6 / 11 / 1e9  # Gelem/s
-    # the maps run their 128-deep products as three bf16 tensor-core passes
-    maps_flops = 3 * (2 * N * (B * r * r + (B - 1) * r * H) + 2 * N * B * K * (r * r + 2 * r * H))
+    """stage -> (bound, unit, algorithmic amount per launch, peak)."""
+    N, B, V, d, K, r = w["N"], w["slots"] - 1, w["V"], w["d"], w["K"], w["r"]
     return {
         "topk": ("hbm", "GB/s", N * B * V * 2, pk["hbm_gbs"]),
         "proj": ("hbm", "GB/s", N * B * K * d * 2 + N * B * d * 2, pk["hbm_gbs"]),
-        "maps": ("tensor", "TFLOP/s", maps_flops, pk["bf16_tflops"]),
-        "pair_walk": ("alu", "Gelem/s", N * (B - 1) * K * K * H, gelu_peak),
+        "maps": ("tensor", "TFLOP/s", maps_method_flops(w), pk["bf16_tflops"]),
+        # the pair loop's element rate at its own operation count
+        "pair_walk": ("alu", "Gelem/s", N * (B - 1) * K * K * w["H"],
+                      fma_lane_rate(pk) / FMA_LANE_OPS_PER_GELU / 1e9),
+        "cos_score": ("alu", "GFLOP/s", 2 * N * (B - 1) * K * K * r, 2 * fma_lane_rate(pk) / 1e9),
     }
 
 
@@ -125,6 +171,40 @@ def kernel_traffic(kernel: str):
         if os.path.exists(src) and hashlib.sha256(open(src, "rb").read()).hexdigest() == m.group(2):
             return float(m.group(1))
     return None
+
+
+def stage_entries(stage_ms, calls, w, pk):
+    model = stage_model(w, pk)
+    stages = {}
+    tot = max(sum(stage_ms.values()), 1e-9)
+    for name, ms in stage_ms.items():
+        avg_s = ms / max(calls, 1) / 1e3
+        bound, unit, amount, peak = model.get(name, ("latency", "us", 0, None))
+        ent = {"us": avg_s * 1e6, "share": ms / tot, "bound": bound}
+        if bound == "hbm":
+            ent.update(achieved=amount / avg_s / 1e9, unit="GB/s", peak=peak, frac=amount / avg_s / 1e9 / peak,
+                       bytes=amount)
+        elif bound == "tensor":
+            ach = amount / avg_s / 1e12
+            ent.update(achieved=ach, unit="TFLOP/s", peak=peak, frac=ach / peak, flops=amount,
+                       issued_flops=3 * amount,
+                       note="the method's flops; the kernel issues 3x them (bf16 hi/lo passes) in a "
+                            "latency-bound chain of short phases")
+        elif bound == "alu" and name == "pair_walk":
+            ach = amount / avg_s / 1e9
+            plain = fma_lane_rate(pk) / 1e12
+            ent.update(achieved=ach, unit="Gelem/s", peak=peak, frac=ach / peak, elements=amount,
+                       peak_derivation=f"152 SMs x 128 fp32 lanes x {pk['sm_max_mhz']:.0f} MHz / "
+                                       f"{FMA_LANE_OPS_PER_GELU} FMA-pipe lane operations per element "
+                                       "(this kernel's own count)",
+                       fma_lane_ops_tera_per_s=ach * FMA_LANE_OPS_PER_GELU / 1e3,
+                       plain_fma_lane_rate_tera_per_s=plain,
+                       frac_of_plain_fma_rate=ach * FMA_LANE_OPS_PER_GELU / 1e3 / plain)
+        elif bound == "alu":
+            ach = amount / avg_s / 1e9
+            ent.update(achieved=ach, unit=unit, peak=peak, frac=ach / peak, flops=amount)
+        stages[name] = ent
+    return stages
 
 
 # ------------------------------------------------------------------ clocks
@@ -219,37 +299,88 @@ def gpu_embedding(torch, seed, V, d, device):
     return E
 
 
-# ------------------------------------------------------------------ CPU oracle baseline
-def cpu_baseline(w, n_req: int, logits_np, hidden_np, E_np, targets_np, weights_np, path_rule: int = 0,
-                 beam_width: int = 4, beam_topm: int = 0):
+def make_weights_np(w, seed):
+    import numpy as np
+    import synth
+    rng = np.random.default_rng(seed)
+    return synth.make_weights(rng, w["d"]) if w["variant"] == 0 else synth.make_cosine_weights(rng, w["d"])
+
+
+def u16(torch, t):
+    import numpy as np
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+# ------------------------------------------------------------------ the oracle leg (CPU baseline + parity)
+def oracle_leg(w, host, weights_np, check_reqs, path_rule, beam_width, beam_topm, all_core_reqs):
+    """Runs the CPU oracle (test infrastructure; never on the product path) on
+    sampled requests of one input set: single-threaded on `check_reqs` (the
+    per-request time) and on all host cores over `all_core_reqs` requests;
+    returns the baseline figures and the oracle's answers for the parity check."""
     import oracle
+    logits, hidden, E, targets = host
     m = oracle.Model(weights_np, V=w["V"], d=w["d"], slots=w["slots"], K=w["K"], beam_width=beam_width,
                      beam_topm=beam_topm)
-    threads = os.cpu_count() or 1
-    req = list(range(min(n_req, w["N"])))
-    oracle.correct_batch(m, logits_np[:1], hidden_np[:1], E_np, targets_np[:1], requests=[0], path_rule=path_rule,
-                         threads=1)  # load + page-in
+    model, ncpu = host_cpu()
+    kw = dict(variant=w["variant"], sigma=w["sigma"], path_rule=path_rule)
+    oracle.correct_batch(m, logits, hidden, E, targets, requests=[check_reqs[0]], threads=1, **kw)  # page-in
     t0 = time.perf_counter()
-    oracle.correct_batch(m, logits_np, hidden_np, E_np, targets_np, requests=req, threads=threads,
-                         path_rule=path_rule)
-    dt = time.perf_counter() - t0
-    return {"value": len(req) / dt, "unit": "blocks/s", "cores": min(threads, len(req)),
-            "kind": "oracle",
-            "sample": f"{len(req)} of the 32 requests of one input set, one thread per request, "
-                      f"{dt:.2f} s wall on {threads} host cores"}
+    ref = oracle.correct_batch(m, logits, hidden, E, targets, requests=check_reqs, threads=1, **kw)
+    t_single = time.perf_counter() - t0
+    reqs = list(range(min(all_core_reqs, w["N"])))
+    threads = min(ncpu, len(reqs))
+    t0 = time.perf_counter()
+    oracle.correct_batch(m, logits, hidden, E, targets, requests=reqs, threads=threads, **kw)
+    t_all = time.perf_counter() - t0
+    base = {"value": len(reqs) / t_all, "unit": "blocks/s", "cores": threads, "kind": "oracle",
+            "sample": f"{len(reqs)} of the {w['N']} requests of one input set, one host thread each "
+                      f"({t_all:.2f} s wall); single thread: {len(check_reqs)} requests in {t_single:.2f} s",
+            "single_thread": {"value": len(check_reqs) / t_single, "unit": "blocks/s", "cores": 1,
+                              "requests": len(check_reqs)},
+            "nproc": ncpu, "cpu_model": model, "workload": w["name"]}
+    return base, ref
+
+
+def parity_check(ref, gpu, target_np, B):
+    """The comparison rules of the parity tests on one set of sampled requests:
+    top-K ids and values bit-exact, scores within SCORE_TOL, walk choices equal
+    except where the oracle's top-two margin is below SCORE_TOL (counted),
+    tokens = the chosen candidates' ids and accept_len = verify of those tokens."""
+    import numpy as np
+    import oracle
+    req = list(ref["requests"])
+    ok = bool(np.array_equal(gpu["topk_ids"], ref["topk_ids"]))
+    ok &= bool(np.array_equal(gpu["topk_val"].view(np.uint32), ref["topk_val"].view(np.uint32)))
+    err = float(np.abs(gpu["scores"].astype(np.float64) - ref["scores"]).max())
+    ok &= err <= SCORE_TOL
+    near = 0
+    for j, n in enumerate(req):
+        gc = gpu["choice"][j]
+        sc = ref["scores"][j]
+        ok &= int(gc[0]) == 0
+        for p in range(B - 1):
+            row = sc[p, gc[p]]
+            best = int(np.flatnonzero(row == row.max())[0])
+            if gc[p + 1] != best:
+                second = float(np.max(np.delete(row, best)))
+                if row[best] - second < SCORE_TOL and row[gc[p + 1]] >= row[best] - SCORE_TOL:
+                    near += 1
+                else:
+                    ok = False
+        toks = ref["topk_ids"][j][np.arange(B), gc]
+        ok &= bool(np.array_equal(gpu["tokens"][j], toks))
+        if target_np is not None:
+            ok &= int(gpu["accept_len"][j]) == oracle.verify(toks, target_np[n])
+    if near == 0:
+        ok &= bool(np.array_equal(gpu["tokens"], ref["tokens"]))
+        if target_np is not None:
+            ok &= bool(np.array_equal(gpu["accept_len"], ref["accept_len"]))
+    return bool(ok), err, near
 
 
 # ------------------------------------------------------------------ our arm
-def run_ours(args):
-    import numpy as np
-    import torch
+def setup_dist(torch):
     import torch.distributed as dist
-
-    import __graft_entry__
-    __graft_entry__.build()
-    import draft_correction_slot_gb300 as dc
-    import synth
-
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -257,24 +388,81 @@ def run_ours(args):
     device = torch.device("cuda", local)
     if world > 1:
         dist.init_process_group("nccl", device_id=device)
-    w = dict(WORKLOAD)
+    return dist, world, rank, local, device
+
+
+def max_over_ranks(torch, dist, world, device, x):
+    if world > 1:
+        t = torch.tensor([x], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+    return x
+
+
+def timed_loop(torch, dist, world, device, steps, run_step, hook=None):
+    """`steps` calls bracketed by a barrier and a synchronize on both sides,
+    timed with CUDA events on the launching stream; max over ranks."""
+    if world > 1:
+        dist.barrier()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    torch.cuda.synchronize()
+    t0 = time.time()
+    ev[0].record()
+    for i in range(steps):
+        run_step(i)
+        ev[i + 1].record()
+        if hook is not None:
+            hook(i)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    if world > 1:
+        dist.barrier()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    tot = max_over_ranks(torch, dist, world, device, ev[0].elapsed_time(ev[-1]))
+    return tot, per, t0, t1
+
+
+def run_ours(args):
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import draft_correction_slot_gb300 as dc
+
+    dist, world, rank, local, device = setup_dist(torch)
     pk = peaks()
+    if args.workload == "sweep":
+        line = run_sweep(args, torch, dc, dist, world, rank, local, device, pk)
+    else:
+        line = run_workload(args, WORKLOADS[args.workload], torch, dc, dist, world, rank, local, device, pk)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_workload(args, w, torch, dc, dist, world, rank, local, device, pk):
+    import numpy as np
+
+    w = dict(w)
     N, S, V, d, K = w["N"], w["slots"], w["V"], w["d"], w["K"]
     B = S - 1
-
-    weights_np = synth.make_weights(np.random.default_rng(7 + rank), d)
-    E = gpu_embedding(torch, 11 + rank, V, d, device)
-    sets = [gpu_inputs(torch, 1000 + 97 * rank + s, w, device) for s in range(args.sets)]
+    sets_n = args.sets or w["sets"]
     path_rule = {"greedy": 0, "viterbi": 1, "beam": 2}[args.path_rule]
+    weights_np = make_weights_np(w, 7 + rank)
+    E = gpu_embedding(torch, 11 + rank, V, d, device)
+    sets = [gpu_inputs(torch, 1000 + 97 * rank + s, w, device) for s in range(sets_n)]
     corr = dc.Corrector({k: torch.from_numpy(v) for k, v in weights_np.items()}, V, d, S, K,
-                        max_batch=N, host_staging=True, path_rule=path_rule, beam_width=args.beam_width,
-                        beam_topm=args.beam_topm)
-    outs = [corr.alloc_outputs(N, device, full=False, features=args.features) for _ in range(args.sets)]
+                        max_batch=N, variant=w["variant"], sigma=w["sigma"], host_staging=True,
+                        path_rule=path_rule, beam_width=args.beam_width, beam_topm=args.beam_topm)
+    # full outputs (scores, ids and choices land in these buffers instead of
+    # the workspace: the same work), so that timed iterations can be checked
+    outs = [corr.alloc_outputs(N, device, full=True, features=args.features) for _ in range(sets_n)]
     torch.cuda.synchronize()
 
     def step(i):
-        lg, hd, tg = sets[i % args.sets]
-        corr.correct(lg, hd, E, tg, out=outs[i % args.sets], full=False)
+        lg, hd, tg = sets[i % sets_n]
+        corr.correct(lg, hd, E, tg, out=outs[i % sets_n], full=True)
 
     sampler = ClockSampler(local)
     for i in range(args.warmup):
@@ -285,201 +473,285 @@ def run_ours(args):
     launches_per_step = dc.dcoco_kernel_launches(corr.handle) - launches0
     torch.cuda.synchronize()
 
-    def timed(run_step, tag):
-        if world > 1:
-            dist.barrier()
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-        torch.cuda.synchronize()
-        t0 = time.time()
-        ev[0].record()
-        for i in range(args.steps):
-            run_step(args.warmup + i)
-            ev[i + 1].record()
-        torch.cuda.synchronize()
-        t1 = time.time()
-        if world > 1:
-            dist.barrier()
-        tot = ev[0].elapsed_time(ev[-1])
-        per_ = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
-        if world > 1:
-            t = torch.tensor([tot], device=device)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            tot = float(t.item())
-        return tot, per_, t0, t1
+    # timed iterations checked against the oracle: the first, middle and last
+    # that ran input set 0 (every call on one set must give the same answer)
+    on0 = [i for i in range(args.steps) if (args.warmup + i) % sets_n == 0]
+    checked = sorted({on0[0], on0[len(on0) // 2], on0[-1]}) if on0 else []
+    check_reqs = sorted({0, N // 2, N - 1})
+    keep = {}
+    names = ("topk_ids", "topk_val", "scores", "choice", "tokens", "accept_len", "margin")
 
-    # eager: one dcoco_correct call per step
-    eager_ms, eager_per, _, _ = timed(step, "eager")
-    # graph replay: each input set's call captured once (dcoco_correct allocates
-    # and synchronises nothing, so it is capturable), then replayed
+    def hook(i):
+        if i in checked:  # a copy of 3 requests' outputs after the call, on the same stream
+            keep[i] = {k: outs[0][k][check_reqs].clone() for k in names}
+
+    eager_ms, eager_per, _, _ = timed_loop(torch, dist, world, device, args.steps,
+                                           lambda i: step(args.warmup + i))
     graphs = None
     if not args.no_graph:
+        # each input set's call captured once (dcoco_correct allocates and
+        # synchronises nothing), then replayed
         graphs = []
         cap = torch.cuda.Stream()
-        for s_ in range(args.sets):
+        for s_ in range(sets_n):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=cap):
                 step(s_)
             graphs.append(g)
         torch.cuda.synchronize()
         for i in range(max(3, args.warmup)):
-            graphs[i % args.sets].replay()
+            graphs[i % sets_n].replay()
         torch.cuda.synchronize()
-    if graphs is not None:
-        total_ms, per, t_host0, t_host1 = timed(lambda i: graphs[i % args.sets].replay(), "graph")
+        run = lambda i: graphs[(args.warmup + i) % sets_n].replay()  # noqa: E731
     else:
-        total_ms, per, t_host0, t_host1 = eager_ms, eager_per, None, None
-    if t_host0 is None:
-        t_host0, t_host1 = time.time() - 1.0, time.time()
+        run = lambda i: step(args.warmup + i)  # noqa: E731
+    total_ms, per, t_host0, t_host1 = timed_loop(torch, dist, world, device, args.steps, run, hook)
     launches = launches_per_step * args.steps
-    if world > 1:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
     clocks = sampler.summary(t_host0, t_host1)
 
-    # per-kernel times, live, with stage events on the same stream
+    # per-kernel times, live, with stage events on the same stream (serialised)
     dc.dcoco_stage_timing(corr.handle, True)
-    n_stage_calls = min(args.steps, 200)
-    for i in range(n_stage_calls):
+    for i in range(min(args.steps, 200)):
         step(i)
     stage_ms, calls = dc.dcoco_stage_read(corr.handle)
     dc.dcoco_stage_timing(corr.handle, False)
     sampler.stop()
-    model = stage_model(w, pk)
-    stages = {}
-    for name, ms in stage_ms.items():
-        avg_s = ms / max(calls, 1) / 1e3
-        bound, unit, amount, peak = model.get(name, ("latency", "us", 0, None))
-        ent = {"us": avg_s * 1e6, "share": ms / max(sum(stage_ms.values()), 1e-9), "bound": bound}
-        if bound == "hbm":
-            ent.update(achieved=amount / avg_s / 1e9, unit="GB/s", peak=peak, frac=amount / avg_s / 1e9 / peak,
-                       bytes=amount)
-        elif bound == "tensor":
-            ent.update(achieved=amount / avg_s / 1e12, unit="TFLOP/s", peak=peak,
-                       frac=amount / avg_s / 1e12 / peak, flops=amount,
-                       note="latency-bound chain of short phases; tensor flops over the bf16 peak")
-        elif bound == "alu":
-            ent.update(achieved=amount / avg_s / 1e9, unit="Gelem/s", peak=peak,
-                       frac=amount / avg_s / 1e9 / peak, elements=amount,
-                       note="GELU elements over the fp32 FMA pipe's element rate (11 lane-ops each)")
-        stages[name] = ent
+    stages = stage_entries(stage_ms, calls, w, pk)
     dom = max(stages, key=lambda k: stages[k]["us"])
     de = stages[dom]
     roofline = {"kernel": dom, "bound": de["bound"], "achieved": de.get("achieved"),
                 "peak": de.get("peak"), "unit": de.get("unit"), "frac": de.get("frac"),
-                "traffic": kernel_traffic(dom),
-                "peak_source": f"{pk['source']} ({PEAK_SOURCE.get(de['bound'], 'none')})"}
+                "traffic": kernel_traffic(dom) if w["name"] == WORKLOADS["c32"]["name"] else None,
+                "peak_source": f"{pk['source']} ({'hbm_gbs' if de['bound'] == 'hbm' else de['bound']})"}
 
-    # whole step against the path's byte floor
     path_bytes = algorithmic_bytes(w)
     step_s = total_ms / args.steps / 1e3
     value = world * N / step_s
 
-    # stochastic verification (an entry of its own, reported apart from the headline)
-    stoch = None
-    if args.stochastic_verify:
-        tgen = torch.Generator(device=device)
-        tgen.manual_seed(4242 + rank)
-        tset = []
-        for s_ in range(args.sets):
-            x = torch.randn(N * (B + 1), V, generator=tgen, device=device) * 2.0
-            hot = torch.randint(0, V, (N * (B + 1), 2), generator=tgen, device=device)
-            x.scatter_add_(1, hot, torch.rand(N * (B + 1), 2, generator=tgen, device=device) * 4.0 + 14.0)
-            tl = x.to(torch.bfloat16).view(N, B + 1, V)
-            del x
-            toks = tl[:, :B].float().argmax(-1).to(torch.int32)  # input recipe only: a plausible proposal
-            tset.append((tl, toks, torch.rand(N, B, generator=tgen, device=device),
-                         torch.rand(N, generator=tgen, device=device)))
-        vouts = [corr.verify_stochastic(*tset[i]) for i in range(args.sets)]  # warm-up and outputs
-        torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        reps = max(10, args.steps)
-        e0.record()
-        for i in range(reps):
-            tl, toks, ua, ud = tset[i % args.sets]
-            dc.dcoco_verify_stochastic(corr.handle, N, tl, toks, ua, ud, vouts[i % args.sets]["accept_len"],
-                                       vouts[i % args.sets]["next_token"], vouts[i % args.sets]["q_accept"])
-        e1.record()
-        torch.cuda.synchronize()
-        us = e0.elapsed_time(e1) / reps * 1e3
-        vb = N * (B + 1) * V * 2
-        stoch = {"us_per_call": us, "blocks_per_s": N / (us * 1e-6), "target_logits_bytes": vb,
-                 "achieved_gbs": vb / (us * 1e-6) / 1e9, "frac_of_hbm_peak": vb / (us * 1e-6) / 1e9 / pk["hbm_gbs"],
-                 "mean_accept_len": float(torch.cat([o["accept_len"] for o in vouts]).float().mean()),
-                 "inputs": f"{args.sets} sets of [N, B+1, V] bf16 target logits, 2 boosted tokens per row "
-                           "(U(14,18) over 2 N(0,1)), proposal = per-slot target argmax, uniforms from torch"}
-        del tset, vouts
+    stoch = stochastic_leg(args, torch, dc, corr, w, device, pk, rank) if args.stochastic_verify else None
+    e2e = e2e_leg(args, torch, dc, dist, world, device, corr, sets[0], E, N, B)
 
-    # e2e: host buffers through the C ABI (copies inside the timed region)
-    e2e = None
-    if args.e2e_steps > 0:
-        lg, hd, tg = sets[0]
-        lg_h = lg.view(torch.int16).cpu().pin_memory()
-        hd_h = hd.view(torch.int16).cpu().pin_memory()
-        tg_h = tg.cpu().pin_memory()
-        tok_h = torch.empty(N, B, dtype=torch.int32).pin_memory()
-        acc_h = torch.empty(N, dtype=torch.int32).pin_memory()
-        for _ in range(3):
-            dc.dcoco_correct_host(corr.handle, corr.weights, N, lg_h, hd_h, E, tg_h, tokens=tok_h,
-                                  accept_len=acc_h)
-        t0 = time.perf_counter()
-        for _ in range(args.e2e_steps):
-            dc.dcoco_correct_host(corr.handle, corr.weights, N, lg_h, hd_h, E, tg_h, tokens=tok_h,
-                                  accept_len=acc_h)
-        dt = (time.perf_counter() - t0) / args.e2e_steps
-        if world > 1:
-            t = torch.tensor([dt], device=device)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            dt = float(t.item())
-        e2e = {"value": world * N / dt, "unit": "blocks/s",
-               "h2d_bytes_per_step": lg_h.numel() * 2 + hd_h.numel() * 2 + tg_h.numel() * 4,
-               "d2h_bytes_per_step": tok_h.numel() * 4 + acc_h.numel() * 4,
-               "ms_per_step": dt * 1e3, "api": "dcoco_correct_host (pinned host buffers)"}
-
-    cpu = None
+    cpu, parity = None, None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         lg, hd, tg = sets[0]
-        cpu = cpu_baseline(w, args.cpu_requests, lg.view(torch.int16).cpu().numpy().view(np.uint16),
-                           hd.view(torch.int16).cpu().numpy().view(np.uint16),
-                           E.view(torch.int16).cpu().numpy().view(np.uint16), tg.cpu().numpy(), weights_np,
-                           path_rule, args.beam_width, args.beam_topm)
+        host = (u16(torch, lg), u16(torch, hd), u16(torch, E), tg.cpu().numpy())
+        cpu, ref = oracle_leg(w, host, weights_np, check_reqs, path_rule, args.beam_width, args.beam_topm,
+                              all_core_reqs=min(N, 2 * (os.cpu_count() or 1)))
+        results = []
+        for i in checked:
+            gpu = {k: v.cpu().numpy() for k, v in keep[i].items()}
+            if path_rule == 0:
+                ok, err, near = parity_check(ref, gpu, host[3], B)
+            else:  # the path rules' own decision checks live in the tests; ids and scores here
+                ok = bool(np.array_equal(gpu["topk_ids"], ref["topk_ids"]))
+                err = float(np.abs(gpu["scores"].astype(np.float64) - ref["scores"]).max())
+                ok = ok and err <= SCORE_TOL
+                near = int((gpu["choice"] != ref["choice"]).any(axis=1).sum())
+            results.append((i, ok, err, near))
+        parity = {"parity_ok": all(r[1] for r in results),
+                  "max_score_err": max((r[2] for r in results), default=None),
+                  "near_tie_divergences": sum(r[3] for r in results),
+                  "checked_iterations": [r[0] for r in results], "requests_per_iteration": check_reqs,
+                  "tolerance": SCORE_TOL,
+                  "rules": "ids/values bit-exact, scores |err| <= tol, walk choices equal except counted "
+                           "near ties (oracle top-two margin < tol), tokens = chosen ids, accept_len = verify"}
     corr.close()
 
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": "blocks/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic (seeded, synth/ recipe drawn on the GPU)",
-            "config": {"workload": "qwen3_8b_c32: 32 requests x 16 slots (1 anchor + 15 draft) x "
-                                   "V=151936 bf16 logits, d=4096 bf16 hidden, E[151936,4096] bf16, "
-                                   "K=16, r=128, MLP 386-256-1 fp32 weights",
-                       "global_batch": world * N, "per_gpu_batch": N, "parallelism": f"replicas x{world}",
-                       "inputs": "bf16; arithmetic fp32",
-                       "candidate_features": bool(args.features),
-                       "path_rule": args.path_rule if args.path_rule != "beam" else
-                       f"beam (width {args.beam_width}, top-m {args.beam_topm or K})",
-                       "l2": f"{args.sets} rotating input sets of 160 MB (> 129 MB L2), no flush"},
-            "us_per_block": step_s * 1e6 / N,
-            "step_us": {"p10": 1e3 * sorted(per)[len(per) // 10], "p50": 1e3 * statistics.median(per),
-                        "p90": 1e3 * sorted(per)[(9 * len(per)) // 10]},
-            "path_hbm_roofline": {"bytes_per_step": path_bytes, "achieved_gbs": path_bytes / step_s / 1e9,
-                                  "peak_gbs": pk["hbm_gbs"],
-                                  "frac": path_bytes / step_s / 1e9 / pk["hbm_gbs"],
-                                  "frac_of_nominal": path_bytes / step_s / 1e9 / NOMINAL_HBM_GBS,
-                                  "note": f"logits + gathered embedding rows over {pk['source']} HBM peak "
-                                          f"(frac_of_nominal: over the nominal {NOMINAL_HBM_GBS:.0f} GB/s)"},
-            "roofline": roofline, "stages": stages, "cpu_baseline": cpu, "e2e": e2e,
-            "clocks": clocks, "gpu_launches": launches,
-            **({"stochastic_verify": stoch} if stoch is not None else {}),
-            "execution": ("CUDA graph replay of dcoco_correct, one graph per input set" if graphs is not None
-                          else "one dcoco_correct call per step"),
-            "eager": {"ms_per_step": eager_ms / args.steps, "value": world * N / (eager_ms / args.steps / 1e3),
-                      "step_us_p50": 1e3 * statistics.median(eager_per)},
-        }
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    cfg = {"workload": f"{w['name']}: {w['desc']}", "global_batch": world * N, "per_gpu_batch": N,
+           "parallelism": f"replicas x{world}", "inputs": "bf16; arithmetic fp32",
+           "candidate_features": bool(args.features),
+           "path_rule": args.path_rule if args.path_rule != "beam" else
+           f"beam (width {args.beam_width}, top-m {args.beam_topm or K})",
+           "l2": f"{sets_n} rotating input sets of {N * S * (V + d) * 2 / 1e6:.0f} MB "
+                 f"(> 129 MB L2 in all), no flush"}
+    return {
+        "metric": METRIC if w["name"] == WORKLOADS["c32"]["name"] else
+        f"corrected draft blocks/s ({w['name']}); % of HBM roofline",
+        "value": value, "unit": "blocks/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded, synth/ recipe drawn on the GPU)", "config": cfg,
+        "us_per_block": step_s * 1e6 / N,
+        "step_us": {"p10": 1e3 * sorted(per)[len(per) // 10], "p50": 1e3 * statistics.median(per),
+                    "p90": 1e3 * sorted(per)[(9 * len(per)) // 10]},
+        "path_hbm_roofline": {"bytes_per_step": path_bytes, "achieved_gbs": path_bytes / step_s / 1e9,
+                              "peak_gbs": pk["hbm_gbs"], "frac": path_bytes / step_s / 1e9 / pk["hbm_gbs"],
+                              "frac_of_nominal": path_bytes / step_s / 1e9 / NOMINAL_HBM_GBS,
+                              "note": f"logits + gathered embedding rows over the {pk['source']} HBM peak "
+                                      f"(frac_of_nominal: over the nominal {NOMINAL_HBM_GBS:.0f} GB/s)"},
+        "roofline": roofline, "stages": stages, "cpu_baseline": cpu, "e2e": e2e, "parity": parity,
+        "clocks": clocks, "gpu_launches": launches,
+        **({"stochastic_verify": stoch} if stoch is not None else {}),
+        "execution": ("CUDA graph replay of dcoco_correct, one graph per input set" if graphs is not None
+                      else "one dcoco_correct call per step"),
+        "eager": {"ms_per_step": eager_ms / args.steps, "value": world * N / (eager_ms / args.steps / 1e3),
+                  "step_us_p50": 1e3 * statistics.median(eager_per)},
+    }
+
+
+def e2e_leg(args, torch, dc, dist, world, device, corr, set0, E, N, B):
+    """The same metric through dcoco_correct_host: host buffers in and out, the
+    copies (or the host-link reads) inside the timed region."""
+    if args.e2e_steps <= 0:
+        return None
+    lg, hd, tg = set0
+    lg_h = lg.view(torch.int16).cpu().pin_memory()
+    hd_h = hd.view(torch.int16).cpu().pin_memory()
+    tg_h = tg.cpu().pin_memory()
+    tok_h = torch.empty(N, B, dtype=torch.int32).pin_memory()
+    acc_h = torch.empty(N, dtype=torch.int32).pin_memory()
+    for _ in range(3):
+        dc.dcoco_correct_host(corr.handle, corr.weights, N, lg_h, hd_h, E, tg_h, tokens=tok_h, accept_len=acc_h)
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        dc.dcoco_correct_host(corr.handle, corr.weights, N, lg_h, hd_h, E, tg_h, tokens=tok_h, accept_len=acc_h)
+    dt = max_over_ranks(torch, dist, world, device, (time.perf_counter() - t0) / args.e2e_steps)
+    return {"value": world * N / dt, "unit": "blocks/s",
+            "h2d_bytes_per_step": lg_h.numel() * 2 + hd_h.numel() * 2 + tg_h.numel() * 4,
+            "d2h_bytes_per_step": tok_h.numel() * 4 + acc_h.numel() * 4,
+            "ms_per_step": dt * 1e3, "api": "dcoco_correct_host (pinned host buffers)"}
+
+
+def stochastic_leg(args, torch, dc, corr, w, device, pk, rank):
+    N, B, V = w["N"], w["slots"] - 1, w["V"]
+    sets_n = args.sets or w["sets"]
+    tgen = torch.Generator(device=device)
+    tgen.manual_seed(4242 + rank)
+    tset = []
+    for _ in range(sets_n):
+        x = torch.randn(N * (B + 1), V, generator=tgen, device=device) * 2.0
+        hot = torch.randint(0, V, (N * (B + 1), 2), generator=tgen, device=device)
+        x.scatter_add_(1, hot, torch.rand(N * (B + 1), 2, generator=tgen, device=device) * 4.0 + 14.0)
+        tl = x.to(torch.bfloat16).view(N, B + 1, V)
+        del x
+        toks = tl[:, :B].float().argmax(-1).to(torch.int32)  # input recipe only: a plausible proposal
+        tset.append((tl, toks, torch.rand(N, B, generator=tgen, device=device),
+                     torch.rand(N, generator=tgen, device=device)))
+    vouts = [corr.verify_stochastic(*tset[i]) for i in range(sets_n)]
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(10, args.steps)
+    e0.record()
+    for i in range(reps):
+        tl, toks, ua, ud = tset[i % sets_n]
+        dc.dcoco_verify_stochastic(corr.handle, N, tl, toks, ua, ud, vouts[i % sets_n]["accept_len"],
+                                   vouts[i % sets_n]["next_token"], vouts[i % sets_n]["q_accept"])
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) / reps * 1e3
+    vb = N * (B + 1) * V * 2
+    return {"us_per_call": us, "blocks_per_s": N / (us * 1e-6), "target_logits_bytes": vb,
+            "achieved_gbs": vb / (us * 1e-6) / 1e9, "frac_of_hbm_peak": vb / (us * 1e-6) / 1e9 / pk["hbm_gbs"],
+            "mean_accept_len": float(torch.cat([o["accept_len"] for o in vouts]).float().mean()),
+            "inputs": f"{sets_n} sets of [N, B+1, V] bf16 target logits, 2 boosted tokens per row "
+                      "(U(14,18) over 2 N(0,1)), proposal = per-slot target argmax, uniforms from torch"}
+
+
+# ------------------------------------------------------------------ the serving sweep
+def run_sweep(args, torch, dc, dist, world, rank, local, device, pk):
+    """Concurrency {1..32} x three entropy tiers on Qwen3-8B shapes: per point
+    the call time (CUDA graph replay) and blocks/s; per tier the mean
+    accept_len over 128 requests, oracle-checked on sampled requests."""
+    import numpy as np
+
+    base = dict(WORKLOADS["c32"], planted=64)
+    N, S, V, d, K = base["N"], base["slots"], base["V"], base["d"], base["K"]
+    B = S - 1
+    weights_np = make_weights_np(base, 7 + rank)
+    E = gpu_embedding(torch, 11 + rank, V, d, device)
+    corr = dc.Corrector({k: torch.from_numpy(v) for k, v in weights_np.items()}, V, d, S, K,
+                        max_batch=N, host_staging=True)
+    sampler = ClockSampler(local)
+    reps = max(50, min(args.steps, 400))
+    points, tiers, t_first, t_last = [], [], None, None
+    for ti, (tier, boost) in enumerate(SWEEP_TIERS):
+        w = dict(base, boost=boost, name=f"sweep_{tier}")
+        sets = [gpu_inputs(torch, 3000 + 101 * ti + s, w, device) for s in range(4)]
+        for n in SWEEP_NS:
+            # chunks of n consecutive requests of the four sets: 4 * 32 / n
+            # distinct inputs, 627 MB of logits in all (> L2)
+            chunks = [(s, c0) for c0 in range(0, N, n) for s in range(4)]
+            outs = [corr.alloc_outputs(n, device, full=False) for _ in chunks]
+
+            def call(j, chunks=chunks, outs=outs, n=n, sets=sets):
+                s, c0 = chunks[j]
+                lg, hd, tg = sets[s]
+                corr.correct(lg[c0:c0 + n], hd[c0:c0 + n], E, tg[c0:c0 + n], out=outs[j], full=False)
+
+            for j in range(len(chunks)):
+                call(j)
+            torch.cuda.synchronize()
+            graphs = []
+            cap = torch.cuda.Stream()
+            for j in range(len(chunks)):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cap):
+                    call(j)
+                graphs.append(g)
+            for g in graphs:
+                g.replay()
+            torch.cuda.synchronize()
+            tot, _, h0, h1 = timed_loop(torch, dist, world, device, reps,
+                                        lambda i, graphs=graphs: graphs[i % len(graphs)].replay())
+            t_first = t_first or h0
+            t_last = h1
+            us = tot / reps * 1e3
+            points.append({"tier": tier, "requests": n, "us_per_call": us, "blocks_per_s": world * n / (us * 1e-6),
+                           "us_per_block": us / n,
+                           "hbm_frac": algorithmic_bytes(dict(w, N=n)) / (us * 1e-6) / 1e9 / pk["hbm_gbs"]})
+            del graphs
+        # accept_len at 32 requests over the four sets; sampled requests checked against the oracle
+        accs, sampled = [], None
+        for s in range(4):
+            lg, hd, tg = sets[s]
+            o = corr.correct(lg, hd, E, tg, full=True)
+            torch.cuda.synchronize()
+            accs.append(o["accept_len"].cpu().numpy())
+            if s == 0:
+                sampled = ({k: v[[0, N - 1]].cpu().numpy() for k, v in o.items()},
+                           (u16(torch, lg), u16(torch, hd), tg.cpu().numpy()))
+        acc = np.concatenate(accs)
+        entry = {"tier": tier, "boost": list(boost), "planted": 64, "requests": int(acc.size),
+                 "mean_accept_len": float(acc.mean()), "mean_tau": float(acc.mean()) + 1.0}
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            import oracle
+            gpu, (lgh, hdh, tgh) = sampled
+            m = oracle.Model(weights_np, V=V, d=d, slots=S, K=K)
+            ref = oracle.correct_batch(m, lgh, hdh, u16(torch, E), tgh, requests=[0, N - 1], threads=2)
+            ok, err, near = parity_check(ref, gpu, tgh, B)
+            entry["oracle_check"] = {"requests": [0, N - 1], "parity_ok": ok, "max_score_err": err,
+                                     "near_tie_divergences": near,
+                                     "oracle_accept_len": [int(x) for x in ref["accept_len"]],
+                                     "gpu_accept_len": [int(x) for x in gpu["accept_len"]]}
+        tiers.append(entry)
+        del sets
+    clocks = sampler.summary(t_first, t_last)
+    sampler.stop()
+    head = next(p for p in points if p["tier"] == "U(4,12)" and p["requests"] == N)
+    set0 = gpu_inputs(torch, 5000, base, device)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        lg, hd, tg = set0
+        host = (u16(torch, lg), u16(torch, hd), u16(torch, E), tg.cpu().numpy())
+        cpu, _ = oracle_leg(base, host, weights_np, [0, N - 1], 0, 2, 0, min(N, 2 * (os.cpu_count() or 1)))
+    e2e = e2e_leg(args, torch, dc, dist, world, device, corr, set0, E, N, B)
+    corr.close()
+    return {
+        "metric": "corrected draft blocks/s, serving sweep (requests x entropy tier); % of HBM roofline",
+        "value": head["blocks_per_s"], "unit": "blocks/s", "n_gpus": world, "steps": reps,
+        "warmup": 1, "ms_per_step": head["us_per_call"] / 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded, synth/ recipe drawn on the GPU)",
+        "config": {"workload": "sweep: requests in {1,2,4,8,16,32} x tiers of 64 planted tokens per slot with "
+                               "boost U(2,6) / U(4,12) / U(8,16), Qwen3-8B shapes (V=151936, d=4096, K=16); "
+                               "value = the U(4,12) tier at 32 requests",
+                   "l2": "chunks of n requests from 4 input sets per tier (627 MB of logits per tier)"},
+        "points": points, "tiers": tiers,
+        "roofline": {"kernel": "whole call", "bound": "hbm", "achieved": head["hbm_frac"] * pk["hbm_gbs"],
+                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": head["hbm_frac"], "traffic": None,
+                     "peak_source": pk["source"]},
+        "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+        "gpu_launches": 4 * reps * len(points),
+    }
 
 
 # ------------------------------------------------------------------ one stage alone
@@ -491,21 +763,22 @@ def run_only(args):
     __graft_entry__.build()
     import draft_correction_slot_gb300 as dc
 
-    w = dict(WORKLOAD)
+    w = dict(WORKLOADS["c32"])
     pk = peaks()
     N, S, V, K = w["N"], w["slots"], w["V"], w["K"]
     device = torch.device("cuda", 0)
-    sets = [gpu_inputs(torch, 1000 + s, w, device, with_targets=False)[0] for s in range(args.sets)]
+    sets_n = args.sets or w["sets"]
+    sets = [gpu_inputs(torch, 1000 + s, w, device, with_targets=False)[0] for s in range(sets_n)]
     h = dc.dcoco_create(V, 64, S, K, max_batch=N)
     ids = torch.empty(N, S - 1, K, dtype=torch.int32, device=device)
     vals = torch.empty(N, S - 1, K, dtype=torch.float32, device=device)
     for i in range(args.warmup):
-        dc.dcoco_topk(h, N, sets[i % args.sets], ids, vals)
+        dc.dcoco_topk(h, N, sets[i % sets_n], ids, vals)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
     for i in range(args.steps):
-        dc.dcoco_topk(h, N, sets[i % args.sets], ids, vals)
+        dc.dcoco_topk(h, N, sets[i % sets_n], ids, vals)
     e1.record()
     torch.cuda.synchronize()
     dt = e0.elapsed_time(e1) / args.steps / 1e3
@@ -527,15 +800,15 @@ def run_reference(args):
     import oracle
     import synth
     oracle.build()
-    w = dict(WORKLOAD)
-    threads = os.cpu_count() or 1
-    per_step = max(1, min(threads, w["N"]))
+    w = dict(WORKLOADS.get(args.workload, WORKLOADS["c32"]))
+    model, ncpu = host_cpu()
+    per_step = max(1, min(ncpu, w["N"]))
     rng = np.random.default_rng(1234)
     log(f"[reference] generating inputs ({per_step} requests, embedding table {w['V']}x{w['d']})")
     logits = synth.make_logits(rng, per_step, w["slots"], w["V"], w["planted"], w["boost"])
     hidden = synth.make_hidden(rng, per_step, w["slots"], w["d"])
     E = synth.make_embedding(rng, w["V"], w["d"])
-    weights = synth.make_weights(rng, w["d"])
+    weights = synth.make_weights(rng, w["d"]) if w["variant"] == 0 else synth.make_cosine_weights(rng, w["d"])
     m = oracle.Model(weights, V=w["V"], d=w["d"], slots=w["slots"], K=w["K"])
     top16 = np.stack([np.stack([oracle.topk_row(logits[n, i + 1], 16)[0] for i in range(w["slots"] - 1)])
                       for n in range(per_step)])
@@ -545,7 +818,8 @@ def run_reference(args):
     m.dims.beam_width, m.dims.beam_topm = args.beam_width, args.beam_topm
 
     def step():
-        oracle.correct_batch(m, logits, hidden, E, targets, threads=threads, path_rule=path_rule)
+        oracle.correct_batch(m, logits, hidden, E, targets, threads=per_step, path_rule=path_rule,
+                             variant=w["variant"], sigma=w["sigma"])
 
     for _ in range(args.warmup):
         step()
@@ -559,10 +833,11 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded, synth/ recipe)",
         "impl": "reference",
-        "config": {"workload": "qwen3_8b_c32 (per-step sample: see cpu_baseline)", "global_batch": w["N"],
+        "config": {"workload": f"{w['name']} (per-step sample: see cpu_baseline)", "global_batch": w["N"],
                    "per_gpu_batch": w["N"], "parallelism": "host cores"},
-        "cpu_baseline": {"value": value, "unit": "blocks/s", "cores": threads, "kind": "oracle",
-                         "sample": f"each step: {per_step} of the 32 requests, one host thread each"},
+        "cpu_baseline": {"value": value, "unit": "blocks/s", "cores": per_step, "kind": "oracle",
+                         "sample": f"each step: {per_step} of the {w['N']} requests, one host thread each",
+                         "nproc": ncpu, "cpu_model": model},
         "e2e": {"value": value, "unit": "blocks/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -20,6 +21,7 @@ struct Workspace {
   unsigned long long *part = nullptr;
   float2 *part_lse = nullptr;  // per (row, segment) (maximum, sum of exp) for the candidate features
   unsigned *row_count = nullptr;
+  unsigned *row_ready = nullptr;  // per draft-slot row: top-K stored (1), cleared by the projection
   int32_t *ids = nullptr;
   float *vals = nullptr;
   float *slot_proj = nullptr;  // [N*B][3r]  (variant 1: [N*B][2r])
@@ -50,12 +52,14 @@ struct Workspace {
 namespace {
 constexpr int kMaxStages = 8;
 constexpr int kMaxTimedCalls = 1024;
-const char *const kStageNames[2][kMaxStages] = {
+// Stage lists of the launch orders: 0 the MLP variant, 1 the cosine variant.
+constexpr int kStageKinds = 2;
+const char *const kStageNames[kStageKinds][kMaxStages] = {
     {"topk", "proj", "maps", "pair_walk", nullptr, nullptr, nullptr, nullptr},
     {"topk", "proj", "cos_post", "cos_score", "walk_verify", nullptr, nullptr, nullptr}};
-int stage_count(int variant) {
+int stage_count(int kind) {
   int n = 0;
-  while (n < kMaxStages && kStageNames[variant][n]) ++n;
+  while (n < kMaxStages && kStageNames[kind][n]) ++n;
   return n;
 }
 }  // namespace
@@ -76,6 +80,8 @@ struct dcoco_handle {
   long long launches = 0;            // kernels launched so far
   bool timing = false;               // record per-stage events
   int timed_calls = 0;               // calls recorded since the last read
+  int timed_kind[1024] = {};          // stage list of each recorded call
+  int read_kind = -1;                 // stage list of the last dcoco_stage_read
   std::vector<cudaEvent_t> events;   // kMaxTimedCalls x (stages + 1), created on demand
 };
 
@@ -133,6 +139,7 @@ void carve_workspace(Carver &c, const dcoco_config &cfg, int B, int topk_segment
   ws.part = c.take<unsigned long long>(rows * (size_t)topk_segments_max * K);
   ws.part_lse = c.take<float2>(rows * (size_t)topk_segments_max);
   ws.row_count = c.take<unsigned>(rows);
+  ws.row_ready = c.take<unsigned>(rows);
   ws.ids = c.take<int32_t>(cands);
   ws.vals = c.take<float>(cands);
   ws.slot_proj = c.take<float>(rows * 3 * kR);
@@ -246,16 +253,17 @@ inline int beam_topm(const dcoco_config &cfg) { return cfg.beam_topm > 0 ? cfg.b
 struct StageClock {
   dcoco_handle *h;
   cudaStream_t st;
-  cudaEvent_t *ev = nullptr;  // stages + 1 events of this call, or null
+  cudaEvent_t *ev = nullptr;  // kMaxStages + 1 events of this call, or null
   int s = 0;
-  StageClock(dcoco_handle *h_, cudaStream_t st_) : h(h_), st(st_) {
+  StageClock(dcoco_handle *h_, cudaStream_t st_, int kind) : h(h_), st(st_) {
     if (h->timing && h->timed_calls < kMaxTimedCalls) {
-      const int ns = stage_count(h->cfg.variant) + 1;
-      ev = h->events.data() + (size_t)h->timed_calls * ns;
+      ev = h->events.data() + (size_t)h->timed_calls * (kMaxStages + 1);
+      h->timed_kind[h->timed_calls] = kind;
       ++h->timed_calls;
       cudaEventRecord(ev[0], st);
     }
   }
+  // a launch that ends a stage
   cudaError_t done(cudaError_t e) {
     ++h->launches;
     ++s;
@@ -265,8 +273,11 @@ struct StageClock {
 };
 
 // The launch sequence; all pointers are device pointers and validated.
+// logits_in_host_memory: the logits are page-locked host memory read in
+// place (dcoco_correct_host); the top-K then reads them with ordinary loads
+// (the one-pass kernel) rather than bulk asynchronous copies.
 int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs *in,
-             const dcoco_outputs *out, cudaStream_t st) {
+             const dcoco_outputs *out, cudaStream_t st, bool logits_in_host_memory = false) {
   const dcoco_config &cfg = h->cfg;
   const Workspace &ws = h->ws;
   const int B = h->B, K = cfg.topk, d = cfg.hidden, V = cfg.vocab;
@@ -279,17 +290,13 @@ int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs 
   int32_t *choice = out->choice ? out->choice : ws.choice;
   float *margin = out->margin ? out->margin : ws.margin;
   h->last_stream = st;
-  StageClock clk(h, st);
+  // the top-K hands its rows to the projection one by one (flags), except
+  // with the candidate features (the features' top-K accumulates the
+  // log-sum-exp) or logits in host memory (read by ordinary loads)
+  const bool handoff = out->cand_feat == nullptr && !logits_in_host_memory;
+  StageClock clk(h, st, cfg.variant);
 
   const int rows = N * B, cands = rows * K;
-  const dc::TopkPlan plan = dc::topk_plan(V, N * B, h->topk_wave);
-  // step 1: candidate pools
-  DC_TRY(clk.done(dc::launch_topk(K, logits, in->logits_slot_stride, cfg.slots, N, V, plan,
-                                  ws.part, ws.row_count, ids, vals, st, false, ws.part_lse, out->cand_feat)));
-  // step 2 (and the slot-pair state): the candidate rows and the draft-slot
-  // rows go through one projection launch, which fills the device in one wave.
-  // It overlaps the top-K's tail: its blocks take SMs as the top-K's leave,
-  // the draft-slot tiles start at once and the candidate tiles wait for the ids.
   const int r_out = cfg.variant == 0 ? kR : 2 * kR;          // candidate outputs
   const int s_out = cfg.variant == 0 ? 3 * kR : 2 * kR;      // draft-slot outputs
   dc::ProjJob cj{E, ids, ws.cand_proj, cands, r_out, dc::proj_tc_tiles(cands, r_out)};
@@ -301,8 +308,26 @@ int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs 
     cj.ln_eps = cfg.ln_eps;
   }
   const dc::ProjJob sj{hidden, nullptr, ws.slot_proj, rows, s_out, dc::proj_tc_tiles(rows, s_out)};
-  DC_TRY(clk.done(dc::launch_proj_tc(cj, w->map_cand_hi, w->map_cand_lo, &sj, &w->map_slot_hi,
-                                     &w->map_slot_lo, cfg.slots, B, d, V, h->splits, ws.err, st, true)));
+  // step 1: candidate pools.  Without the candidate features each finished
+  // row releases a flag (features or logits in host memory: no handoff).
+  // (Prefetching the rows' candidate embeddings into L2 from here was
+  // measured: the top-K 4 us slower, the projection no faster.)
+  const dc::TopkPlan plan = dc::topk_plan(V, N * B, h->topk_wave);
+  dc::TopkHandoff hand;
+  if (handoff) {
+    hand.row_ready = ws.row_ready;
+    cj.row_ready = ws.row_ready;
+    cj.cands_per_row = K;
+  }
+  DC_TRY(clk.done(dc::launch_topk(K, logits, in->logits_slot_stride, cfg.slots, N, V, plan, ws.part, ws.row_count,
+                                  ids, vals, st, false, ws.part_lse, out->cand_feat, hand)));
+  // step 2 (and the slot-pair state): the candidate rows and the draft-slot
+  // rows go through one projection launch, which fills the device in one
+  // wave.  It overlaps the top-K's tail: its blocks take SMs as the top-K's
+  // leave, the draft-slot tiles start at once and each candidate tile waits
+  // for its own rows' flags (or, without the handoff, for the whole top-K).
+  DC_TRY(clk.done(dc::launch_proj_tc(cj, w->map_cand_hi, w->map_cand_lo, &sj, &w->map_slot_hi, &w->map_slot_lo,
+                                     cfg.slots, B, d, V, h->splits, ws.err, st, true)));
   if (cfg.variant == 0) {
     // steps 2-3: per-slot / per-pair terms, z and the layer-1 partials U, V
     DC_TRY(clk.done(dc::launch_maps_tc(w->mlp_maps, h->slot_io, h->cand_io, ws.slot_proj, vals, w->mlp, N, B,
@@ -656,7 +681,7 @@ int dcoco_correct_host(dcoco_handle *h, const dcoco_weights *w, int batch, const
   dcoco_outputs dout = {};
   dout.tokens = ws.st_tokens;
   dout.accept_len = in->target_tokens ? ws.st_accept : nullptr;
-  rc = run_path(h, w, batch, &din, &dout, st);
+  rc = run_path(h, w, batch, &din, &dout, st, logits_dev != nullptr);
   if (rc != DCOCO_OK) return rc;
   // outputs: tokens, accept_len (+ optional extras from the workspace)
   DC_TRY(cudaMemcpyAsync(out->tokens, ws.st_tokens, (size_t)batch * B * sizeof(int32_t),
@@ -760,7 +785,7 @@ long long dcoco_kernel_launches(const dcoco_handle *h) { return h ? h->launches 
 int dcoco_stage_timing(dcoco_handle *h, int enable) {
   if (!h) return DCOCO_EINVAL;
   if (enable && h->events.empty()) {
-    const size_t n = (size_t)kMaxTimedCalls * (stage_count(h->cfg.variant) + 1);
+    const size_t n = (size_t)kMaxTimedCalls * (kMaxStages + 1);
     h->events.resize(n, nullptr);
     for (size_t i = 0; i < n; ++i)
       if (cudaEventCreate(&h->events[i]) != cudaSuccess) {
@@ -775,26 +800,33 @@ int dcoco_stage_timing(dcoco_handle *h, int enable) {
 
 int dcoco_stage_read(dcoco_handle *h, int max_stages, float *ms, int *calls, int *n_stages) {
   if (!h || !ms || !calls || !n_stages || max_stages < 0) return DCOCO_EINVAL;
-  const int ns = stage_count(h->cfg.variant);
+  // the stage list of the first recorded call; calls with another list are skipped
+  const int kind = h->timed_calls > 0 ? h->timed_kind[0] : h->cfg.variant;
+  const int ns = stage_count(kind);
+  h->read_kind = kind;
   *n_stages = ns;
-  *calls = h->timed_calls;
+  *calls = 0;
   for (int s = 0; s < max_stages && s < ns; ++s) ms[s] = 0.f;
   for (int c = 0; c < h->timed_calls; ++c) {
-    cudaEvent_t *ev = h->events.data() + (size_t)c * (ns + 1);
+    if (h->timed_kind[c] != kind) continue;
+    cudaEvent_t *ev = h->events.data() + (size_t)c * (kMaxStages + 1);
     if (cudaEventSynchronize(ev[ns]) != cudaSuccess) return DCOCO_ECUDA;
     for (int s = 0; s < max_stages && s < ns; ++s) {
       float t = 0.f;
       if (cudaEventElapsedTime(&t, ev[s], ev[s + 1]) != cudaSuccess) return DCOCO_ECUDA;
       ms[s] += t;
     }
+    ++*calls;
   }
   h->timed_calls = 0;
   return DCOCO_OK;
 }
 
 const char *dcoco_stage_name(const dcoco_handle *h, int s) {
-  if (!h || s < 0 || s >= stage_count(h->cfg.variant)) return nullptr;
-  return kStageNames[h->cfg.variant][s];
+  if (!h) return nullptr;
+  const int kind = h->read_kind >= 0 ? h->read_kind : h->cfg.variant;
+  if (s < 0 || s >= stage_count(kind)) return nullptr;
+  return kStageNames[kind][s];
 }
 
 }  // extern "C"

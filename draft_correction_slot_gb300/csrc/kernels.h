@@ -27,16 +27,28 @@ constexpr int kTopkMaxChunks = 64;
 // holding `slots_per_wave` resident top-K CTAs.
 TopkPlan topk_plan(int V, int rows, int slots_per_wave);
 int topk_min_segments(int V);  // fewest segments whose per-vector maxima fit a CTA
+int topk_max_segment_vecs();   // 16-byte vectors a segment may hold
 int topk_max_segments(int V);
 int topk_occupancy(int K);  // resident top-K CTAs per SM
 // With `feat` (fp32 [rows][K][5]) the same pass also accumulates each row's
 // log-sum-exp and writes the candidates' vocabulary-normalised features
 // [log p, p, l_0 - l_k, k / K, k == 0]; part_lse (float2 [rows][nchunks]) is
 // then needed when nchunks > 1.
+// Handoff to a projection already running beside the top-K (launched
+// before it): the grid is one-dimensional with a row's segments adjacent, so
+// rows finish in order; each finished row releases row_ready[row] = 1 (the
+// projection clears it) and its candidates' embedding rows E[id] (d bf16
+// each) are prefetched into L2.  The kernel then does not wait for the
+// previous kernel in the stream (it is the projection, which waits for it).
+struct TopkHandoff {
+  unsigned *row_ready = nullptr;
+  const uint16_t *E = nullptr;
+  int d = 0;
+};
 cudaError_t launch_topk(int K, const uint16_t *logits, int64_t stride, int slots, int N, int V,
                         const TopkPlan &plan, unsigned long long *part, unsigned *row_count,
                         int32_t *ids, float *vals, cudaStream_t st, bool pdl, float2 *part_lse = nullptr,
-                        float *feat = nullptr);
+                        float *feat = nullptr, const TopkHandoff &hand = TopkHandoff());
 
 // ---------------------------------------------------------------- projections
 // C[m][o] = sum_k A_m[k] * W[o][k] with A_m a bf16 row of length d, on the
@@ -63,6 +75,12 @@ struct ProjJob {
   // rounding remainder, ln_lo) instead of fp32 in C.
   uint16_t *ln_hi = nullptr, *ln_lo = nullptr;
   float ln_eps = 0.f;
+  // With row_ready set (a gathering job launched before the top-K that
+  // fills it, see TopkHandoff), a tile waits for the flags of its draft-slot
+  // rows (candidate m belongs to row m / cands_per_row) instead of for the
+  // previous kernel, and clears them when done.
+  unsigned *row_ready = nullptr;
+  int cands_per_row = 0;
 };
 int proj_tc_splits(int d, int requested);
 int proj_tc_tiles(int M, int No);

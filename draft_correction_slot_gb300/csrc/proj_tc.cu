@@ -72,7 +72,7 @@ struct ProjGeom {
   static constexpr int kSmemUsed = kRingA + kStagesW * 2 * kSubBytes;
   static constexpr uint32_t kTmemCols = MT * 256;  // per accumulator: hi products, then lo
   static_assert(kSmemUsed + 1024 <= 227 * 1024 - 1024, "shared memory");
-  static_assert(MT * 4 * kBoxBytes <= kRingA, "the output tile is staged in the A ring");
+  static_assert(MT * 4 * kBoxBytes <= kSmemUsed, "the output tile is staged in the (idle) rings");
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
@@ -143,6 +143,9 @@ k_proj_tc(ProjJob job0, ProjJob job1, const __grid_constant__ CUtensorMap map0_h
   uint16_t *__restrict__ ln_hi = job.ln_hi;
   uint16_t *__restrict__ ln_lo = job.ln_lo;
   const float ln_eps = job.ln_eps;
+  // candidate rows [m0, m0 + kTileM) come from draft-slot rows row_first..row_last
+  const int row_first = job.row_ready ? m0 / job.cands_per_row : 0;
+  const int row_last = job.row_ready ? (min(m0 + kTileM, M) - 1) / job.cands_per_row : -1;
   const int nkb_total = d / kTileK;
   const int kb0 = split * kb_per_split;
   const int nkb = min(kb_per_split, nkb_total - kb0);
@@ -176,7 +179,16 @@ k_proj_tc(ProjJob job0, ProjJob job1, const __grid_constant__ CUtensorMap map0_h
     // buffer no earlier kernel of the call touches, so it need not wait.  (The
     // weight stream below starts at once either way.)
     static_assert(G::kGather == kTileM, "one gather thread per tile row");
-    if (ids) pdl_wait();
+    if (ids && job.row_ready) {
+      // the tile's draft-slot rows, one waiting thread each: the streaming
+      // top-K releases each row's flag once its ids are stored
+      if (tid <= row_last - row_first &&
+          !wait_flag(job.row_ready + row_first + tid, &s_abort, err))
+        s_abort = 1;
+      asm volatile("bar.sync 1, %0;" ::"n"(G::kGather) : "memory");
+    } else if (ids) {
+      pdl_wait();
+    }
     {
       const int m = m0 + tid;
       int row = 0;  // rows past M load table row 0; their results are never stored
@@ -410,6 +422,9 @@ k_proj_tc(ProjJob job0, ProjJob job1, const __grid_constant__ CUtensorMap map0_h
     }
   }
   cluster_sync();
+  // every CTA of the cluster is past its flag wait: clear the flags for the
+  // next call
+  if (job.row_ready && cluster_ctarank() == 0 && tid <= row_last - row_first) job.row_ready[row_first + tid] = 0u;
 }
 
 }  // namespace
@@ -482,7 +497,7 @@ cudaError_t launch_proj_tc(const ProjJob &a, const CUtensorMap &a_hi, const CUte
   using G = ProjGeom<MT>;
   auto bad = [&](const ProjJob &j) {
     return j.No % kTileN != 0 || j.M < 0 || !j.table || (!j.C && !j.ln_hi) ||
-           (j.ln_hi && (j.No != kTileN || !j.ln_lo)) ||
+           (j.ln_hi && (j.No != kTileN || !j.ln_lo)) || (j.row_ready && (!j.ids || j.cands_per_row < 1)) ||
            j.tiles != ((j.M + G::kTileM - 1) / G::kTileM) * (j.No / kTileN);
   };
   if (d % kTileK != 0 || splits < 1 || splits > kMaxSplits || (kSubM % splits) != 0 || bad(a) ||

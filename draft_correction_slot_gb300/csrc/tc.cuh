@@ -64,6 +64,34 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// Bounded wait until *flag == 1 (acquire, device scope), for flags another
+// kernel running beside this one releases; false on timeout (then `abort`
+// is set and `err` records kErrTimeout) or when another role aborted.
+__device__ __forceinline__ bool wait_flag(const unsigned *flag, volatile int *abort, int *err,
+                                          unsigned long long limit_ns = kWaitNs) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+  if (v == 1u) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(64);
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v == 1u) return true;
+    if ((it & 15u) == 0u) {
+      if (*abort) return false;
+      if (global_ns() - t0 > limit_ns) {
+        *abort = 1;
+        atomicOr(err, ::dc::kErrTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void st_release_gpu(unsigned *p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Bounded wait used only on the abort path, ignoring the abort flag: lets
 // copies and MMAs already issued land before the CTA frees its resources.
 __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {

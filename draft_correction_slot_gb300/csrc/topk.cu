@@ -34,6 +34,7 @@
 #include "common.cuh"
 #include "kernels.h"
 #include "launch.h"
+#include "topk_warp.cuh"
 
 namespace dc {
 
@@ -54,75 +55,7 @@ constexpr int kMaxHitsPerLane = 4;    // hit vectors a lane re-loads (more: dege
 constexpr int kCandElems = 8 * kWarps * 32 * kMaxHitsPerLane / 4;  // key buffer (fits s_raw)
 constexpr uint32_t kNegInf2 = 0xFF80FF80u;
 
-typedef unsigned long long u64;
-
-__device__ __forceinline__ u64 make_key(uint32_t bits16, uint32_t id) {
-  return ((u64)bf16_order_key(bits16) << 32) | (u64)(0xFFFFFFFFu - id);
-}
-
-__device__ __forceinline__ u64 shfl_u64(u64 v, int src) {
-  uint32_t lo = __shfl_sync(DC_FULL_MASK, (uint32_t)v, src);
-  uint32_t hi = __shfl_sync(DC_FULL_MASK, (uint32_t)(v >> 32), src);
-  return ((u64)hi << 32) | lo;
-}
-
-__device__ __forceinline__ u64 shfl_up_u64(u64 v) {
-  uint32_t lo = __shfl_up_sync(DC_FULL_MASK, (uint32_t)v, 1);
-  uint32_t hi = __shfl_up_sync(DC_FULL_MASK, (uint32_t)(v >> 32), 1);
-  return ((u64)hi << 32) | lo;
-}
-
-// Insert `key` (warp-uniform, unique) into the descending register list.
-template <int K>
-__device__ __forceinline__ void warp_insert(u64 &list, u64 &kth, u64 key, int lane) {
-  const u64 prev = shfl_up_u64(list);
-  u64 nl = (list > key) ? list : ((lane == 0 || prev > key) ? key : prev);
-  list = lane < K ? nl : 0ull;
-  kth = shfl_u64(list, K - 1);
-}
-
-__device__ __forceinline__ u64 shfl_xor_key(u64 v, int m) {
-  uint32_t lo = __shfl_xor_sync(DC_FULL_MASK, (uint32_t)v, m);
-  uint32_t hi = __shfl_xor_sync(DC_FULL_MASK, (uint32_t)(v >> 32), m);
-  return ((u64)hi << 32) | lo;
-}
-__device__ __forceinline__ u64 shfl_key(u64 v, int src) { return shfl_u64(v, src); }
-
-// Bitonic sort of one key per lane, descending over the 32 lanes.
-template <class T>
-__device__ __forceinline__ T warp_sort32_desc(T x, int lane) {
-#pragma unroll
-  for (int k = 2; k <= 32; k <<= 1) {
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      const T o = shfl_xor_key(x, j);
-      const bool keep_max = (((lane & j) == 0) == ((lane & k) == 0));
-      x = keep_max ? (o > x ? o : x) : (o < x ? o : x);
-    }
-  }
-  return x;
-}
-
-// Top K of two descending lists held in lanes (a: lanes < K, b: 32 lanes,
-// zero padded): max(a_i, b_{K-1-i}) is the top-K set as a bitonic sequence;
-// a half-cleaner network sorts it.
-template <int K, class T>
-__device__ __forceinline__ T warp_merge_topk(T a, T b, int lane) {
-  const T br = shfl_key(b, (K - 1 - lane) & 31);
-  T x = (lane < K) ? (a > br ? a : br) : T(0);
-#pragma unroll
-  for (int j = K >> 1; j > 0; j >>= 1) {
-    const T o = shfl_xor_key(x, j);
-    const bool lower = (lane & j) == 0;
-    x = lower ? (o > x ? o : x) : (o < x ? o : x);
-  }
-  return lane < K ? x : T(0);
-}
-
-// bf16 bits with order key one below / above `key` (saturating).
-__device__ __forceinline__ uint32_t bf16_from_key(uint32_t key) {
-  return (key & 0x8000u) ? (key & 0x7FFFu) : (~key & 0xFFFFu);
-}
+using namespace topk_warp;
 
 // Logits are read once by the stream and again, for the few vectors that
 // reach the bound, right after it: normal L2 priority keeps those re-reads
@@ -351,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 4)
 k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, int V, int nseg,
        int seg_vecs, u64 *__restrict__ part, unsigned *__restrict__ row_count,
        int32_t *__restrict__ out_ids, float *__restrict__ out_val, float2 *__restrict__ part_lse,
-       float *__restrict__ out_feat) {
+       float *__restrict__ out_feat, TopkHandoff hand) {
   // s_vmax (pass 1-2: per-vector maxima, bf16 bits), s_keys (pass 3:
   // candidate elements) and the fallback's per-warp candidate buffers share
   // storage; each use ends at a barrier before the next begins
@@ -371,7 +304,10 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
   __shared__ float s_lm[kWarps], s_ls[kWarps];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int row = blockIdx.x, seg = blockIdx.y;
+  // with the handoff the grid is one-dimensional, segments of a row adjacent
+  // (blocks are dispatched in index order, so rows finish from the first on)
+  const int row = hand.row_ready ? (int)blockIdx.x / nseg : (int)blockIdx.x;
+  const int seg = hand.row_ready ? (int)blockIdx.x - row * nseg : (int)blockIdx.y;
   const int n = row / B, i = row - n * B;
   const uint16_t *rowp = logits + ((int64_t)n * slots + i + 1) * stride;
   const int nvec = V >> 3, tail = V & 7;
@@ -607,8 +543,9 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
   }
 
   // everything above only reads the logits; the previous kernel in the stream
-  // may still read the buffers written below
-  pdl_wait();
+  // may still read the buffers written below -- except with the handoff, where
+  // the previous kernel is the projection, which waits for this one's rows
+  if (!hand.row_ready) pdl_wait();
   if (nseg > 1) {
     u64 *my = part + ((int64_t)row * nseg + seg) * K;
     if (tid < K) {
@@ -666,6 +603,22 @@ k_topk(const uint16_t *__restrict__ logits, int64_t stride, int slots, int B, in
       f[4] = tid == 0 ? 1.f : 0.f;
     }
   }
+  if (hand.row_ready && warp == 0) {
+    // hand the row to the projection: release its flag once its ids and
+    // values are stored, and bring its candidates' embedding rows to L2
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence();
+      asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(hand.row_ready + row), "r"(1u) : "memory");
+    }
+    if (hand.E && lane < K) {
+      const uint32_t id = 0xFFFFFFFFu - (uint32_t)(s_top[lane] & 0xFFFFFFFFull);
+      if (id < (uint32_t)V)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(hand.E + (int64_t)id * hand.d),
+                     "r"((uint32_t)hand.d * 2u)
+                     : "memory");
+    }
+  }
 }
 
 }  // namespace
@@ -691,6 +644,8 @@ TopkPlan topk_plan(int V, int rows, int slots_per_wave) {
   p.chunk_vecs = (nvec + p.nchunks - 1) / p.nchunks;  // vectors per segment
   return p;
 }
+
+int topk_max_segment_vecs() { return kMaxSegVecs; }
 
 int topk_min_segments(int V) {
   const int nvec = std::max(1, V >> 3);
@@ -726,34 +681,37 @@ template <int K>
 static cudaError_t launch_topk_k(const dim3 &grid, const dim3 &block, cudaStream_t st, bool pdl,
                                  const uint16_t *logits, int64_t stride, int slots, int B, int V, const TopkPlan &plan,
                                  unsigned long long *part, unsigned *row_count, int32_t *ids, float *vals,
-                                 float2 *part_lse, float *feat) {
+                                 float2 *part_lse, float *feat, const TopkHandoff &hand) {
   if (feat)
     return launch_ex(k_topk<K, true>, grid, block, 0, st, pdl, 0, logits, stride, slots, B, V, plan.nchunks,
-                     plan.chunk_vecs, part, row_count, ids, vals, part_lse, feat);
+                     plan.chunk_vecs, part, row_count, ids, vals, part_lse, feat, hand);
   return launch_ex(k_topk<K, false>, grid, block, 0, st, pdl, 0, logits, stride, slots, B, V, plan.nchunks,
-                   plan.chunk_vecs, part, row_count, ids, vals, part_lse, feat);
+                   plan.chunk_vecs, part, row_count, ids, vals, part_lse, feat, hand);
 }
 
 cudaError_t launch_topk(int K, const uint16_t *logits, int64_t stride, int slots, int N, int V,
                         const TopkPlan &plan, unsigned long long *part, unsigned *row_count,
-                        int32_t *ids, float *vals, cudaStream_t st, bool pdl, float2 *part_lse, float *feat) {
+                        int32_t *ids, float *vals, cudaStream_t st, bool pdl, float2 *part_lse, float *feat,
+                        const TopkHandoff &hand) {
   const int B = slots - 1;
   if (N == 0) return cudaSuccess;
   if (feat && plan.nchunks > 1 && !part_lse) return cudaErrorInvalidValue;
-  const dim3 grid(N * B, plan.nchunks), block(kThreads);
+  if (hand.row_ready && feat) return cudaErrorInvalidValue;
+  const dim3 grid = hand.row_ready ? dim3(N * B * plan.nchunks, 1) : dim3(N * B, plan.nchunks);
+  const dim3 block(kThreads);
   cudaError_t e;
   switch (K) {
     case 8:
       e = launch_topk_k<8>(grid, block, st, pdl, logits, stride, slots, B, V, plan, part, row_count, ids, vals,
-                           part_lse, feat);
+                           part_lse, feat, hand);
       break;
     case 16:
       e = launch_topk_k<16>(grid, block, st, pdl, logits, stride, slots, B, V, plan, part, row_count, ids, vals,
-                            part_lse, feat);
+                            part_lse, feat, hand);
       break;
     case 32:
       e = launch_topk_k<32>(grid, block, st, pdl, logits, stride, slots, B, V, plan, part, row_count, ids, vals,
-                            part_lse, feat);
+                            part_lse, feat, hand);
       break;
     default:
       return cudaErrorInvalidValue;

@@ -306,7 +306,7 @@ int dcoco_stage_timing(dcoco_handle *h, int enable);
 int dcoco_stage_read(dcoco_handle *h, int max_stages, float *ms, int *calls, int *n_stages);
 
 /* Tracing: name of kernel stage `s` of the handle's variant ("topk",
- * "slot_proj", ...), or NULL if out of range. */
+ * "proj", ...), or NULL if out of range. */
 const char *dcoco_stage_name(const dcoco_handle *h, int s);
 
 /* Release packed weights / the handle.  NULL is allowed.  Synchronises the
