@@ -132,7 +132,7 @@ def maps_method_flops(w) -> int:
     return 2 * N * (B * r * r + (B - 1) * r * H) + 2 * N * B * K * (r * r + 2 * r * H)
 
 
-FMA_LANE_OPS_PER_GELU = 11  # the pair loop's FMA-pipe lane operations per w2*GELU element
+FMA_LANE_OPS_PER_GELU = 9  # the pair loop's FMA-pipe lane operations per w2*GELU element
 
 
 def fma_lane_rate(pk) -> float:
@@ -478,12 +478,20 @@ def run_workload(args, w, torch, dc, dist, world, rank, local, device, pk):
     on0 = [i for i in range(args.steps) if (args.warmup + i) % sets_n == 0]
     checked = sorted({on0[0], on0[len(on0) // 2], on0[-1]}) if on0 else []
     check_reqs = sorted({0, N // 2, N - 1})
-    keep = {}
     names = ("topk_ids", "topk_val", "scores", "choice", "tokens", "accept_len", "margin")
+    # one device copy of set 0's outputs per checked iteration, allocated (and
+    # the copy exercised) before timing: inside the timed region a checked
+    # iteration adds one device-to-device copy of its ~0.5 MB of outputs
+    keep = {i: {k: torch.empty_like(outs[0][k]) for k in names} for i in checked}
+    for i in checked:
+        for k in names:
+            keep[i][k].copy_(outs[0][k])
+    checked_set = set(checked)
 
     def hook(i):
-        if i in checked:  # a copy of 3 requests' outputs after the call, on the same stream
-            keep[i] = {k: outs[0][k][check_reqs].clone() for k in names}
+        if i in checked_set:
+            for k in names:
+                keep[i][k].copy_(outs[0][k], non_blocking=True)
 
     eager_ms, eager_per, _, _ = timed_loop(torch, dist, world, device, args.steps,
                                            lambda i: step(args.warmup + i))
@@ -539,7 +547,7 @@ def run_workload(args, w, torch, dc, dist, world, rank, local, device, pk):
                               all_core_reqs=min(N, 2 * (os.cpu_count() or 1)))
         results = []
         for i in checked:
-            gpu = {k: v.cpu().numpy() for k, v in keep[i].items()}
+            gpu = {k: v[check_reqs].cpu().numpy() for k, v in keep[i].items()}
             if path_rule == 0:
                 ok, err, near = parity_check(ref, gpu, host[3], B)
             else:  # the path rules' own decision checks live in the tests; ids and scores here

@@ -223,6 +223,35 @@ def test_full_size_batch32_sampled(torch_cuda):
     np.testing.assert_array_equal(g["topk_ids"], top16)
 
 
+@pytest.mark.slow
+def test_full_size_cosine_batch16_sampled(torch_cuda):
+    """The cosine variant at its own batch of 16 (Qwen3-8B shapes, the
+    launch the benchmark times): every request's top-K in full, the oracle
+    on sampled requests."""
+    prob = Problem(41, N=16, V=V_QWEN, d=D_QWEN, variant=1, sigma=1.0, targets=False)
+    top16 = prob.oracle_top16()
+    prob.targets = synth.draw_targets(prob.rng, top16, prob.V)
+    g = run_gpu(prob)
+    np.testing.assert_array_equal(g["topk_ids"], top16)
+    report("cosine batch16", compare(prob, g, prob.oracle(requests=[0, 7, 15])))
+
+
+@pytest.mark.slow
+def test_full_size_wide_k32_d5120_batch32_sampled(torch_cuda):
+    """d = 5120, K = 32, 8 planted tokens per slot with boost U(8,16), at the
+    batch of 32 the benchmark times: 60 candidate tiles of the projection
+    (66 four-CTA clusters with the draft-slot tiles, more than one wave) and
+    1920 pair scores.  Every request's top-K in full (the first 16 of the
+    oracle's top 32 for the targets), the oracle on sampled requests."""
+    prob = Problem(42, N=32, V=V_QWEN, d=5120, K=32, planted=8, boost=(8.0, 16.0), targets=False)
+    top32 = np.stack([np.stack([oracle.topk_row(prob.logits[n, i + 1, :prob.V], 32)[0] for i in range(prob.B)])
+                      for n in range(prob.N)])
+    prob.targets = synth.draw_targets(prob.rng, top32[..., :16], prob.V)
+    g = run_gpu(prob)
+    np.testing.assert_array_equal(g["topk_ids"], top32)
+    report("wide batch32", compare(prob, g, prob.oracle(requests=[0, 31])))
+
+
 def test_host_entry_matches_device_entry(torch_cuda):
     torch = torch_cuda
     import draft_correction_slot_gb300 as dc
