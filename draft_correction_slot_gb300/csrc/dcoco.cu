@@ -90,10 +90,10 @@ struct dcoco_weights {
   int device = 0;
   void *block = nullptr;
   // projection weights as bf16 hi / lo halves, [rows][d] each
-  uint16_t *cand_hi = nullptr, *cand_lo = nullptr;  // W_cand [r][d]  (variant 1: W_io[:, :d], [2r][d])
+  uint16_t *cand_f16 = nullptr;                     // W_cand [r][d] as fp16 (variant 1: W_io[:, :d], [2r][d])
   uint16_t *slot_hi = nullptr, *slot_lo = nullptr;  // [W_ctx ; W_pair[:, :d] ; W_pair[:, d:]] [3r][d]
                                                     // (variant 1: W_io[:, d:], [2r][d])
-  CUtensorMap map_cand_hi, map_cand_lo, map_slot_hi, map_slot_lo;  // TMA maps of the halves
+  CUtensorMap map_cand_f16, map_slot_hi, map_slot_lo;  // TMA maps
   // the 128-deep maps of the MLP as bf16 hi / lo (variant 0): W_fuse[:, :r],
   // W_fuse[:, r:] ([r][r]), [W1[:, r:2r] ; W1[:, 2r:3r]] ([2H][r]), W1[:, :r] ([H][r])
   uint16_t *fb_hi = nullptr, *fb_lo = nullptr, *fg_hi = nullptr, *fg_lo = nullptr;
@@ -114,6 +114,32 @@ inline uint16_t f32_to_bf16(float f) {
   u += 0x7FFFu + ((u >> 16) & 1u);
   return (uint16_t)(u >> 16);
 }
+// fp32 -> fp16 bits, round to nearest even (subnormals kept; beyond the
+// fp16 range: infinity; NaN -> quiet NaN).
+inline uint16_t f32_to_f16(float f) {
+  uint32_t x;
+  std::memcpy(&x, &f, sizeof x);
+  const uint32_t sign = (x >> 16) & 0x8000u, ax = x & 0x7FFFFFFFu;
+  if (ax >= 0x7F800000u) return (uint16_t)(sign | (ax > 0x7F800000u ? 0x7E00u : 0x7C00u));
+  if (ax >= 0x477FF000u) return (uint16_t)(sign | 0x7C00u);  // rounds to 65536 or more
+  if (ax < 0x33000000u) return (uint16_t)sign;                // below 2^-25: rounds to 0
+  const int e = (int)(ax >> 23) - 127;
+  const uint32_t mant = (ax & 0x7FFFFFu) | 0x800000u;         // value = mant 2^(e - 23)
+  uint32_t h, rem, half;
+  if (e >= -14) {  // normal: 10 mantissa bits, 13 dropped
+    h = ((uint32_t)(e + 15) << 10) + ((mant >> 13) & 0x3FFu);
+    rem = mant & 0x1FFFu;
+    half = 0x1000u;
+  } else {         // subnormal: units of 2^-24
+    const int sh = -(e + 1);
+    h = mant >> sh;
+    rem = mant & ((1u << sh) - 1u);
+    half = 1u << (sh - 1);
+  }
+  if (rem > half || (rem == half && (h & 1u))) ++h;  // a carry moves into the exponent correctly
+  return (uint16_t)(sign | h);
+}
+
 inline float bf16_to_f32(uint16_t b) {
   const uint32_t u = (uint32_t)b << 16;
   float f;
@@ -300,6 +326,7 @@ int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs 
   const int r_out = cfg.variant == 0 ? kR : 2 * kR;          // candidate outputs
   const int s_out = cfg.variant == 0 ? 3 * kR : 2 * kR;      // draft-slot outputs
   dc::ProjJob cj{E, ids, ws.cand_proj, cands, r_out, dc::proj_tc_tiles(cands, r_out)};
+  cj.f16 = true;  // the candidate rows in fp16: one MMA per k-step
   if (cfg.variant == 0) {
     // the reduction leaves b = LN0(W_cand E[c]) ready for the fuse product
     cj.C = nullptr;
@@ -326,7 +353,7 @@ int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs 
   // wave.  It overlaps the top-K's tail: its blocks take SMs as the top-K's
   // leave, the draft-slot tiles start at once and each candidate tile waits
   // for its own rows' flags (or, without the handoff, for the whole top-K).
-  DC_TRY(clk.done(dc::launch_proj_tc(cj, w->map_cand_hi, w->map_cand_lo, &sj, &w->map_slot_hi, &w->map_slot_lo,
+  DC_TRY(clk.done(dc::launch_proj_tc(cj, w->map_cand_f16, w->map_cand_f16, &sj, &w->map_slot_hi, &w->map_slot_lo,
                                      cfg.slots, B, d, V, h->splits, ws.err, st, true)));
   if (cfg.variant == 0) {
     // steps 2-3: per-slot / per-pair terms, z and the layer-1 partials U, V
@@ -503,9 +530,12 @@ int dcoco_weights_create(dcoco_handle *h, const dcoco_weight_ptrs *wp, void *str
   // Projection weights: rows of the stacked matrices, split into bf16 hi/lo.
   const int cand_rows = cfg.variant == 0 ? r : 2 * r;
   const int slot_rows = cfg.variant == 0 ? 3 * r : 2 * r;
-  std::vector<uint16_t> proj((size_t)2 * (cand_rows + slot_rows) * d);
-  uint16_t *c_hi = proj.data(), *c_lo = c_hi + (size_t)cand_rows * d;
-  uint16_t *s_hi = c_lo + (size_t)cand_rows * d, *s_lo = s_hi + (size_t)slot_rows * d;
+  std::vector<uint16_t> proj((size_t)(cand_rows + 2 * slot_rows) * d);
+  uint16_t *c_f16 = proj.data();
+  uint16_t *s_hi = c_f16 + (size_t)cand_rows * d, *s_lo = s_hi + (size_t)slot_rows * d;
+  auto f16_row = [&](const float *src, uint16_t *dst) {
+    for (int k = 0; k < d; ++k) dst[k] = f32_to_f16(src[k]);
+  };
   auto split_row = [&](const float *src, uint16_t *hi, uint16_t *lo) {
     for (int k = 0; k < d; ++k) {
       const uint16_t hb = f32_to_bf16(src[k]);
@@ -515,7 +545,7 @@ int dcoco_weights_create(dcoco_handle *h, const dcoco_weight_ptrs *wp, void *str
   };
   if (cfg.variant == 0) {
     for (int o = 0; o < r; ++o) {
-      split_row(w_cand.data() + (size_t)o * d, c_hi + (size_t)o * d, c_lo + (size_t)o * d);
+      f16_row(w_cand.data() + (size_t)o * d, c_f16 + (size_t)o * d);
       split_row(w_ctx.data() + (size_t)o * d, s_hi + (size_t)o * d, s_lo + (size_t)o * d);
       split_row(w_pair.data() + (size_t)o * 2 * d, s_hi + (size_t)(r + o) * d, s_lo + (size_t)(r + o) * d);
       split_row(w_pair.data() + (size_t)o * 2 * d + d, s_hi + (size_t)(2 * r + o) * d,
@@ -523,7 +553,7 @@ int dcoco_weights_create(dcoco_handle *h, const dcoco_weight_ptrs *wp, void *str
     }
   } else {
     for (int o = 0; o < 2 * r; ++o) {
-      split_row(w_io.data() + (size_t)o * 2 * d, c_hi + (size_t)o * d, c_lo + (size_t)o * d);
+      f16_row(w_io.data() + (size_t)o * 2 * d, c_f16 + (size_t)o * d);
       split_row(w_io.data() + (size_t)o * 2 * d + d, s_hi + (size_t)o * d, s_lo + (size_t)o * d);
     }
   }
@@ -588,9 +618,8 @@ int dcoco_weights_create(dcoco_handle *h, const dcoco_weight_ptrs *wp, void *str
     delete w;
     return DCOCO_ECUDA;
   }
-  w->cand_hi = dproj;
-  w->cand_lo = dproj + (size_t)cand_rows * d;
-  w->slot_hi = w->cand_lo + (size_t)cand_rows * d;
+  w->cand_f16 = dproj;
+  w->slot_hi = w->cand_f16 + (size_t)cand_rows * d;
   w->slot_lo = w->slot_hi + (size_t)slot_rows * d;
   if (cfg.variant == 0) {
     w->fb_hi = w->slot_lo + (size_t)slot_rows * d;
@@ -602,8 +631,7 @@ int dcoco_weights_create(dcoco_handle *h, const dcoco_weight_ptrs *wp, void *str
     w->w1s_hi = w->w1ab_lo + n_w1ab;
     w->w1s_lo = w->w1s_hi + n_w1s;
   }
-  if (!dc::encode_bf16_rows_map(&w->map_cand_hi, w->cand_hi, cand_rows, d, 128) ||
-      !dc::encode_bf16_rows_map(&w->map_cand_lo, w->cand_lo, cand_rows, d, 128) ||
+  if (!dc::encode_f16_rows_map(&w->map_cand_f16, w->cand_f16, cand_rows, d, 128) ||
       !dc::encode_bf16_rows_map(&w->map_slot_hi, w->slot_hi, slot_rows, d, 128) ||
       !dc::encode_bf16_rows_map(&w->map_slot_lo, w->slot_lo, slot_rows, d, 128) ||
       (cfg.variant == 0 &&

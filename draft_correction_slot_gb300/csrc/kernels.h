@@ -81,11 +81,17 @@ struct ProjJob {
   // previous kernel, and clears them when done.
   unsigned *row_ready = nullptr;
   int cands_per_row = 0;
+  // fp16 instead of bf16 hi + lo: A is converted in shared memory (its values
+  // must lie within the fp16 range, |a| < 65504) and W comes as one fp16
+  // matrix through the `hi` map (the `lo` map is not read).
+  bool f16 = false;
 };
 int proj_tc_splits(int d, int requested);
 int proj_tc_tiles(int M, int No);
 // 2D bf16 [rows][d] tensor map, 128B swizzle, box 64 x box_rows.
 bool encode_bf16_rows_map(CUtensorMap *map, const void *base, int rows, int d, int box_rows);
+// The same for fp16 elements.
+bool encode_f16_rows_map(CUtensorMap *map, const void *base, int rows, int d, int box_rows);
 // 2D fp32 [rows][cols] tensor map, 128B swizzle, box 32 x box_rows
 // (cols % 32 == 0).
 bool encode_f32_rows_map(CUtensorMap *map, const void *base, int rows, int cols, int box_rows);

@@ -11,7 +11,12 @@
 // one after the other in shared memory, so one N = 256 MMA takes both: its
 // accumulator holds A hi^T in columns [0, 128) and A lo^T in [128, 256), and
 // the epilogue adds the two (fp32).  One N = 256 instruction reads the A
-// block once for both halves.
+// block once for both halves.  A job may instead run in fp16 (the candidate
+// rows: each gathered bf16 row is converted in shared memory, exactly inside
+// the fp16 range, and the weights are rounded to fp16 once, 2^-11 relative):
+// one N = 128 MMA per k-step, half the tensor work and weight bytes, within
+// the score tolerance (the LayerNorm after the product keeps the error
+// relative).
 //
 // Tile: 256 rows (two 128-row accumulators) x 128 outputs, k-blocks of 64
 // (one 128-byte swizzle atom) in 128B-swizzled K-major shared memory.  Each
@@ -55,6 +60,7 @@ constexpr uint32_t kStageTx = 2u * kSubBytes;          // weight bytes per k-blo
 constexpr int kMaxSplits = 8;       // a cluster of at most 8 CTAs (portable size)
 constexpr int kBoxBytes = kSubM * 128;  // one 32-column fp32 box of a 128-row output tile
 constexpr uint32_t kIdesc = tc::idesc_bf16(kSubM, 2 * kTileN);  // hi and lo blocks stacked
+constexpr uint32_t kIdescF16 = tc::idesc_f16(kSubM, kTileN);     // one fp16 weight block
 
 // A CTA owns MT x 128 rows (MT accumulators of 128 x 128 in tensor memory)
 // so that every weight k-block it brings in feeds MT MMAs.  Two rings: the
@@ -86,6 +92,26 @@ __device__ __forceinline__ void cp_async_wait() {
 
 
 using namespace tc;
+
+// The 16-byte chunks this thread gathered into one A stage (rows 16 j
+// apart), bf16 -> fp16 in place (round to nearest; every bf16 value within
+// the fp16 range below 65504 is exact down to 2^-14 and rounded to 2^-24
+// below).
+__device__ __forceinline__ void convert_chunks_f16(uint32_t addr0) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t a = addr0 + j * 2048;
+    uint32_t w[4];
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(a));
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float lo = __uint_as_float(w[q] << 16), hi = __uint_as_float(w[q] & 0xFFFF0000u);
+      asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(w[q]) : "f"(hi), "f"(lo));
+    }
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                 : "memory");
+  }
+}
 
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -143,6 +169,7 @@ k_proj_tc(ProjJob job0, ProjJob job1, const __grid_constant__ CUtensorMap map0_h
   uint16_t *__restrict__ ln_hi = job.ln_hi;
   uint16_t *__restrict__ ln_lo = job.ln_lo;
   const float ln_eps = job.ln_eps;
+  const bool f16 = job.f16;
   // candidate rows [m0, m0 + kTileM) come from draft-slot rows row_first..row_last
   const int row_first = job.row_ready ? m0 / job.cands_per_row : 0;
   const int row_last = job.row_ready ? (min(m0 + kTileM, M) - 1) / job.cands_per_row : -1;
@@ -229,13 +256,18 @@ k_proj_tc(ProjJob job0, ProjJob job1, const __grid_constant__ CUtensorMap map0_h
       cp_async_commit();
       if (it >= kStagesA - 1) {
         cp_async_wait<kStagesA - 1>();
+        const int r = it - (kStagesA - 1);
+        if (f16) convert_chunks_f16(sbase + (r % kStagesA) * G::kStageA + off0);
         fence_proxy_async();
-        mbar_arrive(smem_u32(&full_a[(it - (kStagesA - 1)) % kStagesA]));
+        mbar_arrive(smem_u32(&full_a[r % kStagesA]));
       }
     }
     cp_async_wait<0>();
-    fence_proxy_async();
-    for (int r = max(0, it - (kStagesA - 1)); r < it; ++r) mbar_arrive(smem_u32(&full_a[r % kStagesA]));
+    for (int r = max(0, it - (kStagesA - 1)); r < it; ++r) {
+      if (f16) convert_chunks_f16(sbase + (r % kStagesA) * G::kStageA + off0);
+      fence_proxy_async();
+      mbar_arrive(smem_u32(&full_a[r % kStagesA]));
+    }
   } else if (warp == G::kWarpTma) {
     if (lane == 0) {
       // ------------------------------------------------------------ weight TMA
@@ -247,9 +279,9 @@ k_proj_tc(ProjJob job0, ProjJob job1, const __grid_constant__ CUtensorMap map0_h
         const uint32_t full = smem_u32(&full_w[s]);
         const uint32_t sw = sbase + G::kRingA + s * 2 * kSubBytes;
         const int kx = (kb0 + it) * kTileK;
-        mbar_arrive_expect_tx(full, kStageTx);
+        mbar_arrive_expect_tx(full, f16 ? (uint32_t)kSubBytes : kStageTx);
         tma_load_2d(sw, map_hi, kx, n0, full);
-        tma_load_2d(sw + kSubBytes, map_lo, kx, n0, full);
+        if (!f16) tma_load_2d(sw + kSubBytes, map_lo, kx, n0, full);
       }
     }
   } else if (warp == G::kWarpMma && lane == 0) {
@@ -263,13 +295,14 @@ k_proj_tc(ProjJob job0, ProjJob job1, const __grid_constant__ CUtensorMap map0_h
       const uint32_t sa = sbase + s * G::kStageA, sw = sbase + G::kRingA + t * 2 * kSubBytes;
 #pragma unroll
       for (int k = 0; k < kTileK / 16; ++k) {
-        // B = 256 rows: the hi block's 128, then the lo block's (16 KB further,
-        // the next 8-row groups at the descriptor's 1024-byte stride)
+        // bf16: B = 256 rows, the hi block's 128, then the lo block's (16 KB
+        // further, the next 8-row groups at the descriptor's 1024-byte
+        // stride); fp16: the one weight block, N = 128
         const uint64_t bd = sw128_desc(sw + k * 32);
 #pragma unroll
         for (int h = 0; h < MT; ++h) {
           const uint64_t ad = sw128_desc(sa + h * kSubBytes + k * 32);
-          mma_bf16(tmem + h * 256, ad, bd, kIdesc, (it > 0 || k > 0) ? 1u : 0u);
+          mma_bf16(tmem + h * 256, ad, bd, f16 ? kIdescF16 : kIdesc, (it > 0 || k > 0) ? 1u : 0u);
         }
       }
       mma_commit(smem_u32(&empty_a[s]));
@@ -295,9 +328,11 @@ k_proj_tc(ProjJob job0, ProjJob job1, const __grid_constant__ CUtensorMap map0_h
         float v[32], vl[32];
         const uint32_t t0 = tmem + ((uint32_t)(q4 * 32) << 16) + (uint32_t)(sub * 256 + cc * 32);
         tmem_ld32(t0, v);
-        tmem_ld32(t0 + 128, vl);
+        if (!f16) {
+          tmem_ld32(t0 + 128, vl);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] += vl[k];
+          for (int k = 0; k < 32; ++k) v[k] += vl[k];
+        }
         if (nkb <= 0)  // an empty split holds no products
 #pragma unroll
           for (int k = 0; k < 32; ++k) v[k] = 0.f;
@@ -466,16 +501,27 @@ EncodeTiledFn encode_fn() {
 }
 }  // namespace
 
-bool encode_bf16_rows_map(CUtensorMap *map, const void *base, int rows, int d, int box_rows) {
+namespace {
+bool encode_16bit_rows_map(CUtensorMap *map, CUtensorMapDataType type, const void *base, int rows, int d,
+                           int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn || rows <= 0 || d % kTileK != 0 || (reinterpret_cast<uintptr_t>(base) & 15u)) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
   const cuuint32_t box[2] = {(cuuint32_t)kTileK, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return fn(map, type, 2, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
+bool encode_bf16_rows_map(CUtensorMap *map, const void *base, int rows, int d, int box_rows) {
+  return encode_16bit_rows_map(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rows, d, box_rows);
+}
+
+bool encode_f16_rows_map(CUtensorMap *map, const void *base, int rows, int d, int box_rows) {
+  return encode_16bit_rows_map(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, base, rows, d, box_rows);
 }
 
 bool encode_f32_rows_map(CUtensorMap *map, const void *base, int rows, int cols, int box_rows) {

@@ -118,7 +118,9 @@ typedef struct {
   const void *logits;          /* bf16 [N][slots][stride]; 16-byte aligned   */
   int64_t logits_slot_stride;  /* elements between slot rows; >= V, % 8 == 0 */
   const void *hidden;          /* bf16 [N][slots][d]; 16-byte aligned        */
-  const void *cand_embed;      /* bf16 [V][d] frozen token-embedding table   */
+  const void *cand_embed;      /* bf16 [V][d] frozen token-embedding table;
+                                  entries below 65504 in magnitude (the
+                                  candidate projection runs in fp16)        */
   const int32_t *target_tokens;/* int32 [N][B] target greedy tokens, or NULL */
 } dcoco_inputs;
 
