@@ -384,23 +384,22 @@ void pack_mlp(const dcoco_weight_ptrs &w, std::vector<float> &buf, size_t off[8]
   const int r = kR, H = kH, in = 3 * kR + 2;
   size_t o = 0;
   auto take = [&](size_t n) { size_t at = (o + 63) & ~size_t(63); o = at + n; return at; };
-  off[0] = take(r);      // gamma
-  off[1] = take(r);      // beta
+  off[0] = take(0);      // (unused)
+  off[1] = take(0);      // (unused)
   off[2] = take(H);      // w_la = W1[:, 3r]
   off[3] = take(H);      // w_lb = W1[:, 3r+1]
-  off[4] = take(H);      // b1
+  off[4] = take(H);      // b1' = b1 + W1[:, r:2r] beta + W1[:, 2r:3r] beta (beta of z, moved into P)
   off[5] = take(H);      // w2
   off[6] = take(1);      // b2
   off[7] = take((size_t)r * r);  // W_fuse[:, r:], in the candidate maps' register order
   buf.assign(o, 0.f);
-  for (int k = 0; k < r; ++k) {
-    buf[off[0] + k] = w.ln_gamma[k];
-    buf[off[1] + k] = w.ln_beta[k];
-  }
   for (int j = 0; j < H; ++j) {
     buf[off[2] + j] = w.w1[(size_t)j * in + 3 * r];
     buf[off[3] + j] = w.w1[(size_t)j * in + 3 * r + 1];
-    buf[off[4] + j] = w.b1[j];
+    double bj = w.b1[j];
+    for (int k = 0; k < r; ++k)
+      bj += ((double)w.w1[(size_t)j * in + r + k] + (double)w.w1[(size_t)j * in + 2 * r + k]) * w.ln_beta[k];
+    buf[off[4] + j] = (float)bj;
     buf[off[5] + j] = w.w2[j];
   }
   buf[off[6]] = w.b2[0];
@@ -576,9 +575,15 @@ int dcoco_weights_create(dcoco_handle *h, const dcoco_weight_ptrs *wp, void *str
       split_vec(w_fuse.data() + (size_t)o * 2 * kR + kR, fgh + (size_t)o * kR, fgl + (size_t)o * kR);
     }
     const size_t in1 = 3 * kR + 2;
+    // the candidate parts of layer 1 take z's gamma: W1[:, r:2r] diag(gamma), W1[:, 2r:3r] diag(gamma)
+    std::vector<float> wa(kR), wb(kR);
     for (int j = 0; j < kH; ++j) {
-      split_vec(w1.data() + j * in1 + kR, w1h + (size_t)j * kR, w1l + (size_t)j * kR);
-      split_vec(w1.data() + j * in1 + 2 * kR, w1h + (size_t)(kH + j) * kR, w1l + (size_t)(kH + j) * kR);
+      for (int k = 0; k < kR; ++k) {
+        wa[k] = (float)((double)w1[j * in1 + kR + k] * gam[k]);
+        wb[k] = (float)((double)w1[j * in1 + 2 * kR + k] * gam[k]);
+      }
+      split_vec(wa.data(), w1h + (size_t)j * kR, w1l + (size_t)j * kR);
+      split_vec(wb.data(), w1h + (size_t)(kH + j) * kR, w1l + (size_t)(kH + j) * kR);
       split_vec(w1.data() + j * in1, wsh + (size_t)j * kR, wsl + (size_t)j * kR);
     }
     proj.insert(proj.end(), cm.begin(), cm.end());
@@ -649,7 +654,7 @@ int dcoco_weights_create(dcoco_handle *h, const dcoco_weight_ptrs *wp, void *str
   }
   if (cfg.variant == 0) {
     dc::MlpWeightsDev &m = w->mlp;
-    m.gamma = dmlp + off[0]; m.beta = dmlp + off[1]; m.w_la = dmlp + off[2]; m.w_lb = dmlp + off[3];
+    m.w_la = dmlp + off[2]; m.w_lb = dmlp + off[3];
     m.b1 = dmlp + off[4]; m.w2 = dmlp + off[5]; m.b2 = dmlp + off[6]; m.w_fg = dmlp + off[7];
   }
   *out = w;

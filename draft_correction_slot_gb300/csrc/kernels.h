@@ -101,11 +101,9 @@ cudaError_t launch_proj_tc(const ProjJob &a, const CUtensorMap &a_hi, const CUte
 
 // ---------------------------------------------------------------- representations
 struct MlpWeightsDev {
-  const float *gamma;   // [r]
-  const float *beta;    // [r]
   const float *w_la;    // [H]     W1[:, 3r]
   const float *w_lb;    // [H]     W1[:, 3r+1]
-  const float *b1;      // [H]
+  const float *b1;      // [H]  b1 + W1[:, r:2r] beta + W1[:, 2r:3r] beta
   const float *w2;      // [H]
   const float *b2;      // [1]
   const float *w_fg;    // [r][r]  W_fuse[:, r:], in the candidate maps' register order
@@ -113,19 +111,22 @@ struct MlpWeightsDev {
 
 // Tensor-core forms of the per-slot and per-candidate steps.  The maps
 // address bf16 hi / lo halves (box 64 x 128, 128B swizzle) of W_fuse[:, :r]
-// and W_fuse[:, r:] ([r][r] each), [W1[:, r:2r] ; W1[:, 2r:3r]] ([2H][r]) and
-// W1[:, :r] ([H][r]).
+// and W_fuse[:, r:] ([r][r] each), [W1[:, r:2r] ; W1[:, 2r:3r]] diag(gamma)
+// ([2H][r]) and W1[:, :r] ([H][r]).
 struct MlpMaps {
   CUtensorMap fb_hi, fb_lo, w1_hi, w1_lo, fg_hi, fg_lo, w1s_hi, w1s_lo;
 };
 // The per-slot and per-candidate maps, in one launch (no block waits for
 // another).  Per draft slot i (used for i < B-1):
-// P_i = W1[:, :r] (W_pair[:, :d] h_i + W_pair[:, d:] h_{i+1}) + b1 ([rows][H]).
+// P_i = W1[:, :r] (W_pair[:, :d] h_i + W_pair[:, d:] h_{i+1}) + b1' ([rows][H]),
+// b1' = b1 + W1[:, r:2r] beta + W1[:, 2r:3r] beta.
 // slot_proj is [N*B][3r] = (W_ctx h | W_pair[:, :d] h | W_pair[:, d:] h).
 // Per candidate: b = LN0(W_cand E[c]) (from the projection, as bf16 hi and
 // lo), g = LN0(W_ctx h) of its slot,
 // z = gamma*LN0(W_fuse[:, :r] b + W_fuse[:, r:] g) + beta,
-// U = W1_a z + w_la l, V = W1_b z + w_lb l.  M = N * B * K candidates
+// U = W1_a z + w_la l, V = W1_b z + w_lb l, computed as U = (W1_a diag(gamma))
+// n + w_la l with n = LN0(...) (beta's share W1_a beta + W1_b beta is in P,
+// so P + U + V is unchanged).  M = N * B * K candidates
 // (8 <= K, K divides 128), candidate m belongs to draft slot m / K.
 // Tiles move by TMA: `slot.sp` reads slot_proj, `slot.p` writes P,
 // `cand.u` / `cand.v` write U and V ([rows][H]) -- fp32 maps with box

@@ -56,7 +56,7 @@ struct MapsParams {
   CandIoMaps cand;
   const float *slot_proj;  // [N*B][3r]
   const float *w_fg;       // W_fuse[:, r:], fp32 [r][r]
-  const float *topk_val, *gamma, *beta, *w_la, *w_lb, *b1;
+  const float *topk_val, *w_la, *w_lb, *b1;
   int NB;                  // draft slots in the call
   int slot_ctas;           // 2 per 128-slot tile (the two halves of P)
   int K, M;                // candidates per slot, candidates in the call
@@ -370,7 +370,7 @@ __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int ti
   __shared__ float s_red[2][4 * kRows];
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ float s_gam[kR], s_bet[kR], s_wl[kH];         // gamma, beta, this half's w_l
+  __shared__ float s_wl[kH];                               // this half's w_l
   __shared__ __align__(16) float s_g[kMaxSlots][kGLd];     // LN0(W_ctx h) of the tile's slots
   __shared__ __align__(16) float s_gf[kMaxSlots][kR];      // Gf of the tile's slots
   __shared__ float s_gq[2][4][kR];                         // Gf quarter partials, two slots in flight
@@ -443,10 +443,10 @@ __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int ti
     const uint32_t lane_base = tmem + ((uint32_t)(qd * 32) << 16);
     // Weights first (they do not depend on the previous kernel), all loads in
     // flight before any use: this thread's slice of W_fuse[:, r:] (output go,
-    // inputs [32 gk, 32 gk + 32)) to registers; gamma, beta and w_l reach
-    // shared memory after the dependency wait (the z phase reads them, behind
-    // several row barriers).  The input quarter gk is the same for the whole
-    // warp, so every read of g below is a broadcast.
+    // inputs [32 gk, 32 gk + 32)) to registers; w_l reaches shared memory
+    // after the dependency wait (the output phase reads it, behind several
+    // row barriers).  The input quarter gk is the same for the whole warp, so
+    // every read of g below is a broadcast.
     const int gk = warp & 3, go = (warp >> 2) * 32 + lane;
     float wfg[32];
     {
@@ -458,16 +458,11 @@ __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int ti
         wfg[4 * i] = v.x; wfg[4 * i + 1] = v.y; wfg[4 * i + 2] = v.z; wfg[4 * i + 3] = v.w;
       }
     }
-    const float gam = tid < kR ? __ldg(mp.gamma + tid) : 0.f, bet = tid < kR ? __ldg(mp.beta + tid) : 0.f;
     const float wlv = tid < kH ? __ldg((half == 0 ? mp.w_la : mp.w_lb) + tid) : 0.f;
     float x[kQ];
     // W_ctx h of the tile's slots (slot_proj, from the previous kernel); one
     // warp per slot, four columns per lane
     pdl_wait();
-    if (tid < kR) {
-      s_gam[tid] = gam;
-      s_bet[tid] = bet;
-    }
     if (tid < kH) s_wl[tid] = wlv;
     const int gs = slot0 + warp;
     float4 gx = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -507,8 +502,10 @@ __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int ti
       if (gk == 0) s_gf[sl][go] = (gq[0][go] + gq[1][go]) + (gq[2][go] + gq[3][go]);
     }
 
-    // z = gamma * LN0(y + Gf[slot]) + beta  (every row thread takes part: the
-    // LayerNorm holds row barriers)
+    // z = gamma * LN0(y + Gf[slot]) + beta, with gamma folded into the
+    // layer-1 weights and beta into P's bias when the weights are packed:
+    // the A operand of layer 1 is LN0(y + Gf[slot]) itself (every row thread
+    // takes part: the LayerNorm holds row barriers)
     // (the row barrier also publishes s_gf)
     const bool ok = rows_all(mbar_wait(smem_u32(&bar_fuse), 0, &s_abort, err) && !s_abort);
     tc_fence_after();
@@ -526,8 +523,6 @@ __device__ __forceinline__ void cand_role(const MapsParams &mp, int half, int ti
         for (int k = 0; k < kQ; ++k) x[k] = 0.f;
       }
       ln0_part(x, eps, s_red[0], s_red[1], r, q);
-#pragma unroll
-      for (int k = 0; k < kQ; ++k) x[k] = fmaf(s_gam[q * kQ + k], x[k], s_bet[q * kQ + k]);
       store_split_part(smem + kOffA, smem + kOffA + kMat, r, q, x);
     }
     fence_proxy_async();
@@ -616,8 +611,6 @@ cudaError_t launch_maps_tc(const MlpMaps &maps, const SlotIoMaps &slot, const Ca
   mp.slot_proj = slot_proj;
   mp.w_fg = w.w_fg;
   mp.topk_val = topk_val;
-  mp.gamma = w.gamma;
-  mp.beta = w.beta;
   mp.w_la = w.w_la;
   mp.w_lb = w.w_lb;
   mp.b1 = w.b1;
