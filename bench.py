@@ -150,7 +150,8 @@ def stage_model(w, pk):
         # the pair loop's element rate at its own operation count
         "pair_walk": ("alu", "Gelem/s", N * (B - 1) * K * K * w["H"],
                       fma_lane_rate(pk) / FMA_LANE_OPS_PER_GELU / 1e9),
-        "cos_score": ("alu", "GFLOP/s", 2 * N * (B - 1) * K * K * r, 2 * fma_lane_rate(pk) / 1e9),
+        # the cosine variant's fused normalise + score + walk launch, at its dot products' flops
+        "cos_pair_walk": ("alu", "GFLOP/s", 2 * N * (B - 1) * K * K * r, 2 * fma_lane_rate(pk) / 1e9),
     }
 
 

@@ -28,8 +28,8 @@ struct Workspace {
   float *cand_proj = nullptr;  // variant 1: [N*B*K][2r]
   uint16_t *b_hi = nullptr, *b_lo = nullptr;  // variant 0: LN0(W_cand E[c]) as bf16 hi, lo [N*B*K][r]
   float *P = nullptr;          // [N*B][H] (rows of the last slot unused)
-  float *U = nullptr;          // [N*B*K][H]  (variant 1: O [N*B*K][r])
-  float *V = nullptr;          // [N*B*K][H]  (variant 1: I [N*B*K][r])
+  float *U = nullptr;          // [N*B*K][H]  (variant 0)
+  float *V = nullptr;          // [N*B*K][H]  (variant 0)
   float *scores = nullptr;     // [N*(B-1)][K][K]
   int32_t *choice = nullptr;   // [N*B]
   float *margin = nullptr;     // [N*(B-1)]
@@ -56,7 +56,7 @@ constexpr int kMaxTimedCalls = 1024;
 constexpr int kStageKinds = 2;
 const char *const kStageNames[kStageKinds][kMaxStages] = {
     {"topk", "proj", "maps", "pair_walk", nullptr, nullptr, nullptr, nullptr},
-    {"topk", "proj", "cos_post", "cos_score", "walk_verify", nullptr, nullptr, nullptr}};
+    {"topk", "proj", "cos_pair_walk", nullptr, nullptr, nullptr, nullptr, nullptr}};
 int stage_count(int kind) {
   int n = 0;
   while (n < kMaxStages && kStageNames[kind][n]) ++n;
@@ -174,8 +174,8 @@ void carve_workspace(Carver &c, const dcoco_config &cfg, int B, int topk_segment
   ws.b_hi = c.take<uint16_t>(cfg.variant == 0 ? cands * kR : 0);
   ws.b_lo = c.take<uint16_t>(cfg.variant == 0 ? cands * kR : 0);
   ws.P = c.take<float>(N * B * kH);
-  ws.U = c.take<float>(cands * kH);
-  ws.V = c.take<float>(cands * kH);
+  ws.U = c.take<float>(cfg.variant == 0 ? cands * kH : 0);
+  ws.V = c.take<float>(cfg.variant == 0 ? cands * kH : 0);
   ws.scores = c.take<float>(N * (B - 1) * K * K);
   ws.choice = c.take<int32_t>(rows);
   ws.margin = c.take<float>(N * (B - 1));
@@ -368,13 +368,12 @@ int run_path(dcoco_handle *h, const dcoco_weights *w, int N, const dcoco_inputs 
                                                scores, wk, st)));
     return DCOCO_OK;
   }
-  DC_TRY(clk.done(dc::launch_cos_post(K, ws.cand_proj, ws.slot_proj, N, B, ws.U, ws.V, st)));
-  DC_TRY(clk.done(dc::launch_cos_score(K, ws.U, ws.V, vals, cfg.sigma, N, B, scores, st)));
-  // step 5: walk + verify
-  DC_TRY(clk.done(dc::launch_walk_verify(K, scores, ids, in->target_tokens, N, B, out->tokens,
-                                         choice, margin,
-                                         in->target_tokens ? out->accept_len : nullptr, cfg.path_rule,
-                                         cfg.beam_width, beam_topm(cfg), st)));
+  // steps 4-5: normalised in/out vectors, all (B-1) K^2 cosine scores, then
+  // each request's walk and verify in its last block
+  const dc::WalkArgs wk{ids, in->target_tokens, out->tokens, choice,
+                        in->target_tokens ? out->accept_len : nullptr, margin, ws.req_count,
+                        cfg.path_rule, cfg.beam_width, beam_topm(cfg)};
+  DC_TRY(clk.done(dc::launch_cos_pair_walk(K, ws.cand_proj, ws.slot_proj, vals, cfg.sigma, N, B, scores, wk, st)));
   return DCOCO_OK;
 }
 

@@ -146,8 +146,11 @@ cudaError_t launch_maps_tc(const MlpMaps &maps, const SlotIoMaps &slot, const Ca
                            int K, float eps, int *err, cudaStream_t st);
 
 // Step 5 outputs and state for a launch that ends with the walk: per-request
-// arrays as in launch_walk_verify, and req_count (N entries, zero between
-// calls) counting each request's finished pairs.
+// arrays (tokens, choice, accept_len [N][B] / [N]; margin [N][B-1]; target or
+// null) and req_count (N entries, zero between calls) counting each
+// request's finished pairs.  path_rule 0: prefix-first greedy walk; 1:
+// highest-scoring path (Viterbi); 2: beam walk (beam_width 1..4, beam_topm
+// 1..K).
 struct WalkArgs {
   const int32_t *topk_ids;
   const int32_t *target;  // or null
@@ -161,18 +164,18 @@ struct WalkArgs {
 
 // S[n,p,a,b] = l_{p+1}(b) + b2 + sum_j w2_j GELU(P_pj + U_{p,a,j} + V_{p+1,b,j}),
 // with P indexed by draft slot ([N*B][H]),
-// then, in the last block of each request, the walk and verify of
-// launch_walk_verify.
+// then, in the last block of each request, its path selection and verify.
 cudaError_t launch_pair_score_walk(int K, const float *U, const float *V, const float *P,
                                    const float *topk_val, const float *w2, const float *b2, int N, int B,
                                    float *scores, const WalkArgs &wk, cudaStream_t st);
 
 // ---------------------------------------------------------------- cosine variant
-// y = cand_io[m] + slot_io[slot(m)]; out/in halves L2-normalised -> O, I [M][r].
-cudaError_t launch_cos_post(int K, const float *cand_io, const float *slot_io, int N, int B,
-                            float *O, float *I, cudaStream_t st);
-cudaError_t launch_cos_score(int K, const float *O, const float *I, const float *topk_val,
-                             float sigma, int N, int B, float *scores, cudaStream_t st);
+// y = cand_io[m] + slot_io[slot(m)] ([M][2r] and [N*B][2r]), the out half
+// (columns 0..r-1) and the in half L2-normalised (x / max(|x|, 1e-12));
+// S[n,p,a,b] = sigma <o_{p,a}, i_{p+1,b}> + l_{p+1}(b); then, in the last
+// block of each request, its path selection and verify.
+cudaError_t launch_cos_pair_walk(int K, const float *cand_io, const float *slot_io, const float *topk_val,
+                                 float sigma, int N, int B, float *scores, const WalkArgs &wk, cudaStream_t st);
 
 // ---------------------------------------------------------------- stochastic verify
 // Point-mass proposal `tokens` [N][B] against target logits [N][B+1][stride]
@@ -189,14 +192,6 @@ cudaError_t launch_verify_stochastic(const uint16_t *target, int64_t stride, int
                                      float *chunk_m, float *chunk_s, float *row_lse, float *q_acc,
                                      unsigned *req_count, int32_t *accept_len, int32_t *next_token,
                                      cudaStream_t st);
-
-// ---------------------------------------------------------------- walk + verify
-// path_rule 0: prefix-first greedy walk; 1: highest-scoring path (Viterbi);
-// 2: beam walk (beam_width 1..4, beam_topm 1..K).
-cudaError_t launch_walk_verify(int K, const float *scores, const int32_t *topk_ids,
-                               const int32_t *target, int N, int B, int32_t *tokens,
-                               int32_t *choice, float *margin, int32_t *accept_len,
-                               int path_rule, int beam_width, int beam_topm, cudaStream_t st);
 
 // One CTA waits (tc::mbar_wait, limit_ns) on an mbarrier nothing completes:
 // the wait expires and ORs kErrTimeout into *err.

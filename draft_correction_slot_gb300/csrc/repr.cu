@@ -1,6 +1,6 @@
 // repr.cu -- step 4, the K x K transition scores of every slot pair (with
-// step 5 in the last block of each request), and the cosine variant's
-// per-candidate vectors and scores.
+// step 5 in the last block of each request), for the MLP and the cosine
+// variants.
 //
 // DCOCO page ("Contextual Correction of Parallel Drafts for Speculative
 // Decoding"), Method step details (4):
@@ -24,6 +24,48 @@ namespace {
 constexpr int R = 128;  // representation width
 constexpr int H = 256;  // MLP hidden width
 
+
+// ---------------------------------------------------------------- step 5
+// The last block of request n to finish its pair (counted in req_count,
+// zero between calls) selects the request's path (greedy walk, highest-
+// scoring path or beam walk) and verifies it.  Called by every thread of a
+// 256-thread block after the block's scores are stored; `sm` is the block's
+// dynamic shared memory (the walk's tables, and the request's scores for
+// path rules 1 and 2 when they fit).
+template <int K>
+__device__ __forceinline__ void request_tail(float *sm, int n, int B, const float *scores, const WalkArgs &wk) {
+  const int tid = threadIdx.x;
+  __shared__ int s_last;
+  __shared__ int s_choice[32];
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(&wk.req_count[n], 1u) == (unsigned)(B - 2);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  int *s_best = reinterpret_cast<int *>(sm);
+  float *s_gap = sm + kWalkMaxRows;
+  const int64_t slot0 = (int64_t)n * B;
+  const float *sc = scores + (int64_t)n * (B - 1) * K * K;
+  const int32_t *tg = wk.target ? wk.target + slot0 : nullptr;
+  int32_t *ch = wk.choice ? wk.choice + slot0 : nullptr, *al = wk.accept_len ? wk.accept_len + n : nullptr;
+  float *mg = wk.margin ? wk.margin + (int64_t)n * (B - 1) : nullptr;
+  if (wk.path_rule != 0) {
+    // the request's scores go to shared memory past the walk's tables when they fit
+    float *s_sc = sm + 2 * kWalkMaxRows;
+    const bool fits = (2 * kWalkMaxRows + (size_t)(B - 1) * K * K) * sizeof(float) <= dynamic_smem_bytes();
+    if (wk.path_rule == 1)
+      viterbi_verify_request<K>(sc, wk.topk_ids + slot0 * K, tg, B, wk.tokens + slot0, ch, mg, al, s_best, s_gap,
+                                s_choice, fits ? s_sc : nullptr);
+    else
+      beam_verify_request<K>(sc, wk.topk_ids + slot0 * K, tg, B, wk.tokens + slot0, ch, mg, al, wk.beam_width,
+                             wk.beam_topm, s_best, s_gap, s_choice, fits ? s_sc : nullptr);
+  } else {
+    walk_verify_request<K>(sc, wk.topk_ids + slot0 * K, tg, B, wk.tokens + slot0, ch, mg, al, s_best, s_gap,
+                           s_choice, reinterpret_cast<int *>(sm + 2 * kWalkMaxRows));
+  }
+  if (tid == 0) wk.req_count[n] = 0u;  // ready for the next call
+}
 
 // ---------------------------------------------------------------- pair scores
 // With x = (P_p + U_{p,a} + V_{p+1,b}) / sqrt(2) and w' = w2 / sqrt(2),
@@ -226,90 +268,60 @@ k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
     scores[(int64_t)np * K * K + e] = s_tv[bb] + bias + (dab[aa] + dab[K + bb]) + sum;
   }
 
-  // ---------------------------------------------------------------- step 5
-  // The last block of request n to finish its pair (counted in req_count,
-  // zero between calls) selects the request's path (greedy walk, highest-
-  // scoring path or beam walk) and verifies it.
-  __shared__ int s_last;
-  __shared__ int s_choice[32];
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = atomicAdd(&wk.req_count[n], 1u) == (unsigned)(B - 2);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  int *s_best = reinterpret_cast<int *>(sm);
-  float *s_gap = sm + kWalkMaxRows;
-  const int64_t slot0 = (int64_t)n * B;
-  const float *sc = scores + (int64_t)n * (B - 1) * K * K;
-  const int32_t *tg = wk.target ? wk.target + slot0 : nullptr;
-  int32_t *ch = wk.choice ? wk.choice + slot0 : nullptr, *al = wk.accept_len ? wk.accept_len + n : nullptr;
-  float *mg = wk.margin ? wk.margin + (int64_t)n * (B - 1) : nullptr;
-  if (wk.path_rule != 0) {
-    // the request's scores go to shared memory past the walk's tables when they fit
-    float *s_sc = sm + 2 * kWalkMaxRows;
-    const bool fits = (2 * kWalkMaxRows + (size_t)(B - 1) * K * K) * sizeof(float) <= dynamic_smem_bytes();
-    if (wk.path_rule == 1)
-      viterbi_verify_request<K>(sc, wk.topk_ids + slot0 * K, tg, B, wk.tokens + slot0, ch, mg, al, s_best, s_gap,
-                                s_choice, fits ? s_sc : nullptr);
-    else
-      beam_verify_request<K>(sc, wk.topk_ids + slot0 * K, tg, B, wk.tokens + slot0, ch, mg, al, wk.beam_width,
-                             wk.beam_topm, s_best, s_gap, s_choice, fits ? s_sc : nullptr);
-  } else {
-    walk_verify_request<K>(sc, wk.topk_ids + slot0 * K, tg, B, wk.tokens + slot0, ch, mg, al, s_best, s_gap,
-                           s_choice, reinterpret_cast<int *>(sm + 2 * kWalkMaxRows));
-  }
-  if (tid == 0) wk.req_count[n] = 0u;  // ready for the next call
+  request_tail<K>(sm, n, B, scores, wk);
 }
 
 // ---------------------------------------------------------------- cosine variant
-__global__ void __launch_bounds__(256)
-k_cos_post(const float *__restrict__ cand_io, const float *__restrict__ slot_io, int K, int M,
-           float *__restrict__ O, float *__restrict__ I) {
-  const int lane = threadIdx.x & 31;
-  const int m = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (m >= M) return;
-  const int slot = m / K;
-  float o[4], in[4];
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int k = lane + 32 * u;
-    o[u] = cand_io[(int64_t)m * 2 * R + k] + slot_io[(int64_t)slot * 2 * R + k];
-    in[u] = cand_io[(int64_t)m * 2 * R + R + k] + slot_io[(int64_t)slot * 2 * R + R + k];
-  }
-  float no = warp_sum(o[0] * o[0] + o[1] * o[1] + o[2] * o[2] + o[3] * o[3]);
-  float ni = warp_sum(in[0] * in[0] + in[1] * in[1] + in[2] * in[2] + in[3] * in[3]);
-  const float so = 1.0f / fmaxf(sqrtf(no), 1e-12f), si = 1.0f / fmaxf(sqrtf(ni), 1e-12f);
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int k = lane + 32 * u;
-    O[(int64_t)m * R + k] = o[u] * so;
-    I[(int64_t)m * R + k] = in[u] * si;
-  }
-}
+// One block per slot pair (n, p), the cosine variant's steps 4-5 in one
+// launch: the out-vectors of slot p's candidates and the in-vectors of slot
+// p+1's are summed from their candidate and draft-slot parts and
+// normalised (x / max(|x|, 1e-12), one warp per vector) into shared memory,
+// then S_p(a, b) = sigma <o_a, i_b> + l_{p+1}(b), then the request tail.
+// (Each slot's vectors are normalised by the two blocks that read them.)
+template <int K>
+struct CosGeom {
+  static constexpr size_t vec_floats = 2 * (size_t)K * (R + 1);
+  static constexpr size_t min_floats = vec_floats > 3 * (size_t)kWalkMaxRows ? vec_floats : 3 * (size_t)kWalkMaxRows;
+};
 
 template <int K>
 __global__ void __launch_bounds__(256)
-k_cos_score(const float *__restrict__ O, const float *__restrict__ I,
-            const float *__restrict__ topk_val, float sigma, int B, float *__restrict__ scores) {
-  __shared__ float os[K][R + 1];
-  __shared__ float is[K][R + 1];
+k_cos_pair(const float *__restrict__ cand_io, const float *__restrict__ slot_io,
+           const float *__restrict__ topk_val, float sigma, int B, float *__restrict__ scores, WalkArgs wk) {
+  extern __shared__ float sm[];
+  float(*os)[R + 1] = reinterpret_cast<float(*)[R + 1]>(sm);
+  float(*is)[R + 1] = reinterpret_cast<float(*)[R + 1]>(sm + K * (R + 1));
   const int np = blockIdx.x;
   const int n = np / (B - 1), p = np - n * (B - 1);
-  const int64_t ca = ((int64_t)n * B + p) * K, cb = ca + K;
-  for (int e = threadIdx.x; e < K * R; e += 256) {
-    const int c = e / R, k = e - c * R;
-    os[c][k] = O[(ca + c) * R + k];
-    is[c][k] = I[(cb + c) * R + k];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_trigger();
+  pdl_wait();  // cand_io, slot_io (and this call's outputs) belong to the previous kernels until here
+  const int64_t sa = (int64_t)n * B + p, sb = sa + 1;  // draft-slot rows of slots p and p+1
+  // everything this call's earlier kernels wrote is read through L2 (ld.cg)
+  for (int row = warp; row < 2 * K; row += 8) {
+    const bool out = row < K;
+    const int c = out ? row : row - K;
+    const float *cv = cand_io + ((out ? sa : sb) * K + c) * 2 * R + (out ? 0 : R);
+    const float *sv = slot_io + (out ? sa : sb) * 2 * R + (out ? 0 : R);
+    float x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) x[u] = __ldcg(cv + lane + 32 * u) + __ldcg(sv + lane + 32 * u);
+    const float ss = warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]);
+    const float scale = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
+    float *dst = out ? os[c] : is[c];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) dst[lane + 32 * u] = x[u] * scale;
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < K * K; e += 256) {
+  for (int e = tid; e < K * K; e += 256) {
     const int a = e / K, bb = e - a * K;
     float acc = 0.f;
 #pragma unroll 8
     for (int k = 0; k < R; ++k) acc = fmaf(os[a][k], is[bb][k], acc);
-    scores[(int64_t)np * K * K + e] = fmaf(sigma, acc, topk_val[cb + bb]);
+    scores[(int64_t)np * K * K + e] = fmaf(sigma, acc, __ldcg(topk_val + sb * K + bb));
   }
+  __syncthreads();  // the request tail reuses the vectors' shared memory
+  request_tail<K>(sm, n, B, scores, wk);
 }
 
 }  // namespace
@@ -356,25 +368,33 @@ cudaError_t launch_pair_score_walk(int K, const float *U, const float *V, const 
   }
 }
 
-cudaError_t launch_cos_post(int K, const float *cand_io, const float *slot_io, int N, int B,
-                            float *O, float *I, cudaStream_t st) {
-  const int M = N * B * K;
-  if (M == 0) return cudaSuccess;
-  k_cos_post<<<(M + 7) / 8, 256, 0, st>>>(cand_io, slot_io, K, M, O, I);
+
+template <int K>
+static cudaError_t cos_pair_k(const float *cand_io, const float *slot_io, const float *tv, float sigma, int N,
+                              int B, float *scores, const WalkArgs &wk, cudaStream_t st) {
+  // path rules 1 and 2 stage the request's scores in shared memory when the
+  // device allows it (up to 227 KB a block)
+  size_t floats = CosGeom<K>::min_floats;
+  const size_t with_scores = 2 * (size_t)kWalkMaxRows + (size_t)(B - 1) * K * K;
+  if (wk.path_rule != 0 && with_scores * sizeof(float) <= 200 * 1024 && with_scores > floats) floats = with_scores;
+  const size_t smem = floats * sizeof(float);
+  cudaError_t e = cudaFuncSetAttribute(k_cos_pair<K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  e = launch_ex(k_cos_pair<K>, dim3(N * (B - 1)), dim3(256), smem, st, true, 0, cand_io, slot_io, tv, sigma, B,
+                scores, wk);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
-cudaError_t launch_cos_score(int K, const float *O, const float *I, const float *topk_val,
-                             float sigma, int N, int B, float *scores, cudaStream_t st) {
+cudaError_t launch_cos_pair_walk(int K, const float *cand_io, const float *slot_io, const float *topk_val,
+                                 float sigma, int N, int B, float *scores, const WalkArgs &wk, cudaStream_t st) {
   if (N == 0) return cudaSuccess;
-  const int grid = N * (B - 1);
   switch (K) {
-    case 8: k_cos_score<8><<<grid, 256, 0, st>>>(O, I, topk_val, sigma, B, scores); break;
-    case 16: k_cos_score<16><<<grid, 256, 0, st>>>(O, I, topk_val, sigma, B, scores); break;
-    case 32: k_cos_score<32><<<grid, 256, 0, st>>>(O, I, topk_val, sigma, B, scores); break;
+    case 8: return cos_pair_k<8>(cand_io, slot_io, topk_val, sigma, N, B, scores, wk, st);
+    case 16: return cos_pair_k<16>(cand_io, slot_io, topk_val, sigma, N, B, scores, wk, st);
+    case 32: return cos_pair_k<32>(cand_io, slot_io, topk_val, sigma, N, B, scores, wk, st);
     default: return cudaErrorInvalidValue;
   }
-  return cudaGetLastError();
 }
 
 }  // namespace dc
