@@ -133,7 +133,9 @@ struct PairGeom {
   // row stride (floats, even): the 64-bit reads of a half-warp hit distinct banks
   static constexpr int LD = K == 32 ? H + 2 : H + 4;
   static constexpr int RED = K * K + 1;            // partial-sum row stride
-  static constexpr size_t pair_floats = 2 * (size_t)K * LD + H + 2 * K + (size_t)NS * RED;
+  // the partial sums reuse the staged rows once the main loop is done
+  static_assert((size_t)NS * RED <= 2 * (size_t)K * LD, "partial sums fit the staged rows");
+  static constexpr size_t pair_floats = 2 * (size_t)K * LD + H + 2 * K;
   // the walk reuses the first 3 kWalkMaxRows words (best, gap, the request's ids)
   static constexpr size_t smem_floats = pair_floats > 3 * (size_t)kWalkMaxRows ? pair_floats : 3 * (size_t)kWalkMaxRows;
 };
@@ -154,7 +156,7 @@ k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
   float *vs = pu + K * G::LD;       // [K][LD]  V_{p+1,b} / sqrt(2)
   float *w2s = vs + K * G::LD;      // [H]      w2 / sqrt(2)
   float *dab = w2s + H;             // [2K]     d_a, then d_b
-  float *red = dab + 2 * K;         // [NS][RED] partial sums
+  float *red = sm;                  // [NS][RED] partial sums, over pu and vs after the main loop
   const int np = blockIdx.x;        // n * (B-1) + p
   const int n = np / (B - 1), p = np - n * (B - 1);
   const int tid = threadIdx.x;
@@ -249,6 +251,7 @@ k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
         acc[i][k] = f2_fma(t, f2_fma(rr, mone, one), acc[i][k]);
       }
   }
+  __syncthreads();  // every thread is done with pu and vs, which the partial sums overwrite
   float *rs = red + sl * G::RED;
 #pragma unroll
   for (int i = 0; i < G::T; ++i)
