@@ -457,14 +457,14 @@ int dcoco_create(const dcoco_config *cfg, dcoco_handle **out) {
   }
   h->topk_wave = sms * dc::topk_occupancy(cfg->topk);
   {
-    // split-K of the projection: up to four CTAs per tile, as many as keep
-    // the largest call (max_batch) in one wave of one CTA per SM (a second
-    // wave repeats the fill, drain and reduction); fixed per handle, so
-    // results do not depend on the batch
+    // split-K of the projection: up to eight CTAs per tile (a portable
+    // cluster), as many as keep the largest call (max_batch) in one wave of
+    // one CTA per SM (a second wave repeats the fill, drain and reduction);
+    // fixed per handle, so results do not depend on the batch
     const int rows_cap = cfg->max_batch * h->B, cands_cap = rows_cap * cfg->topk;
     const int r_out = cfg->variant == 0 ? kR : 2 * kR, s_out = cfg->variant == 0 ? 3 * kR : 2 * kR;
     const int tiles = dc::proj_tc_tiles(cands_cap, r_out) + dc::proj_tc_tiles(rows_cap, s_out);
-    int want = 4;
+    int want = 8;
     while (want > 1 && (long long)tiles * want > sms) want /= 2;
     h->splits = dc::proj_tc_splits(cfg->hidden, want);
   }

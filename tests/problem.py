@@ -75,15 +75,21 @@ def bf16_tensor(a: np.ndarray, device="cuda"):
     return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
 
 
+def make_corrector(prob: Problem, max_batch: int | None = None):
+    import torch
+    import draft_correction_slot_gb300 as dc
+    return dc.Corrector({k: torch.from_numpy(v) for k, v in prob.w.items()}, prob.V, prob.d,
+                        prob.slots, prob.K, max_batch=max_batch or prob.N, variant=prob.variant,
+                        sigma=prob.sigma, path_rule=prob.path_rule, beam_width=prob.beam_width,
+                        beam_topm=prob.beam_topm)
+
+
 def run_gpu(prob: Problem, max_batch: int | None = None, corr=None, E_dev=None):
     import torch
     import draft_correction_slot_gb300 as dc
     own = corr is None
     if own:
-        corr = dc.Corrector({k: torch.from_numpy(v) for k, v in prob.w.items()}, prob.V, prob.d,
-                            prob.slots, prob.K, max_batch=max_batch or prob.N, variant=prob.variant,
-                            sigma=prob.sigma, path_rule=prob.path_rule, beam_width=prob.beam_width,
-                            beam_topm=prob.beam_topm)
+        corr = make_corrector(prob, max_batch)
     E_dev = E_dev if E_dev is not None else bf16_tensor(prob.E)
     tg = None if prob.targets is None else torch.from_numpy(prob.targets).cuda()
     out = corr.correct(bf16_tensor(prob.logits), bf16_tensor(prob.hidden), E_dev, tg,

@@ -9,7 +9,7 @@ import pytest
 
 import oracle
 import synth
-from problem import compare_path, Problem, bf16_tensor, compare, run_gpu
+from problem import make_corrector, compare_path, Problem, bf16_tensor, compare, run_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -186,17 +186,31 @@ def test_short_block(torch_cuda):
 
 
 def test_determinism_and_batch_invariance(torch_cuda):
+    """Within one handle: the same call twice gives the same bits, and a
+    request's results do not depend on the batch it came in.  A handle whose
+    max_batch selects another projection split count (here 4 and 32 requests:
+    eight and four splits) sums the projection in another order: its
+    discrete outputs are the same and its scores agree to fp32 rounding."""
     prob = Problem(9, N=4, V=V_QWEN, d=D_QWEN, targets=True)
-    a = run_gpu(prob)
-    b = run_gpu(prob, max_batch=32)
-    for k in a:
-        np.testing.assert_array_equal(a[k], b[k], err_msg=f"{k} not deterministic")
-    one = copy.copy(prob)
-    one.N = 1
-    one.logits, one.hidden, one.targets = prob.logits[2:3], prob.hidden[2:3], prob.targets[2:3]
-    c = run_gpu(one)
-    for k in c:
-        np.testing.assert_array_equal(c[k][0], a[k][2], err_msg=f"{k} depends on the batch")
+    corr = make_corrector(prob, max_batch=32)
+    try:
+        a = run_gpu(prob, corr=corr)
+        a2 = run_gpu(prob, corr=corr)
+        for k in a:
+            np.testing.assert_array_equal(a[k], a2[k], err_msg=f"{k} not deterministic")
+        one = copy.copy(prob)
+        one.N = 1
+        one.logits, one.hidden, one.targets = prob.logits[2:3], prob.hidden[2:3], prob.targets[2:3]
+        c = run_gpu(one, corr=corr)
+        for k in c:
+            np.testing.assert_array_equal(c[k][0], a[k][2], err_msg=f"{k} depends on the batch")
+    finally:
+        corr.close()
+    b = run_gpu(prob)  # a handle for 4 requests: eight splits instead of four
+    for k in ("tokens", "choice", "accept_len", "topk_ids", "topk_val"):
+        if k in a:
+            np.testing.assert_array_equal(a[k], b[k], err_msg=f"{k} differs between split counts")
+    np.testing.assert_allclose(a["scores"], b["scores"], rtol=0, atol=1e-4)
 
 
 @pytest.mark.parametrize("tier,boost", [("low", (2.0, 6.0)), ("mid", (4.0, 12.0)), ("high", (8.0, 16.0))])
