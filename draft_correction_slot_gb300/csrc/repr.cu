@@ -300,28 +300,48 @@ k_cos_pair(const float *__restrict__ cand_io, const float *__restrict__ slot_io,
   pdl_trigger();
   pdl_wait();  // cand_io, slot_io (and this call's outputs) belong to the previous kernels until here
   const int64_t sa = (int64_t)n * B + p, sb = sa + 1;  // draft-slot rows of slots p and p+1
-  // everything this call's earlier kernels wrote is read through L2 (ld.cg)
-  for (int row = warp; row < 2 * K; row += 8) {
+  // everything this call's earlier kernels wrote is read through L2 (ld.cg);
+  // a warp's 2K / 8 vectors load together, then sum, normalise and store
+  constexpr int RW = 2 * K / 8;  // vectors per warp
+  float x[RW][4];
+#pragma unroll
+  for (int i = 0; i < RW; ++i) {
+    const int row = warp + 8 * i;
     const bool out = row < K;
     const int c = out ? row : row - K;
     const float *cv = cand_io + ((out ? sa : sb) * K + c) * 2 * R + (out ? 0 : R);
     const float *sv = slot_io + (out ? sa : sb) * 2 * R + (out ? 0 : R);
-    float x[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) x[u] = __ldcg(cv + lane + 32 * u) + __ldcg(sv + lane + 32 * u);
-    const float ss = warp_sum(x[0] * x[0] + x[1] * x[1] + x[2] * x[2] + x[3] * x[3]);
+    for (int u = 0; u < 4; ++u) x[i][u] = __ldcg(cv + lane + 32 * u) + __ldcg(sv + lane + 32 * u);
+  }
+  const float tv = tid < K ? __ldcg(topk_val + sb * K + tid) : 0.f;  // l_{p+1}(b)
+#pragma unroll
+  for (int i = 0; i < RW; ++i) {
+    const int row = warp + 8 * i;
+    const bool out = row < K;
+    const int c = out ? row : row - K;
+    const float ss = warp_sum(x[i][0] * x[i][0] + x[i][1] * x[i][1] + x[i][2] * x[i][2] + x[i][3] * x[i][3]);
     const float scale = 1.0f / fmaxf(sqrtf(ss), 1e-12f);
     float *dst = out ? os[c] : is[c];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) dst[lane + 32 * u] = x[u] * scale;
+    for (int u = 0; u < 4; ++u) dst[lane + 32 * u] = x[i][u] * scale;
   }
+  __shared__ float s_tv[32];
+  if (tid < K) s_tv[tid] = tv;
   __syncthreads();
+  // each dot product as four interleaved partial sums (k mod 4), added as
+  // (p0 + p1) + (p2 + p3)
   for (int e = tid; e < K * K; e += 256) {
     const int a = e / K, bb = e - a * K;
-    float acc = 0.f;
+    float p0 = 0.f, p1 = 0.f, p2 = 0.f, p3 = 0.f;
 #pragma unroll 8
-    for (int k = 0; k < R; ++k) acc = fmaf(os[a][k], is[bb][k], acc);
-    scores[(int64_t)np * K * K + e] = fmaf(sigma, acc, __ldcg(topk_val + sb * K + bb));
+    for (int k = 0; k < R; k += 4) {
+      p0 = fmaf(os[a][k], is[bb][k], p0);
+      p1 = fmaf(os[a][k + 1], is[bb][k + 1], p1);
+      p2 = fmaf(os[a][k + 2], is[bb][k + 2], p2);
+      p3 = fmaf(os[a][k + 3], is[bb][k + 3], p3);
+    }
+    scores[(int64_t)np * K * K + e] = fmaf(sigma, (p0 + p1) + (p2 + p3), s_tv[bb]);
   }
   __syncthreads();  // the request tail reuses the vectors' shared memory
   request_tail<K>(sm, n, B, scores, wk);
