@@ -214,18 +214,70 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
+    # NVML clocks-event reason bits (read-only queries; nothing is set)
+    _REASON_BITS = {"hw_slowdown": 0x8, "hw_thermal_slowdown": 0x40, "sw_thermal_slowdown": 0x20,
+                    "sw_power_cap": 0x4}
+
     def __init__(self, gpu_index: int):
         self.samples = []
         self.proc = None
+        self._stop = False
+        self.source = "none"
+        # this process's GPU by PCI address (the CUDA index need not be the
+        # physical one); NVML through ctypes every 10 ms, else nvidia-smi
+        bus = None
+        try:
+            import torch
+            pr = torch.cuda.get_device_properties(gpu_index)
+            bus = f"{pr.pci_domain_id:08X}:{pr.pci_bus_id:02X}:{pr.pci_device_id:02X}.0"
+        except Exception:
+            bus = None
+        if bus and self._start_nvml(bus):
+            return
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-i", str(gpu_index), "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                 "-i", bus or str(gpu_index), "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
                 text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            self.source = "nvidia-smi"
         except (OSError, FileNotFoundError):
             self.proc = None
+
+    def _start_nvml(self, bus: str) -> bool:
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return False
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+                return False
+            reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        except (OSError, AttributeError):
+            return False
+        c, mx, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) != 0:
+            return False
+
+        def loop():
+            while not self._stop:
+                ok = lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(c)) == 0
+                okp = lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw)) == 0
+                okr = reasons_fn(h, ctypes.byref(rs)) == 0
+                if ok:
+                    act = [("Active" if okr and (rs.value & bit) else "Not Active")
+                           for bit in self._REASON_BITS.values()]
+                    self.samples.append((time.time(), [str(c.value), str(mx.value),
+                                                       f"{pw.value / 1000.0:.2f}" if okp else "",
+                                                       hex(rs.value) if okr else ""] + act))
+                time.sleep(0.01)
+        self.t = threading.Thread(target=loop, daemon=True)
+        self.t.start()
+        self.source = "nvml"
+        return True
 
     def _read(self):
         for line in self.proc.stdout:
@@ -234,6 +286,7 @@ class ClockSampler:
                 self.samples.append((time.time(), parts))
 
     def stop(self):
+        self._stop = True
         if self.proc:
             self.proc.terminate()
             try:
@@ -260,7 +313,7 @@ class ClockSampler:
         reasons = sorted({names[i] for p in win for i in range(4) if p[4 + i].lower() == "active"})
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": num(win[0][1]), "power_w_max": max((num(p[2]) or 0) for p in win),
-                "reasons": reasons, "samples": len(win), "window": note}
+                "reasons": reasons, "samples": len(win), "window": note, "source": self.source}
 
 
 # ------------------------------------------------------------------ inputs (GPU, seeded)
