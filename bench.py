@@ -132,7 +132,7 @@ def maps_method_flops(w) -> int:
     return 2 * N * (B * r * r + (B - 1) * r * H) + 2 * N * B * K * (r * r + 2 * r * H)
 
 
-FMA_LANE_OPS_PER_GELU = 9  # the pair loop's FMA-pipe lane operations per w2*GELU element
+FMA_LANE_OPS_PER_GELU = 8  # the pair loop's FMA-pipe lane operations per w2*GELU element
 
 
 def fma_lane_rate(pk) -> float:

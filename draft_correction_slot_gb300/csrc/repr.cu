@@ -81,7 +81,9 @@ __device__ __forceinline__ void request_tail(float *sm, int n, int B, const floa
 // error stays below 7e-7 for every x in [0, 12], and beyond, p falls like
 // -x^5, so 2^p underflows to 0 as erfc does.  Per element: five FMAs and one
 // hardware base-2 exponential (the special-function unit's fastest
-// operation), then w' |x| (1 - erfc(|x|)) -- nine FMA-pipe lane operations.
+// operation), then w' |x| (1 - erfc(|x|)) as |x| (w' - w' erfc(|x|)), one
+// FMA for the bracket and one into the accumulator -- eight FMA-pipe lane
+// operations.
 constexpr float kErfc0 = -3.75319205e-05f, kErfc1 = -1.62746069f, kErfc2 = -0.919982363f;
 constexpr float kErfc3 = -0.146592411f, kErfc4 = 0.028338989f, kErfc5 = -0.00267746694f;
 
@@ -98,11 +100,6 @@ __device__ __forceinline__ void f2_unpack(f2_t v, float &lo, float &hi) {
 __device__ __forceinline__ f2_t f2_fma(f2_t a, f2_t b, f2_t c) {
   f2_t d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
-}
-__device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
-  f2_t d;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
 __device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
@@ -215,7 +212,6 @@ k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
   const int a0 = (blk / (K / G::T)) * G::T, b0 = (blk % (K / G::T)) * G::T;
   const f2_t c0 = f2_pack(kErfc0, kErfc0), c1 = f2_pack(kErfc1, kErfc1), c2 = f2_pack(kErfc2, kErfc2);
   const f2_t c3 = f2_pack(kErfc3, kErfc3), c4 = f2_pack(kErfc4, kErfc4), c5 = f2_pack(kErfc5, kErfc5);
-  const f2_t one = f2_pack(1.f, 1.f), mone = f2_pack(-1.f, -1.f);
   f2_t acc[G::T][G::T];
 #pragma unroll
   for (int i = 0; i < G::T; ++i)
@@ -225,7 +221,7 @@ k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
   for (int jj = 0; jj < G::JP; ++jj) {
     const int j = 2 * (sl + jj * G::NS);
     const float2 wv = *reinterpret_cast<const float2 *>(w2s + j);
-    const f2_t w = f2_pack(wv.x, wv.y);
+    const f2_t w = f2_pack(wv.x, wv.y), nw = f2_pack(-wv.x, -wv.y);
     f2_t xa[G::T], yb[G::T];
 #pragma unroll
     for (int i = 0; i < G::T; ++i) {
@@ -247,8 +243,8 @@ k_pair_score(const float *__restrict__ U, const float *__restrict__ V,
         float q0, q1;
         f2_unpack(q, q0, q1);
         const f2_t rr = f2_pack(ex2_approx(q0), ex2_approx(q1));  // erfc(|x|)
-        const f2_t t = f2_mul(w, ax);
-        acc[i][k] = f2_fma(t, f2_fma(rr, mone, one), acc[i][k]);
+        // w' |x| (1 - erfc) = |x| (w' - w' erfc): two operations
+        acc[i][k] = f2_fma(ax, f2_fma(nw, rr, w), acc[i][k]);
       }
   }
   __syncthreads();  // every thread is done with pu and vs, which the partial sums overwrite
